@@ -1,0 +1,229 @@
+// CPU oracle for the routed MoE layer.  TEST INFRASTRUCTURE ONLY: see moe_oracle.h.
+//
+// Plain single-threaded C++17.  Every step follows the definition it cites, in the
+// order the definition states it; no blocking, fusion or reordering.  Sums run in
+// ascending index order in the accumulation type (float for the parity reference,
+// double for the shadow that bounds the float version's rounding error).
+#include "moe_oracle.h"
+
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+namespace {
+
+// E2M1 (OCP MX v1.0 FP4): 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit.
+// Exponent field 0 is subnormal: value = 2^(1-1) * (m / 2) = m / 2.
+// Otherwise value = 2^(e-1) * (1 + m / 2).  No infinities or NaN.
+double e2m1_exact(uint32_t nibble) {
+  const uint32_t s = (nibble >> 3) & 1u;
+  const uint32_t e = (nibble >> 1) & 3u;
+  const uint32_t m = nibble & 1u;
+  double mag;
+  if (e == 0) {
+    mag = 0.5 * static_cast<double>(m);
+  } else {
+    mag = std::ldexp(1.0 + 0.5 * static_cast<double>(m), static_cast<int>(e) - 1);
+  }
+  return s ? -mag : mag;
+}
+
+// E4M3 (OCP MX v1.0 FP8 "FN"): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits.
+// Exponent field 0 is subnormal: 2^(1-7) * (m / 8).  S.1111.111 is NaN; there are no
+// infinities, so exponent field 15 with m < 7 is an ordinary normal number (max 448).
+double e4m3_exact(uint32_t byte) {
+  const uint32_t s = (byte >> 7) & 1u;
+  const uint32_t e = (byte >> 3) & 15u;
+  const uint32_t m = byte & 7u;
+  if (e == 15u && m == 7u) return std::nan("");
+  double mag;
+  if (e == 0) {
+    mag = std::ldexp(static_cast<double>(m) / 8.0, -6);
+  } else {
+    mag = std::ldexp(1.0 + static_cast<double>(m) / 8.0, static_cast<int>(e) - 7);
+  }
+  return s ? -mag : mag;
+}
+
+// BF16 is the upper half of an IEEE binary32 pattern.
+float bf16_to_float(uint16_t bits) {
+  const uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+// One NVFP4 weight: code nibble c of a row (element 2i in the low nibble of byte i),
+// its block scale (one E4M3 per 16 consecutive elements) and the tensor scale.  The
+// product of an E2M1 value, an E4M3 value and an FP32 scale is formed in Acc; for
+// float it is exact whenever the tensor scale is a power of two (6 significant bits).
+template <typename Acc>
+Acc nvfp4_weight(const uint8_t* codes, const uint8_t* scales, float tensor_scale, int c) {
+  const uint32_t byte = codes[c >> 1];
+  const uint32_t nib = (c & 1) ? (byte >> 4) : (byte & 15u);
+  const Acc v = static_cast<Acc>(e2m1_exact(nib));
+  const Acc s = static_cast<Acc>(e4m3_exact(scales[c >> 4]));
+  return v * s * static_cast<Acc>(tensor_scale);
+}
+
+// Router for one token (routing paragraph of "Fused MoE routing"; selection paragraph
+// of "Router: selection and expert-task production"):
+//   1. softmax over the E logits: p_e = exp(l_e - max) / sum_e exp(l_e - max);
+//   2. choose k experts by repeated maxima of the logits, larger first, ties to the
+//      lower expert index (the strict '>' keeps the first, i.e. lowest, index; float
+//      comparison treats -0 and +0 as equal);
+//   3. renormalise: w_j = p_{s_j} / sum_{i<k} p_{s_i}.
+// Selecting on the logits instead of the rounded probabilities gives the same order
+// in exact arithmetic (softmax is strictly increasing) and keeps the ids independent
+// of the exponential's rounding.
+template <typename Acc>
+void route_token(int E, int k, const float* l, int32_t* ids, Acc* w) {
+  float mx = l[0];
+  for (int e = 1; e < E; ++e) mx = (l[e] > mx) ? l[e] : mx;
+  std::vector<Acc> ex(E);
+  Acc z = 0;
+  for (int e = 0; e < E; ++e) {
+    ex[e] = std::exp(static_cast<Acc>(l[e]) - static_cast<Acc>(mx));
+    z += ex[e];
+  }
+  std::vector<Acc> p(E);
+  for (int e = 0; e < E; ++e) p[e] = ex[e] / z;
+
+  std::vector<char> used(E, 0);
+  for (int j = 0; j < k; ++j) {
+    int best = -1;
+    for (int e = 0; e < E; ++e) {
+      if (used[e]) continue;
+      if (best < 0 || l[e] > l[best]) best = e;
+    }
+    used[best] = 1;
+    ids[j] = best;
+  }
+  Acc sel = 0;
+  for (int j = 0; j < k; ++j) sel += p[ids[j]];
+  for (int j = 0; j < k; ++j) w[j] = p[ids[j]] / sel;
+}
+
+template <typename Acc>
+int route_topk(int T, int E, int k, const float* logits, int32_t* ids, Acc* weights) {
+  if (T < 0 || E <= 0 || k <= 0 || k > E) return -1;
+  for (int t = 0; t < T; ++t) {
+    route_token<Acc>(E, k, logits + static_cast<size_t>(t) * E, ids + static_cast<size_t>(t) * k,
+                     weights + static_cast<size_t>(t) * k);
+  }
+  return 0;
+}
+
+// Expert FFN plus weighted un-route for every selected token ("First implementation
+// boundary", steps 2-4: gate/up with SiLU*multiply, down projection, routes summed in
+// a fixed order).  For token t and slot j with expert e:
+//   g_n = sum_c x_c Wg[e][n][c],  u_n = sum_c x_c Wu[e][n][c]           (n < F)
+//   h_n = silu(g_n) * u_n,        silu(z) = z / (1 + exp(-z))
+//   y_r = sum_n h_n W2[e][r][n]                                         (r < d)
+//   out[t][r] = residual[t][r] + sum_{j=0..k-1} w_{t,j} y_{t,j,r}
+template <typename Acc>
+int moe_experts(int T, int d, int F, int E, int k, const uint16_t* hidden, const int32_t* ids,
+                const Acc* weights, const uint8_t* w13c, const uint8_t* w13s, float w13_ts,
+                const uint8_t* w2c, const uint8_t* w2s, float w2_ts, const uint16_t* residual,
+                const uint8_t* mask, Acc* out) {
+  if (T < 0 || d <= 0 || F <= 0 || E <= 0 || k <= 0 || k > E || d % 16 || F % 16) return -1;
+  const size_t d2 = static_cast<size_t>(d) / 2, d16 = static_cast<size_t>(d) / 16;
+  const size_t f2 = static_cast<size_t>(F) / 2, f16 = static_cast<size_t>(F) / 16;
+  std::vector<Acc> x(d), g(F), u(F), h(F), y(d), acc(d);
+  for (int t = 0; t < T; ++t) {
+    if (mask && !mask[t]) continue;
+    for (int c = 0; c < d; ++c) x[c] = static_cast<Acc>(bf16_to_float(hidden[static_cast<size_t>(t) * d + c]));
+    for (int r = 0; r < d; ++r) acc[r] = 0;
+    for (int j = 0; j < k; ++j) {
+      const int e = ids[static_cast<size_t>(t) * k + j];
+      if (e < 0 || e >= E) return -1;
+      for (int n = 0; n < F; ++n) {
+        const size_t rg = static_cast<size_t>(e) * 2 * F + n;      // gate row
+        const size_t ru = static_cast<size_t>(e) * 2 * F + F + n;  // up row
+        Acc sg = 0, su = 0;
+        for (int c = 0; c < d; ++c) sg += x[c] * nvfp4_weight<Acc>(w13c + rg * d2, w13s + rg * d16, w13_ts, c);
+        for (int c = 0; c < d; ++c) su += x[c] * nvfp4_weight<Acc>(w13c + ru * d2, w13s + ru * d16, w13_ts, c);
+        g[n] = sg;
+        u[n] = su;
+      }
+      for (int n = 0; n < F; ++n) h[n] = g[n] / (static_cast<Acc>(1) + std::exp(-g[n])) * u[n];
+      for (int r = 0; r < d; ++r) {
+        const size_t rr = static_cast<size_t>(e) * d + r;
+        Acc s = 0;
+        for (int n = 0; n < F; ++n) s += h[n] * nvfp4_weight<Acc>(w2c + rr * f2, w2s + rr * f16, w2_ts, n);
+        y[r] = s;
+      }
+      const Acc wj = weights[static_cast<size_t>(t) * k + j];
+      for (int r = 0; r < d; ++r) acc[r] += wj * y[r];
+    }
+    for (int r = 0; r < d; ++r) {
+      const Acc res = residual ? static_cast<Acc>(bf16_to_float(residual[static_cast<size_t>(t) * d + r])) : 0;
+      out[static_cast<size_t>(t) * d + r] = res + acc[r];
+    }
+  }
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+float oracle_e2m1_value(uint32_t nibble) { return static_cast<float>(e2m1_exact(nibble & 15u)); }
+
+float oracle_e4m3_value(uint32_t byte) { return static_cast<float>(e4m3_exact(byte & 255u)); }
+
+int oracle_dequant_row(const uint8_t* codes, const uint8_t* scales, float tensor_scale, int K,
+                       float* out) {
+  if (K <= 0 || K % 16) return -1;
+  for (int c = 0; c < K; ++c) out[c] = nvfp4_weight<float>(codes, scales, tensor_scale, c);
+  return 0;
+}
+
+int oracle_route_topk_f32(int T, int E, int k, const float* logits, int32_t* ids, float* weights) {
+  return route_topk<float>(T, E, k, logits, ids, weights);
+}
+
+int oracle_route_topk_f64(int T, int E, int k, const float* logits, int32_t* ids, double* weights) {
+  return route_topk<double>(T, E, k, logits, ids, weights);
+}
+
+// Bucketing of routes by expert (the compact expert-presence list of "First
+// implementation boundary", step 1): per-expert counts, their exclusive prefix sum,
+// and the touched experts in ascending order.
+int oracle_plan(int T, int E, int k, const int32_t* ids, int32_t* counts, int32_t* offsets,
+                int32_t* touched) {
+  if (T < 0 || E <= 0 || k <= 0) return -1;
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (size_t r = 0; r < static_cast<size_t>(T) * k; ++r) {
+    const int e = ids[r];
+    if (e < 0 || e >= E) return -1;
+    counts[e] += 1;
+  }
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  int U = 0;
+  for (int e = 0; e < E; ++e) {
+    if (counts[e] > 0) touched[U++] = e;
+  }
+  return U;
+}
+
+int oracle_moe_experts_f32(int T, int d, int F, int E, int k, const uint16_t* hidden_bf16,
+                           const int32_t* ids, const float* weights, const uint8_t* w13_codes,
+                           const uint8_t* w13_scales, float w13_ts, const uint8_t* w2_codes,
+                           const uint8_t* w2_scales, float w2_ts, const uint16_t* residual_bf16,
+                           const uint8_t* token_mask, float* out) {
+  return moe_experts<float>(T, d, F, E, k, hidden_bf16, ids, weights, w13_codes, w13_scales, w13_ts,
+                            w2_codes, w2_scales, w2_ts, residual_bf16, token_mask, out);
+}
+
+int oracle_moe_experts_f64(int T, int d, int F, int E, int k, const uint16_t* hidden_bf16,
+                           const int32_t* ids, const double* weights, const uint8_t* w13_codes,
+                           const uint8_t* w13_scales, float w13_ts, const uint8_t* w2_codes,
+                           const uint8_t* w2_scales, float w2_ts, const uint16_t* residual_bf16,
+                           const uint8_t* token_mask, double* out) {
+  return moe_experts<double>(T, d, F, E, k, hidden_bf16, ids, weights, w13_codes, w13_scales, w13_ts,
+                             w2_codes, w2_scales, w2_ts, residual_bf16, token_mask, out);
+}
+
+}  // extern "C"
