@@ -1,0 +1,475 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE layer (router + plan + NVFP4 experts + un-route) on GB300.
+
+One step = one layer call (moe_route_topk, moe_plan, moe_forward) on one batch of the
+workload.  Steps cycle over 12 independent layer weight sets (10.9 GB for the d=2048
+shapes), so the streamed weights never fit the 129 MB L2.  The timed region replays
+CUDA graphs of those calls; the expert kernel is additionally timed alone with CUDA
+events for its roofline figure; `e2e` times the public C-ABI call with host buffers
+(H2D of logits/hidden/residual, D2H of the output) per step.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "MoE layer µs and tokens/s at T=4/32/256/8192; % of HBM roofline (unique-expert bytes)"
+DEFAULT_STEPS = {"tiny": 20000, "b1": 48000, "b8": 12000, "b64": 6000, "prefill": 1200, "b64_literal": 6000}
+WORKLOAD = {
+    "tiny": "tiny parity case: T=4 d=256 ffn=128 E=16 top-2",
+    "b1": "decode verify B=1 (1 request x 4 rows): T=4 d=2048 ffn=512 E=512 top-10, NVFP4 experts",
+    "b8": "decode verify B=8 (8 requests x 4 rows, per-request expert bias): T=32 d=2048 ffn=512 E=512 top-10",
+    "b64": "decode batch B=64 (Zipf expert popularity): T=256 d=2048 ffn=512 E=512 top-10",
+    "prefill": "prefill chunk: T=8192 d=2048 ffn=512 E=512 top-10",
+    "b64_literal": "decode batch B=64, literal Zipf coefficient: T=256 d=2048 ffn=512 E=512 top-10",
+}
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=None)
+    p.add_argument("--config", default="b1", choices=sorted(mi.CONFIGS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--algo", default="tcgen05", choices=["tcgen05", "simt"])
+    p.add_argument("--layers", type=int, default=None, help="weight sets cycled (default 12)")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; replicas, no data-path collective)
+# ----------------------------------------------------------------------------------
+class Dist:
+    def __init__(self, torch):
+        self.torch = torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            if self.torch.cuda.is_available():
+                self.pg.barrier(device_ids=[self.local])
+            else:
+                self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if self.pg is None:
+            return v
+        dev = f"cuda:{self.local}" if self.torch.cuda.is_available() else "cpu"
+        t = self.torch.tensor([v], dtype=self.torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profiled_traffic(config: str):
+    """DRAM bytes per expert-kernel launch from the committed ncu summary of this workload,
+    or None if there is none or the kernel source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", f"expert_tc_{config}_dram.txt")
+    src = os.path.join(ROOT, "routed_moe_decode_gb300", "csrc", "expert_tc.cu")
+    if not os.path.exists(path):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("expert_tc.cu sha256[:16]") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline field)
+# ----------------------------------------------------------------------------------
+def time_oracle(cfg, inp, budget_s: float, max_steps: int | None = None, warmup: int = 1):
+    """Oracle on one token per step (routing of the batch + that token's k expert routes),
+    cycling over the batch's tokens until the budget (or max_steps) is used."""
+    from oracle import oracle as O
+    ids, wts = O.route_topk(inp["logits"], cfg.k)
+    dims = (cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k)
+    out = np.zeros((cfg.T, cfg.d), np.float32)
+
+    def one(t):
+        mask = np.zeros(cfg.T, np.uint8)
+        mask[t] = 1
+        O.route_topk(inp["logits"][t:t + 1], cfg.k)
+        O.moe_experts(dims, inp["hidden"], ids, wts, inp, inp["residual"], mask, out=out)
+
+    for i in range(warmup):
+        one(i % cfg.T)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        one(n % cfg.T)
+        n += 1
+        el = time.perf_counter() - t0
+        if (max_steps is not None and n >= max_steps) or el >= budget_s:
+            break
+    return n, el
+
+
+def reference_arm(args, cfg, dist):
+    if dist.rank != 0:
+        return None
+    steps = args.steps if args.steps is not None else 10
+    warm = min(args.warmup if args.warmup is not None else 1, 2)
+    inp = mi.gen_layer(cfg, seed=0, layer=0)
+    n, el = time_oracle(cfg, inp, budget_s=120.0, max_steps=steps, warmup=warm)
+    value = n / el
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": n,
+        "warmup": warm, "ms_per_step": 1e3 * el / n, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded moe_inputs workload)",
+        "config": {"workload": WORKLOAD[cfg.name], "T": cfg.T, "d": cfg.d, "ffn": cfg.ffn, "E": cfg.E, "k": cfg.k,
+                   "step": "one token of the batch (its k expert routes) through the CPU oracle"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} single-token steps of layer 0 ({cfg.name}), FP32 C++ oracle, 1 thread"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+# ----------------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------------
+def our_arm(args, cfg, dist, torch):
+    import __graft_entry__
+    __graft_entry__.build()  # no-op when the in-tree library is current
+    import routed_moe_decode_gb300 as moe
+    dev = torch.device(f"cuda:{dist.local}")
+    torch.cuda.set_device(dev)
+    algo = moe.ALGO_TCGEN05 if args.algo == "tcgen05" else moe.ALGO_SIMT
+    L = args.layers if args.layers is not None else min(12, max(1, cfg.layers))
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[cfg.name]
+    W = args.warmup if args.warmup is not None else max(3, 2 * L)
+    W = max(W, 3)
+    shape = moe.shape_of(cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k)
+
+    # ---- inputs: L independent layers, resident in HBM ----
+    t_gen = time.perf_counter()
+    Wd, logits, hidden, resid, host = [], [], [], [], []
+    keep_host = None
+    for layer in range(L):
+        inp = mi.gen_layer(cfg, seed=0, layer=layer)
+        w = {n: torch.from_numpy(inp[n]).to(dev) for n in ("w13_codes", "w13_scales", "w2_codes", "w2_scales")}
+        w["w13_ts"], w["w2_ts"] = inp["w13_ts"], inp["w2_ts"]
+        Wd.append(w)
+        logits.append(torch.from_numpy(inp["logits"]).to(dev))
+        hidden.append(torch.from_numpy(inp["hidden"].view(np.int16)).to(dev).view(torch.bfloat16))
+        resid.append(torch.from_numpy(inp["residual"].view(np.int16)).to(dev).view(torch.bfloat16))
+        host.append({k_: inp[k_] for k_ in ("logits", "hidden", "residual")})
+        if layer == 0:
+            keep_host = inp
+    torch.cuda.synchronize()
+    t_gen = time.perf_counter() - t_gen
+
+    ws = moe.Workspace(shape, device=dev)
+    ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+    wts = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
+    out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
+
+    def step(l):
+        moe.route_topk(shape, logits[l], ids, wts)
+        moe.plan(shape, ids, wts, ws)
+        moe.forward_prepare(shape, hidden[l], ws)
+        moe.forward_experts(shape, Wd[l], resid[l], out, ws, algo)
+
+    kernels_per_step = 4 if algo == moe.ALGO_TCGEN05 else 6
+
+    # ---- unique experts per layer (outside any timed region) ----
+    U = []
+    for l in range(L):
+        step(l)
+        u, _ = moe.plan_summary(shape, ws)
+        U.append(u)
+    if moe.read_status(ws):
+        raise RuntimeError("device status bits set during set-up")
+    bpe = mi.weight_bytes_per_expert(cfg)
+    act_bytes = cfg.T * cfg.d * 2 * 3  # hidden read, residual read, output write (BF16)
+    unique_bytes = [u * bpe for u in U]
+
+    # ---- CUDA graphs: one of all L layers, one per single layer (for K % L) ----
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for l in range(L):
+            step(l)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g_all = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_all):
+        for l in range(L):
+            step(l)
+    g_one = []
+    for l in range(L):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(l)
+        g_one.append(g)
+
+    def run_steps(n, offset=0):
+        done = 0
+        while done < n and (offset + done) % L != 0:
+            g_one[(offset + done) % L].replay()
+            done += 1
+        while n - done >= L:
+            g_all.replay()
+            done += L
+        while done < n:
+            g_one[(offset + done) % L].replay()
+            done += 1
+
+    # ---- warm-up and timed region ----
+    run_steps(W)
+    torch.cuda.synchronize()
+    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}")
+    sampler.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    run_steps(K, offset=W % L)
+    ev1.record()
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = sampler.stop()
+    t_ms = ev0.elapsed_time(ev1)
+    t_ms = dist.max(t_ms)
+    status = moe.read_status(ws)
+
+    steps_layers = [(W + i) % L for i in range(K)]
+    tokens = cfg.T * K * dist.world
+    value = tokens / (t_ms * 1e-3)
+    us_per_layer = 1e3 * t_ms / K
+    mean_unique = sum(unique_bytes[l] for l in steps_layers) / K
+
+    # ---- expert kernel alone: CUDA events around each launch ----
+    Kk = min(K, 2000)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(Kk)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(Kk)]
+    kbytes = 0.0
+    for i in range(Kk):
+        l = i % L
+        moe.route_topk(shape, logits[l], ids, wts)
+        moe.plan(shape, ids, wts, ws)
+        moe.forward_prepare(shape, hidden[l], ws)
+        starts[i].record()
+        moe.forward_experts(shape, Wd[l], resid[l], out, ws, algo)
+        ends[i].record()
+        kbytes += unique_bytes[l] + act_bytes
+    torch.cuda.synchronize()
+    kdur_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    k_avg_ms = sum(kdur_ms) / Kk
+    achieved = kbytes / Kk / (k_avg_ms * 1e-3) / 1e9
+    peak, peak_kind = load_peaks()
+    traffic = profiled_traffic(cfg.name) if algo == moe.ALGO_TCGEN05 else None
+
+    # ---- end to end through the public C-ABI call with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        Ke = min(K, 3000)
+        pin = [{k_: torch.from_numpy(h[k_] if k_ == "logits" else h[k_].view(np.int16)).pin_memory()
+                for k_ in ("logits", "hidden", "residual")} for h in host]
+        d_log = torch.empty_like(logits[0])
+        d_hid = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device=dev)
+        d_res = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device=dev)
+        h_out = torch.empty((cfg.T, cfg.d), dtype=torch.int16).pin_memory()
+
+        def e2e_step(l):
+            d_log.copy_(pin[l]["logits"], non_blocking=True)
+            d_hid.copy_(pin[l]["hidden"], non_blocking=True)
+            d_res.copy_(pin[l]["residual"], non_blocking=True)
+            moe.layer(shape, d_log, d_hid.view(torch.bfloat16), Wd[l], d_res.view(torch.bfloat16), out, ids, wts, ws)
+            h_out.copy_(out.view(torch.int16), non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i % L)
+        torch.cuda.synchronize()
+        dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(Ke):
+            e2e_step(i % L)
+        e1.record()
+        e1.synchronize()
+        et = dist.max(e0.elapsed_time(e1))
+        e2e = {"value": cfg.T * Ke * dist.world / (et * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": cfg.T * cfg.E * 4 + 2 * cfg.T * cfg.d * 2,
+               "d2h_bytes_per_step": cfg.T * cfg.d * 2, "steps": Ke,
+               "us_per_layer": 1e3 * et / Ke}
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, one GPU only) ----
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        n, el = time_oracle(cfg, keep_host, budget_s=args.cpu_seconds)
+        cpu = {"value": n / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} single-token steps of layer 0 ({cfg.name}) through the FP32 C++ oracle, "
+                         f"{el:.1f} s on 1 host thread"}
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": dist.world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": t_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic (seeded moe_inputs workload; random NVFP4 weights)",
+        "config": {
+            "workload": WORKLOAD[cfg.name], "T": cfg.T, "d": cfg.d, "ffn": cfg.ffn, "E": cfg.E, "k": cfg.k,
+            "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU",
+            "algo": args.algo, "weights": "NVFP4 (E2M1 + E4M3/16 + FP32)", "mma": "FP16 x FP16 -> FP32",
+            "layers_cycled": L, "l2": f"inputs larger than L2: {L} layer weight sets "
+                                      f"({L * cfg.E * bpe / 1e9:.1f} GB) cycled",
+            "timing": f"CUDA graphs of {L} layer calls replayed; events on the launch stream",
+            "us_per_layer": us_per_layer,
+            "unique_experts_mean": sum(U[l] for l in steps_layers) / K,
+            "unique_bytes_mean": mean_unique,
+            "hbm_frac_layer": (mean_unique / (us_per_layer * 1e-6) / 1e9) / peak,
+            "input_gen_s": round(t_gen, 1),
+        },
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "expert_tc_kernel" if algo == moe.ALGO_TCGEN05 else "simt kernels",
+                     "kernel_us": 1e3 * k_avg_ms, "peak_kind": f"{peak_kind} copy bandwidth",
+                     "algorithmic_bytes": "unique experts x 1769472 B + BF16 hidden/residual/out"},
+        "clocks": clocks,
+        "gpu_launches": kernels_per_step * K,
+        "device_status": status,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
+
+
+def main():
+    args = parse_args()
+    cfg = mi.CONFIGS[args.config]
+    import torch
+    dist = Dist(torch)
+    try:
+        if args.impl == "reference":
+            line = reference_arm(args, cfg, dist)
+        else:
+            if not torch.cuda.is_available():
+                raise SystemExit("bench.py: no CUDA device (the CUDA path has no CPU fallback)")
+            line = our_arm(args, cfg, dist, torch)
+        if dist.rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

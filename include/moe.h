@@ -1,0 +1,201 @@
+/*
+ * libroutedmoe: routed mixture-of-experts layer for speculative-decode verify steps and
+ * prefill chunks on GB300 (sm_103a).  C ABI over plain pointers; no C++ or torch types.
+ *
+ * The layer (token t, hidden x_t in BF16, router logits l_t in FP32):
+ *   1. router   p = softmax(l_t) over E experts; the k largest logits are selected
+ *               (larger first, equal values -> lower expert index); the selected
+ *               probabilities are renormalised to sum to one.
+ *   2. experts  for each selected expert e with weight w:
+ *                 g = x W13[e][0:F]^T,  u = x W13[e][F:2F]^T,  h = silu(g) * u,
+ *                 y = h W2[e]^T
+ *   3. un-route out_t = residual_t + sum_{j<k} w_j y_j   (slots summed in order, BF16 out)
+ * Expert weights are NVFP4: E2M1 codes (two per byte, element 2i in the low nibble),
+ * one E4M3 scale per 16 consecutive elements along the reduction dimension, and one
+ * FP32 scale per tensor.
+ *
+ * Passages that define the operations (pages on the Qwen3.8-Flash-Next MoE path):
+ *   - "How I forked vLLM and made Qwen3.8-Flash-Next decode 1.6x faster on one GPU":
+ *     section "The model and the constraint" (512 experts, top-10, NVFP4 experts) and
+ *     section "5. Hand-written kernels", paragraph "Fused MoE routing" (warp-per-token
+ *     softmax, top-k arg-max on float keys, lowest id wins ties, counts / scan /
+ *     scatter of routes to experts).
+ *   - "Persistent execution for Flash-Next GGUF on SM70": section "First implementation
+ *     boundary" (router GEMV outside the boundary; compact expert-presence list with
+ *     route positions; workers over (expert, output stripe) tasks that load each
+ *     expert's weights once; gate/up with SiLU*multiply publishing per-expert
+ *     readiness; down fused with the weighted unroute, routes summed in a fixed order,
+ *     no arrival-ordered float atomics); section "MonoMoE" (precomputed router logits
+ *     are the input; explicit ordering, valid zero intermediates, deterministic output
+ *     reduction); the paragraph on epoch/workspace ownership under graph replays.
+ *   - "How I forked vLLM ...", section "5. Hand-written kernels", paragraph "PDL
+ *     weight-prefetch GEMV": fixed-size workspace that CUDA graphs never see replaced.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers, row-major, 16-byte aligned, owned by the
+ *     caller; the library allocates no device memory and keeps no per-call state
+ *     outside the caller's workspace (only a read-only per-device property cache).
+ *   - Work is enqueued asynchronously on `stream` (0 = legacy default stream); no
+ *     host synchronisation, no device-to-host copy, no host-visible size depends on
+ *     data, so every call can be captured in a CUDA graph.
+ *   - Host-detectable errors (null pointers, unsupported shapes, misalignment, a
+ *     workspace that is too small) return a negative moe_status before anything is
+ *     enqueued.  Device-detected conditions (an expert id out of range, a bounded wait
+ *     that gave up, hidden values outside FP16 range, an FP16 intermediate that
+ *     saturated) are OR-ed into a status word inside the workspace; read it with
+ *     moe_read_device_status after synchronising the stream.
+ *   - Calls on distinct workspaces may run concurrently; calls sharing a workspace
+ *     must be ordered on one stream.
+ */
+#ifndef ROUTED_MOE_H
+#define ROUTED_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned pointer */
+  MOE_ERR_UNSUPPORTED = -2, /* shape outside what the kernels implement (see moe_shape) */
+  MOE_ERR_WORKSPACE = -3,   /* workspace null, misaligned or smaller than moe_workspace_bytes */
+  MOE_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed (no device, launch error) */
+  MOE_ERR_DEVICE = -5       /* moe_read_device_status found device-side error bits */
+} moe_status;
+
+/* Device status bits (OR-ed into the workspace status word by kernels). */
+#define MOE_DEV_BAD_EXPERT_ID 0x1u  /* a routing id was outside [0, E) in moe_plan */
+#define MOE_DEV_TIMEOUT 0x2u        /* a bounded wait in the expert kernel gave up */
+#define MOE_DEV_HIDDEN_RANGE 0x4u   /* |hidden| exceeded the FP16 range (65504) */
+#define MOE_DEV_H_SATURATED 0x8u    /* |silu(g)*u| exceeded 2^4 * 65504 and was clamped */
+
+/* Layer shape.  T tokens (rows of the call), d hidden size, ffn expert intermediate
+ * size, E experts, k experts per token.  Supported: 1 <= T <= 65536, 1 <= k <= 32,
+ * k <= E <= 1024, d % 128 == 0, ffn % 128 == 0, 128 <= d <= 16384, 128 <= ffn <= 8192. */
+typedef struct moe_shape {
+  int32_t T, d, ffn, E, k;
+} moe_shape;
+
+/* Expert-kernel selection for moe_forward_algo. */
+typedef enum moe_algo {
+  MOE_ALGO_AUTO = 0,     /* the tensor-core persistent kernel */
+  MOE_ALGO_TCGEN05 = 1,  /* persistent stripe kernel: TMA weight stream, in-register NVFP4
+                            dequantisation into tensor memory, tcgen05 MMA (FP32 accumulate),
+                            readiness counters between gate/up and down, fused un-route */
+  MOE_ALGO_SIMT = 2      /* CUDA-core kernels, one launch per stage (ablation baseline) */
+} moe_algo;
+
+/* Human-readable name of a status code (static string, never NULL). */
+MOE_API const char* moe_status_string(int status);
+
+/* Message of the last failed CUDA call made by this library on the calling host thread
+ * (empty string if none).  Static thread-local storage, never NULL. */
+MOE_API const char* moe_last_cuda_error(void);
+
+/* Bytes of device workspace needed for `shape` (0 if the shape is unsupported).
+ * The workspace holds the routing plan, per-call counters, the FP16 copy of the
+ * hidden rows, the gate/up intermediate, per-route down outputs and the status word.
+ * It must be 256-byte aligned.  Pure host function: needs no GPU. */
+MOE_API size_t moe_workspace_bytes(const moe_shape* shape);
+
+/* Zero the status word of a freshly allocated workspace (enqueued on `stream`).  Call once
+ * after allocation; every other field is (re)written by moe_plan / moe_forward. */
+MOE_API int moe_workspace_init(void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Check a shape without touching the GPU: MOE_OK, MOE_ERR_INVALID_ARG or
+ * MOE_ERR_UNSUPPORTED. */
+MOE_API int moe_check_shape(const moe_shape* shape);
+
+/* Step 1, router ("Fused MoE routing"; "Router: selection and expert-task production").
+ *   logits  [T, E]  float32, finite values (non-finite logits are outside the contract)
+ *   ids     [T, k]  int32 out: selected experts in selection order (value desc, ties to
+ *                   the lower index; -0 and +0 compare equal)
+ *   weights [T, k]  float32 out: renormalised softmax probabilities of the selection
+ * One warp per token. */
+MOE_API int moe_route_topk(const moe_shape* shape, const float* logits, int32_t* ids, float* weights,
+                   moe_stream_t stream);
+
+/* Step 2, bucketing ("First implementation boundary", step 1): per-expert route counts,
+ * their exclusive prefix sum, the ascending list of touched experts, each route's
+ * position in expert-major order, the per-expert task prefix sums used by the expert
+ * kernel, and a copy of the routing weights, all written into `workspace`.
+ *   ids     [T, k] int32, values in [0, E) (violations set MOE_DEV_BAD_EXPERT_ID)
+ *   weights [T, k] float32
+ * Must precede every moe_forward whose routing changed. */
+MOE_API int moe_plan(const moe_shape* shape, const int32_t* ids, const float* weights, void* workspace,
+             size_t workspace_bytes, moe_stream_t stream);
+
+/* Steps 3-4, experts and un-route, using the plan in `workspace`:
+ *   hidden     [T, d]          BF16, |values| <= 65504
+ *   w13_codes  [E, 2*ffn, d/2] uint8 E2M1 pairs; rows [0, ffn) gate, [ffn, 2*ffn) up
+ *   w13_scales [E, 2*ffn, d/16] uint8 E4M3 block scales
+ *   w13_scale  FP32 tensor scale of W13
+ *   w2_codes   [E, d, ffn/2]   uint8 E2M1 pairs
+ *   w2_scales  [E, d, ffn/16]  uint8 E4M3 block scales
+ *   w2_scale   FP32 tensor scale of W2
+ *   residual   [T, d] BF16 or NULL (treated as zero)
+ *   out        [T, d] BF16; may alias residual (each element is read before written)
+ * Every moe_forward re-zeroes the counters it uses, so it may be repeated on one plan.
+ * moe_forward is moe_forward_algo(..., MOE_ALGO_AUTO). */
+MOE_API int moe_forward(const moe_shape* shape, const void* hidden, const uint8_t* w13_codes,
+                const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes,
+                const uint8_t* w2_scales, float w2_scale, const void* residual, void* out,
+                void* workspace, size_t workspace_bytes, moe_stream_t stream);
+MOE_API int moe_forward_algo(const moe_shape* shape, const void* hidden, const uint8_t* w13_codes,
+                     const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes,
+                     const uint8_t* w2_scales, float w2_scale, const void* residual, void* out,
+                     void* workspace, size_t workspace_bytes, int algo, moe_stream_t stream);
+
+/* The two halves of moe_forward_algo, for callers that schedule them separately:
+ * moe_forward_prepare zeroes the counters of the call and stages `hidden` as FP16 in the
+ * workspace (one small kernel); moe_forward_experts runs the expert kernel(s) on that
+ * staging and the plan.  Arguments as for moe_forward_algo. */
+MOE_API int moe_forward_prepare(const moe_shape* shape, const void* hidden, void* workspace,
+                                size_t workspace_bytes, moe_stream_t stream);
+MOE_API int moe_forward_experts(const moe_shape* shape, const uint8_t* w13_codes,
+                                const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes,
+                                const uint8_t* w2_scales, float w2_scale, const void* residual,
+                                void* out, void* workspace, size_t workspace_bytes, int algo,
+                                moe_stream_t stream);
+
+/* Whole layer: moe_route_topk + moe_plan + moe_forward on one stream, with ids/weights
+ * written to the caller's [T, k] buffers. */
+MOE_API int moe_layer(const moe_shape* shape, const float* logits, const void* hidden,
+              const uint8_t* w13_codes, const uint8_t* w13_scales, float w13_scale,
+              const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+              const void* residual, void* out, int32_t* ids, float* weights, void* workspace,
+              size_t workspace_bytes, moe_stream_t stream);
+
+/* Copy the device status word to *status_bits (blocking copy on `stream`; call after the
+ * work of interest has been enqueued) and clear it when `clear` is non-zero.  Returns
+ * MOE_OK if no bit is set, MOE_ERR_DEVICE if any is. */
+MOE_API int moe_read_device_status(const void* workspace, int clear, uint32_t* status_bits,
+                           moe_stream_t stream);
+
+/* Read back the plan summary: number of touched experts U and the largest per-expert
+ * row count (blocking copy on `stream`; diagnostic use, e.g. for byte accounting). */
+MOE_API int moe_plan_summary(const moe_shape* shape, const void* workspace, int32_t* touched_experts,
+                     int32_t* max_rows, moe_stream_t stream);
+
+/* Device-side plan arrays inside the workspace, for tests: pointers to counts [E],
+ * offsets [E+1], touched [E] (first U valid), route_pos [T*k] (position of route
+ * t*k+j in expert-major order) and pos_token [T*k].  Returns MOE_OK or an error. */
+MOE_API int moe_plan_views(const moe_shape* shape, void* workspace, int32_t** counts, int32_t** offsets,
+                   int32_t** touched, int32_t** route_pos, int32_t** pos_token);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROUTED_MOE_H */

@@ -1,0 +1,44 @@
+/*
+ * Self-test entry points of libroutedmoe: each runs one building block of the expert
+ * kernel in isolation so that tests can check it against host-computed expectations.
+ * They are not part of the layer; the paper has no counterpart for them.
+ *
+ * All pointers are device pointers owned by the caller; work is enqueued on `stream`.
+ * Return values are moe_status codes (see moe.h).
+ */
+#ifndef ROUTED_MOE_SELFTEST_H
+#define ROUTED_MOE_SELFTEST_H
+
+#include <stdint.h>
+
+#include "moe.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* NVFP4 decode as used by the dequantisation warps.
+ *   words  [n] uint32: eight E2M1 codes each (element 2i in the low nibble of byte i)
+ *   out    [4n] uint32: f16x2 values, out[4w + b] = (element 2b, element 2b+1) of word w
+ *   pairs  [m] uint32: two E4M3 bytes in the low 16 bits (low byte -> low half)
+ *   sout   [m] uint32: f16x2 of the two scale values */
+MOE_API int moe_selftest_decode(const uint32_t* words, int n, uint32_t* out, const uint32_t* pairs, int m,
+                                uint32_t* sout, moe_stream_t stream);
+
+/* One TMA load of a 64-byte x 64-row box of a [rows, row_bytes] uint8 matrix at byte
+ * column x (a multiple of 16) and row y, with the 64-byte swizzle the expert kernel
+ * uses; out [4096] receives the raw shared-memory image. */
+MOE_API int moe_selftest_tma(const uint8_t* src, int rows, int row_bytes, int x, int y, uint8_t* out,
+                             moe_stream_t stream);
+
+/* One 128 x 16 x 128 product on the tensor core the way the expert kernel issues it:
+ * A [128, 128] FP16 (row-major) written to tensor memory by 128 threads, B [16, 128]
+ * FP16 (row-major) stored in shared memory in 128-byte swizzled K-major atoms, eight
+ * kind::f16 MMAs with FP32 accumulation, result D [128, 16] FP32 (row-major) = A B^T. */
+MOE_API int moe_selftest_mma(const void* A, const void* B, float* D, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROUTED_MOE_SELFTEST_H */

@@ -53,16 +53,31 @@ float bf16_to_float(uint16_t bits) {
   return f;
 }
 
+// The two decode functions tabulated once (16 and 256 entries): the tables hold exactly
+// the values of e2m1_exact / e4m3_exact, so lookups change nothing but speed.
+struct DecodeTables {
+  double e2m1[16];
+  double e4m3[256];
+  DecodeTables() {
+    for (uint32_t i = 0; i < 16; ++i) e2m1[i] = e2m1_exact(i);
+    for (uint32_t i = 0; i < 256; ++i) e4m3[i] = e4m3_exact(i);
+  }
+};
+const DecodeTables& tables() {
+  static const DecodeTables t;
+  return t;
+}
+
 // One NVFP4 weight: code nibble c of a row (element 2i in the low nibble of byte i),
 // its block scale (one E4M3 per 16 consecutive elements) and the tensor scale.  The
 // product of an E2M1 value, an E4M3 value and an FP32 scale is formed in Acc; for
 // float it is exact whenever the tensor scale is a power of two (6 significant bits).
 template <typename Acc>
-Acc nvfp4_weight(const uint8_t* codes, const uint8_t* scales, float tensor_scale, int c) {
+Acc nvfp4_weight(const DecodeTables& tb, const uint8_t* codes, const uint8_t* scales, float tensor_scale, int c) {
   const uint32_t byte = codes[c >> 1];
   const uint32_t nib = (c & 1) ? (byte >> 4) : (byte & 15u);
-  const Acc v = static_cast<Acc>(e2m1_exact(nib));
-  const Acc s = static_cast<Acc>(e4m3_exact(scales[c >> 4]));
+  const Acc v = static_cast<Acc>(tb.e2m1[nib]);
+  const Acc s = static_cast<Acc>(tb.e4m3[scales[c >> 4]]);
   return v * s * static_cast<Acc>(tensor_scale);
 }
 
@@ -127,6 +142,7 @@ int moe_experts(int T, int d, int F, int E, int k, const uint16_t* hidden, const
                 const uint8_t* w2c, const uint8_t* w2s, float w2_ts, const uint16_t* residual,
                 const uint8_t* mask, Acc* out) {
   if (T < 0 || d <= 0 || F <= 0 || E <= 0 || k <= 0 || k > E || d % 16 || F % 16) return -1;
+  const DecodeTables& tb = tables();
   const size_t d2 = static_cast<size_t>(d) / 2, d16 = static_cast<size_t>(d) / 16;
   const size_t f2 = static_cast<size_t>(F) / 2, f16 = static_cast<size_t>(F) / 16;
   std::vector<Acc> x(d), g(F), u(F), h(F), y(d), acc(d);
@@ -141,8 +157,8 @@ int moe_experts(int T, int d, int F, int E, int k, const uint16_t* hidden, const
         const size_t rg = static_cast<size_t>(e) * 2 * F + n;      // gate row
         const size_t ru = static_cast<size_t>(e) * 2 * F + F + n;  // up row
         Acc sg = 0, su = 0;
-        for (int c = 0; c < d; ++c) sg += x[c] * nvfp4_weight<Acc>(w13c + rg * d2, w13s + rg * d16, w13_ts, c);
-        for (int c = 0; c < d; ++c) su += x[c] * nvfp4_weight<Acc>(w13c + ru * d2, w13s + ru * d16, w13_ts, c);
+        for (int c = 0; c < d; ++c) sg += x[c] * nvfp4_weight<Acc>(tb, w13c + rg * d2, w13s + rg * d16, w13_ts, c);
+        for (int c = 0; c < d; ++c) su += x[c] * nvfp4_weight<Acc>(tb, w13c + ru * d2, w13s + ru * d16, w13_ts, c);
         g[n] = sg;
         u[n] = su;
       }
@@ -150,7 +166,7 @@ int moe_experts(int T, int d, int F, int E, int k, const uint16_t* hidden, const
       for (int r = 0; r < d; ++r) {
         const size_t rr = static_cast<size_t>(e) * d + r;
         Acc s = 0;
-        for (int n = 0; n < F; ++n) s += h[n] * nvfp4_weight<Acc>(w2c + rr * f2, w2s + rr * f16, w2_ts, n);
+        for (int n = 0; n < F; ++n) s += h[n] * nvfp4_weight<Acc>(tb, w2c + rr * f2, w2s + rr * f16, w2_ts, n);
         y[r] = s;
       }
       const Acc wj = weights[static_cast<size_t>(t) * k + j];
@@ -175,7 +191,7 @@ float oracle_e4m3_value(uint32_t byte) { return static_cast<float>(e4m3_exact(by
 int oracle_dequant_row(const uint8_t* codes, const uint8_t* scales, float tensor_scale, int K,
                        float* out) {
   if (K <= 0 || K % 16) return -1;
-  for (int c = 0; c < K; ++c) out[c] = nvfp4_weight<float>(codes, scales, tensor_scale, c);
+  for (int c = 0; c < K; ++c) out[c] = nvfp4_weight<float>(tables(), codes, scales, tensor_scale, c);
   return 0;
 }
 

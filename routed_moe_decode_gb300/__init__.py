@@ -1,0 +1,22 @@
+"""Routed mixture-of-experts layer (softmax top-k router, NVFP4 experts, fused un-route)
+for GB300 (sm_103a): the C-ABI library libroutedmoe.so plus a thin ctypes binding.
+
+High-level use (torch tensors on a CUDA device):
+
+    import routed_moe_decode_gb300 as moe
+    layer = moe.MoeLayer(T, d, ffn, E, k)
+    out = layer(logits, hidden, weights, residual)     # weights: dict of NVFP4 tensors
+
+The package contains no compute of its own: every step runs in the library's kernels.
+"""
+from ._lib import (ALGO_AUTO, ALGO_SIMT, ALGO_TCGEN05, MOE_DEV_BAD_EXPERT_ID, MOE_DEV_H_SATURATED,
+                   MOE_DEV_HIDDEN_RANGE, MOE_DEV_TIMEOUT, MoeError, Shape, Workspace, check_shape, forward,
+                   forward_experts, forward_prepare,
+                   layer, lib, plan, plan_summary, plan_views, read_status, route_topk, shape_of,
+                   workspace_bytes)
+from .layer import MoeLayer
+
+__all__ = ["ALGO_AUTO", "ALGO_SIMT", "ALGO_TCGEN05", "MOE_DEV_BAD_EXPERT_ID", "MOE_DEV_H_SATURATED",
+           "MOE_DEV_HIDDEN_RANGE", "MOE_DEV_TIMEOUT", "MoeError", "MoeLayer", "Shape", "Workspace",
+           "check_shape", "forward", "forward_experts", "forward_prepare", "layer", "lib", "plan", "plan_summary", "plan_views", "read_status",
+           "route_topk", "shape_of", "workspace_bytes"]

@@ -1,0 +1,201 @@
+"""ctypes binding of libroutedmoe.so: argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels; this module turns torch
+tensors into device pointers and the current torch stream into a cudaStream_t.  If the
+shared library has not been built, every call raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libroutedmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_WORKSPACE = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_DEVICE = -5
+
+MOE_DEV_BAD_EXPERT_ID = 0x1
+MOE_DEV_TIMEOUT = 0x2
+MOE_DEV_HIDDEN_RANGE = 0x4
+MOE_DEV_H_SATURATED = 0x8
+
+ALGO_AUTO = 0
+ALGO_TCGEN05 = 1
+ALGO_SIMT = 2
+
+# Every function declared in include/moe.h, with (restype, argtypes).
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("ffn", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32)]
+
+
+_SP = ctypes.POINTER(Shape)
+SIGNATURES = {
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_last_cuda_error": (ctypes.c_char_p, []),
+    "moe_workspace_bytes": (ctypes.c_size_t, [_SP]),
+    "moe_workspace_init": (_I, [_P, ctypes.c_size_t, _P]),
+    "moe_check_shape": (_I, [_SP]),
+    "moe_route_topk": (_I, [_SP, _P, _P, _P, _P]),
+    "moe_plan": (_I, [_SP, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_forward": (_I, [_SP, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_forward_algo": (_I, [_SP, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _I, _P]),
+    "moe_forward_prepare": (_I, [_SP, _P, _P, ctypes.c_size_t, _P]),
+    "moe_forward_experts": (_I, [_SP, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _I, _P]),
+    "moe_layer": (_I, [_SP, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_read_device_status": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint32), _P]),
+    "moe_plan_summary": (_I, [_SP, _P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), _P]),
+    "moe_plan_views": (_I, [_SP, _P] + [ctypes.POINTER(ctypes.c_void_p)] * 5),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, rc):
+        msg = lib().moe_status_string(rc).decode()
+        extra = lib().moe_last_cuda_error().decode()
+        super().__init__(f"{fn} -> {rc} ({msg}){': ' + extra if extra and rc == MOE_ERR_CUDA else ''}")
+        self.rc = rc
+
+
+def lib():
+    """The loaded shared library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build the CUDA extension first "
+                                   "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(fn, rc):
+    if rc != MOE_OK:
+        raise MoeError(fn, rc)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def shape_of(T, d, ffn, E, k) -> Shape:
+    return Shape(int(T), int(d), int(ffn), int(E), int(k))
+
+
+def workspace_bytes(shape: Shape) -> int:
+    return int(lib().moe_workspace_bytes(ctypes.byref(shape)))
+
+
+def check_shape(shape: Shape) -> int:
+    return int(lib().moe_check_shape(ctypes.byref(shape)))
+
+
+class Workspace:
+    """Caller-owned device workspace for one shape (allocated through torch)."""
+
+    def __init__(self, shape: Shape, device="cuda", stream=None):
+        self.shape = shape
+        self.nbytes = workspace_bytes(shape)
+        if self.nbytes == 0:
+            raise MoeError("moe_workspace_bytes", MOE_ERR_UNSUPPORTED)
+        self.buf = torch.empty(self.nbytes + 256, dtype=torch.uint8, device=device)
+        off = (-self.buf.data_ptr()) % 256
+        self.tensor = self.buf[off:off + self.nbytes]
+        _check("moe_workspace_init", lib().moe_workspace_init(_ptr(self.tensor), self.nbytes, _stream(stream)))
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.tensor.data_ptr())
+
+
+def route_topk(shape: Shape, logits, ids, weights, stream=None):
+    _check("moe_route_topk", lib().moe_route_topk(ctypes.byref(shape), _ptr(logits), _ptr(ids), _ptr(weights),
+                                                  _stream(stream)))
+
+
+def plan(shape: Shape, ids, weights, ws: Workspace, stream=None):
+    _check("moe_plan", lib().moe_plan(ctypes.byref(shape), _ptr(ids), _ptr(weights), ws.ptr, ws.nbytes,
+                                      _stream(stream)))
+
+
+def forward(shape: Shape, hidden, w: dict, residual, out, ws: Workspace, algo: int = ALGO_AUTO, stream=None):
+    _check("moe_forward_algo", lib().moe_forward_algo(
+        ctypes.byref(shape), _ptr(hidden), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]), float(w["w13_ts"]),
+        _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]), _ptr(residual), _ptr(out), ws.ptr,
+        ws.nbytes, int(algo), _stream(stream)))
+
+
+def forward_prepare(shape: Shape, hidden, ws: Workspace, stream=None):
+    _check("moe_forward_prepare", lib().moe_forward_prepare(ctypes.byref(shape), _ptr(hidden), ws.ptr, ws.nbytes,
+                                                            _stream(stream)))
+
+
+def forward_experts(shape: Shape, w: dict, residual, out, ws: Workspace, algo: int = ALGO_AUTO, stream=None):
+    _check("moe_forward_experts", lib().moe_forward_experts(
+        ctypes.byref(shape), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]), float(w["w13_ts"]),
+        _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]), _ptr(residual), _ptr(out), ws.ptr,
+        ws.nbytes, int(algo), _stream(stream)))
+
+
+def layer(shape: Shape, logits, hidden, w: dict, residual, out, ids, weights, ws: Workspace, stream=None):
+    _check("moe_layer", lib().moe_layer(
+        ctypes.byref(shape), _ptr(logits), _ptr(hidden), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]),
+        float(w["w13_ts"]), _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]), _ptr(residual),
+        _ptr(out), _ptr(ids), _ptr(weights), ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def read_status(ws: Workspace, clear: bool = True, stream=None) -> int:
+    bits = ctypes.c_uint32(0)
+    rc = lib().moe_read_device_status(ws.ptr, 1 if clear else 0, ctypes.byref(bits), _stream(stream))
+    if rc not in (MOE_OK, MOE_ERR_DEVICE):
+        raise MoeError("moe_read_device_status", rc)
+    return int(bits.value)
+
+
+def plan_summary(shape: Shape, ws: Workspace, stream=None):
+    u = ctypes.c_int32(0)
+    m = ctypes.c_int32(0)
+    _check("moe_plan_summary", lib().moe_plan_summary(ctypes.byref(shape), ws.ptr, ctypes.byref(u),
+                                                      ctypes.byref(m), _stream(stream)))
+    return int(u.value), int(m.value)
+
+
+def plan_views(shape: Shape, ws: Workspace):
+    """Device tensors viewing the plan arrays inside the workspace."""
+    ptrs = [ctypes.c_void_p() for _ in range(5)]
+    _check("moe_plan_views", lib().moe_plan_views(ctypes.byref(shape), ws.ptr, *[ctypes.byref(p) for p in ptrs]))
+    base = ws.tensor.data_ptr()
+    R = shape.T * shape.k
+    sizes = [shape.E, shape.E + 1, shape.E, R, R]
+    out = []
+    for p, n in zip(ptrs, sizes):
+        off = p.value - base
+        out.append(ws.tensor[off:off + 4 * n].view(torch.int32))
+    return dict(zip(("counts", "offsets", "touched", "route_pos", "pos_token"), out))

@@ -1,0 +1,361 @@
+// Host entry points of the C ABI declared in include/moe.h.
+#include <cuda.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "moe_kernels.cuh"
+
+namespace {
+
+using moe::WsLayout;
+
+thread_local char g_last_error[256] = "";
+
+void set_error(const char* where, cudaError_t e) {
+  snprintf(g_last_error, sizeof g_last_error, "%s: %s", where, cudaGetErrorString(e));
+}
+
+// Per-device launch properties, filled once per device and read-only afterwards.
+struct DeviceInfo {
+  int num_sms = 0;
+  bool ready = false;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { set_error("cudaGetDevice", e); return MOE_ERR_CUDA; }
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!g_dev[dev].ready) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) { set_error("cudaDeviceGetAttribute", e); return MOE_ERR_CUDA; }
+    g_dev[dev].num_sms = sms;
+    g_dev[dev].ready = true;
+  }
+  *out = g_dev[dev];
+  return MOE_OK;
+}
+
+int get_encoder(EncodeTiledFn* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  *fn = g_encode;
+  return g_encode ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace moe {
+
+// 2-D uint8 tensor map over a [rows, row_bytes] code matrix: 64-byte x 64-row boxes,
+// 64-byte swizzle (conflict-free row-per-thread reads of 16-byte chunks).
+int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows) {
+  EncodeTiledFn enc = nullptr;
+  if (get_encoder(&enc) != MOE_OK) { snprintf(g_last_error, sizeof g_last_error, "no cuTensorMapEncodeTiled"); return MOE_ERR_CUDA; }
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+namespace {
+
+using moe::encode_codes_map;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_shape(const moe_shape* s) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (s->T < 0 || s->d <= 0 || s->ffn <= 0 || s->E <= 0 || s->k <= 0) return MOE_ERR_INVALID_ARG;
+  if (s->k > s->E) return MOE_ERR_INVALID_ARG;
+  if (s->T > 65536 || s->k > 32 || s->E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (s->d % 128 || s->ffn % 128 || s->d < 128 || s->ffn < 128 || s->d > 16384 || s->ffn > 8192)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int check_ws(const moe_shape* s, const void* ws, size_t bytes) {
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  if (bytes < moe::ws_layout(*s).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+moe::ExpertArgs expert_args(const moe_shape* s, const WsLayout& L, void* ws, const uint8_t* w13c,
+                            const uint8_t* w13s, float w13_ts, const uint8_t* w2c, const uint8_t* w2s, float w2_ts,
+                            const void* residual, void* out) {
+  moe::ExpertArgs a{};
+  a.T = s->T; a.d = s->d; a.F = s->ffn; a.E = s->E; a.k = s->k; a.R = L.R;
+  a.KS = L.KS; a.S_gu = L.S_gu; a.S_dn = L.S_dn;
+  a.nck_gu = s->d / L.KS / moe::kChunkK;
+  a.nck_dn = s->ffn / moe::kChunkK;
+  a.w13_ts = w13_ts; a.w2_ts = w2_ts;
+  a.w13_codes = w13c; a.w13_scales = w13s; a.w2_codes = w2c; a.w2_scales = w2s;
+  a.meta = at<int>(ws, L.meta);
+  a.counts = at<int>(ws, L.counts);
+  a.offsets = at<int>(ws, L.offsets);
+  a.touched = at<int>(ws, L.touched);
+  a.gu_start = at<int>(ws, L.gu_start);
+  a.dn_start = at<int>(ws, L.dn_start);
+  a.pos_tok = at<int>(ws, L.pos_tok);
+  a.route_pos = at<int>(ws, L.route_pos);
+  a.route_w = at<float>(ws, L.route_w);
+  a.x16 = at<__half>(ws, L.x16);
+  a.hs16 = at<__half>(ws, L.hs16);
+  a.gu_part = at<float>(ws, L.gu_part);
+  a.y = at<float>(ws, L.y);
+  a.ready = at<uint32_t>(ws, L.ready);
+  a.cnt_gu = at<uint32_t>(ws, L.cnt_gu);
+  a.comb_cnt = at<uint32_t>(ws, L.comb_cnt);
+  a.status = at<int>(ws, L.status);
+  a.residual = static_cast<const __nv_bfloat16*>(residual);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: null pointer, bad size or misaligned pointer";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: shape outside the implemented range";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace null, misaligned or too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE: device-side status bits are set";
+    default: return "unknown moe_status";
+  }
+}
+
+const char* moe_last_cuda_error(void) { return g_last_error; }
+
+int moe_check_shape(const moe_shape* shape) { return check_shape(shape); }
+
+size_t moe_workspace_bytes(const moe_shape* shape) {
+  if (check_shape(shape) != MOE_OK) return 0;
+  return moe::ws_layout(*shape).total;
+}
+
+int moe_workspace_init(void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return MOE_ERR_WORKSPACE;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, 256, stream);
+  if (e != cudaSuccess) { set_error("cudaMemsetAsync", e); return MOE_ERR_CUDA; }
+  return MOE_OK;
+}
+
+int moe_route_topk(const moe_shape* shape, const float* logits, int32_t* ids, float* weights,
+                   moe_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (shape->T == 0) return MOE_OK;
+  if (!logits || !ids || !weights || !aligned(logits, 16) || !aligned(ids, 4) || !aligned(weights, 4))
+    return MOE_ERR_INVALID_ARG;
+  cudaError_t e = moe::launch_route_topk(logits, shape->T, shape->E, shape->k, ids, weights, stream);
+  if (e != cudaSuccess) { set_error("route_topk launch", e); return MOE_ERR_CUDA; }
+  return MOE_OK;
+}
+
+int moe_plan(const moe_shape* shape, const int32_t* ids, const float* weights, void* workspace,
+             size_t workspace_bytes, moe_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (shape->T == 0) return MOE_OK;
+  if (!ids || !weights) return MOE_ERR_INVALID_ARG;
+  rc = check_ws(shape, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
+  const WsLayout L = moe::ws_layout(*shape);
+  moe::PlanArgs a{};
+  a.T = shape->T; a.E = shape->E; a.k = shape->k; a.KS = L.KS; a.S_gu = L.S_gu; a.S_dn = L.S_dn;
+  a.ids = ids; a.weights = weights;
+  a.status = at<int>(workspace, L.status);
+  a.meta = at<int>(workspace, L.meta);
+  a.counts = at<int>(workspace, L.counts);
+  a.offsets = at<int>(workspace, L.offsets);
+  a.touched = at<int>(workspace, L.touched);
+  a.gu_start = at<int>(workspace, L.gu_start);
+  a.dn_start = at<int>(workspace, L.dn_start);
+  a.route_pos = at<int>(workspace, L.route_pos);
+  a.pos_tok = at<int>(workspace, L.pos_tok);
+  a.route_w = at<float>(workspace, L.route_w);
+  cudaError_t e = moe::launch_plan(a, stream);
+  if (e != cudaSuccess) { set_error("plan launch", e); return MOE_ERR_CUDA; }
+  return MOE_OK;
+}
+
+int moe_forward_prepare(const moe_shape* shape, const void* hidden, void* workspace, size_t workspace_bytes,
+                        moe_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (shape->T == 0) return MOE_OK;
+  if (!hidden || !aligned(hidden, 16)) return MOE_ERR_INVALID_ARG;
+  rc = check_ws(shape, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
+  const WsLayout L = moe::ws_layout(*shape);
+  moe::PrepArgs p{};
+  p.T = shape->T; p.d = shape->d; p.E = shape->E; p.S_dn = L.S_dn; p.max_units = L.max_units;
+  p.hidden = static_cast<const __nv_bfloat16*>(hidden);
+  p.x16 = at<__half>(workspace, L.x16);
+  p.ready = at<uint32_t>(workspace, L.ready);
+  p.cnt_gu = at<uint32_t>(workspace, L.cnt_gu);
+  p.comb_cnt = at<uint32_t>(workspace, L.comb_cnt);
+  p.status = at<int>(workspace, L.status);
+  cudaError_t e = moe::launch_prep(p, stream);
+  if (e != cudaSuccess) { set_error("prep launch", e); return MOE_ERR_CUDA; }
+  return MOE_OK;
+}
+
+int moe_forward_experts(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
+                        float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+                        const void* residual, void* out, void* workspace, size_t workspace_bytes, int algo,
+                        moe_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (shape->T == 0) return MOE_OK;
+  if (!w13_codes || !w13_scales || !w2_codes || !w2_scales || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w13_codes, 16) || !aligned(w13_scales, 16) || !aligned(w2_codes, 16) || !aligned(w2_scales, 16) ||
+      !aligned(out, 16) || (residual && !aligned(residual, 16)))
+    return MOE_ERR_INVALID_ARG;
+  if (algo != MOE_ALGO_AUTO && algo != MOE_ALGO_TCGEN05 && algo != MOE_ALGO_SIMT) return MOE_ERR_INVALID_ARG;
+  rc = check_ws(shape, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
+  const WsLayout L = moe::ws_layout(*shape);
+  const moe::ExpertArgs a = expert_args(shape, L, workspace, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales,
+                                        w2_scale, residual, out);
+  cudaError_t e;
+  if (algo == MOE_ALGO_SIMT) {
+    e = moe::launch_expert_simt(a, stream);
+    if (e != cudaSuccess) { set_error("simt launch", e); return MOE_ERR_CUDA; }
+    return MOE_OK;
+  }
+  DeviceInfo di;
+  rc = device_info(&di);
+  if (rc != MOE_OK) return rc;
+  CUtensorMap tm13, tm2;
+  rc = encode_codes_map(&tm13, w13_codes, static_cast<uint64_t>(shape->d) / 2,
+                        static_cast<uint64_t>(shape->E) * 2 * shape->ffn);
+  if (rc != MOE_OK) return rc;
+  rc = encode_codes_map(&tm2, w2_codes, static_cast<uint64_t>(shape->ffn) / 2,
+                        static_cast<uint64_t>(shape->E) * shape->d);
+  if (rc != MOE_OK) return rc;
+  e = moe::launch_expert_tc(a, tm13, tm2, di.num_sms, stream);
+  if (e != cudaSuccess) { set_error("expert_tc launch", e); return MOE_ERR_CUDA; }
+  return MOE_OK;
+}
+
+int moe_forward_algo(const moe_shape* shape, const void* hidden, const uint8_t* w13_codes,
+                     const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes,
+                     const uint8_t* w2_scales, float w2_scale, const void* residual, void* out,
+                     void* workspace, size_t workspace_bytes, int algo, moe_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (shape->T == 0) return MOE_OK;
+  if (!hidden || !w13_codes || !w13_scales || !w2_codes || !w2_scales || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16)) return MOE_ERR_INVALID_ARG;
+  if (algo != MOE_ALGO_AUTO && algo != MOE_ALGO_TCGEN05 && algo != MOE_ALGO_SIMT) return MOE_ERR_INVALID_ARG;
+  rc = check_ws(shape, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
+  rc = moe_forward_prepare(shape, hidden, workspace, workspace_bytes, stream);
+  if (rc != MOE_OK) return rc;
+  return moe_forward_experts(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
+                             workspace, workspace_bytes, algo, stream);
+}
+
+int moe_forward(const moe_shape* shape, const void* hidden, const uint8_t* w13_codes, const uint8_t* w13_scales,
+                float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+                const void* residual, void* out, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  return moe_forward_algo(shape, hidden, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual,
+                          out, workspace, workspace_bytes, MOE_ALGO_AUTO, stream);
+}
+
+int moe_layer(const moe_shape* shape, const float* logits, const void* hidden, const uint8_t* w13_codes,
+              const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales,
+              float w2_scale, const void* residual, void* out, int32_t* ids, float* weights, void* workspace,
+              size_t workspace_bytes, moe_stream_t stream) {
+  int rc = moe_route_topk(shape, logits, ids, weights, stream);
+  if (rc != MOE_OK) return rc;
+  rc = moe_plan(shape, ids, weights, workspace, workspace_bytes, stream);
+  if (rc != MOE_OK) return rc;
+  return moe_forward(shape, hidden, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
+                     workspace, workspace_bytes, stream);
+}
+
+int moe_read_device_status(const void* workspace, int clear, uint32_t* status_bits, moe_stream_t stream) {
+  if (!workspace || !status_bits || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) { set_error("status read", e); return MOE_ERR_CUDA; }
+  if (clear) {
+    e = cudaMemsetAsync(const_cast<void*>(workspace), 0, sizeof v, stream);
+    if (e != cudaSuccess) { set_error("status clear", e); return MOE_ERR_CUDA; }
+  }
+  *status_bits = v;
+  return v ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+int moe_plan_summary(const moe_shape* shape, const void* workspace, int32_t* touched_experts, int32_t* max_rows,
+                     moe_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (!workspace || !aligned(workspace, 256) || !touched_experts || !max_rows) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = moe::ws_layout(*shape);
+  int32_t meta[moe::META_WORDS];
+  cudaError_t e = cudaMemcpyAsync(meta, static_cast<const char*>(workspace) + L.meta, sizeof meta,
+                                  cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) { set_error("plan summary", e); return MOE_ERR_CUDA; }
+  *touched_experts = meta[moe::META_U];
+  *max_rows = meta[moe::META_MAXROWS];
+  return MOE_OK;
+}
+
+int moe_plan_views(const moe_shape* shape, void* workspace, int32_t** counts, int32_t** offsets, int32_t** touched,
+                   int32_t** route_pos, int32_t** pos_token) {
+  int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (!workspace || !counts || !offsets || !touched || !route_pos || !pos_token) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = moe::ws_layout(*shape);
+  *counts = at<int32_t>(workspace, L.counts);
+  *offsets = at<int32_t>(workspace, L.offsets);
+  *touched = at<int32_t>(workspace, L.touched);
+  *route_pos = at<int32_t>(workspace, L.route_pos);
+  *pos_token = at<int32_t>(workspace, L.pos_tok);
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// Kernel argument blocks and host-side launchers of the routed-MoE CUDA path.
+#pragma once
+
+#include <cuda.h>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+struct PlanArgs {
+  int T, E, k, KS, S_gu, S_dn;
+  const int32_t* ids;
+  const float* weights;
+  int* status;
+  int* meta;
+  int* counts;
+  int* offsets;
+  int* touched;
+  int* gu_start;
+  int* dn_start;
+  int* route_pos;
+  int* pos_tok;
+  float* route_w;
+};
+
+struct PrepArgs {
+  int T, d, E, S_dn, max_units;
+  const __nv_bfloat16* hidden;
+  __half* x16;
+  uint32_t* ready;
+  uint32_t* cnt_gu;
+  uint32_t* comb_cnt;
+  int* status;
+};
+
+// Everything the expert kernels read besides the two tensor maps.
+struct ExpertArgs {
+  int T, d, F, E, k, R, KS, S_gu, S_dn, nck_gu, nck_dn;
+  float w13_ts, w2_ts;
+  const uint8_t* w13_codes;
+  const uint8_t* w13_scales;
+  const uint8_t* w2_codes;
+  const uint8_t* w2_scales;
+  const int* meta;
+  const int* counts;
+  const int* offsets;
+  const int* touched;
+  const int* gu_start;
+  const int* dn_start;
+  const int* pos_tok;
+  const int* route_pos;
+  const float* route_w;
+  const __half* x16;
+  __half* hs16;
+  float* gu_part;
+  float* y;
+  uint32_t* ready;
+  uint32_t* cnt_gu;
+  uint32_t* comb_cnt;
+  int* status;
+  const __nv_bfloat16* residual;
+  __nv_bfloat16* out;
+};
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* weights,
+                              cudaStream_t stream);
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream);
+cudaError_t launch_expert_tc(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
+                             int num_sms, cudaStream_t stream);
+cudaError_t launch_expert_simt(const ExpertArgs& a, cudaStream_t stream);
+size_t expert_tc_smem_bytes();
+int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows);
+
+}  // namespace moe

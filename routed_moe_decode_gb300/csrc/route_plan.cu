@@ -1,0 +1,224 @@
+// Router (softmax + top-k + renormalisation) and bucketing (plan) kernels.
+//
+// Router: one warp per token ("Fused MoE routing" in "How I forked vLLM and made
+// Qwen3.8-Flash-Next decode 1.6x faster on one GPU", section 5; "Router: selection and
+// expert-task production" in "Persistent execution for Flash-Next GGUF on SM70").  Lane
+// l holds logits l + 32 i.  The softmax denominator is a warp reduction; selection is k
+// rounds of a warp arg-max on order-preserving float keys with the lowest expert id
+// winning ties (redux.sync max of the key, then redux.sync min of the candidate ids).
+// Selection compares the logits; softmax is monotone, so this is the same selection as
+// on probabilities and keeps the ids independent of the exponential's rounding.
+//
+// Plan: one CTA.  Per-expert counts (shared-memory atomics), exclusive scan, the
+// ascending touched-expert list, each route's position in expert-major order, and the
+// per-touched-expert task prefix sums the expert kernel decodes its task ids with
+// ("First implementation boundary", step 1: compact expert-presence list plus the
+// original route positions; no gather of token features).
+#include <cfloat>
+
+#include "moe_common.cuh"
+#include "moe_kernels.cuh"
+
+namespace moe {
+
+constexpr uint32_t kFull = 0xffffffffu;
+
+template <int NPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                         int32_t* __restrict__ ids, float* __restrict__ weights) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const float* row = logits + static_cast<size_t>(t) * E;
+  float v[NPL];
+  uint32_t key[NPL];
+  float mx = -FLT_MAX;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    const bool ok = e < E;
+    v[i] = ok ? __ldg(row + e) : -FLT_MAX;
+    key[i] = ok ? float_key(v[i]) : 0u;  // 0 is below every real key: never selected
+    mx = fmaxf(mx, v[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    if (lane + 32 * i < E) s += expf(v[i] - mx);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+  const float z = s;
+
+  uint32_t used = 0;
+  int my_id = 0;
+  float my_p = 0.f;
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0;
+    int bi = -1;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      if (!((used >> i) & 1u) && key[i] > bk) {
+        bk = key[i];
+        bi = i;
+      }
+    }
+    const uint32_t kmax = __reduce_max_sync(kFull, bk);
+    const uint32_t cand = (bi >= 0 && bk == kmax) ? static_cast<uint32_t>(lane + 32 * bi) : 0xffffffffu;
+    const uint32_t idx = __reduce_min_sync(kFull, cand);
+    const int owner = static_cast<int>(idx & 31u);
+    const int slot = static_cast<int>(idx >> 5);
+    if (lane == owner) used |= 1u << slot;
+    float lv = 0.f;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) lv = (i == slot) ? v[i] : lv;
+    lv = __shfl_sync(kFull, lv, owner);
+    if (lane == j) {
+      my_id = static_cast<int>(idx);
+      my_p = expf(lv - mx) / z;
+    }
+  }
+  // renormalise over the selection, summed in slot order
+  float sel = 0.f;
+  for (int j = 0; j < k; ++j) sel += __shfl_sync(kFull, my_p, j);
+  if (lane < k) {
+    ids[static_cast<size_t>(t) * k + lane] = my_id;
+    weights[static_cast<size_t>(t) * k + lane] = my_p / sel;
+  }
+}
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* weights,
+                              cudaStream_t stream) {
+  const int npl = (E + 31) / 32;
+  const dim3 grid((T + 7) / 8), block(256);
+  if (npl <= 1) route_topk_kernel<1><<<grid, block, 0, stream>>>(logits, T, E, k, ids, weights);
+  else if (npl <= 2) route_topk_kernel<2><<<grid, block, 0, stream>>>(logits, T, E, k, ids, weights);
+  else if (npl <= 4) route_topk_kernel<4><<<grid, block, 0, stream>>>(logits, T, E, k, ids, weights);
+  else if (npl <= 8) route_topk_kernel<8><<<grid, block, 0, stream>>>(logits, T, E, k, ids, weights);
+  else if (npl <= 16) route_topk_kernel<16><<<grid, block, 0, stream>>>(logits, T, E, k, ids, weights);
+  else route_topk_kernel<32><<<grid, block, 0, stream>>>(logits, T, E, k, ids, weights);
+  return cudaGetLastError();
+}
+
+// Exclusive scan of one int per thread across a 1024-thread block; returns the total.
+__device__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(kFull, wi, o);
+      if (lane >= o) wi += n;
+    }
+    warp_sums[lane] = wi - w;  // exclusive warp offsets
+    if (lane == 31) warp_sums[32] = wi;
+  }
+  __syncthreads();
+  const int out = warp_sums[warp] + incl - v;
+  total = warp_sums[32];
+  __syncthreads();
+  return out;
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
+  __shared__ int s_counts[1024];
+  __shared__ int s_cursor[1024];
+  __shared__ int s_scan[33];
+  const int tid = threadIdx.x;
+  const int E = a.E, R = a.T * a.k;
+  if (tid < E) s_counts[tid] = 0;
+  __syncthreads();
+  for (int r = tid; r < R; r += blockDim.x) {
+    const int e = a.ids[r];
+    a.route_w[r] = a.weights[r];
+    if (e < 0 || e >= E) {
+      atomicOr(a.status, static_cast<int>(MOE_DEV_BAD_EXPERT_ID));
+    } else {
+      atomicAdd(&s_counts[e], 1);
+    }
+  }
+  __syncthreads();
+  const int cnt = tid < E ? s_counts[tid] : 0;
+  int total = 0;
+  const int off = block_exclusive_scan(cnt, s_scan, total);
+  const int flag = cnt > 0 ? 1 : 0;
+  int U = 0;
+  const int rank = block_exclusive_scan(flag, s_scan, U);
+  if (tid < E) {
+    a.counts[tid] = cnt;
+    a.offsets[tid] = off;
+    s_cursor[tid] = off;
+    if (flag) a.touched[rank] = tid;
+  }
+  if (tid == 0) a.offsets[E] = total;
+  // per touched expert: passes of kRowsPerPass rows, gate/up and down task counts
+  const int npass = flag ? (cnt + kRowsPerPass - 1) / kRowsPerPass : 0;
+  const int ngu = npass * a.S_gu * a.KS;
+  const int ndn = npass * a.S_dn;
+  // scatter per-touched values to thread `rank` through shared memory (reuse s_counts)
+  __syncthreads();
+  if (flag) s_counts[rank] = (ngu << 0);
+  __syncthreads();
+  int gu_total = 0;
+  const int gu_v = tid < U ? s_counts[tid] : 0;
+  const int gu_start = block_exclusive_scan(gu_v, s_scan, gu_total);
+  __syncthreads();
+  if (flag) s_counts[rank] = ndn;
+  __syncthreads();
+  int dn_total = 0;
+  const int dn_v = tid < U ? s_counts[tid] : 0;
+  const int dn_start = block_exclusive_scan(dn_v, s_scan, dn_total);
+  if (tid < U) {
+    a.gu_start[tid] = gu_start;
+    a.dn_start[tid] = dn_start;
+  }
+  if (tid == 0) {
+    a.gu_start[U] = gu_total;
+    a.dn_start[U] = dn_total;
+  }
+  // largest row count and number of gate/up units (pass, stripe) over touched experts
+  int mx = cnt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(kFull, mx, o));
+  if ((tid & 31) == 0) s_scan[tid >> 5] = mx;
+  __syncthreads();
+  if (tid == 0) {
+    int m = 0;
+    for (int w = 0; w < 32; ++w) m = max(m, s_scan[w]);
+    a.meta[META_U] = U;
+    a.meta[META_NGU] = gu_total;
+    a.meta[META_NDN] = dn_total;
+    a.meta[META_MAXROWS] = m;
+    a.meta[META_NUNITS] = gu_total / a.KS;
+  }
+  __syncthreads();
+  // route positions in expert-major order
+  for (int r = tid; r < R; r += blockDim.x) {
+    const int e = a.ids[r];
+    if (e < 0 || e >= E) {
+      a.route_pos[r] = -1;
+      continue;
+    }
+    const int pos = atomicAdd(&s_cursor[e], 1);
+    a.route_pos[r] = pos;
+    a.pos_tok[pos] = r / a.k;
+  }
+}
+
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
+  plan_kernel<<<1, 1024, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,60 @@
+"""Helpers of the GPU parity tests: upload seeded inputs, run the C-ABI path, compare."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import torch
+
+import moe_inputs as mi
+
+# Tolerance of the layer output against the FP32 oracle (max and mean relative error).
+MAX_ABS_OVER_RMS = 2e-2
+MEAN_REL = 5e-3
+WEIGHT_RTOL = 2e-6
+
+
+def bf16_tensor(bits: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def device_weights(inp: dict, dev) -> dict:
+    w = {n: torch.from_numpy(np.ascontiguousarray(inp[n])).to(dev)
+         for n in ("w13_codes", "w13_scales", "w2_codes", "w2_scales")}
+    w["w13_ts"], w["w2_ts"] = float(inp["w13_ts"]), float(inp["w2_ts"])
+    return w
+
+
+@functools.lru_cache(maxsize=8)
+def config_inputs(name: str, seed: int = 0, layer: int = 0) -> dict:
+    return mi.gen_layer(mi.CONFIGS[name], seed=seed, layer=layer)
+
+
+def run_layer(cfg, inp: dict, algo=0, dev="cuda", residual=True, w=None):
+    """Router + plan + experts through the C ABI.  Returns (ids, weights, out_f32, layer)."""
+    import routed_moe_decode_gb300 as moe
+    dev = torch.device(dev)
+    if w is None:
+        w = device_weights(inp, dev)
+    layer = moe.MoeLayer(cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k, device=dev, algo=algo)
+    logits = torch.from_numpy(np.ascontiguousarray(inp["logits"])).to(dev)
+    hidden = bf16_tensor(inp["hidden"], dev)
+    res = bf16_tensor(inp["residual"], dev) if residual else None
+    out = layer(logits, hidden, w, res)
+    torch.cuda.synchronize()
+    return layer.ids.cpu().numpy(), layer.weights.cpu().numpy(), out.float().cpu().numpy(), layer
+
+
+def parity_metrics(got: np.ndarray, ref: np.ndarray):
+    ref = ref.astype(np.float64)
+    err = np.abs(got.astype(np.float64) - ref)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    return float(err.max()) / rms, float(err.sum() / np.abs(ref).sum())
+
+
+def assert_parity(got: np.ndarray, ref: np.ndarray, what=""):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    mx, mean_rel = parity_metrics(got, ref)
+    assert mx <= MAX_ABS_OVER_RMS and mean_rel <= MEAN_REL, \
+        f"{what}: max|d|/rms {mx:.3e} (<= {MAX_ABS_OVER_RMS}), mean rel {mean_rel:.3e} (<= {MEAN_REL})"
+    return mx, mean_rel

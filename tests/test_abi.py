@@ -1,0 +1,82 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
+function its headers declare, sizes its workspace and rejects bad arguments before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from conftest import ROOT
+
+INCLUDE = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def L():
+    __graft_entry__.build()
+    from routed_moe_decode_gb300 import _lib
+    return _lib
+
+
+def _declared_functions():
+    names = set()
+    for h in ("moe.h", "moe_selftest.h"):
+        text = open(os.path.join(INCLUDE, h)).read()
+        names.update(re.findall(r"^MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_every_declared_function_is_exported(L):
+    names = _declared_functions()
+    assert len(names) >= 16
+    lib = ctypes.CDLL(L.LIB_PATH)
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+    # the binding's table covers the public header
+    public = set(re.findall(r"^MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(",
+                            open(os.path.join(INCLUDE, "moe.h")).read(), flags=re.M))
+    assert public <= set(L.SIGNATURES)
+
+
+def test_status_strings(L):
+    for rc in (0, -1, -2, -3, -4, -5):
+        assert L.lib().moe_status_string(rc).decode().startswith("MOE_")
+    assert L.lib().moe_status_string(7).decode() == "unknown moe_status"
+
+
+def test_workspace_size_and_shape_checks(L):
+    b1 = L.shape_of(4, 2048, 512, 512, 10)
+    n = L.workspace_bytes(b1)
+    assert n > 0 and n % 256 == 0
+    # the per-route down outputs dominate and grow with T
+    big = L.workspace_bytes(L.shape_of(8192, 2048, 512, 512, 10))
+    assert big > 8192 * 10 * 2048 * 4
+    assert L.check_shape(L.shape_of(4, 2048, 512, 512, 10)) == 0
+    assert L.check_shape(L.shape_of(4, 2048, 512, 8, 10)) == L.MOE_ERR_INVALID_ARG  # k > E
+    assert L.check_shape(L.shape_of(4, 2000, 512, 512, 10)) == L.MOE_ERR_UNSUPPORTED  # d % 128
+    assert L.check_shape(L.shape_of(4, 2048, 512, 2048, 10)) == L.MOE_ERR_UNSUPPORTED  # E > 1024
+    assert L.check_shape(L.shape_of(4, 2048, 512, 512, 40)) == L.MOE_ERR_UNSUPPORTED  # k > 32
+    assert L.check_shape(L.shape_of(-1, 2048, 512, 512, 10)) == L.MOE_ERR_INVALID_ARG
+    assert L.workspace_bytes(L.shape_of(4, 2000, 512, 512, 10)) == 0
+
+
+def test_bad_arguments_rejected_on_host(L):
+    lib = L.lib()
+    s = L.shape_of(4, 256, 128, 16, 2)
+    sp = ctypes.byref(s)
+    assert lib.moe_route_topk(sp, None, None, None, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_plan(sp, None, None, None, 0, None) == L.MOE_ERR_INVALID_ARG
+    fake = ctypes.c_void_p(0x100000)
+    assert lib.moe_plan(sp, fake, fake, None, 0, None) == L.MOE_ERR_WORKSPACE
+    assert lib.moe_plan(sp, fake, fake, ctypes.c_void_p(0x100010), 1 << 30, None) == L.MOE_ERR_WORKSPACE
+    assert lib.moe_plan(sp, fake, fake, fake, 16, None) == L.MOE_ERR_WORKSPACE
+    # misaligned hidden, unknown algorithm
+    args = [sp, ctypes.c_void_p(0x100002), fake, fake, 1.0, fake, fake, 1.0, None, fake, fake, 1 << 30]
+    assert lib.moe_forward_algo(*args, 0, None) == L.MOE_ERR_INVALID_ARG
+    args[1] = fake
+    assert lib.moe_forward_algo(*args, 9, None) == L.MOE_ERR_INVALID_ARG
+    # T = 0 is an empty, valid call that enqueues nothing
+    z = L.shape_of(0, 256, 128, 16, 2)
+    assert lib.moe_route_topk(ctypes.byref(z), None, None, None, None) == 0

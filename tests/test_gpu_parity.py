@@ -1,0 +1,274 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Routing ids must match bit for bit; routing weights within 2e-6 relative; the layer
+output within max|d| <= 2e-2 * RMS(ref) and sum|d| / sum|ref| <= 5e-3.  Small workloads
+are compared on every output; the full-size workloads on every routing id and on the
+outputs of a sample of tokens the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from gpu_helpers import (WEIGHT_RTOL, assert_parity, bf16_tensor, config_inputs, device_weights, parity_metrics,
+                         run_layer)
+from oracle import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+ALGOS = {"tcgen05": 1, "simt": 2}
+
+# tokens checked against the oracle at full size (all tokens when None)
+SAMPLES = {
+    "tiny": None,
+    "b1": None,
+    "b8": [0, 1, 2, 3, 13, 22, 30, 31],
+    "b64": [0, 1, 37, 100, 128, 200, 254, 255],
+    "b64_literal": [0, 5, 77, 255],
+    "prefill": [0, 1, 2, 1000, 4095, 6000, 8190, 8191],
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _check_layer(cfg, inp, algo, tokens=None, residual=True):
+    ids, wts, out, layer = run_layer(cfg, inp, algo=algo, residual=residual)
+    assert layer.status() == 0
+    ids_ref, w_ref = O.route_topk(inp["logits"], cfg.k)
+    np.testing.assert_array_equal(ids, ids_ref)
+    np.testing.assert_allclose(wts, w_ref, rtol=WEIGHT_RTOL, atol=1e-7)
+    mask = None
+    if tokens is not None:
+        mask = np.zeros(cfg.T, np.uint8)
+        mask[tokens] = 1
+    res = inp["residual"] if residual else None
+    ref = O.moe_experts((cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k), inp["hidden"], ids_ref, w_ref, inp, res, mask)
+    rows = slice(None) if tokens is None else tokens
+    return assert_parity(out[rows], ref[rows], f"{cfg.name} algo {algo}")
+
+
+@pytest.mark.parametrize("name", ["tiny", "b1", "b8", "b64", "b64_literal", "prefill"])
+def test_layer_parity_tcgen05(name):
+    cfg = mi.CONFIGS[name]
+    _check_layer(cfg, config_inputs(name), ALGOS["tcgen05"], SAMPLES[name])
+
+
+@pytest.mark.parametrize("name", ["tiny", "b1", "b8"])
+def test_layer_parity_simt(name):
+    cfg = mi.CONFIGS[name]
+    _check_layer(cfg, config_inputs(name), ALGOS["simt"], SAMPLES[name])
+
+
+def test_last_layer_weight_set_parity():
+    cfg = mi.CONFIGS["b1"]
+    _check_layer(cfg, mi.gen_layer(cfg, seed=0, layer=11), ALGOS["tcgen05"])
+
+
+@pytest.mark.parametrize("T,d,F,E,k", [(1, 256, 128, 16, 1), (5, 256, 128, 16, 2), (33, 512, 256, 64, 8),
+                                       (100, 256, 128, 32, 4), (3, 384, 384, 1000, 7), (7, 128, 128, 40, 32),
+                                       (64, 1024, 256, 16, 16)])
+def test_ragged_and_edge_shapes(T, d, F, E, k):
+    cfg = mi.CONFIGS["tiny"].replace(name=f"edge{T}x{d}x{F}x{E}x{k}", T=T, d=d, ffn=F, E=E, k=k, tag=100 + T)
+    inp = mi.gen_layer(cfg, seed=3)
+    _check_layer(cfg, inp, ALGOS["tcgen05"])
+
+
+def _route_only(logits, k):
+    import routed_moe_decode_gb300 as moe
+    T, E = logits.shape
+    shape = moe.shape_of(T, 128, 128, E, k)
+    dl = torch.from_numpy(np.ascontiguousarray(logits, dtype=np.float32)).cuda()
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    moe.route_topk(shape, dl, ids, w)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy()
+
+
+@pytest.mark.parametrize("E,k", [(512, 10), (64, 8), (16, 2), (1000, 32), (33, 33)])
+def test_route_ties_and_signed_zero(E, k):
+    rng = np.random.default_rng(E + k)
+    T = 300
+    logits = (rng.integers(-3, 4, size=(T, E)) * 0.25).astype(np.float32)  # heavy ties
+    logits[:10] = 0.0
+    logits[5:10, ::3] = -0.0  # -0 and +0 compare equal: lower index wins
+    ids, w = _route_only(logits, k)
+    ids_ref, w_ref = O.route_topk(logits, k)
+    np.testing.assert_array_equal(ids, ids_ref)
+    np.testing.assert_allclose(w, w_ref, rtol=WEIGHT_RTOL, atol=1e-7)
+
+
+@pytest.mark.parametrize("name", ["b1", "b8", "b64", "prefill"])
+def test_route_full_size_bit_exact(name):
+    cfg = mi.CONFIGS[name]
+    for layer in (0, 5):
+        logits = mi.gen_logits(cfg, 0, layer)
+        ids, w = _route_only(logits, cfg.k)
+        ids_ref, w_ref = O.route_topk(logits, cfg.k)
+        np.testing.assert_array_equal(ids, ids_ref)
+        np.testing.assert_allclose(w, w_ref, rtol=WEIGHT_RTOL, atol=1e-7)
+
+
+@pytest.mark.parametrize("name", ["tiny", "b8", "b64", "prefill"])
+def test_plan_matches_oracle_bucketing(name):
+    import routed_moe_decode_gb300 as moe
+    cfg = mi.CONFIGS[name]
+    logits = mi.gen_logits(cfg, 0, 0)
+    layer = moe.MoeLayer(cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k)
+    layer.route(torch.from_numpy(logits).cuda())
+    layer.plan()
+    torch.cuda.synchronize()
+    ids = layer.ids.cpu().numpy()
+    counts, offsets, touched = O.plan(ids, cfg.E)
+    v = {key: t.cpu().numpy() for key, t in moe.plan_views(layer.shape, layer.ws).items()}
+    U, maxrows = moe.plan_summary(layer.shape, layer.ws)
+    np.testing.assert_array_equal(v["counts"], counts)
+    np.testing.assert_array_equal(v["offsets"], offsets)
+    assert U == len(touched) and maxrows == counts.max()
+    np.testing.assert_array_equal(v["touched"][:U], touched)
+    # route positions: a bijection onto [0, T*k) that keeps each route inside its expert's segment
+    pos = v["route_pos"]
+    assert sorted(pos.tolist()) == list(range(cfg.T * cfg.k))
+    e_of_route = ids.ravel()
+    assert np.all(pos >= offsets[e_of_route]) and np.all(pos < offsets[e_of_route + 1])
+    np.testing.assert_array_equal(v["pos_token"][pos], np.arange(cfg.T * cfg.k) // cfg.k)
+    assert layer.status() == 0
+
+
+def test_bad_expert_id_sets_status():
+    import routed_moe_decode_gb300 as moe
+    shape = moe.shape_of(4, 256, 128, 16, 2)
+    ws = moe.Workspace(shape)
+    ids = torch.tensor([[0, 1], [2, 16], [3, 4], [5, -1]], dtype=torch.int32, device="cuda")
+    w = torch.full((4, 2), 0.5, device="cuda")
+    moe.plan(shape, ids, w, ws)
+    torch.cuda.synchronize()
+    assert moe.read_status(ws) & moe.MOE_DEV_BAD_EXPERT_ID
+    assert moe.read_status(ws) == 0  # cleared by the first read
+
+
+def test_zero_hidden_gives_residual_exactly():
+    cfg = mi.CONFIGS["b1"]
+    inp = dict(config_inputs("b1"))
+    inp["hidden"] = np.zeros_like(inp["hidden"])
+    _, _, out, _ = run_layer(cfg, inp, algo=1)
+    res = (inp["residual"].astype(np.uint32) << 16).view(np.float32)
+    np.testing.assert_array_equal(out, res)
+
+
+def test_no_residual_and_out_aliasing_residual():
+    cfg = mi.CONFIGS["b8"]
+    inp = config_inputs("b8")
+    _check_layer(cfg, inp, 1, SAMPLES["b8"], residual=False)
+    import routed_moe_decode_gb300 as moe
+    w = device_weights(inp, "cuda")
+    layer = moe.MoeLayer(cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k)
+    hidden = bf16_tensor(inp["hidden"], "cuda")
+    buf = bf16_tensor(inp["residual"], "cuda").clone()
+    ref_out = layer(torch.from_numpy(inp["logits"]).cuda(), hidden, w, buf.clone())
+    out = layer(torch.from_numpy(inp["logits"]).cuda(), hidden, w, buf, out=buf)  # in place
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out)
+
+
+def _shared_or_disjoint_logits(T, E, k, shared):
+    logits = np.random.default_rng(9).standard_normal((T, E)).astype(np.float32)
+    if shared:  # every token on the same k experts
+        logits[:, 7:7 + k] += 50.0
+    else:  # no two tokens share an expert
+        for t in range(T):
+            logits[t, t * k:(t + 1) * k] += 50.0
+    return logits
+
+
+@pytest.mark.parametrize("shared,T", [(True, 4), (True, 64), (True, 100), (False, 32)])
+def test_all_equal_and_all_disjoint_routing(shared, T):
+    cfg = mi.CONFIGS["b1"].replace(name=f"route_shared{shared}{T}", T=T, tag=50 + T)
+    inp = dict(config_inputs("b1"))  # b1's weights; this workload's own activations
+    inp.update(mi.gen_layer(cfg, seed=1, weights=False))
+    inp["logits"] = _shared_or_disjoint_logits(T, cfg.E, cfg.k, shared)
+    tokens = None if T <= 32 else [0, 1, T // 2, T - 1]
+    _check_layer(cfg, inp, 1, tokens)
+
+
+def test_all_experts_identical_output_independent_of_routing():
+    cfg = mi.CONFIGS["tiny"].replace(name="same_experts", T=16, tag=77)
+    inp = dict(mi.gen_layer(cfg, seed=2))
+    for key in ("w13_codes", "w13_scales", "w2_codes", "w2_scales"):
+        inp[key] = np.ascontiguousarray(np.broadcast_to(inp[key][:1], inp[key].shape))
+    _, _, a, _ = run_layer(cfg, inp, algo=1)
+    inp2 = dict(inp, logits=np.ascontiguousarray(inp["logits"][:, ::-1]))
+    _, _, b, _ = run_layer(cfg, inp2, algo=1)
+    mx, mean_rel = parity_metrics(a, b)
+    assert mx < 2e-2 and mean_rel < 2e-3
+    _check_layer(cfg, inp, 1)
+
+
+def test_repeat_is_bitwise_deterministic_and_forward_reuses_plan():
+    import routed_moe_decode_gb300 as moe
+    cfg = mi.CONFIGS["b8"]
+    inp = config_inputs("b8")
+    w = device_weights(inp, "cuda")
+    layer = moe.MoeLayer(cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k)
+    logits = torch.from_numpy(inp["logits"]).cuda()
+    hidden = bf16_tensor(inp["hidden"], "cuda")
+    res = bf16_tensor(inp["residual"], "cuda")
+    first = layer(logits, hidden, w, res)
+    outs = [layer.experts(hidden, w, res) for _ in range(3)]  # forward again on the same plan
+    outs.append(layer(logits, hidden, w, res))
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o, first)
+    assert layer.status() == 0
+
+
+def test_cuda_graph_replays_with_changed_inputs():
+    import routed_moe_decode_gb300 as moe
+    cfg = mi.CONFIGS["b8"]
+    a = config_inputs("b8", 0, 0)
+    b = mi.gen_layer(cfg, seed=0, layer=1, weights=False)
+    w = device_weights(a, "cuda")
+    layer = moe.MoeLayer(cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k)
+    logits = torch.from_numpy(a["logits"]).cuda()
+    hidden = bf16_tensor(a["hidden"], "cuda")
+    res = bf16_tensor(a["residual"], "cuda")
+    out = torch.empty_like(res)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer(logits, hidden, w, res, out=out)  # warm-up (and per-device setup) outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer(logits, hidden, w, res, out=out)
+    for src in (b, a, b):
+        logits.copy_(torch.from_numpy(src["logits"]))
+        hidden.copy_(bf16_tensor(src["hidden"], "cuda"))
+        res.copy_(bf16_tensor(src["residual"], "cuda"))
+        g.replay()
+        torch.cuda.synchronize()
+        ids_ref, w_ref = O.route_topk(src["logits"], cfg.k)
+        np.testing.assert_array_equal(layer.ids.cpu().numpy(), ids_ref)
+        toks = SAMPLES["b8"][:4]
+        mask = np.zeros(cfg.T, np.uint8)
+        mask[toks] = 1
+        ref = O.moe_experts((cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k), src["hidden"], ids_ref, w_ref, a,
+                            src["residual"], mask)
+        assert_parity(out.float().cpu().numpy()[toks], ref[toks], "graph replay")
+    assert layer.status() == 0
+
+
+def test_hidden_out_of_fp16_range_sets_status():
+    cfg = mi.CONFIGS["tiny"]
+    inp = dict(config_inputs("tiny"))
+    hid = inp["hidden"].copy()
+    hid[1, 3] = 0x4780  # bf16 65536.0, above the FP16 maximum
+    inp["hidden"] = hid
+    _, _, _, layer = run_layer(cfg, inp, algo=1)
+    import routed_moe_decode_gb300 as moe
+    assert layer.status() & moe.MOE_DEV_HIDDEN_RANGE
