@@ -14,7 +14,7 @@ from ._lib import (ALGO_AUTO, ALGO_SIMT, ALGO_TCGEN05, MOE_DEV_BAD_EXPERT_ID, MO
                    forward_experts, forward_prepare,
                    layer, lib, plan, plan_summary, plan_views, read_status, route_topk, shape_of,
                    workspace_bytes)
-from .layer import MoeLayer
+from ._layer import MoeLayer
 
 __all__ = ["ALGO_AUTO", "ALGO_SIMT", "ALGO_TCGEN05", "MOE_DEV_BAD_EXPERT_ID", "MOE_DEV_H_SATURATED",
            "MOE_DEV_HIDDEN_RANGE", "MOE_DEV_TIMEOUT", "MoeError", "MoeLayer", "Shape", "Workspace",

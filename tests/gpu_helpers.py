@@ -2,6 +2,8 @@
 from __future__ import annotations
 
 import functools
+import json
+import os
 
 import numpy as np
 import torch
@@ -55,6 +57,11 @@ def parity_metrics(got: np.ndarray, ref: np.ndarray):
 def assert_parity(got: np.ndarray, ref: np.ndarray, what=""):
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     mx, mean_rel = parity_metrics(got, ref)
+    log = os.environ.get("MOE_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"case": what, "rows": int(got.shape[0]), "max_abs_over_rms": mx,
+                                "mean_rel": mean_rel}) + "\n")
     assert mx <= MAX_ABS_OVER_RMS and mean_rel <= MEAN_REL, \
         f"{what}: max|d|/rms {mx:.3e} (<= {MAX_ABS_OVER_RMS}), mean rel {mean_rel:.3e} (<= {MEAN_REL})"
     return mx, mean_rel
