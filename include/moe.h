@@ -177,6 +177,35 @@ MOE_API int moe_layer(const moe_shape* shape, const float* logits, const void* h
               const void* residual, void* out, int32_t* ids, float* weights, void* workspace,
               size_t workspace_bytes, moe_stream_t stream);
 
+/* The whole layer (moe_layer) with its scratch in a fixed device array of the library
+ * instead of a caller-provided workspace.  The pages have no counterpart for this entry
+ * point.  It is for callers that cannot allocate device memory: code running while a
+ * CUDA graph is being captured (cudaMalloc is not capturable), plug-ins whose host
+ * framework owns all device memory through its own allocator, and latency-critical
+ * loops where cudaMalloc's implicit device synchronisation is not acceptable.  Such
+ * callers still pass every input and output (logits, hidden, weights, residual, out,
+ * ids, weights) exactly as for moe_layer; this call allocates nothing (no cudaMalloc,
+ * no cudaFree, no allocating library routine).
+ *   - Scratch: a file-scope 16 MiB (16777216-byte) device array in the library, present
+ *     on every GPU that loads the library until the process exits.  Shapes with
+ *     moe_workspace_bytes(shape) larger than that return MOE_ERR_WORKSPACE (with a
+ *     message in moe_last_cuda_error); this covers the decode-verify shapes (e.g.
+ *     T = 4 or 32 with d = 2048, ffn = 512, E = 512, k = 10), not large prefill chunks.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before any
+ *     stream capture.
+ *   - Sharing: every call uses the same array and leaves its contents behind; the call
+ *     clears what must start at zero (status word, counters) itself.  Calls whose work
+ *     overlaps on the GPU (different streams, or several host threads) race on the
+ *     array: serialise them.  Device-side status bits are not reported by this call.
+ * Returns as moe_layer. */
+MOE_API int moe_layer_static_workspace(const moe_shape* shape, const float* logits,
+                                       const void* hidden, const uint8_t* w13_codes,
+                                       const uint8_t* w13_scales, float w13_scale,
+                                       const uint8_t* w2_codes, const uint8_t* w2_scales,
+                                       float w2_scale, const void* residual, void* out,
+                                       int32_t* ids, float* weights, moe_stream_t stream);
+
 /* Copy the device status word to *status_bits (blocking copy on `stream`; call after the
  * work of interest has been enqueued) and clear it when `clear` is non-zero.  Returns
  * MOE_OK if no bit is set, MOE_ERR_DEVICE if any is. */

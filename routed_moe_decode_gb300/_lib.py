@@ -56,6 +56,7 @@ SIGNATURES = {
     "moe_forward_prepare": (_I, [_SP, _P, _P, ctypes.c_size_t, _P]),
     "moe_forward_experts": (_I, [_SP, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _I, _P]),
     "moe_layer": (_I, [_SP, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_layer_static_workspace": (_I, [_SP, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P]),
     "moe_read_device_status": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint32), _P]),
     "moe_plan_summary": (_I, [_SP, _P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), _P]),
     "moe_plan_views": (_I, [_SP, _P] + [ctypes.POINTER(ctypes.c_void_p)] * 5),
@@ -69,7 +70,8 @@ class MoeError(RuntimeError):
     def __init__(self, fn, rc):
         msg = lib().moe_status_string(rc).decode()
         extra = lib().moe_last_cuda_error().decode()
-        super().__init__(f"{fn} -> {rc} ({msg}){': ' + extra if extra and rc == MOE_ERR_CUDA else ''}")
+        show = extra and rc in (MOE_ERR_CUDA, MOE_ERR_WORKSPACE)
+        super().__init__(f"{fn} -> {rc} ({msg}){': ' + extra if show else ''}")
         self.rc = rc
 
 

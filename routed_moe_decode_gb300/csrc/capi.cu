@@ -85,6 +85,8 @@ int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint
   return MOE_OK;
 }
 
+void set_last_error_message(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
 }  // namespace moe
 
 namespace {

@@ -71,5 +71,7 @@ cudaError_t launch_expert_tc(const ExpertArgs& a, const CUtensorMap& tm_w13, con
 cudaError_t launch_expert_simt(const ExpertArgs& a, cudaStream_t stream);
 size_t expert_tc_smem_bytes();
 int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows);
+// Record a message for moe_last_cuda_error on the calling host thread.
+void set_last_error_message(const char* msg);
 
 }  // namespace moe
