@@ -49,7 +49,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=None)
     p.add_argument("--config", default="b1", choices=sorted(mi.CONFIGS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--algo", default="tcgen05", choices=["tcgen05", "simt"])
+    p.add_argument("--algo", default="auto", choices=["auto", "mma", "tcgen05", "simt"])
     p.add_argument("--layers", type=int, default=None, help="weight sets cycled (default 12)")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -160,11 +160,11 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def profiled_traffic(config: str):
+def profiled_traffic(config: str, kernel: str):
     """DRAM bytes per expert-kernel launch from the committed ncu summary of this workload,
     or None if there is none or the kernel source changed since it was captured."""
-    path = os.path.join(ROOT, "profiles", f"expert_tc_{config}_dram.txt")
-    src = os.path.join(ROOT, "routed_moe_decode_gb300", "csrc", "expert_tc.cu")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{config}_dram.txt")
+    src = os.path.join(ROOT, "routed_moe_decode_gb300", "csrc", f"{kernel}.cu")
     if not os.path.exists(path):
         return None
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
@@ -173,7 +173,7 @@ def profiled_traffic(config: str):
         if ":" in line:
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
-    if vals.get("expert_tc.cu sha256[:16]") != digest:
+    if vals.get(f"{kernel}.cu sha256[:16]") != digest:
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -241,7 +241,7 @@ def our_arm(args, cfg, dist, torch):
     import routed_moe_decode_gb300 as moe
     dev = torch.device(f"cuda:{dist.local}")
     torch.cuda.set_device(dev)
-    algo = moe.ALGO_TCGEN05 if args.algo == "tcgen05" else moe.ALGO_SIMT
+    algo = {"auto": moe.ALGO_AUTO, "mma": moe.ALGO_MMA, "tcgen05": moe.ALGO_TCGEN05, "simt": moe.ALGO_SIMT}[args.algo]
     L = args.layers if args.layers is not None else min(12, max(1, cfg.layers))
     K = args.steps if args.steps is not None else DEFAULT_STEPS[cfg.name]
     W = args.warmup if args.warmup is not None else max(3, 2 * L)
@@ -277,7 +277,7 @@ def our_arm(args, cfg, dist, torch):
         moe.forward_prepare(shape, hidden[l], ws)
         moe.forward_experts(shape, Wd[l], resid[l], out, ws, algo)
 
-    kernels_per_step = 4 if algo == moe.ALGO_TCGEN05 else 6
+    kernels_per_step = 6 if algo == moe.ALGO_SIMT else 5  # route, plan, prep, expert(s), un-route
 
     # ---- unique experts per layer (outside any timed region) ----
     U = []
@@ -367,7 +367,8 @@ def our_arm(args, cfg, dist, torch):
     k_avg_ms = sum(kdur_ms) / Kk
     achieved = kbytes / Kk / (k_avg_ms * 1e-3) / 1e9
     peak, peak_kind = load_peaks()
-    traffic = profiled_traffic(cfg.name) if algo == moe.ALGO_TCGEN05 else None
+    kname = {moe.ALGO_AUTO: "expert_mma", moe.ALGO_MMA: "expert_mma", moe.ALGO_TCGEN05: "expert_tc"}.get(algo)
+    traffic = profiled_traffic(cfg.name, kname) if kname else None
 
     # ---- end to end through the public C-ABI call with host buffers ----
     e2e = None
@@ -439,7 +440,7 @@ def our_arm(args, cfg, dist, torch):
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "expert_tc_kernel" if algo == moe.ALGO_TCGEN05 else "simt kernels",
+                     "kernel": f"{kname}_kernel" if kname else "simt kernels",
                      "kernel_us": 1e3 * k_avg_ms, "peak_kind": f"{peak_kind} copy bandwidth",
                      "algorithmic_bytes": "unique experts x 1769472 B + BF16 hidden/residual/out"},
         "clocks": clocks,

@@ -89,11 +89,18 @@ typedef struct moe_shape {
 
 /* Expert-kernel selection for moe_forward_algo. */
 typedef enum moe_algo {
-  MOE_ALGO_AUTO = 0,     /* the tensor-core persistent kernel */
+  MOE_ALGO_AUTO = 0,     /* MOE_ALGO_MMA where it applies (d and ffn multiples of 256, at most
+                            2048), MOE_ALGO_TCGEN05 otherwise */
   MOE_ALGO_TCGEN05 = 1,  /* persistent stripe kernel: TMA weight stream, in-register NVFP4
                             dequantisation into tensor memory, tcgen05 MMA (FP32 accumulate),
-                            readiness counters between gate/up and down, fused un-route */
-  MOE_ALGO_SIMT = 2      /* CUDA-core kernels, one launch per stage (ablation baseline) */
+                            16-row column groups, readiness counters between gate/up and down */
+  MOE_ALGO_SIMT = 2,     /* CUDA-core kernels, one launch per stage (ablation baseline) */
+  MOE_ALGO_MMA = 3       /* persistent stripe kernel: TMA weight stream, in-register NVFP4
+                            dequantisation into the A fragments of warp-level m16n8k16 tensor-core
+                            MMAs (weights stationary, routed rows as the 8-wide operand, FP32
+                            accumulate), gate and up of one F index in one warp, readiness
+                            counters between gate/up and down; needs d and ffn multiples of 256
+                            and at most 2048 (MOE_ERR_UNSUPPORTED otherwise) */
 } moe_algo;
 
 /* Human-readable name of a status code (static string, never NULL). */

@@ -18,12 +18,14 @@ extern "C" {
 #endif
 
 /* NVFP4 decode as used by the dequantisation warps.
- *   words  [n] uint32: eight E2M1 codes each (element 2i in the low nibble of byte i)
- *   out    [4n] uint32: f16x2 values, out[4w + b] = (element 2b, element 2b+1) of word w
- *   pairs  [m] uint32: two E4M3 bytes in the low 16 bits (low byte -> low half)
- *   sout   [m] uint32: f16x2 of the two scale values */
-MOE_API int moe_selftest_decode(const uint32_t* words, int n, uint32_t* out, const uint32_t* pairs, int m,
-                                uint32_t* sout, moe_stream_t stream);
+ *   words     [n] uint32: eight E2M1 codes each (element 2i in the low nibble of byte i)
+ *   out       [4n] uint32: hardware conversion, f16x2 out[4w + b] = (element 2b, element 2b+1)
+ *   out_shift [4n] uint32: integer construction, f16x2 out_shift[4w + j] = (element j,
+ *             element j+4) of word w, each half the FP16 pattern of value * 2^-14
+ *   pairs     [m] uint32: two E4M3 bytes in the low 16 bits (low byte -> low half)
+ *   sout      [m] uint32: f16x2 of the two scale values */
+MOE_API int moe_selftest_decode(const uint32_t* words, int n, uint32_t* out, uint32_t* out_shift,
+                                const uint32_t* pairs, int m, uint32_t* sout, moe_stream_t stream);
 
 /* One TMA load of a 64-byte x 64-row box of a [rows, row_bytes] uint8 matrix at byte
  * column x (a multiple of 16) and row y, with the 64-byte swizzle the expert kernel
@@ -36,6 +38,21 @@ MOE_API int moe_selftest_tma(const uint8_t* src, int rows, int row_bytes, int x,
  * FP16 (row-major) stored in shared memory in 128-byte swizzled K-major atoms, eight
  * kind::f16 MMAs with FP32 accumulation, result D [128, 16] FP32 (row-major) = A B^T. */
 MOE_API int moe_selftest_mma(const void* A, const void* B, float* D, moe_stream_t stream);
+
+/* The tensor-core expert kernel and the un-route kernel exactly as moe_forward_experts
+ * runs them (after moe_plan and moe_forward_prepare), with a timeline recorded into
+ * `trace`: per CTA 8 roles x 128 uint64 events (event code << 56 | index << 40 | low 40
+ * bits of %globaltimer in ns); zero-initialise the buffer (multiProcessorCount x 8192 bytes).
+ * Roles: 0 weight producer (1 task published, 2 chunk issued), 1 activation producer
+ * (3 readiness met, 4 chunk issued), 2 first dequantisation warp (5 chunk landed, 6 chunk in
+ * tensor memory), 3 MMA (7 chunk issued), 4 epilogue (8 accumulator ready, 9 task done),
+ * 5 CTA (10 start, 11 end). */
+MOE_API int moe_selftest_expert_trace(const moe_shape* shape, const uint8_t* w13_codes,
+                                      const uint8_t* w13_scales, float w13_scale,
+                                      const uint8_t* w2_codes, const uint8_t* w2_scales,
+                                      float w2_scale, const void* residual, void* out,
+                                      void* workspace, size_t workspace_bytes,
+                                      unsigned long long* trace, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

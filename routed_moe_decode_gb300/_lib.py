@@ -30,6 +30,7 @@ MOE_DEV_H_SATURATED = 0x8
 ALGO_AUTO = 0
 ALGO_TCGEN05 = 1
 ALGO_SIMT = 2
+ALGO_MMA = 3
 
 # Every function declared in include/moe.h, with (restype, argtypes).
 _P = ctypes.c_void_p

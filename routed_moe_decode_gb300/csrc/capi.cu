@@ -5,6 +5,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "../../include/moe_selftest.h"
 #include "moe_kernels.cuh"
 
 namespace {
@@ -66,18 +67,21 @@ int get_encoder(EncodeTiledFn* fn) {
 
 namespace moe {
 
-// 2-D uint8 tensor map over a [rows, row_bytes] code matrix: 64-byte x 64-row boxes,
-// 64-byte swizzle (conflict-free row-per-thread reads of 16-byte chunks).
-int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows) {
+// 2-D uint8 tensor map over a [rows, row_bytes] code matrix: box_bytes x 64-row boxes
+// with the swizzle of the same width (64 or 128 bytes), so that threads reading 16-byte
+// chunks of consecutive rows hit distinct banks.
+int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes) {
   EncodeTiledFn enc = nullptr;
   if (get_encoder(&enc) != MOE_OK) { snprintf(g_last_error, sizeof g_last_error, "no cuTensorMapEncodeTiled"); return MOE_ERR_CUDA; }
   cuuint64_t dims[2] = {row_bytes, rows};
   cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {64, 64};
+  if (box_bytes != 64 && box_bytes != 128) return MOE_ERR_INVALID_ARG;
+  cuuint32_t box[2] = {box_bytes, 64};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
     return MOE_ERR_CUDA;
@@ -121,8 +125,8 @@ moe::ExpertArgs expert_args(const moe_shape* s, const WsLayout& L, void* ws, con
                             const void* residual, void* out) {
   moe::ExpertArgs a{};
   a.T = s->T; a.d = s->d; a.F = s->ffn; a.E = s->E; a.k = s->k; a.R = L.R;
-  a.KS = L.KS; a.S_gu = L.S_gu; a.S_dn = L.S_dn;
-  a.nck_gu = s->d / L.KS / moe::kChunkK;
+  a.S_gu = L.S_gu; a.S_dn = L.S_dn;
+  a.nck_gu = s->d / moe::kChunkK;
   a.nck_dn = s->ffn / moe::kChunkK;
   a.w13_ts = w13_ts; a.w2_ts = w2_ts;
   a.w13_codes = w13c; a.w13_scales = w13s; a.w2_codes = w2c; a.w2_scales = w2s;
@@ -130,18 +134,15 @@ moe::ExpertArgs expert_args(const moe_shape* s, const WsLayout& L, void* ws, con
   a.counts = at<int>(ws, L.counts);
   a.offsets = at<int>(ws, L.offsets);
   a.touched = at<int>(ws, L.touched);
-  a.gu_start = at<int>(ws, L.gu_start);
-  a.dn_start = at<int>(ws, L.dn_start);
   a.pos_tok = at<int>(ws, L.pos_tok);
   a.route_pos = at<int>(ws, L.route_pos);
   a.route_w = at<float>(ws, L.route_w);
+  a.tasks = at<moe::TaskEntry>(ws, L.tasks);
   a.x16 = at<__half>(ws, L.x16);
   a.hs16 = at<__half>(ws, L.hs16);
-  a.gu_part = at<float>(ws, L.gu_part);
   a.y = at<float>(ws, L.y);
   a.ready = at<uint32_t>(ws, L.ready);
-  a.cnt_gu = at<uint32_t>(ws, L.cnt_gu);
-  a.comb_cnt = at<uint32_t>(ws, L.comb_cnt);
+  a.ticket = at<uint32_t>(ws, L.ticket);
   a.status = at<int>(ws, L.status);
   a.residual = static_cast<const __nv_bfloat16*>(residual);
   a.out = static_cast<__nv_bfloat16*>(out);
@@ -202,7 +203,7 @@ int moe_plan(const moe_shape* shape, const int32_t* ids, const float* weights, v
   if (rc != MOE_OK) return rc;
   const WsLayout L = moe::ws_layout(*shape);
   moe::PlanArgs a{};
-  a.T = shape->T; a.E = shape->E; a.k = shape->k; a.KS = L.KS; a.S_gu = L.S_gu; a.S_dn = L.S_dn;
+  a.T = shape->T; a.E = shape->E; a.k = shape->k; a.S_gu = L.S_gu; a.S_dn = L.S_dn;
   a.ids = ids; a.weights = weights;
   a.status = at<int>(workspace, L.status);
   a.meta = at<int>(workspace, L.meta);
@@ -214,6 +215,7 @@ int moe_plan(const moe_shape* shape, const int32_t* ids, const float* weights, v
   a.route_pos = at<int>(workspace, L.route_pos);
   a.pos_tok = at<int>(workspace, L.pos_tok);
   a.route_w = at<float>(workspace, L.route_w);
+  a.tasks = at<moe::TaskEntry>(workspace, L.tasks);
   cudaError_t e = moe::launch_plan(a, stream);
   if (e != cudaSuccess) { set_error("plan launch", e); return MOE_ERR_CUDA; }
   return MOE_OK;
@@ -229,22 +231,21 @@ int moe_forward_prepare(const moe_shape* shape, const void* hidden, void* worksp
   if (rc != MOE_OK) return rc;
   const WsLayout L = moe::ws_layout(*shape);
   moe::PrepArgs p{};
-  p.T = shape->T; p.d = shape->d; p.E = shape->E; p.S_dn = L.S_dn; p.max_units = L.max_units;
+  p.T = shape->T; p.d = shape->d; p.E = shape->E;
   p.hidden = static_cast<const __nv_bfloat16*>(hidden);
   p.x16 = at<__half>(workspace, L.x16);
   p.ready = at<uint32_t>(workspace, L.ready);
-  p.cnt_gu = at<uint32_t>(workspace, L.cnt_gu);
-  p.comb_cnt = at<uint32_t>(workspace, L.comb_cnt);
+  p.ticket = at<uint32_t>(workspace, L.ticket);
   p.status = at<int>(workspace, L.status);
   cudaError_t e = moe::launch_prep(p, stream);
   if (e != cudaSuccess) { set_error("prep launch", e); return MOE_ERR_CUDA; }
   return MOE_OK;
 }
 
-int moe_forward_experts(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
-                        float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
-                        const void* residual, void* out, void* workspace, size_t workspace_bytes, int algo,
-                        moe_stream_t stream) {
+static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
+                                float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+                                const void* residual, void* out, void* workspace, size_t workspace_bytes, int algo,
+                                unsigned long long* trace, moe_stream_t stream) {
   int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   if (shape->T == 0) return MOE_OK;
@@ -252,12 +253,13 @@ int moe_forward_experts(const moe_shape* shape, const uint8_t* w13_codes, const 
   if (!aligned(w13_codes, 16) || !aligned(w13_scales, 16) || !aligned(w2_codes, 16) || !aligned(w2_scales, 16) ||
       !aligned(out, 16) || (residual && !aligned(residual, 16)))
     return MOE_ERR_INVALID_ARG;
-  if (algo != MOE_ALGO_AUTO && algo != MOE_ALGO_TCGEN05 && algo != MOE_ALGO_SIMT) return MOE_ERR_INVALID_ARG;
+  if (algo < MOE_ALGO_AUTO || algo > MOE_ALGO_MMA) return MOE_ERR_INVALID_ARG;
   rc = check_ws(shape, workspace, workspace_bytes);
   if (rc != MOE_OK) return rc;
   const WsLayout L = moe::ws_layout(*shape);
-  const moe::ExpertArgs a = expert_args(shape, L, workspace, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales,
-                                        w2_scale, residual, out);
+  moe::ExpertArgs a = expert_args(shape, L, workspace, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales,
+                                  w2_scale, residual, out);
+  a.trace = trace;
   cudaError_t e;
   if (algo == MOE_ALGO_SIMT) {
     e = moe::launch_expert_simt(a, stream);
@@ -267,16 +269,44 @@ int moe_forward_experts(const moe_shape* shape, const uint8_t* w13_codes, const 
   DeviceInfo di;
   rc = device_info(&di);
   if (rc != MOE_OK) return rc;
+  const bool mma_ok = moe::expert_mma_supports(shape->d, shape->ffn);
+  if (algo == MOE_ALGO_MMA && !mma_ok) return MOE_ERR_UNSUPPORTED;
+  const bool use_mma = algo == MOE_ALGO_MMA || (algo == MOE_ALGO_AUTO && mma_ok);
+  const uint32_t box = use_mma ? 128u : 64u;
   CUtensorMap tm13, tm2;
   rc = encode_codes_map(&tm13, w13_codes, static_cast<uint64_t>(shape->d) / 2,
-                        static_cast<uint64_t>(shape->E) * 2 * shape->ffn);
+                        static_cast<uint64_t>(shape->E) * 2 * shape->ffn, box);
   if (rc != MOE_OK) return rc;
   rc = encode_codes_map(&tm2, w2_codes, static_cast<uint64_t>(shape->ffn) / 2,
-                        static_cast<uint64_t>(shape->E) * shape->d);
+                        static_cast<uint64_t>(shape->E) * shape->d, box);
   if (rc != MOE_OK) return rc;
-  e = moe::launch_expert_tc(a, tm13, tm2, di.num_sms, stream);
-  if (e != cudaSuccess) { set_error("expert_tc launch", e); return MOE_ERR_CUDA; }
+  if (use_mma) {
+    e = moe::launch_expert_mma(a, tm13, tm2, di.num_sms, stream);
+    if (e != cudaSuccess) { set_error("expert_mma launch", e); return MOE_ERR_CUDA; }
+  } else {
+    e = moe::launch_expert_tc(a, tm13, tm2, di.num_sms, stream);
+    if (e != cudaSuccess) { set_error("expert_tc launch", e); return MOE_ERR_CUDA; }
+  }
+  e = moe::launch_combine(a, stream);
+  if (e != cudaSuccess) { set_error("combine launch", e); return MOE_ERR_CUDA; }
   return MOE_OK;
+}
+
+int moe_forward_experts(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
+                        float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+                        const void* residual, void* out, void* workspace, size_t workspace_bytes, int algo,
+                        moe_stream_t stream) {
+  return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
+                              workspace, workspace_bytes, algo, nullptr, stream);
+}
+
+int moe_selftest_expert_trace(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
+                              float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+                              const void* residual, void* out, void* workspace, size_t workspace_bytes,
+                              unsigned long long* trace, moe_stream_t stream) {
+  if (!trace) return MOE_ERR_INVALID_ARG;
+  return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
+                              workspace, workspace_bytes, MOE_ALGO_AUTO, trace, stream);
 }
 
 int moe_forward_algo(const moe_shape* shape, const void* hidden, const uint8_t* w13_codes,
@@ -288,7 +318,7 @@ int moe_forward_algo(const moe_shape* shape, const void* hidden, const uint8_t* 
   if (shape->T == 0) return MOE_OK;
   if (!hidden || !w13_codes || !w13_scales || !w2_codes || !w2_scales || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned(hidden, 16)) return MOE_ERR_INVALID_ARG;
-  if (algo != MOE_ALGO_AUTO && algo != MOE_ALGO_TCGEN05 && algo != MOE_ALGO_SIMT) return MOE_ERR_INVALID_ARG;
+  if (algo < MOE_ALGO_AUTO || algo > MOE_ALGO_MMA) return MOE_ERR_INVALID_ARG;
   rc = check_ws(shape, workspace, workspace_bytes);
   if (rc != MOE_OK) return rc;
   rc = moe_forward_prepare(shape, hidden, workspace, workspace_bytes, stream);

@@ -1,0 +1,567 @@
+// Decode-shaped expert kernel: weight-stationary GEMV on the warp-level tensor-core MMA.
+//
+// For the few routed rows of a verify step (1-64 per expert) a tcgen05 MMA is bound by
+// its fixed per-instruction time (~94 ns whatever N <= 128, measured on GB300), so a
+// 128x16 FP16 A tile per instruction cannot keep up with the weight stream.  Here the
+// dequantised weights stay in registers as the 16-row A fragment of mma.sync m16n8k16 and
+// the routed rows are its 8-column B operand: one weight fragment serves every row, and
+// the warp MMA sustains several times the per-SM HBM share of weights (the multi-row
+// weight-stationary GEMV described in the b12x tensor-core GEMV notes of the pages).
+//
+// Structure (one resident CTA per SM, tasks from the plan's task table via tickets):
+//   warp 0      task fetcher + weight producer: per task one bulk copy of the task's block
+//               scales (its rows are contiguous), then per 256-K chunk two TMA tiles of E2M1
+//               codes (64 rows x 128 B each, 128-byte swizzle) into a ring;
+//   warp 1      activation producer: per chunk and 8-row tile, one bulk copy per routed row
+//               (512 B of FP16 hidden for gate/up, of h for down) into a padded tile;
+//   warps 2-9   compute: each owns 16 weight rows of the 128-row tile.  Gate/up tasks give
+//               warp w gate rows 8w..8w+7 as fragment rows 0-7 and the up rows of the same
+//               F indices as fragment rows 8-15, so h = silu(g) * u is formed in registers.
+// Each thread dequantises 2 rows x 64 elements per chunk (exact FP16: E2M1 x E4M3 has at
+// most 6 significant bits), feeds 16 MMAs per 8-row tile with FP32 accumulation, and
+// writes h (FP16) or per-route down outputs (FP32) at the end of the task.  Gate/up warps
+// publish readiness per expert; down tasks' activation loads wait for it.  Only the bulk
+// copy engine writes shared memory, so the consumers need no proxy fences.
+#include "moe_kernels.cuh"
+
+namespace moe {
+
+namespace mk {
+
+constexpr int kChunk = 256;                     // K elements per chunk (128 B of codes per row)
+constexpr int kStagesA = 8;
+constexpr int kStageA = 16384;                  // 2 halves x 64 rows x 128 B (SWIZZLE_128B)
+constexpr int kScaleSlot = 16384;               // 128 rows x up to 128 scale bytes
+constexpr int kStagesB = 12;
+constexpr int kTileRows = 8;
+constexpr int kRowPitchB = 2 * kChunk + 16;     // padded FP16 row of one chunk (528 B)
+constexpr int kStageB = kTileRows * kRowPitchB;  // 4224
+constexpr int kMaxTiles = kRowsPerPass / kTileRows;  // 8
+constexpr int kComputeWarps = 8;
+constexpr int kThreads = 32 * (2 + kComputeWarps);
+constexpr int kTaskSlots = 8;
+constexpr int kTaskConsumers = 1 + kComputeWarps;
+constexpr long long kTimeoutCycles = 1ll << 33;
+
+struct Smem {
+  uint8_t ring_a[kStagesA][kStageA];
+  uint8_t scales[2][kScaleSlot];
+  uint8_t ring_b[kStagesB][kStageB];
+  TaskEntry task[kTaskSlots];
+  uint64_t full_a[kStagesA];
+  uint64_t empty_a[kStagesA];
+  uint64_t full_b[kStagesB];
+  uint64_t empty_b[kStagesB];
+  uint64_t sc_full[2];
+  uint64_t sc_empty[2];
+  uint64_t task_full[kTaskSlots];
+  uint64_t task_empty[kTaskSlots];
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) return false;
+    if (clock64() - t0 > kTimeoutCycles) {
+      *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
+      atomicOr(status, static_cast<int>(MOE_DEV_TIMEOUT));
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status) {
+  const bool ok = bounded_wait(bar, parity, sm, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* status) {
+  const int q = n % kTaskSlots;
+  const uint32_t ph = static_cast<uint32_t>((n / kTaskSlots) & 1);
+  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, sm, status)) return false;
+  out = sm.task[q];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&sm.task_empty[q]));
+  return true;
+}
+
+// D += A * B for one m16n8k16 step (FP16 inputs, FP32 accumulators).
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Dequantise 32 elements (16 bytes of codes, two 16-element scale blocks) of one row into
+// 16 FP16x2 registers in fragment order: register 4j + i belongs to word j; see kCvtWords
+// for the pairing of each word kind.
+__device__ __forceinline__ void dequant32(const uint4 codes, uint32_t scale_pair_bytes, uint32_t (&o)[16]) {
+  const uint32_t s2 = e4m3x2_to_f16x2(scale_pair_bytes);  // (block 0, block 1)
+  const uint32_t sb0 = bcast_lo_half(s2), sb1 = bcast_hi_half(s2);
+  const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t sraw = j < 2 ? sb0 : sb1;
+    uint32_t r0, r1, r2, r3, scale;
+    if (j < kCvtWords) {
+      e2m1x8_to_f16x2x4(w[j], r0, r1, r2, r3);
+      scale = hmul2_bits(sraw, 0x20002000u);  // x 2^-7
+    } else {
+      e2m1x8_to_f16x2x4_shift(w[j], r0, r1, r2, r3);
+      scale = hmul2_bits(sraw, 0x58005800u);  // x 2^7
+    }
+    o[4 * j + 0] = hmul2_bits(r0, scale);
+    o[4 * j + 1] = hmul2_bits(r1, scale);
+    o[4 * j + 2] = hmul2_bits(r2, scale);
+    o[4 * j + 3] = hmul2_bits(r3, scale);
+  }
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+
+__device__ __forceinline__ __half h_store_value(float h, int* status) {
+  float v = h * kHScale;
+  if (fabsf(v) > 65504.f) {
+    atomicOr(status, static_cast<int>(MOE_DEV_H_SATURATED));
+    v = copysignf(65504.f, v);
+  }
+  return __float2half_rn(v);
+}
+
+__device__ __forceinline__ void trace_ev(const ExpertArgs& a, int role, int& cnt, int code, int idx) {
+  if (a.trace != nullptr && cnt < kTracePerRole) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    a.trace[(static_cast<size_t>(blockIdx.x) * kTraceRoles + role) * kTracePerRole + cnt] =
+        (static_cast<unsigned long long>(code) << 56) | (static_cast<unsigned long long>(idx & 0xffff) << 40) |
+        (t & 0xffffffffffull);
+    ++cnt;
+  }
+}
+
+}  // namespace mk
+
+using namespace mk;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    expert_mma_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_w2,
+                      const __grid_constant__ ExpertArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int i = 0; i < kStagesA; ++i) {
+      mbar_init(smem_addr(&sm.full_a[i]), 1);
+      mbar_init(smem_addr(&sm.empty_a[i]), kComputeWarps);
+    }
+    for (int i = 0; i < kStagesB; ++i) {
+      mbar_init(smem_addr(&sm.full_b[i]), 1);
+      mbar_init(smem_addr(&sm.empty_b[i]), kComputeWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&sm.sc_full[i]), 1);
+      mbar_init(smem_addr(&sm.sc_empty[i]), kComputeWarps);
+    }
+    for (int i = 0; i < kTaskSlots; ++i) {
+      mbar_init(smem_addr(&sm.task_full[i]), 1);
+      mbar_init(smem_addr(&sm.task_empty[i]), kTaskConsumers);
+    }
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_w13);
+    prefetch_tmap(&tm_w2);
+  }
+  __syncthreads();
+  const uint32_t ringa0 = smem_addr(&sm.ring_a[0][0]);
+  const uint32_t ringb0 = smem_addr(&sm.ring_b[0][0]);
+  int tcnt = 0;
+  if (tid == 0) trace_ev(a, 5, tcnt, 10, 0);
+
+  if (warp == 0) {
+    // ------------- task fetcher + weight producer (tickets two tasks ahead) -------------
+    const uint64_t pol = policy_evict_first();
+    const int ntot = __ldg(a.meta + META_NGU) + __ldg(a.meta + META_NDN);
+    const TaskEntry kEnd = TaskEntry{-1, 0, 0, 0};
+    int stage = 0, issued = 0, n = 0, chunk_seq = 0;
+    uint32_t phase = 0;
+    int cur = blockIdx.x, nxt = ntot;
+    TaskEntry entry = kEnd, entry_nxt = kEnd;
+    if (lane == 0 && cur < ntot) {
+      entry = a.tasks[cur];
+      nxt = static_cast<int>(atomicAdd(a.ticket, 1u)) + static_cast<int>(gridDim.x);
+      if (nxt < ntot) entry_nxt = a.tasks[nxt];
+    }
+    bool ok = true;
+    while (ok) {
+      const int q = n % kTaskSlots;
+      if (!warp_wait(smem_addr(&sm.task_empty[q]), static_cast<uint32_t>(((n / kTaskSlots) & 1) ^ 1), sm,
+                     a.status)) {
+        ok = false;
+        break;
+      }
+      const bool live = __shfl_sync(0xffffffffu, cur, 0) < ntot;
+      if (lane == 0) {
+        sm.task[q] = live ? entry : kEnd;
+        mbar_arrive(smem_addr(&sm.task_full[q]));
+        trace_ev(a, 0, tcnt, 1, cur);
+      }
+      if (!live) break;
+      const int x = __shfl_sync(0xffffffffu, entry.x, 0);
+      const int z = __shfl_sync(0xffffffffu, entry.z, 0);
+      const int s = __shfl_sync(0xffffffffu, entry.w, 0);
+      int nxt2 = ntot;
+      if (lane == 0 && nxt < ntot) nxt2 = static_cast<int>(atomicAdd(a.ticket, 1u)) + static_cast<int>(gridDim.x);
+      const int e = x & 0xffff;
+      const bool is_dn = ((z >> 16) & 1) != 0;
+      int rA0, rA1, nck;
+      const CUtensorMap* tm;
+      if (!is_dn) {
+        rA0 = e * 2 * a.F + s * kGuRows;
+        rA1 = rA0 + a.F;
+        tm = &tm_w13;
+        nck = a.d / kChunk;
+      } else {
+        rA0 = e * a.d + s * kDnRows;
+        rA1 = rA0 + 64;
+        tm = &tm_w2;
+        nck = a.F / kChunk;
+      }
+      // block scales of the task's 128 rows: contiguous per 64-row half
+      const int sn = n & 1;
+      if (!warp_wait(smem_addr(&sm.sc_empty[sn]), static_cast<uint32_t>(((n >> 1) & 1) ^ 1), sm, a.status)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        const uint32_t sbar = smem_addr(&sm.sc_full[sn]);
+        const uint32_t sdst = smem_addr(&sm.scales[sn][0]);
+        if (!is_dn) {
+          const uint32_t half_bytes = 64u * static_cast<uint32_t>(a.d / 16);
+          mbar_arrive_expect_tx(sbar, 2 * half_bytes);
+          bulk_copy_g2s(sdst, a.w13_scales + static_cast<size_t>(rA0) * (a.d / 16), half_bytes, sbar);
+          bulk_copy_g2s(sdst + half_bytes, a.w13_scales + static_cast<size_t>(rA1) * (a.d / 16), half_bytes, sbar);
+        } else {
+          const uint32_t bytes = 128u * static_cast<uint32_t>(a.F / 16);
+          mbar_arrive_expect_tx(sbar, bytes);
+          bulk_copy_g2s(sdst, a.w2_scales + static_cast<size_t>(rA0) * (a.F / 16), bytes, sbar);
+        }
+      }
+      ++n;
+      for (int c = 0; c < nck; ++c) {
+        if (!warp_wait(smem_addr(&sm.empty_a[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
+        if (lane == 0) {
+          const uint32_t sb = ringa0 + stage * kStageA;
+          const uint32_t fa = smem_addr(&sm.full_a[stage]);
+          mbar_arrive_expect_tx(fa, kStageA);
+          tma_load_2d(sb, tm, c * (kChunk / 2), rA0, fa, pol);
+          tma_load_2d(sb + kStageA / 2, tm, c * (kChunk / 2), rA1, fa, pol);
+          trace_ev(a, 0, tcnt, 2, chunk_seq);
+        }
+        ++chunk_seq;
+        ++issued;
+        if (++stage == kStagesA) { stage = 0; phase ^= 1u; }
+      }
+      if (lane == 0) {
+        cur = nxt;
+        entry = entry_nxt;
+        nxt = nxt2;
+        entry_nxt = nxt < ntot ? a.tasks[nxt] : kEnd;
+      }
+    }
+    // drain: every copy this warp started has landed before the CTA exits
+    if (lane == 0) {
+      int st = stage;
+      uint32_t ph = phase;
+      for (int i = 0; i < min(issued, kStagesA); ++i) {
+        if (--st < 0) { st = kStagesA - 1; ph ^= 1u; }
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kTimeoutCycles) {}
+      }
+      for (int m = max(0, n - 2); m < n; ++m) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_addr(&sm.sc_full[m & 1]), static_cast<uint32_t>((m >> 1) & 1)) &&
+               clock64() - t0 < kTimeoutCycles) {}
+      }
+    }
+  } else if (warp == 1) {
+    // ------------- activation producer: 8-row tiles, one bulk copy per routed row -------------
+    const uint64_t pol_keep = 0;
+    (void)pol_keep;
+    int stage = 0, n = 0, issued = 0, chunk_seq = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    while (ok) {
+      TaskEntry te;
+      if (!take_task(sm, n++, te, a.status)) break;
+      if (te.x < 0) break;
+      const int e = te.x & 0xffff, u = (te.x >> 16) & 0xffff, row0 = te.y, rows = te.z & 0xffff;
+      const bool is_dn = ((te.z >> 16) & 1) != 0;
+      if (is_dn) {
+        // every gate/up warp of every stripe (all passes) of this expert must have published
+        const int npass = (__ldg(a.counts + e) + kRowsPerPass - 1) / kRowsPerPass;
+        const uint32_t target = static_cast<uint32_t>(npass * a.S_gu * kComputeWarps);
+        int good = 1;
+        if (lane == 0) {
+          const long long t0 = clock64();
+          while (ld_acquire_u32(a.ready + u) < target) {
+            if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) { good = 0; break; }
+            if (clock64() - t0 > kTimeoutCycles) {
+              *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
+              atomicOr(a.status, static_cast<int>(MOE_DEV_TIMEOUT));
+              good = 0;
+              break;
+            }
+            __nanosleep(32);
+          }
+          trace_ev(a, 1, tcnt, 3, n);
+        }
+        if (!__shfl_sync(0xffffffffu, good, 0)) break;
+      }
+      const int nck = is_dn ? a.F / kChunk : a.d / kChunk;
+      // lane l owns routed rows l and l + 32 of the pass
+      const __half* src0;
+      const __half* src1;
+      if (is_dn) {
+        src0 = a.hs16 + static_cast<size_t>(row0 + lane) * a.F;
+        src1 = a.hs16 + static_cast<size_t>(row0 + lane + 32) * a.F;
+      } else {
+        const int t0 = lane < rows ? __ldg(a.pos_tok + row0 + lane) : 0;
+        const int t1 = lane + 32 < rows ? __ldg(a.pos_tok + row0 + lane + 32) : 0;
+        src0 = a.x16 + static_cast<size_t>(t0) * a.d;
+        src1 = a.x16 + static_cast<size_t>(t1) * a.d;
+      }
+      const int nt = (rows + kTileRows - 1) / kTileRows;
+      for (int c = 0; ok && c < nck; ++c) {
+        for (int t = 0; t < nt; ++t) {
+          if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
+          const int trows = min(kTileRows, rows - t * kTileRows);
+          const uint32_t fb = smem_addr(&sm.full_b[stage]);
+          if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(trows) * (2 * kChunk));
+          __syncwarp();
+          // lanes 0..trows-1 copy their tile row: routed row r = 8t + lane
+          const int r = t * kTileRows + lane;
+          const __half* p0 = reinterpret_cast<const __half*>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src0), r & 31));
+          const __half* p1 = reinterpret_cast<const __half*>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src1), r & 31));
+          if (lane < trows) {
+            const __half* src = (r < 32 ? p0 : p1) + c * kChunk;
+            bulk_copy_g2s(ringb0 + stage * kStageB + lane * kRowPitchB, src, 2 * kChunk, fb);
+          }
+          ++issued;
+          if (++stage == kStagesB) { stage = 0; phase ^= 1u; }
+        }
+        if (lane == 0) trace_ev(a, 1, tcnt, 4, chunk_seq);
+        ++chunk_seq;
+      }
+    }
+    if (lane == 0) {
+      int st = stage;
+      uint32_t ph = phase;
+      for (int i = 0; i < min(issued, kStagesB); ++i) {
+        if (--st < 0) { st = kStagesB - 1; ph ^= 1u; }
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_addr(&sm.full_b[st]), ph) && clock64() - t0 < kTimeoutCycles) {}
+      }
+    }
+  } else {
+    // ------------- compute warps: dequantise into A fragments, mma.sync, epilogue -------------
+    const int cw = warp - 2;  // 0..7
+    const int g = lane >> 2, q = lane & 3;
+    int stage_a = 0, stage_b = 0, n = 0, chunk_seq = 0;
+    uint32_t phase_a = 0, phase_b = 0;
+    bool ok = true;
+    while (ok) {
+      TaskEntry te;
+      if (!take_task(sm, n, te, a.status)) break;
+      if (te.x < 0) break;
+      const int u = (te.x >> 16) & 0xffff, row0 = te.y, rows = te.z & 0xffff, s = te.w;
+      const bool is_dn = ((te.z >> 16) & 1) != 0;
+      const int K = is_dn ? a.F : a.d;
+      const int nck = K / kChunk;
+      const int nt = (rows + kTileRows - 1) / kTileRows;
+      // local rows (0..127 of the A tile) of fragment rows g and g + 8
+      const int lra = is_dn ? 16 * cw + g : 8 * cw + g;
+      const int lrb = is_dn ? 16 * cw + g + 8 : 64 + 8 * cw + g;
+      const int sn = n & 1;
+      if (!warp_wait(smem_addr(&sm.sc_full[sn]), static_cast<uint32_t>((n >> 1) & 1), sm, a.status)) break;
+      const uint8_t* srow_a = &sm.scales[sn][0] + lra * (K / 16) + 2 * q;
+      const uint8_t* srow_b = &sm.scales[sn][0] + lrb * (K / 16) + 2 * q;
+      float acc[kMaxTiles][4];
+#pragma unroll
+      for (int t = 0; t < kMaxTiles; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+      for (int c = 0; c < nck; ++c) {
+        if (!warp_wait(smem_addr(&sm.full_a[stage_a]), phase_a, sm, a.status)) { ok = false; break; }
+        if (cw == 0 && lane == 0) trace_ev(a, 2, tcnt, 5, chunk_seq);
+        // codes: sub-chunk h covers K [128h, 128h+128); thread q its elements [32q, 32q+32),
+        // i.e. 16-byte chunk 4h + q of the 128-byte row, stored at (chunk ^ (row & 7))
+        const uint8_t* st = &sm.ring_a[stage_a][0];
+        const int ha = lra >> 6, ra = lra & 63, hb = lrb >> 6, rb = lrb & 63;
+        const uint8_t* pa = st + ha * (kStageA / 2) + ra * 128;
+        const uint8_t* pb = st + hb * (kStageA / 2) + rb * 128;
+        uint4 ca[2], cb[2];
+        uint32_t sa[2], sbv[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          ca[h] = *reinterpret_cast<const uint4*>(pa + (((4 * h + q) ^ (ra & 7)) << 4));
+          cb[h] = *reinterpret_cast<const uint4*>(pb + (((4 * h + q) ^ (rb & 7)) << 4));
+          sa[h] = *reinterpret_cast<const uint16_t*>(srow_a + 16 * c + 8 * h);
+          sbv[h] = *reinterpret_cast<const uint16_t*>(srow_b + 16 * c + 8 * h);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.empty_a[stage_a]));
+        if (++stage_a == kStagesA) { stage_a = 0; phase_a ^= 1u; }
+        uint32_t fa[2][16], fb[2][16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          dequant32(ca[h], sa[h], fa[h]);
+          dequant32(cb[h], sbv[h], fb[h]);
+        }
+        // The 16 k-steps of a chunk go to independent accumulator sets where tiles leave
+        // registers free (8 sets for one 8-row tile, 4 per tile for two), so consecutive MMAs
+        // do not wait on each other; the sets are summed at the end of the task.
+#pragma unroll
+        for (int t = 0; t < kMaxTiles; ++t) {
+          if (t < nt) {
+            if (!warp_wait(smem_addr(&sm.full_b[stage_b]), phase_b, sm, a.status)) { ok = false; break; }
+            // tile row g, elements [128h + 32q, +32) in four 16-byte pieces
+            const uint8_t* brow = &sm.ring_b[stage_b][0] + g * kRowPitchB + 64 * q;
+            uint4 xb[2][4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int jp = 0; jp < 4; ++jp) xb[h][jp] = *reinterpret_cast<const uint4*>(brow + 256 * h + 16 * jp);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&sm.empty_b[stage_b]));
+            if (++stage_b == kStagesB) { stage_b = 0; phase_b ^= 1u; }
+            if (nt == 1) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  // word j covers k-steps 2j (registers 4j, 4j+1) and 2j+1 (4j+2, 4j+3)
+                  mma_16816(acc[(4 * h + j) & 7], fa[h][4 * j + 0], fb[h][4 * j + 0], fa[h][4 * j + 1],
+                            fb[h][4 * j + 1], xb[h][j].x, xb[h][j].y);
+                  mma_16816(acc[(4 * h + j + 4) & 7], fa[h][4 * j + 2], fb[h][4 * j + 2], fa[h][4 * j + 3],
+                            fb[h][4 * j + 3], xb[h][j].z, xb[h][j].w);
+                }
+            } else if (nt == 2) {
+              if (t < 2) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    mma_16816(acc[4 * t + ((2 * h + j) & 3)], fa[h][4 * j + 0], fb[h][4 * j + 0], fa[h][4 * j + 1],
+                              fb[h][4 * j + 1], xb[h][j].x, xb[h][j].y);
+                    mma_16816(acc[4 * t + ((2 * h + j + 2) & 3)], fa[h][4 * j + 2], fb[h][4 * j + 2],
+                              fa[h][4 * j + 3], fb[h][4 * j + 3], xb[h][j].z, xb[h][j].w);
+                  }
+              }
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  mma_16816(acc[t], fa[h][4 * j + 0], fb[h][4 * j + 0], fa[h][4 * j + 1], fb[h][4 * j + 1],
+                            xb[h][j].x, xb[h][j].y);
+                  mma_16816(acc[t], fa[h][4 * j + 2], fb[h][4 * j + 2], fa[h][4 * j + 3], fb[h][4 * j + 3],
+                            xb[h][j].z, xb[h][j].w);
+                }
+            }
+          }
+        }
+        if (!ok) break;
+        if (cw == 0 && lane == 0) trace_ev(a, 2, tcnt, 6, chunk_seq);
+        ++chunk_seq;
+      }
+      if (!ok) break;
+      // the task's scales are no longer needed
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&sm.sc_empty[sn]));
+      ++n;
+      // fold the independent accumulator sets into one set per tile
+      if (nt == 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          acc[0][i] = ((acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i])) +
+                      ((acc[4][i] + acc[5][i]) + (acc[6][i] + acc[7][i]));
+      } else if (nt == 2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[0][i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);
+          acc[1][i] = (acc[4][i] + acc[5][i]) + (acc[6][i] + acc[7][i]);
+        }
+      }
+      // ---- epilogue: rows g / g+8, routed rows 8t + 2q, 8t + 2q + 1 ----
+      if (!is_dn) {
+        const int nidx = act_pos(s * kGuRows + 8 * cw + g);  // storage position of element n
+        const float sc = a.w13_ts * kAccUnscale;
+#pragma unroll
+        for (int t = 0; t < kMaxTiles; ++t) {
+          if (t < nt) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int r = t * kTileRows + 2 * q + cc;
+              if (r < rows)
+                a.hs16[static_cast<size_t>(row0 + r) * a.F + nidx] =
+                    h_store_value(silu_mul(acc[t][cc] * sc, acc[t][2 + cc] * sc), a.status);
+            }
+          }
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atom_add_acqrel_u32(a.ready + u, 1u);
+      } else {
+        const float sc = a.w2_ts * kHUnscale * kAccUnscale;
+        const int ra = s * kDnRows + lra, rb = s * kDnRows + lrb;
+#pragma unroll
+        for (int t = 0; t < kMaxTiles; ++t) {
+          if (t < nt) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int r = t * kTileRows + 2 * q + cc;
+              if (r < rows) {
+                float* yrow = a.y + static_cast<size_t>(row0 + r) * a.d;
+                yrow[ra] = acc[t][cc] * sc;
+                yrow[rb] = acc[t][2 + cc] * sc;
+              }
+            }
+          }
+        }
+      }
+      if (cw == 0 && lane == 0) trace_ev(a, 4, tcnt, 9, n);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int c2 = 1;
+    trace_ev(a, 5, c2, 11, 0);
+  }
+}
+
+size_t expert_mma_smem_bytes() { return sizeof(Smem) + 1024; }
+
+bool expert_mma_supports(int d, int F) {
+  return d % kChunk == 0 && F % kChunk == 0 && d / 16 <= kScaleSlot / 128 && F / 16 <= kScaleSlot / 128;
+}
+
+cudaError_t launch_expert_mma(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
+                              int num_sms, cudaStream_t stream) {
+  const size_t smem = expert_mma_smem_bytes();
+  cudaError_t err = cudaFuncSetAttribute(expert_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  expert_mma_kernel<<<num_sms, kThreads, smem, stream>>>(tm_w13, tm_w2, a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

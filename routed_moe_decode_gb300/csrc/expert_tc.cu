@@ -1,11 +1,14 @@
-// Persistent weight-stripe expert kernel (gate/up + SiLU*mul, down + weighted un-route)
-// on the 5th-generation tensor core.
+// Persistent weight-stripe expert kernel (gate/up + SiLU*mul, down projection) on the
+// 5th-generation tensor core, followed by the fixed-order un-route kernel.
 //
 // Design (the pages' ideas re-derived for sm_103a; "Persistent execution for Flash-Next
 // GGUF on SM70", sections "MonoMoE" and "First implementation boundary"):
-//   * one resident CTA per SM walks a static list of tasks; every gate/up task id is
-//     below every down task id, so a CTA that waits on a down task only waits for work
-//     that resident CTAs already own (forward progress without a grid barrier);
+//   * one resident CTA per SM takes tasks from the plan's task table through a ticket
+//     counter (first ticket = CTA index); every gate/up task precedes every down task in
+//     the table, so a CTA waiting on a down task only waits for tasks that resident CTAs
+//     already hold (forward progress without a grid barrier);
+//   * one warp fetches tickets ahead and publishes the decoded task to the other roles
+//     through a shared-memory task ring, so no role decodes tasks from global memory;
 //   * each task streams one stripe of one touched expert's NVFP4 weights exactly once,
 //     whatever the number of routed rows (unique-expert reuse): TMA tiles of E2M1 codes
 //     (64-byte swizzled rows) plus cp.async block scales into a multi-stage ring;
@@ -14,90 +17,77 @@
 //     tensor memory, where it is the A operand of tcgen05.mma (kind::f16, FP32
 //     accumulators in tensor memory); the routed token rows are the N = 16 operand in
 //     shared memory (128-byte swizzle), so one weight pass serves up to 64 rows;
-//   * gate/up tasks publish per-expert readiness counters after their FP16 h rows are
-//     stored (release); down tasks wait on them (acquire) before loading h, while their
+//   * gate/up tasks publish a per-expert readiness counter after their FP16 h rows are
+//     stored (release); down tasks wait on it (acquire) before loading h, while their
 //     weights already stream;
-//   * down tasks write per-route FP32 outputs; the CTA whose counter increment completes
-//     a (token, 128-column stripe) sums the k routes in slot order, adds the residual
-//     and writes BF16 (fixed-order reduction, no float atomics);
-//   * every wait is bounded: on expiry the CTA records MOE_DEV_TIMEOUT, drains its own
-//     copies and MMAs, frees tensor memory and returns.
+//   * down tasks store per-route FP32 outputs; the un-route kernel then sums the k
+//     routes of each token in slot order and adds the residual (fixed-order reduction,
+//     no float atomics);
+//   * every wait is bounded: on expiry the CTA records MOE_DEV_TIMEOUT, every role stops
+//     (warp-uniform decisions), the producer drains its copies, the MMA warp its MMAs,
+//     and tensor memory is freed.
 //
-// Warp roles (352 threads): 0-3 epilogue, 4-7 dequantisation, 8 weight producer (TMA +
-// scales), 9 activation producer (cp.async), 10 MMA issuer and tensor-memory owner.
+// Warp roles (352 threads): 0-3 epilogue, 4-7 dequantisation, 8 weight producer and task
+// fetcher, 9 activation producer, 10 MMA issuer and tensor-memory owner.
 #include "moe_kernels.cuh"
 
 namespace moe {
 
 namespace tc {
 
-constexpr int kStages = 7;
+constexpr int kStagesA = 14;        // weight ring (codes + scales), released by the dequant warps
+constexpr int kStagesB = 16;        // activation ring (one 16-row group per stage), released by the MMA
 constexpr int kStageCodes = 8192;   // 2 halves x 64 rows x 64 B (SWIZZLE_64B)
 constexpr int kStageScales = 1024;  // 128 rows x 8 B
-constexpr int kStageB = 16384;      // 4 groups x 2 atoms x (16 rows x 128 B), SWIZZLE_128B
+constexpr int kStageA = kStageCodes + kStageScales;  // 9216, a multiple of 1024
 constexpr int kOffScales = kStageCodes;
-constexpr int kOffB = kStageCodes + kStageScales;  // 9216, 1024-aligned
-constexpr int kStageBytes = kStageCodes + kStageScales + kStageB;
+constexpr int kStageB = 4096;       // one group: 2 atoms x (16 rows x 128 B), SWIZZLE_128B
 constexpr int kNumA = 4;            // tensor-memory A buffers (64 columns each)
-constexpr int kNumD = 2;            // tensor-memory accumulator buffers (64 columns each)
+constexpr int kNumD = 4;            // tensor-memory accumulator buffers (64 columns each)
 constexpr int kDCol0 = kNumA * 64;  // first accumulator column
 constexpr int kTmemCols = 512;
+constexpr int kTaskSlots = 8;
+constexpr int kTaskConsumers = 10;  // activation producer, 4 dequant warps, MMA, 4 epilogue warps
 constexpr int kThreads = 352;
 constexpr long long kTimeoutCycles = 1ll << 33;  // ~4 s at 2 GHz
 
 struct Smem {
-  uint8_t ring[kStages][kStageBytes];
+  uint8_t ring_b[kStagesB][kStageB];
+  uint8_t ring_a[kStagesA][kStageA];
   float xch[kRowsPerPass * 64];  // up-projection values handed to the gate threads
-  uint64_t full_a[kStages];
-  uint64_t full_b[kStages];
-  uint64_t empty[kStages];
+  TaskEntry task[kTaskSlots];
+  uint64_t full_a[kStagesA];
+  uint64_t empty_a[kStagesA];
+  uint64_t full_b[kStagesB];
+  uint64_t empty_b[kStagesB];
   uint64_t a_full[kNumA];
   uint64_t a_empty[kNumA];
   uint64_t d_full[kNumD];
   uint64_t d_empty[kNumD];
+  uint64_t task_full[kTaskSlots];
+  uint64_t task_empty[kTaskSlots];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int last_flag;
-  int comb_tok[kRowsPerPass];
 };
 
+// Decoded task (from a TaskEntry); `valid` is false for the end-of-work sentinel.
 struct Task {
-  int is_dn, u, e, pass, s, part, row0, rows, nck, gid;
+  bool valid;
+  bool is_dn;
+  int e, u, row0, rows, s, nck;
 };
 
-__device__ __forceinline__ Task decode_task(const ExpertArgs& a, int t, int U, int ngu) {
-  Task k{};
-  const bool dn = t >= ngu;
-  const int* start = dn ? a.dn_start : a.gu_start;
-  int local = dn ? t - ngu : t;
-  int lo = 0, hi = U;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(start + mid) <= local) lo = mid;
-    else hi = mid;
-  }
-  local -= __ldg(start + lo);
-  k.is_dn = dn;
-  k.u = lo;
-  k.e = __ldg(a.touched + lo);
-  k.gid = t;
-  if (!dn) {
-    const int per_pass = a.S_gu * a.KS;
-    k.pass = local / per_pass;
-    const int rem = local - k.pass * per_pass;
-    k.s = rem / a.KS;
-    k.part = rem - k.s * a.KS;
-    k.nck = a.nck_gu;
-  } else {
-    k.pass = local / a.S_dn;
-    k.s = local - k.pass * a.S_dn;
-    k.part = 0;
-    k.nck = a.nck_dn;
-  }
-  const int m = __ldg(a.counts + k.e);
-  k.row0 = __ldg(a.offsets + k.e) + k.pass * kRowsPerPass;
-  k.rows = min(kRowsPerPass, m - k.pass * kRowsPerPass);
+__device__ __forceinline__ Task unpack(const TaskEntry& t, const ExpertArgs& a) {
+  Task k;
+  k.valid = t.x >= 0;
+  k.e = t.x & 0xffff;
+  k.u = (t.x >> 16) & 0xffff;
+  k.row0 = t.y;
+  k.rows = t.z & 0xffff;
+  k.is_dn = ((t.z >> 16) & 1) != 0;
+  k.s = t.w;
+  k.nck = k.is_dn ? a.nck_dn : a.nck_gu;
   return k;
 }
 
@@ -122,6 +112,18 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Smem& s
   return __all_sync(0xffffffffu, ok);
 }
 
+// Task-ring consumer: wait for slot n, copy the entry, release the slot (one arrival per
+// consuming warp, made by lane 0 after the warp has the entry).
+__device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* status) {
+  const int q = n % kTaskSlots;
+  const uint32_t ph = static_cast<uint32_t>((n / kTaskSlots) & 1);
+  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, sm, status)) return false;
+  out = sm.task[q];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&sm.task_empty[q]));
+  return true;
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
 __device__ __forceinline__ __half h_store_value(float h, int* status) {
@@ -131,6 +133,18 @@ __device__ __forceinline__ __half h_store_value(float h, int* status) {
     v = copysignf(65504.f, v);
   }
   return __float2half_rn(v);
+}
+
+// Optional timeline event (lane 0 of a role; no-op unless a trace buffer is given).
+__device__ __forceinline__ void trace_ev(const ExpertArgs& a, int role, int& cnt, int code, int idx) {
+  if (a.trace != nullptr && cnt < kTracePerRole) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    a.trace[(static_cast<size_t>(blockIdx.x) * kTraceRoles + role) * kTracePerRole + cnt] =
+        (static_cast<unsigned long long>(code) << 56) | (static_cast<unsigned long long>(idx & 0xffff) << 40) |
+        (t & 0xffffffffffull);
+    ++cnt;
+  }
 }
 
 }  // namespace tc
@@ -149,10 +163,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kStagesA; ++i) {
       mbar_init(smem_addr(&sm.full_a[i]), 33);  // 32 cp.async arrivals + 1 expect_tx arrival
+      mbar_init(smem_addr(&sm.empty_a[i]), 4);  // the four dequantisation warps
+    }
+    for (int i = 0; i < kStagesB; ++i) {
       mbar_init(smem_addr(&sm.full_b[i]), 32);
-      mbar_init(smem_addr(&sm.empty[i]), 1);
+      mbar_init(smem_addr(&sm.empty_b[i]), 1);  // MMA commit
     }
     for (int i = 0; i < kNumA; ++i) {
       mbar_init(smem_addr(&sm.a_full[i]), 4);
@@ -161,6 +178,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNumD; ++i) {
       mbar_init(smem_addr(&sm.d_full[i]), 1);
       mbar_init(smem_addr(&sm.d_empty[i]), 4);
+    }
+    for (int i = 0; i < kTaskSlots; ++i) {
+      mbar_init(smem_addr(&sm.task_full[i]), 1);
+      mbar_init(smem_addr(&sm.task_empty[i]), kTaskConsumers);
     }
     mbar_init(smem_addr(&sm.drain), 1);
     sm.abort_flag = 0;
@@ -174,205 +195,306 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-
-  const int U = __ldg(a.meta + META_U);
-  const int ngu = __ldg(a.meta + META_NGU);
-  const int ntot = ngu + __ldg(a.meta + META_NDN);
-  const uint32_t ring0 = smem_addr(&sm.ring[0][0]);
+  const uint32_t ringa0 = smem_addr(&sm.ring_a[0][0]);
+  const uint32_t ringb0 = smem_addr(&sm.ring_b[0][0]);
+  int tcnt = 0;  // trace events of this thread's role
+  if (tid == 0) trace_ev(a, 5, tcnt, 10, 0);
 
   if (warp == 8) {
-    // ---------------- weight producer: TMA code tiles + cp.async block scales ----------------
+    // ------------- task fetcher + weight producer: TMA code tiles, cp.async scales -------------
+    // Tickets run two tasks ahead: the ticket of task i+2 is taken when task i starts and its
+    // table entry is loaded when task i ends, so neither latency stalls the copies.
     const uint64_t pol = policy_evict_first();
-    int stage = 0, issued = 0;
+    const int ntot = __ldg(a.meta + META_NGU) + __ldg(a.meta + META_NDN);
+    const TaskEntry kEnd = TaskEntry{-1, 0, 0, 0};
+    int stage = 0, issued = 0, n = 0, chunk_seq = 0;
     uint32_t phase = 0;
-    for (int t = blockIdx.x; t < ntot; t += gridDim.x) {
-      const Task tk = decode_task(a, t, U, ngu);
-      int rA0, rA1, sstride;
+    int cur = blockIdx.x, nxt = ntot;  // second ticket: the first dynamic one
+    TaskEntry entry = kEnd, entry_nxt = kEnd;
+    if (lane == 0) {
+      if (cur < ntot) entry = a.tasks[cur];
+      if (cur < ntot) {
+        nxt = static_cast<int>(atomicAdd(a.ticket, 1u)) + static_cast<int>(gridDim.x);
+        if (nxt < ntot) entry_nxt = a.tasks[nxt];
+      }
+    }
+    bool ok = true;
+    while (ok) {
+      // publish the current task (or the end-of-work sentinel) to the consumers
+      const int q = n % kTaskSlots;
+      if (!warp_wait(smem_addr(&sm.task_empty[q]), static_cast<uint32_t>(((n / kTaskSlots) & 1) ^ 1), sm,
+                     a.status)) {
+        ok = false;
+        break;
+      }
+      const bool live = __shfl_sync(0xffffffffu, cur, 0) < ntot;
+      if (lane == 0) {
+        sm.task[q] = live ? entry : kEnd;
+        mbar_arrive(smem_addr(&sm.task_full[q]));
+        trace_ev(a, 0, tcnt, 1, cur);
+      }
+      ++n;
+      if (!live) break;
+      const int x = __shfl_sync(0xffffffffu, entry.x, 0);
+      const int z = __shfl_sync(0xffffffffu, entry.z, 0);
+      const int s = __shfl_sync(0xffffffffu, entry.w, 0);
+      int nxt2 = ntot;
+      if (lane == 0 && nxt < ntot) nxt2 = static_cast<int>(atomicAdd(a.ticket, 1u)) + static_cast<int>(gridDim.x);
+      const int e = x & 0xffff;
+      const bool is_dn = ((z >> 16) & 1) != 0;
+      int rA0, rA1, sstride, nck;
       const CUtensorMap* tm;
       const uint8_t* sbase;
-      if (!tk.is_dn) {
-        rA0 = tk.e * 2 * a.F + tk.s * kGuRows;
+      if (!is_dn) {
+        rA0 = e * 2 * a.F + s * kGuRows;
         rA1 = rA0 + a.F;
         sstride = a.d / 16;
         tm = &tm_w13;
         sbase = a.w13_scales;
+        nck = a.nck_gu;
       } else {
-        rA0 = tk.e * a.d + tk.s * kDnRows;
+        rA0 = e * a.d + s * kDnRows;
         rA1 = rA0 + 64;
         sstride = a.F / 16;
         tm = &tm_w2;
         sbase = a.w2_scales;
+        nck = a.nck_dn;
       }
-      const int kpart = tk.is_dn ? 0 : tk.part * (a.d / a.KS);
-      bool ok = true;
-      for (int c = 0; c < tk.nck; ++c) {
-        if (!warp_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
-        const int kb = kpart + c * kChunkK;
-        const uint32_t sbase_smem = ring0 + stage * kStageBytes;
+      for (int c = 0; c < nck; ++c) {
+        if (!warp_wait(smem_addr(&sm.empty_a[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
+        const int kb = c * kChunkK;
+        const uint32_t sb = ringa0 + stage * kStageA;
         const uint32_t fa = smem_addr(&sm.full_a[stage]);
         if (lane == 0) {
           mbar_arrive_expect_tx(fa, kStageCodes);
-          tma_load_2d(sbase_smem, tm, kb / 2, rA0, fa, pol);
-          tma_load_2d(sbase_smem + kStageCodes / 2, tm, kb / 2, rA1, fa, pol);
+          tma_load_2d(sb, tm, kb / 2, rA0, fa, pol);
+          tma_load_2d(sb + kStageCodes / 2, tm, kb / 2, rA1, fa, pol);
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int i = lane + 32 * q;
+        for (int qq = 0; qq < 4; ++qq) {
+          const int i = lane + 32 * qq;
           const int grow = i < 64 ? rA0 + i : rA1 + (i - 64);
-          cp_async_8(sbase_smem + kOffScales + i * 8, sbase + static_cast<size_t>(grow) * sstride + kb / 16);
+          cp_async_8(sb + kOffScales + i * 8, sbase + static_cast<size_t>(grow) * sstride + kb / 16);
         }
         cp_async_arrive_noinc(fa);
+        if (lane == 0) trace_ev(a, 0, tcnt, 2, chunk_seq);
+        ++chunk_seq;
         ++issued;
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (++stage == kStagesA) { stage = 0; phase ^= 1u; }
       }
-      if (!ok) break;
+      // advance: task i+1 becomes current, task i+2's entry is loaded now
+      if (lane == 0) {
+        cur = nxt;
+        entry = entry_nxt;
+        nxt = nxt2;
+        entry_nxt = nxt < ntot ? a.tasks[nxt] : kEnd;
+      }
     }
     cp_async_wait_all();
     // drain: the last phase issued on every stage must have landed before the CTA exits
     if (lane == 0) {
       int st = stage;
       uint32_t ph = phase;
-      for (int n = 0; n < min(issued, kStages); ++n) {
-        if (--st < 0) { st = kStages - 1; ph ^= 1u; }
+      for (int i = 0; i < min(issued, kStagesA); ++i) {
+        if (--st < 0) { st = kStagesA - 1; ph ^= 1u; }
         const long long t0 = clock64();
         while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kTimeoutCycles) {}
       }
     }
   } else if (warp == 9) {
     // ---------------- activation producer: routed rows (FP16) via cp.async ----------------
-    int stage = 0;
+    int stage = 0, n = 0, chunk_seq = 0;
     uint32_t phase = 0;
-    for (int t = blockIdx.x; t < ntot; t += gridDim.x) {
-      const Task tk = decode_task(a, t, U, ngu);
-      bool ok = true;
+    bool ok = true;
+    while (ok) {
+      TaskEntry te;
+      if (!take_task(sm, n++, te, a.status)) break;
+      const Task tk = unpack(te, a);
+      if (!tk.valid) break;
       if (tk.is_dn) {
-        // all gate/up stripes of this expert (every pass) must have published h
+        // every gate/up stripe of this expert (all passes) must have published its h rows
         const int npass = (__ldg(a.counts + tk.e) + kRowsPerPass - 1) / kRowsPerPass;
         const uint32_t target = static_cast<uint32_t>(npass * a.S_gu);
+        int good = 1;
         if (lane == 0) {
           const long long t0 = clock64();
           while (ld_acquire_u32(a.ready + tk.u) < target) {
-            if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) { ok = false; break; }
+            if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) { good = 0; break; }
             if (clock64() - t0 > kTimeoutCycles) {
               *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
               atomicOr(a.status, static_cast<int>(MOE_DEV_TIMEOUT));
-              ok = false;
+              good = 0;
               break;
             }
-            __nanosleep(64);
+            __nanosleep(32);
           }
+          trace_ev(a, 1, tcnt, 3, n);
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
+        if (!__shfl_sync(0xffffffffu, good, 0)) break;
       }
-      const int kpart = tk.is_dn ? 0 : tk.part * (a.d / a.KS);
-      for (int c = 0; c < tk.nck; ++c) {
-        if (!warp_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
-        const int kb = kpart + c * kChunkK;
-        const uint32_t bbase = ring0 + stage * kStageBytes + kOffB;
-        const int g = lane & 15;  // 16-byte granule of the 256-byte row chunk
-        for (int r0 = 0; r0 < tk.rows; r0 += 2) {
-          const int r = r0 + (lane >> 4);
-          if (r < tk.rows) {
-            const __half* src = tk.is_dn ? a.hs16 + static_cast<size_t>(tk.row0 + r) * a.F + kb + g * 8
-                                         : a.x16 + static_cast<size_t>(__ldg(a.pos_tok + tk.row0 + r)) * a.d + kb + g * 8;
-            const int atom = g >> 3, ch = g & 7, grp = r >> 4, rr = r & 15;
-            const uint32_t dst = bbase + grp * 4096 + atom * 2048 + (rr >> 3) * 1024 + (rr & 7) * 128 +
-                                 ((ch ^ (rr & 7)) << 4);
-            cp_async_16(dst, src);
+      // source row of each routed row of this pass: lanes hold rows lane and lane + 32
+      const __half* src0 = nullptr;
+      const __half* src1 = nullptr;
+      if (tk.is_dn) {
+        src0 = a.hs16 + static_cast<size_t>(tk.row0 + lane) * a.F;
+        src1 = a.hs16 + static_cast<size_t>(tk.row0 + lane + 32) * a.F;
+      } else {
+        const int t0 = lane < tk.rows ? __ldg(a.pos_tok + tk.row0 + lane) : 0;
+        const int t1 = lane + 32 < tk.rows ? __ldg(a.pos_tok + tk.row0 + lane + 32) : 0;
+        src0 = a.x16 + static_cast<size_t>(t0) * a.d;
+        src1 = a.x16 + static_cast<size_t>(t1) * a.d;
+      }
+      const int g = lane & 15;  // 16-byte granule of the 256-byte row chunk
+      const int atom = g >> 3, ch = g & 7;
+      const int G = (tk.rows + kGroupRows - 1) / kGroupRows;
+      for (int c = 0; ok && c < tk.nck; ++c) {
+        const int kb = c * kChunkK;
+        for (int grp = 0; grp < G; ++grp) {
+          if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
+          const uint32_t bbase = ringb0 + stage * kStageB;
+          const int rend = min(tk.rows, (grp + 1) * kGroupRows);
+          for (int r0 = grp * kGroupRows; r0 < rend; r0 += 2) {
+            const int r = r0 + (lane >> 4);
+            // row r's base pointer lives in lane (r & 31), register src0 (r < 32) or src1
+            const __half* p0 = reinterpret_cast<const __half*>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src0), r & 31));
+            const __half* p1 = reinterpret_cast<const __half*>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src1), r & 31));
+            if (r < rend) {
+              const __half* src = (r < 32 ? p0 : p1) + kb + g * 8;
+              const int rr = r & 15;
+              const uint32_t dst = bbase + atom * 2048 + (rr >> 3) * 1024 + (rr & 7) * 128 + ((ch ^ (rr & 7)) << 4);
+              cp_async_16(dst, src);
+            }
           }
+          cp_async_arrive_noinc(smem_addr(&sm.full_b[stage]));
+          if (++stage == kStagesB) { stage = 0; phase ^= 1u; }
         }
-        cp_async_arrive_noinc(smem_addr(&sm.full_b[stage]));
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (lane == 0) trace_ev(a, 1, tcnt, 4, chunk_seq);
+        ++chunk_seq;
       }
-      if (!ok) break;
     }
     cp_async_wait_all();
   } else if (warp >= 4 && warp < 8) {
     // ---------------- dequantisation: NVFP4 -> FP16 A tile in tensor memory ----------------
-    const int i = tid - 128;           // A row of this thread (= tensor-memory lane)
+    const int i = tid - 128;  // A row of this thread (= tensor-memory lane)
     const int half = i >> 6, r = i & 63;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    int stage = 0, abuf = 0;
+    int stage = 0, abuf = 0, n = 0, chunk_seq = 0, tcnt2 = 0;
     uint32_t phase = 0, aphase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < ntot && ok; t += gridDim.x) {
-      const Task tk = decode_task(a, t, U, ngu);
+    while (ok) {
+      TaskEntry te;
+      if (!take_task(sm, n++, te, a.status)) break;
+      const Task tk = unpack(te, a);
+      if (!tk.valid) break;
       for (int c = 0; c < tk.nck; ++c) {
         if (!warp_wait(smem_addr(&sm.full_a[stage]), phase, sm, a.status)) { ok = false; break; }
-        if (!warp_wait(smem_addr(&sm.a_empty[abuf]), aphase ^ 1u, sm, a.status)) { ok = false; break; }
-        tc_fence_after();
-        const uint8_t* st = &sm.ring[stage][0];
+        if (warp == 4 && lane == 0) trace_ev(a, 2, tcnt, 5, chunk_seq);
+        const uint8_t* st = &sm.ring_a[stage][0];
         const uint8_t* crow = st + half * (kStageCodes / 2) + r * 64;
         uint4 q[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) q[j] = *reinterpret_cast<const uint4*>(crow + ((j ^ ((r >> 1) & 3)) << 4));
         const uint2 sc = *reinterpret_cast<const uint2*>(st + kOffScales + i * 8);
         uint32_t v[64];
+        // block scales s (one per 16 elements) as FP16x2 pairs, pre-multiplied by 2^-7 for
+        // the conversion kind and by 2^7 for the shift kind (see kCvtWords)
         const uint32_t s01 = e4m3x2_to_f16x2(sc.x), s23 = e4m3x2_to_f16x2(sc.x >> 16);
         const uint32_t s45 = e4m3x2_to_f16x2(sc.y), s67 = e4m3x2_to_f16x2(sc.y >> 16);
-        const uint32_t sb[8] = {bcast_lo_half(s01), bcast_hi_half(s01), bcast_lo_half(s23), bcast_hi_half(s23),
-                                bcast_lo_half(s45), bcast_hi_half(s45), bcast_lo_half(s67), bcast_hi_half(s67)};
+        const uint32_t sp[4] = {s01, s23, s45, s67};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint32_t w[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            const uint32_t scale = sb[2 * j + (h >> 1)];  // 16 elements (2 words) per block
-            uint32_t o0, o1, o2, o3;
-            e2m1x8_to_f16x2x4(w[h], o0, o1, o2, o3);
-            v[16 * j + 4 * h + 0] = hmul2_bits(o0, scale);
-            v[16 * j + 4 * h + 1] = hmul2_bits(o1, scale);
-            v[16 * j + 4 * h + 2] = hmul2_bits(o2, scale);
-            v[16 * j + 4 * h + 3] = hmul2_bits(o3, scale);
+            const int wi = 4 * j + h;   // word index in the row chunk (8 elements each)
+            const int blk = wi >> 1;    // 16-element scale block
+            const uint32_t pair = sp[blk >> 1];
+            const uint32_t sraw = (blk & 1) ? bcast_hi_half(pair) : bcast_lo_half(pair);
+            uint32_t o0, o1, o2, o3, scale;
+            if ((wi & 3) < kCvtWords) {
+              e2m1x8_to_f16x2x4(w[h], o0, o1, o2, o3);
+              scale = hmul2_bits(sraw, 0x20002000u);   // x 2^-7
+            } else {
+              e2m1x8_to_f16x2x4_shift(w[h], o0, o1, o2, o3);
+              scale = hmul2_bits(sraw, 0x58005800u);   // x 2^7
+            }
+            v[4 * wi + 0] = hmul2_bits(o0, scale);
+            v[4 * wi + 1] = hmul2_bits(o1, scale);
+            v[4 * wi + 2] = hmul2_bits(o2, scale);
+            v[4 * wi + 3] = hmul2_bits(o3, scale);
           }
         }
+        // the weight stage is consumed (its bytes are in registers): hand it back
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.empty_a[stage]));
+        if (!warp_wait(smem_addr(&sm.a_empty[abuf]), aphase ^ 1u, sm, a.status)) { ok = false; break; }
+        if (warp == 4 && lane == 0) trace_ev(a, 7, tcnt2, 15, chunk_seq);
+        tc_fence_after();
         tmem_st_x64(tmem + lane_base + abuf * 64, v);
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.a_full[abuf]));
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (warp == 4 && lane == 0) trace_ev(a, 2, tcnt, 6, chunk_seq);
+        ++chunk_seq;
+        if (++stage == kStagesA) { stage = 0; phase ^= 1u; }
         if (++abuf == kNumA) { abuf = 0; aphase ^= 1u; }
       }
     }
   } else if (warp == 10) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(128, kGroupRows);
-      int stage = 0, abuf = 0, dbuf = 0;
-      uint32_t phase = 0, aphase = 0, dphase = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < ntot && ok; t += gridDim.x) {
-        const Task tk = decode_task(a, t, U, ngu);
+    // ---------------- MMA issuer (one lane; the whole warp takes the tasks) ----------------
+    const uint32_t idesc = idesc_f16_f32(128, kGroupRows);
+    int stage = 0, abuf = 0, dbuf = 0, n = 0, chunk_seq = 0;
+    uint32_t phase = 0, aphase = 0, dphase = 0;
+    bool ok = true;
+    while (ok) {
+      TaskEntry te;
+      if (!take_task(sm, n++, te, a.status)) break;
+      const Task tk = unpack(te, a);
+      if (!tk.valid) break;
+      if (lane == 0) {
         const int G = (tk.rows + kGroupRows - 1) / kGroupRows;
-        if (!bounded_wait(smem_addr(&sm.d_empty[dbuf]), dphase ^ 1u, sm, a.status)) { ok = false; break; }
+        if (!bounded_wait(smem_addr(&sm.d_empty[dbuf]), dphase ^ 1u, sm, a.status)) ok = false;
         tc_fence_after();
         const uint32_t dcol = tmem + kDCol0 + dbuf * 64;
-        for (int c = 0; c < tk.nck; ++c) {
-          if (!bounded_wait(smem_addr(&sm.full_b[stage]), phase, sm, a.status)) { ok = false; break; }
+        for (int c = 0; ok && c < tk.nck; ++c) {
           if (!bounded_wait(smem_addr(&sm.a_full[abuf]), aphase, sm, a.status)) { ok = false; break; }
+          trace_ev(a, 6, tcnt, 12, chunk_seq);
           tc_fence_after();
-          fence_proxy_async_smem();
-          const uint32_t bbase = ring0 + stage * kStageBytes + kOffB;
-          for (int g = 0; g < G; ++g) {
+          for (int g = 0; ok && g < G; ++g) {
+            const int bst = (stage + g) % kStagesB;
+            const uint32_t bph = phase ^ static_cast<uint32_t>((stage + g) >= kStagesB ? 1 : 0);
+            if (!bounded_wait(smem_addr(&sm.full_b[bst]), bph, sm, a.status)) { ok = false; break; }
+            tc_fence_after();
+            fence_proxy_async_smem();
+            if (g == 0) trace_ev(a, 6, tcnt, 13, chunk_seq);
+            const uint32_t bbase = ringb0 + bst * kStageB;
 #pragma unroll
             for (int kk = 0; kk < kChunkK / 16; ++kk) {
-              const uint64_t bdesc = smem_desc_sw128(bbase + g * 4096 + (kk >> 2) * 2048 + (kk & 3) * 32, 1024);
+              const uint64_t bdesc = smem_desc_sw128(bbase + (kk >> 2) * 2048 + (kk & 3) * 32, 1024);
               tc_mma_f16_ts(dcol + g * kGroupRows, tmem + abuf * 64 + kk * 8, bdesc, idesc,
                             (c > 0 || kk > 0) ? 1u : 0u);
             }
+            if (g == G - 1) trace_ev(a, 6, tcnt, 14, chunk_seq);
+            tc_commit(smem_addr(&sm.empty_b[bst]));
           }
+          if (!ok) break;
           tc_commit(smem_addr(&sm.a_empty[abuf]));
-          tc_commit(smem_addr(&sm.empty[stage]));
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          trace_ev(a, 3, tcnt, 7, chunk_seq);
+          ++chunk_seq;
+          stage += G;
+          if (stage >= kStagesB) { stage -= kStagesB; phase ^= 1u; }
           if (++abuf == kNumA) { abuf = 0; aphase ^= 1u; }
         }
-        if (!ok) break;
-        tc_commit(smem_addr(&sm.d_full[dbuf]));
+        if (ok) tc_commit(smem_addr(&sm.d_full[dbuf]));
         if (++dbuf == kNumD) { dbuf = 0; dphase ^= 1u; }
       }
-      // all issued MMAs complete before tensor memory is released
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0) {
+      // every issued MMA completes before tensor memory is released
       tc_commit(smem_addr(&sm.drain));
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_addr(&sm.drain), 0) && clock64() - t0 < kTimeoutCycles) {}
@@ -382,13 +504,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue (warps 0-3): thread i owns accumulator lane i ----------------
     const int i = tid;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    int dbuf = 0;
+    int dbuf = 0, n = 0;
     uint32_t dphase = 0;
-    for (int t = blockIdx.x; t < ntot; t += gridDim.x) {
-      const Task tk = decode_task(a, t, U, ngu);
+    while (true) {
+      TaskEntry te;
+      const bool got_task = take_task(sm, n++, te, a.status);
+      if (!named_bar_and(2, 128, got_task)) break;
+      const Task tk = unpack(te, a);
+      if (!tk.valid) break;
       const int G = (tk.rows + kGroupRows - 1) / kGroupRows;
       const bool got = warp_wait(smem_addr(&sm.d_full[dbuf]), dphase, sm, a.status);
       if (!named_bar_and(2, 128, got)) break;
+      if (tid == 0) trace_ev(a, 4, tcnt, 8, n);
       tc_fence_after();
       uint32_t accb[kMaxGroups][16];
 #pragma unroll
@@ -399,99 +526,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&sm.d_empty[dbuf]));
+      if (tid == 0) trace_ev(a, 4, tcnt, 16, n);
       if (++dbuf == kNumD) { dbuf = 0; dphase ^= 1u; }
-      float acc[kRowsPerPass];
-#pragma unroll
-      for (int c = 0; c < kRowsPerPass; ++c) acc[c] = __uint_as_float(accb[c >> 4][c & 15]);
 
       if (!tk.is_dn) {
-        bool have = true;
-        if (a.KS > 1) {
-          // split-K partial: store, then the last of the KS parts reduces in part order
-          const int col = i < 64 ? tk.s * kGuRows + i : a.F + tk.s * kGuRows + (i - 64);
-          float* base = a.gu_part + (static_cast<size_t>(tk.part) * a.R + tk.row0) * (2 * a.F) + col;
+        // gate/up stripe: up values to the gate threads, h = silu(g) * u stored as FP16
+        if (i >= 64) {
 #pragma unroll
           for (int c = 0; c < kRowsPerPass; ++c)
-            if (c < tk.rows) base[static_cast<size_t>(c) * 2 * a.F] = acc[c];
-          __threadfence();
-          named_bar_sync(1, 128);
-          if (i == 0) {
-            const uint32_t old = atom_add_acqrel_u32(a.cnt_gu + tk.gid / a.KS, 1u);
-            sm.last_flag = (old == static_cast<uint32_t>(a.KS - 1)) ? 1 : 0;
-          }
-          named_bar_sync(1, 128);
-          have = sm.last_flag != 0;
-          if (have) {
-            __threadfence();
-            const float* pb = a.gu_part + static_cast<size_t>(tk.row0) * (2 * a.F) + col;
-#pragma unroll
-            for (int c = 0; c < kRowsPerPass; ++c) {
-              if (c < tk.rows) {
-                float v = 0.f;
-                for (int p = 0; p < a.KS; ++p) v += __ldcg(pb + (static_cast<size_t>(p) * a.R + c) * 2 * a.F);
-                acc[c] = v;
-              }
-            }
-          }
+            if (c < tk.rows) sm.xch[c * 64 + (i - 64)] = __uint_as_float(accb[c >> 4][c & 15]);
         }
-        if (have) {
-          if (i >= 64) {
+        named_bar_sync(1, 128);
+        if (i < 64) {
+          const int nidx = act_pos(tk.s * kGuRows + i);  // storage position of element n
+          const float sc13 = a.w13_ts * kAccUnscale;
 #pragma unroll
-            for (int c = 0; c < kRowsPerPass; ++c)
-              if (c < tk.rows) sm.xch[c * 64 + (i - 64)] = acc[c];
-          }
-          named_bar_sync(1, 128);
-          if (i < 64) {
-            const int n = tk.s * kGuRows + i;
-#pragma unroll
-            for (int c = 0; c < kRowsPerPass; ++c) {
-              if (c < tk.rows) {
-                const float g = acc[c] * a.w13_ts;
-                const float u = sm.xch[c * 64 + i] * a.w13_ts;
-                a.hs16[static_cast<size_t>(tk.row0 + c) * a.F + n] = h_store_value(silu_mul(g, u), a.status);
-              }
+          for (int c = 0; c < kRowsPerPass; ++c) {
+            if (c < tk.rows) {
+              const float gv = __uint_as_float(accb[c >> 4][c & 15]) * sc13;
+              const float uv = sm.xch[c * 64 + i] * sc13;
+              a.hs16[static_cast<size_t>(tk.row0 + c) * a.F + nidx] = h_store_value(silu_mul(gv, uv), a.status);
             }
           }
           __threadfence();
-          named_bar_sync(1, 128);
-          if (i == 0) atom_add_acqrel_u32(a.ready + tk.u, 1u);
         }
+        named_bar_sync(1, 128);
+        if (i == 0) atom_add_acqrel_u32(a.ready + tk.u, 1u);
       } else {
-        // down stripe: per-route FP32 outputs, then fixed-order combine by the last arrival
+        // down stripe: per-route FP32 outputs (summed over routes by the un-route kernel)
         const int rcol = tk.s * kDnRows + i;
-        const float scale = a.w2_ts * kHUnscale;
+        const float scale = a.w2_ts * kHUnscale * kAccUnscale;
 #pragma unroll
         for (int c = 0; c < kRowsPerPass; ++c)
-          if (c < tk.rows) a.y[static_cast<size_t>(tk.row0 + c) * a.d + rcol] = acc[c] * scale;
-        __threadfence();
-        named_bar_sync(1, 128);
-        if (i < tk.rows) {
-          const int tok = __ldg(a.pos_tok + tk.row0 + i);
-          const uint32_t old = atom_add_acqrel_u32(a.comb_cnt + static_cast<size_t>(tok) * a.S_dn + tk.s, 1u);
-          sm.comb_tok[i] = (old == static_cast<uint32_t>(a.k - 1)) ? tok : -1;
-        }
-        named_bar_sync(1, 128);
-        __threadfence();
-        for (int c = 0; c < tk.rows; ++c) {
-          const int tok = sm.comb_tok[c];
-          if (tok < 0) continue;
-          float accum = 0.f;
-          for (int j = 0; j < a.k; ++j) {
-            const int pos = __ldg(a.route_pos + tok * a.k + j);
-            const float w = __ldg(a.route_w + tok * a.k + j);
-            accum += w * __ldcg(a.y + static_cast<size_t>(pos) * a.d + rcol);
-          }
-          const size_t o = static_cast<size_t>(tok) * a.d + rcol;
-          const float res = a.residual ? __bfloat162float(a.residual[o]) : 0.f;
-          a.out[o] = __float2bfloat16_rn(res + accum);
-        }
-        named_bar_sync(1, 128);
+          if (c < tk.rows)
+            a.y[static_cast<size_t>(tk.row0 + c) * a.d + rcol] = __uint_as_float(accb[c >> 4][c & 15]) * scale;
       }
+      if (tid == 0) trace_ev(a, 4, tcnt, 9, n);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) {
+    int c2 = 1;
+    trace_ev(a, 5, c2, 11, 0);
+  }
   if (warp == 10) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -511,6 +590,51 @@ cudaError_t launch_expert_tc(const ExpertArgs& a, const CUtensorMap& tm_w13, con
 }
 
 // ---------------------------------------------------------------------------------
+// Un-route: out[t] = residual[t] + sum_{j<k} w_{t,j} y_{pos(t,j)}, slots in order, FP32,
+// one BF16 rounding ("First implementation boundary", step 4: routes summed in a fixed
+// order).  Each thread owns 4 consecutive columns of one token.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
+  const int t = blockIdx.x;
+  const int r = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+  if (r >= a.d) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int* rp = a.route_pos + static_cast<size_t>(t) * a.k;
+  const float* rw = a.route_w + static_cast<size_t>(t) * a.k;
+#pragma unroll 4
+  for (int j = 0; j < a.k; ++j) {
+    const int pos = __ldg(rp + j);
+    if (pos < 0) continue;
+    const float w = __ldg(rw + j);
+    const float4 yv = __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<size_t>(pos) * a.d + r));
+    acc.x += w * yv.x;
+    acc.y += w * yv.y;
+    acc.z += w * yv.z;
+    acc.w += w * yv.w;
+  }
+  const size_t o = static_cast<size_t>(t) * a.d + r;
+  float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (a.residual) {
+    const uint2 rb = *reinterpret_cast<const uint2*>(a.residual + o);
+    const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rb.x));
+    const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rb.y));
+    res = make_float4(r0.x, r0.y, r1.x, r1.y);
+  }
+  __nv_bfloat162 o0 = __floats2bfloat162_rn(res.x + acc.x, res.y + acc.y);
+  __nv_bfloat162 o1 = __floats2bfloat162_rn(res.z + acc.z, res.w + acc.w);
+  uint2 ob;
+  ob.x = *reinterpret_cast<uint32_t*>(&o0);
+  ob.y = *reinterpret_cast<uint32_t*>(&o1);
+  *reinterpret_cast<uint2*>(a.out + o) = ob;
+}
+
+cudaError_t launch_combine(const ExpertArgs& a, cudaStream_t stream) {
+  const dim3 grid(a.T, (a.d / 4 + 255) / 256);
+  combine_kernel<<<grid, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------
 // Per-call preparation: zero the counters this call uses and convert the hidden rows to
 // FP16 (the tensor-core operand type), flagging values outside the FP16 range.
 // ---------------------------------------------------------------------------------
@@ -518,20 +642,29 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs p) {
   const size_t gtid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t i = gtid; i < static_cast<size_t>(p.E); i += nthreads) p.ready[i] = 0u;
-  for (size_t i = gtid; i < static_cast<size_t>(p.max_units); i += nthreads) p.cnt_gu[i] = 0u;
-  for (size_t i = gtid; i < static_cast<size_t>(p.T) * p.S_dn; i += nthreads) p.comb_cnt[i] = 0u;
+  if (gtid == 0) *p.ticket = 0u;
   const size_t n8 = static_cast<size_t>(p.T) * p.d / 8;
   bool bad = false;
   for (size_t i = gtid; i < n8; i += nthreads) {
     const uint4 raw = reinterpret_cast<const uint4*>(p.hidden)[i];
     const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 t = __bfloat1622float2(b[j]);
+      f[2 * j] = t.x;
+      f[2 * j + 1] = t.y;
+    }
+    // 8-element groups of the shift kind are stored in the dequantisation's pairing
+    const bool perm = shift_group(static_cast<int>((i * 8) % static_cast<size_t>(p.d)));
     uint4 o;
     __half2* h = reinterpret_cast<__half2*>(&o);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = __bfloat1622float2(b[j]);
-      bad |= !(fabsf(f.x) <= 65504.f) || !(fabsf(f.y) <= 65504.f);
-      h[j] = __floats2half2_rn(f.x, f.y);
+    for (int q = 0; q < 4; ++q) {
+      const float lo = perm ? f[perm_elem(2 * q)] : f[2 * q];
+      const float hi = perm ? f[perm_elem(2 * q + 1)] : f[2 * q + 1];
+      bad |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
+      h[q] = __floats2half2_rn(lo, hi);
     }
     reinterpret_cast<uint4*>(p.x16)[i] = o;
   }
@@ -540,9 +673,7 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs p) {
 
 cudaError_t launch_prep(const PrepArgs& p, cudaStream_t stream) {
   const size_t n8 = static_cast<size_t>(p.T) * p.d / 8;
-  size_t work = n8;
-  if (static_cast<size_t>(p.T) * p.S_dn > work) work = static_cast<size_t>(p.T) * p.S_dn;
-  if (static_cast<size_t>(p.max_units) > work) work = p.max_units;
+  size_t work = n8 > static_cast<size_t>(p.E) ? n8 : static_cast<size_t>(p.E);
   int blocks = static_cast<int>((work + 255) / 256);
   if (blocks > 1184) blocks = 1184;
   if (blocks < 1) blocks = 1;

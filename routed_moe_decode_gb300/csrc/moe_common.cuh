@@ -15,7 +15,7 @@ namespace moe {
 // ---------------------------------------------------------------------------------
 // Geometry of the expert tasks.
 //   gate/up task : one expert, 64 F-rows of the gate projection plus the same 64 rows
-//                  of the up projection (a 128-row A tile), one K slice of d/KS;
+//                  of the up projection (a 128-row A tile), the full K = d;
 //   down task    : one expert, 128 d-rows of W2, the full K = ffn;
 //   rows         : at most kRowsPerPass routed rows per pass; experts with more rows
 //                  run several passes (each re-reads the weights).
@@ -30,37 +30,56 @@ constexpr int kMaxGroups = kRowsPerPass / kGroupRows;
 constexpr float kHScale = 0.0625f;  // h is stored as FP16(h * 2^-4)
 constexpr float kHUnscale = 16.0f;
 
+// Dequantisation handles E2M1 codes in words of 8 (32 consecutive elements = 4 words per
+// thread and row).  Words whose index mod 4 is below kCvtWords use the hardware
+// E2M1->FP16 conversion, which pairs neighbouring elements (2i, 2i+1) in one FP16x2
+// register; the others build FP16 bit patterns with integer shifts, which pairs elements
+// (j, j+4) of the word.  The two run on different pipes.  The FP16 activations (hidden
+// and h) are stored with the same pairing: in an 8-element group of the shift kind,
+// storage position p holds element perm_elem(p).  Both kinds leave a factor 2^-7 in the
+// products (the conversion kind is scaled by s * 2^-7, the shift kind, whose bits encode
+// w * 2^-14, by s * 2^7); kAccUnscale undoes it.
+constexpr int kCvtWords = 2;
+constexpr float kAccUnscale = 128.0f;
+
+__host__ __device__ constexpr bool shift_group(int k) { return ((k & 31) >> 3) >= kCvtWords; }
+// storage position of element o (0..7) inside a shift-kind group: elements 0..3 at the
+// even positions, 4..7 at the odd ones
+__host__ __device__ constexpr int perm_pos(int o) { return o < 4 ? 2 * o : 2 * (o - 4) + 1; }
+// element stored at position p (0..7) inside a shift-kind group
+__host__ __device__ constexpr int perm_elem(int p) { return (p & 1) ? (p >> 1) + 4 : (p >> 1); }
+// storage index of element k of an activation row
+__host__ __device__ constexpr int act_pos(int k) { return shift_group(k) ? (k & ~7) + perm_pos(k & 7) : k; }
+
 struct WsLayout {
   size_t status, meta, counts, offsets, touched, gu_start, dn_start, route_pos, pos_tok, route_w;
-  size_t ready, cnt_gu, comb_cnt, x16, hs16, gu_part, y, total;
-  int KS;         // gate/up K split (1, 2 or 4)
+  size_t ready, ticket, tasks, x16, hs16, y, total;
   int S_gu;       // gate/up stripes per expert (ffn / 64)
   int S_dn;       // down stripes per expert (d / 128)
-  int max_units;  // capacity of the gate/up unit counters
+  int max_tasks;  // capacity of the task table
   int R;          // routes = T * k
 };
 
 // meta words
-enum { META_U = 0, META_NGU = 1, META_NDN = 2, META_MAXROWS = 3, META_NUNITS = 4, META_WORDS = 8 };
+enum { META_U = 0, META_NGU = 1, META_NDN = 2, META_MAXROWS = 3, META_WORDS = 8 };
+
+// One expert task as the plan writes it (16 bytes):
+//   x = expert id | touched index << 16, y = first routed row (expert-major position),
+//   z = rows in this pass | is_down << 16, w = stripe index.
+struct TaskEntry {
+  int x, y, z, w;
+};
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
-inline int choose_ks(const moe_shape& s) {
-  const int R = s.T * s.k;
-  const int nk = s.d / kChunkK;
-  if (R > 512) return 1;
-  if (nk % 4 == 0) return 4;
-  if (nk % 2 == 0) return 2;
-  return 1;
-}
 
 inline WsLayout ws_layout(const moe_shape& s) {
   WsLayout L{};
   L.R = s.T * s.k;
-  L.KS = choose_ks(s);
   L.S_gu = s.ffn / kGuRows;
   L.S_dn = s.d / kDnRows;
-  L.max_units = L.S_gu * (s.E + (L.R + kRowsPerPass - 1) / kRowsPerPass + 1);
+  // passes over all experts: at most one per touched expert plus one per 64 extra rows
+  const int max_passes = s.E + (L.R + kRowsPerPass - 1) / kRowsPerPass;
+  L.max_tasks = max_passes * (L.S_gu + L.S_dn);
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   L.status = take(64);
@@ -74,11 +93,10 @@ inline WsLayout ws_layout(const moe_shape& s) {
   L.pos_tok = take(size_t(L.R) * 4);
   L.route_w = take(size_t(L.R) * 4);
   L.ready = take(size_t(s.E) * 4);
-  L.cnt_gu = take(size_t(L.max_units) * 4);
-  L.comb_cnt = take(size_t(s.T) * L.S_dn * 4);
+  L.ticket = take(4);
+  L.tasks = take(size_t(L.max_tasks) * sizeof(TaskEntry));
   L.x16 = take(size_t(s.T) * s.d * 2);
   L.hs16 = take(size_t(L.R) * s.ffn * 2);
-  L.gu_part = take(L.KS > 1 ? size_t(L.KS) * L.R * 2 * s.ffn * 4 : 0);
   L.y = take(size_t(L.R) * s.d * 4);
   L.total = o;
   return L;
@@ -136,6 +154,20 @@ MOE_DEVICE void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16),
+// completing on `bar` through its transaction count.
+MOE_DEVICE void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+MOE_DEVICE void bulk_copy_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
 MOE_DEVICE void prefetch_tmap(const void* tmap) {
@@ -256,6 +288,17 @@ MOE_DEVICE uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   const uint16_t h = static_cast<uint16_t>(two_bytes & 0xFFFFu);
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o) : "h"(h));
   return o;
+}
+// Eight E2M1 codes (one word) to four FP16x2 registers with integer operations: register
+// j holds elements (j, j+4) as the bit patterns of w * 2^-14 (E2M1's exponent and mantissa
+// bits dropped into FP16's exponent LSBs and mantissa MSB; E2M1 exponent 0 lands on FP16
+// subnormals, which is again w * 2^-14).
+MOE_DEVICE void e2m1x8_to_f16x2x4_shift(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2, uint32_t& o3) {
+  const uint32_t kMag = 0x0E000E00u, kSign = 0x80008000u;
+  o0 = ((w << 9) & kMag) | ((w << 12) & kSign);
+  o1 = ((w << 5) & kMag) | ((w << 8) & kSign);
+  o2 = ((w << 1) & kMag) | ((w << 4) & kSign);
+  o3 = ((w >> 3) & kMag) | (w & kSign);
 }
 MOE_DEVICE uint32_t hmul2_bits(uint32_t a, uint32_t b) {
   uint32_t o;

@@ -8,7 +8,7 @@
 namespace moe {
 
 struct PlanArgs {
-  int T, E, k, KS, S_gu, S_dn;
+  int T, E, k, S_gu, S_dn;
   const int32_t* ids;
   const float* weights;
   int* status;
@@ -21,21 +21,21 @@ struct PlanArgs {
   int* route_pos;
   int* pos_tok;
   float* route_w;
+  TaskEntry* tasks;
 };
 
 struct PrepArgs {
-  int T, d, E, S_dn, max_units;
+  int T, d, E;
   const __nv_bfloat16* hidden;
   __half* x16;
   uint32_t* ready;
-  uint32_t* cnt_gu;
-  uint32_t* comb_cnt;
+  uint32_t* ticket;
   int* status;
 };
 
 // Everything the expert kernels read besides the two tensor maps.
 struct ExpertArgs {
-  int T, d, F, E, k, R, KS, S_gu, S_dn, nck_gu, nck_dn;
+  int T, d, F, E, k, R, S_gu, S_dn, nck_gu, nck_dn;
   float w13_ts, w2_ts;
   const uint8_t* w13_codes;
   const uint8_t* w13_scales;
@@ -45,22 +45,25 @@ struct ExpertArgs {
   const int* counts;
   const int* offsets;
   const int* touched;
-  const int* gu_start;
-  const int* dn_start;
   const int* pos_tok;
   const int* route_pos;
   const float* route_w;
+  const TaskEntry* tasks;
   const __half* x16;
   __half* hs16;
-  float* gu_part;
   float* y;
   uint32_t* ready;
-  uint32_t* cnt_gu;
-  uint32_t* comb_cnt;
+  uint32_t* ticket;
   int* status;
   const __nv_bfloat16* residual;
   __nv_bfloat16* out;
+  // optional timeline (diagnostics, off when null): per CTA kTraceRoles x kTracePerRole
+  // uint64 events = event code << 56 | index << 40 | %globaltimer low 40 bits
+  unsigned long long* trace;
 };
+
+constexpr int kTraceRoles = 8;
+constexpr int kTracePerRole = 128;
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* weights,
                               cudaStream_t stream);
@@ -68,9 +71,15 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream);
 cudaError_t launch_expert_tc(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
                              int num_sms, cudaStream_t stream);
+cudaError_t launch_expert_mma(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
+                              int num_sms, cudaStream_t stream);
 cudaError_t launch_expert_simt(const ExpertArgs& a, cudaStream_t stream);
+cudaError_t launch_combine(const ExpertArgs& a, cudaStream_t stream);
 size_t expert_tc_smem_bytes();
-int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows);
+size_t expert_mma_smem_bytes();
+int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes);
+// Shapes the decode (warp-MMA) kernel handles: d, ffn multiples of 256 and at most 2048.
+bool expert_mma_supports(int d, int F);
 // Record a message for moe_last_cuda_error on the calling host thread.
 void set_last_error_message(const char* msg);
 

@@ -11,9 +11,9 @@
 //
 // Plan: one CTA.  Per-expert counts (shared-memory atomics), exclusive scan, the
 // ascending touched-expert list, each route's position in expert-major order, and the
-// per-touched-expert task prefix sums the expert kernel decodes its task ids with
-// ("First implementation boundary", step 1: compact expert-presence list plus the
-// original route positions; no gather of token features).
+// expert kernel's task table (all gate/up tasks, then all down tasks) ("First
+// implementation boundary", step 1: compact expert-presence list plus the original
+// route positions; no gather of token features).
 #include <cfloat>
 
 #include "moe_common.cuh"
@@ -162,13 +162,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
     if (flag) a.touched[rank] = tid;
   }
   if (tid == 0) a.offsets[E] = total;
-  // per touched expert: passes of kRowsPerPass rows, gate/up and down task counts
+  // per touched expert: passes of kRowsPerPass rows; gate/up and down task counts
   const int npass = flag ? (cnt + kRowsPerPass - 1) / kRowsPerPass : 0;
-  const int ngu = npass * a.S_gu * a.KS;
+  const int ngu = npass * a.S_gu;
   const int ndn = npass * a.S_dn;
-  // scatter per-touched values to thread `rank` through shared memory (reuse s_counts)
   __syncthreads();
-  if (flag) s_counts[rank] = (ngu << 0);
+  if (flag) s_counts[rank] = ngu;  // gather per-touched values at index `rank`
   __syncthreads();
   int gu_total = 0;
   const int gu_v = tid < U ? s_counts[tid] : 0;
@@ -187,7 +186,27 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
     a.gu_start[U] = gu_total;
     a.dn_start[U] = dn_total;
   }
-  // largest row count and number of gate/up units (pass, stripe) over touched experts
+  // the task table: all gate/up tasks (touched order, pass, stripe), then all down tasks
+  __syncthreads();
+  if (flag) {
+    s_counts[rank] = tid;  // expert of touched index `rank`
+  }
+  __syncthreads();
+  if (tid < U) {
+    const int e = s_counts[tid];
+    const int m = a.counts[e];
+    const int base = a.offsets[e];
+    const int np = (m + kRowsPerPass - 1) / kRowsPerPass;
+    int gi = gu_start;
+    int di = gu_total + dn_start;
+    for (int p = 0; p < np; ++p) {
+      const int rows = min(kRowsPerPass, m - p * kRowsPerPass);
+      const int row0 = base + p * kRowsPerPass;
+      for (int s2 = 0; s2 < a.S_gu; ++s2) a.tasks[gi++] = TaskEntry{e | (tid << 16), row0, rows, s2};
+      for (int s2 = 0; s2 < a.S_dn; ++s2) a.tasks[di++] = TaskEntry{e | (tid << 16), row0, rows | (1 << 16), s2};
+    }
+  }
+  // largest row count over the experts
   int mx = cnt;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(kFull, mx, o));
@@ -200,7 +219,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
     a.meta[META_NGU] = gu_total;
     a.meta[META_NDN] = dn_total;
     a.meta[META_MAXROWS] = m;
-    a.meta[META_NUNITS] = gu_total / a.KS;
   }
   __syncthreads();
   // route positions in expert-major order

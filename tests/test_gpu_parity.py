@@ -16,7 +16,7 @@ from oracle import oracle as O
 
 pytestmark = pytest.mark.gpu
 
-ALGOS = {"tcgen05": 1, "simt": 2}
+ALGOS = {"auto": 0, "tcgen05": 1, "simt": 2, "mma": 3}
 
 # tokens checked against the oracle at full size (all tokens when None)
 SAMPLES = {
@@ -51,7 +51,13 @@ def _check_layer(cfg, inp, algo, tokens=None, residual=True):
     return assert_parity(out[rows], ref[rows], f"{cfg.name} algo {algo}")
 
 
-@pytest.mark.parametrize("name", ["tiny", "b1", "b8", "b64", "b64_literal", "prefill"])
+@pytest.mark.parametrize("name", ["b1", "b8", "b64", "b64_literal", "prefill"])
+def test_layer_parity_mma(name):
+    cfg = mi.CONFIGS[name]
+    _check_layer(cfg, config_inputs(name), ALGOS["mma"], SAMPLES[name])
+
+
+@pytest.mark.parametrize("name", ["tiny", "b1", "b8", "b64", "prefill"])
 def test_layer_parity_tcgen05(name):
     cfg = mi.CONFIGS[name]
     _check_layer(cfg, config_inputs(name), ALGOS["tcgen05"], SAMPLES[name])
@@ -65,7 +71,7 @@ def test_layer_parity_simt(name):
 
 def test_last_layer_weight_set_parity():
     cfg = mi.CONFIGS["b1"]
-    _check_layer(cfg, mi.gen_layer(cfg, seed=0, layer=11), ALGOS["tcgen05"])
+    _check_layer(cfg, mi.gen_layer(cfg, seed=0, layer=11), ALGOS["auto"])
 
 
 @pytest.mark.parametrize("T,d,F,E,k", [(1, 256, 128, 16, 1), (5, 256, 128, 16, 2), (33, 512, 256, 64, 8),
@@ -74,7 +80,25 @@ def test_last_layer_weight_set_parity():
 def test_ragged_and_edge_shapes(T, d, F, E, k):
     cfg = mi.CONFIGS["tiny"].replace(name=f"edge{T}x{d}x{F}x{E}x{k}", T=T, d=d, ffn=F, E=E, k=k, tag=100 + T)
     inp = mi.gen_layer(cfg, seed=3)
+    _check_layer(cfg, inp, ALGOS["auto"])
     _check_layer(cfg, inp, ALGOS["tcgen05"])
+
+
+@pytest.mark.parametrize("T,d,F,E,k", [(1, 256, 256, 16, 1), (5, 512, 256, 16, 2), (33, 512, 512, 64, 8),
+                                       (100, 256, 256, 32, 4), (7, 1024, 256, 40, 32), (64, 1024, 256, 16, 16),
+                                       (130, 256, 256, 4, 4)])
+def test_mma_path_shapes(T, d, F, E, k):
+    # (130, ..., E=4, k=4): every expert holds all 130 rows -> three 64-row passes
+    cfg = mi.CONFIGS["tiny"].replace(name=f"mma{T}x{d}x{F}x{E}x{k}", T=T, d=d, ffn=F, E=E, k=k, tag=200 + T)
+    inp = mi.gen_layer(cfg, seed=4)
+    _check_layer(cfg, inp, ALGOS["mma"])
+
+
+def test_mma_path_rejects_unsupported_shape():
+    import routed_moe_decode_gb300 as moe
+    cfg = mi.CONFIGS["tiny"]  # ffn = 128 is not a multiple of 256
+    with pytest.raises(moe.MoeError):
+        run_layer(cfg, dict(config_inputs("tiny")), algo=ALGOS["mma"])
 
 
 def _route_only(logits, k):
@@ -155,7 +179,7 @@ def test_zero_hidden_gives_residual_exactly():
     cfg = mi.CONFIGS["b1"]
     inp = dict(config_inputs("b1"))
     inp["hidden"] = np.zeros_like(inp["hidden"])
-    _, _, out, _ = run_layer(cfg, inp, algo=1)
+    _, _, out, _ = run_layer(cfg, inp, algo=0)
     res = (inp["residual"].astype(np.uint32) << 16).view(np.float32)
     np.testing.assert_array_equal(out, res)
 
@@ -163,7 +187,7 @@ def test_zero_hidden_gives_residual_exactly():
 def test_no_residual_and_out_aliasing_residual():
     cfg = mi.CONFIGS["b8"]
     inp = config_inputs("b8")
-    _check_layer(cfg, inp, 1, SAMPLES["b8"], residual=False)
+    _check_layer(cfg, inp, 0, SAMPLES["b8"], residual=False)
     import routed_moe_decode_gb300 as moe
     w = device_weights(inp, "cuda")
     layer = moe.MoeLayer(cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k)
@@ -192,7 +216,7 @@ def test_all_equal_and_all_disjoint_routing(shared, T):
     inp.update(mi.gen_layer(cfg, seed=1, weights=False))
     inp["logits"] = _shared_or_disjoint_logits(T, cfg.E, cfg.k, shared)
     tokens = None if T <= 32 else [0, 1, T // 2, T - 1]
-    _check_layer(cfg, inp, 1, tokens)
+    _check_layer(cfg, inp, 0, tokens)
 
 
 def test_all_experts_identical_output_independent_of_routing():
@@ -200,12 +224,12 @@ def test_all_experts_identical_output_independent_of_routing():
     inp = dict(mi.gen_layer(cfg, seed=2))
     for key in ("w13_codes", "w13_scales", "w2_codes", "w2_scales"):
         inp[key] = np.ascontiguousarray(np.broadcast_to(inp[key][:1], inp[key].shape))
-    _, _, a, _ = run_layer(cfg, inp, algo=1)
+    _, _, a, _ = run_layer(cfg, inp, algo=0)
     inp2 = dict(inp, logits=np.ascontiguousarray(inp["logits"][:, ::-1]))
-    _, _, b, _ = run_layer(cfg, inp2, algo=1)
+    _, _, b, _ = run_layer(cfg, inp2, algo=0)
     mx, mean_rel = parity_metrics(a, b)
     assert mx < 2e-2 and mean_rel < 2e-3
-    _check_layer(cfg, inp, 1)
+    _check_layer(cfg, inp, 0)
 
 
 def test_repeat_is_bitwise_deterministic_and_forward_reuses_plan():
@@ -269,6 +293,6 @@ def test_hidden_out_of_fp16_range_sets_status():
     hid = inp["hidden"].copy()
     hid[1, 3] = 0x4780  # bf16 65536.0, above the FP16 maximum
     inp["hidden"] = hid
-    _, _, _, layer = run_layer(cfg, inp, algo=1)
+    _, _, _, layer = run_layer(cfg, inp, algo=0)
     import routed_moe_decode_gb300 as moe
     assert layer.status() & moe.MOE_DEV_HIDDEN_RANGE
