@@ -89,7 +89,7 @@ typedef struct moe_shape {
 
 /* Expert-kernel selection for moe_forward_algo. */
 typedef enum moe_algo {
-  MOE_ALGO_AUTO = 0,     /* MOE_ALGO_MMA where it applies (d and ffn multiples of 256, at most
+  MOE_ALGO_AUTO = 0,     /* MOE_ALGO_MMA where it applies (d and ffn powers of two from 256 to
                             2048), MOE_ALGO_TCGEN05 otherwise */
   MOE_ALGO_TCGEN05 = 1,  /* persistent stripe kernel: TMA weight stream, in-register NVFP4
                             dequantisation into tensor memory, tcgen05 MMA (FP32 accumulate),
@@ -99,8 +99,8 @@ typedef enum moe_algo {
                             dequantisation into the A fragments of warp-level m16n8k16 tensor-core
                             MMAs (weights stationary, routed rows as the 8-wide operand, FP32
                             accumulate), gate and up of one F index in one warp, readiness
-                            counters between gate/up and down; needs d and ffn multiples of 256
-                            and at most 2048 (MOE_ERR_UNSUPPORTED otherwise) */
+                            counters between gate/up and down; needs d and ffn powers of two from
+                            256 to 2048 (MOE_ERR_UNSUPPORTED otherwise) */
 } moe_algo;
 
 /* Human-readable name of a status code (static string, never NULL). */

@@ -20,12 +20,10 @@ extern "C" {
 /* NVFP4 decode as used by the dequantisation warps.
  *   words     [n] uint32: eight E2M1 codes each (element 2i in the low nibble of byte i)
  *   out       [4n] uint32: hardware conversion, f16x2 out[4w + b] = (element 2b, element 2b+1)
- *   out_shift [4n] uint32: integer construction, f16x2 out_shift[4w + j] = (element j,
- *             element j+4) of word w, each half the FP16 pattern of value * 2^-14
  *   pairs     [m] uint32: two E4M3 bytes in the low 16 bits (low byte -> low half)
  *   sout      [m] uint32: f16x2 of the two scale values */
-MOE_API int moe_selftest_decode(const uint32_t* words, int n, uint32_t* out, uint32_t* out_shift,
-                                const uint32_t* pairs, int m, uint32_t* sout, moe_stream_t stream);
+MOE_API int moe_selftest_decode(const uint32_t* words, int n, uint32_t* out, const uint32_t* pairs, int m,
+                                uint32_t* sout, moe_stream_t stream);
 
 /* One TMA load of a 64-byte x 64-row box of a [rows, row_bytes] uint8 matrix at byte
  * column x (a multiple of 16) and row y, with the 64-byte swizzle the expert kernel

@@ -4,24 +4,30 @@
 // its fixed per-instruction time (~94 ns whatever N <= 128, measured on GB300), so a
 // 128x16 FP16 A tile per instruction cannot keep up with the weight stream.  Here the
 // dequantised weights stay in registers as the 16-row A fragment of mma.sync m16n8k16 and
-// the routed rows are its 8-column B operand: one weight fragment serves every row, and
-// the warp MMA sustains several times the per-SM HBM share of weights (the multi-row
-// weight-stationary GEMV described in the b12x tensor-core GEMV notes of the pages).
+// the routed rows are its 8-column B operand: one weight fragment serves every row (the
+// multi-row weight-stationary GEMV described in the b12x tensor-core GEMV notes of the
+// pages).
 //
 // Structure (one resident CTA per SM, tasks from the plan's task table via tickets):
-//   warp 0      task fetcher + weight producer: per task one bulk copy of the task's block
-//               scales (its rows are contiguous), then per 256-K chunk two TMA tiles of E2M1
-//               codes (64 rows x 128 B each, 128-byte swizzle) into a ring;
+//   warp 0      task fetcher + weight producer: per task one TMA tile of the task's block
+//               scales (swizzled like the codes), then per 256-K chunk two TMA tiles of
+//               E2M1 codes (64 rows x 128 B each, 128-byte swizzle) into a ring;
 //   warp 1      activation producer: per chunk and 8-row tile, one bulk copy per routed row
 //               (512 B of FP16 hidden for gate/up, of h for down) into a padded tile;
-//   warps 2-9   compute: each owns 16 weight rows of the 128-row tile.  Gate/up tasks give
-//               warp w gate rows 8w..8w+7 as fragment rows 0-7 and the up rows of the same
-//               F indices as fragment rows 8-15, so h = silu(g) * u is formed in registers.
+//   warp 2      publisher: after the compute warps have written a gate/up task's h rows it
+//               releases them to other CTAs (one fence and one reduction per task), so the
+//               compute warps never wait on the fence;
+//   warps 3-10  compute: each owns 16 weight rows of the 128-row tile.  Gate/up tasks give
+//               warp w gate rows of one 8-row group as fragment rows 0-7 and the up rows of
+//               the same F indices as fragment rows 8-15, so h = silu(g) * u is formed in
+//               registers.
+// Fragment row g holds tile row 8w + frag_row(g): the permutation puts the two rows that
+// one 8-lane shared-memory phase reads on different halves of the 128-byte swizzle, so the
+// code and scale reads are free of bank conflicts.
 // Each thread dequantises 2 rows x 64 elements per chunk (exact FP16: E2M1 x E4M3 has at
 // most 6 significant bits), feeds 16 MMAs per 8-row tile with FP32 accumulation, and
-// writes h (FP16) or per-route down outputs (FP32) at the end of the task.  Gate/up warps
-// publish readiness per expert; down tasks' activation loads wait for it.  Only the bulk
-// copy engine writes shared memory, so the consumers need no proxy fences.
+// writes h (FP16) or per-route down outputs (FP32) at the end of the task.  Only the TMA
+// and bulk-copy engines write shared memory, so the consumers need no proxy fences.
 #include "moe_kernels.cuh"
 
 namespace moe {
@@ -38,9 +44,13 @@ constexpr int kRowPitchB = 2 * kChunk + 16;     // padded FP16 row of one chunk 
 constexpr int kStageB = kTileRows * kRowPitchB;  // 4224
 constexpr int kMaxTiles = kRowsPerPass / kTileRows;  // 8
 constexpr int kComputeWarps = 8;
-constexpr int kThreads = 32 * (2 + kComputeWarps);
+constexpr int kFirstCompute = 3;
+constexpr int kThreads = 32 * (kFirstCompute + kComputeWarps);
 constexpr int kTaskSlots = 8;
-constexpr int kTaskConsumers = 1 + kComputeWarps;
+constexpr int kTaskConsumers = 2 + kComputeWarps;  // activation producer, publisher, compute
+// Compute warps run at most kTaskSlots tasks ahead of the publisher (it frees each task
+// slot before waiting on that task), so twice as many publication slots never wrap early.
+constexpr int kPubSlots = 2 * kTaskSlots;
 constexpr long long kTimeoutCycles = 1ll << 33;
 
 struct Smem {
@@ -56,6 +66,7 @@ struct Smem {
   uint64_t sc_empty[2];
   uint64_t task_full[kTaskSlots];
   uint64_t task_empty[kTaskSlots];
+  uint64_t pub_full[kPubSlots];
   int abort_flag;
 };
 
@@ -88,6 +99,17 @@ __device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* 
   return true;
 }
 
+// Tile row (0..7 within an 8-row group) held by fragment row g: 0, 4, 1, 5, 2, 6, 3, 7.
+__device__ __forceinline__ int frag_row(int g) { return ((g & 1) << 2) | (g >> 1); }
+
+// Offset in a scale slot of the 16-byte piece c of tile row r, for rows of P = 16, 32, 64 or
+// 128 bytes written by a TMA load with the matching swizzle (none, 32, 64 or 128 bytes: the
+// piece index is XORed with address bits 7 and up).
+__device__ __forceinline__ uint32_t scale_piece(int r, int P, int c) {
+  const int rowoff = r * P;
+  return static_cast<uint32_t>(rowoff + ((c ^ ((rowoff >> 7) & ((P >> 4) - 1))) << 4));
+}
+
 // D += A * B for one m16n8k16 step (FP16 inputs, FP32 accumulators).
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
@@ -98,24 +120,52 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// B fragments of one 8-row activation tile for sub-chunk h: tile row g, elements
+// [128h + 32q, +32) as four 16-byte pieces (piece j feeds k-steps (h, j, 0) and (h, j, 1)).
+// Rows past the task's routed rows were not copied and enter as zeros.
+__device__ __forceinline__ void load_b_frag(const uint8_t* tile, int g, int q, int h, bool live, uint4 (&x)[4]) {
+  const uint8_t* row = tile + g * kRowPitchB + 64 * q + 256 * h;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) x[j] = live ? *reinterpret_cast<const uint4*>(row + 16 * j) : make_uint4(0, 0, 0, 0);
+}
+
+// One thread's share of a 256-K chunk: per sub-chunk h the 16 code bytes and the two block
+// scales of its rows a (fragment row g) and b (fragment row g + 8).
+struct ChunkCodes {
+  uint4 ca[2], cb[2];
+  uint32_t sa[2], sb[2];
+};
+
+// codes: sub-chunk h covers K [128h, 128h+128); thread q its elements [32q, 32q+32), i.e.
+// 16-byte piece 4h + q of the 128-byte row, stored at (piece ^ (row & 7)); scales: blocks
+// 16c + 8h + 2q and the next one, i.e. bytes 8h + 2q of the row's 16-byte piece c.
+__device__ __forceinline__ void load_chunk_codes(const uint8_t* stage, const uint8_t* sbase, int lra, int lrb, int P,
+                                                 int c, int q, ChunkCodes& o) {
+  const int ra = lra & 63, rb = lrb & 63;
+  const uint8_t* pa = stage + (lra >> 6) * (kStageA / 2) + ra * 128;
+  const uint8_t* pb = stage + (lrb >> 6) * (kStageA / 2) + rb * 128;
+  const uint8_t* qa = sbase + scale_piece(lra, P, c) + 2 * q;
+  const uint8_t* qb = sbase + scale_piece(lrb, P, c) + 2 * q;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    o.ca[h] = *reinterpret_cast<const uint4*>(pa + (((4 * h + q) ^ (ra & 7)) << 4));
+    o.cb[h] = *reinterpret_cast<const uint4*>(pb + (((4 * h + q) ^ (rb & 7)) << 4));
+    o.sa[h] = *reinterpret_cast<const uint16_t*>(qa + 8 * h);
+    o.sb[h] = *reinterpret_cast<const uint16_t*>(qb + 8 * h);
+  }
+}
+
 // Dequantise 32 elements (16 bytes of codes, two 16-element scale blocks) of one row into
-// 16 FP16x2 registers in fragment order: register 4j + i belongs to word j; see kCvtWords
-// for the pairing of each word kind.
+// 16 FP16x2 registers in fragment order: register 4j + i holds elements (8j + 2i, 8j + 2i + 1).
 __device__ __forceinline__ void dequant32(const uint4 codes, uint32_t scale_pair_bytes, uint32_t (&o)[16]) {
   const uint32_t s2 = e4m3x2_to_f16x2(scale_pair_bytes);  // (block 0, block 1)
   const uint32_t sb0 = bcast_lo_half(s2), sb1 = bcast_hi_half(s2);
   const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const uint32_t sraw = j < 2 ? sb0 : sb1;
-    uint32_t r0, r1, r2, r3, scale;
-    if (j < kCvtWords) {
-      e2m1x8_to_f16x2x4(w[j], r0, r1, r2, r3);
-      scale = hmul2_bits(sraw, 0x20002000u);  // x 2^-7
-    } else {
-      e2m1x8_to_f16x2x4_shift(w[j], r0, r1, r2, r3);
-      scale = hmul2_bits(sraw, 0x58005800u);  // x 2^7
-    }
+    const uint32_t scale = j < 2 ? sb0 : sb1;
+    uint32_t r0, r1, r2, r3;
+    e2m1x8_to_f16x2x4(w[j], r0, r1, r2, r3);
     o[4 * j + 0] = hmul2_bits(r0, scale);
     o[4 * j + 1] = hmul2_bits(r1, scale);
     o[4 * j + 2] = hmul2_bits(r2, scale);
@@ -151,6 +201,7 @@ using namespace mk;
 
 __global__ void __launch_bounds__(kThreads, 1)
     expert_mma_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_w2,
+                      const __grid_constant__ CUtensorMap tm_s13, const __grid_constant__ CUtensorMap tm_s2,
                       const __grid_constant__ ExpertArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -173,16 +224,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&sm.task_full[i]), 1);
       mbar_init(smem_addr(&sm.task_empty[i]), kTaskConsumers);
     }
+    for (int i = 0; i < kPubSlots; ++i) mbar_init(smem_addr(&sm.pub_full[i]), kComputeWarps);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_w13);
     prefetch_tmap(&tm_w2);
+    prefetch_tmap(&tm_s13);
+    prefetch_tmap(&tm_s2);
   }
   __syncthreads();
   const uint32_t ringa0 = smem_addr(&sm.ring_a[0][0]);
   const uint32_t ringb0 = smem_addr(&sm.ring_b[0][0]);
+  const int P13 = a.d / 16, P2 = a.F / 16;  // scale bytes per row of w13 / w2
   int tcnt = 0;
   if (tid == 0) trace_ev(a, 5, tcnt, 10, 0);
 
@@ -235,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tm = &tm_w2;
         nck = a.F / kChunk;
       }
-      // block scales of the task's 128 rows: contiguous per 64-row half
+      // block scales of the task's 128 rows (gate/up: two 64-row boxes; down: one box)
       const int sn = n & 1;
       if (!warp_wait(smem_addr(&sm.sc_empty[sn]), static_cast<uint32_t>(((n >> 1) & 1) ^ 1), sm, a.status)) {
         ok = false;
@@ -245,14 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sbar = smem_addr(&sm.sc_full[sn]);
         const uint32_t sdst = smem_addr(&sm.scales[sn][0]);
         if (!is_dn) {
-          const uint32_t half_bytes = 64u * static_cast<uint32_t>(a.d / 16);
-          mbar_arrive_expect_tx(sbar, 2 * half_bytes);
-          bulk_copy_g2s(sdst, a.w13_scales + static_cast<size_t>(rA0) * (a.d / 16), half_bytes, sbar);
-          bulk_copy_g2s(sdst + half_bytes, a.w13_scales + static_cast<size_t>(rA1) * (a.d / 16), half_bytes, sbar);
+          mbar_arrive_expect_tx(sbar, 128u * static_cast<uint32_t>(P13));
+          tma_load_2d(sdst, &tm_s13, 0, rA0, sbar, pol);
+          tma_load_2d(sdst + 64u * static_cast<uint32_t>(P13), &tm_s13, 0, rA1, sbar, pol);
         } else {
-          const uint32_t bytes = 128u * static_cast<uint32_t>(a.F / 16);
-          mbar_arrive_expect_tx(sbar, bytes);
-          bulk_copy_g2s(sdst, a.w2_scales + static_cast<size_t>(rA0) * (a.F / 16), bytes, sbar);
+          mbar_arrive_expect_tx(sbar, 128u * static_cast<uint32_t>(P2));
+          tma_load_2d(sdst, &tm_s2, 0, rA0, sbar, pol);
         }
       }
       ++n;
@@ -294,8 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------- activation producer: 8-row tiles, one bulk copy per routed row -------------
-    const uint64_t pol_keep = 0;
-    (void)pol_keep;
     int stage = 0, n = 0, issued = 0, chunk_seq = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -306,25 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = te.x & 0xffff, u = (te.x >> 16) & 0xffff, row0 = te.y, rows = te.z & 0xffff;
       const bool is_dn = ((te.z >> 16) & 1) != 0;
       if (is_dn) {
-        // every gate/up warp of every stripe (all passes) of this expert must have published
+        // every gate/up task of every stripe (all passes) of this expert must have published
         const int npass = (__ldg(a.counts + e) + kRowsPerPass - 1) / kRowsPerPass;
-        const uint32_t target = static_cast<uint32_t>(npass * a.S_gu * kComputeWarps);
-        int good = 1;
-        if (lane == 0) {
-          const long long t0 = clock64();
-          while (ld_acquire_u32(a.ready + u) < target) {
-            if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) { good = 0; break; }
-            if (clock64() - t0 > kTimeoutCycles) {
-              *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
-              atomicOr(a.status, static_cast<int>(MOE_DEV_TIMEOUT));
-              good = 0;
-              break;
-            }
-            __nanosleep(32);
-          }
-          trace_ev(a, 1, tcnt, 3, n);
-        }
-        if (!__shfl_sync(0xffffffffu, good, 0)) break;
+        const uint32_t target = static_cast<uint32_t>(npass * a.S_gu);
+        const bool good = warp_wait_counter(a.ready + u, target, &sm.abort_flag, a.status, kTimeoutCycles);
+        if (lane == 0) trace_ev(a, 1, tcnt, 3, n);
+        if (!good) break;
       }
       const int nck = is_dn ? a.F / kChunk : a.d / kChunk;
       // lane l owns routed rows l and l + 32 of the pass
@@ -373,122 +411,174 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (!mbar_try_wait(smem_addr(&sm.full_b[st]), ph) && clock64() - t0 < kTimeoutCycles) {}
       }
     }
+  } else if (warp == 2) {
+    // ------------- publisher: release each finished gate/up task's h rows -------------
+    int n = 0, gu_n = 0;
+    while (true) {
+      TaskEntry te;
+      if (!take_task(sm, n++, te, a.status)) break;
+      if (te.x < 0) break;
+      if ((te.z >> 16) & 1) continue;  // down task: nothing to publish
+      const int u = (te.x >> 16) & 0xffff;
+      const int slot = gu_n % kPubSlots;
+      const uint32_t ph = static_cast<uint32_t>((gu_n / kPubSlots) & 1);
+      ++gu_n;
+      // the compute warps' h stores are ordered before their arrivals (warp barrier, then a
+      // release arrive); this acquire wait plus a GPU-scope fence makes the reduction below
+      // release all of them
+      if (!warp_wait(smem_addr(&sm.pub_full[slot]), ph, sm, a.status)) break;
+      if (lane == 0) {
+        fence_acq_rel_gpu();
+        red_add_relaxed_gpu_u32(a.ready + u, 1u);
+        trace_ev(a, 4, tcnt, 9, gu_n);
+      }
+      __syncwarp();
+    }
   } else {
     // ------------- compute warps: dequantise into A fragments, mma.sync, epilogue -------------
-    const int cw = warp - 2;  // 0..7
+    const int cw = warp - kFirstCompute;  // 0..7
     const int g = lane >> 2, q = lane & 3;
-    int stage_a = 0, stage_b = 0, n = 0, chunk_seq = 0;
+    const int fr = frag_row(g);
+    int tcnt3 = 0, tcnt6 = 0;
+    int stage_a = 0, stage_b = 0, n = 0, gu_n = 0, chunk_seq = 0;
     uint32_t phase_a = 0, phase_b = 0;
     bool ok = true;
     while (ok) {
       TaskEntry te;
       if (!take_task(sm, n, te, a.status)) break;
       if (te.x < 0) break;
-      const int u = (te.x >> 16) & 0xffff, row0 = te.y, rows = te.z & 0xffff, s = te.w;
+      const int row0 = te.y, rows = te.z & 0xffff, s = te.w;
       const bool is_dn = ((te.z >> 16) & 1) != 0;
       const int K = is_dn ? a.F : a.d;
+      const int P = is_dn ? P2 : P13;
       const int nck = K / kChunk;
       const int nt = (rows + kTileRows - 1) / kTileRows;
-      // local rows (0..127 of the A tile) of fragment rows g and g + 8
-      const int lra = is_dn ? 16 * cw + g : 8 * cw + g;
-      const int lrb = is_dn ? 16 * cw + g + 8 : 64 + 8 * cw + g;
+      // tile rows (0..127) of fragment rows g and g + 8
+      const int lra = is_dn ? 16 * cw + fr : 8 * cw + fr;
+      const int lrb = is_dn ? 16 * cw + 8 + fr : 64 + 8 * cw + fr;
       const int sn = n & 1;
       if (!warp_wait(smem_addr(&sm.sc_full[sn]), static_cast<uint32_t>((n >> 1) & 1), sm, a.status)) break;
-      const uint8_t* srow_a = &sm.scales[sn][0] + lra * (K / 16) + 2 * q;
-      const uint8_t* srow_b = &sm.scales[sn][0] + lrb * (K / 16) + 2 * q;
+      const uint8_t* sbase = &sm.scales[sn][0];
       float acc[kMaxTiles][4];
 #pragma unroll
       for (int t = 0; t < kMaxTiles; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+      // codes and scales of chunk c are loaded into registers during chunk c - 1, so their
+      // shared-memory latency overlaps the previous chunk's MMAs
+      ChunkCodes next;
+      if (!warp_wait(smem_addr(&sm.full_a[stage_a]), phase_a, sm, a.status)) break;
+      load_chunk_codes(&sm.ring_a[stage_a][0], sbase, lra, lrb, P, 0, q, next);
       for (int c = 0; c < nck; ++c) {
-        if (!warp_wait(smem_addr(&sm.full_a[stage_a]), phase_a, sm, a.status)) { ok = false; break; }
         if (cw == 0 && lane == 0) trace_ev(a, 2, tcnt, 5, chunk_seq);
-        // codes: sub-chunk h covers K [128h, 128h+128); thread q its elements [32q, 32q+32),
-        // i.e. 16-byte chunk 4h + q of the 128-byte row, stored at (chunk ^ (row & 7))
-        const uint8_t* st = &sm.ring_a[stage_a][0];
-        const int ha = lra >> 6, ra = lra & 63, hb = lrb >> 6, rb = lrb & 63;
-        const uint8_t* pa = st + ha * (kStageA / 2) + ra * 128;
-        const uint8_t* pb = st + hb * (kStageA / 2) + rb * 128;
-        uint4 ca[2], cb[2];
-        uint32_t sa[2], sbv[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          ca[h] = *reinterpret_cast<const uint4*>(pa + (((4 * h + q) ^ (ra & 7)) << 4));
-          cb[h] = *reinterpret_cast<const uint4*>(pb + (((4 * h + q) ^ (rb & 7)) << 4));
-          sa[h] = *reinterpret_cast<const uint16_t*>(srow_a + 16 * c + 8 * h);
-          sbv[h] = *reinterpret_cast<const uint16_t*>(srow_b + 16 * c + 8 * h);
-        }
+        const ChunkCodes cur = next;
+        // the stage's bytes are in registers: hand it back to the producer
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.empty_a[stage_a]));
         if (++stage_a == kStagesA) { stage_a = 0; phase_a ^= 1u; }
-        uint32_t fa[2][16], fb[2][16];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          dequant32(ca[h], sa[h], fa[h]);
-          dequant32(cb[h], sbv[h], fb[h]);
+        if (c + 1 < nck) {
+          if (!warp_wait(smem_addr(&sm.full_a[stage_a]), phase_a, sm, a.status)) { ok = false; break; }
+          load_chunk_codes(&sm.ring_a[stage_a][0], sbase, lra, lrb, P, c + 1, q, next);
         }
-        // The 16 k-steps of a chunk go to independent accumulator sets where tiles leave
-        // registers free (8 sets for one 8-row tile, 4 per tile for two), so consecutive MMAs
-        // do not wait on each other; the sets are summed at the end of the task.
+        // the chunk's activation tiles (the producer runs ahead, so they are normally there)
+        {
+          int sbt = stage_b;
+          uint32_t pbt = phase_b;
+          for (int t = 0; t < nt; ++t) {
+            if (!warp_wait(smem_addr(&sm.full_b[sbt]), pbt, sm, a.status)) { ok = false; break; }
+            if (++sbt == kStagesB) { sbt = 0; pbt ^= 1u; }
+          }
+          if (!ok) break;
+        }
+        if (cw == 0 && lane == 0) trace_ev(a, 6, tcnt6, 13, chunk_seq);
+        // Per sub-chunk h: activation fragments first (their latency overlaps the
+        // dequantisation), then the 32 weights per row of this thread, then the MMAs.
+        // MMA k-step (h, j, x): A registers 4j + 2x, 4j + 2x + 1, B word pair x of piece j.
+        // Few tiles leave accumulator registers free: their k-steps are spread over
+        // independent accumulators (8 for one tile, 4 per tile for two) so that consecutive
+        // MMAs do not wait on each other; the sets are summed after the task.
+        const uint8_t* b0 = &sm.ring_b[stage_b][0];
+        if (nt == 1) {
+          const bool live = g < rows;
 #pragma unroll
-        for (int t = 0; t < kMaxTiles; ++t) {
-          if (t < nt) {
-            if (!warp_wait(smem_addr(&sm.full_b[stage_b]), phase_b, sm, a.status)) { ok = false; break; }
-            // tile row g, elements [128h + 32q, +32) in four 16-byte pieces
-            const uint8_t* brow = &sm.ring_b[stage_b][0] + g * kRowPitchB + 64 * q;
-            uint4 xb[2][4];
+          for (int h = 0; h < 2; ++h) {
+            uint4 xb[4];
+            load_b_frag(b0, g, q, h, live, xb);
+            uint32_t fa[16], fb[16];
+            dequant32(cur.ca[h], cur.sa[h], fa);
+            dequant32(cur.cb[h], cur.sb[h], fb);
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+            for (int j = 0; j < 4; ++j) {
+              mma_16816(acc[2 * j], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], xb[j].x, xb[j].y);
+              mma_16816(acc[2 * j + 1], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], xb[j].z,
+                        xb[j].w);
+            }
+          }
+        } else if (nt == 2) {
+          const uint8_t* b1 = &sm.ring_b[stage_b + 1 == kStagesB ? 0 : stage_b + 1][0];
+          const bool live0 = g < rows, live1 = g < rows - kTileRows;
 #pragma unroll
-              for (int jp = 0; jp < 4; ++jp) xb[h][jp] = *reinterpret_cast<const uint4*>(brow + 256 * h + 16 * jp);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&sm.empty_b[stage_b]));
-            if (++stage_b == kStagesB) { stage_b = 0; phase_b ^= 1u; }
-            if (nt == 1) {
+          for (int h = 0; h < 2; ++h) {
+            uint4 x0[4], x1[4];
+            load_b_frag(b0, g, q, h, live0, x0);
+            load_b_frag(b1, g, q, h, live1, x1);
+            uint32_t fa[16], fb[16];
+            dequant32(cur.ca[h], cur.sa[h], fa);
+            dequant32(cur.cb[h], cur.sb[h], fb);
 #pragma unroll
-              for (int h = 0; h < 2; ++h)
+            for (int j = 0; j < 4; ++j) {
+              const int ch = (2 * j) & 3;
+              mma_16816(acc[ch], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], x0[j].x, x0[j].y);
+              mma_16816(acc[4 + ch], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], x1[j].x, x1[j].y);
+              mma_16816(acc[ch + 1], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], x0[j].z, x0[j].w);
+              mma_16816(acc[5 + ch], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], x1[j].z, x1[j].w);
+            }
+          }
+        } else {
+          // tiles in pairs, the two accumulators interleaved (the second of an odd last pair
+          // multiplies zeros into an accumulator that is never stored)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t fa[16], fb[16];
+            dequant32(cur.ca[h], cur.sa[h], fa);
+            dequant32(cur.cb[h], cur.sb[h], fb);
+#pragma unroll
+            for (int tp = 0; tp < kMaxTiles / 2; ++tp) {
+              if (2 * tp < nt) {
+                const int t0 = 2 * tp, t1 = 2 * tp + 1;
+                const uint8_t* s0 = &sm.ring_b[(stage_b + t0) % kStagesB][0];
+                const uint8_t* s1 = &sm.ring_b[(stage_b + t1) % kStagesB][0];
+                const bool live0 = g < rows - t0 * kTileRows;
+                const bool live1 = t1 < nt && g < rows - t1 * kTileRows;
+                uint4 x0[4], x1[4];
+                load_b_frag(s0, g, q, h, live0, x0);
+                load_b_frag(s1, g, q, h, live1, x1);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                  // word j covers k-steps 2j (registers 4j, 4j+1) and 2j+1 (4j+2, 4j+3)
-                  mma_16816(acc[(4 * h + j) & 7], fa[h][4 * j + 0], fb[h][4 * j + 0], fa[h][4 * j + 1],
-                            fb[h][4 * j + 1], xb[h][j].x, xb[h][j].y);
-                  mma_16816(acc[(4 * h + j + 4) & 7], fa[h][4 * j + 2], fb[h][4 * j + 2], fa[h][4 * j + 3],
-                            fb[h][4 * j + 3], xb[h][j].z, xb[h][j].w);
+                  mma_16816(acc[t0], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], x0[j].x, x0[j].y);
+                  mma_16816(acc[t1], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], x1[j].x, x1[j].y);
+                  mma_16816(acc[t0], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], x0[j].z, x0[j].w);
+                  mma_16816(acc[t1], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], x1[j].z, x1[j].w);
                 }
-            } else if (nt == 2) {
-              if (t < 2) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    mma_16816(acc[4 * t + ((2 * h + j) & 3)], fa[h][4 * j + 0], fb[h][4 * j + 0], fa[h][4 * j + 1],
-                              fb[h][4 * j + 1], xb[h][j].x, xb[h][j].y);
-                    mma_16816(acc[4 * t + ((2 * h + j + 2) & 3)], fa[h][4 * j + 2], fb[h][4 * j + 2],
-                              fa[h][4 * j + 3], fb[h][4 * j + 3], xb[h][j].z, xb[h][j].w);
-                  }
               }
-            } else {
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  mma_16816(acc[t], fa[h][4 * j + 0], fb[h][4 * j + 0], fa[h][4 * j + 1], fb[h][4 * j + 1],
-                            xb[h][j].x, xb[h][j].y);
-                  mma_16816(acc[t], fa[h][4 * j + 2], fb[h][4 * j + 2], fa[h][4 * j + 3], fb[h][4 * j + 3],
-                            xb[h][j].z, xb[h][j].w);
-                }
             }
           }
         }
-        if (!ok) break;
+        if (cw == 0 && lane == 0) trace_ev(a, 3, tcnt3, 12, chunk_seq);
+        // the chunk's activation tiles are consumed
+        __syncwarp();
+        if (lane == 0) {
+          int sbt = stage_b;
+          for (int t = 0; t < nt; ++t) {
+            mbar_arrive(smem_addr(&sm.empty_b[sbt]));
+            if (++sbt == kStagesB) sbt = 0;
+          }
+        }
+        stage_b += nt;
+        if (stage_b >= kStagesB) { stage_b -= kStagesB; phase_b ^= 1u; }
         if (cw == 0 && lane == 0) trace_ev(a, 2, tcnt, 6, chunk_seq);
         ++chunk_seq;
       }
       if (!ok) break;
-      // the task's scales are no longer needed
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&sm.sc_empty[sn]));
-      ++n;
-      // fold the independent accumulator sets into one set per tile
+      // fold the independent accumulator sets into one per tile
       if (nt == 1) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -501,10 +591,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[1][i] = (acc[4][i] + acc[5][i]) + (acc[6][i] + acc[7][i]);
         }
       }
-      // ---- epilogue: rows g / g+8, routed rows 8t + 2q, 8t + 2q + 1 ----
+      if (!ok) break;
+      // the task's scales are no longer needed
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&sm.sc_empty[sn]));
+      ++n;
+      // ---- epilogue: fragment rows g / g+8, routed rows 8t + 2q, 8t + 2q + 1 ----
       if (!is_dn) {
-        const int nidx = act_pos(s * kGuRows + 8 * cw + g);  // storage position of element n
-        const float sc = a.w13_ts * kAccUnscale;
+        const int nidx = s * kGuRows + 8 * cw + fr;  // element n of h
+        const float sc = a.w13_ts;
 #pragma unroll
         for (int t = 0; t < kMaxTiles; ++t) {
           if (t < nt) {
@@ -517,11 +612,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        __threadfence();
+        // hand the task to the publisher
         __syncwarp();
-        if (lane == 0) atom_add_acqrel_u32(a.ready + u, 1u);
+        if (lane == 0) mbar_arrive(smem_addr(&sm.pub_full[gu_n % kPubSlots]));
+        ++gu_n;
       } else {
-        const float sc = a.w2_ts * kHUnscale * kAccUnscale;
+        const float sc = a.w2_ts * kHUnscale;
         const int ra = s * kDnRows + lra, rb = s * kDnRows + lrb;
 #pragma unroll
         for (int t = 0; t < kMaxTiles; ++t) {
@@ -538,7 +634,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (cw == 0 && lane == 0) trace_ev(a, 4, tcnt, 9, n);
     }
   }
   __syncthreads();
@@ -551,16 +646,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t expert_mma_smem_bytes() { return sizeof(Smem) + 1024; }
 
 bool expert_mma_supports(int d, int F) {
-  return d % kChunk == 0 && F % kChunk == 0 && d / 16 <= kScaleSlot / 128 && F / 16 <= kScaleSlot / 128;
+  const auto pow2_in_range = [](int v) { return v >= kChunk && v <= 2048 && (v & (v - 1)) == 0; };
+  return pow2_in_range(d) && pow2_in_range(F);
 }
 
 cudaError_t launch_expert_mma(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
-                              int num_sms, cudaStream_t stream) {
+                              const CUtensorMap& tm_s13, const CUtensorMap& tm_s2, int num_sms,
+                              cudaStream_t stream) {
   const size_t smem = expert_mma_smem_bytes();
   cudaError_t err = cudaFuncSetAttribute(expert_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  expert_mma_kernel<<<num_sms, kThreads, smem, stream>>>(tm_w13, tm_w2, a);
+  expert_mma_kernel<<<num_sms, kThreads, smem, stream>>>(tm_w13, tm_w2, tm_s13, tm_s2, a);
   return cudaGetLastError();
 }
 

@@ -49,9 +49,6 @@ __device__ void row_dot(const uint8_t* codes, const uint8_t* scales, int K, cons
     float wv[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) wv[q] = lut[(w >> (4 * q)) & 15u] * s;
-    // activation storage of this 8-element group: natural order, or the dequantisation's
-    // pairing (position p holds element perm_elem(p)) for groups of the shift kind
-    const bool perm = shift_group(k0);
 #pragma unroll
     for (int j = 0; j < kTok; ++j) {
       if (j < nrows) {
@@ -61,8 +58,8 @@ __device__ void row_dot(const uint8_t* codes, const uint8_t* scales, int K, cons
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float2 f = __half22float2(xh[q]);
-          a = fmaf(perm ? wv[perm_elem(2 * q)] : wv[2 * q], f.x, a);
-          a = fmaf(perm ? wv[perm_elem(2 * q + 1)] : wv[2 * q + 1], f.y, a);
+          a = fmaf(wv[2 * q], f.x, a);
+          a = fmaf(wv[2 * q + 1], f.y, a);
         }
         acc[j] = a;
       }
@@ -107,7 +104,7 @@ __global__ void __launch_bounds__(256) simt_gateup_kernel(ExpertArgs a) {
           atomicOr(a.status, static_cast<int>(MOE_DEV_H_SATURATED));
           h = copysignf(65504.f, h);
         }
-        a.hs16[static_cast<size_t>(off + r0 + lane) * a.F + act_pos(n)] = __float2half_rn(h);
+        a.hs16[static_cast<size_t>(off + r0 + lane) * a.F + n] = __float2half_rn(h);
       }
     }
   }

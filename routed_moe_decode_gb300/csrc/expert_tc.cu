@@ -315,22 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every gate/up stripe of this expert (all passes) must have published its h rows
         const int npass = (__ldg(a.counts + tk.e) + kRowsPerPass - 1) / kRowsPerPass;
         const uint32_t target = static_cast<uint32_t>(npass * a.S_gu);
-        int good = 1;
-        if (lane == 0) {
-          const long long t0 = clock64();
-          while (ld_acquire_u32(a.ready + tk.u) < target) {
-            if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) { good = 0; break; }
-            if (clock64() - t0 > kTimeoutCycles) {
-              *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
-              atomicOr(a.status, static_cast<int>(MOE_DEV_TIMEOUT));
-              good = 0;
-              break;
-            }
-            __nanosleep(32);
-          }
-          trace_ev(a, 1, tcnt, 3, n);
-        }
-        if (!__shfl_sync(0xffffffffu, good, 0)) break;
+        const bool good = warp_wait_counter(a.ready + tk.u, target, &sm.abort_flag, a.status, kTimeoutCycles);
+        if (lane == 0) trace_ev(a, 1, tcnt, 3, n);
+        if (!good) break;
       }
       // source row of each routed row of this pass: lanes hold rows lane and lane + 32
       const __half* src0 = nullptr;
@@ -398,8 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 4; ++j) q[j] = *reinterpret_cast<const uint4*>(crow + ((j ^ ((r >> 1) & 3)) << 4));
         const uint2 sc = *reinterpret_cast<const uint2*>(st + kOffScales + i * 8);
         uint32_t v[64];
-        // block scales s (one per 16 elements) as FP16x2 pairs, pre-multiplied by 2^-7 for
-        // the conversion kind and by 2^7 for the shift kind (see kCvtWords)
+        // block scales s (one per 16 elements) as FP16x2 pairs
         const uint32_t s01 = e4m3x2_to_f16x2(sc.x), s23 = e4m3x2_to_f16x2(sc.x >> 16);
         const uint32_t s45 = e4m3x2_to_f16x2(sc.y), s67 = e4m3x2_to_f16x2(sc.y >> 16);
         const uint32_t sp[4] = {s01, s23, s45, s67};
@@ -412,18 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int blk = wi >> 1;    // 16-element scale block
             const uint32_t pair = sp[blk >> 1];
             const uint32_t sraw = (blk & 1) ? bcast_hi_half(pair) : bcast_lo_half(pair);
-            uint32_t o0, o1, o2, o3, scale;
-            if ((wi & 3) < kCvtWords) {
-              e2m1x8_to_f16x2x4(w[h], o0, o1, o2, o3);
-              scale = hmul2_bits(sraw, 0x20002000u);   // x 2^-7
-            } else {
-              e2m1x8_to_f16x2x4_shift(w[h], o0, o1, o2, o3);
-              scale = hmul2_bits(sraw, 0x58005800u);   // x 2^7
-            }
-            v[4 * wi + 0] = hmul2_bits(o0, scale);
-            v[4 * wi + 1] = hmul2_bits(o1, scale);
-            v[4 * wi + 2] = hmul2_bits(o2, scale);
-            v[4 * wi + 3] = hmul2_bits(o3, scale);
+            uint32_t o0, o1, o2, o3;
+            e2m1x8_to_f16x2x4(w[h], o0, o1, o2, o3);
+            v[4 * wi + 0] = hmul2_bits(o0, sraw);
+            v[4 * wi + 1] = hmul2_bits(o1, sraw);
+            v[4 * wi + 2] = hmul2_bits(o2, sraw);
+            v[4 * wi + 3] = hmul2_bits(o3, sraw);
           }
         }
         // the weight stage is consumed (its bytes are in registers): hand it back
@@ -538,8 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_bar_sync(1, 128);
         if (i < 64) {
-          const int nidx = act_pos(tk.s * kGuRows + i);  // storage position of element n
-          const float sc13 = a.w13_ts * kAccUnscale;
+          const int nidx = tk.s * kGuRows + i;  // element n of h
+          const float sc13 = a.w13_ts;
 #pragma unroll
           for (int c = 0; c < kRowsPerPass; ++c) {
             if (c < tk.rows) {
@@ -555,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // down stripe: per-route FP32 outputs (summed over routes by the un-route kernel)
         const int rcol = tk.s * kDnRows + i;
-        const float scale = a.w2_ts * kHUnscale * kAccUnscale;
+        const float scale = a.w2_ts * kHUnscale;
 #pragma unroll
         for (int c = 0; c < kRowsPerPass; ++c)
           if (c < tk.rows)
@@ -655,16 +635,12 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs p) {
       f[2 * j] = t.x;
       f[2 * j + 1] = t.y;
     }
-    // 8-element groups of the shift kind are stored in the dequantisation's pairing
-    const bool perm = shift_group(static_cast<int>((i * 8) % static_cast<size_t>(p.d)));
     uint4 o;
     __half2* h = reinterpret_cast<__half2*>(&o);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float lo = perm ? f[perm_elem(2 * q)] : f[2 * q];
-      const float hi = perm ? f[perm_elem(2 * q + 1)] : f[2 * q + 1];
-      bad |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
-      h[q] = __floats2half2_rn(lo, hi);
+      bad |= !(fabsf(f[2 * q]) <= 65504.f) || !(fabsf(f[2 * q + 1]) <= 65504.f);
+      h[q] = __floats2half2_rn(f[2 * q], f[2 * q + 1]);
     }
     reinterpret_cast<uint4*>(p.x16)[i] = o;
   }

@@ -30,26 +30,10 @@ constexpr int kMaxGroups = kRowsPerPass / kGroupRows;
 constexpr float kHScale = 0.0625f;  // h is stored as FP16(h * 2^-4)
 constexpr float kHUnscale = 16.0f;
 
-// Dequantisation handles E2M1 codes in words of 8 (32 consecutive elements = 4 words per
-// thread and row).  Words whose index mod 4 is below kCvtWords use the hardware
-// E2M1->FP16 conversion, which pairs neighbouring elements (2i, 2i+1) in one FP16x2
-// register; the others build FP16 bit patterns with integer shifts, which pairs elements
-// (j, j+4) of the word.  The two run on different pipes.  The FP16 activations (hidden
-// and h) are stored with the same pairing: in an 8-element group of the shift kind,
-// storage position p holds element perm_elem(p).  Both kinds leave a factor 2^-7 in the
-// products (the conversion kind is scaled by s * 2^-7, the shift kind, whose bits encode
-// w * 2^-14, by s * 2^7); kAccUnscale undoes it.
-constexpr int kCvtWords = 2;
-constexpr float kAccUnscale = 128.0f;
-
-__host__ __device__ constexpr bool shift_group(int k) { return ((k & 31) >> 3) >= kCvtWords; }
-// storage position of element o (0..7) inside a shift-kind group: elements 0..3 at the
-// even positions, 4..7 at the odd ones
-__host__ __device__ constexpr int perm_pos(int o) { return o < 4 ? 2 * o : 2 * (o - 4) + 1; }
-// element stored at position p (0..7) inside a shift-kind group
-__host__ __device__ constexpr int perm_elem(int p) { return (p & 1) ? (p >> 1) + 4 : (p >> 1); }
-// storage index of element k of an activation row
-__host__ __device__ constexpr int act_pos(int k) { return shift_group(k) ? (k & ~7) + perm_pos(k & 7) : k; }
+// Dequantisation converts E2M1 codes with the hardware E2M1->FP16 conversion (one
+// instruction per code byte, elements (2i, 2i+1) into one FP16x2 register) and multiplies
+// by the FP16 block scale: E2M1 x E4M3 needs at most 6 significant bits and lies within
+// [2^-10, 2688], so the product is exact in FP16.  Activations are stored in natural order.
 
 struct WsLayout {
   size_t status, meta, counts, offsets, touched, gu_start, dn_start, route_pos, pos_tok, route_w;
@@ -142,6 +126,8 @@ MOE_DEVICE bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 MOE_DEVICE void fence_barrier_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 MOE_DEVICE void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+MOE_DEVICE void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+MOE_DEVICE void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // ---- TMA (tensor) and cp.async ----
 MOE_DEVICE uint64_t policy_evict_first() {
@@ -289,17 +275,6 @@ MOE_DEVICE uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o) : "h"(h));
   return o;
 }
-// Eight E2M1 codes (one word) to four FP16x2 registers with integer operations: register
-// j holds elements (j, j+4) as the bit patterns of w * 2^-14 (E2M1's exponent and mantissa
-// bits dropped into FP16's exponent LSBs and mantissa MSB; E2M1 exponent 0 lands on FP16
-// subnormals, which is again w * 2^-14).
-MOE_DEVICE void e2m1x8_to_f16x2x4_shift(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2, uint32_t& o3) {
-  const uint32_t kMag = 0x0E000E00u, kSign = 0x80008000u;
-  o0 = ((w << 9) & kMag) | ((w << 12) & kSign);
-  o1 = ((w << 5) & kMag) | ((w << 8) & kSign);
-  o2 = ((w << 1) & kMag) | ((w << 4) & kSign);
-  o3 = ((w >> 3) & kMag) | (w & kSign);
-}
 MOE_DEVICE uint32_t hmul2_bits(uint32_t a, uint32_t b) {
   uint32_t o;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o) : "r"(a), "r"(b));
@@ -313,6 +288,33 @@ MOE_DEVICE uint32_t ld_acquire_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+MOE_DEVICE void red_add_relaxed_gpu_u32(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Warp-wide wait until *ctr >= target: lane 0 polls with acquire loads, giving up after
+// `timeout` cycles (sets *abort_flag and MOE_DEV_TIMEOUT) or when *abort_flag is raised.
+// On success the warp's later global reads, bulk copies included, are ordered after the
+// writes the counter's producers released.  Returns the same value on every lane.
+MOE_DEVICE bool warp_wait_counter(const uint32_t* ctr, uint32_t target, volatile int* abort_flag, int* status,
+                                  long long timeout) {
+  int good = 1;
+  if ((threadIdx.x & 31) == 0) {
+    const long long t0 = clock64();
+    while (ld_acquire_u32(ctr) < target) {
+      if (*abort_flag) { good = 0; break; }
+      if (clock64() - t0 > timeout) {
+        *abort_flag = 1;
+        atomicOr(status, static_cast<int>(MOE_DEV_TIMEOUT));
+        good = 0;
+        break;
+      }
+      __nanosleep(32);
+    }
+  }
+  __syncwarp();
+  fence_proxy_async_global();
+  return __shfl_sync(0xffffffffu, good, 0) != 0;
 }
 MOE_DEVICE uint32_t atom_add_acqrel_u32(uint32_t* p, uint32_t v) {
   uint32_t old;

@@ -72,13 +72,17 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream);
 cudaError_t launch_expert_tc(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
                              int num_sms, cudaStream_t stream);
 cudaError_t launch_expert_mma(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
-                              int num_sms, cudaStream_t stream);
+                              const CUtensorMap& tm_s13, const CUtensorMap& tm_s2, int num_sms,
+                              cudaStream_t stream);
 cudaError_t launch_expert_simt(const ExpertArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const ExpertArgs& a, cudaStream_t stream);
 size_t expert_tc_smem_bytes();
 size_t expert_mma_smem_bytes();
 int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes);
-// Shapes the decode (warp-MMA) kernel handles: d, ffn multiples of 256 and at most 2048.
+// Tensor map of a [rows, row_bytes] uint8 matrix (row_bytes 16, 32, 64 or 128) loaded in
+// boxes of box_rows full rows, swizzled by the row size (none for 16 bytes).
+int encode_scales_map(CUtensorMap* tm, const void* base, uint32_t row_bytes, uint64_t rows, uint32_t box_rows);
+// Shapes the decode (warp-MMA) kernel handles: d and ffn powers of two from 256 to 2048.
 bool expert_mma_supports(int d, int F);
 // Record a message for moe_last_cuda_error on the calling host thread.
 void set_last_error_message(const char* msg);

@@ -6,8 +6,8 @@
 namespace moe {
 namespace {
 
-__global__ void selftest_decode_kernel(const uint32_t* words, int n, uint32_t* out, uint32_t* out_shift,
-                                       const uint32_t* pairs, int m, uint32_t* sout) {
+__global__ void selftest_decode_kernel(const uint32_t* words, int n, uint32_t* out, const uint32_t* pairs, int m,
+                                       uint32_t* sout) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) {
     uint32_t o0, o1, o2, o3;
@@ -16,11 +16,6 @@ __global__ void selftest_decode_kernel(const uint32_t* words, int n, uint32_t* o
     out[4 * i + 1] = o1;
     out[4 * i + 2] = o2;
     out[4 * i + 3] = o3;
-    e2m1x8_to_f16x2x4_shift(words[i], o0, o1, o2, o3);
-    out_shift[4 * i + 0] = o0;
-    out_shift[4 * i + 1] = o1;
-    out_shift[4 * i + 2] = o2;
-    out_shift[4 * i + 3] = o3;
   }
   if (i < m) sout[i] = e4m3x2_to_f16x2(pairs[i]);
 }
@@ -109,12 +104,12 @@ __global__ void __launch_bounds__(128) selftest_mma_kernel(const __half* A, cons
 
 extern "C" {
 
-int moe_selftest_decode(const uint32_t* words, int n, uint32_t* out, uint32_t* out_shift, const uint32_t* pairs,
-                        int m, uint32_t* sout, moe_stream_t stream) {
-  if (n < 0 || m < 0 || (n && (!words || !out || !out_shift)) || (m && (!pairs || !sout))) return MOE_ERR_INVALID_ARG;
+int moe_selftest_decode(const uint32_t* words, int n, uint32_t* out, const uint32_t* pairs, int m, uint32_t* sout,
+                        moe_stream_t stream) {
+  if (n < 0 || m < 0 || (n && (!words || !out)) || (m && (!pairs || !sout))) return MOE_ERR_INVALID_ARG;
   const int total = n > m ? n : m;
   if (total == 0) return MOE_OK;
-  moe::selftest_decode_kernel<<<(total + 127) / 128, 128, 0, stream>>>(words, n, out, out_shift, pairs, m, sout);
+  moe::selftest_decode_kernel<<<(total + 127) / 128, 128, 0, stream>>>(words, n, out, pairs, m, sout);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

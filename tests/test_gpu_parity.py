@@ -86,7 +86,7 @@ def test_ragged_and_edge_shapes(T, d, F, E, k):
 
 @pytest.mark.parametrize("T,d,F,E,k", [(1, 256, 256, 16, 1), (5, 512, 256, 16, 2), (33, 512, 512, 64, 8),
                                        (100, 256, 256, 32, 4), (7, 1024, 256, 40, 32), (64, 1024, 256, 16, 16),
-                                       (130, 256, 256, 4, 4)])
+                                       (130, 256, 256, 4, 4), (9, 512, 1024, 16, 4), (9, 256, 2048, 8, 2)])
 def test_mma_path_shapes(T, d, F, E, k):
     # (130, ..., E=4, k=4): every expert holds all 130 rows -> three 64-row passes
     cfg = mi.CONFIGS["tiny"].replace(name=f"mma{T}x{d}x{F}x{E}x{k}", T=T, d=d, ffn=F, E=E, k=k, tag=200 + T)
@@ -96,9 +96,12 @@ def test_mma_path_shapes(T, d, F, E, k):
 
 def test_mma_path_rejects_unsupported_shape():
     import routed_moe_decode_gb300 as moe
-    cfg = mi.CONFIGS["tiny"]  # ffn = 128 is not a multiple of 256
+    cfg = mi.CONFIGS["tiny"]  # ffn = 128 is below the 256-element chunk
     with pytest.raises(moe.MoeError):
         run_layer(cfg, dict(config_inputs("tiny")), algo=ALGOS["mma"])
+    cfg = cfg.replace(name="mma_d768", d=768, ffn=256)  # not a power of two
+    with pytest.raises(moe.MoeError):
+        run_layer(cfg, mi.gen_layer(cfg, seed=5), algo=ALGOS["mma"])
 
 
 def _route_only(logits, k):
