@@ -124,6 +124,10 @@ MOE_API int moe_workspace_init(void* workspace, size_t workspace_bytes, moe_stre
  * MOE_ERR_UNSUPPORTED. */
 MOE_API int moe_check_shape(const moe_shape* shape);
 
+/* The expert kernel MOE_ALGO_AUTO selects for a shape (MOE_ALGO_MMA or MOE_ALGO_TCGEN05),
+ * or a negative status when the shape is invalid.  Pure host function: needs no GPU. */
+MOE_API int moe_auto_algo(const moe_shape* shape);
+
 /* Step 1, router ("Fused MoE routing"; "Router: selection and expert-task production").
  *   logits  [T, E]  float32, finite values (non-finite logits are outside the contract)
  *   ids     [T, k]  int32 out: selected experts in selection order (value desc, ties to

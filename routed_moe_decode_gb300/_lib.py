@@ -50,6 +50,7 @@ SIGNATURES = {
     "moe_workspace_bytes": (ctypes.c_size_t, [_SP]),
     "moe_workspace_init": (_I, [_P, ctypes.c_size_t, _P]),
     "moe_check_shape": (_I, [_SP]),
+    "moe_auto_algo": (_I, [_SP]),
     "moe_route_topk": (_I, [_SP, _P, _P, _P, _P]),
     "moe_plan": (_I, [_SP, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_forward": (_I, [_SP, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -118,6 +119,14 @@ def workspace_bytes(shape: Shape) -> int:
 
 def check_shape(shape: Shape) -> int:
     return int(lib().moe_check_shape(ctypes.byref(shape)))
+
+
+def auto_algo(shape: Shape) -> int:
+    """The expert kernel ALGO_AUTO picks for `shape` (ALGO_MMA or ALGO_TCGEN05)."""
+    rc = int(lib().moe_auto_algo(ctypes.byref(shape)))
+    if rc < 0:
+        raise MoeError("moe_auto_algo", rc)
+    return rc
 
 
 class Workspace:

@@ -195,6 +195,12 @@ const char* moe_last_cuda_error(void) { return g_last_error; }
 
 int moe_check_shape(const moe_shape* shape) { return check_shape(shape); }
 
+int moe_auto_algo(const moe_shape* shape) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc < 0 ? rc : -rc;
+  return moe::expert_mma_supports(shape->d, shape->ffn) ? MOE_ALGO_MMA : MOE_ALGO_TCGEN05;
+}
+
 size_t moe_workspace_bytes(const moe_shape* shape) {
   if (check_shape(shape) != MOE_OK) return 0;
   return moe::ws_layout(*shape).total;

@@ -62,6 +62,17 @@ def test_workspace_size_and_shape_checks(L):
     assert L.workspace_bytes(L.shape_of(4, 2000, 512, 512, 10)) == 0
 
 
+def test_auto_algo_selection(L):
+    # decode kernel: d and ffn powers of two from 256 to 2048; the tcgen05 kernel otherwise
+    assert L.auto_algo(L.shape_of(4, 2048, 512, 512, 10)) == L.ALGO_MMA
+    assert L.auto_algo(L.shape_of(8192, 256, 2048, 64, 8)) == L.ALGO_MMA
+    assert L.auto_algo(L.shape_of(4, 768, 512, 64, 8)) == L.ALGO_TCGEN05
+    assert L.auto_algo(L.shape_of(4, 2048, 128, 64, 8)) == L.ALGO_TCGEN05
+    assert L.auto_algo(L.shape_of(4, 4096, 512, 64, 8)) == L.ALGO_TCGEN05
+    with pytest.raises(L.MoeError):
+        L.auto_algo(L.shape_of(4, 2000, 512, 512, 10))
+
+
 def test_bad_arguments_rejected_on_host(L):
     lib = L.lib()
     s = L.shape_of(4, 256, 128, 16, 2)
