@@ -271,13 +271,21 @@ def our_arm(args, cfg, dist, torch):
     wts = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
     out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
 
+    fused_front = algo == moe.ALGO_AUTO and cfg.T * cfg.k <= 16384
+
     def step(l):
+        if algo == moe.ALGO_AUTO:
+            # the public one-call layer (fused router + plan front for moderate T * k)
+            moe.layer(shape, logits[l], hidden[l], Wd[l], resid[l], out, ids, wts, ws)
+            return
         moe.route_topk(shape, logits[l], ids, wts)
         moe.plan(shape, ids, wts, ws)
         moe.forward_prepare(shape, hidden[l], ws)
         moe.forward_experts(shape, Wd[l], resid[l], out, ws, algo)
 
-    kernels_per_step = 6 if algo == moe.ALGO_SIMT else 5  # route, plan, prep, expert(s), un-route
+    # front kernel(s), expert kernel(s), un-route kernel
+    front_kernels = 1 if fused_front else 3
+    kernels_per_step = front_kernels + (2 if algo == moe.ALGO_SIMT else 1) + 1
 
     # ---- unique experts per layer (outside any timed region) ----
     U = []

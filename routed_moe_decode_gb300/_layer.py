@@ -9,8 +9,9 @@ from . import _lib
 class MoeLayer:
     """Routed MoE layer of a fixed shape on one CUDA device.
 
-    __call__ runs router, plan and experts (three C-ABI calls on the current stream) and
-    returns the BF16 output [T, d].  Weights are a dict of device tensors:
+    __call__ runs the whole layer and returns the BF16 output [T, d]: with the automatic
+    kernel choice one moe_layer call (fused router + plan front for moderate T * k), else
+    router, plan and experts as three C-ABI calls on the current stream.  Weights are a dict of device tensors:
     w13_codes [E, 2*ffn, d/2] uint8, w13_scales [E, 2*ffn, d/16] uint8 (E4M3),
     w2_codes [E, d, ffn/2] uint8, w2_scales [E, d, ffn/16] uint8, and the FP32 tensor
     scales w13_ts / w2_ts (Python floats).
@@ -41,6 +42,11 @@ class MoeLayer:
         return out
 
     def __call__(self, logits, hidden, w, residual=None, out=None):
+        if self.algo == _lib.ALGO_AUTO:
+            if out is None:
+                out = torch.empty((self.shape.T, self.shape.d), dtype=torch.bfloat16, device=self.device)
+            _lib.layer(self.shape, logits, hidden, w, residual, out, self.ids, self.weights, self.ws)
+            return out
         self.route(logits)
         self.plan()
         return self.experts(hidden, w, residual, out)

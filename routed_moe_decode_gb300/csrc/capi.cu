@@ -225,16 +225,8 @@ int moe_route_topk(const moe_shape* shape, const float* logits, int32_t* ids, fl
   return MOE_OK;
 }
 
-int moe_plan(const moe_shape* shape, const int32_t* ids, const float* weights, void* workspace,
-             size_t workspace_bytes, moe_stream_t stream) {
-  int rc = check_shape(shape);
-  if (rc != MOE_OK) return rc;
-  if (shape->T == 0) return MOE_OK;
-  if (!ids || !weights) return MOE_ERR_INVALID_ARG;
-  rc = check_ws(shape, workspace, workspace_bytes);
-  if (rc != MOE_OK) return rc;
-  const WsLayout L = moe::ws_layout(*shape);
-  moe::PlanArgs a{};
+static void fill_plan_args(moe::PlanArgs& a, const moe_shape* shape, const WsLayout& L, void* workspace,
+                           const int32_t* ids, const float* weights) {
   a.T = shape->T; a.E = shape->E; a.k = shape->k; a.S_gu = L.S_gu; a.S_dn = L.S_dn;
   a.ids = ids; a.weights = weights;
   a.status = at<int>(workspace, L.status);
@@ -248,6 +240,19 @@ int moe_plan(const moe_shape* shape, const int32_t* ids, const float* weights, v
   a.pos_tok = at<int>(workspace, L.pos_tok);
   a.route_w = at<float>(workspace, L.route_w);
   a.tasks = at<moe::TaskEntry>(workspace, L.tasks);
+}
+
+int moe_plan(const moe_shape* shape, const int32_t* ids, const float* weights, void* workspace,
+             size_t workspace_bytes, moe_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (shape->T == 0) return MOE_OK;
+  if (!ids || !weights) return MOE_ERR_INVALID_ARG;
+  rc = check_ws(shape, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
+  const WsLayout L = moe::ws_layout(*shape);
+  moe::PlanArgs a{};
+  fill_plan_args(a, shape, L, workspace, ids, weights);
   cudaError_t e = moe::launch_plan(a, stream);
   if (e != cudaSuccess) { set_error("plan launch", e); return MOE_ERR_CUDA; }
   return MOE_OK;
@@ -377,12 +382,37 @@ int moe_layer(const moe_shape* shape, const float* logits, const void* hidden, c
               const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales,
               float w2_scale, const void* residual, void* out, int32_t* ids, float* weights, void* workspace,
               size_t workspace_bytes, moe_stream_t stream) {
-  int rc = moe_route_topk(shape, logits, ids, weights, stream);
+  int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
-  rc = moe_plan(shape, ids, weights, workspace, workspace_bytes, stream);
+  if (shape->T == 0) return MOE_OK;
+  if (shape->T * shape->k > moe::kFrontMaxRoutes) {
+    // large batches: separate router, plan and preparation kernels
+    rc = moe_route_topk(shape, logits, ids, weights, stream);
+    if (rc != MOE_OK) return rc;
+    rc = moe_plan(shape, ids, weights, workspace, workspace_bytes, stream);
+    if (rc != MOE_OK) return rc;
+    return moe_forward(shape, hidden, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual,
+                       out, workspace, workspace_bytes, stream);
+  }
+  if (!logits || !hidden || !ids || !weights || !aligned(logits, 16) || !aligned(hidden, 16) || !aligned(ids, 4) ||
+      !aligned(weights, 4))
+    return MOE_ERR_INVALID_ARG;
+  rc = check_ws(shape, workspace, workspace_bytes);
   if (rc != MOE_OK) return rc;
-  return moe_forward(shape, hidden, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
-                     workspace, workspace_bytes, stream);
+  const WsLayout L = moe::ws_layout(*shape);
+  moe::FrontArgs f{};
+  fill_plan_args(f.plan, shape, L, workspace, ids, weights);
+  f.d = shape->d;
+  f.logits = logits;
+  f.hidden = static_cast<const __nv_bfloat16*>(hidden);
+  f.x16 = at<__half>(workspace, L.x16);
+  f.ready = at<uint32_t>(workspace, L.ready);
+  f.ticket = at<uint32_t>(workspace, L.ticket);
+  f.done = at<uint32_t>(workspace, L.front_done);
+  cudaError_t e = moe::launch_front(f, stream);
+  if (e != cudaSuccess) { set_error("front launch", e); return MOE_ERR_CUDA; }
+  return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
+                              workspace, workspace_bytes, MOE_ALGO_AUTO, nullptr, stream);
 }
 
 int moe_read_device_status(const void* workspace, int clear, uint32_t* status_bits, moe_stream_t stream) {

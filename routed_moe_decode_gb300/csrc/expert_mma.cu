@@ -453,6 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int P = is_dn ? P2 : P13;
       const int nck = K / kChunk;
       const int nt = (rows + kTileRows - 1) / kTileRows;
+      // Accumulation layout: one- and two-tile passes spread their k-steps over independent
+      // accumulator sets; an expert with several passes keeps one set per tile in every pass,
+      // so a route's result does not depend on which pass the plan put it in.
+      const bool multi = ((te.z >> 17) & 1) != 0;
+      const int mode = multi ? 0 : (nt == 1 ? 1 : (nt == 2 ? 2 : 0));
       // tile rows (0..127) of fragment rows g and g + 8
       const int lra = is_dn ? 16 * cw + fr : 8 * cw + fr;
       const int lrb = is_dn ? 16 * cw + 8 + fr : 64 + 8 * cw + fr;
@@ -496,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // independent accumulators (8 for one tile, 4 per tile for two) so that consecutive
         // MMAs do not wait on each other; the sets are summed after the task.
         const uint8_t* b0 = &sm.ring_b[stage_b][0];
-        if (nt == 1) {
+        if (mode == 1) {
           const bool live = g < rows;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -512,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         xb[j].w);
             }
           }
-        } else if (nt == 2) {
+        } else if (mode == 2) {
           const uint8_t* b1 = &sm.ring_b[stage_b + 1 == kStagesB ? 0 : stage_b + 1][0];
           const bool live0 = g < rows, live1 = g < rows - kTileRows;
 #pragma unroll
@@ -579,12 +584,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // fold the independent accumulator sets into one per tile
-      if (nt == 1) {
+      if (mode == 1) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           acc[0][i] = ((acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i])) +
                       ((acc[4][i] + acc[5][i]) + (acc[6][i] + acc[7][i]));
-      } else if (nt == 2) {
+      } else if (mode == 2) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           acc[0][i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);

@@ -38,6 +38,7 @@ constexpr float kHUnscale = 16.0f;
 struct WsLayout {
   size_t status, meta, counts, offsets, touched, gu_start, dn_start, route_pos, pos_tok, route_w;
   size_t ready, ticket, tasks, x16, hs16, y, total;
+  size_t front_done;  // arrival counter of the fused front, inside the zeroed status block
   int S_gu;       // gate/up stripes per expert (ffn / 64)
   int S_dn;       // down stripes per expert (d / 128)
   int max_tasks;  // capacity of the task table
@@ -49,7 +50,8 @@ enum { META_U = 0, META_NGU = 1, META_NDN = 2, META_MAXROWS = 3, META_WORDS = 8 
 
 // One expert task as the plan writes it (16 bytes):
 //   x = expert id | touched index << 16, y = first routed row (expert-major position),
-//   z = rows in this pass | is_down << 16, w = stripe index.
+//   z = rows in this pass | is_down << 16 | (expert has more than one pass) << 17,
+//   w = stripe index.
 struct TaskEntry {
   int x, y, z, w;
 };
@@ -67,6 +69,7 @@ inline WsLayout ws_layout(const moe_shape& s) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   L.status = take(64);
+  L.front_done = L.status + 64;
   L.meta = take(META_WORDS * 4);
   L.counts = take(size_t(s.E) * 4);
   L.offsets = take(size_t(s.E + 1) * 4);

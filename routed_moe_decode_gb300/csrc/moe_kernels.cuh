@@ -24,6 +24,19 @@ struct PlanArgs {
   TaskEntry* tasks;
 };
 
+// The fused front (router + plan + FP16 hidden) for T * k up to kFrontMaxRoutes.
+struct FrontArgs {
+  PlanArgs plan;  // plan.ids / plan.weights receive the router's output
+  int d;
+  const float* logits;
+  const __nv_bfloat16* hidden;
+  __half* x16;
+  uint32_t* ready;
+  uint32_t* ticket;
+  uint32_t* done;  // CTA arrival counter: zero between calls
+};
+constexpr int kFrontMaxRoutes = 16384;
+
 struct PrepArgs {
   int T, d, E;
   const __nv_bfloat16* hidden;
@@ -68,6 +81,7 @@ constexpr int kTracePerRole = 128;
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* weights,
                               cudaStream_t stream);
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
+cudaError_t launch_front(const FrontArgs& f, cudaStream_t stream);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream);
 cudaError_t launch_expert_tc(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
                              int num_sms, cudaStream_t stream);

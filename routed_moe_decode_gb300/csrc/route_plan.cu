@@ -23,12 +23,12 @@ namespace moe {
 
 constexpr uint32_t kFull = 0xffffffffu;
 
+// Route token t (one warp): softmax over the E logits, k rounds of arg-max selection,
+// renormalised weights.  Writes ids[t, :k] and weights[t, :k].
 template <int NPL>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                         int32_t* __restrict__ ids, float* __restrict__ weights) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
+__device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E, int k,
+                                            int32_t* __restrict__ ids, float* __restrict__ weights) {
+  const int lane = threadIdx.x & 31;
   const float* row = logits + static_cast<size_t>(t) * E;
   float v[NPL];
   uint32_t key[NPL];
@@ -89,6 +89,14 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   }
 }
 
+template <int NPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                         int32_t* __restrict__ ids, float* __restrict__ weights) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  route_token<NPL>(logits, t, E, k, ids, weights);
+}
+
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* weights,
                               cudaStream_t stream) {
   const int npl = (E + 31) / 32;
@@ -131,7 +139,9 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
   return out;
 }
 
-__global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
+// The plan for all T * k routes, computed by one 1024-thread CTA.  ids/weights are read past
+// L1: in the fused front they were written by other CTAs of the same launch.
+__device__ __forceinline__ void plan_block(const PlanArgs& a) {
   __shared__ int s_counts[1024];
   __shared__ int s_cursor[1024];
   __shared__ int s_scan[33];
@@ -140,8 +150,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
   if (tid < E) s_counts[tid] = 0;
   __syncthreads();
   for (int r = tid; r < R; r += blockDim.x) {
-    const int e = a.ids[r];
-    a.route_w[r] = a.weights[r];
+    const int e = __ldcg(a.ids + r);
+    a.route_w[r] = __ldcg(a.weights + r);
     if (e < 0 || e >= E) {
       atomicOr(a.status, static_cast<int>(MOE_DEV_BAD_EXPERT_ID));
     } else {
@@ -202,8 +212,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
     for (int p = 0; p < np; ++p) {
       const int rows = min(kRowsPerPass, m - p * kRowsPerPass);
       const int row0 = base + p * kRowsPerPass;
-      for (int s2 = 0; s2 < a.S_gu; ++s2) a.tasks[gi++] = TaskEntry{e | (tid << 16), row0, rows, s2};
-      for (int s2 = 0; s2 < a.S_dn; ++s2) a.tasks[di++] = TaskEntry{e | (tid << 16), row0, rows | (1 << 16), s2};
+      const int z = rows | (np > 1 ? 1 << 17 : 0);
+      for (int s2 = 0; s2 < a.S_gu; ++s2) a.tasks[gi++] = TaskEntry{e | (tid << 16), row0, z, s2};
+      for (int s2 = 0; s2 < a.S_dn; ++s2) a.tasks[di++] = TaskEntry{e | (tid << 16), row0, z | (1 << 16), s2};
     }
   }
   // largest row count over the experts
@@ -223,7 +234,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
   __syncthreads();
   // route positions in expert-major order
   for (int r = tid; r < R; r += blockDim.x) {
-    const int e = a.ids[r];
+    const int e = __ldcg(a.ids + r);
     if (e < 0 || e >= E) {
       a.route_pos[r] = -1;
       continue;
@@ -232,6 +243,71 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
     a.route_pos[r] = pos;
     a.pos_tok[pos] = r / a.k;
   }
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) { plan_block(a); }
+
+// ---------------------------------------------------------------------------------
+// Fused front for moderate T * k: each 1024-thread CTA routes 32 tokens (one per warp) and
+// converts their hidden rows to FP16; CTA 0 zeroes the expert kernel's counters; the last
+// CTA to finish (arrival counter, reset by that CTA for the next call) builds the plan.
+// ---------------------------------------------------------------------------------
+template <int NPL>
+__global__ void __launch_bounds__(1024) front_kernel(FrontArgs f) {
+  __shared__ int s_last;
+  const int warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * 32 + warp;
+  const PlanArgs& a = f.plan;
+  if (t < a.T) route_token<NPL>(f.logits, t, a.E, a.k, const_cast<int32_t*>(a.ids), const_cast<float*>(a.weights));
+  // hidden rows of this CTA's tokens -> FP16, flagging values outside the FP16 range
+  {
+    const int t0 = blockIdx.x * 32, nt = min(32, a.T - t0);
+    const size_t n8 = static_cast<size_t>(nt) * f.d / 8;
+    const uint4* src = reinterpret_cast<const uint4*>(f.hidden + static_cast<size_t>(t0) * f.d);
+    uint4* dst = reinterpret_cast<uint4*>(f.x16 + static_cast<size_t>(t0) * f.d);
+    bool bad = false;
+    for (size_t i = threadIdx.x; i < n8; i += blockDim.x) {
+      const uint4 raw = src[i];
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      uint4 o;
+      __half2* h = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 v = __bfloat1622float2(b[q]);
+        bad |= !(fabsf(v.x) <= 65504.f) || !(fabsf(v.y) <= 65504.f);
+        h[q] = __floats2half2_rn(v.x, v.y);
+      }
+      dst[i] = o;
+    }
+    if (bad) atomicOr(a.status, static_cast<int>(MOE_DEV_HIDDEN_RANGE));
+  }
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < a.E; i += blockDim.x) f.ready[i] = 0u;
+    if (threadIdx.x == 0) *f.ticket = 0u;
+  }
+  // the last CTA to arrive sees every route
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(f.done, 1u) == gridDim.x - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  plan_block(a);
+  if (threadIdx.x == 0) *f.done = 0u;
+}
+
+cudaError_t launch_front(const FrontArgs& f, cudaStream_t stream) {
+  const int npl = (f.plan.E + 31) / 32;
+  const dim3 grid((f.plan.T + 31) / 32), block(1024);
+  if (npl <= 1) front_kernel<1><<<grid, block, 0, stream>>>(f);
+  else if (npl <= 2) front_kernel<2><<<grid, block, 0, stream>>>(f);
+  else if (npl <= 4) front_kernel<4><<<grid, block, 0, stream>>>(f);
+  else if (npl <= 8) front_kernel<8><<<grid, block, 0, stream>>>(f);
+  else if (npl <= 16) front_kernel<16><<<grid, block, 0, stream>>>(f);
+  else front_kernel<32><<<grid, block, 0, stream>>>(f);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {

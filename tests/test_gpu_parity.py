@@ -58,6 +58,38 @@ def test_layer_parity_mma(name):
 
 
 @pytest.mark.parametrize("name", ["tiny", "b1", "b8", "b64", "prefill"])
+def test_layer_parity_auto(name):
+    # the one-call layer: fused router + plan front (T * k <= 16384), separate kernels above
+    cfg = mi.CONFIGS[name]
+    _check_layer(cfg, config_inputs(name), ALGOS["auto"], SAMPLES[name])
+
+
+@pytest.mark.parametrize("T,d,F,E,k", [(4, 2048, 512, 512, 10), (33, 512, 256, 64, 8), (100, 256, 256, 1000, 7),
+                                       (256, 2048, 512, 512, 10), (64, 256, 512, 16, 1), (1638, 256, 256, 64, 10),
+                                       (1639, 256, 256, 64, 10)])
+def test_fused_front_matches_separate_calls(T, d, F, E, k):
+    # one moe_layer call (multi-CTA fronts, the last one building the plan; the last shape
+    # has T * k just above the fused front's limit) against router + plan + forward
+    import routed_moe_decode_gb300 as moe
+    cfg = mi.CONFIGS["tiny"].replace(name=f"front{T}x{d}x{F}x{E}x{k}", T=T, d=d, ffn=F, E=E, k=k, tag=300 + T)
+    inp = mi.gen_layer(cfg, seed=6)
+    w = device_weights(inp, "cuda")
+    logits = torch.from_numpy(inp["logits"]).cuda()
+    hidden = bf16_tensor(inp["hidden"], "cuda")
+    res = bf16_tensor(inp["residual"], "cuda")
+    fused = moe.MoeLayer(T, d, F, E, k)
+    outs = [fused(logits, hidden, w, res) for _ in range(3)]  # the arrival counter resets itself
+    sep = moe.MoeLayer(T, d, F, E, k, algo=moe.auto_algo(fused.shape))
+    ref = sep(logits, hidden, w, res)
+    torch.cuda.synchronize()
+    assert fused.status() == 0 and sep.status() == 0
+    assert torch.equal(fused.ids, sep.ids) and torch.equal(fused.weights, sep.weights)
+    for o in outs:
+        assert torch.equal(o, ref)
+    assert moe.plan_summary(fused.shape, fused.ws) == moe.plan_summary(sep.shape, sep.ws)
+
+
+@pytest.mark.parametrize("name", ["tiny", "b1", "b8", "b64", "prefill"])
 def test_layer_parity_tcgen05(name):
     cfg = mi.CONFIGS[name]
     _check_layer(cfg, config_inputs(name), ALGOS["tcgen05"], SAMPLES[name])
