@@ -180,8 +180,24 @@ MOE_API int moe_forward_experts(const moe_shape* shape, const uint8_t* w13_codes
                                 void* out, void* workspace, size_t workspace_bytes, int algo,
                                 moe_stream_t stream);
 
-/* Whole layer: moe_route_topk + moe_plan + moe_forward on one stream, with ids/weights
- * written to the caller's [T, k] buffers. */
+/* moe_forward_experts in two launches' worth of parts, for callers that want to time or
+ * schedule them apart: moe_forward_expert_kernels runs only the expert kernel(s) (gate/up,
+ * SiLU·mul, down projection into the per-route FP32 outputs of the workspace);
+ * moe_forward_unroute runs only the weighted un-route (out = residual + the token's routes
+ * in slot order, "fuses down with weighted unroute" in "Persistent execution for
+ * Flash-Next GGUF on SM70").  Arguments as for moe_forward_experts. */
+MOE_API int moe_forward_expert_kernels(const moe_shape* shape, const uint8_t* w13_codes,
+                                       const uint8_t* w13_scales, float w13_scale,
+                                       const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+                                       void* workspace, size_t workspace_bytes, int algo,
+                                       moe_stream_t stream);
+MOE_API int moe_forward_unroute(const moe_shape* shape, const void* residual, void* out, void* workspace,
+                                size_t workspace_bytes, moe_stream_t stream);
+
+/* Whole layer: router, plan and forward on one stream, with ids/weights written to the
+ * caller's [T, k] buffers.  For T * k up to 16384 the router, the FP16 staging of hidden
+ * and the plan run as one fused launch (the last CTA to finish routing builds the plan);
+ * larger batches use moe_route_topk + moe_plan + moe_forward. */
 MOE_API int moe_layer(const moe_shape* shape, const float* logits, const void* hidden,
               const uint8_t* w13_codes, const uint8_t* w13_scales, float w13_scale,
               const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,

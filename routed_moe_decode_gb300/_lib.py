@@ -57,6 +57,8 @@ SIGNATURES = {
     "moe_forward_algo": (_I, [_SP, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _I, _P]),
     "moe_forward_prepare": (_I, [_SP, _P, _P, ctypes.c_size_t, _P]),
     "moe_forward_experts": (_I, [_SP, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _I, _P]),
+    "moe_forward_expert_kernels": (_I, [_SP, _P, _P, _F, _P, _P, _F, _P, ctypes.c_size_t, _I, _P]),
+    "moe_forward_unroute": (_I, [_SP, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_layer": (_I, [_SP, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_layer_static_workspace": (_I, [_SP, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P]),
     "moe_read_device_status": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint32), _P]),
@@ -174,6 +176,19 @@ def forward_experts(shape: Shape, w: dict, residual, out, ws: Workspace, algo: i
         ctypes.byref(shape), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]), float(w["w13_ts"]),
         _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]), _ptr(residual), _ptr(out), ws.ptr,
         ws.nbytes, int(algo), _stream(stream)))
+
+
+def forward_expert_kernels(shape: Shape, w: dict, ws: Workspace, algo: int = ALGO_AUTO, stream=None):
+    """The expert kernel(s) alone (per-route down outputs into the workspace)."""
+    _check("moe_forward_expert_kernels", lib().moe_forward_expert_kernels(
+        ctypes.byref(shape), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]), float(w["w13_ts"]),
+        _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]), ws.ptr, ws.nbytes, algo, _stream(stream)))
+
+
+def forward_unroute(shape: Shape, residual, out, ws: Workspace, stream=None):
+    """The weighted un-route alone: out = residual + the token's routes in slot order."""
+    _check("moe_forward_unroute", lib().moe_forward_unroute(
+        ctypes.byref(shape), _ptr(residual), _ptr(out), ws.ptr, ws.nbytes, _stream(stream)))
 
 
 def layer(shape: Shape, logits, hidden, w: dict, residual, out, ids, weights, ws: Workspace, stream=None):

@@ -279,16 +279,20 @@ int moe_forward_prepare(const moe_shape* shape, const void* hidden, void* worksp
   return MOE_OK;
 }
 
+enum { kStageExperts = 1, kStageUnroute = 2 };
+
 static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
                                 float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
                                 const void* residual, void* out, void* workspace, size_t workspace_bytes, int algo,
-                                unsigned long long* trace, moe_stream_t stream) {
+                                unsigned long long* trace, moe_stream_t stream, int stages = kStageExperts | kStageUnroute) {
   int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   if (shape->T == 0) return MOE_OK;
-  if (!w13_codes || !w13_scales || !w2_codes || !w2_scales || !out) return MOE_ERR_INVALID_ARG;
-  if (!aligned(w13_codes, 16) || !aligned(w13_scales, 16) || !aligned(w2_codes, 16) || !aligned(w2_scales, 16) ||
-      !aligned(out, 16) || (residual && !aligned(residual, 16)))
+  if ((stages & kStageExperts) &&
+      (!w13_codes || !w13_scales || !w2_codes || !w2_scales || !aligned(w13_codes, 16) || !aligned(w13_scales, 16) ||
+       !aligned(w2_codes, 16) || !aligned(w2_scales, 16)))
+    return MOE_ERR_INVALID_ARG;
+  if ((stages & kStageUnroute) && (!out || !aligned(out, 16) || (residual && !aligned(residual, 16))))
     return MOE_ERR_INVALID_ARG;
   if (algo < MOE_ALGO_AUTO || algo > MOE_ALGO_MMA) return MOE_ERR_INVALID_ARG;
   rc = check_ws(shape, workspace, workspace_bytes);
@@ -298,9 +302,18 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
                                   w2_scale, residual, out);
   a.trace = trace;
   cudaError_t e;
+  if (!(stages & kStageExperts)) {
+    e = moe::launch_combine(a, stream);
+    if (e != cudaSuccess) { set_error("combine launch", e); return MOE_ERR_CUDA; }
+    return MOE_OK;
+  }
   if (algo == MOE_ALGO_SIMT) {
     e = moe::launch_expert_simt(a, stream);
     if (e != cudaSuccess) { set_error("simt launch", e); return MOE_ERR_CUDA; }
+    if (stages & kStageUnroute) {
+      e = moe::launch_combine(a, stream);
+      if (e != cudaSuccess) { set_error("combine launch", e); return MOE_ERR_CUDA; }
+    }
     return MOE_OK;
   }
   DeviceInfo di;
@@ -331,9 +344,24 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     e = moe::launch_expert_tc(a, tm13, tm2, di.num_sms, stream);
     if (e != cudaSuccess) { set_error("expert_tc launch", e); return MOE_ERR_CUDA; }
   }
-  e = moe::launch_combine(a, stream);
-  if (e != cudaSuccess) { set_error("combine launch", e); return MOE_ERR_CUDA; }
+  if (stages & kStageUnroute) {
+    e = moe::launch_combine(a, stream);
+    if (e != cudaSuccess) { set_error("combine launch", e); return MOE_ERR_CUDA; }
+  }
   return MOE_OK;
+}
+
+int moe_forward_expert_kernels(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
+                               float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+                               void* workspace, size_t workspace_bytes, int algo, moe_stream_t stream) {
+  return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, nullptr,
+                              nullptr, workspace, workspace_bytes, algo, nullptr, stream, kStageExperts);
+}
+
+int moe_forward_unroute(const moe_shape* shape, const void* residual, void* out, void* workspace,
+                        size_t workspace_bytes, moe_stream_t stream) {
+  return forward_experts_impl(shape, nullptr, nullptr, 0.f, nullptr, nullptr, 0.f, residual, out, workspace,
+                              workspace_bytes, MOE_ALGO_AUTO, nullptr, stream, kStageUnroute);
 }
 
 int moe_forward_experts(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,

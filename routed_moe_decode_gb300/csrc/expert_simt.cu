@@ -1,5 +1,6 @@
-// CUDA-core expert path: one launch per stage (gate/up, down, un-route), one warp per
-// weight row, FP32 FMA on weights dequantised through a shared-memory E2M1 table.
+// CUDA-core expert path: one launch per stage (gate/up, down; the shared un-route kernel
+// follows), one warp per weight row, FP32 FMA on weights dequantised through a
+// shared-memory E2M1 table.
 //
 // Kept as the ablation baseline of the tensor-core kernel: it reads each touched
 // expert's weights once per group of 8 routed rows (unique-expert reuse without the
@@ -142,22 +143,6 @@ __global__ void __launch_bounds__(256) simt_down_kernel(ExpertArgs a) {
   }
 }
 
-// out[t] = residual[t] + sum_{j<k} w_{t,j} y_{t,j}, slots in order.
-__global__ void __launch_bounds__(256) simt_combine_kernel(ExpertArgs a) {
-  const int t = blockIdx.x;
-  for (int r = threadIdx.x; r < a.d; r += blockDim.x) {
-    float accum = 0.f;
-    for (int j = 0; j < a.k; ++j) {
-      const int pos = __ldg(a.route_pos + t * a.k + j);
-      if (pos < 0) continue;
-      accum += __ldg(a.route_w + t * a.k + j) * a.y[static_cast<size_t>(pos) * a.d + r];
-    }
-    const size_t o = static_cast<size_t>(t) * a.d + r;
-    const float res = a.residual ? __bfloat162float(a.residual[o]) : 0.f;
-    a.out[o] = __float2bfloat16_rn(res + accum);
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_expert_simt(const ExpertArgs& a, cudaStream_t stream) {
@@ -165,9 +150,6 @@ cudaError_t launch_expert_simt(const ExpertArgs& a, cudaStream_t stream) {
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   simt_down_kernel<<<dim3(a.E, (a.d + 31) / 32), 256, 0, stream>>>(a);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  simt_combine_kernel<<<a.T, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -89,6 +89,27 @@ def test_fused_front_matches_separate_calls(T, d, F, E, k):
     assert moe.plan_summary(fused.shape, fused.ws) == moe.plan_summary(sep.shape, sep.ws)
 
 
+@pytest.mark.parametrize("algo", ["mma", "tcgen05", "simt"])
+def test_split_expert_and_unroute_calls(algo):
+    # moe_forward_expert_kernels + moe_forward_unroute == moe_forward_experts, bit for bit
+    import routed_moe_decode_gb300 as moe
+    cfg = mi.CONFIGS["b8"]
+    inp = config_inputs("b8")
+    w = device_weights(inp, "cuda")
+    layer = moe.MoeLayer(cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k, algo=ALGOS[algo])
+    logits = torch.from_numpy(inp["logits"]).cuda()
+    hidden = bf16_tensor(inp["hidden"], "cuda")
+    res = bf16_tensor(inp["residual"], "cuda")
+    ref = layer(logits, hidden, w, res)
+    moe.forward_prepare(layer.shape, hidden, layer.ws)
+    moe.forward_expert_kernels(layer.shape, w, layer.ws, ALGOS[algo])
+    out = torch.empty_like(ref)
+    moe.forward_unroute(layer.shape, res, out, layer.ws)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(out, ref)
+
+
 @pytest.mark.parametrize("name", ["tiny", "b1", "b8", "b64", "prefill"])
 def test_layer_parity_tcgen05(name):
     cfg = mi.CONFIGS[name]
