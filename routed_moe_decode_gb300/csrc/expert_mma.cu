@@ -60,7 +60,6 @@ struct Smem {
   TaskEntry task[kTaskSlots];
   uint64_t full_a[kStagesA];
   uint64_t empty_a[kStagesA];
-  uint64_t full_b[kStagesB];
   uint64_t empty_b[kStagesB];
   uint64_t sc_full[2];
   uint64_t sc_empty[2];
@@ -208,14 +207,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
+    // a chunk's stage is full once both producers have arrived and all its bytes (codes
+    // and activation tiles) have landed
     for (int i = 0; i < kStagesA; ++i) {
-      mbar_init(smem_addr(&sm.full_a[i]), 1);
+      mbar_init(smem_addr(&sm.full_a[i]), 2);
       mbar_init(smem_addr(&sm.empty_a[i]), kComputeWarps);
     }
-    for (int i = 0; i < kStagesB; ++i) {
-      mbar_init(smem_addr(&sm.full_b[i]), 1);
-      mbar_init(smem_addr(&sm.empty_b[i]), kComputeWarps);
-    }
+    for (int i = 0; i < kStagesB; ++i) mbar_init(smem_addr(&sm.empty_b[i]), kComputeWarps);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&sm.sc_full[i]), 1);
       mbar_init(smem_addr(&sm.sc_empty[i]), kComputeWarps);
@@ -347,8 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------- activation producer: 8-row tiles, one bulk copy per routed row -------------
-    int stage = 0, n = 0, issued = 0, chunk_seq = 0;
-    uint32_t phase = 0;
+    // The copies complete on the weight stage's barrier of the same chunk (the chunk order
+    // is the task order in both producers), so compute warps wait on one barrier per chunk.
+    int stage = 0, n = 0, issued = 0, chunk_seq = 0, stage_a = 0;
+    uint32_t phase = 0, phase_a = 0;
     bool ok = true;
     while (ok) {
       TaskEntry te;
@@ -379,12 +379,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int nt = (rows + kTileRows - 1) / kTileRows;
       for (int c = 0; ok && c < nck; ++c) {
+        // the chunk's weight stage must be free before this chunk's bytes are announced on it
+        if (!warp_wait(smem_addr(&sm.empty_a[stage_a]), phase_a ^ 1u, sm, a.status)) { ok = false; break; }
+        const uint32_t fa = smem_addr(&sm.full_a[stage_a]);
+        if (lane == 0) mbar_arrive_expect_tx(fa, static_cast<uint32_t>(rows) * (2 * kChunk));
         for (int t = 0; t < nt; ++t) {
           if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
           const int trows = min(kTileRows, rows - t * kTileRows);
-          const uint32_t fb = smem_addr(&sm.full_b[stage]);
-          if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(trows) * (2 * kChunk));
-          __syncwarp();
           // lanes 0..trows-1 copy their tile row: routed row r = 8t + lane
           const int r = t * kTileRows + lane;
           const __half* p0 = reinterpret_cast<const __half*>(
@@ -393,24 +394,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src1), r & 31));
           if (lane < trows) {
             const __half* src = (r < 32 ? p0 : p1) + c * kChunk;
-            bulk_copy_g2s(ringb0 + stage * kStageB + lane * kRowPitchB, src, 2 * kChunk, fb);
+            bulk_copy_g2s(ringb0 + stage * kStageB + lane * kRowPitchB, src, 2 * kChunk, fa);
           }
           ++issued;
           if (++stage == kStagesB) { stage = 0; phase ^= 1u; }
         }
         if (lane == 0) trace_ev(a, 1, tcnt, 4, chunk_seq);
         ++chunk_seq;
+        if (++stage_a == kStagesA) { stage_a = 0; phase_a ^= 1u; }
       }
     }
+    // drain: every copy this warp started has landed before the CTA exits
     if (lane == 0) {
-      int st = stage;
-      uint32_t ph = phase;
-      for (int i = 0; i < min(issued, kStagesB); ++i) {
-        if (--st < 0) { st = kStagesB - 1; ph ^= 1u; }
+      int st = stage_a;
+      uint32_t ph = phase_a;
+      for (int i = 0; i < min(chunk_seq, kStagesA); ++i) {
+        if (--st < 0) { st = kStagesA - 1; ph ^= 1u; }
         const long long t0 = clock64();
-        while (!mbar_try_wait(smem_addr(&sm.full_b[st]), ph) && clock64() - t0 < kTimeoutCycles) {}
+        while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kTimeoutCycles) {}
       }
     }
+    (void)issued;
   } else if (warp == 2) {
     // ------------- publisher: release each finished gate/up task's h rows -------------
     int n = 0, gu_n = 0;
@@ -441,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int fr = frag_row(g);
     int tcnt3 = 0, tcnt6 = 0;
     int stage_a = 0, stage_b = 0, n = 0, gu_n = 0, chunk_seq = 0;
-    uint32_t phase_a = 0, phase_b = 0;
+    uint32_t phase_a = 0;
     bool ok = true;
     while (ok) {
       TaskEntry te;
@@ -479,19 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.empty_a[stage_a]));
         if (++stage_a == kStagesA) { stage_a = 0; phase_a ^= 1u; }
-        if (c + 1 < nck) {
+        // The next chunk's stage is full only once its activation tiles have landed too.  If
+        // two chunks' tiles do not fit in the tile ring together, they can land only after this
+        // chunk releases its tiles, so the next chunk is then loaded after the release.
+        const bool early = 2 * nt <= kStagesB;
+        if (early && c + 1 < nck) {
           if (!warp_wait(smem_addr(&sm.full_a[stage_a]), phase_a, sm, a.status)) { ok = false; break; }
           load_chunk_codes(&sm.ring_a[stage_a][0], sbase, lra, lrb, P, c + 1, q, next);
-        }
-        // the chunk's activation tiles (the producer runs ahead, so they are normally there)
-        {
-          int sbt = stage_b;
-          uint32_t pbt = phase_b;
-          for (int t = 0; t < nt; ++t) {
-            if (!warp_wait(smem_addr(&sm.full_b[sbt]), pbt, sm, a.status)) { ok = false; break; }
-            if (++sbt == kStagesB) { sbt = 0; pbt ^= 1u; }
-          }
-          if (!ok) break;
         }
         if (cw == 0 && lane == 0) trace_ev(a, 6, tcnt6, 13, chunk_seq);
         // Per sub-chunk h: activation fragments first (their latency overlaps the
@@ -578,7 +576,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         stage_b += nt;
-        if (stage_b >= kStagesB) { stage_b -= kStagesB; phase_b ^= 1u; }
+        if (stage_b >= kStagesB) stage_b -= kStagesB;
+        if (!early && c + 1 < nck) {
+          if (!warp_wait(smem_addr(&sm.full_a[stage_a]), phase_a, sm, a.status)) { ok = false; break; }
+          load_chunk_codes(&sm.ring_a[stage_a][0], sbase, lra, lrb, P, c + 1, q, next);
+        }
         if (cw == 0 && lane == 0) trace_ev(a, 2, tcnt, 6, chunk_seq);
         ++chunk_seq;
       }
