@@ -37,14 +37,15 @@ MOE_API int moe_selftest_tma(const uint8_t* src, int rows, int row_bytes, int x,
  * kind::f16 MMAs with FP32 accumulation, result D [128, 16] FP32 (row-major) = A B^T. */
 MOE_API int moe_selftest_mma(const void* A, const void* B, float* D, moe_stream_t stream);
 
-/* The tensor-core expert kernel and the un-route kernel exactly as moe_forward_experts
- * runs them (after moe_plan and moe_forward_prepare), with a timeline recorded into
+/* The expert kernel and the un-route kernel exactly as moe_forward_experts runs them with
+ * MOE_ALGO_AUTO (after moe_plan and moe_forward_prepare), with a timeline recorded into
  * `trace`: per CTA 8 roles x 128 uint64 events (event code << 56 | index << 40 | low 40
  * bits of %globaltimer in ns); zero-initialise the buffer (multiProcessorCount x 8192 bytes).
- * Roles: 0 weight producer (1 task published, 2 chunk issued), 1 activation producer
- * (3 readiness met, 4 chunk issued), 2 first dequantisation warp (5 chunk landed, 6 chunk in
- * tensor memory), 3 MMA (7 chunk issued), 4 epilogue (8 accumulator ready, 9 task done),
- * 5 CTA (10 start, 11 end). */
+ * Warp-MMA kernel: role 0 weight producer (1 task published, 2 chunk issued), 1 activation
+ * producer (3 readiness met, 4 chunk issued), 4 publisher (9 gate/up task released),
+ * 5 CTA (10 start, 11 end).  tcgen05 kernel: roles 0 and 1 as above, 2 first
+ * dequantisation warp (5 chunk landed, 6 chunk in tensor memory), 3 MMA (7 chunk issued),
+ * 4 epilogue (8 accumulator ready, 9 task done), 5 CTA (10 start, 11 end). */
 MOE_API int moe_selftest_expert_trace(const moe_shape* shape, const uint8_t* w13_codes,
                                       const uint8_t* w13_scales, float w13_scale,
                                       const uint8_t* w2_codes, const uint8_t* w2_scales,

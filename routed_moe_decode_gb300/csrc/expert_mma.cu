@@ -172,6 +172,146 @@ __device__ __forceinline__ void dequant32(const uint4 codes, uint32_t scale_pair
   }
 }
 
+// Per-warp pipeline position of the compute warps.
+struct ComputeState {
+  int stage_a, stage_b;
+  uint32_t phase_a;
+};
+
+// The chunk loop of one task for one compute warp, one instantiation per accumulation
+// layout so that a task runs one tight loop.  acc receives, per 8-row tile t, the FP32
+// partial products of fragment rows g / g + 8 with the task's routed rows.
+//   MODE 1 (one tile):  the 16 k-steps of a chunk go to 8 independent accumulators;
+//   MODE 2 (two tiles): 4 accumulators per tile;
+//   MODE 0 (otherwise, and every pass of a multi-pass expert): one accumulator per tile,
+//                       tiles in pairs (the second of an odd last pair multiplies zeros
+//                       into an accumulator that is never stored).
+// The independent sets are summed (fixed order) before returning.  Returns false when a
+// bounded wait gave up.
+template <int MODE>
+__device__ __forceinline__ bool run_chunks(Smem& sm, const ExpertArgs& a, ComputeState& cs, float (&acc)[kMaxTiles][4],
+                                           const uint8_t* sbase, int lra, int lrb, int P, int nck, int nt, int rows,
+                                           int g, int q) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int t = 0; t < kMaxTiles; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+  // codes and scales of chunk c are loaded into registers during chunk c - 1, so their
+  // shared-memory latency overlaps the previous chunk's MMAs.  A chunk's stage is full only
+  // once its activation tiles have landed too; if two chunks' tiles do not fit in the tile
+  // ring together, they land only after this chunk releases its tiles, so the next chunk is
+  // then loaded after the release.
+  const bool early = MODE != 0 || 2 * nt <= kStagesB;
+  ChunkCodes next;
+  if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, sm, a.status)) return false;
+  load_chunk_codes(&sm.ring_a[cs.stage_a][0], sbase, lra, lrb, P, 0, q, next);
+  for (int c = 0; c < nck; ++c) {
+    const ChunkCodes cur = next;
+    // the stage's bytes are in registers: hand it back to the producer
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&sm.empty_a[cs.stage_a]));
+    if (++cs.stage_a == kStagesA) { cs.stage_a = 0; cs.phase_a ^= 1u; }
+    if (early && c + 1 < nck) {
+      if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, sm, a.status)) return false;
+      load_chunk_codes(&sm.ring_a[cs.stage_a][0], sbase, lra, lrb, P, c + 1, q, next);
+    }
+    // Per sub-chunk h: activation fragments first (their latency overlaps the
+    // dequantisation), then the 32 weights per row of this thread, then the MMAs.
+    // MMA k-step (h, j, x): A registers 4j + 2x, 4j + 2x + 1, B word pair x of piece j.
+    const uint8_t* b0 = &sm.ring_b[cs.stage_b][0];
+    if constexpr (MODE == 1) {
+      const bool live = g < rows;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint4 xb[4];
+        load_b_frag(b0, g, q, h, live, xb);
+        uint32_t fa[16], fb[16];
+        dequant32(cur.ca[h], cur.sa[h], fa);
+        dequant32(cur.cb[h], cur.sb[h], fb);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          mma_16816(acc[2 * j], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], xb[j].x, xb[j].y);
+          mma_16816(acc[2 * j + 1], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], xb[j].z, xb[j].w);
+        }
+      }
+    } else if constexpr (MODE == 2) {
+      const uint8_t* b1 = &sm.ring_b[cs.stage_b + 1 == kStagesB ? 0 : cs.stage_b + 1][0];
+      const bool live0 = g < rows, live1 = g < rows - kTileRows;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint4 x0[4], x1[4];
+        load_b_frag(b0, g, q, h, live0, x0);
+        load_b_frag(b1, g, q, h, live1, x1);
+        uint32_t fa[16], fb[16];
+        dequant32(cur.ca[h], cur.sa[h], fa);
+        dequant32(cur.cb[h], cur.sb[h], fb);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int ch = (2 * j) & 3;
+          mma_16816(acc[ch], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], x0[j].x, x0[j].y);
+          mma_16816(acc[4 + ch], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], x1[j].x, x1[j].y);
+          mma_16816(acc[ch + 1], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], x0[j].z, x0[j].w);
+          mma_16816(acc[5 + ch], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], x1[j].z, x1[j].w);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t fa[16], fb[16];
+        dequant32(cur.ca[h], cur.sa[h], fa);
+        dequant32(cur.cb[h], cur.sb[h], fb);
+#pragma unroll
+        for (int tp = 0; tp < kMaxTiles / 2; ++tp) {
+          if (2 * tp < nt) {
+            const int t0 = 2 * tp, t1 = 2 * tp + 1;
+            const uint8_t* s0 = &sm.ring_b[(cs.stage_b + t0) % kStagesB][0];
+            const uint8_t* s1 = &sm.ring_b[(cs.stage_b + t1) % kStagesB][0];
+            const bool live0 = g < rows - t0 * kTileRows;
+            const bool live1 = t1 < nt && g < rows - t1 * kTileRows;
+            uint4 x0[4], x1[4];
+            load_b_frag(s0, g, q, h, live0, x0);
+            load_b_frag(s1, g, q, h, live1, x1);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              mma_16816(acc[t0], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], x0[j].x, x0[j].y);
+              mma_16816(acc[t1], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], x1[j].x, x1[j].y);
+              mma_16816(acc[t0], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], x0[j].z, x0[j].w);
+              mma_16816(acc[t1], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], x1[j].z, x1[j].w);
+            }
+          }
+        }
+      }
+    }
+    // the chunk's activation tiles are consumed
+    __syncwarp();
+    if (lane == 0) {
+      int sbt = cs.stage_b;
+      for (int t = 0; t < nt; ++t) {
+        mbar_arrive(smem_addr(&sm.empty_b[sbt]));
+        if (++sbt == kStagesB) sbt = 0;
+      }
+    }
+    cs.stage_b += nt;
+    if (cs.stage_b >= kStagesB) cs.stage_b -= kStagesB;
+    if (!early && c + 1 < nck) {
+      if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, sm, a.status)) return false;
+      load_chunk_codes(&sm.ring_a[cs.stage_a][0], sbase, lra, lrb, P, c + 1, q, next);
+    }
+  }
+  // fold the independent accumulator sets into one per tile
+  if constexpr (MODE == 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      acc[0][i] = ((acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i])) + ((acc[4][i] + acc[5][i]) + (acc[6][i] + acc[7][i]));
+  } else if constexpr (MODE == 2) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[0][i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);
+      acc[1][i] = (acc[4][i] + acc[5][i]) + (acc[6][i] + acc[7][i]);
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
 __device__ __forceinline__ __half h_store_value(float h, int* status) {
@@ -443,9 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cw = warp - kFirstCompute;  // 0..7
     const int g = lane >> 2, q = lane & 3;
     const int fr = frag_row(g);
-    int tcnt3 = 0, tcnt6 = 0;
-    int stage_a = 0, stage_b = 0, n = 0, gu_n = 0, chunk_seq = 0;
-    uint32_t phase_a = 0;
+    ComputeState cs{0, 0, 0u};
+    int n = 0, gu_n = 0;
     bool ok = true;
     while (ok) {
       TaskEntry te;
@@ -469,135 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(smem_addr(&sm.sc_full[sn]), static_cast<uint32_t>((n >> 1) & 1), sm, a.status)) break;
       const uint8_t* sbase = &sm.scales[sn][0];
       float acc[kMaxTiles][4];
-#pragma unroll
-      for (int t = 0; t < kMaxTiles; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-      // codes and scales of chunk c are loaded into registers during chunk c - 1, so their
-      // shared-memory latency overlaps the previous chunk's MMAs
-      ChunkCodes next;
-      if (!warp_wait(smem_addr(&sm.full_a[stage_a]), phase_a, sm, a.status)) break;
-      load_chunk_codes(&sm.ring_a[stage_a][0], sbase, lra, lrb, P, 0, q, next);
-      for (int c = 0; c < nck; ++c) {
-        if (cw == 0 && lane == 0) trace_ev(a, 2, tcnt, 5, chunk_seq);
-        const ChunkCodes cur = next;
-        // the stage's bytes are in registers: hand it back to the producer
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sm.empty_a[stage_a]));
-        if (++stage_a == kStagesA) { stage_a = 0; phase_a ^= 1u; }
-        // The next chunk's stage is full only once its activation tiles have landed too.  If
-        // two chunks' tiles do not fit in the tile ring together, they can land only after this
-        // chunk releases its tiles, so the next chunk is then loaded after the release.
-        const bool early = 2 * nt <= kStagesB;
-        if (early && c + 1 < nck) {
-          if (!warp_wait(smem_addr(&sm.full_a[stage_a]), phase_a, sm, a.status)) { ok = false; break; }
-          load_chunk_codes(&sm.ring_a[stage_a][0], sbase, lra, lrb, P, c + 1, q, next);
-        }
-        if (cw == 0 && lane == 0) trace_ev(a, 6, tcnt6, 13, chunk_seq);
-        // Per sub-chunk h: activation fragments first (their latency overlaps the
-        // dequantisation), then the 32 weights per row of this thread, then the MMAs.
-        // MMA k-step (h, j, x): A registers 4j + 2x, 4j + 2x + 1, B word pair x of piece j.
-        // Few tiles leave accumulator registers free: their k-steps are spread over
-        // independent accumulators (8 for one tile, 4 per tile for two) so that consecutive
-        // MMAs do not wait on each other; the sets are summed after the task.
-        const uint8_t* b0 = &sm.ring_b[stage_b][0];
-        if (mode == 1) {
-          const bool live = g < rows;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint4 xb[4];
-            load_b_frag(b0, g, q, h, live, xb);
-            uint32_t fa[16], fb[16];
-            dequant32(cur.ca[h], cur.sa[h], fa);
-            dequant32(cur.cb[h], cur.sb[h], fb);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              mma_16816(acc[2 * j], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], xb[j].x, xb[j].y);
-              mma_16816(acc[2 * j + 1], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], xb[j].z,
-                        xb[j].w);
-            }
-          }
-        } else if (mode == 2) {
-          const uint8_t* b1 = &sm.ring_b[stage_b + 1 == kStagesB ? 0 : stage_b + 1][0];
-          const bool live0 = g < rows, live1 = g < rows - kTileRows;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint4 x0[4], x1[4];
-            load_b_frag(b0, g, q, h, live0, x0);
-            load_b_frag(b1, g, q, h, live1, x1);
-            uint32_t fa[16], fb[16];
-            dequant32(cur.ca[h], cur.sa[h], fa);
-            dequant32(cur.cb[h], cur.sb[h], fb);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int ch = (2 * j) & 3;
-              mma_16816(acc[ch], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], x0[j].x, x0[j].y);
-              mma_16816(acc[4 + ch], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], x1[j].x, x1[j].y);
-              mma_16816(acc[ch + 1], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], x0[j].z, x0[j].w);
-              mma_16816(acc[5 + ch], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], x1[j].z, x1[j].w);
-            }
-          }
-        } else {
-          // tiles in pairs, the two accumulators interleaved (the second of an odd last pair
-          // multiplies zeros into an accumulator that is never stored)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t fa[16], fb[16];
-            dequant32(cur.ca[h], cur.sa[h], fa);
-            dequant32(cur.cb[h], cur.sb[h], fb);
-#pragma unroll
-            for (int tp = 0; tp < kMaxTiles / 2; ++tp) {
-              if (2 * tp < nt) {
-                const int t0 = 2 * tp, t1 = 2 * tp + 1;
-                const uint8_t* s0 = &sm.ring_b[(stage_b + t0) % kStagesB][0];
-                const uint8_t* s1 = &sm.ring_b[(stage_b + t1) % kStagesB][0];
-                const bool live0 = g < rows - t0 * kTileRows;
-                const bool live1 = t1 < nt && g < rows - t1 * kTileRows;
-                uint4 x0[4], x1[4];
-                load_b_frag(s0, g, q, h, live0, x0);
-                load_b_frag(s1, g, q, h, live1, x1);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  mma_16816(acc[t0], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], x0[j].x, x0[j].y);
-                  mma_16816(acc[t1], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], x1[j].x, x1[j].y);
-                  mma_16816(acc[t0], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], x0[j].z, x0[j].w);
-                  mma_16816(acc[t1], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], x1[j].z, x1[j].w);
-                }
-              }
-            }
-          }
-        }
-        if (cw == 0 && lane == 0) trace_ev(a, 3, tcnt3, 12, chunk_seq);
-        // the chunk's activation tiles are consumed
-        __syncwarp();
-        if (lane == 0) {
-          int sbt = stage_b;
-          for (int t = 0; t < nt; ++t) {
-            mbar_arrive(smem_addr(&sm.empty_b[sbt]));
-            if (++sbt == kStagesB) sbt = 0;
-          }
-        }
-        stage_b += nt;
-        if (stage_b >= kStagesB) stage_b -= kStagesB;
-        if (!early && c + 1 < nck) {
-          if (!warp_wait(smem_addr(&sm.full_a[stage_a]), phase_a, sm, a.status)) { ok = false; break; }
-          load_chunk_codes(&sm.ring_a[stage_a][0], sbase, lra, lrb, P, c + 1, q, next);
-        }
-        if (cw == 0 && lane == 0) trace_ev(a, 2, tcnt, 6, chunk_seq);
-        ++chunk_seq;
-      }
-      if (!ok) break;
-      // fold the independent accumulator sets into one per tile
-      if (mode == 1) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          acc[0][i] = ((acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i])) +
-                      ((acc[4][i] + acc[5][i]) + (acc[6][i] + acc[7][i]));
-      } else if (mode == 2) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[0][i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);
-          acc[1][i] = (acc[4][i] + acc[5][i]) + (acc[6][i] + acc[7][i]);
-        }
-      }
+      if (mode == 1) ok = run_chunks<1>(sm, a, cs, acc, sbase, lra, lrb, P, nck, nt, rows, g, q);
+      else if (mode == 2) ok = run_chunks<2>(sm, a, cs, acc, sbase, lra, lrb, P, nck, nt, rows, g, q);
+      else ok = run_chunks<0>(sm, a, cs, acc, sbase, lra, lrb, P, nck, nt, rows, g, q);
       if (!ok) break;
       // the task's scales are no longer needed
       __syncwarp();
