@@ -372,6 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_s13);
     prefetch_tmap(&tm_s2);
   }
+  // everything above is local to the CTA; the plan and the counters come from the
+  // preceding kernel
+  pdl_wait();
+  pdl_launch_dependents();
   __syncthreads();
   const uint32_t ringa0 = smem_addr(&sm.ring_a[0][0]);
   const uint32_t ringb0 = smem_addr(&sm.ring_b[0][0]);
@@ -677,8 +681,8 @@ cudaError_t launch_expert_mma(const ExpertArgs& a, const CUtensorMap& tm_w13, co
   cudaError_t err = cudaFuncSetAttribute(expert_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  expert_mma_kernel<<<num_sms, kThreads, smem, stream>>>(tm_w13, tm_w2, tm_s13, tm_s2, a);
-  return cudaGetLastError();
+  return launch_pdl(expert_mma_kernel, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, tm_s13, tm_s2,
+                    a);
 }
 
 }  // namespace moe

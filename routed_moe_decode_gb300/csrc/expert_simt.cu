@@ -72,6 +72,7 @@ __device__ void row_dot(const uint8_t* codes, const uint8_t* scales, int K, cons
 
 __global__ void __launch_bounds__(256) simt_gateup_kernel(ExpertArgs a) {
   __shared__ float lut[16];
+  pdl_wait();
   if (threadIdx.x < 16) lut[threadIdx.x] = e2m1_from_bits(threadIdx.x);
   __syncthreads();
   const int u = blockIdx.x;
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(256) simt_gateup_kernel(ExpertArgs a) {
 
 __global__ void __launch_bounds__(256) simt_down_kernel(ExpertArgs a) {
   __shared__ float lut[16];
+  pdl_wait();
   if (threadIdx.x < 16) lut[threadIdx.x] = e2m1_from_bits(threadIdx.x);
   __syncthreads();
   const int u = blockIdx.x;

@@ -191,6 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_w13);
     prefetch_tmap(&tm_w2);
   }
+  // everything above is local to the CTA; the plan and the counters come from the
+  // preceding kernel
+  pdl_wait();
+  pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -565,8 +569,7 @@ cudaError_t launch_expert_tc(const ExpertArgs& a, const CUtensorMap& tm_w13, con
   cudaError_t err = cudaFuncSetAttribute(expert_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  expert_tc_kernel<<<num_sms, kThreads, smem, stream>>>(tm_w13, tm_w2, a);
-  return cudaGetLastError();
+  return launch_pdl(expert_tc_kernel, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, a);
 }
 
 // ---------------------------------------------------------------------------------
@@ -575,6 +578,8 @@ cudaError_t launch_expert_tc(const ExpertArgs& a, const CUtensorMap& tm_w13, con
 // order).  Each thread owns 4 consecutive columns of one token.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x;
   const int r = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
   if (r >= a.d) return;
@@ -610,8 +615,7 @@ __global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
 
 cudaError_t launch_combine(const ExpertArgs& a, cudaStream_t stream) {
   const dim3 grid(a.T, (a.d / 4 + 255) / 256);
-  combine_kernel<<<grid, 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid, dim3(256), 0, stream, a);
 }
 
 // ---------------------------------------------------------------------------------
@@ -619,6 +623,8 @@ cudaError_t launch_combine(const ExpertArgs& a, cudaStream_t stream) {
 // FP16 (the tensor-core operand type), flagging values outside the FP16 range.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) prep_kernel(PrepArgs p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const size_t gtid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t i = gtid; i < static_cast<size_t>(p.E); i += nthreads) p.ready[i] = 0u;
@@ -653,8 +659,7 @@ cudaError_t launch_prep(const PrepArgs& p, cudaStream_t stream) {
   int blocks = static_cast<int>((work + 255) / 256);
   if (blocks > 1184) blocks = 1184;
   if (blocks < 1) blocks = 1;
-  prep_kernel<<<blocks, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(prep_kernel, dim3(blocks), dim3(256), 0, stream, p);
 }
 
 }  // namespace moe

@@ -127,6 +127,12 @@ MOE_DEVICE bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Programmatic dependent launch: every kernel of the library may start while the previous
+// kernel in its stream is finishing; pdl_wait() blocks until that kernel has completed and
+// its writes are visible, and must precede any access to the workspace, inputs or outputs.
+// pdl_launch_dependents() lets the next kernel in the stream start early (it still waits).
+MOE_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_DEVICE void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 MOE_DEVICE void fence_barrier_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 MOE_DEVICE void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 MOE_DEVICE void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }

@@ -78,6 +78,24 @@ struct ExpertArgs {
 constexpr int kTraceRoles = 8;
 constexpr int kTracePerRole = 128;
 
+// Launch `kernel` as a programmatic dependent of the preceding work in `stream` (it may
+// begin while its predecessor finishes; the kernels order themselves with pdl_wait).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* weights,
                               cudaStream_t stream);
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);

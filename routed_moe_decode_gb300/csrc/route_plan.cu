@@ -92,6 +92,8 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
 template <int NPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int32_t* __restrict__ ids, float* __restrict__ weights) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
   route_token<NPL>(logits, t, E, k, ids, weights);
@@ -101,13 +103,10 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
                               cudaStream_t stream) {
   const int npl = (E + 31) / 32;
   const dim3 grid((T + 7) / 8), block(256);
-  if (npl <= 1) route_topk_kernel<1><<<grid, block, 0, stream>>>(logits, T, E, k, ids, weights);
-  else if (npl <= 2) route_topk_kernel<2><<<grid, block, 0, stream>>>(logits, T, E, k, ids, weights);
-  else if (npl <= 4) route_topk_kernel<4><<<grid, block, 0, stream>>>(logits, T, E, k, ids, weights);
-  else if (npl <= 8) route_topk_kernel<8><<<grid, block, 0, stream>>>(logits, T, E, k, ids, weights);
-  else if (npl <= 16) route_topk_kernel<16><<<grid, block, 0, stream>>>(logits, T, E, k, ids, weights);
-  else route_topk_kernel<32><<<grid, block, 0, stream>>>(logits, T, E, k, ids, weights);
-  return cudaGetLastError();
+  void (*kern)(const float*, int, int, int, int32_t*, float*) =
+      npl <= 1 ? route_topk_kernel<1> : npl <= 2 ? route_topk_kernel<2> : npl <= 4 ? route_topk_kernel<4>
+      : npl <= 8 ? route_topk_kernel<8> : npl <= 16 ? route_topk_kernel<16> : route_topk_kernel<32>;
+  return launch_pdl(kern, grid, block, 0, stream, logits, T, E, k, ids, weights);
 }
 
 // Exclusive scan of one int per thread across a 1024-thread block; returns the total.
@@ -245,7 +244,11 @@ __device__ __forceinline__ void plan_block(const PlanArgs& a) {
   }
 }
 
-__global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) { plan_block(a); }
+__global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
+  plan_block(a);
+}
 
 // ---------------------------------------------------------------------------------
 // Fused front for moderate T * k: each 1024-thread CTA routes 32 tokens (one per warp) and
@@ -255,6 +258,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) { plan_block(a);
 template <int NPL>
 __global__ void __launch_bounds__(1024) front_kernel(FrontArgs f) {
   __shared__ int s_last;
+  pdl_wait();
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int t = blockIdx.x * 32 + warp;
   const PlanArgs& a = f.plan;
@@ -301,18 +306,13 @@ __global__ void __launch_bounds__(1024) front_kernel(FrontArgs f) {
 cudaError_t launch_front(const FrontArgs& f, cudaStream_t stream) {
   const int npl = (f.plan.E + 31) / 32;
   const dim3 grid((f.plan.T + 31) / 32), block(1024);
-  if (npl <= 1) front_kernel<1><<<grid, block, 0, stream>>>(f);
-  else if (npl <= 2) front_kernel<2><<<grid, block, 0, stream>>>(f);
-  else if (npl <= 4) front_kernel<4><<<grid, block, 0, stream>>>(f);
-  else if (npl <= 8) front_kernel<8><<<grid, block, 0, stream>>>(f);
-  else if (npl <= 16) front_kernel<16><<<grid, block, 0, stream>>>(f);
-  else front_kernel<32><<<grid, block, 0, stream>>>(f);
-  return cudaGetLastError();
+  void (*kern)(FrontArgs) = npl <= 1 ? front_kernel<1> : npl <= 2 ? front_kernel<2> : npl <= 4 ? front_kernel<4>
+                           : npl <= 8 ? front_kernel<8> : npl <= 16 ? front_kernel<16> : front_kernel<32>;
+  return launch_pdl(kern, grid, block, 0, stream, f);
 }
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
-  plan_kernel<<<1, 1024, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, a);
 }
 
 }  // namespace moe
