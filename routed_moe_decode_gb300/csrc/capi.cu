@@ -92,21 +92,13 @@ int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint
 int encode_scales_map(CUtensorMap* tm, const void* base, uint32_t row_bytes, uint64_t rows, uint32_t box_rows) {
   EncodeTiledFn enc = nullptr;
   if (get_encoder(&enc) != MOE_OK) { snprintf(g_last_error, sizeof g_last_error, "no cuTensorMapEncodeTiled"); return MOE_ERR_CUDA; }
-  CUtensorMapSwizzle swz;
-  switch (row_bytes) {
-    case 16: swz = CU_TENSOR_MAP_SWIZZLE_NONE; break;
-    case 32: swz = CU_TENSOR_MAP_SWIZZLE_32B; break;
-    case 64: swz = CU_TENSOR_MAP_SWIZZLE_64B; break;
-    case 128: swz = CU_TENSOR_MAP_SWIZZLE_128B; break;
-    default: return MOE_ERR_INVALID_ARG;
-  }
-  if (box_rows == 0 || box_rows > 256) return MOE_ERR_INVALID_ARG;
+  if (row_bytes < 16 || row_bytes % 16 || box_rows == 0 || box_rows > 256) return MOE_ERR_INVALID_ARG;
   cuuint64_t dims[2] = {row_bytes, rows};
   cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {row_bytes, box_rows};
+  cuuint32_t box[2] = {16, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
@@ -336,7 +328,7 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
                                 static_cast<uint64_t>(shape->E) * 2 * shape->ffn, 64);
     if (rc != MOE_OK) return rc;
     rc = moe::encode_scales_map(&ts2, w2_scales, static_cast<uint32_t>(shape->ffn / 16),
-                                static_cast<uint64_t>(shape->E) * shape->d, 128);
+                                static_cast<uint64_t>(shape->E) * shape->d, 64);
     if (rc != MOE_OK) return rc;
     e = moe::launch_expert_mma(a, tm13, tm2, ts13, ts2, di.num_sms, stream);
     if (e != cudaSuccess) { set_error("expert_mma launch", e); return MOE_ERR_CUDA; }

@@ -9,9 +9,9 @@
 // pages).
 //
 // Structure (one resident CTA per SM, tasks from the plan's task table via tickets):
-//   warp 0      task fetcher + weight producer: per task one TMA tile of the task's block
-//               scales (swizzled like the codes), then per 256-K chunk two TMA tiles of
-//               E2M1 codes (64 rows x 128 B each, 128-byte swizzle) into a ring;
+//   warp 0      task fetcher + weight producer: per 256-K chunk two TMA tiles of E2M1 codes
+//               (64 rows x 128 B each, 128-byte swizzle) and two of the chunk's block scales
+//               (64 rows x 16 B) into one stage of a ring, so short tasks never starve it;
 //   warp 1      activation producer: per chunk and 8-row tile, one bulk copy per routed row
 //               (512 B of FP16 hidden for gate/up, of h for down) into a padded tile;
 //   warp 2      publisher: after the compute warps have written a gate/up task's h rows it
@@ -23,7 +23,7 @@
 //               registers.
 // Fragment row g holds tile row 8w + frag_row(g): the permutation puts the two rows that
 // one 8-lane shared-memory phase reads on different halves of the 128-byte swizzle, so the
-// code and scale reads are free of bank conflicts.
+// code reads are free of bank conflicts (the scale reads, 8 rows x 16 B, are too).
 // Each thread dequantises 2 rows x 64 elements per chunk (exact FP16: E2M1 x E4M3 has at
 // most 6 significant bits), feeds 16 MMAs per 8-row tile with FP32 accumulation, and
 // writes h (FP16) or per-route down outputs (FP32) at the end of the task.  Only the TMA
@@ -35,9 +35,10 @@ namespace moe {
 namespace mk {
 
 constexpr int kChunk = 256;                     // K elements per chunk (128 B of codes per row)
-constexpr int kStagesA = 8;
-constexpr int kStageA = 16384;                  // 2 halves x 64 rows x 128 B (SWIZZLE_128B)
-constexpr int kScaleSlot = 16384;               // 128 rows x up to 128 scale bytes
+constexpr int kStagesA = 9;
+constexpr int kCodeBytes = 16384;               // codes: 2 halves x 64 rows x 128 B (SWIZZLE_128B)
+constexpr int kScaleBytes = 2048;               // block scales: 128 rows x 16 B (the chunk's 16 blocks)
+constexpr int kStageA = kCodeBytes + kScaleBytes;
 constexpr int kStagesB = 12;
 constexpr int kTileRows = 8;
 constexpr int kRowPitchB = 2 * kChunk + 16;     // padded FP16 row of one chunk (528 B)
@@ -55,14 +56,11 @@ constexpr long long kTimeoutCycles = 1ll << 33;
 
 struct Smem {
   uint8_t ring_a[kStagesA][kStageA];
-  uint8_t scales[2][kScaleSlot];
   uint8_t ring_b[kStagesB][kStageB];
   TaskEntry task[kTaskSlots];
   uint64_t full_a[kStagesA];
   uint64_t empty_a[kStagesA];
   uint64_t empty_b[kStagesB];
-  uint64_t sc_full[2];
-  uint64_t sc_empty[2];
   uint64_t task_full[kTaskSlots];
   uint64_t task_empty[kTaskSlots];
   uint64_t pub_full[kPubSlots];
@@ -101,14 +99,6 @@ __device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* 
 // Tile row (0..7 within an 8-row group) held by fragment row g: 0, 4, 1, 5, 2, 6, 3, 7.
 __device__ __forceinline__ int frag_row(int g) { return ((g & 1) << 2) | (g >> 1); }
 
-// Offset in a scale slot of the 16-byte piece c of tile row r, for rows of P = 16, 32, 64 or
-// 128 bytes written by a TMA load with the matching swizzle (none, 32, 64 or 128 bytes: the
-// piece index is XORed with address bits 7 and up).
-__device__ __forceinline__ uint32_t scale_piece(int r, int P, int c) {
-  const int rowoff = r * P;
-  return static_cast<uint32_t>(rowoff + ((c ^ ((rowoff >> 7) & ((P >> 4) - 1))) << 4));
-}
-
 // D += A * B for one m16n8k16 step (FP16 inputs, FP32 accumulators).
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
@@ -136,15 +126,14 @@ struct ChunkCodes {
 };
 
 // codes: sub-chunk h covers K [128h, 128h+128); thread q its elements [32q, 32q+32), i.e.
-// 16-byte piece 4h + q of the 128-byte row, stored at (piece ^ (row & 7)); scales: blocks
-// 16c + 8h + 2q and the next one, i.e. bytes 8h + 2q of the row's 16-byte piece c.
-__device__ __forceinline__ void load_chunk_codes(const uint8_t* stage, const uint8_t* sbase, int lra, int lrb, int P,
-                                                 int c, int q, ChunkCodes& o) {
+// 16-byte piece 4h + q of the 128-byte row, stored at (piece ^ (row & 7)); scales: the
+// chunk's blocks 8h + 2q and 8h + 2q + 1, i.e. bytes 8h + 2q of the row's 16 scale bytes.
+__device__ __forceinline__ void load_chunk_codes(const uint8_t* stage, int lra, int lrb, int q, ChunkCodes& o) {
   const int ra = lra & 63, rb = lrb & 63;
-  const uint8_t* pa = stage + (lra >> 6) * (kStageA / 2) + ra * 128;
-  const uint8_t* pb = stage + (lrb >> 6) * (kStageA / 2) + rb * 128;
-  const uint8_t* qa = sbase + scale_piece(lra, P, c) + 2 * q;
-  const uint8_t* qb = sbase + scale_piece(lrb, P, c) + 2 * q;
+  const uint8_t* pa = stage + (lra >> 6) * (kCodeBytes / 2) + ra * 128;
+  const uint8_t* pb = stage + (lrb >> 6) * (kCodeBytes / 2) + rb * 128;
+  const uint8_t* qa = stage + kCodeBytes + lra * 16 + 2 * q;
+  const uint8_t* qb = stage + kCodeBytes + lrb * 16 + 2 * q;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     o.ca[h] = *reinterpret_cast<const uint4*>(pa + (((4 * h + q) ^ (ra & 7)) << 4));
@@ -190,8 +179,7 @@ struct ComputeState {
 // bounded wait gave up.
 template <int MODE>
 __device__ __forceinline__ bool run_chunks(Smem& sm, const ExpertArgs& a, ComputeState& cs, float (&acc)[kMaxTiles][4],
-                                           const uint8_t* sbase, int lra, int lrb, int P, int nck, int nt, int rows,
-                                           int g, int q) {
+                                           int lra, int lrb, int nck, int nt, int rows, int g, int q) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int t = 0; t < kMaxTiles; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
@@ -203,7 +191,7 @@ __device__ __forceinline__ bool run_chunks(Smem& sm, const ExpertArgs& a, Comput
   const bool early = MODE != 0 || 2 * nt <= kStagesB;
   ChunkCodes next;
   if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, sm, a.status)) return false;
-  load_chunk_codes(&sm.ring_a[cs.stage_a][0], sbase, lra, lrb, P, 0, q, next);
+  load_chunk_codes(&sm.ring_a[cs.stage_a][0], lra, lrb, q, next);
   for (int c = 0; c < nck; ++c) {
     const ChunkCodes cur = next;
     // the stage's bytes are in registers: hand it back to the producer
@@ -212,7 +200,7 @@ __device__ __forceinline__ bool run_chunks(Smem& sm, const ExpertArgs& a, Comput
     if (++cs.stage_a == kStagesA) { cs.stage_a = 0; cs.phase_a ^= 1u; }
     if (early && c + 1 < nck) {
       if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, sm, a.status)) return false;
-      load_chunk_codes(&sm.ring_a[cs.stage_a][0], sbase, lra, lrb, P, c + 1, q, next);
+      load_chunk_codes(&sm.ring_a[cs.stage_a][0], lra, lrb, q, next);
     }
     // Per sub-chunk h: activation fragments first (their latency overlaps the
     // dequantisation), then the 32 weights per row of this thread, then the MMAs.
@@ -294,7 +282,7 @@ __device__ __forceinline__ bool run_chunks(Smem& sm, const ExpertArgs& a, Comput
     if (cs.stage_b >= kStagesB) cs.stage_b -= kStagesB;
     if (!early && c + 1 < nck) {
       if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, sm, a.status)) return false;
-      load_chunk_codes(&sm.ring_a[cs.stage_a][0], sbase, lra, lrb, P, c + 1, q, next);
+      load_chunk_codes(&sm.ring_a[cs.stage_a][0], lra, lrb, q, next);
     }
   }
   // fold the independent accumulator sets into one per tile
@@ -354,10 +342,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&sm.empty_a[i]), kComputeWarps);
     }
     for (int i = 0; i < kStagesB; ++i) mbar_init(smem_addr(&sm.empty_b[i]), kComputeWarps);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_addr(&sm.sc_full[i]), 1);
-      mbar_init(smem_addr(&sm.sc_empty[i]), kComputeWarps);
-    }
     for (int i = 0; i < kTaskSlots; ++i) {
       mbar_init(smem_addr(&sm.task_full[i]), 1);
       mbar_init(smem_addr(&sm.task_empty[i]), kTaskConsumers);
@@ -379,7 +363,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   const uint32_t ringa0 = smem_addr(&sm.ring_a[0][0]);
   const uint32_t ringb0 = smem_addr(&sm.ring_b[0][0]);
-  const int P13 = a.d / 16, P2 = a.F / 16;  // scale bytes per row of w13 / w2
   int tcnt = 0;
   if (tid == 0) trace_ev(a, 5, tcnt, 10, 0);
 
@@ -432,24 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tm = &tm_w2;
         nck = a.F / kChunk;
       }
-      // block scales of the task's 128 rows (gate/up: two 64-row boxes; down: one box)
-      const int sn = n & 1;
-      if (!warp_wait(smem_addr(&sm.sc_empty[sn]), static_cast<uint32_t>(((n >> 1) & 1) ^ 1), sm, a.status)) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        const uint32_t sbar = smem_addr(&sm.sc_full[sn]);
-        const uint32_t sdst = smem_addr(&sm.scales[sn][0]);
-        if (!is_dn) {
-          mbar_arrive_expect_tx(sbar, 128u * static_cast<uint32_t>(P13));
-          tma_load_2d(sdst, &tm_s13, 0, rA0, sbar, pol);
-          tma_load_2d(sdst + 64u * static_cast<uint32_t>(P13), &tm_s13, 0, rA1, sbar, pol);
-        } else {
-          mbar_arrive_expect_tx(sbar, 128u * static_cast<uint32_t>(P2));
-          tma_load_2d(sdst, &tm_s2, 0, rA0, sbar, pol);
-        }
-      }
+      const CUtensorMap* tms = is_dn ? &tm_s2 : &tm_s13;
       ++n;
       for (int c = 0; c < nck; ++c) {
         if (!warp_wait(smem_addr(&sm.empty_a[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
@@ -458,7 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fa = smem_addr(&sm.full_a[stage]);
           mbar_arrive_expect_tx(fa, kStageA);
           tma_load_2d(sb, tm, c * (kChunk / 2), rA0, fa, pol);
-          tma_load_2d(sb + kStageA / 2, tm, c * (kChunk / 2), rA1, fa, pol);
+          tma_load_2d(sb + kCodeBytes / 2, tm, c * (kChunk / 2), rA1, fa, pol);
+          // the chunk's 16 block scales of each row (16 bytes at column 16c)
+          tma_load_2d(sb + kCodeBytes, tms, c * (kChunk / 16), rA0, fa, pol);
+          tma_load_2d(sb + kCodeBytes + kScaleBytes / 2, tms, c * (kChunk / 16), rA1, fa, pol);
           trace_ev(a, 0, tcnt, 2, chunk_seq);
         }
         ++chunk_seq;
@@ -480,11 +449,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (--st < 0) { st = kStagesA - 1; ph ^= 1u; }
         const long long t0 = clock64();
         while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kTimeoutCycles) {}
-      }
-      for (int m = max(0, n - 2); m < n; ++m) {
-        const long long t0 = clock64();
-        while (!mbar_try_wait(smem_addr(&sm.sc_full[m & 1]), static_cast<uint32_t>((m >> 1) & 1)) &&
-               clock64() - t0 < kTimeoutCycles) {}
       }
     }
   } else if (warp == 1) {
@@ -597,7 +561,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row0 = te.y, rows = te.z & 0xffff, s = te.w;
       const bool is_dn = ((te.z >> 16) & 1) != 0;
       const int K = is_dn ? a.F : a.d;
-      const int P = is_dn ? P2 : P13;
       const int nck = K / kChunk;
       const int nt = (rows + kTileRows - 1) / kTileRows;
       // Accumulation layout: one- and two-tile passes spread their k-steps over independent
@@ -608,17 +571,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile rows (0..127) of fragment rows g and g + 8
       const int lra = is_dn ? 16 * cw + fr : 8 * cw + fr;
       const int lrb = is_dn ? 16 * cw + 8 + fr : 64 + 8 * cw + fr;
-      const int sn = n & 1;
-      if (!warp_wait(smem_addr(&sm.sc_full[sn]), static_cast<uint32_t>((n >> 1) & 1), sm, a.status)) break;
-      const uint8_t* sbase = &sm.scales[sn][0];
       float acc[kMaxTiles][4];
-      if (mode == 1) ok = run_chunks<1>(sm, a, cs, acc, sbase, lra, lrb, P, nck, nt, rows, g, q);
-      else if (mode == 2) ok = run_chunks<2>(sm, a, cs, acc, sbase, lra, lrb, P, nck, nt, rows, g, q);
-      else ok = run_chunks<0>(sm, a, cs, acc, sbase, lra, lrb, P, nck, nt, rows, g, q);
+      if (mode == 1) ok = run_chunks<1>(sm, a, cs, acc, lra, lrb, nck, nt, rows, g, q);
+      else if (mode == 2) ok = run_chunks<2>(sm, a, cs, acc, lra, lrb, nck, nt, rows, g, q);
+      else ok = run_chunks<0>(sm, a, cs, acc, lra, lrb, nck, nt, rows, g, q);
       if (!ok) break;
-      // the task's scales are no longer needed
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&sm.sc_empty[sn]));
       ++n;
       // ---- epilogue: fragment rows g / g+8, routed rows 8t + 2q, 8t + 2q + 1 ----
       if (!is_dn) {

@@ -111,8 +111,8 @@ cudaError_t launch_combine(const ExpertArgs& a, cudaStream_t stream);
 size_t expert_tc_smem_bytes();
 size_t expert_mma_smem_bytes();
 int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes);
-// Tensor map of a [rows, row_bytes] uint8 matrix (row_bytes 16, 32, 64 or 128) loaded in
-// boxes of box_rows full rows, swizzled by the row size (none for 16 bytes).
+// Tensor map of a [rows, row_bytes] uint8 matrix (row_bytes a multiple of 16) loaded in
+// unswizzled boxes of 16 bytes x box_rows rows.
 int encode_scales_map(CUtensorMap* tm, const void* base, uint32_t row_bytes, uint64_t rows, uint32_t box_rows);
 // Shapes the decode (warp-MMA) kernel handles: d and ffn powers of two from 256 to 2048.
 bool expert_mma_supports(int d, int F);
