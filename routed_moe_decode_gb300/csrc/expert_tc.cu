@@ -586,16 +586,28 @@ __global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int* rp = a.route_pos + static_cast<size_t>(t) * a.k;
   const float* rw = a.route_w + static_cast<size_t>(t) * a.k;
-#pragma unroll 4
-  for (int j = 0; j < a.k; ++j) {
-    const int pos = __ldg(rp + j);
-    if (pos < 0) continue;
-    const float w = __ldg(rw + j);
-    const float4 yv = __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<size_t>(pos) * a.d + r));
-    acc.x += w * yv.x;
-    acc.y += w * yv.y;
-    acc.z += w * yv.z;
-    acc.w += w * yv.w;
+  for (int j0 = 0; j0 < a.k; j0 += 8) {
+    // eight slots' loads in flight together, accumulated in slot order
+    int pos[8];
+    float w[8];
+    float4 yv[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      pos[jj] = j0 + jj < a.k ? __ldg(rp + j0 + jj) : -1;
+      w[jj] = j0 + jj < a.k ? __ldg(rw + j0 + jj) : 0.f;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj)
+      yv[jj] = pos[jj] >= 0 ? __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<size_t>(pos[jj]) * a.d + r))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      if (pos[jj] < 0) continue;
+      acc.x += w[jj] * yv[jj].x;
+      acc.y += w[jj] * yv[jj].y;
+      acc.z += w[jj] * yv[jj].z;
+      acc.w += w[jj] * yv[jj].w;
+    }
   }
   const size_t o = static_cast<size_t>(t) * a.d + r;
   float4 res = make_float4(0.f, 0.f, 0.f, 0.f);

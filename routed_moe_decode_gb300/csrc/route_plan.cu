@@ -27,7 +27,8 @@ constexpr uint32_t kFull = 0xffffffffu;
 // renormalised weights.  Writes ids[t, :k] and weights[t, :k].
 template <int NPL>
 __device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E, int k,
-                                            int32_t* __restrict__ ids, float* __restrict__ weights) {
+                                            int32_t* __restrict__ ids, float* __restrict__ weights,
+                                            int* s_ids = nullptr, float* s_w = nullptr, int s_row = 0) {
   const int lane = threadIdx.x & 31;
   const float* row = logits + static_cast<size_t>(t) * E;
   float v[NPL];
@@ -86,6 +87,10 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
   if (lane < k) {
     ids[static_cast<size_t>(t) * k + lane] = my_id;
     weights[static_cast<size_t>(t) * k + lane] = my_p / sel;
+    if (s_ids != nullptr) {
+      s_ids[s_row * k + lane] = my_id;
+      s_w[s_row * k + lane] = my_p / sel;
+    }
   }
 }
 
@@ -244,51 +249,198 @@ __device__ __forceinline__ void plan_block(const PlanArgs& a) {
   }
 }
 
+// The plan for up to kPlanCached * 1024 routes in one 1024-thread CTA, with one pass over
+// the routes (each thread keeps its routes' experts and in-bucket ranks in registers) and one
+// block scan of (count, touched flag, passes) packed in 64 bits.  ids/weights come from
+// shared memory (from_smem) or from global memory past L1 (written by other CTAs).  Route
+// positions within a bucket follow shared-memory atomic order (outputs do not depend on it).
+constexpr int kPlanCached = 16;
+
+__device__ __forceinline__ long long block_exclusive_scan64(long long v, long long* warp_sums, long long& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const long long w = warp_sums[lane];
+    long long wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long n = __shfl_up_sync(kFull, wi, o);
+      if (lane >= o) wi += n;
+    }
+    warp_sums[lane] = wi - w;
+    if (lane == 31) warp_sums[32] = wi;
+  }
+  __syncthreads();
+  total = warp_sums[32];
+  return warp_sums[warp] + incl - v;
+}
+
+__device__ __forceinline__ void plan_block_cached(const PlanArgs& a, const int* ids_src, const float* w_src,
+                                                  bool from_smem) {
+  __shared__ int s_off[1024];
+  __shared__ int s_num[1024];
+  __shared__ long long s_scan64[33];
+  const int tid = threadIdx.x;
+  const int E = a.E, R = a.T * a.k;
+  if (tid < E) s_num[tid] = 0;
+  __syncthreads();
+  int ev[kPlanCached], rk[kPlanCached];
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < kPlanCached; ++j) {
+    const int r = tid + j * 1024;
+    ev[j] = -1;
+    rk[j] = 0;
+    if (r < R) {
+      const int e = from_smem ? ids_src[r] : __ldcg(ids_src + r);
+      a.route_w[r] = from_smem ? w_src[r] : __ldcg(w_src + r);
+      if (e < 0 || e >= E) {
+        bad = true;
+        a.route_pos[r] = -1;
+      } else {
+        ev[j] = e;
+        rk[j] = atomicAdd(&s_num[e], 1);
+      }
+    }
+  }
+  if (bad) atomicOr(a.status, static_cast<int>(MOE_DEV_BAD_EXPERT_ID));
+  __syncthreads();
+  // count (bits 0..21), touched flag (22..33), passes (34..63)
+  const int cnt = tid < E ? s_num[tid] : 0;
+  const int flag = cnt > 0 ? 1 : 0;
+  const int np = (cnt + kRowsPerPass - 1) / kRowsPerPass;
+  long long tot = 0;
+  const long long pre = block_exclusive_scan64(
+      static_cast<long long>(cnt) | (static_cast<long long>(flag) << 22) | (static_cast<long long>(np) << 34), s_scan64,
+      tot);
+  const int off = static_cast<int>(pre & 0x3fffff);
+  const int rank = static_cast<int>((pre >> 22) & 0xfff);
+  const int pass0 = static_cast<int>(pre >> 34);
+  const int total = static_cast<int>(tot & 0x3fffff);
+  const int U = static_cast<int>((tot >> 22) & 0xfff);
+  const int passes = static_cast<int>(tot >> 34);
+  if (tid < E) {
+    a.counts[tid] = cnt;
+    a.offsets[tid] = off;
+    s_off[tid] = off;
+    if (flag) {
+      a.touched[rank] = tid;
+      a.gu_start[rank] = pass0 * a.S_gu;
+      a.dn_start[rank] = pass0 * a.S_dn;
+    }
+  }
+  // largest row count over the experts
+  int mx = cnt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(kFull, mx, o));
+  if ((tid & 31) == 0) s_scan64[tid >> 5] = mx;
+  __syncthreads();
+  if (tid == 0) {
+    long long m = 0;
+    for (int w = 0; w < 32; ++w) m = max(m, s_scan64[w]);
+    a.offsets[E] = total;
+    a.gu_start[U] = passes * a.S_gu;
+    a.dn_start[U] = passes * a.S_dn;
+    a.meta[META_U] = U;
+    a.meta[META_NGU] = passes * a.S_gu;
+    a.meta[META_NDN] = passes * a.S_dn;
+    a.meta[META_MAXROWS] = static_cast<int>(m);
+  }
+  // route positions in expert-major order
+#pragma unroll
+  for (int j = 0; j < kPlanCached; ++j) {
+    const int r = tid + j * 1024;
+    if (ev[j] >= 0) {
+      const int pos = s_off[ev[j]] + rk[j];
+      a.route_pos[r] = pos;
+      a.pos_tok[pos] = r / a.k;
+    }
+  }
+  // the task table: all gate/up tasks (touched order, pass, stripe), then all down tasks;
+  // each touched expert's thread writes its own entries
+  if (tid < E && flag) {
+    int gi = pass0 * a.S_gu, di = passes * a.S_gu + pass0 * a.S_dn;
+    for (int p = 0; p < np; ++p) {
+      const int rows = min(kRowsPerPass, cnt - p * kRowsPerPass);
+      const int row0 = off + p * kRowsPerPass;
+      const int z = rows | (np > 1 ? 1 << 17 : 0);
+      for (int s2 = 0; s2 < a.S_gu; ++s2) a.tasks[gi++] = TaskEntry{tid | (rank << 16), row0, z, s2};
+      for (int s2 = 0; s2 < a.S_dn; ++s2) a.tasks[di++] = TaskEntry{tid | (rank << 16), row0, z | (1 << 16), s2};
+    }
+  }
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
   pdl_wait();
   pdl_launch_dependents();
-  plan_block(a);
+  if (a.T * a.k <= kPlanCached * 1024) plan_block_cached(a, a.ids, a.weights, false);
+  else plan_block(a);
 }
 
 // ---------------------------------------------------------------------------------
 // Fused front for moderate T * k: each 1024-thread CTA routes 32 tokens (one per warp) and
-// converts their hidden rows to FP16; CTA 0 zeroes the expert kernel's counters; the last
-// CTA to finish (arrival counter, reset by that CTA for the next call) builds the plan.
+// converts their hidden rows to FP16; CTA 0 zeroes the expert kernel's counters.  With one
+// CTA it builds the plan itself from its routes in shared memory; otherwise the last CTA to
+// finish (arrival counter, reset by that CTA for the next call) builds it.
 // ---------------------------------------------------------------------------------
+// hidden rows [t0, t0 + nt) -> FP16 by threads `first` + i * `stride`, flagging values
+// outside the FP16 range
+__device__ __forceinline__ void convert_hidden(const FrontArgs& f, int t0, int nt, int first, int stride) {
+  const size_t n8 = static_cast<size_t>(nt) * f.d / 8;
+  const uint4* src = reinterpret_cast<const uint4*>(f.hidden + static_cast<size_t>(t0) * f.d);
+  uint4* dst = reinterpret_cast<uint4*>(f.x16 + static_cast<size_t>(t0) * f.d);
+  bool bad = false;
+  for (size_t i = first; i < n8; i += stride) {
+    const uint4 raw = src[i];
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    uint4 o;
+    __half2* h = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 v = __bfloat1622float2(b[q]);
+      bad |= !(fabsf(v.x) <= 65504.f) || !(fabsf(v.y) <= 65504.f);
+      h[q] = __floats2half2_rn(v.x, v.y);
+    }
+    dst[i] = o;
+  }
+  if (bad) atomicOr(f.plan.status, static_cast<int>(MOE_DEV_HIDDEN_RANGE));
+}
+
 template <int NPL>
 __global__ void __launch_bounds__(1024) front_kernel(FrontArgs f) {
   __shared__ int s_last;
+  __shared__ int s_ids[1024];  // one CTA: its routes, handed to the plan through shared memory
+  __shared__ float s_w[1024];
   pdl_wait();
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5;
-  const int t = blockIdx.x * 32 + warp;
   const PlanArgs& a = f.plan;
-  if (t < a.T) route_token<NPL>(f.logits, t, a.E, a.k, const_cast<int32_t*>(a.ids), const_cast<float*>(a.weights));
-  // hidden rows of this CTA's tokens -> FP16, flagging values outside the FP16 range
-  {
-    const int t0 = blockIdx.x * 32, nt = min(32, a.T - t0);
-    const size_t n8 = static_cast<size_t>(nt) * f.d / 8;
-    const uint4* src = reinterpret_cast<const uint4*>(f.hidden + static_cast<size_t>(t0) * f.d);
-    uint4* dst = reinterpret_cast<uint4*>(f.x16 + static_cast<size_t>(t0) * f.d);
-    bool bad = false;
-    for (size_t i = threadIdx.x; i < n8; i += blockDim.x) {
-      const uint4 raw = src[i];
-      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
-      uint4 o;
-      __half2* h = reinterpret_cast<__half2*>(&o);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 v = __bfloat1622float2(b[q]);
-        bad |= !(fabsf(v.x) <= 65504.f) || !(fabsf(v.y) <= 65504.f);
-        h[q] = __floats2half2_rn(v.x, v.y);
-      }
-      dst[i] = o;
-    }
-    if (bad) atomicOr(a.status, static_cast<int>(MOE_DEV_HIDDEN_RANGE));
+  const int t0 = blockIdx.x * 32, nt = min(32, a.T - t0);
+  const bool single = gridDim.x == 1;
+  // warps 0..nt-1 route one token each; the other warps stage the hidden rows meanwhile
+  if (warp < nt)
+    route_token<NPL>(f.logits, t0 + warp, a.E, a.k, const_cast<int32_t*>(a.ids), const_cast<float*>(a.weights),
+                     single ? s_ids : nullptr, s_w, warp);
+  if (nt < 32) {
+    if (warp >= nt) convert_hidden(f, t0, nt, threadIdx.x - nt * 32, (32 - nt) * 32);
+  } else {
+    convert_hidden(f, t0, nt, threadIdx.x, blockDim.x);
   }
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < a.E; i += blockDim.x) f.ready[i] = 0u;
     if (threadIdx.x == 0) *f.ticket = 0u;
+  }
+  if (single) {
+    __syncthreads();
+    plan_block_cached(a, s_ids, s_w, true);
+    return;
   }
   // the last CTA to arrive sees every route
   __syncthreads();
@@ -299,7 +451,8 @@ __global__ void __launch_bounds__(1024) front_kernel(FrontArgs f) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  plan_block(a);
+  if (a.T * a.k <= kPlanCached * 1024) plan_block_cached(a, a.ids, a.weights, false);
+  else plan_block(a);
   if (threadIdx.x == 0) *f.done = 0u;
 }
 
