@@ -194,10 +194,20 @@ MOE_API int moe_forward_expert_kernels(const moe_shape* shape, const uint8_t* w1
 MOE_API int moe_forward_unroute(const moe_shape* shape, const void* residual, void* out, void* workspace,
                                 size_t workspace_bytes, moe_stream_t stream);
 
+/* Steps 1-2 together with moe_forward_prepare's staging: the router (ids/weights written
+ * to the caller's [T, k] buffers), the plan in `workspace`, the FP16 copy of `hidden` and
+ * the reset of the expert kernel's counters.  For T * k up to 16384 this is one fused
+ * launch (the last CTA to finish routing builds the plan); larger batches run
+ * moe_route_topk + moe_plan + moe_forward_prepare.  Afterwards moe_forward_experts (or
+ * moe_forward_expert_kernels + moe_forward_unroute) completes the layer.  Arguments as for
+ * moe_route_topk, moe_plan and moe_forward_prepare; returns MOE_OK or an error code. */
+MOE_API int moe_front(const moe_shape* shape, const float* logits, const void* hidden, int32_t* ids,
+                      float* weights, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* Whole layer: router, plan and forward on one stream, with ids/weights written to the
  * caller's [T, k] buffers.  For T * k up to 16384 the router, the FP16 staging of hidden
- * and the plan run as one fused launch (the last CTA to finish routing builds the plan);
- * larger batches use moe_route_topk + moe_plan + moe_forward. */
+ * and the plan run as one fused launch (moe_front); moe_layer is moe_front followed by
+ * moe_forward_experts with MOE_ALGO_AUTO. */
 MOE_API int moe_layer(const moe_shape* shape, const float* logits, const void* hidden,
               const uint8_t* w13_codes, const uint8_t* w13_scales, float w13_scale,
               const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,

@@ -59,6 +59,7 @@ SIGNATURES = {
     "moe_forward_experts": (_I, [_SP, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _I, _P]),
     "moe_forward_expert_kernels": (_I, [_SP, _P, _P, _F, _P, _P, _F, _P, ctypes.c_size_t, _I, _P]),
     "moe_forward_unroute": (_I, [_SP, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_front": (_I, [_SP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_layer": (_I, [_SP, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_layer_static_workspace": (_I, [_SP, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P]),
     "moe_read_device_status": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint32), _P]),
@@ -189,6 +190,11 @@ def forward_unroute(shape: Shape, residual, out, ws: Workspace, stream=None):
     """The weighted un-route alone: out = residual + the token's routes in slot order."""
     _check("moe_forward_unroute", lib().moe_forward_unroute(
         ctypes.byref(shape), _ptr(residual), _ptr(out), ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def front(shape: Shape, logits, hidden, ids, weights, ws: Workspace, stream=None):
+    _check("moe_front", lib().moe_front(ctypes.byref(shape), _ptr(logits), _ptr(hidden), _ptr(ids), _ptr(weights),
+                                        ws.ptr, ws.nbytes, _stream(stream)))
 
 
 def layer(shape: Shape, logits, hidden, w: dict, residual, out, ids, weights, ws: Workspace, stream=None):

@@ -398,10 +398,8 @@ int moe_forward(const moe_shape* shape, const void* hidden, const uint8_t* w13_c
                           out, workspace, workspace_bytes, MOE_ALGO_AUTO, stream);
 }
 
-int moe_layer(const moe_shape* shape, const float* logits, const void* hidden, const uint8_t* w13_codes,
-              const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales,
-              float w2_scale, const void* residual, void* out, int32_t* ids, float* weights, void* workspace,
-              size_t workspace_bytes, moe_stream_t stream) {
+int moe_front(const moe_shape* shape, const float* logits, const void* hidden, int32_t* ids, float* weights,
+              void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   if (shape->T == 0) return MOE_OK;
@@ -411,8 +409,7 @@ int moe_layer(const moe_shape* shape, const float* logits, const void* hidden, c
     if (rc != MOE_OK) return rc;
     rc = moe_plan(shape, ids, weights, workspace, workspace_bytes, stream);
     if (rc != MOE_OK) return rc;
-    return moe_forward(shape, hidden, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual,
-                       out, workspace, workspace_bytes, stream);
+    return moe_forward_prepare(shape, hidden, workspace, workspace_bytes, stream);
   }
   if (!logits || !hidden || !ids || !weights || !aligned(logits, 16) || !aligned(hidden, 16) || !aligned(ids, 4) ||
       !aligned(weights, 4))
@@ -431,6 +428,19 @@ int moe_layer(const moe_shape* shape, const float* logits, const void* hidden, c
   f.done = at<uint32_t>(workspace, L.front_done);
   cudaError_t e = moe::launch_front(f, stream);
   if (e != cudaSuccess) { set_error("front launch", e); return MOE_ERR_CUDA; }
+  return MOE_OK;
+}
+
+int moe_layer(const moe_shape* shape, const float* logits, const void* hidden, const uint8_t* w13_codes,
+              const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales,
+              float w2_scale, const void* residual, void* out, int32_t* ids, float* weights, void* workspace,
+              size_t workspace_bytes, moe_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (shape->T == 0) return MOE_OK;
+  if (!w13_codes || !w13_scales || !w2_codes || !w2_scales || !out) return MOE_ERR_INVALID_ARG;
+  rc = moe_front(shape, logits, hidden, ids, weights, workspace, workspace_bytes, stream);
+  if (rc != MOE_OK) return rc;
   return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
                               workspace, workspace_bytes, MOE_ALGO_AUTO, nullptr, stream);
 }

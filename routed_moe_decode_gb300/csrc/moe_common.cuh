@@ -52,7 +52,7 @@ enum { META_U = 0, META_NGU = 1, META_NDN = 2, META_MAXROWS = 3, META_WORDS = 8 
 //   x = expert id | touched index << 16, y = first routed row (expert-major position),
 //   z = rows in this pass | is_down << 16 | (expert has more than one pass) << 17,
 //   w = stripe index.
-struct TaskEntry {
+struct alignas(16) TaskEntry {
   int x, y, z, w;
 };
 

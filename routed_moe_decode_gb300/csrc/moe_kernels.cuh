@@ -34,6 +34,7 @@ struct FrontArgs {
   uint32_t* ready;
   uint32_t* ticket;
   uint32_t* done;  // CTA arrival counter: zero between calls
+  int tpc;         // tokens routed per CTA (one warp each), at most 32
 };
 constexpr int kFrontMaxRoutes = 16384;
 
@@ -99,7 +100,7 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* weights,
                               cudaStream_t stream);
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
-cudaError_t launch_front(const FrontArgs& f, cudaStream_t stream);
+cudaError_t launch_front(FrontArgs f, cudaStream_t stream);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream);
 cudaError_t launch_expert_tc(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
                              int num_sms, cudaStream_t stream);

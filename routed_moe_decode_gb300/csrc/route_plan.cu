@@ -23,42 +23,35 @@ namespace moe {
 
 constexpr uint32_t kFull = 0xffffffffu;
 
-// Route token t (one warp): softmax over the E logits, k rounds of arg-max selection,
-// renormalised weights.  Writes ids[t, :k] and weights[t, :k].
-template <int NPL>
-__device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E, int k,
-                                            int32_t* __restrict__ ids, float* __restrict__ weights,
-                                            int* s_ids = nullptr, float* s_w = nullptr, int s_row = 0) {
-  const int lane = threadIdx.x & 31;
-  const float* row = logits + static_cast<size_t>(t) * E;
-  float v[NPL];
-  uint32_t key[NPL];
-  float mx = -FLT_MAX;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    const bool ok = e < E;
-    v[i] = ok ? __ldg(row + e) : -FLT_MAX;
-    key[i] = ok ? float_key(v[i]) : 0u;  // 0 is below every real key: never selected
-    mx = fmaxf(mx, v[i]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    if (lane + 32 * i < E) s += expf(v[i] - mx);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-  const float z = s;
+// Inverse of float_key: the float whose key is `k` (+0 for the shared key of +-0).
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
 
+// Insert key `x` of slot `i` into the descending list c[0..C) (slots in s[]); slots arrive in
+// ascending order and only a strictly larger key moves ahead, so equal keys keep the lower
+// slot (the lower expert id) first.
+template <int C>
+__device__ __forceinline__ void cache_insert(uint32_t (&c)[C], int (&s)[C], uint32_t x, int i) {
+#pragma unroll
+  for (int m = C - 1; m > 0; --m) {
+    const bool above = x > c[m - 1], here = x > c[m];
+    s[m] = above ? s[m - 1] : (here ? i : s[m]);
+    c[m] = above ? c[m - 1] : (here ? x : c[m]);
+  }
+  s[0] = x > c[0] ? i : s[0];
+  c[0] = x > c[0] ? x : c[0];
+}
+
+// Exact selection by k rounds over all of a lane's keys (no list): the fallback of
+// route_token when a lane runs out of listed keys.  Same ordering and tie rule.
+template <int NPL>
+__device__ __forceinline__ void select_scan(const uint32_t (&key)[NPL], int k, uint32_t& my_key, int& my_id) {
+  const int lane = threadIdx.x & 31;
   uint32_t used = 0;
-  int my_id = 0;
-  float my_p = 0.f;
   for (int j = 0; j < k; ++j) {
     uint32_t bk = 0;
-    int bi = -1;
+    int bi = 0;
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
       if (!((used >> i) & 1u) && key[i] > bk) {
@@ -67,29 +60,101 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
       }
     }
     const uint32_t kmax = __reduce_max_sync(kFull, bk);
-    const uint32_t cand = (bi >= 0 && bk == kmax) ? static_cast<uint32_t>(lane + 32 * bi) : 0xffffffffu;
+    const uint32_t cand = bk == kmax ? static_cast<uint32_t>(lane + 32 * bi) : 0xffffffffu;
     const uint32_t idx = __reduce_min_sync(kFull, cand);
-    const int owner = static_cast<int>(idx & 31u);
-    const int slot = static_cast<int>(idx >> 5);
-    if (lane == owner) used |= 1u << slot;
-    float lv = 0.f;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) lv = (i == slot) ? v[i] : lv;
-    lv = __shfl_sync(kFull, lv, owner);
+    if (static_cast<int>(idx & 31u) == lane) used |= 1u << (idx >> 5);
     if (lane == j) {
+      my_key = kmax;
       my_id = static_cast<int>(idx);
-      my_p = expf(lv - mx) / z;
     }
   }
-  // renormalise over the selection, summed in slot order
-  float sel = 0.f;
-  for (int j = 0; j < k; ++j) sel += __shfl_sync(kFull, my_p, j);
+}
+
+// Route token t (one warp): softmax over the E logits, k rounds of arg-max selection,
+// renormalised weights.  Writes ids[t, :k] and weights[t, :k] (and the shared-memory copies
+// s_ids/s_w at row s_row when given).
+//
+// Each lane keeps its best min(NPL, 4) keys in a sorted register list; a round is one
+// warp max over the lanes' heads, one warp min over the expert ids holding that key (the
+// lowest id wins ties), and a shift of the winner's list.  If a lane gave away its whole
+// list while holding further keys, the rounds may have missed one of those, and the
+// selection is redone by full scans.  The selected logit is recovered from its key (the key
+// is a bijection of the float bits); the probabilities are formed after the rounds, one per
+// lane.
+template <int NPL>
+__device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E, int k,
+                                            int32_t* __restrict__ ids, float* __restrict__ weights,
+                                            int* s_ids = nullptr, float* s_w = nullptr, int s_row = 0) {
+  constexpr int C = NPL < 4 ? NPL : 4;
+  const int lane = threadIdx.x & 31;
+  const float* row = logits + static_cast<size_t>(t) * E;
+  float v[NPL];
+  uint32_t key[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    const bool ok = e < E;
+    v[i] = ok ? __ldg(row + e) : -FLT_MAX;
+    key[i] = ok ? float_key(v[i]) : 0u;  // 0 is below every real key: never selected
+  }
+  uint32_t ck[C];
+  int cs[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    ck[c] = 0u;
+    cs[c] = 0;
+  }
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) cache_insert<C>(ck, cs, key[i], i);
+  // the largest logit: its key is the largest head
+  const uint32_t kmax0 = __reduce_max_sync(kFull, ck[0]);
+  const float mx = key_float(kmax0);
+  float sp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    if (lane + 32 * i < E) sp[i & 3] += expf(v[i] - mx);
+  }
+  float s = (sp[0] + sp[1]) + (sp[2] + sp[3]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+  const float z = s;
+
+  int nused = 0;
+  uint32_t my_key = 0;
+  int my_id = 0;
+  uint32_t kmax = kmax0;
+  for (int j = 0; j < k; ++j) {
+    if (j > 0) kmax = __reduce_max_sync(kFull, ck[0]);
+    const uint32_t cand = ck[0] == kmax ? static_cast<uint32_t>(lane + 32 * cs[0]) : 0xffffffffu;
+    const uint32_t idx = __reduce_min_sync(kFull, cand);
+    if (lane == j) {
+      my_key = kmax;
+      my_id = static_cast<int>(idx);
+    }
+    const bool own = static_cast<int>(idx & 31u) == lane;
+    nused += own ? 1 : 0;
+#pragma unroll
+    for (int c = 0; c + 1 < C; ++c) {
+      ck[c] = own ? ck[c + 1] : ck[c];
+      cs[c] = own ? cs[c + 1] : cs[c];
+    }
+    ck[C - 1] = own ? 0u : ck[C - 1];
+  }
+  if constexpr (NPL > C) {
+    const int nvalid = min(NPL, (E - lane + 31) / 32);
+    if (__any_sync(kFull, nused >= C && nvalid > C)) select_scan<NPL>(key, k, my_key, my_id);
+  }
+  // renormalise over the selection
+  const float p = lane < k ? expf(key_float(my_key) - mx) / z : 0.f;
+  float sel = p;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sel += __shfl_xor_sync(kFull, sel, o);
   if (lane < k) {
     ids[static_cast<size_t>(t) * k + lane] = my_id;
-    weights[static_cast<size_t>(t) * k + lane] = my_p / sel;
+    weights[static_cast<size_t>(t) * k + lane] = p / sel;
     if (s_ids != nullptr) {
       s_ids[s_row * k + lane] = my_id;
-      s_w[s_row * k + lane] = my_p / sel;
+      s_w[s_row * k + lane] = p / sel;
     }
   }
 }
@@ -250,51 +315,89 @@ __device__ __forceinline__ void plan_block(const PlanArgs& a) {
 }
 
 // The plan for up to kPlanCached * 1024 routes in one 1024-thread CTA, with one pass over
-// the routes (each thread keeps its routes' experts and in-bucket ranks in registers) and one
-// block scan of (count, touched flag, passes) packed in 64 bits.  ids/weights come from
-// shared memory (from_smem) or from global memory past L1 (written by other CTAs).  Route
-// positions within a bucket follow shared-memory atomic order (outputs do not depend on it).
+// the routes (each thread keeps NJ routes' experts and in-bucket ranks in registers) and one
+// block scan of (count, touched flag, extra passes) packed in one word: 32 bits when every
+// field fits (NJ = 1: at most 1024 routes), else 64 bits.  ids/weights come from shared
+// memory (from_smem) or from global memory past L1 (written by other CTAs).  Route positions
+// within a bucket follow shared-memory atomic order (outputs do not depend on it).
 constexpr int kPlanCached = 16;
+constexpr int kPlanMaxPasses = 1024 + kPlanCached * 1024 / kRowsPerPass;  // E + R / kRowsPerPass
 
-__device__ __forceinline__ long long block_exclusive_scan64(long long v, long long* warp_sums, long long& total) {
+struct PlanSmem {
+  int off[1024];
+  int num[1024];
+  int expert[1024];  // touched index -> expert
+  int pass0[1024];   // touched index -> its first pass
+  int pass_rank[kPlanMaxPasses];  // pass -> touched index
+  unsigned long long sum[33];
+  int mx[33];
+};
+
+template <int NJ>
+struct PlanPack;
+template <>
+struct PlanPack<1> {  // count <= 1024, touched <= 1024, extra passes <= 16
+  using V = uint32_t;
+  static constexpr int kF = 11, kX = 22;
+};
+template <>
+struct PlanPack<4> {  // count <= 4096, touched <= 1024, extra passes <= 64
+  using V = uint32_t;
+  static constexpr int kF = 13, kX = 24;
+};
+template <>
+struct PlanPack<kPlanCached> {
+  using V = unsigned long long;
+  static constexpr int kF = 22, kX = 34;
+};
+
+// Exclusive scan of one V per thread over a 1024-thread block, with the block total and the
+// block maximum of `m` (warp reductions; two barriers).
+template <typename V>
+__device__ __forceinline__ V block_scan_max(V v, int m, PlanSmem& ps, V& total, int& mtotal) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  long long incl = v;
+  V incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const long long n = __shfl_up_sync(kFull, incl, o);
+    const V n = __shfl_up_sync(kFull, incl, o);
     if (lane >= o) incl += n;
   }
-  if (lane == 31) warp_sums[warp] = incl;
+  const int wm = __reduce_max_sync(kFull, m);
+  if (lane == 31) ps.sum[warp] = incl;
+  if (lane == 0) ps.mx[warp] = wm;
   __syncthreads();
   if (warp == 0) {
-    const long long w = warp_sums[lane];
-    long long wi = w;
+    const V w = static_cast<V>(ps.sum[lane]);
+    V wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const long long n = __shfl_up_sync(kFull, wi, o);
+      const V n = __shfl_up_sync(kFull, wi, o);
       if (lane >= o) wi += n;
     }
-    warp_sums[lane] = wi - w;
-    if (lane == 31) warp_sums[32] = wi;
+    ps.sum[lane] = wi - w;
+    if (lane == 31) ps.sum[32] = wi;
+    const int mm = __reduce_max_sync(kFull, ps.mx[lane]);
+    if (lane == 0) ps.mx[32] = mm;
   }
   __syncthreads();
-  total = warp_sums[32];
-  return warp_sums[warp] + incl - v;
+  total = static_cast<V>(ps.sum[32]);
+  mtotal = ps.mx[32];
+  return static_cast<V>(ps.sum[warp]) + incl - v;
 }
 
+template <int NJ>
 __device__ __forceinline__ void plan_block_cached(const PlanArgs& a, const int* ids_src, const float* w_src,
-                                                  bool from_smem) {
-  __shared__ int s_off[1024];
-  __shared__ int s_num[1024];
-  __shared__ long long s_scan64[33];
+                                                  bool from_smem, PlanSmem& ps) {
+  using Pk = PlanPack<NJ>;
+  using V = typename Pk::V;
   const int tid = threadIdx.x;
   const int E = a.E, R = a.T * a.k;
-  if (tid < E) s_num[tid] = 0;
+  if (tid < E) ps.num[tid] = 0;
   __syncthreads();
-  int ev[kPlanCached], rk[kPlanCached];
+  int ev[NJ], rk[NJ];
   bool bad = false;
 #pragma unroll
-  for (int j = 0; j < kPlanCached; ++j) {
+  for (int j = 0; j < NJ; ++j) {
     const int r = tid + j * 1024;
     ev[j] = -1;
     rk[j] = 0;
@@ -306,87 +409,103 @@ __device__ __forceinline__ void plan_block_cached(const PlanArgs& a, const int* 
         a.route_pos[r] = -1;
       } else {
         ev[j] = e;
-        rk[j] = atomicAdd(&s_num[e], 1);
+        rk[j] = atomicAdd(&ps.num[e], 1);
       }
     }
   }
   if (bad) atomicOr(a.status, static_cast<int>(MOE_DEV_BAD_EXPERT_ID));
   __syncthreads();
-  // count (bits 0..21), touched flag (22..33), passes (34..63)
-  const int cnt = tid < E ? s_num[tid] : 0;
+  const int cnt = tid < E ? ps.num[tid] : 0;
   const int flag = cnt > 0 ? 1 : 0;
   const int np = (cnt + kRowsPerPass - 1) / kRowsPerPass;
-  long long tot = 0;
-  const long long pre = block_exclusive_scan64(
-      static_cast<long long>(cnt) | (static_cast<long long>(flag) << 22) | (static_cast<long long>(np) << 34), s_scan64,
-      tot);
-  const int off = static_cast<int>(pre & 0x3fffff);
-  const int rank = static_cast<int>((pre >> 22) & 0xfff);
-  const int pass0 = static_cast<int>(pre >> 34);
-  const int total = static_cast<int>(tot & 0x3fffff);
-  const int U = static_cast<int>((tot >> 22) & 0xfff);
-  const int passes = static_cast<int>(tot >> 34);
+  V tot = 0;
+  int mx = 0;
+  const V pre = block_scan_max<V>(static_cast<V>(cnt) | (static_cast<V>(flag) << Pk::kF) |
+                                      (static_cast<V>(np - flag) << Pk::kX),
+                                  cnt, ps, tot, mx);
+  constexpr V kMaskC = (V(1) << Pk::kF) - 1, kMaskF = (V(1) << (Pk::kX - Pk::kF)) - 1;
+  const int off = static_cast<int>(pre & kMaskC);
+  const int rank = static_cast<int>((pre >> Pk::kF) & kMaskF);
+  const int pass0 = rank + static_cast<int>(pre >> Pk::kX);
+  const int total = static_cast<int>(tot & kMaskC);
+  const int U = static_cast<int>((tot >> Pk::kF) & kMaskF);
+  const int passes = U + static_cast<int>(tot >> Pk::kX);
   if (tid < E) {
     a.counts[tid] = cnt;
     a.offsets[tid] = off;
-    s_off[tid] = off;
+    ps.off[tid] = off;
     if (flag) {
-      a.touched[rank] = tid;
-      a.gu_start[rank] = pass0 * a.S_gu;
-      a.dn_start[rank] = pass0 * a.S_dn;
+      ps.expert[rank] = tid;
+      ps.pass0[rank] = pass0;
+      for (int p = 0; p < np; ++p) ps.pass_rank[pass0 + p] = rank;
     }
   }
-  // largest row count over the experts
-  int mx = cnt;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(kFull, mx, o));
-  if ((tid & 31) == 0) s_scan64[tid >> 5] = mx;
-  __syncthreads();
   if (tid == 0) {
-    long long m = 0;
-    for (int w = 0; w < 32; ++w) m = max(m, s_scan64[w]);
     a.offsets[E] = total;
     a.gu_start[U] = passes * a.S_gu;
     a.dn_start[U] = passes * a.S_dn;
     a.meta[META_U] = U;
     a.meta[META_NGU] = passes * a.S_gu;
     a.meta[META_NDN] = passes * a.S_dn;
-    a.meta[META_MAXROWS] = static_cast<int>(m);
+    a.meta[META_MAXROWS] = mx;
+  }
+  __syncthreads();
+  // touched list in touched order (coalesced)
+  for (int r = tid; r < U; r += blockDim.x) {
+    a.touched[r] = ps.expert[r];
+    a.gu_start[r] = ps.pass0[r] * a.S_gu;
+    a.dn_start[r] = ps.pass0[r] * a.S_dn;
   }
   // route positions in expert-major order
 #pragma unroll
-  for (int j = 0; j < kPlanCached; ++j) {
+  for (int j = 0; j < NJ; ++j) {
     const int r = tid + j * 1024;
     if (ev[j] >= 0) {
-      const int pos = s_off[ev[j]] + rk[j];
+      const int pos = ps.off[ev[j]] + rk[j];
       a.route_pos[r] = pos;
       a.pos_tok[pos] = r / a.k;
     }
   }
   // the task table: all gate/up tasks (touched order, pass, stripe), then all down tasks;
-  // each touched expert's thread writes its own entries
-  if (tid < E && flag) {
-    int gi = pass0 * a.S_gu, di = passes * a.S_gu + pass0 * a.S_dn;
-    for (int p = 0; p < np; ++p) {
-      const int rows = min(kRowsPerPass, cnt - p * kRowsPerPass);
-      const int row0 = off + p * kRowsPerPass;
-      const int z = rows | (np > 1 ? 1 << 17 : 0);
-      for (int s2 = 0; s2 < a.S_gu; ++s2) a.tasks[gi++] = TaskEntry{tid | (rank << 16), row0, z, s2};
-      for (int s2 = 0; s2 < a.S_dn; ++s2) a.tasks[di++] = TaskEntry{tid | (rank << 16), row0, z | (1 << 16), s2};
-    }
+  // consecutive threads write consecutive 16-byte entries
+  const int ngu = passes * a.S_gu, ntask = ngu + passes * a.S_dn;
+  int4* tasks = reinterpret_cast<int4*>(a.tasks);
+  for (int i = tid; i < ntask; i += blockDim.x) {
+    const bool dn = i >= ngu;
+    const int j = dn ? i - ngu : i;
+    const int S = dn ? a.S_dn : a.S_gu;
+    const int P = j / S, s2 = j - P * S;
+    const int rk2 = ps.pass_rank[P];
+    const int e = ps.expert[rk2];
+    const int p = P - ps.pass0[rk2];
+    const int c = ps.num[e];
+    const int rows = min(kRowsPerPass, c - p * kRowsPerPass);
+    const int z = rows | (dn ? 1 << 16 : 0) | (c > kRowsPerPass ? 1 << 17 : 0);
+    tasks[i] = make_int4(e | (rk2 << 16), ps.off[e] + p * kRowsPerPass, z, s2);
   }
 }
 
+// plan of the routes in ids_src/w_src by the best-fitting variant (R <= kPlanCached * 1024)
+__device__ __forceinline__ void plan_cached(const PlanArgs& a, const int* ids_src, const float* w_src,
+                                            bool from_smem, PlanSmem& ps) {
+  const int R = a.T * a.k;
+  if (R <= 1024) plan_block_cached<1>(a, ids_src, w_src, from_smem, ps);
+  else if (R <= 4096) plan_block_cached<4>(a, ids_src, w_src, from_smem, ps);
+  else plan_block_cached<kPlanCached>(a, ids_src, w_src, from_smem, ps);
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
+  __shared__ PlanSmem ps;
   pdl_wait();
   pdl_launch_dependents();
-  if (a.T * a.k <= kPlanCached * 1024) plan_block_cached(a, a.ids, a.weights, false);
+  if (a.T * a.k <= kPlanCached * 1024) plan_cached(a, a.ids, a.weights, false, ps);
   else plan_block(a);
 }
 
 // ---------------------------------------------------------------------------------
-// Fused front for moderate T * k: each 1024-thread CTA routes 32 tokens (one per warp) and
-// converts their hidden rows to FP16; CTA 0 zeroes the expert kernel's counters.  With one
+// Fused front for moderate T * k: each 1024-thread CTA routes f.tpc tokens (one per warp;
+// few per CTA, so that the latency-bound selection of different tokens runs on different
+// SMs) and converts their hidden rows to FP16; CTA 0 zeroes the expert kernel's counters.  With one
 // CTA it builds the plan itself from its routes in shared memory; otherwise the last CTA to
 // finish (arrival counter, reset by that CTA for the next call) builds it.
 // ---------------------------------------------------------------------------------
@@ -418,11 +537,12 @@ __global__ void __launch_bounds__(1024) front_kernel(FrontArgs f) {
   __shared__ int s_last;
   __shared__ int s_ids[1024];  // one CTA: its routes, handed to the plan through shared memory
   __shared__ float s_w[1024];
+  __shared__ PlanSmem ps;
   pdl_wait();
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const PlanArgs& a = f.plan;
-  const int t0 = blockIdx.x * 32, nt = min(32, a.T - t0);
+  const int t0 = blockIdx.x * f.tpc, nt = min(f.tpc, a.T - t0);
   const bool single = gridDim.x == 1;
   // warps 0..nt-1 route one token each; the other warps stage the hidden rows meanwhile
   if (warp < nt)
@@ -439,7 +559,7 @@ __global__ void __launch_bounds__(1024) front_kernel(FrontArgs f) {
   }
   if (single) {
     __syncthreads();
-    plan_block_cached(a, s_ids, s_w, true);
+    plan_cached(a, s_ids, s_w, true, ps);
     return;
   }
   // the last CTA to arrive sees every route
@@ -451,14 +571,16 @@ __global__ void __launch_bounds__(1024) front_kernel(FrontArgs f) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  if (a.T * a.k <= kPlanCached * 1024) plan_block_cached(a, a.ids, a.weights, false);
+  if (a.T * a.k <= kPlanCached * 1024) plan_cached(a, a.ids, a.weights, false, ps);
   else plan_block(a);
   if (threadIdx.x == 0) *f.done = 0u;
 }
 
-cudaError_t launch_front(const FrontArgs& f, cudaStream_t stream) {
+cudaError_t launch_front(FrontArgs f, cudaStream_t stream) {
   const int npl = (f.plan.E + 31) / 32;
-  const dim3 grid((f.plan.T + 31) / 32), block(1024);
+  // tokens per CTA: 4 while the CTAs fit the SMs in one wave, up to 32 beyond
+  f.tpc = min(32, max(4, (f.plan.T + 147) / 148));
+  const dim3 grid((f.plan.T + f.tpc - 1) / f.tpc), block(1024);
   void (*kern)(FrontArgs) = npl <= 1 ? front_kernel<1> : npl <= 2 ? front_kernel<2> : npl <= 4 ? front_kernel<4>
                            : npl <= 8 ? front_kernel<8> : npl <= 16 ? front_kernel<16> : front_kernel<32>;
   return launch_pdl(kern, grid, block, 0, stream, f);

@@ -182,6 +182,26 @@ def test_route_ties_and_signed_zero(E, k):
     np.testing.assert_allclose(w, w_ref, rtol=WEIGHT_RTOL, atol=1e-7)
 
 
+@pytest.mark.parametrize("E,k", [(512, 10), (1024, 32), (96, 12)])
+def test_route_winners_concentrated_in_few_experts_mod_32(E, k):
+    # every winner sits at an expert id of one residue mod 32 (or two), so one warp lane
+    # holds more winners than it keeps sorted at a time and must rebuild its list
+    rng = np.random.default_rng(7 * E + k)
+    T = 64
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    for t in range(T):
+        lanes = [t % 32] if t % 2 == 0 else [t % 32, (t * 7 + 3) % 32]
+        for ln in lanes:
+            sel = np.arange(ln, E, 32)
+            logits[t, sel] = 10.0 + rng.standard_normal(sel.size).astype(np.float32)
+            if t % 4 == 0:
+                logits[t, sel[::2]] = 11.0  # exact ties inside the lane
+    ids, w = _route_only(logits, k)
+    ids_ref, w_ref = O.route_topk(logits, k)
+    np.testing.assert_array_equal(ids, ids_ref)
+    np.testing.assert_allclose(w, w_ref, rtol=WEIGHT_RTOL, atol=1e-7)
+
+
 @pytest.mark.parametrize("name", ["b1", "b8", "b64", "prefill"])
 def test_route_full_size_bit_exact(name):
     cfg = mi.CONFIGS[name]
