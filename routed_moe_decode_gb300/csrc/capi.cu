@@ -160,6 +160,7 @@ moe::ExpertArgs expert_args(const moe_shape* s, const WsLayout& L, void* ws, con
   a.hs16 = at<__half>(ws, L.hs16);
   a.y = at<float>(ws, L.y);
   a.ready = at<uint32_t>(ws, L.ready);
+  a.dn_done = a.ready + s->E;
   a.ticket = at<uint32_t>(ws, L.ticket);
   a.status = at<int>(ws, L.status);
   a.residual = static_cast<const __nv_bfloat16*>(residual);
@@ -260,7 +261,7 @@ int moe_forward_prepare(const moe_shape* shape, const void* hidden, void* worksp
   if (rc != MOE_OK) return rc;
   const WsLayout L = moe::ws_layout(*shape);
   moe::PrepArgs p{};
-  p.T = shape->T; p.d = shape->d; p.E = shape->E;
+  p.T = shape->T; p.d = shape->d; p.E = shape->E; p.S_dn = L.S_dn;
   p.hidden = static_cast<const __nv_bfloat16*>(hidden);
   p.x16 = at<__half>(workspace, L.x16);
   p.ready = at<uint32_t>(workspace, L.ready);
@@ -330,8 +331,11 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     rc = moe::encode_scales_map(&ts2, w2_scales, static_cast<uint32_t>(shape->ffn / 16),
                                 static_cast<uint64_t>(shape->E) * shape->d, 64);
     if (rc != MOE_OK) return rc;
+    // for few tokens the decode kernel runs the un-route as trailing tasks of its own
+    a.ncb = (stages & kStageUnroute) ? moe::expert_mma_unroute_tasks(shape->T, L.S_dn) : 0;
     e = moe::launch_expert_mma(a, tm13, tm2, ts13, ts2, di.num_sms, stream);
     if (e != cudaSuccess) { set_error("expert_mma launch", e); return MOE_ERR_CUDA; }
+    if (a.ncb > 0) return MOE_OK;
   } else {
     e = moe::launch_expert_tc(a, tm13, tm2, di.num_sms, stream);
     if (e != cudaSuccess) { set_error("expert_tc launch", e); return MOE_ERR_CUDA; }

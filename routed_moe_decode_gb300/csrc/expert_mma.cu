@@ -96,6 +96,17 @@ __device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* 
   return true;
 }
 
+// Task i of the ticket order: entry i of the plan's table, or, past its ntask entries, one of
+// the a.ncb un-route tasks: stripe c mod S_dn (128 output columns) of the tokens
+// [8 (c / S_dn), +8), one token per compute warp (c = i - ntask).
+__device__ __forceinline__ TaskEntry task_at(const ExpertArgs& a, int i, int ntask) {
+  if (i < ntask) return a.tasks[i];
+  const int c = i - ntask;
+  return TaskEntry{0, kComputeWarps * (c / a.S_dn), 1 << 18, c % a.S_dn};
+}
+
+__device__ __forceinline__ bool is_unroute(const TaskEntry& t) { return ((t.z >> 18) & 1) != 0; }
+
 // Tile row (0..7 within an 8-row group) held by fragment row g: 0, 4, 1, 5, 2, 6, 3, 7.
 __device__ __forceinline__ int frag_row(int g) { return ((g & 1) << 2) | (g >> 1); }
 
@@ -326,6 +337,10 @@ __device__ __forceinline__ void trace_ev(const ExpertArgs& a, int role, int& cnt
 
 using namespace mk;
 
+// kFused: the kernel also runs the un-route, as a.ncb tasks after every expert task (each
+// waits for the down tasks of its stripe); otherwise the un-route is a kernel of its own and
+// none of that code is compiled in.
+template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_mma_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_w2,
                       const __grid_constant__ CUtensorMap tm_s13, const __grid_constant__ CUtensorMap tm_s2,
@@ -369,16 +384,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------- task fetcher + weight producer (tickets two tasks ahead) -------------
     const uint64_t pol = policy_evict_first();
-    const int ntot = __ldg(a.meta + META_NGU) + __ldg(a.meta + META_NDN);
+    const int ntask = __ldg(a.meta + META_NGU) + __ldg(a.meta + META_NDN);
+    const int ntot = ntask + (kFused ? a.ncb : 0);
     const TaskEntry kEnd = TaskEntry{-1, 0, 0, 0};
     int stage = 0, issued = 0, n = 0, chunk_seq = 0;
     uint32_t phase = 0;
     int cur = blockIdx.x, nxt = ntot;
     TaskEntry entry = kEnd, entry_nxt = kEnd;
     if (lane == 0 && cur < ntot) {
-      entry = a.tasks[cur];
+      entry = kFused ? task_at(a, cur, ntask) : a.tasks[cur];
       nxt = static_cast<int>(atomicAdd(a.ticket, 1u)) + static_cast<int>(gridDim.x);
-      if (nxt < ntot) entry_nxt = a.tasks[nxt];
+      if (nxt < ntot) entry_nxt = kFused ? task_at(a, nxt, ntask) : a.tasks[nxt];
     }
     bool ok = true;
     while (ok) {
@@ -415,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tm = &tm_w2;
         nck = a.F / kChunk;
       }
+      if (kFused && ((z >> 18) & 1)) nck = 0;  // un-route task: no weights
       const CUtensorMap* tms = is_dn ? &tm_s2 : &tm_s13;
       ++n;
       for (int c = 0; c < nck; ++c) {
@@ -438,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur = nxt;
         entry = entry_nxt;
         nxt = nxt2;
-        entry_nxt = nxt < ntot ? a.tasks[nxt] : kEnd;
+        entry_nxt = nxt < ntot ? (kFused ? task_at(a, nxt, ntask) : a.tasks[nxt]) : kEnd;
       }
     }
     // drain: every copy this warp started has landed before the CTA exits
@@ -462,6 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       TaskEntry te;
       if (!take_task(sm, n++, te, a.status)) break;
       if (te.x < 0) break;
+      if (kFused && is_unroute(te)) continue;
       const int e = te.x & 0xffff, u = (te.x >> 16) & 0xffff, row0 = te.y, rows = te.z & 0xffff;
       const bool is_dn = ((te.z >> 16) & 1) != 0;
       if (is_dn) {
@@ -524,14 +542,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     (void)issued;
   } else if (warp == 2) {
-    // ------------- publisher: release each finished gate/up task's h rows -------------
+    // ------------- publisher: release each finished gate/up task's h rows (fused: and each
+    // finished down task's y rows, counted per stripe) -------------
     int n = 0, gu_n = 0;
     while (true) {
       TaskEntry te;
       if (!take_task(sm, n++, te, a.status)) break;
       if (te.x < 0) break;
-      if ((te.z >> 16) & 1) continue;  // down task: nothing to publish
-      const int u = (te.x >> 16) & 0xffff;
+      if (kFused && is_unroute(te)) continue;
+      const bool dn = ((te.z >> 16) & 1) != 0;
+      if (dn && !kFused) continue;  // down task, un-route in its own kernel: nothing to publish
+      uint32_t* ctr = dn ? a.dn_done + te.w : a.ready + ((te.x >> 16) & 0xffff);
       const int slot = gu_n % kPubSlots;
       const uint32_t ph = static_cast<uint32_t>((gu_n / kPubSlots) & 1);
       ++gu_n;
@@ -541,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(smem_addr(&sm.pub_full[slot]), ph, sm, a.status)) break;
       if (lane == 0) {
         fence_acq_rel_gpu();
-        red_add_relaxed_gpu_u32(a.ready + u, 1u);
+        red_add_relaxed_gpu_u32(ctr, 1u);
         trace_ev(a, 4, tcnt, 9, gu_n);
       }
       __syncwarp();
@@ -558,6 +579,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       TaskEntry te;
       if (!take_task(sm, n, te, a.status)) break;
       if (te.x < 0) break;
+      if constexpr (kFused) {
+        if (is_unroute(te)) {
+          ++n;
+          const int t = min(te.y + cw, a.T - 1), c = te.w * kDnRows + 4 * lane;
+          Unroute4Pre u;
+          unroute4_pre(a, t, c, u);
+          // every down task of the stripe (one per pass) has published its y columns
+          const uint32_t dn_per_stripe = static_cast<uint32_t>(__ldg(a.meta + META_NDN) / a.S_dn);
+          if (!warp_wait_counter(a.dn_done + te.w, dn_per_stripe, &sm.abort_flag, a.status, kTimeoutCycles)) break;
+          if (te.y + cw < a.T) unroute4_post(a, t, c, u);
+          continue;
+        }
+      }
       const int row0 = te.y, rows = te.z & 0xffff, s = te.w;
       const bool is_dn = ((te.z >> 16) & 1) != 0;
       const int K = is_dn ? a.F : a.d;
@@ -614,6 +648,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if constexpr (kFused) {
+          // hand the task to the publisher: the un-route waits for its stripe
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&sm.pub_full[gu_n % kPubSlots]));
+          ++gu_n;
+        }
       }
     }
   }
@@ -626,6 +666,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t expert_mma_smem_bytes() { return sizeof(Smem) + 1024; }
 
+// The un-route runs inside the kernel for at most this many tokens (measured: for more, the
+// separate un-route kernel after the expert kernel is faster).
+constexpr int kFuseMaxTokens = 8;
+
+int expert_mma_unroute_tasks(int T, int S_dn) {
+  return T <= kFuseMaxTokens ? S_dn * ((T + kComputeWarps - 1) / kComputeWarps) : 0;
+}
+
 bool expert_mma_supports(int d, int F) {
   const auto pow2_in_range = [](int v) { return v >= kChunk && v <= 2048 && (v & (v - 1)) == 0; };
   return pow2_in_range(d) && pow2_in_range(F);
@@ -635,11 +683,11 @@ cudaError_t launch_expert_mma(const ExpertArgs& a, const CUtensorMap& tm_w13, co
                               const CUtensorMap& tm_s13, const CUtensorMap& tm_s2, int num_sms,
                               cudaStream_t stream) {
   const size_t smem = expert_mma_smem_bytes();
-  cudaError_t err = cudaFuncSetAttribute(expert_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const ExpertArgs) =
+      a.ncb > 0 ? expert_mma_kernel<true> : expert_mma_kernel<false>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  return launch_pdl(expert_mma_kernel, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, tm_s13, tm_s2,
-                    a);
+  return launch_pdl(kern, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, tm_s13, tm_s2, a);
 }
 
 }  // namespace moe

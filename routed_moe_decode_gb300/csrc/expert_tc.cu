@@ -581,48 +581,9 @@ __global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x;
-  const int r = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
-  if (r >= a.d) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int* rp = a.route_pos + static_cast<size_t>(t) * a.k;
-  const float* rw = a.route_w + static_cast<size_t>(t) * a.k;
-  for (int j0 = 0; j0 < a.k; j0 += 8) {
-    // eight slots' loads in flight together, accumulated in slot order
-    int pos[8];
-    float w[8];
-    float4 yv[8];
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      pos[jj] = j0 + jj < a.k ? __ldg(rp + j0 + jj) : -1;
-      w[jj] = j0 + jj < a.k ? __ldg(rw + j0 + jj) : 0.f;
-    }
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj)
-      yv[jj] = pos[jj] >= 0 ? __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<size_t>(pos[jj]) * a.d + r))
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      if (pos[jj] < 0) continue;
-      acc.x += w[jj] * yv[jj].x;
-      acc.y += w[jj] * yv[jj].y;
-      acc.z += w[jj] * yv[jj].z;
-      acc.w += w[jj] * yv[jj].w;
-    }
-  }
-  const size_t o = static_cast<size_t>(t) * a.d + r;
-  float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (a.residual) {
-    const uint2 rb = *reinterpret_cast<const uint2*>(a.residual + o);
-    const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rb.x));
-    const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rb.y));
-    res = make_float4(r0.x, r0.y, r1.x, r1.y);
-  }
-  __nv_bfloat162 o0 = __floats2bfloat162_rn(res.x + acc.x, res.y + acc.y);
-  __nv_bfloat162 o1 = __floats2bfloat162_rn(res.z + acc.z, res.w + acc.w);
-  uint2 ob;
-  ob.x = *reinterpret_cast<uint32_t*>(&o0);
-  ob.y = *reinterpret_cast<uint32_t*>(&o1);
-  *reinterpret_cast<uint2*>(a.out + o) = ob;
+  const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+  if (c >= a.d) return;
+  unroute4(a, t, c);
 }
 
 cudaError_t launch_combine(const ExpertArgs& a, cudaStream_t stream) {
@@ -639,7 +600,7 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs p) {
   pdl_launch_dependents();
   const size_t gtid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
-  for (size_t i = gtid; i < static_cast<size_t>(p.E); i += nthreads) p.ready[i] = 0u;
+  for (size_t i = gtid; i < static_cast<size_t>(p.E + p.S_dn); i += nthreads) p.ready[i] = 0u;
   if (gtid == 0) *p.ticket = 0u;
   const size_t n8 = static_cast<size_t>(p.T) * p.d / 8;
   bool bad = false;
@@ -667,7 +628,8 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs p) {
 
 cudaError_t launch_prep(const PrepArgs& p, cudaStream_t stream) {
   const size_t n8 = static_cast<size_t>(p.T) * p.d / 8;
-  size_t work = n8 > static_cast<size_t>(p.E) ? n8 : static_cast<size_t>(p.E);
+  const size_t nr = static_cast<size_t>(p.E + p.S_dn);
+  size_t work = n8 > nr ? n8 : nr;
   int blocks = static_cast<int>((work + 255) / 256);
   if (blocks > 1184) blocks = 1184;
   if (blocks < 1) blocks = 1;

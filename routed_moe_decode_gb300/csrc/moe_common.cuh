@@ -79,7 +79,7 @@ inline WsLayout ws_layout(const moe_shape& s) {
   L.route_pos = take(size_t(L.R) * 4);
   L.pos_tok = take(size_t(L.R) * 4);
   L.route_w = take(size_t(L.R) * 4);
-  L.ready = take(size_t(s.E) * 4);
+  L.ready = take(size_t(s.E + L.S_dn) * 4);  // gate/up readiness [E], down completion per stripe [S_dn]
   L.ticket = take(4);
   L.tasks = take(size_t(L.max_tasks) * sizeof(TaskEntry));
   L.x16 = take(size_t(s.T) * s.d * 2);

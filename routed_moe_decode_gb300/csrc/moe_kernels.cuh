@@ -39,7 +39,7 @@ struct FrontArgs {
 constexpr int kFrontMaxRoutes = 16384;
 
 struct PrepArgs {
-  int T, d, E;
+  int T, d, E, S_dn;
   const __nv_bfloat16* hidden;
   __half* x16;
   uint32_t* ready;
@@ -66,15 +66,132 @@ struct ExpertArgs {
   const __half* x16;
   __half* hs16;
   float* y;
-  uint32_t* ready;
+  uint32_t* ready;    // per touched expert: gate/up tasks published
+  uint32_t* dn_done;  // per down stripe: down tasks published (ready + E)
   uint32_t* ticket;
   int* status;
   const __nv_bfloat16* residual;
   __nv_bfloat16* out;
+  int ncb;  // un-route tasks appended to the task order (0: the un-route runs as its own kernel)
   // optional timeline (diagnostics, off when null): per CTA kTraceRoles x kTracePerRole
   // uint64 events = event code << 56 | index << 40 | %globaltimer low 40 bits
   unsigned long long* trace;
 };
+
+// Un-route of four consecutive columns [c, c + 4) of token t: out = residual + sum_j w_{t,j}
+// y_{pos(t,j)}, FP32, slots in order, one BF16 rounding ("First implementation boundary",
+// step 4: routes summed in a fixed order).  The loads of eight slots are in flight together.
+// y is read past L1 (it may have been written by the calling kernel).  Shared by the un-route
+// kernel and the expert kernel's fused un-route, so both give the same bits.
+__device__ __forceinline__ void unroute4(const ExpertArgs& a, int t, int c) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int* rp = a.route_pos + static_cast<size_t>(t) * a.k;
+  const float* rw = a.route_w + static_cast<size_t>(t) * a.k;
+  for (int j0 = 0; j0 < a.k; j0 += 8) {
+    int pos[8];
+    float w[8];
+    float4 yv[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      pos[jj] = j0 + jj < a.k ? __ldg(rp + j0 + jj) : -1;
+      w[jj] = j0 + jj < a.k ? __ldg(rw + j0 + jj) : 0.f;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj)
+      yv[jj] = pos[jj] >= 0 ? __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<size_t>(pos[jj]) * a.d + c))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      if (pos[jj] < 0) continue;
+      acc.x += w[jj] * yv[jj].x;
+      acc.y += w[jj] * yv[jj].y;
+      acc.z += w[jj] * yv[jj].z;
+      acc.w += w[jj] * yv[jj].w;
+    }
+  }
+  const size_t o = static_cast<size_t>(t) * a.d + c;
+  float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (a.residual) {
+    const uint2 rb = *reinterpret_cast<const uint2*>(a.residual + o);
+    const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rb.x));
+    const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rb.y));
+    res = make_float4(r0.x, r0.y, r1.x, r1.y);
+  }
+  __nv_bfloat162 o0 = __floats2bfloat162_rn(res.x + acc.x, res.y + acc.y);
+  __nv_bfloat162 o1 = __floats2bfloat162_rn(res.z + acc.z, res.w + acc.w);
+  uint2 ob;
+  ob.x = *reinterpret_cast<uint32_t*>(&o0);
+  ob.y = *reinterpret_cast<uint32_t*>(&o1);
+  *reinterpret_cast<uint2*>(a.out + o) = ob;
+}
+
+// unroute4 in two halves for a caller that must wait for y: the slot positions and weights
+// of the first 16 slots and the residual are loaded before the wait (they do not depend on
+// y), the rest after it.  Same arithmetic in the same order as unroute4, so the same bits.
+struct Unroute4Pre {
+  int pos[16];
+  float w[16];
+  float4 res;
+};
+
+__device__ __forceinline__ void unroute4_pre(const ExpertArgs& a, int t, int c, Unroute4Pre& u) {
+  const int* rp = a.route_pos + static_cast<size_t>(t) * a.k;
+  const float* rw = a.route_w + static_cast<size_t>(t) * a.k;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    u.pos[j] = j < a.k ? __ldg(rp + j) : -1;
+    u.w[j] = j < a.k ? __ldg(rw + j) : 0.f;
+  }
+  u.res = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (a.residual) {
+    const uint2 rb = *reinterpret_cast<const uint2*>(a.residual + static_cast<size_t>(t) * a.d + c);
+    const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rb.x));
+    const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rb.y));
+    u.res = make_float4(r0.x, r0.y, r1.x, r1.y);
+  }
+}
+
+__device__ __forceinline__ void unroute4_post(const ExpertArgs& a, int t, int c, const Unroute4Pre& u) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int* rp = a.route_pos + static_cast<size_t>(t) * a.k;
+  const float* rw = a.route_w + static_cast<size_t>(t) * a.k;
+  for (int j0 = 0; j0 < a.k; j0 += 8) {
+    int pos[8];
+    float w[8];
+    float4 yv[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      if (j0 == 0) {
+        pos[jj] = u.pos[jj];
+        w[jj] = u.w[jj];
+      } else if (j0 == 8) {
+        pos[jj] = u.pos[8 + jj];
+        w[jj] = u.w[8 + jj];
+      } else {
+        pos[jj] = j0 + jj < a.k ? __ldg(rp + j0 + jj) : -1;
+        w[jj] = j0 + jj < a.k ? __ldg(rw + j0 + jj) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj)
+      yv[jj] = pos[jj] >= 0 ? __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<size_t>(pos[jj]) * a.d + c))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      if (pos[jj] < 0) continue;
+      acc.x += w[jj] * yv[jj].x;
+      acc.y += w[jj] * yv[jj].y;
+      acc.z += w[jj] * yv[jj].z;
+      acc.w += w[jj] * yv[jj].w;
+    }
+  }
+  __nv_bfloat162 o0 = __floats2bfloat162_rn(u.res.x + acc.x, u.res.y + acc.y);
+  __nv_bfloat162 o1 = __floats2bfloat162_rn(u.res.z + acc.z, u.res.w + acc.w);
+  uint2 ob;
+  ob.x = *reinterpret_cast<uint32_t*>(&o0);
+  ob.y = *reinterpret_cast<uint32_t*>(&o1);
+  *reinterpret_cast<uint2*>(a.out + static_cast<size_t>(t) * a.d + c) = ob;
+}
 
 constexpr int kTraceRoles = 8;
 constexpr int kTracePerRole = 128;
@@ -111,6 +228,8 @@ cudaError_t launch_expert_simt(const ExpertArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const ExpertArgs& a, cudaStream_t stream);
 size_t expert_tc_smem_bytes();
 size_t expert_mma_smem_bytes();
+// number of un-route tasks the decode kernel appends when it runs the un-route itself
+int expert_mma_unroute_tasks(int T, int S_dn);
 int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes);
 // Tensor map of a [rows, row_bytes] uint8 matrix (row_bytes a multiple of 16) loaded in
 // unswizzled boxes of 16 bytes x box_rows rows.

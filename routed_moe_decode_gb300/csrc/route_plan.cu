@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(1024) front_kernel(FrontArgs f) {
     convert_hidden(f, t0, nt, threadIdx.x, blockDim.x);
   }
   if (blockIdx.x == 0) {
-    for (int i = threadIdx.x; i < a.E; i += blockDim.x) f.ready[i] = 0u;
+    for (int i = threadIdx.x; i < a.E + a.S_dn; i += blockDim.x) f.ready[i] = 0u;
     if (threadIdx.x == 0) *f.ticket = 0u;
   }
   if (single) {
