@@ -283,9 +283,10 @@ def our_arm(args, cfg, dist, torch):
         moe.forward_prepare(shape, hidden[l], ws)
         moe.forward_experts(shape, Wd[l], resid[l], out, ws, algo)
 
-    # front kernel(s), expert kernel(s), un-route kernel
+    # front kernel(s), expert kernel(s), un-route kernel (none when the expert kernel runs it)
+    fused_unroute = moe.unroute_fused(shape, algo)
     front_kernels = 1 if fused_front else 3
-    kernels_per_step = front_kernels + (2 if algo == moe.ALGO_SIMT else 1) + 1
+    kernels_per_step = front_kernels + (2 if algo == moe.ALGO_SIMT else 1) + (0 if fused_unroute else 1)
 
     # ---- unique experts per layer (outside any timed region) ----
     U = []
@@ -300,6 +301,9 @@ def our_arm(args, cfg, dist, torch):
     # expert kernel besides the weights: FP16 hidden read, FP16 h written and read back,
     # FP32 per-route down outputs written
     act_bytes = cfg.T * cfg.d * 2 + 2 * R * cfg.ffn * 2 + R * cfg.d * 4
+    if fused_unroute:
+        # and the un-route: per-route outputs read back, positions and weights, residual, out
+        act_bytes += R * cfg.d * 4 + R * 8 + 2 * cfg.T * cfg.d * 2
     unique_bytes = [u * bpe for u in U]
 
     # ---- CUDA graphs: one of all L layers, one per single layer (for K % L) ----
@@ -373,9 +377,13 @@ def our_arm(args, cfg, dist, torch):
         moe.plan(shape, ids, wts, ws)
         moe.forward_prepare(shape, hidden[l], ws)
         starts[i].record()
-        moe.forward_expert_kernels(shape, Wd[l], ws, algo)
-        ends[i].record()
-        moe.forward_unroute(shape, resid[l], out, ws)
+        if fused_unroute:
+            moe.forward_experts(shape, Wd[l], resid[l], out, ws, algo)  # one kernel
+            ends[i].record()
+        else:
+            moe.forward_expert_kernels(shape, Wd[l], ws, algo)
+            ends[i].record()
+            moe.forward_unroute(shape, resid[l], out, ws)
         kbytes += unique_bytes[l] + act_bytes
     torch.cuda.synchronize()
     kdur_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
@@ -455,9 +463,12 @@ def our_arm(args, cfg, dist, torch):
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": f"{kname}_kernel" if kname else "simt kernels",
+                     "kernel": (f"{kname}_kernel" + ("<fused un-route>" if fused_unroute else "")) if kname
+                               else "simt kernels",
                      "kernel_us": 1e3 * k_avg_ms, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "algorithmic_bytes": "unique experts x NVFP4 bytes per expert + FP16 hidden + FP16 h (write+read) + FP32 per-route down outputs"},
+                     "algorithmic_bytes": "unique experts x NVFP4 bytes per expert + FP16 hidden + FP16 h (write+read) + FP32 per-route down outputs"
+                                          + (" (written and read back) + route positions and weights + BF16 residual and out"
+                                             if fused_unroute else "")},
         "clocks": clocks,
         "gpu_launches": kernels_per_step * K,
         "device_status": status,

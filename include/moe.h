@@ -128,6 +128,13 @@ MOE_API int moe_check_shape(const moe_shape* shape);
  * or a negative status when the shape is invalid.  Pure host function: needs no GPU. */
 MOE_API int moe_auto_algo(const moe_shape* shape);
 
+/* 1 if moe_forward_experts / moe_forward_algo / moe_layer with `algo` run the weighted
+ * un-route inside the expert kernel (the decode kernel does so for T <= 8: trailing
+ * un-route tasks that wait for the down tasks of their 128-column stripe), 0 if it runs as
+ * a kernel of its own after the expert kernel, or a negative status for an invalid shape
+ * or algo.  The two give identical bits.  Pure host function: needs no GPU. */
+MOE_API int moe_unroute_fused(const moe_shape* shape, int algo);
+
 /* Step 1, router ("Fused MoE routing"; "Router: selection and expert-task production").
  *   logits  [T, E]  float32, finite values (non-finite logits are outside the contract)
  *   ids     [T, k]  int32 out: selected experts in selection order (value desc, ties to

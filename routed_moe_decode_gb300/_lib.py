@@ -51,6 +51,7 @@ SIGNATURES = {
     "moe_workspace_init": (_I, [_P, ctypes.c_size_t, _P]),
     "moe_check_shape": (_I, [_SP]),
     "moe_auto_algo": (_I, [_SP]),
+    "moe_unroute_fused": (_I, [_SP, _I]),
     "moe_route_topk": (_I, [_SP, _P, _P, _P, _P]),
     "moe_plan": (_I, [_SP, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_forward": (_I, [_SP, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -122,6 +123,14 @@ def workspace_bytes(shape: Shape) -> int:
 
 def check_shape(shape: Shape) -> int:
     return int(lib().moe_check_shape(ctypes.byref(shape)))
+
+
+def unroute_fused(shape: Shape, algo: int = ALGO_AUTO) -> bool:
+    """True if the expert kernel of `algo` runs the un-route itself for `shape`."""
+    rc = int(lib().moe_unroute_fused(ctypes.byref(shape), int(algo)))
+    if rc < 0:
+        raise MoeError("moe_unroute_fused", rc)
+    return rc == 1
 
 
 def auto_algo(shape: Shape) -> int:

@@ -156,6 +156,7 @@ moe::ExpertArgs expert_args(const moe_shape* s, const WsLayout& L, void* ws, con
   a.route_pos = at<int>(ws, L.route_pos);
   a.route_w = at<float>(ws, L.route_w);
   a.tasks = at<moe::TaskEntry>(ws, L.tasks);
+  a.task_cap = L.max_tasks;
   a.x16 = at<__half>(ws, L.x16);
   a.hs16 = at<__half>(ws, L.hs16);
   a.y = at<float>(ws, L.y);
@@ -192,6 +193,16 @@ int moe_auto_algo(const moe_shape* shape) {
   const int rc = check_shape(shape);
   if (rc != MOE_OK) return rc < 0 ? rc : -rc;
   return moe::expert_mma_supports(shape->d, shape->ffn) ? MOE_ALGO_MMA : MOE_ALGO_TCGEN05;
+}
+
+int moe_unroute_fused(const moe_shape* shape, int algo) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc < 0 ? rc : -rc;
+  if (algo < MOE_ALGO_AUTO || algo > MOE_ALGO_MMA) return MOE_ERR_INVALID_ARG;
+  const bool mma_ok = moe::expert_mma_supports(shape->d, shape->ffn);
+  const bool use_mma = algo == MOE_ALGO_MMA || (algo == MOE_ALGO_AUTO && mma_ok);
+  if (!use_mma || !mma_ok) return 0;
+  return moe::expert_mma_unroute_tasks(shape->T, moe::ws_layout(*shape).S_dn) > 0 ? 1 : 0;
 }
 
 size_t moe_workspace_bytes(const moe_shape* shape) {

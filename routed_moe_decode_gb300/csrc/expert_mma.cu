@@ -16,11 +16,14 @@
 //               (512 B of FP16 hidden for gate/up, of h for down) into a padded tile;
 //   warp 2      publisher: after the compute warps have written a gate/up task's h rows it
 //               releases them to other CTAs (one fence and one reduction per task), so the
-//               compute warps never wait on the fence;
+//               compute warps never wait on the fence; with the un-route fused it releases
+//               each down task's y rows the same way, counted per 128-column stripe;
 //   warps 3-10  compute: each owns 16 weight rows of the 128-row tile.  Gate/up tasks give
 //               warp w gate rows of one 8-row group as fragment rows 0-7 and the up rows of
 //               the same F indices as fragment rows 8-15, so h = silu(g) * u is formed in
-//               registers.
+//               registers.  With the un-route fused (few tokens), trailing un-route tasks
+//               give each compute warp one token's 128 columns of one stripe, once every
+//               down task of that stripe has been released.
 // Fragment row g holds tile row 8w + frag_row(g): the permutation puts the two rows that
 // one 8-lane shared-memory phase reads on different halves of the 128-byte swizzle, so the
 // code reads are free of bank conflicts (the scale reads, 8 rows x 16 B, are too).
@@ -53,6 +56,10 @@ constexpr int kTaskConsumers = 2 + kComputeWarps;  // activation producer, publi
 // slot before waiting on that task), so twice as many publication slots never wrap early.
 constexpr int kPubSlots = 2 * kTaskSlots;
 constexpr long long kTimeoutCycles = 1ll << 33;
+// The producer claims its next task (ticket) only once at most kReserve of its chunks are
+// in flight: late enough that the last tasks go to whichever CTA frees up first, early
+// enough that the ticket and table round trips are hidden behind the chunks still queued.
+constexpr int kReserve = 4;
 
 struct Smem {
   uint8_t ring_a[kStagesA][kStageA];
@@ -382,19 +389,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) trace_ev(a, 5, tcnt, 10, 0);
 
   if (warp == 0) {
-    // ------------- task fetcher + weight producer (tickets two tasks ahead) -------------
+    // ------------- task fetcher + weight producer (next ticket taken late: kReserve) -------------
     const uint64_t pol = policy_evict_first();
     const int ntask = __ldg(a.meta + META_NGU) + __ldg(a.meta + META_NDN);
     const int ntot = ntask + (kFused ? a.ncb : 0);
     const TaskEntry kEnd = TaskEntry{-1, 0, 0, 0};
     int stage = 0, issued = 0, n = 0, chunk_seq = 0;
     uint32_t phase = 0;
-    int cur = blockIdx.x, nxt = ntot;
-    TaskEntry entry = kEnd, entry_nxt = kEnd;
-    if (lane == 0 && cur < ntot) {
-      entry = kFused ? task_at(a, cur, ntask) : a.tasks[cur];
-      nxt = static_cast<int>(atomicAdd(a.ticket, 1u)) + static_cast<int>(gridDim.x);
-      if (nxt < ntot) entry_nxt = kFused ? task_at(a, nxt, ntask) : a.tasks[nxt];
+    int cur = blockIdx.x;
+    TaskEntry entry = kEnd;
+    if (lane == 0) {
+      // the first entry is loaded alongside the task counts (the table has room for it)
+      const TaskEntry raw = a.tasks[min(cur, a.task_cap - 1)];
+      entry = cur < ntask ? raw : (cur < ntot ? task_at(a, cur, ntask) : kEnd);
     }
     bool ok = true;
     while (ok) {
@@ -414,8 +421,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int x = __shfl_sync(0xffffffffu, entry.x, 0);
       const int z = __shfl_sync(0xffffffffu, entry.z, 0);
       const int s = __shfl_sync(0xffffffffu, entry.w, 0);
-      int nxt2 = ntot;
-      if (lane == 0 && nxt < ntot) nxt2 = static_cast<int>(atomicAdd(a.ticket, 1u)) + static_cast<int>(gridDim.x);
       const int e = x & 0xffff;
       const bool is_dn = ((z >> 16) & 1) != 0;
       int rA0, rA1, nck;
@@ -451,11 +456,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++issued;
         if (++stage == kStagesA) { stage = 0; phase ^= 1u; }
       }
+      if (!ok) break;
+      // take the next ticket once at most kReserve chunks are in flight, so that a task is
+      // claimed shortly before this CTA can start it
+      if (issued > kReserve) {
+        const int sq = issued - 1 - kReserve + kStagesA;  // the issue that reuses that chunk's stage
+        if (!warp_wait(smem_addr(&sm.empty_a[sq % kStagesA]), static_cast<uint32_t>(((sq / kStagesA) & 1) ^ 1), sm,
+                       a.status)) {
+          ok = false;
+          break;
+        }
+      }
       if (lane == 0) {
-        cur = nxt;
-        entry = entry_nxt;
-        nxt = nxt2;
-        entry_nxt = nxt < ntot ? (kFused ? task_at(a, nxt, ntask) : a.tasks[nxt]) : kEnd;
+        cur = static_cast<int>(atomicAdd(a.ticket, 1u)) + static_cast<int>(gridDim.x);
+        entry = cur < ntot ? (kFused ? task_at(a, cur, ntask) : a.tasks[cur]) : kEnd;
       }
     }
     // drain: every copy this warp started has landed before the CTA exits

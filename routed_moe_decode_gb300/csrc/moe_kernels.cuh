@@ -73,6 +73,7 @@ struct ExpertArgs {
   const __nv_bfloat16* residual;
   __nv_bfloat16* out;
   int ncb;  // un-route tasks appended to the task order (0: the un-route runs as its own kernel)
+  int task_cap;  // entries the task table has room for
   // optional timeline (diagnostics, off when null): per CTA kTraceRoles x kTracePerRole
   // uint64 events = event code << 56 | index << 40 | %globaltimer low 40 bits
   unsigned long long* trace;

@@ -73,6 +73,19 @@ def test_auto_algo_selection(L):
         L.auto_algo(L.shape_of(4, 2000, 512, 512, 10))
 
 
+def test_unroute_fused_selection(L):
+    # the decode kernel runs the un-route itself for T <= 8; other kernels never do
+    assert L.unroute_fused(L.shape_of(4, 2048, 512, 512, 10))
+    assert L.unroute_fused(L.shape_of(8, 2048, 512, 512, 10), L.ALGO_MMA)
+    assert not L.unroute_fused(L.shape_of(9, 2048, 512, 512, 10))
+    assert not L.unroute_fused(L.shape_of(32, 2048, 512, 512, 10))
+    assert not L.unroute_fused(L.shape_of(4, 2048, 512, 512, 10), L.ALGO_TCGEN05)
+    assert not L.unroute_fused(L.shape_of(4, 2048, 512, 512, 10), L.ALGO_SIMT)
+    assert not L.unroute_fused(L.shape_of(4, 768, 512, 64, 8))
+    with pytest.raises(L.MoeError):
+        L.unroute_fused(L.shape_of(4, 2048, 512, 512, 10), 7)
+
+
 def test_bad_arguments_rejected_on_host(L):
     lib = L.lib()
     s = L.shape_of(4, 256, 128, 16, 2)
