@@ -42,8 +42,9 @@ MOE_API int moe_selftest_mma(const void* A, const void* B, float* D, moe_stream_
  * `trace`: per CTA 8 roles x 128 uint64 events (event code << 56 | index << 40 | low 40
  * bits of %globaltimer in ns); zero-initialise the buffer (multiProcessorCount x 8192 bytes).
  * Warp-MMA kernel: role 0 weight producer (1 task published, 2 chunk issued), 1 activation
- * producer (3 readiness met, 4 chunk issued), 4 publisher (9 gate/up task released),
- * 5 CTA (10 start, 11 end).  tcgen05 kernel: roles 0 and 1 as above, 2 first
+ * producer (3 readiness met, 4 chunk issued), 2 and 3 first and last compute warp (5 task
+ * taken, index bit 15 = down task; 6 chunks done; 12 un-route wait begins, 13 wait met),
+ * 4 publisher (9 task released), 5 CTA (10 start, 11 end).  tcgen05 kernel: roles 0 and 1 as above, 2 first
  * dequantisation warp (5 chunk landed, 6 chunk in tensor memory), 3 MMA (7 chunk issued),
  * 4 epilogue (8 accumulator ready, 9 task done), 5 CTA (10 start, 11 end). */
 MOE_API int moe_selftest_expert_trace(const moe_shape* shape, const uint8_t* w13_codes,

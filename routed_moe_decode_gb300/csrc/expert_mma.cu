@@ -589,6 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ComputeState cs{0, 0, 0u};
     int n = 0, gu_n = 0;
     bool ok = true;
+    // timeline (diagnostics only): the first and the last compute warp record task boundaries
+    const bool tr = a.trace != nullptr && lane == 0 && (cw == 0 || cw == kComputeWarps - 1);
+    const int trole = cw == 0 ? 2 : 3;
     while (ok) {
       TaskEntry te;
       if (!take_task(sm, n, te, a.status)) break;
@@ -601,11 +604,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           unroute4_pre(a, t, c, u);
           // every down task of the stripe (one per pass) has published its y columns
           const uint32_t dn_per_stripe = static_cast<uint32_t>(__ldg(a.meta + META_NDN) / a.S_dn);
+          if (tr) trace_ev(a, trole, tcnt, 12, n);
           if (!warp_wait_counter(a.dn_done + te.w, dn_per_stripe, &sm.abort_flag, a.status, kTimeoutCycles)) break;
+          if (tr) trace_ev(a, trole, tcnt, 13, n);
           if (te.y + cw < a.T) unroute4_post(a, t, c, u);
           continue;
         }
       }
+      if (tr) trace_ev(a, trole, tcnt, 5, (((te.z >> 16) & 1) << 15) | (n & 0x7fff));
       const int row0 = te.y, rows = te.z & 0xffff, s = te.w;
       const bool is_dn = ((te.z >> 16) & 1) != 0;
       const int K = is_dn ? a.F : a.d;
@@ -624,6 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       else if (mode == 2) ok = run_chunks<2>(sm, a, cs, acc, lra, lrb, nck, nt, rows, g, q);
       else ok = run_chunks<0>(sm, a, cs, acc, lra, lrb, nck, nt, rows, g, q);
       if (!ok) break;
+      if (tr) trace_ev(a, trole, tcnt, 6, n);
       ++n;
       // ---- epilogue: fragment rows g / g+8, routed rows 8t + 2q, 8t + 2q + 1 ----
       if (!is_dn) {
