@@ -49,7 +49,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=None)
     p.add_argument("--config", default="b1", choices=sorted(mi.CONFIGS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--algo", default="auto", choices=["auto", "mma", "tcgen05", "simt"])
+    p.add_argument("--algo", default="auto", choices=["auto", "mma", "tcgen05", "simt", "wide"])
     p.add_argument("--layers", type=int, default=None, help="weight sets cycled (default 12)")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -241,7 +241,8 @@ def our_arm(args, cfg, dist, torch):
     import routed_moe_decode_gb300 as moe
     dev = torch.device(f"cuda:{dist.local}")
     torch.cuda.set_device(dev)
-    algo = {"auto": moe.ALGO_AUTO, "mma": moe.ALGO_MMA, "tcgen05": moe.ALGO_TCGEN05, "simt": moe.ALGO_SIMT}[args.algo]
+    algo = {"auto": moe.ALGO_AUTO, "mma": moe.ALGO_MMA, "tcgen05": moe.ALGO_TCGEN05, "simt": moe.ALGO_SIMT,
+            "wide": moe.ALGO_WIDE}[args.algo]
     L = args.layers if args.layers is not None else min(12, max(1, cfg.layers))
     K = args.steps if args.steps is not None else DEFAULT_STEPS[cfg.name]
     W = args.warmup if args.warmup is not None else max(3, 2 * L)
@@ -390,7 +391,8 @@ def our_arm(args, cfg, dist, torch):
     k_avg_ms = sum(kdur_ms) / Kk
     achieved = kbytes / Kk / (k_avg_ms * 1e-3) / 1e9
     peak, peak_kind = load_peaks()
-    kname = {moe.ALGO_AUTO: "expert_mma", moe.ALGO_MMA: "expert_mma", moe.ALGO_TCGEN05: "expert_tc"}.get(algo)
+    kname = {moe.ALGO_AUTO: "expert_mma", moe.ALGO_MMA: "expert_mma", moe.ALGO_TCGEN05: "expert_tc",
+             moe.ALGO_WIDE: "expert_wide"}.get(algo)
     traffic = profiled_traffic(cfg.name, kname) if kname else None
 
     # ---- end to end through the public C-ABI call with host buffers ----

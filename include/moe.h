@@ -95,12 +95,17 @@ typedef enum moe_algo {
                             dequantisation into tensor memory, tcgen05 MMA (FP32 accumulate),
                             16-row column groups, readiness counters between gate/up and down */
   MOE_ALGO_SIMT = 2,     /* CUDA-core kernels, one launch per stage (ablation baseline) */
-  MOE_ALGO_MMA = 3       /* persistent stripe kernel: TMA weight stream, in-register NVFP4
+  MOE_ALGO_MMA = 3,      /* persistent stripe kernel: TMA weight stream, in-register NVFP4
                             dequantisation into the A fragments of warp-level m16n8k16 tensor-core
                             MMAs (weights stationary, routed rows as the 8-wide operand, FP32
                             accumulate), gate and up of one F index in one warp, readiness
                             counters between gate/up and down; needs d and ffn powers of two from
                             256 to 2048 (MOE_ERR_UNSUPPORTED otherwise) */
+  MOE_ALGO_WIDE = 4      /* persistent stripe kernel for many routed rows per expert (prefill
+                            chunks): as MOE_ALGO_TCGEN05, but up to 192 routed rows per weight
+                            pass in one tcgen05 MMA per 16-element K step (N = rows rounded up
+                            to 16), two tensor-memory accumulators so that a task's epilogue
+                            overlaps the next task's MMAs */
 } moe_algo;
 
 /* Human-readable name of a status code (static string, never NULL). */

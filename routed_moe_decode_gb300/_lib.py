@@ -31,6 +31,7 @@ ALGO_AUTO = 0
 ALGO_TCGEN05 = 1
 ALGO_SIMT = 2
 ALGO_MMA = 3
+ALGO_WIDE = 4
 
 # Every function declared in include/moe.h, with (restype, argtypes).
 _P = ctypes.c_void_p

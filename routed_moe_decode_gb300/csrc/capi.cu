@@ -198,10 +198,10 @@ int moe_auto_algo(const moe_shape* shape) {
 int moe_unroute_fused(const moe_shape* shape, int algo) {
   const int rc = check_shape(shape);
   if (rc != MOE_OK) return rc < 0 ? rc : -rc;
-  if (algo < MOE_ALGO_AUTO || algo > MOE_ALGO_MMA) return MOE_ERR_INVALID_ARG;
+  if (algo < MOE_ALGO_AUTO || algo > MOE_ALGO_WIDE) return MOE_ERR_INVALID_ARG;
   const bool mma_ok = moe::expert_mma_supports(shape->d, shape->ffn);
   const bool use_mma = algo == MOE_ALGO_MMA || (algo == MOE_ALGO_AUTO && mma_ok);
-  if (!use_mma || !mma_ok) return 0;
+  if (!use_mma || !mma_ok) return 0;  // MOE_ALGO_WIDE, MOE_ALGO_TCGEN05, MOE_ALGO_SIMT
   return moe::expert_mma_unroute_tasks(shape->T, moe::ws_layout(*shape).S_dn) > 0 ? 1 : 0;
 }
 
@@ -298,7 +298,7 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     return MOE_ERR_INVALID_ARG;
   if ((stages & kStageUnroute) && (!out || !aligned(out, 16) || (residual && !aligned(residual, 16))))
     return MOE_ERR_INVALID_ARG;
-  if (algo < MOE_ALGO_AUTO || algo > MOE_ALGO_MMA) return MOE_ERR_INVALID_ARG;
+  if (algo < MOE_ALGO_AUTO || algo > MOE_ALGO_WIDE) return MOE_ERR_INVALID_ARG;
   rc = check_ws(shape, workspace, workspace_bytes);
   if (rc != MOE_OK) return rc;
   const WsLayout L = moe::ws_layout(*shape);
@@ -325,7 +325,8 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
   if (rc != MOE_OK) return rc;
   const bool mma_ok = moe::expert_mma_supports(shape->d, shape->ffn);
   if (algo == MOE_ALGO_MMA && !mma_ok) return MOE_ERR_UNSUPPORTED;
-  const bool use_mma = algo == MOE_ALGO_MMA || (algo == MOE_ALGO_AUTO && mma_ok);
+  const bool use_wide = algo == MOE_ALGO_WIDE;
+  const bool use_mma = !use_wide && (algo == MOE_ALGO_MMA || (algo == MOE_ALGO_AUTO && mma_ok));
   const uint32_t box = use_mma ? 128u : 64u;
   CUtensorMap tm13, tm2;
   rc = encode_codes_map(&tm13, w13_codes, static_cast<uint64_t>(shape->d) / 2,
@@ -347,6 +348,16 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     e = moe::launch_expert_mma(a, tm13, tm2, ts13, ts2, di.num_sms, stream);
     if (e != cudaSuccess) { set_error("expert_mma launch", e); return MOE_ERR_CUDA; }
     if (a.ncb > 0) return MOE_OK;
+  } else if (use_wide) {
+    // the wide kernel's own task table (passes of kWideRows rows), from the plan's arrays
+    moe::TaskEntry* tasks_w = at<moe::TaskEntry>(workspace, L.tasks_w);
+    e = moe::launch_wide_plan(a, tasks_w, stream);
+    if (e != cudaSuccess) { set_error("wide plan launch", e); return MOE_ERR_CUDA; }
+    moe::ExpertArgs aw = a;
+    aw.tasks = tasks_w;
+    aw.task_cap = L.max_tasks_w;
+    e = moe::launch_expert_wide(aw, tm13, tm2, di.num_sms, stream);
+    if (e != cudaSuccess) { set_error("expert_wide launch", e); return MOE_ERR_CUDA; }
   } else {
     e = moe::launch_expert_tc(a, tm13, tm2, di.num_sms, stream);
     if (e != cudaSuccess) { set_error("expert_tc launch", e); return MOE_ERR_CUDA; }
@@ -397,7 +408,7 @@ int moe_forward_algo(const moe_shape* shape, const void* hidden, const uint8_t* 
   if (shape->T == 0) return MOE_OK;
   if (!hidden || !w13_codes || !w13_scales || !w2_codes || !w2_scales || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned(hidden, 16)) return MOE_ERR_INVALID_ARG;
-  if (algo < MOE_ALGO_AUTO || algo > MOE_ALGO_MMA) return MOE_ERR_INVALID_ARG;
+  if (algo < MOE_ALGO_AUTO || algo > MOE_ALGO_WIDE) return MOE_ERR_INVALID_ARG;
   rc = check_ws(shape, workspace, workspace_bytes);
   if (rc != MOE_OK) return rc;
   rc = moe_forward_prepare(shape, hidden, workspace, workspace_bytes, stream);

@@ -1,0 +1,564 @@
+// Expert kernel for many routed rows per expert (prefill chunks): the weight-stripe task of
+// the persistent tcgen05 kernel, with up to kWideRows (192) routed rows per weight pass in
+// ONE tcgen05.mma per 16-element K step (N = the pass's rows rounded up to 16).
+//
+// "Persistent execution for Flash-Next GGUF on SM70", sections "MonoMoE" and "First
+// implementation boundary", restated for sm_103a: one resident CTA per SM takes tasks through
+// a ticket counter; every gate/up task precedes every down task, so a CTA that waits on a down
+// task only waits for work resident CTAs already hold.  A task streams one 128-row stripe of
+// one touched expert's NVFP4 weights once per pass, whatever the pass's row count.
+//
+// Warp roles (384 threads):
+//   0-3   epilogue: thread i owns accumulator lane i; gate/up tasks hand the up values to the
+//         gate threads through shared memory (16 columns at a time) and store FP16 h; down
+//         tasks store per-route FP32 outputs (summed by the un-route kernel in slot order);
+//   4-7   dequantisation: thread i owns A row i; each 128-K chunk of E2M1 codes (TMA tile,
+//         64-byte swizzle) and its E4M3 block scales become exact FP16 in registers and are
+//         stored into tensor memory, where they are the A operand (M = 128);
+//   8     task fetcher + weight producer (TMA codes, cp.async scales);
+//   9-10  activation producers: the pass's routed rows (FP16 hidden rows for gate/up, FP16 h
+//         rows for down) copied 16 bytes at a time into 128-byte swizzled K-major tiles, the B
+//         operand (N up to 192);
+//   11    MMA issuer and tensor-memory owner: 8 kind::f16 MMAs per chunk into one of two
+//         accumulator buffers, so the epilogue of a task overlaps the next task's MMAs.
+// Tensor memory (512 columns): two A buffers of 64 columns, two accumulators of 192 columns.
+#include "moe_kernels.cuh"
+
+namespace moe {
+
+namespace wd {
+
+constexpr int kStagesA = 6;                          // weight ring (codes + scales)
+constexpr int kStagesB = 3;                          // activation ring (one chunk each)
+constexpr int kStageCodes = 8192;                    // 2 halves x 64 rows x 64 B (SWIZZLE_64B)
+constexpr int kStageScales = 1024;                   // 128 rows x 8 B
+constexpr int kStageA = kStageCodes + kStageScales;  // 9216, a multiple of 1024
+constexpr int kAtomB = kWideRows * 128;              // one 64-K atom of a B tile (24576 B)
+constexpr int kStageB = 2 * kAtomB;                  // a 128-K chunk of up to 192 rows
+constexpr int kNumA = 2;                             // A buffers (64 columns each)
+constexpr int kNumD = 2;                             // accumulators (kWideRows columns each)
+constexpr int kDCol0 = kNumA * 64;
+constexpr int kTmemCols = 512;
+constexpr int kTaskSlots = 8;
+constexpr int kActWarps = 2;
+constexpr int kTaskConsumers = kActWarps + 4 + 1 + 4;  // activation, dequant, MMA, epilogue warps
+constexpr int kThreads = 384;
+constexpr int kWarpFetch = 8, kWarpAct0 = 9, kWarpMma = 11;
+constexpr long long kTimeoutCycles = 1ll << 33;
+
+static_assert(kDCol0 + kNumD * kWideRows <= kTmemCols, "tensor memory budget");
+static_assert(kWideRows % 16 == 0 && kWideRows <= 256, "MMA N limit");
+
+struct Smem {
+  uint8_t ring_b[kStagesB][kStageB];
+  uint8_t ring_a[kStagesA][kStageA];
+  float xch[16 * 64];              // up-projection values handed to the gate threads
+  int rowoff[kActWarps][kWideRows / kActWarps];  // per activation warp: element offsets of its rows
+  TaskEntry task[kTaskSlots];
+  uint64_t full_a[kStagesA];
+  uint64_t empty_a[kStagesA];
+  uint64_t full_b[kStagesB];
+  uint64_t empty_b[kStagesB];
+  uint64_t a_full[kNumA];
+  uint64_t a_empty[kNumA];
+  uint64_t d_full[kNumD];
+  uint64_t d_empty[kNumD];
+  uint64_t task_full[kTaskSlots];
+  uint64_t task_empty[kTaskSlots];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct Task {
+  bool valid, is_dn;
+  int e, u, row0, rows, s, nck;
+};
+
+__device__ __forceinline__ Task unpack(const TaskEntry& t, const ExpertArgs& a) {
+  Task k;
+  k.valid = t.x >= 0;
+  k.e = t.x & 0xffff;
+  k.u = (t.x >> 16) & 0xffff;
+  k.row0 = t.y;
+  k.rows = t.z & 0xffff;
+  k.is_dn = ((t.z >> 16) & 1) != 0;
+  k.s = t.w;
+  k.nck = k.is_dn ? a.nck_dn : a.nck_gu;
+  return k;
+}
+
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) return false;
+    if (clock64() - t0 > kTimeoutCycles) {
+      *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
+      atomicOr(status, static_cast<int>(MOE_DEV_TIMEOUT));
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status) {
+  const bool ok = bounded_wait(bar, parity, sm, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* status) {
+  const int q = n % kTaskSlots;
+  const uint32_t ph = static_cast<uint32_t>((n / kTaskSlots) & 1);
+  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, sm, status)) return false;
+  out = sm.task[q];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&sm.task_empty[q]));
+  return true;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+
+__device__ __forceinline__ __half h_store_value(float h, int* status) {
+  float v = h * kHScale;
+  if (fabsf(v) > 65504.f) {
+    atomicOr(status, static_cast<int>(MOE_DEV_H_SATURATED));
+    v = copysignf(65504.f, v);
+  }
+  return __float2half_rn(v);
+}
+
+// MMA N for a pass of `rows` routed rows: a multiple of 16 (kind::f16 with M = 128).
+__device__ __forceinline__ int mma_n(int rows) { return (rows + 15) & ~15; }
+
+}  // namespace wd
+
+using namespace wd;
+
+// ---------------------------------------------------------------------------------
+// Task table of the wide kernel, built from the plan's per-expert arrays (touched list,
+// counts, offsets): per touched expert, passes of kWideRows rows; all gate/up tasks
+// (touched order, pass, stripe) first, then all down tasks.  One 1024-thread CTA, one thread
+// per touched expert (U <= E <= 1024).
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) wide_plan_kernel(const int* meta_in, int* meta, const int* touched,
+                                                         const int* counts, const int* offsets, TaskEntry* tasks,
+                                                         int S_gu, int S_dn) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ int s_warp[32];
+  __shared__ int s_total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int U = __ldcg(meta_in + META_U);
+  int e = 0, m = 0, np = 0;
+  if (tid < U) {
+    e = __ldcg(touched + tid);
+    m = __ldcg(counts + e);
+    np = (m + kWideRows - 1) / kWideRows;
+  }
+  // exclusive scan of the pass counts over the block
+  int incl = np;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    s_warp[lane] = wi - w;  // exclusive prefix of the warp totals
+    if (lane == 31) s_total = wi;
+  }
+  __syncthreads();
+  const int before = s_warp[warp] + incl - np;
+  const int total = s_total;
+  if (tid < U) {
+    const int base = __ldcg(offsets + e);
+    int gi = before * S_gu;
+    int di = total * S_gu + before * S_dn;
+    for (int p = 0; p < np; ++p) {
+      const int rows = min(kWideRows, m - p * kWideRows);
+      const int z = rows | (np > 1 ? 1 << 17 : 0);
+      const int row0 = base + p * kWideRows;
+      for (int s2 = 0; s2 < S_gu; ++s2) tasks[gi++] = TaskEntry{e | (tid << 16), row0, z, s2};
+      for (int s2 = 0; s2 < S_dn; ++s2) tasks[di++] = TaskEntry{e | (tid << 16), row0, z | (1 << 16), s2};
+    }
+  }
+  if (tid == 0) {
+    meta[META_WGU] = total * S_gu;
+    meta[META_WDN] = total * S_dn;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    expert_wide_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_w2,
+                       const __grid_constant__ ExpertArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kStagesA; ++i) {
+      mbar_init(smem_addr(&sm.full_a[i]), 33);  // 32 cp.async arrivals + 1 expect_tx arrival
+      mbar_init(smem_addr(&sm.empty_a[i]), 4);  // the four dequantisation warps
+    }
+    for (int i = 0; i < kStagesB; ++i) {
+      mbar_init(smem_addr(&sm.full_b[i]), 32 * kActWarps);
+      mbar_init(smem_addr(&sm.empty_b[i]), 1);  // MMA commit
+    }
+    for (int i = 0; i < kNumA; ++i) {
+      mbar_init(smem_addr(&sm.a_full[i]), 4);
+      mbar_init(smem_addr(&sm.a_empty[i]), 1);
+    }
+    for (int i = 0; i < kNumD; ++i) {
+      mbar_init(smem_addr(&sm.d_full[i]), 1);
+      mbar_init(smem_addr(&sm.d_empty[i]), 4);
+    }
+    for (int i = 0; i < kTaskSlots; ++i) {
+      mbar_init(smem_addr(&sm.task_full[i]), 1);
+      mbar_init(smem_addr(&sm.task_empty[i]), kTaskConsumers);
+    }
+    mbar_init(smem_addr(&sm.drain), 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpFetch && lane == 0) {
+    prefetch_tmap(&tm_w13);
+    prefetch_tmap(&tm_w2);
+  }
+  // everything above is local to the CTA; the task table and the counters come from the
+  // preceding kernels
+  pdl_wait();
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const uint32_t ringa0 = smem_addr(&sm.ring_a[0][0]);
+  const uint32_t ringb0 = smem_addr(&sm.ring_b[0][0]);
+
+  if (warp == kWarpFetch) {
+    // ------------- task fetcher + weight producer: TMA code tiles, cp.async scales -------------
+    // The ticket of task i+2 is taken when task i starts and its entry loaded when task i
+    // ends, so neither latency stalls the copies.
+    const uint64_t pol = policy_evict_first();
+    const int ntot = __ldcg(a.meta + META_WGU) + __ldcg(a.meta + META_WDN);
+    const TaskEntry kEnd = TaskEntry{-1, 0, 0, 0};
+    int stage = 0, issued = 0, n = 0;
+    uint32_t phase = 0;
+    int cur = blockIdx.x, nxt = ntot;
+    TaskEntry entry = kEnd, entry_nxt = kEnd;
+    if (lane == 0 && cur < ntot) {
+      entry = a.tasks[cur];
+      nxt = static_cast<int>(atomicAdd(a.ticket, 1u)) + static_cast<int>(gridDim.x);
+      if (nxt < ntot) entry_nxt = a.tasks[nxt];
+    }
+    bool ok = true;
+    while (ok) {
+      const int q = n % kTaskSlots;
+      if (!warp_wait(smem_addr(&sm.task_empty[q]), static_cast<uint32_t>(((n / kTaskSlots) & 1) ^ 1), sm,
+                     a.status)) {
+        ok = false;
+        break;
+      }
+      const bool live = __shfl_sync(0xffffffffu, cur, 0) < ntot;
+      if (lane == 0) {
+        sm.task[q] = live ? entry : kEnd;
+        mbar_arrive(smem_addr(&sm.task_full[q]));
+      }
+      ++n;
+      if (!live) break;
+      const int x = __shfl_sync(0xffffffffu, entry.x, 0);
+      const int z = __shfl_sync(0xffffffffu, entry.z, 0);
+      const int s = __shfl_sync(0xffffffffu, entry.w, 0);
+      int nxt2 = ntot;
+      if (lane == 0 && nxt < ntot) nxt2 = static_cast<int>(atomicAdd(a.ticket, 1u)) + static_cast<int>(gridDim.x);
+      const int e = x & 0xffff;
+      const bool is_dn = ((z >> 16) & 1) != 0;
+      const int rA0 = is_dn ? e * a.d + s * kDnRows : e * 2 * a.F + s * kGuRows;
+      const int rA1 = is_dn ? rA0 + 64 : rA0 + a.F;
+      const int sstride = is_dn ? a.F / 16 : a.d / 16;
+      const CUtensorMap* tm = is_dn ? &tm_w2 : &tm_w13;
+      const uint8_t* sbase = is_dn ? a.w2_scales : a.w13_scales;
+      const int nck = is_dn ? a.nck_dn : a.nck_gu;
+      for (int c = 0; c < nck; ++c) {
+        if (!warp_wait(smem_addr(&sm.empty_a[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
+        const int kb = c * kChunkK;
+        const uint32_t sb = ringa0 + stage * kStageA;
+        const uint32_t fa = smem_addr(&sm.full_a[stage]);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fa, kStageCodes);
+          tma_load_2d(sb, tm, kb / 2, rA0, fa, pol);
+          tma_load_2d(sb + kStageCodes / 2, tm, kb / 2, rA1, fa, pol);
+        }
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const int i = lane + 32 * qq;
+          const int grow = i < 64 ? rA0 + i : rA1 + (i - 64);
+          cp_async_8(sb + kStageCodes + i * 8, sbase + static_cast<size_t>(grow) * sstride + kb / 16);
+        }
+        cp_async_arrive_noinc(fa);
+        ++issued;
+        if (++stage == kStagesA) { stage = 0; phase ^= 1u; }
+      }
+      if (lane == 0) {
+        cur = nxt;
+        entry = entry_nxt;
+        nxt = nxt2;
+        entry_nxt = nxt < ntot ? a.tasks[nxt] : kEnd;
+      }
+    }
+    cp_async_wait_all();
+    // drain: the last phase issued on every stage has landed before the CTA exits
+    if (lane == 0) {
+      int st = stage;
+      uint32_t ph = phase;
+      for (int i = 0; i < min(issued, kStagesA); ++i) {
+        if (--st < 0) { st = kStagesA - 1; ph ^= 1u; }
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kTimeoutCycles) {}
+      }
+    }
+  } else if (warp == kWarpAct0 || warp == kWarpAct0 + 1) {
+    // ------------- activation producers: the pass's routed rows via cp.async -------------
+    // Lane L (0..63 over both warps) copies 16-byte granule L % 16 of rows r0 + L / 16,
+    // r0 = 0, 4, 8, ...: warp aw serves the rows r with (r % 4) / 2 == aw, and keeps their
+    // source offsets in its own table.
+    const int aw = warp - kWarpAct0;
+    const int L = 32 * aw + lane;
+    const int gi = L & 15, atom = gi >> 3, ch = gi & 7;
+    int* rowoff = sm.rowoff[aw];
+    int stage = 0, n = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    while (ok) {
+      TaskEntry te;
+      if (!take_task(sm, n++, te, a.status)) break;
+      const Task tk = unpack(te, a);
+      if (!tk.valid) break;
+      if (tk.is_dn) {
+        // every gate/up stripe of this expert (all passes) has published its h rows
+        const int npass = (__ldg(a.counts + tk.e) + kWideRows - 1) / kWideRows;
+        const uint32_t target = static_cast<uint32_t>(npass * a.S_gu);
+        if (!warp_wait_counter(a.ready + tk.u, target, &sm.abort_flag, a.status, kTimeoutCycles)) break;
+      }
+      for (int idx = lane; idx < kWideRows / kActWarps; idx += 32) {
+        const int r = (idx >> 1) * 4 + 2 * aw + (idx & 1);
+        int off = 0;
+        if (r < tk.rows)
+          off = tk.is_dn ? (tk.row0 + r) * a.F : __ldg(a.pos_tok + tk.row0 + r) * a.d;
+        rowoff[idx] = off;
+      }
+      __syncwarp();
+      const __half* src_base = tk.is_dn ? a.hs16 : a.x16;
+      const int N = mma_n(tk.rows);
+      for (int c = 0; ok && c < tk.nck; ++c) {
+        if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
+        const uint32_t bbase = ringb0 + stage * kStageB + atom * kAtomB;
+        const int kb = c * kChunkK + gi * 8;
+        for (int r0 = 0; r0 < N; r0 += 4) {
+          const int r = r0 + (L >> 4);
+          if (r < tk.rows) {
+            const int idx = (r >> 2) * 2 + (r & 1);
+            const __half* src = src_base + rowoff[idx] + kb;
+            cp_async_16(bbase + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4), src);
+          }
+        }
+        cp_async_arrive_noinc(smem_addr(&sm.full_b[stage]));
+        if (++stage == kStagesB) { stage = 0; phase ^= 1u; }
+      }
+      __syncwarp();
+    }
+    cp_async_wait_all();
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- dequantisation: NVFP4 -> FP16 A tile in tensor memory ----------------
+    const int i = tid - 128;  // A row of this thread (= tensor-memory lane)
+    const int half = i >> 6, r = i & 63;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    int stage = 0, abuf = 0, n = 0;
+    uint32_t phase = 0, aphase = 0;
+    bool ok = true;
+    while (ok) {
+      TaskEntry te;
+      if (!take_task(sm, n++, te, a.status)) break;
+      const Task tk = unpack(te, a);
+      if (!tk.valid) break;
+      for (int c = 0; c < tk.nck; ++c) {
+        if (!warp_wait(smem_addr(&sm.full_a[stage]), phase, sm, a.status)) { ok = false; break; }
+        const uint8_t* st = &sm.ring_a[stage][0];
+        const uint8_t* crow = st + half * (kStageCodes / 2) + r * 64;
+        uint4 q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) q[j] = *reinterpret_cast<const uint4*>(crow + ((j ^ ((r >> 1) & 3)) << 4));
+        const uint2 sc = *reinterpret_cast<const uint2*>(st + kStageCodes + i * 8);
+        uint32_t v[64];
+        const uint32_t sp[4] = {e4m3x2_to_f16x2(sc.x), e4m3x2_to_f16x2(sc.x >> 16), e4m3x2_to_f16x2(sc.y),
+                                e4m3x2_to_f16x2(sc.y >> 16)};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t w[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int wi = 4 * j + h;  // word of the row chunk (8 elements)
+            const int blk = wi >> 1;   // 16-element scale block
+            const uint32_t sraw = (blk & 1) ? bcast_hi_half(sp[blk >> 1]) : bcast_lo_half(sp[blk >> 1]);
+            uint32_t o0, o1, o2, o3;
+            e2m1x8_to_f16x2x4(w[h], o0, o1, o2, o3);
+            v[4 * wi + 0] = hmul2_bits(o0, sraw);
+            v[4 * wi + 1] = hmul2_bits(o1, sraw);
+            v[4 * wi + 2] = hmul2_bits(o2, sraw);
+            v[4 * wi + 3] = hmul2_bits(o3, sraw);
+          }
+        }
+        // the weight stage is consumed (its bytes are in registers): hand it back
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.empty_a[stage]));
+        if (!warp_wait(smem_addr(&sm.a_empty[abuf]), aphase ^ 1u, sm, a.status)) { ok = false; break; }
+        tc_fence_after();
+        tmem_st_x64(tmem + lane_base + abuf * 64, v);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.a_full[abuf]));
+        if (++stage == kStagesA) { stage = 0; phase ^= 1u; }
+        if (++abuf == kNumA) { abuf = 0; aphase ^= 1u; }
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------- MMA issuer (one lane; the whole warp takes the tasks) ----------------
+    int stage = 0, abuf = 0, dbuf = 0, n = 0;
+    uint32_t phase = 0, aphase = 0, dphase = 0;
+    bool ok = true;
+    while (ok) {
+      TaskEntry te;
+      if (!take_task(sm, n++, te, a.status)) break;
+      const Task tk = unpack(te, a);
+      if (!tk.valid) break;
+      if (lane == 0) {
+        const uint32_t idesc = idesc_f16_f32(128, mma_n(tk.rows));
+        if (!bounded_wait(smem_addr(&sm.d_empty[dbuf]), dphase ^ 1u, sm, a.status)) ok = false;
+        tc_fence_after();
+        const uint32_t dcol = tmem + kDCol0 + dbuf * kWideRows;
+        for (int c = 0; ok && c < tk.nck; ++c) {
+          if (!bounded_wait(smem_addr(&sm.a_full[abuf]), aphase, sm, a.status)) { ok = false; break; }
+          if (!bounded_wait(smem_addr(&sm.full_b[stage]), phase, sm, a.status)) { ok = false; break; }
+          tc_fence_after();
+          fence_proxy_async_smem();
+          const uint32_t bbase = ringb0 + stage * kStageB;
+#pragma unroll
+          for (int kk = 0; kk < kChunkK / 16; ++kk) {
+            const uint64_t bdesc = smem_desc_sw128(bbase + (kk >> 2) * kAtomB + (kk & 3) * 32, 1024);
+            tc_mma_f16_ts(dcol, tmem + abuf * 64 + kk * 8, bdesc, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_addr(&sm.empty_b[stage]));
+          tc_commit(smem_addr(&sm.a_empty[abuf]));
+          if (++stage == kStagesB) { stage = 0; phase ^= 1u; }
+          if (++abuf == kNumA) { abuf = 0; aphase ^= 1u; }
+        }
+        if (ok) tc_commit(smem_addr(&sm.d_full[dbuf]));
+      }
+      if (++dbuf == kNumD) { dbuf = 0; dphase ^= 1u; }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0) {
+      // every issued MMA completes before tensor memory is released
+      tc_commit(smem_addr(&sm.drain));
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_addr(&sm.drain), 0) && clock64() - t0 < kTimeoutCycles) {}
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 0-3): thread i owns accumulator lane i ----------------
+    const int i = tid;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    int dbuf = 0, n = 0;
+    uint32_t dphase = 0;
+    while (true) {
+      TaskEntry te;
+      const bool got_task = take_task(sm, n++, te, a.status);
+      if (!named_bar_and(2, 128, got_task)) break;
+      const Task tk = unpack(te, a);
+      if (!tk.valid) break;
+      const bool got = warp_wait(smem_addr(&sm.d_full[dbuf]), dphase, sm, a.status);
+      if (!named_bar_and(2, 128, got)) break;
+      tc_fence_after();
+      const uint32_t dcol = tmem + lane_base + kDCol0 + dbuf * kWideRows;
+      const float sc13 = a.w13_ts, sc2 = a.w2_ts * kHUnscale;
+      for (int c0 = 0; c0 < tk.rows; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_x16(dcol + c0, v);
+        tc_wait_ld();
+        if (!tk.is_dn) {
+          // gate rows are lanes 0-63, the up rows of the same F indices lanes 64-127
+          if (i >= 64) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sm.xch[j * 64 + (i - 64)] = __uint_as_float(v[j]);
+          }
+          named_bar_sync(1, 128);
+          if (i < 64) {
+            __half* hcol = a.hs16 + static_cast<size_t>(tk.row0) * a.F + tk.s * kGuRows + i;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (c0 + j < tk.rows)
+                hcol[static_cast<size_t>(c0 + j) * a.F] =
+                    h_store_value(silu_mul(__uint_as_float(v[j]) * sc13, sm.xch[j * 64 + i] * sc13), a.status);
+            }
+          }
+          named_bar_sync(1, 128);
+        } else {
+          float* ycol = a.y + static_cast<size_t>(tk.row0) * a.d + tk.s * kDnRows + i;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < tk.rows) ycol[static_cast<size_t>(c0 + j) * a.d] = __uint_as_float(v[j]) * sc2;
+        }
+      }
+      // the accumulator is read: hand it back to the MMA warp
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&sm.d_empty[dbuf]));
+      if (++dbuf == kNumD) { dbuf = 0; dphase ^= 1u; }
+      if (!tk.is_dn) {
+        // publish this stripe's h rows (release) for the down tasks of the expert
+        if (i < 64) __threadfence();
+        named_bar_sync(1, 128);
+        if (i == 0) atom_add_acqrel_u32(a.ready + tk.u, 1u);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+size_t expert_wide_smem_bytes() { return sizeof(Smem) + 1024; }
+
+cudaError_t launch_expert_wide(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
+                               int num_sms, cudaStream_t stream) {
+  const size_t smem = expert_wide_smem_bytes();
+  cudaError_t err = cudaFuncSetAttribute(expert_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  return launch_pdl(expert_wide_kernel, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, a);
+}
+
+cudaError_t launch_wide_plan(const ExpertArgs& a, TaskEntry* tasks_w, cudaStream_t stream) {
+  return launch_pdl(wide_plan_kernel, dim3(1), dim3(1024), 0, stream, a.meta, const_cast<int*>(a.meta), a.touched,
+                    a.counts, a.offsets, tasks_w, a.S_gu, a.S_dn);
+}
+
+}  // namespace moe

@@ -27,6 +27,7 @@ constexpr int kDnRows = 128;        // d-rows per down task
 constexpr int kRowsPerPass = 64;    // token rows handled per pass (4 MMA groups of 16)
 constexpr int kGroupRows = 16;      // MMA N per group
 constexpr int kMaxGroups = kRowsPerPass / kGroupRows;
+constexpr int kWideRows = 192;      // routed rows per pass of the wide (many-rows) kernel
 constexpr float kHScale = 0.0625f;  // h is stored as FP16(h * 2^-4)
 constexpr float kHUnscale = 16.0f;
 
@@ -37,16 +38,17 @@ constexpr float kHUnscale = 16.0f;
 
 struct WsLayout {
   size_t status, meta, counts, offsets, touched, gu_start, dn_start, route_pos, pos_tok, route_w;
-  size_t ready, ticket, tasks, x16, hs16, y, total;
+  size_t ready, ticket, tasks, tasks_w, x16, hs16, y, total;
   size_t front_done;  // arrival counter of the fused front, inside the zeroed status block
   int S_gu;       // gate/up stripes per expert (ffn / 64)
   int S_dn;       // down stripes per expert (d / 128)
   int max_tasks;  // capacity of the task table
+  int max_tasks_w;  // capacity of the wide kernel's task table (passes of kWideRows rows)
   int R;          // routes = T * k
 };
 
 // meta words
-enum { META_U = 0, META_NGU = 1, META_NDN = 2, META_MAXROWS = 3, META_WORDS = 8 };
+enum { META_U = 0, META_NGU = 1, META_NDN = 2, META_MAXROWS = 3, META_WGU = 4, META_WDN = 5, META_WORDS = 8 };
 
 // One expert task as the plan writes it (16 bytes):
 //   x = expert id | touched index << 16, y = first routed row (expert-major position),
@@ -66,6 +68,7 @@ inline WsLayout ws_layout(const moe_shape& s) {
   // passes over all experts: at most one per touched expert plus one per 64 extra rows
   const int max_passes = s.E + (L.R + kRowsPerPass - 1) / kRowsPerPass;
   L.max_tasks = max_passes * (L.S_gu + L.S_dn);
+  L.max_tasks_w = (s.E + (L.R + kWideRows - 1) / kWideRows) * (L.S_gu + L.S_dn);
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   L.status = take(64);
@@ -82,6 +85,7 @@ inline WsLayout ws_layout(const moe_shape& s) {
   L.ready = take(size_t(s.E + L.S_dn) * 4);  // gate/up readiness [E], down completion per stripe [S_dn]
   L.ticket = take(4);
   L.tasks = take(size_t(L.max_tasks) * sizeof(TaskEntry));
+  L.tasks_w = take(size_t(L.max_tasks_w) * sizeof(TaskEntry));
   L.x16 = take(size_t(s.T) * s.d * 2);
   L.hs16 = take(size_t(L.R) * s.ffn * 2);
   L.y = take(size_t(L.R) * s.d * 4);

@@ -226,6 +226,12 @@ cudaError_t launch_expert_mma(const ExpertArgs& a, const CUtensorMap& tm_w13, co
                               const CUtensorMap& tm_s13, const CUtensorMap& tm_s2, int num_sms,
                               cudaStream_t stream);
 cudaError_t launch_expert_simt(const ExpertArgs& a, cudaStream_t stream);
+// The many-rows kernel: its task table (passes of kWideRows rows) is built from the plan's
+// per-expert arrays by launch_wide_plan, then launch_expert_wide runs with a.tasks = that table.
+cudaError_t launch_wide_plan(const ExpertArgs& a, TaskEntry* tasks_w, cudaStream_t stream);
+cudaError_t launch_expert_wide(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
+                               int num_sms, cudaStream_t stream);
+size_t expert_wide_smem_bytes();
 cudaError_t launch_combine(const ExpertArgs& a, cudaStream_t stream);
 size_t expert_tc_smem_bytes();
 size_t expert_mma_smem_bytes();

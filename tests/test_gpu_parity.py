@@ -16,7 +16,7 @@ from oracle import oracle as O
 
 pytestmark = pytest.mark.gpu
 
-ALGOS = {"auto": 0, "tcgen05": 1, "simt": 2, "mma": 3}
+ALGOS = {"auto": 0, "tcgen05": 1, "simt": 2, "mma": 3, "wide": 4}
 
 # tokens checked against the oracle at full size (all tokens when None)
 SAMPLES = {
@@ -89,7 +89,7 @@ def test_fused_front_matches_separate_calls(T, d, F, E, k):
     assert moe.plan_summary(fused.shape, fused.ws) == moe.plan_summary(sep.shape, sep.ws)
 
 
-@pytest.mark.parametrize("algo", ["mma", "tcgen05", "simt"])
+@pytest.mark.parametrize("algo", ["mma", "tcgen05", "simt", "wide"])
 def test_split_expert_and_unroute_calls(algo):
     # moe_forward_expert_kernels + moe_forward_unroute == moe_forward_experts, bit for bit
     import routed_moe_decode_gb300 as moe
@@ -116,6 +116,22 @@ def test_layer_parity_tcgen05(name):
     _check_layer(cfg, config_inputs(name), ALGOS["tcgen05"], SAMPLES[name])
 
 
+@pytest.mark.parametrize("name", ["tiny", "b1", "b8", "b64", "prefill"])
+def test_layer_parity_wide(name):
+    cfg = mi.CONFIGS[name]
+    _check_layer(cfg, config_inputs(name), ALGOS["wide"], SAMPLES[name])
+
+
+@pytest.mark.parametrize("T,d,F,E,k", [(400, 256, 128, 4, 2), (1000, 512, 256, 8, 2), (300, 384, 384, 3, 1),
+                                       (385, 256, 256, 2, 1), (17, 128, 128, 1, 1), (190, 1024, 512, 32, 32)])
+def test_wide_path_many_rows(T, d, F, E, k):
+    # (400, .., E=4, k=2): ~200 rows per expert, (1000, .., 8, 2): ~250, (385, .., 2, 1): two
+    # passes of 192 and a ragged third; (190, .., 32, 32): every expert holds all 190 rows
+    cfg = mi.CONFIGS["tiny"].replace(name=f"wide{T}x{d}x{F}x{E}x{k}", T=T, d=d, ffn=F, E=E, k=k, tag=300 + T)
+    inp = mi.gen_layer(cfg, seed=6)
+    _check_layer(cfg, inp, ALGOS["wide"])
+
+
 @pytest.mark.parametrize("name", ["tiny", "b1", "b8"])
 def test_layer_parity_simt(name):
     cfg = mi.CONFIGS[name]
@@ -135,6 +151,7 @@ def test_ragged_and_edge_shapes(T, d, F, E, k):
     inp = mi.gen_layer(cfg, seed=3)
     _check_layer(cfg, inp, ALGOS["auto"])
     _check_layer(cfg, inp, ALGOS["tcgen05"])
+    _check_layer(cfg, inp, ALGOS["wide"])
 
 
 @pytest.mark.parametrize("T,d,F,E,k", [(1, 256, 256, 16, 1), (5, 512, 256, 16, 2), (33, 512, 512, 64, 8),
