@@ -160,6 +160,17 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
+def load_tensor_peak():
+    """Dense FP16/BF16 tensor peak in TFLOP/s for a kernel timed alone (the burst figure):
+    kind::f16 MMAs run FP16 and BF16 operands at the same rate."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), "measured cuBLAS bf16 GEMM (burst)"
+    return 1900.0, "fallback bf16 (burst)"
+
+
 def profiled_traffic(config: str, kernel: str):
     """DRAM bytes per expert-kernel launch from the committed ncu summary of this workload,
     or None if there is none or the kernel source changed since it was captured."""
@@ -218,6 +229,20 @@ def reference_arm(args, cfg, dist):
     inp = mi.gen_layer(cfg, seed=0, layer=0)
     n, el = time_oracle(cfg, inp, budget_s=120.0, max_steps=steps, warmup=warm)
     value = n / el
+    roofline_hbm = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "peak_kind": f"{peak_kind} copy bandwidth",
+                    "algorithmic_bytes": "unique experts x NVFP4 bytes per expert + FP16 hidden + FP16 h (write+read) + "
+                                         "FP32 per-route down outputs"
+                                         + (" (written and read back) + route positions and weights + BF16 residual and out"
+                                            if fused_unroute else "")}
+    # the wide kernel is a dense contraction: 2 flops per weight per routed row, gate/up
+    # (2F x d) and down (d x F) for each of the T * k routes
+    tpeak, tpeak_kind = load_tensor_peak()
+    tflops = 6.0 * R * cfg.d * cfg.ffn / (k_avg_ms * 1e-3) / 1e12
+    roofline_tensor = {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
+                       "peak_kind": tpeak_kind, "mma": "tcgen05 kind::f16 (FP16 x FP16 -> FP32)",
+                       "algorithmic_flops": "6 x T x k x d x ffn per launch",
+                       "hbm_achieved_gbs": achieved, "hbm_frac": achieved / peak}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": n,
         "warmup": warm, "ms_per_step": 1e3 * el / n, "higher_is_better": True, "scaling": "weak",
@@ -286,8 +311,11 @@ def our_arm(args, cfg, dist, torch):
 
     # front kernel(s), expert kernel(s), un-route kernel (none when the expert kernel runs it)
     fused_unroute = moe.unroute_fused(shape, algo)
+    run_algo = moe.auto_algo(shape) if algo == moe.ALGO_AUTO else algo
     front_kernels = 1 if fused_front else 3
-    kernels_per_step = front_kernels + (2 if algo == moe.ALGO_SIMT else 1) + (0 if fused_unroute else 1)
+    # the SIMT path runs two expert kernels, the wide kernel one plus its task-table kernel
+    expert_kernels = 2 if run_algo in (moe.ALGO_SIMT, moe.ALGO_WIDE) else 1
+    kernels_per_step = front_kernels + expert_kernels + (0 if fused_unroute else 1)
 
     # ---- unique experts per layer (outside any timed region) ----
     U = []
@@ -391,8 +419,7 @@ def our_arm(args, cfg, dist, torch):
     k_avg_ms = sum(kdur_ms) / Kk
     achieved = kbytes / Kk / (k_avg_ms * 1e-3) / 1e9
     peak, peak_kind = load_peaks()
-    kname = {moe.ALGO_AUTO: "expert_mma", moe.ALGO_MMA: "expert_mma", moe.ALGO_TCGEN05: "expert_tc",
-             moe.ALGO_WIDE: "expert_wide"}.get(algo)
+    kname = {moe.ALGO_MMA: "expert_mma", moe.ALGO_TCGEN05: "expert_tc", moe.ALGO_WIDE: "expert_wide"}.get(run_algo)
     traffic = profiled_traffic(cfg.name, kname) if kname else None
 
     # ---- end to end through the public C-ABI call with host buffers ----
@@ -437,6 +464,20 @@ def our_arm(args, cfg, dist, torch):
                "sample": f"{n} single-token steps of layer 0 ({cfg.name}) through the FP32 C++ oracle, "
                          f"{el:.1f} s on 1 host thread"}
 
+    roofline_hbm = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "peak_kind": f"{peak_kind} copy bandwidth",
+                    "algorithmic_bytes": "unique experts x NVFP4 bytes per expert + FP16 hidden + FP16 h (write+read) + "
+                                         "FP32 per-route down outputs"
+                                         + (" (written and read back) + route positions and weights + BF16 residual and out"
+                                            if fused_unroute else "")}
+    # the wide kernel is a dense contraction: 2 flops per weight per routed row, gate/up
+    # (2F x d) and down (d x F) for each of the T * k routes
+    tpeak, tpeak_kind = load_tensor_peak()
+    tflops = 6.0 * R * cfg.d * cfg.ffn / (k_avg_ms * 1e-3) / 1e12
+    roofline_tensor = {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
+                       "peak_kind": tpeak_kind, "mma": "tcgen05 kind::f16 (FP16 x FP16 -> FP32)",
+                       "algorithmic_flops": "6 x T x k x d x ffn per launch",
+                       "hbm_achieved_gbs": achieved, "hbm_frac": achieved / peak}
     line = {
         "metric": METRIC,
         "value": value,
@@ -463,18 +504,16 @@ def our_arm(args, cfg, dist, torch):
             "hbm_frac_layer": (mean_unique / (us_per_layer * 1e-6) / 1e9) / peak,
             "input_gen_s": round(t_gen, 1),
         },
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": (f"{kname}_kernel" + ("<fused un-route>" if fused_unroute else "")) if kname
-                               else "simt kernels",
-                     "kernel_us": 1e3 * k_avg_ms, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "algorithmic_bytes": "unique experts x NVFP4 bytes per expert + FP16 hidden + FP16 h (write+read) + FP32 per-route down outputs"
-                                          + (" (written and read back) + route positions and weights + BF16 residual and out"
-                                             if fused_unroute else "")},
+        "roofline": roofline_hbm if run_algo != moe.ALGO_WIDE else roofline_tensor,
         "clocks": clocks,
         "gpu_launches": kernels_per_step * K,
         "device_status": status,
     }
+    line["roofline"].update({"traffic": traffic,
+                     "kernel": (f"{kname}_kernel" + ("<fused un-route>" if fused_unroute else "")
+                                + (" (after its task-table kernel)" if run_algo == moe.ALGO_WIDE else "")) if kname
+                               else "simt kernels",
+                     "kernel_us": 1e3 * k_avg_ms})
     if e2e is not None:
         line["e2e"] = e2e
     if cpu is not None:

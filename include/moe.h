@@ -89,8 +89,10 @@ typedef struct moe_shape {
 
 /* Expert-kernel selection for moe_forward_algo. */
 typedef enum moe_algo {
-  MOE_ALGO_AUTO = 0,     /* MOE_ALGO_MMA where it applies (d and ffn powers of two from 256 to
-                            2048), MOE_ALGO_TCGEN05 otherwise */
+  MOE_ALGO_AUTO = 0,     /* MOE_ALGO_WIDE when the routes average at least 32 rows per expert
+                            (T * k >= 32 * E, e.g. prefill chunks), else MOE_ALGO_MMA where it
+                            applies (d and ffn powers of two from 256 to 2048), else
+                            MOE_ALGO_TCGEN05 */
   MOE_ALGO_TCGEN05 = 1,  /* persistent stripe kernel: TMA weight stream, in-register NVFP4
                             dequantisation into tensor memory, tcgen05 MMA (FP32 accumulate),
                             16-row column groups, readiness counters between gate/up and down */
@@ -129,7 +131,8 @@ MOE_API int moe_workspace_init(void* workspace, size_t workspace_bytes, moe_stre
  * MOE_ERR_UNSUPPORTED. */
 MOE_API int moe_check_shape(const moe_shape* shape);
 
-/* The expert kernel MOE_ALGO_AUTO selects for a shape (MOE_ALGO_MMA or MOE_ALGO_TCGEN05),
+/* The expert kernel MOE_ALGO_AUTO selects for a shape (MOE_ALGO_WIDE, MOE_ALGO_MMA or
+ * MOE_ALGO_TCGEN05),
  * or a negative status when the shape is invalid.  Pure host function: needs no GPU. */
 MOE_API int moe_auto_algo(const moe_shape* shape);
 

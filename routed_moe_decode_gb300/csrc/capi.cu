@@ -189,10 +189,20 @@ const char* moe_last_cuda_error(void) { return g_last_error; }
 
 int moe_check_shape(const moe_shape* shape) { return check_shape(shape); }
 
+// The kernel MOE_ALGO_AUTO runs: the wide tcgen05 kernel when the routes average at least
+// kWideAutoRows rows per expert (prefill chunks: each weight pass is then a real dense
+// contraction), else the warp-MMA decode kernel where its shape limits allow, else the
+// 16-row-group tcgen05 kernel.
+constexpr int kWideAutoRows = 32;
+static int auto_choice(const moe_shape* s) {
+  if (static_cast<long long>(s->T) * s->k >= static_cast<long long>(kWideAutoRows) * s->E) return MOE_ALGO_WIDE;
+  return moe::expert_mma_supports(s->d, s->ffn) ? MOE_ALGO_MMA : MOE_ALGO_TCGEN05;
+}
+
 int moe_auto_algo(const moe_shape* shape) {
   const int rc = check_shape(shape);
   if (rc != MOE_OK) return rc < 0 ? rc : -rc;
-  return moe::expert_mma_supports(shape->d, shape->ffn) ? MOE_ALGO_MMA : MOE_ALGO_TCGEN05;
+  return auto_choice(shape);
 }
 
 int moe_unroute_fused(const moe_shape* shape, int algo) {
@@ -200,8 +210,8 @@ int moe_unroute_fused(const moe_shape* shape, int algo) {
   if (rc != MOE_OK) return rc < 0 ? rc : -rc;
   if (algo < MOE_ALGO_AUTO || algo > MOE_ALGO_WIDE) return MOE_ERR_INVALID_ARG;
   const bool mma_ok = moe::expert_mma_supports(shape->d, shape->ffn);
-  const bool use_mma = algo == MOE_ALGO_MMA || (algo == MOE_ALGO_AUTO && mma_ok);
-  if (!use_mma || !mma_ok) return 0;  // MOE_ALGO_WIDE, MOE_ALGO_TCGEN05, MOE_ALGO_SIMT
+  const int run = algo == MOE_ALGO_AUTO ? auto_choice(shape) : algo;
+  if (run != MOE_ALGO_MMA || !mma_ok) return 0;  // MOE_ALGO_WIDE, MOE_ALGO_TCGEN05, MOE_ALGO_SIMT
   return moe::expert_mma_unroute_tasks(shape->T, moe::ws_layout(*shape).S_dn) > 0 ? 1 : 0;
 }
 
@@ -325,8 +335,9 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
   if (rc != MOE_OK) return rc;
   const bool mma_ok = moe::expert_mma_supports(shape->d, shape->ffn);
   if (algo == MOE_ALGO_MMA && !mma_ok) return MOE_ERR_UNSUPPORTED;
-  const bool use_wide = algo == MOE_ALGO_WIDE;
-  const bool use_mma = !use_wide && (algo == MOE_ALGO_MMA || (algo == MOE_ALGO_AUTO && mma_ok));
+  const int run = algo == MOE_ALGO_AUTO ? auto_choice(shape) : algo;
+  const bool use_wide = run == MOE_ALGO_WIDE;
+  const bool use_mma = run == MOE_ALGO_MMA;
   const uint32_t box = use_mma ? 128u : 64u;
   CUtensorMap tm13, tm2;
   rc = encode_codes_map(&tm13, w13_codes, static_cast<uint64_t>(shape->d) / 2,

@@ -8,18 +8,20 @@
 // task only waits for work resident CTAs already hold.  A task streams one 128-row stripe of
 // one touched expert's NVFP4 weights once per pass, whatever the pass's row count.
 //
-// Warp roles (384 threads):
-//   0-3   epilogue: thread i owns accumulator lane i; gate/up tasks hand the up values to the
-//         gate threads through shared memory (16 columns at a time) and store FP16 h; down
-//         tasks store per-route FP32 outputs (summed by the un-route kernel in slot order);
-//   4-7   dequantisation: thread i owns A row i; each 128-K chunk of E2M1 codes (TMA tile,
+// Warp roles (576 threads):
+//   0-7   epilogue, two groups of four warps taking alternate 32-column slices of an
+//         accumulator; thread t owns accumulator lane t % 128.  Gate/up tasks exchange half of
+//         the gate and up values between the lane halves through shared memory, so that all
+//         128 threads of a group form h = silu(g) * u (FP16); down tasks store per-route FP32
+//         outputs (summed by the un-route kernel in slot order);
+//   8-11  dequantisation: thread i owns A row i; each 128-K chunk of E2M1 codes (TMA tile,
 //         64-byte swizzle) and its E4M3 block scales become exact FP16 in registers and are
 //         stored into tensor memory, where they are the A operand (M = 128);
-//   8     task fetcher + weight producer (TMA codes, cp.async scales);
-//   9-10  activation producers: the pass's routed rows (FP16 hidden rows for gate/up, FP16 h
+//   12    task fetcher + weight producer (TMA codes, cp.async scales);
+//   13-16 activation producers: the pass's routed rows (FP16 hidden rows for gate/up, FP16 h
 //         rows for down) copied 16 bytes at a time into 128-byte swizzled K-major tiles, the B
 //         operand (N up to 192);
-//   11    MMA issuer and tensor-memory owner: 8 kind::f16 MMAs per chunk into one of two
+//   17    MMA issuer and tensor-memory owner: 8 kind::f16 MMAs per chunk into one of two
 //         accumulator buffers, so the epilogue of a task overlaps the next task's MMAs.
 // Tensor memory (512 columns): two A buffers of 64 columns, two accumulators of 192 columns.
 #include "moe_kernels.cuh"
@@ -40,10 +42,14 @@ constexpr int kNumD = 2;                             // accumulators (kWideRows 
 constexpr int kDCol0 = kNumA * 64;
 constexpr int kTmemCols = 512;
 constexpr int kTaskSlots = 8;
-constexpr int kActWarps = 2;
-constexpr int kTaskConsumers = kActWarps + 4 + 1 + 4;  // activation, dequant, MMA, epilogue warps
-constexpr int kThreads = 384;
-constexpr int kWarpFetch = 8, kWarpAct0 = 9, kWarpMma = 11;
+constexpr int kActWarps = 4;
+constexpr int kEpiWarps = 8;   // two groups of four: alternate 32-column slices of an accumulator
+constexpr int kWarpDeq0 = kEpiWarps;                           // 8-11
+constexpr int kWarpFetch = kWarpDeq0 + 4;                      // 12
+constexpr int kWarpAct0 = kWarpFetch + 1;                      // 13-16
+constexpr int kWarpMma = kWarpAct0 + kActWarps;                // 17
+constexpr int kThreads = 32 * (kWarpMma + 1);                  // 576
+constexpr int kTaskConsumers = kActWarps + 4 + 1 + kEpiWarps;  // activation, dequant, MMA, epilogue warps
 constexpr long long kTimeoutCycles = 1ll << 33;
 
 static_assert(kDCol0 + kNumD * kWideRows <= kTmemCols, "tensor memory budget");
@@ -52,7 +58,7 @@ static_assert(kWideRows % 16 == 0 && kWideRows <= 256, "MMA N limit");
 struct Smem {
   uint8_t ring_b[kStagesB][kStageB];
   uint8_t ring_a[kStagesA][kStageA];
-  float xch[16 * 64];              // up-projection values handed to the gate threads
+  float xch[2][32 * 64];           // per epilogue group: gate/up values exchanged between lane halves
   int rowoff[kActWarps][kWideRows / kActWarps];  // per activation warp: element offsets of its rows
   TaskEntry task[kTaskSlots];
   uint64_t full_a[kStagesA];
@@ -116,8 +122,6 @@ __device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* 
   if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&sm.task_empty[q]));
   return true;
 }
-
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
 __device__ __forceinline__ __half h_store_value(float h, int* status) {
   float v = h * kHScale;
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kNumD; ++i) {
       mbar_init(smem_addr(&sm.d_full[i]), 1);
-      mbar_init(smem_addr(&sm.d_empty[i]), 4);
+      mbar_init(smem_addr(&sm.d_empty[i]), kEpiWarps);
     }
     for (int i = 0; i < kTaskSlots; ++i) {
       mbar_init(smem_addr(&sm.task_full[i]), 1);
@@ -330,14 +334,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kTimeoutCycles) {}
       }
     }
-  } else if (warp == kWarpAct0 || warp == kWarpAct0 + 1) {
+  } else if (warp >= kWarpAct0 && warp < kWarpAct0 + kActWarps) {
     // ------------- activation producers: the pass's routed rows via cp.async -------------
-    // Lane L (0..63 over both warps) copies 16-byte granule L % 16 of rows r0 + L / 16,
-    // r0 = 0, 4, 8, ...: warp aw serves the rows r with (r % 4) / 2 == aw, and keeps their
-    // source offsets in its own table.
+    // Lane L (0..127 over the four warps) copies 16-byte granule L % 16 of rows r0 + L / 16,
+    // r0 = 0, 8, 16, ...: warp aw serves the rows r with (r % 8) / 2 == aw and keeps their
+    // source offsets in its own table (entry (r / 8) * 2 + r % 2).
     const int aw = warp - kWarpAct0;
     const int L = 32 * aw + lane;
     const int gi = L & 15, atom = gi >> 3, ch = gi & 7;
+    const int rsub = L >> 4;  // row within each group of 8 rows
     int* rowoff = sm.rowoff[aw];
     int stage = 0, n = 0;
     uint32_t phase = 0;
@@ -354,26 +359,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait_counter(a.ready + tk.u, target, &sm.abort_flag, a.status, kTimeoutCycles)) break;
       }
       for (int idx = lane; idx < kWideRows / kActWarps; idx += 32) {
-        const int r = (idx >> 1) * 4 + 2 * aw + (idx & 1);
-        int off = 0;
-        if (r < tk.rows)
-          off = tk.is_dn ? (tk.row0 + r) * a.F : __ldg(a.pos_tok + tk.row0 + r) * a.d;
+        const int r = (idx >> 1) * 8 + 2 * aw + (idx & 1);
+        int off = -1;
+        if (r < tk.rows) off = tk.is_dn ? (tk.row0 + r) * a.F : __ldg(a.pos_tok + tk.row0 + r) * a.d;
         rowoff[idx] = off;
       }
       __syncwarp();
       const __half* src_base = tk.is_dn ? a.hs16 : a.x16;
-      const int N = mma_n(tk.rows);
+      const int ngroups = (tk.rows + 7) / 8;
       for (int c = 0; ok && c < tk.nck; ++c) {
         if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
-        const uint32_t bbase = ringb0 + stage * kStageB + atom * kAtomB;
+        const uint32_t bbase = ringb0 + stage * kStageB + atom * kAtomB + rsub * 128 + ((ch ^ rsub) << 4);
         const int kb = c * kChunkK + gi * 8;
-        for (int r0 = 0; r0 < N; r0 += 4) {
-          const int r = r0 + (L >> 4);
-          if (r < tk.rows) {
-            const int idx = (r >> 2) * 2 + (r & 1);
-            const __half* src = src_base + rowoff[idx] + kb;
-            cp_async_16(bbase + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4), src);
-          }
+        // eight row groups per batch: the offsets are read first, then the copies issued
+        for (int g0 = 0; g0 < ngroups; g0 += 8) {
+          int off[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) off[u] = g0 + u < ngroups ? rowoff[(g0 + u) * 2 + (rsub & 1)] : -1;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (off[u] >= 0) cp_async_16(bbase + (g0 + u) * 1024, src_base + off[u] + kb);
         }
         cp_async_arrive_noinc(smem_addr(&sm.full_b[stage]));
         if (++stage == kStagesB) { stage = 0; phase ^= 1u; }
@@ -381,9 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
     cp_async_wait_all();
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= kWarpDeq0 && warp < kWarpDeq0 + 4) {
     // ---------------- dequantisation: NVFP4 -> FP16 A tile in tensor memory ----------------
-    const int i = tid - 128;  // A row of this thread (= tensor-memory lane)
+    const int i = tid - 32 * kWarpDeq0;  // A row of this thread (= tensor-memory lane)
     const int half = i >> 6, r = i & 63;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     int stage = 0, abuf = 0, n = 0;
@@ -479,47 +484,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue (warps 0-3): thread i owns accumulator lane i ----------------
-    const int i = tid;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // ---------------- epilogue (warps 0-7): thread t owns accumulator lane t % 128 ----------------
+    const int i = tid & 127;   // accumulator lane
+    const int grp = tid >> 7;  // slices 2k + grp of 32 columns
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    float* xch = sm.xch[grp];
     int dbuf = 0, n = 0;
     uint32_t dphase = 0;
     while (true) {
       TaskEntry te;
       const bool got_task = take_task(sm, n++, te, a.status);
-      if (!named_bar_and(2, 128, got_task)) break;
+      if (!named_bar_and(2, 32 * kEpiWarps, got_task)) break;
       const Task tk = unpack(te, a);
       if (!tk.valid) break;
       const bool got = warp_wait(smem_addr(&sm.d_full[dbuf]), dphase, sm, a.status);
-      if (!named_bar_and(2, 128, got)) break;
+      if (!named_bar_and(2, 32 * kEpiWarps, got)) break;
       tc_fence_after();
       const uint32_t dcol = tmem + lane_base + kDCol0 + dbuf * kWideRows;
       const float sc13 = a.w13_ts, sc2 = a.w2_ts * kHUnscale;
-      for (int c0 = 0; c0 < tk.rows; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld_x16(dcol + c0, v);
+      for (int c0 = 32 * grp; c0 < tk.rows; c0 += 64) {
+        uint32_t v[32];
+        tmem_ld_x32(dcol + c0, v);
         tc_wait_ld();
         if (!tk.is_dn) {
-          // gate rows are lanes 0-63, the up rows of the same F indices lanes 64-127
-          if (i >= 64) {
+          // Lanes n < 64 hold the gate row of F index n, lanes n + 64 the up row.  Lane n
+          // forms h for columns 0-15 of the slice, lane n + 64 for columns 16-31: the up
+          // values of columns 0-15 and the gate values of columns 16-31 cross over.
+          const int nF = i & 63;
+          const bool up = i >= 64;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) sm.xch[j * 64 + (i - 64)] = __uint_as_float(v[j]);
-          }
-          named_bar_sync(1, 128);
-          if (i < 64) {
-            __half* hcol = a.hs16 + static_cast<size_t>(tk.row0) * a.F + tk.s * kGuRows + i;
+          for (int j = 0; j < 16; ++j) xch[(up ? j : 16 + j) * 64 + nF] = __uint_as_float(up ? v[j] : v[16 + j]);
+          named_bar_sync(4 + grp, 128);
+          __half* hcol = a.hs16 + static_cast<size_t>(tk.row0) * a.F + tk.s * kGuRows + nF;
+          const int j0 = up ? 16 : 0;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (c0 + j < tk.rows)
-                hcol[static_cast<size_t>(c0 + j) * a.F] =
-                    h_store_value(silu_mul(__uint_as_float(v[j]) * sc13, sm.xch[j * 64 + i] * sc13), a.status);
-            }
+          for (int j = 0; j < 16; ++j) {
+            const int c = c0 + j0 + j;
+            const float own = __uint_as_float(up ? v[16 + j] : v[j]) * sc13, other = xch[(j0 + j) * 64 + nF] * sc13;
+            const float g = up ? other : own, u = up ? own : other;
+            if (c < tk.rows)
+              hcol[static_cast<size_t>(c) * a.F] = h_store_value(__fdividef(g, 1.0f + __expf(-g)) * u, a.status);
           }
-          named_bar_sync(1, 128);
+          named_bar_sync(4 + grp, 128);
         } else {
           float* ycol = a.y + static_cast<size_t>(tk.row0) * a.d + tk.s * kDnRows + i;
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
+          for (int j = 0; j < 32; ++j)
             if (c0 + j < tk.rows) ycol[static_cast<size_t>(c0 + j) * a.d] = __uint_as_float(v[j]) * sc2;
         }
       }
@@ -530,9 +540,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++dbuf == kNumD) { dbuf = 0; dphase ^= 1u; }
       if (!tk.is_dn) {
         // publish this stripe's h rows (release) for the down tasks of the expert
-        if (i < 64) __threadfence();
-        named_bar_sync(1, 128);
-        if (i == 0) atom_add_acqrel_u32(a.ready + tk.u, 1u);
+        __threadfence();
+        named_bar_sync(3, 32 * kEpiWarps);
+        if (tid == 0) atom_add_acqrel_u32(a.ready + tk.u, 1u);
       }
     }
   }

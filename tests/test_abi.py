@@ -63,9 +63,14 @@ def test_workspace_size_and_shape_checks(L):
 
 
 def test_auto_algo_selection(L):
-    # decode kernel: d and ffn powers of two from 256 to 2048; the tcgen05 kernel otherwise
+    # the wide kernel for >= 32 routed rows per expert on average; else the decode kernel for d
+    # and ffn powers of two from 256 to 2048; the tcgen05 kernel otherwise
     assert L.auto_algo(L.shape_of(4, 2048, 512, 512, 10)) == L.ALGO_MMA
-    assert L.auto_algo(L.shape_of(8192, 256, 2048, 64, 8)) == L.ALGO_MMA
+    assert L.auto_algo(L.shape_of(8192, 256, 2048, 64, 8)) == L.ALGO_WIDE  # 1024 rows per expert
+    assert L.auto_algo(L.shape_of(8192, 2048, 512, 512, 10)) == L.ALGO_WIDE  # prefill chunk: 160
+    assert L.auto_algo(L.shape_of(256, 2048, 512, 512, 10)) == L.ALGO_MMA  # decode batch: 5
+    assert L.auto_algo(L.shape_of(1637, 2048, 512, 512, 10)) == L.ALGO_MMA  # just below 32 rows
+    assert L.auto_algo(L.shape_of(1639, 2048, 512, 512, 10)) == L.ALGO_WIDE
     assert L.auto_algo(L.shape_of(4, 768, 512, 64, 8)) == L.ALGO_TCGEN05
     assert L.auto_algo(L.shape_of(4, 2048, 128, 64, 8)) == L.ALGO_TCGEN05
     assert L.auto_algo(L.shape_of(4, 4096, 512, 64, 8)) == L.ALGO_TCGEN05
