@@ -79,6 +79,8 @@ typedef enum moe_status {
 #define MOE_DEV_TIMEOUT 0x2u        /* a bounded wait in the expert kernel gave up */
 #define MOE_DEV_HIDDEN_RANGE 0x4u   /* |hidden| exceeded the FP16 range (65504) */
 #define MOE_DEV_H_SATURATED 0x8u    /* |silu(g)*u| exceeded 2^4 * 65504 and was clamped */
+#define MOE_DEV_Y_SATURATED 0x10u   /* MOE_ALGO_WIDE: a per-route down output exceeded 2^4 * 65504
+                                       and was clamped */
 
 /* Layer shape.  T tokens (rows of the call), d hidden size, ffn expert intermediate
  * size, E experts, k experts per token.  Supported: 1 <= T <= 65536, 1 <= k <= 32,

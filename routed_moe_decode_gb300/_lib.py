@@ -26,6 +26,7 @@ MOE_DEV_BAD_EXPERT_ID = 0x1
 MOE_DEV_TIMEOUT = 0x2
 MOE_DEV_HIDDEN_RANGE = 0x4
 MOE_DEV_H_SATURATED = 0x8
+MOE_DEV_Y_SATURATED = 0x10
 
 ALGO_AUTO = 0
 ALGO_TCGEN05 = 1

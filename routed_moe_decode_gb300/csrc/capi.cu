@@ -254,6 +254,7 @@ static void fill_plan_args(moe::PlanArgs& a, const moe_shape* shape, const WsLay
   a.pos_tok = at<int>(workspace, L.pos_tok);
   a.route_w = at<float>(workspace, L.route_w);
   a.tasks = at<moe::TaskEntry>(workspace, L.tasks);
+  a.hist = at<int>(workspace, L.hist);
 }
 
 int moe_plan(const moe_shape* shape, const int32_t* ids, const float* weights, void* workspace,

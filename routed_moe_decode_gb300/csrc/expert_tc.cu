@@ -583,7 +583,9 @@ __global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
   const int t = blockIdx.x;
   const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
   if (c >= a.d) return;
-  unroute4(a, t, c);
+  // the expert kernel that ran records the format of its per-route outputs in the plan meta
+  if (__ldcg(a.meta + META_YFMT) != 0) unroute4_y16(a, t, c);
+  else unroute4(a, t, c);
 }
 
 cudaError_t launch_combine(const ExpertArgs& a, cudaStream_t stream) {

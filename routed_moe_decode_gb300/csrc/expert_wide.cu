@@ -12,8 +12,8 @@
 //   0-7   epilogue, two groups of four warps taking alternate 32-column slices of an
 //         accumulator; thread t owns accumulator lane t % 128.  Gate/up tasks exchange half of
 //         the gate and up values between the lane halves through shared memory, so that all
-//         128 threads of a group form h = silu(g) * u (FP16); down tasks store per-route FP32
-//         outputs (summed by the un-route kernel in slot order);
+//         128 threads of a group form h = silu(g) * u (FP16); down tasks store per-route
+//         outputs as FP16(y * 2^-4) (summed by the un-route kernel in slot order, in FP32);
 //   8-11  dequantisation: thread i owns A row i; each 128-K chunk of E2M1 codes (TMA tile,
 //         64-byte swizzle) and its E4M3 block scales become exact FP16 in registers and are
 //         stored into tensor memory, where they are the A operand (M = 128);
@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(1024) wide_plan_kernel(const int* meta_in, int
   if (tid == 0) {
     meta[META_WGU] = total * S_gu;
     meta[META_WDN] = total * S_dn;
+    meta[META_YFMT] = 1;  // this kernel's down tasks store FP16(y * 2^-4)
   }
 }
 
@@ -527,10 +528,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           named_bar_sync(4 + grp, 128);
         } else {
-          float* ycol = a.y + static_cast<size_t>(tk.row0) * a.d + tk.s * kDnRows + i;
+          // per-route outputs as FP16(y * 2^-4): half the bytes of FP32 for the un-route to read
+          __half* ycol = reinterpret_cast<__half*>(a.y) + static_cast<size_t>(tk.row0) * a.d + tk.s * kDnRows + i;
+          bool sat = false;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c0 + j < tk.rows) ycol[static_cast<size_t>(c0 + j) * a.d] = __uint_as_float(v[j]) * sc2;
+          for (int j = 0; j < 32; ++j) {
+            if (c0 + j < tk.rows) {
+              float yv = __uint_as_float(v[j]) * (sc2 * kYScale);
+              if (fabsf(yv) > 65504.f) {
+                sat = true;
+                yv = copysignf(65504.f, yv);
+              }
+              ycol[static_cast<size_t>(c0 + j) * a.d] = __float2half_rn(yv);
+            }
+          }
+          if (sat) atomicOr(a.status, static_cast<int>(MOE_DEV_Y_SATURATED));
         }
       }
       // the accumulator is read: hand it back to the MMA warp

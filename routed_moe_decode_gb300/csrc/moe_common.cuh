@@ -28,6 +28,7 @@ constexpr int kRowsPerPass = 64;    // token rows handled per pass (4 MMA groups
 constexpr int kGroupRows = 16;      // MMA N per group
 constexpr int kMaxGroups = kRowsPerPass / kGroupRows;
 constexpr int kWideRows = 192;      // routed rows per pass of the wide (many-rows) kernel
+constexpr int kPlanSlice = 4096;    // routes per CTA of the multi-CTA plan (many routes)
 constexpr float kHScale = 0.0625f;  // h is stored as FP16(h * 2^-4)
 constexpr float kHUnscale = 16.0f;
 
@@ -38,7 +39,7 @@ constexpr float kHUnscale = 16.0f;
 
 struct WsLayout {
   size_t status, meta, counts, offsets, touched, gu_start, dn_start, route_pos, pos_tok, route_w;
-  size_t ready, ticket, tasks, tasks_w, x16, hs16, y, total;
+  size_t ready, ticket, tasks, tasks_w, hist, x16, hs16, y, total;
   size_t front_done;  // arrival counter of the fused front, inside the zeroed status block
   int S_gu;       // gate/up stripes per expert (ffn / 64)
   int S_dn;       // down stripes per expert (d / 128)
@@ -48,7 +49,12 @@ struct WsLayout {
 };
 
 // meta words
-enum { META_U = 0, META_NGU = 1, META_NDN = 2, META_MAXROWS = 3, META_WGU = 4, META_WDN = 5, META_WORDS = 8 };
+// META_YFMT: format of the per-route down outputs y: 0 FP32, 1 FP16(y * 2^-4) (wide kernel);
+// the plan writes 0, the wide kernel's task-table kernel 1, the un-route kernel reads it.
+enum { META_U = 0, META_NGU = 1, META_NDN = 2, META_MAXROWS = 3, META_WGU = 4, META_WDN = 5, META_YFMT = 6,
+       META_WORDS = 8 };
+constexpr float kYScale = 0.0625f;  // FP16 per-route down outputs hold y * 2^-4
+constexpr float kYUnscale = 16.0f;
 
 // One expert task as the plan writes it (16 bytes):
 //   x = expert id | touched index << 16, y = first routed row (expert-major position),
@@ -86,6 +92,7 @@ inline WsLayout ws_layout(const moe_shape& s) {
   L.ticket = take(4);
   L.tasks = take(size_t(L.max_tasks) * sizeof(TaskEntry));
   L.tasks_w = take(size_t(L.max_tasks_w) * sizeof(TaskEntry));
+  L.hist = take(size_t((L.R + kPlanSlice - 1) / kPlanSlice) * s.E * 4);  // multi-CTA plan: a histogram per slice
   L.x16 = take(size_t(s.T) * s.d * 2);
   L.hs16 = take(size_t(L.R) * s.ffn * 2);
   L.y = take(size_t(L.R) * s.d * 4);

@@ -22,6 +22,7 @@ struct PlanArgs {
   int* pos_tok;
   float* route_w;
   TaskEntry* tasks;
+  int* hist;  // [ceil(T * k / kPlanSlice), E] scratch of the multi-CTA plan (many routes)
 };
 
 // The fused front (router + plan + FP16 hidden) for T * k up to kFrontMaxRoutes.
@@ -108,6 +109,53 @@ __device__ __forceinline__ void unroute4(const ExpertArgs& a, int t, int c) {
       acc.y += w[jj] * yv[jj].y;
       acc.z += w[jj] * yv[jj].z;
       acc.w += w[jj] * yv[jj].w;
+    }
+  }
+  const size_t o = static_cast<size_t>(t) * a.d + c;
+  float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (a.residual) {
+    const uint2 rb = *reinterpret_cast<const uint2*>(a.residual + o);
+    const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rb.x));
+    const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rb.y));
+    res = make_float4(r0.x, r0.y, r1.x, r1.y);
+  }
+  __nv_bfloat162 o0 = __floats2bfloat162_rn(res.x + acc.x, res.y + acc.y);
+  __nv_bfloat162 o1 = __floats2bfloat162_rn(res.z + acc.z, res.w + acc.w);
+  uint2 ob;
+  ob.x = *reinterpret_cast<uint32_t*>(&o0);
+  ob.y = *reinterpret_cast<uint32_t*>(&o1);
+  *reinterpret_cast<uint2*>(a.out + o) = ob;
+}
+
+// unroute4 for per-route outputs stored as FP16(y * 2^-4) (the wide kernel): the same slot
+// order and FP32 accumulation.
+__device__ __forceinline__ void unroute4_y16(const ExpertArgs& a, int t, int c) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int* rp = a.route_pos + static_cast<size_t>(t) * a.k;
+  const float* rw = a.route_w + static_cast<size_t>(t) * a.k;
+  const __half* y16 = reinterpret_cast<const __half*>(a.y);
+  for (int j0 = 0; j0 < a.k; j0 += 8) {
+    int pos[8];
+    float w[8];
+    uint2 yv[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      pos[jj] = j0 + jj < a.k ? __ldg(rp + j0 + jj) : -1;
+      w[jj] = j0 + jj < a.k ? __ldg(rw + j0 + jj) * kYUnscale : 0.f;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj)
+      yv[jj] = pos[jj] >= 0 ? __ldcg(reinterpret_cast<const uint2*>(y16 + static_cast<size_t>(pos[jj]) * a.d + c))
+                            : make_uint2(0, 0);
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      if (pos[jj] < 0) continue;
+      const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&yv[jj].x));
+      const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&yv[jj].y));
+      acc.x += w[jj] * lo.x;
+      acc.y += w[jj] * lo.y;
+      acc.z += w[jj] * hi.x;
+      acc.w += w[jj] * hi.y;
     }
   }
   const size_t o = static_cast<size_t>(t) * a.d + c;

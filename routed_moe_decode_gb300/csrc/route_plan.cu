@@ -208,27 +208,12 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
   return out;
 }
 
-// The plan for all T * k routes, computed by one 1024-thread CTA.  ids/weights are read past
-// L1: in the fused front they were written by other CTAs of the same launch.
-__device__ __forceinline__ void plan_block(const PlanArgs& a) {
-  __shared__ int s_counts[1024];
-  __shared__ int s_cursor[1024];
-  __shared__ int s_scan[33];
+// Everything of the plan that follows from the per-expert counts (thread e of a 1024-thread
+// CTA holds count cnt of expert e): offsets, touched list, task-pass prefix sums, the task
+// table and the meta words.  s_counts is scratch of 1024 ints.  Returns expert tid's offset.
+__device__ __forceinline__ int plan_from_counts(const PlanArgs& a, int cnt, int* s_counts, int* s_scan) {
   const int tid = threadIdx.x;
-  const int E = a.E, R = a.T * a.k;
-  if (tid < E) s_counts[tid] = 0;
-  __syncthreads();
-  for (int r = tid; r < R; r += blockDim.x) {
-    const int e = __ldcg(a.ids + r);
-    a.route_w[r] = __ldcg(a.weights + r);
-    if (e < 0 || e >= E) {
-      atomicOr(a.status, static_cast<int>(MOE_DEV_BAD_EXPERT_ID));
-    } else {
-      atomicAdd(&s_counts[e], 1);
-    }
-  }
-  __syncthreads();
-  const int cnt = tid < E ? s_counts[tid] : 0;
+  const int E = a.E;
   int total = 0;
   const int off = block_exclusive_scan(cnt, s_scan, total);
   const int flag = cnt > 0 ? 1 : 0;
@@ -237,7 +222,6 @@ __device__ __forceinline__ void plan_block(const PlanArgs& a) {
   if (tid < E) {
     a.counts[tid] = cnt;
     a.offsets[tid] = off;
-    s_cursor[tid] = off;
     if (flag) a.touched[rank] = tid;
   }
   if (tid == 0) a.offsets[E] = total;
@@ -299,7 +283,35 @@ __device__ __forceinline__ void plan_block(const PlanArgs& a) {
     a.meta[META_NGU] = gu_total;
     a.meta[META_NDN] = dn_total;
     a.meta[META_MAXROWS] = m;
+    a.meta[META_YFMT] = 0;
   }
+  __syncthreads();
+  return off;
+}
+
+// The plan for all T * k routes, computed by one 1024-thread CTA.  ids/weights are read past
+// L1: in the fused front they were written by other CTAs of the same launch.
+__device__ __forceinline__ void plan_block(const PlanArgs& a) {
+  __shared__ int s_counts[1024];
+  __shared__ int s_cursor[1024];
+  __shared__ int s_scan[33];
+  const int tid = threadIdx.x;
+  const int E = a.E, R = a.T * a.k;
+  if (tid < E) s_counts[tid] = 0;
+  __syncthreads();
+  for (int r = tid; r < R; r += blockDim.x) {
+    const int e = __ldcg(a.ids + r);
+    a.route_w[r] = __ldcg(a.weights + r);
+    if (e < 0 || e >= E) {
+      atomicOr(a.status, static_cast<int>(MOE_DEV_BAD_EXPERT_ID));
+    } else {
+      atomicAdd(&s_counts[e], 1);
+    }
+  }
+  __syncthreads();
+  const int cnt = tid < E ? s_counts[tid] : 0;
+  const int off = plan_from_counts(a, cnt, s_counts, s_scan);
+  if (tid < E) s_cursor[tid] = off;
   __syncthreads();
   // route positions in expert-major order
   for (int r = tid; r < R; r += blockDim.x) {
@@ -448,6 +460,7 @@ __device__ __forceinline__ void plan_block_cached(const PlanArgs& a, const int* 
     a.meta[META_NGU] = passes * a.S_gu;
     a.meta[META_NDN] = passes * a.S_dn;
     a.meta[META_MAXROWS] = mx;
+    a.meta[META_YFMT] = 0;
   }
   __syncthreads();
   // touched list in touched order (coalesced)
@@ -586,8 +599,83 @@ cudaError_t launch_front(FrontArgs f, cudaStream_t stream) {
   return launch_pdl(kern, grid, block, 0, stream, f);
 }
 
+// ---------------------------------------------------------------------------------
+// The plan for many routes (prefill chunks) over several CTAs, in three launches:
+//   1. per slice of kPlanSlice routes: route weights copied, expert histogram of the slice
+//      (hist row = slice);
+//   2. one CTA: per-expert counts summed over the slices, everything that follows from them
+//      (plan_from_counts), and each slice's first position in every expert's bucket (written
+//      over the histogram);
+//   3. per slice: route positions from the slice's bucket bases (shared-memory cursors).
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) plan_hist_kernel(PlanArgs a, int* hist) {
+  __shared__ int s_counts[1024];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tid = threadIdx.x, E = a.E, R = a.T * a.k;
+  if (tid < E) s_counts[tid] = 0;
+  __syncthreads();
+  const int r1 = min(R, (blockIdx.x + 1) * kPlanSlice);
+  for (int r = blockIdx.x * kPlanSlice + tid; r < r1; r += blockDim.x) {
+    const int e = __ldcg(a.ids + r);
+    a.route_w[r] = __ldcg(a.weights + r);
+    if (e < 0 || e >= E) atomicOr(a.status, static_cast<int>(MOE_DEV_BAD_EXPERT_ID));
+    else atomicAdd(&s_counts[e], 1);
+  }
+  __syncthreads();
+  if (tid < E) hist[static_cast<size_t>(blockIdx.x) * E + tid] = s_counts[tid];
+}
+
+__global__ void __launch_bounds__(1024) plan_scan_kernel(PlanArgs a, int* hist, int slices) {
+  __shared__ int s_counts[1024];
+  __shared__ int s_scan[33];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tid = threadIdx.x, E = a.E;
+  int cnt = 0;
+  if (tid < E)
+    for (int g = 0; g < slices; ++g) cnt += __ldcg(hist + static_cast<size_t>(g) * E + tid);
+  const int off = plan_from_counts(a, cnt, s_counts, s_scan);
+  if (tid < E) {
+    int run = off;
+    for (int g = 0; g < slices; ++g) {
+      int* h = hist + static_cast<size_t>(g) * E + tid;
+      const int c = *h;
+      *h = run;
+      run += c;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024) plan_scatter_kernel(PlanArgs a, const int* hist) {
+  __shared__ int s_cursor[1024];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tid = threadIdx.x, E = a.E, R = a.T * a.k;
+  if (tid < E) s_cursor[tid] = __ldcg(hist + static_cast<size_t>(blockIdx.x) * E + tid);
+  __syncthreads();
+  const int r1 = min(R, (blockIdx.x + 1) * kPlanSlice);
+  for (int r = blockIdx.x * kPlanSlice + tid; r < r1; r += blockDim.x) {
+    const int e = __ldcg(a.ids + r);
+    if (e < 0 || e >= E) {
+      a.route_pos[r] = -1;
+      continue;
+    }
+    const int pos = atomicAdd(&s_cursor[e], 1);
+    a.route_pos[r] = pos;
+    a.pos_tok[pos] = r / a.k;
+  }
+}
+
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
-  return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, a);
+  const int R = a.T * a.k;
+  if (R <= kPlanCached * 1024 || a.hist == nullptr) return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, a);
+  const int slices = (R + kPlanSlice - 1) / kPlanSlice;
+  cudaError_t e = launch_pdl(plan_hist_kernel, dim3(slices), dim3(1024), 0, stream, a, a.hist);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(plan_scan_kernel, dim3(1), dim3(1024), 0, stream, a, a.hist, slices);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(plan_scatter_kernel, dim3(slices), dim3(1024), 0, stream, a, static_cast<const int*>(a.hist));
 }
 
 }  // namespace moe
