@@ -231,6 +231,25 @@ MOE_API int moe_layer(const moe_shape* shape, const float* logits, const void* h
               const void* residual, void* out, int32_t* ids, float* weights, void* workspace,
               size_t workspace_bytes, moe_stream_t stream);
 
+/* Expert-parallel shard of moe_layer: the layer restricted to the experts [e_begin, e_end),
+ * for a deployment that splits the experts over GPUs ("TokenSpeed: Qwen3.8-Flash-Next
+ * optimisations", section on the benchmark settings: expert parallelism of 4 on 4x GB300).
+ * Routing runs over all E experts (ids/weights as moe_layer, identical on every shard); only
+ * the routes to local experts are planned and computed, so
+ *     out = residual + sum over the token's slots j with e_begin <= id_j < e_end of w_j y_j,
+ * slots in order, FP32, one BF16 rounding.  Summing the shards' outputs (residual passed to
+ * one shard only, NULL to the others) gives the layer up to those per-shard roundings.
+ *   w13_codes/w13_scales/w2_codes/w2_scales hold the local experts only: entry e - e_begin
+ *   is expert e ([e_end - e_begin, 2*ffn, d/2] and so on).
+ * Other arguments, ownership and errors as moe_layer; 0 <= e_begin < e_end <= E, else
+ * MOE_ERR_INVALID_ARG.  The range applies to this call on the calling host thread only. */
+MOE_API int moe_layer_expert_range(const moe_shape* shape, int e_begin, int e_end, const float* logits,
+                                   const void* hidden, const uint8_t* w13_codes, const uint8_t* w13_scales,
+                                   float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales,
+                                   float w2_scale, const void* residual, void* out, int32_t* ids,
+                                   float* weights, void* workspace, size_t workspace_bytes,
+                                   moe_stream_t stream);
+
 /* The whole layer (moe_layer) with its scratch in a fixed device array of the library
  * instead of a caller-provided workspace.  The pages have no counterpart for this entry
  * point.  It is for callers that cannot allocate device memory: code running while a

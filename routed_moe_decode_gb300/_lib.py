@@ -64,6 +64,8 @@ SIGNATURES = {
     "moe_forward_unroute": (_I, [_SP, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_front": (_I, [_SP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_layer": (_I, [_SP, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_layer_expert_range": (_I, [_SP, _I, _I, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P,
+                                    ctypes.c_size_t, _P]),
     "moe_layer_static_workspace": (_I, [_SP, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P]),
     "moe_read_device_status": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint32), _P]),
     "moe_plan_summary": (_I, [_SP, _P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), _P]),
@@ -213,6 +215,16 @@ def layer(shape: Shape, logits, hidden, w: dict, residual, out, ids, weights, ws
         ctypes.byref(shape), _ptr(logits), _ptr(hidden), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]),
         float(w["w13_ts"]), _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]), _ptr(residual),
         _ptr(out), _ptr(ids), _ptr(weights), ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def layer_expert_range(shape: Shape, e_begin: int, e_end: int, logits, hidden, w: dict, residual, out, ids,
+                       weights, ws: Workspace, stream=None):
+    """moe_layer restricted to the experts [e_begin, e_end) (one expert-parallel shard); `w`
+    holds those experts' weights only (entry e - e_begin is expert e)."""
+    _check("moe_layer_expert_range", lib().moe_layer_expert_range(
+        ctypes.byref(shape), int(e_begin), int(e_end), _ptr(logits), _ptr(hidden), _ptr(w["w13_codes"]),
+        _ptr(w["w13_scales"]), float(w["w13_ts"]), _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]),
+        _ptr(residual), _ptr(out), _ptr(ids), _ptr(weights), ws.ptr, ws.nbytes, _stream(stream)))
 
 
 def read_status(ws: Workspace, clear: bool = True, stream=None) -> int:

@@ -138,6 +138,19 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
+// Experts a call computes (moe_layer_expert_range sets it for the duration of its call on
+// this host thread; every other entry point sees all experts).
+struct ExpertRange {
+  int lo = 0, hi = -1;  // hi < 0: all E experts
+};
+thread_local ExpertRange g_range;
+struct RangeScope {
+  RangeScope(int lo, int hi) { g_range = ExpertRange{lo, hi}; }
+  ~RangeScope() { g_range = ExpertRange{}; }
+};
+int range_lo() { return g_range.hi < 0 ? 0 : g_range.lo; }
+int range_hi(const moe_shape* s) { return g_range.hi < 0 ? s->E : g_range.hi; }
+
 moe::ExpertArgs expert_args(const moe_shape* s, const WsLayout& L, void* ws, const uint8_t* w13c,
                             const uint8_t* w13s, float w13_ts, const uint8_t* w2c, const uint8_t* w2s, float w2_ts,
                             const void* residual, void* out) {
@@ -166,6 +179,7 @@ moe::ExpertArgs expert_args(const moe_shape* s, const WsLayout& L, void* ws, con
   a.status = at<int>(ws, L.status);
   a.residual = static_cast<const __nv_bfloat16*>(residual);
   a.out = static_cast<__nv_bfloat16*>(out);
+  a.e_lo = range_lo();
   return a;
 }
 
@@ -255,6 +269,8 @@ static void fill_plan_args(moe::PlanArgs& a, const moe_shape* shape, const WsLay
   a.route_w = at<float>(workspace, L.route_w);
   a.tasks = at<moe::TaskEntry>(workspace, L.tasks);
   a.hist = at<int>(workspace, L.hist);
+  a.e_lo = range_lo();
+  a.e_hi = range_hi(shape);
 }
 
 int moe_plan(const moe_shape* shape, const int32_t* ids, const float* weights, void* workspace,
@@ -342,18 +358,18 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
   const uint32_t box = use_mma ? 128u : 64u;
   CUtensorMap tm13, tm2;
   rc = encode_codes_map(&tm13, w13_codes, static_cast<uint64_t>(shape->d) / 2,
-                        static_cast<uint64_t>(shape->E) * 2 * shape->ffn, box);
+                        static_cast<uint64_t>(range_hi(shape) - range_lo()) * 2 * shape->ffn, box);
   if (rc != MOE_OK) return rc;
   rc = encode_codes_map(&tm2, w2_codes, static_cast<uint64_t>(shape->ffn) / 2,
-                        static_cast<uint64_t>(shape->E) * shape->d, box);
+                        static_cast<uint64_t>(range_hi(shape) - range_lo()) * shape->d, box);
   if (rc != MOE_OK) return rc;
   if (use_mma) {
     CUtensorMap ts13, ts2;
     rc = moe::encode_scales_map(&ts13, w13_scales, static_cast<uint32_t>(shape->d / 16),
-                                static_cast<uint64_t>(shape->E) * 2 * shape->ffn, 64);
+                                static_cast<uint64_t>(range_hi(shape) - range_lo()) * 2 * shape->ffn, 64);
     if (rc != MOE_OK) return rc;
     rc = moe::encode_scales_map(&ts2, w2_scales, static_cast<uint32_t>(shape->ffn / 16),
-                                static_cast<uint64_t>(shape->E) * shape->d, 64);
+                                static_cast<uint64_t>(range_hi(shape) - range_lo()) * shape->d, 64);
     if (rc != MOE_OK) return rc;
     // for few tokens the decode kernel runs the un-route as trailing tasks of its own
     a.ncb = (stages & kStageUnroute) ? moe::expert_mma_unroute_tasks(shape->T, L.S_dn) : 0;
@@ -481,6 +497,19 @@ int moe_layer(const moe_shape* shape, const float* logits, const void* hidden, c
   if (rc != MOE_OK) return rc;
   return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
                               workspace, workspace_bytes, MOE_ALGO_AUTO, nullptr, stream);
+}
+
+int moe_layer_expert_range(const moe_shape* shape, int e_begin, int e_end, const float* logits, const void* hidden,
+                           const uint8_t* w13_codes, const uint8_t* w13_scales, float w13_scale,
+                           const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale, const void* residual,
+                           void* out, int32_t* ids, float* weights, void* workspace, size_t workspace_bytes,
+                           moe_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (e_begin < 0 || e_end > shape->E || e_begin >= e_end) return MOE_ERR_INVALID_ARG;
+  RangeScope scope(e_begin, e_end);
+  return moe_layer(shape, logits, hidden, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual,
+                   out, ids, weights, workspace, workspace_bytes, stream);
 }
 
 int moe_read_device_status(const void* workspace, int clear, uint32_t* status_bits, moe_stream_t stream) {

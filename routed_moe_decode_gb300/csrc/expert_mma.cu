@@ -426,12 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int rA0, rA1, nck;
       const CUtensorMap* tm;
       if (!is_dn) {
-        rA0 = e * 2 * a.F + s * kGuRows;
+        rA0 = (e - a.e_lo) * 2 * a.F + s * kGuRows;
         rA1 = rA0 + a.F;
         tm = &tm_w13;
         nck = a.d / kChunk;
       } else {
-        rA0 = e * a.d + s * kDnRows;
+        rA0 = (e - a.e_lo) * a.d + s * kDnRows;
         rA1 = rA0 + 64;
         tm = &tm_w2;
         nck = a.F / kChunk;

@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(256) simt_gateup_kernel(ExpertArgs a) {
   for (int nn = 0; nn < 4; ++nn) {
     const int n = blockIdx.y * 32 + warp * 4 + nn;
     if (n >= a.F) break;
-    const size_t rg = static_cast<size_t>(e) * 2 * a.F + n, ru = rg + a.F;
+    const size_t rg = static_cast<size_t>(e - a.e_lo) * 2 * a.F + n, ru = rg + a.F;
     for (int r0 = 0; r0 < m; r0 += kTok) {
       const int nr = min(kTok, m - r0);
       const __half* xr[kTok];
@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(256) simt_down_kernel(ExpertArgs a) {
   for (int rr = 0; rr < 4; ++rr) {
     const int r = blockIdx.y * 32 + warp * 4 + rr;
     if (r >= a.d) break;
-    const size_t wr = static_cast<size_t>(e) * a.d + r;
+    const size_t wr = static_cast<size_t>(e - a.e_lo) * a.d + r;
     for (int r0 = 0; r0 < m; r0 += kTok) {
       const int nr = min(kTok, m - r0);
       const __half* hr[kTok];

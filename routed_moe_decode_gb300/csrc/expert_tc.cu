@@ -250,14 +250,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* tm;
       const uint8_t* sbase;
       if (!is_dn) {
-        rA0 = e * 2 * a.F + s * kGuRows;
+        rA0 = (e - a.e_lo) * 2 * a.F + s * kGuRows;
         rA1 = rA0 + a.F;
         sstride = a.d / 16;
         tm = &tm_w13;
         sbase = a.w13_scales;
         nck = a.nck_gu;
       } else {
-        rA0 = e * a.d + s * kDnRows;
+        rA0 = (e - a.e_lo) * a.d + s * kDnRows;
         rA1 = rA0 + 64;
         sstride = a.F / 16;
         tm = &tm_w2;

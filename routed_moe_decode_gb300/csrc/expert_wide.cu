@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && nxt < ntot) nxt2 = static_cast<int>(atomicAdd(a.ticket, 1u)) + static_cast<int>(gridDim.x);
       const int e = x & 0xffff;
       const bool is_dn = ((z >> 16) & 1) != 0;
-      const int rA0 = is_dn ? e * a.d + s * kDnRows : e * 2 * a.F + s * kGuRows;
+      const int rA0 = is_dn ? (e - a.e_lo) * a.d + s * kDnRows : (e - a.e_lo) * 2 * a.F + s * kGuRows;
       const int rA1 = is_dn ? rA0 + 64 : rA0 + a.F;
       const int sstride = is_dn ? a.F / 16 : a.d / 16;
       const CUtensorMap* tm = is_dn ? &tm_w2 : &tm_w13;

@@ -9,6 +9,7 @@ namespace moe {
 
 struct PlanArgs {
   int T, E, k, S_gu, S_dn;
+  int e_lo, e_hi;  // experts this call plans: [e_lo, e_hi) (all: [0, E))
   const int32_t* ids;
   const float* weights;
   int* status;
@@ -73,6 +74,7 @@ struct ExpertArgs {
   int* status;
   const __nv_bfloat16* residual;
   __nv_bfloat16* out;
+  int e_lo;  // first expert of the weight tensors passed in (expert e's weights are entry e - e_lo)
   int ncb;  // un-route tasks appended to the task order (0: the un-route runs as its own kernel)
   int task_cap;  // entries the task table has room for
   // optional timeline (diagnostics, off when null): per CTA kTraceRoles x kTracePerRole

@@ -208,6 +208,11 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
   return out;
 }
 
+// Expert-parallel sharding: a call plans (and computes) only the routes of the experts in
+// [e_lo, e_hi); the other routes get no bucket and route position -1, which the un-route
+// skips, so the call's output is the partial sum over its experts.
+__device__ __forceinline__ bool local_expert(const PlanArgs& a, int e) { return e >= a.e_lo && e < a.e_hi; }
+
 // Everything of the plan that follows from the per-expert counts (thread e of a 1024-thread
 // CTA holds count cnt of expert e): offsets, touched list, task-pass prefix sums, the task
 // table and the meta words.  s_counts is scratch of 1024 ints.  Returns expert tid's offset.
@@ -304,7 +309,7 @@ __device__ __forceinline__ void plan_block(const PlanArgs& a) {
     a.route_w[r] = __ldcg(a.weights + r);
     if (e < 0 || e >= E) {
       atomicOr(a.status, static_cast<int>(MOE_DEV_BAD_EXPERT_ID));
-    } else {
+    } else if (local_expert(a, e)) {
       atomicAdd(&s_counts[e], 1);
     }
   }
@@ -316,7 +321,7 @@ __device__ __forceinline__ void plan_block(const PlanArgs& a) {
   // route positions in expert-major order
   for (int r = tid; r < R; r += blockDim.x) {
     const int e = __ldcg(a.ids + r);
-    if (e < 0 || e >= E) {
+    if (e < 0 || e >= E || !local_expert(a, e)) {
       a.route_pos[r] = -1;
       continue;
     }
@@ -419,6 +424,8 @@ __device__ __forceinline__ void plan_block_cached(const PlanArgs& a, const int* 
       if (e < 0 || e >= E) {
         bad = true;
         a.route_pos[r] = -1;
+      } else if (!local_expert(a, e)) {
+        a.route_pos[r] = -1;  // another shard's expert
       } else {
         ev[j] = e;
         rk[j] = atomicAdd(&ps.num[e], 1);
@@ -620,7 +627,7 @@ __global__ void __launch_bounds__(1024) plan_hist_kernel(PlanArgs a, int* hist) 
     const int e = __ldcg(a.ids + r);
     a.route_w[r] = __ldcg(a.weights + r);
     if (e < 0 || e >= E) atomicOr(a.status, static_cast<int>(MOE_DEV_BAD_EXPERT_ID));
-    else atomicAdd(&s_counts[e], 1);
+    else if (local_expert(a, e)) atomicAdd(&s_counts[e], 1);
   }
   __syncthreads();
   if (tid < E) hist[static_cast<size_t>(blockIdx.x) * E + tid] = s_counts[tid];
@@ -657,7 +664,7 @@ __global__ void __launch_bounds__(1024) plan_scatter_kernel(PlanArgs a, const in
   const int r1 = min(R, (blockIdx.x + 1) * kPlanSlice);
   for (int r = blockIdx.x * kPlanSlice + tid; r < r1; r += blockDim.x) {
     const int e = __ldcg(a.ids + r);
-    if (e < 0 || e >= E) {
+    if (e < 0 || e >= E || !local_expert(a, e)) {
       a.route_pos[r] = -1;
       continue;
     }

@@ -10,8 +10,8 @@ import pytest
 import torch
 
 import moe_inputs as mi
-from gpu_helpers import (WEIGHT_RTOL, assert_parity, bf16_tensor, config_inputs, device_weights, parity_metrics,
-                         run_layer)
+from gpu_helpers import (MAX_ABS_OVER_RMS, MEAN_REL, WEIGHT_RTOL, assert_parity, bf16_tensor, config_inputs,
+                         device_weights, parity_metrics, run_layer)
 from oracle import oracle as O
 
 pytestmark = pytest.mark.gpu
@@ -389,3 +389,70 @@ def test_hidden_out_of_fp16_range_sets_status():
     _, _, _, layer = run_layer(cfg, inp, algo=0)
     import routed_moe_decode_gb300 as moe
     assert layer.status() & moe.MOE_DEV_HIDDEN_RANGE
+
+
+def _shard_partial_oracle(cfg, inp, ids, wts, e_begin, e_end, residual):
+    """Oracle of one expert shard: the slots of other shards' experts get weight 0, so they
+    add exactly nothing; the residual is added by one shard only."""
+    w = np.where((ids >= e_begin) & (ids < e_end), wts, 0.0).astype(np.float32)
+    return O.moe_experts((cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k), inp["hidden"], ids, w, inp,
+                         inp["residual"] if residual else None)
+
+
+@pytest.mark.parametrize("name,bounds", [
+    ("tiny", (0, 8, 16)), ("b1", (0, 128, 256, 384, 512)), ("b8", (0, 200, 512)),
+    ("ep2048x256x128x64x16", (0, 32, 64)),   # 32768 routes: multi-CTA plan and the wide kernel
+])
+def test_expert_parallel_shards_sum_to_layer(name, bounds):
+    """moe_layer_expert_range on each shard of a partition of the experts (local weights
+    only, residual on the first shard): every shard matches its partial oracle, the ids
+    agree across shards, and the shards' outputs summed in FP32 match the whole layer."""
+    import routed_moe_decode_gb300 as moe
+    if name in mi.CONFIGS:
+        cfg = mi.CONFIGS[name]
+        inp = config_inputs(name)
+    else:
+        cfg = mi.CONFIGS["tiny"].replace(name=name, T=2048, d=256, ffn=128, E=64, k=16, tag=400)
+        inp = mi.gen_layer(cfg, seed=7)
+    dev = torch.device("cuda")
+    shape = moe.shape_of(cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k)
+    logits = torch.from_numpy(np.ascontiguousarray(inp["logits"])).to(dev)
+    hidden = bf16_tensor(inp["hidden"], dev)
+    res = bf16_tensor(inp["residual"], dev)
+    ids_ref, wts_ref = O.route_topk(inp["logits"], cfg.k)
+    full = O.moe_experts((cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k), inp["hidden"], ids_ref, wts_ref, inp, inp["residual"])
+    full64 = full.astype(np.float64)
+    rms, l1 = float(np.sqrt(np.mean(full64 ** 2))), float(np.abs(full64).sum())
+    total = np.zeros((cfg.T, cfg.d), np.float64)
+    for si, (e0, e1) in enumerate(zip(bounds[:-1], bounds[1:])):
+        local = {n: np.ascontiguousarray(inp[n][e0:e1]) for n in ("w13_codes", "w13_scales", "w2_codes", "w2_scales")}
+        local["w13_ts"], local["w2_ts"] = inp["w13_ts"], inp["w2_ts"]
+        w = device_weights(local, dev)
+        ws = moe.Workspace(shape)
+        ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+        wts = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
+        out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
+        moe.layer_expert_range(shape, e0, e1, logits, hidden, w, res if si == 0 else None, out, ids, wts, ws)
+        torch.cuda.synchronize()
+        assert moe.read_status(ws) == 0
+        assert np.array_equal(ids.cpu().numpy(), ids_ref)
+        got = out.float().cpu().numpy()
+        ref = _shard_partial_oracle(cfg, inp, ids_ref, wts_ref, e0, e1, si == 0)
+        # a shard's output is part of the layer's: its error is measured on the layer's scale
+        err = np.abs(got.astype(np.float64) - ref)
+        assert np.all(np.isfinite(got))
+        assert err.max() <= MAX_ABS_OVER_RMS * rms and err.sum() <= MEAN_REL * l1, \
+            f"{name} shard [{e0},{e1}): max|d| {err.max():.3g} (rms {rms:.3g}), sum|d| / sum|layer| {err.sum() / l1:.3e}"
+        total += got
+    assert_parity(total.astype(np.float32), full, f"{name} sum of {len(bounds) - 1} shards")
+
+
+def test_expert_range_rejects_bad_bounds():
+    import routed_moe_decode_gb300 as moe
+    cfg = mi.CONFIGS["tiny"]
+    shape = moe.shape_of(cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k)
+    for e0, e1 in ((-1, 4), (4, 4), (8, 17), (9, 3)):
+        with pytest.raises(moe.MoeError):
+            moe.layer_expert_range(shape, e0, e1, None, None, {"w13_codes": None, "w13_scales": None, "w13_ts": 1.0,
+                                                              "w2_codes": None, "w2_scales": None, "w2_ts": 1.0},
+                                   None, None, None, None, moe.Workspace(shape))
