@@ -59,7 +59,9 @@ struct Smem {
   uint8_t ring_b[kStagesB][kStageB];
   uint8_t ring_a[kStagesA][kStageA];
   float xch[2][32 * 64];           // per epilogue group: gate/up values exchanged between lane halves
-  int rowoff[kActWarps][kWideRows / kActWarps];  // per activation warp: element offsets of its rows
+  // per activation warp: source of each of its rows in 16-byte units (fits 32 bits for every
+  // supported shape: T * d and T * k * ffn elements are below 2^34)
+  uint32_t rowoff16[kActWarps][kWideRows / kActWarps];
   TaskEntry task[kTaskSlots];
   uint64_t full_a[kStagesA];
   uint64_t empty_a[kStagesA];
@@ -344,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int L = 32 * aw + lane;
     const int gi = L & 15, atom = gi >> 3, ch = gi & 7;
     const int rsub = L >> 4;  // row within each group of 8 rows
-    int* rowoff = sm.rowoff[aw];
+    uint32_t* rowoff16 = sm.rowoff16[aw];
+    constexpr uint32_t kNoRow = 0xffffffffu;
     int stage = 0, n = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -361,25 +364,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int idx = lane; idx < kWideRows / kActWarps; idx += 32) {
         const int r = (idx >> 1) * 8 + 2 * aw + (idx & 1);
-        int off = -1;
-        if (r < tk.rows) off = tk.is_dn ? (tk.row0 + r) * a.F : __ldg(a.pos_tok + tk.row0 + r) * a.d;
-        rowoff[idx] = off;
+        uint32_t off = kNoRow;
+        if (r < tk.rows) {
+          const size_t row = tk.is_dn ? static_cast<size_t>(tk.row0 + r) : static_cast<size_t>(__ldg(a.pos_tok + tk.row0 + r));
+          off = static_cast<uint32_t>(row * (tk.is_dn ? a.F : a.d) / 8);
+        }
+        rowoff16[idx] = off;
       }
       __syncwarp();
-      const __half* src_base = tk.is_dn ? a.hs16 : a.x16;
+      const uint4* src_base = reinterpret_cast<const uint4*>(tk.is_dn ? a.hs16 : a.x16);
       const int ngroups = (tk.rows + 7) / 8;
       for (int c = 0; ok && c < tk.nck; ++c) {
         if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
         const uint32_t bbase = ringb0 + stage * kStageB + atom * kAtomB + rsub * 128 + ((ch ^ rsub) << 4);
-        const int kb = c * kChunkK + gi * 8;
+        const uint32_t kb16 = static_cast<uint32_t>(c * (kChunkK / 8) + gi);  // 16-byte units
         // eight row groups per batch: the offsets are read first, then the copies issued
         for (int g0 = 0; g0 < ngroups; g0 += 8) {
-          int off[8];
+          uint32_t off[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) off[u] = g0 + u < ngroups ? rowoff[(g0 + u) * 2 + (rsub & 1)] : -1;
+          for (int u = 0; u < 8; ++u) off[u] = g0 + u < ngroups ? rowoff16[(g0 + u) * 2 + (rsub & 1)] : kNoRow;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            if (off[u] >= 0) cp_async_16(bbase + (g0 + u) * 1024, src_base + off[u] + kb);
+            if (off[u] != kNoRow) cp_async_16(bbase + (g0 + u) * 1024, src_base + (off[u] + kb16));
         }
         cp_async_arrive_noinc(smem_addr(&sm.full_b[stage]));
         if (++stage == kStagesB) { stage = 0; phase ^= 1u; }
