@@ -160,6 +160,9 @@ MOE_API int moe_route_topk(const moe_shape* shape, const float* logits, int32_t*
  * kernel, and a copy of the routing weights, all written into `workspace`.
  *   ids     [T, k] int32, values in [0, E) (violations set MOE_DEV_BAD_EXPERT_ID)
  *   weights [T, k] float32
+ * One 1024-thread CTA for T * k up to 16384 routes; above that three launches (per-slice
+ * histograms of 4096 routes, one scan CTA, per-slice positions).  The order of the routes
+ * inside one expert's bucket is not fixed (results do not depend on it).
  * Must precede every moe_forward whose routing changed. */
 MOE_API int moe_plan(const moe_shape* shape, const int32_t* ids, const float* weights, void* workspace,
              size_t workspace_bytes, moe_stream_t stream);
@@ -199,7 +202,8 @@ MOE_API int moe_forward_experts(const moe_shape* shape, const uint8_t* w13_codes
 
 /* moe_forward_experts in two launches' worth of parts, for callers that want to time or
  * schedule them apart: moe_forward_expert_kernels runs only the expert kernel(s) (gate/up,
- * SiLU·mul, down projection into the per-route FP32 outputs of the workspace);
+ * SiLU·mul, down projection into the per-route outputs of the workspace: FP32, or
+ * FP16(y * 2^-4) from MOE_ALGO_WIDE, recorded in the plan for the un-route);
  * moe_forward_unroute runs only the weighted un-route (out = residual + the token's routes
  * in slot order, "fuses down with weighted unroute" in "Persistent execution for
  * Flash-Next GGUF on SM70").  Arguments as for moe_forward_experts. */
