@@ -229,20 +229,6 @@ def reference_arm(args, cfg, dist):
     inp = mi.gen_layer(cfg, seed=0, layer=0)
     n, el = time_oracle(cfg, inp, budget_s=120.0, max_steps=steps, warmup=warm)
     value = n / el
-    roofline_hbm = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                    "peak_kind": f"{peak_kind} copy bandwidth",
-                    "algorithmic_bytes": "unique experts x NVFP4 bytes per expert + FP16 hidden + FP16 h (write+read) + "
-                                         "FP32 per-route down outputs"
-                                         + (" (written and read back) + route positions and weights + BF16 residual and out"
-                                            if fused_unroute else "")}
-    # the wide kernel is a dense contraction: 2 flops per weight per routed row, gate/up
-    # (2F x d) and down (d x F) for each of the T * k routes
-    tpeak, tpeak_kind = load_tensor_peak()
-    tflops = 6.0 * R * cfg.d * cfg.ffn / (k_avg_ms * 1e-3) / 1e12
-    roofline_tensor = {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
-                       "peak_kind": tpeak_kind, "mma": "tcgen05 kind::f16 (FP16 x FP16 -> FP32)",
-                       "algorithmic_flops": "6 x T x k x d x ffn per launch",
-                       "hbm_achieved_gbs": achieved, "hbm_frac": achieved / peak}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": n,
         "warmup": warm, "ms_per_step": 1e3 * el / n, "higher_is_better": True, "scaling": "weak",
