@@ -109,3 +109,17 @@ def test_bad_arguments_rejected_on_host(L):
     # T = 0 is an empty, valid call that enqueues nothing
     z = L.shape_of(0, 256, 128, 16, 2)
     assert lib.moe_route_topk(ctypes.byref(z), None, None, None, None) == 0
+
+
+def test_expert_range_bounds_rejected_on_host(L):
+    """moe_layer_expert_range checks its expert block before touching anything."""
+    lib = L.lib()
+    s = L.shape_of(4, 256, 128, 16, 2)
+    sp = ctypes.byref(s)
+    rest = [None] * 2 + [None, None, 1.0, None, None, 1.0, None, None, None, None, None, 0, None]
+    for e0, e1 in ((-1, 4), (4, 4), (9, 3), (8, 17)):
+        assert lib.moe_layer_expert_range(sp, e0, e1, *rest) == L.MOE_ERR_INVALID_ARG
+    bad = L.shape_of(4, 200, 128, 16, 2)  # d not a multiple of 128
+    assert lib.moe_layer_expert_range(ctypes.byref(bad), 0, 8, *rest) == L.MOE_ERR_UNSUPPORTED
+    # a valid block with missing weights fails on the host as moe_layer does
+    assert lib.moe_layer_expert_range(sp, 0, 8, *rest) == L.MOE_ERR_INVALID_ARG
