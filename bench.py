@@ -8,6 +8,11 @@ CUDA graphs of those calls; the expert kernel is additionally timed alone with C
 events for its roofline figure; `e2e` times the public C-ABI call with host buffers
 (H2D of logits/hidden/residual, D2H of the output) per step.
 
+A default run (B=1 verify, MOE_ALGO_AUTO) also measures the metric's other
+configurations -- T=32, T=256 and the T=8192 prefill chunk -- on the same weight sets,
+each with its own steps, warm-up, expert-kernel samples, roofline and clock record,
+under "configs" in the same line; the headline `value` stays the B=1 figure.
+
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead.
 """
 from __future__ import annotations
@@ -54,6 +59,10 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-sub-configs", action="store_true",
+                   help="measure the headline configuration only (default: also T=32, 256 and 8192)")
+    p.add_argument("--kernel-samples", type=int, default=None,
+                   help="expert-kernel launches timed alone for the roofline (default max(400, min(steps, 2000)))")
     return p.parse_args()
 
 
@@ -181,10 +190,12 @@ def profiled_traffic(config: str, kernel: str):
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     vals = {}
     for line in open(path):
-        if ":" in line:
-            k, v = line.split(":", 1)
-            vals[k.strip()] = v.strip()
-    if vals.get(f"{kernel}.cu sha256[:16]") != digest:
+        if line.startswith("#") or ":" not in line:
+            continue
+        # the source hash line's key holds a colon itself ("<kernel>.cu sha256[:16]: <hex>")
+        k, v = line.rsplit(":", 1) if "sha256[:16]" in line else line.split(":", 1)
+        vals[k.strip()] = v.strip()
+    if vals.get(f"{kernel}.cu sha256[:16]", vals.get("source_sha256_16")) != digest:
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -246,43 +257,35 @@ def reference_arm(args, cfg, dist):
 # ----------------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------------
-def our_arm(args, cfg, dist, torch):
-    import __graft_entry__
-    __graft_entry__.build()  # no-op when the in-tree library is current
-    import routed_moe_decode_gb300 as moe
-    dev = torch.device(f"cuda:{dist.local}")
-    torch.cuda.set_device(dev)
-    algo = {"auto": moe.ALGO_AUTO, "mma": moe.ALGO_MMA, "tcgen05": moe.ALGO_TCGEN05, "simt": moe.ALGO_SIMT,
-            "wide": moe.ALGO_WIDE}[args.algo]
-    L = args.layers if args.layers is not None else min(12, max(1, cfg.layers))
-    K = args.steps if args.steps is not None else DEFAULT_STEPS[cfg.name]
-    W = args.warmup if args.warmup is not None else max(3, 2 * L)
-    W = max(W, 3)
-    shape = moe.shape_of(cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k)
-
-    # ---- inputs: L independent layers, resident in HBM ----
-    t_gen = time.perf_counter()
-    Wd, logits, hidden, resid, host = [], [], [], [], []
-    keep_host = None
+def load_weight_sets(cfg, L, dev, torch):
+    """L independent layer weight sets of `cfg`, resident in HBM."""
+    Wd = []
     for layer in range(L):
-        inp = mi.gen_layer(cfg, seed=0, layer=layer)
-        w = {n: torch.from_numpy(inp[n]).to(dev) for n in ("w13_codes", "w13_scales", "w2_codes", "w2_scales")}
-        w["w13_ts"], w["w2_ts"] = inp["w13_ts"], inp["w2_ts"]
-        Wd.append(w)
+        w = mi.gen_weights(cfg, seed=0, layer=layer)
+        d = {n: torch.from_numpy(w[n]).to(dev) for n in ("w13_codes", "w13_scales", "w2_codes", "w2_scales")}
+        d["w13_ts"], d["w2_ts"] = w["w13_ts"], w["w2_ts"]
+        Wd.append(d)
+    torch.cuda.synchronize()
+    return Wd
+
+
+def measure(cfg, moe, torch, dist, dev, Wd, algo, K, W, kernel_samples, e2e_steps=0, clock_gpu=None):
+    """Time K layer calls of `cfg` (CUDA-graph replays over the weight sets Wd, inputs of
+    each layer resident in HBM), then the expert kernel alone over `kernel_samples`
+    launches, then (if e2e_steps) the public call with host buffers.  Returns a dict."""
+    L = len(Wd)
+    shape = moe.shape_of(cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k)
+    logits, hidden, resid, host = [], [], [], []
+    for layer in range(L):
+        inp = mi.gen_layer(cfg, seed=0, layer=layer, weights=False)
         logits.append(torch.from_numpy(inp["logits"]).to(dev))
         hidden.append(torch.from_numpy(inp["hidden"].view(np.int16)).to(dev).view(torch.bfloat16))
         resid.append(torch.from_numpy(inp["residual"].view(np.int16)).to(dev).view(torch.bfloat16))
-        host.append({k_: inp[k_] for k_ in ("logits", "hidden", "residual")})
-        if layer == 0:
-            keep_host = inp
-    torch.cuda.synchronize()
-    t_gen = time.perf_counter() - t_gen
-
+        host.append(inp)
     ws = moe.Workspace(shape, device=dev)
     ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
     wts = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
     out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
-
     fused_front = algo == moe.ALGO_AUTO and cfg.T * cfg.k <= 16384
 
     def step(l):
@@ -355,8 +358,7 @@ def our_arm(args, cfg, dist, torch):
     # ---- warm-up and timed region ----
     run_steps(W)
     torch.cuda.synchronize()
-    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
-    sampler = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}")
+    sampler = ClockSampler(clock_gpu)
     sampler.start()
     dist.barrier()
     torch.cuda.synchronize()
@@ -371,17 +373,16 @@ def our_arm(args, cfg, dist, torch):
     t_ms = ev0.elapsed_time(ev1)
     t_ms = dist.max(t_ms)
     status = moe.read_status(ws)
+    del g_all, g_one
 
     steps_layers = [(W + i) % L for i in range(K)]
-    tokens = cfg.T * K * dist.world
-    value = tokens / (t_ms * 1e-3)
     us_per_layer = 1e3 * t_ms / K
     mean_unique = sum(unique_bytes[l] for l in steps_layers) / K
 
-    # ---- expert kernel alone: CUDA events around each launch ----
+    # ---- expert kernel alone: CUDA events around each launch (outside the timed region) ----
     # A GPU-side sleep first keeps the device busy while the host enqueues the front
     # kernels, the events and the expert kernel, so the events bracket GPU work only.
-    Kk = min(K, 2000)
+    Kk = kernel_samples
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(Kk)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(Kk)]
     kbytes = 0.0
@@ -410,8 +411,8 @@ def our_arm(args, cfg, dist, torch):
 
     # ---- end to end through the public C-ABI call with host buffers ----
     e2e = None
-    if not args.no_e2e:
-        Ke = min(K, 3000)
+    if e2e_steps:
+        Ke = e2e_steps
         pin = [{k_: torch.from_numpy(h[k_] if k_ == "logits" else h[k_].view(np.int16)).pin_memory()
                 for k_ in ("logits", "hidden", "residual")} for h in host]
         d_log = torch.empty_like(logits[0])
@@ -442,20 +443,13 @@ def our_arm(args, cfg, dist, torch):
                "d2h_bytes_per_step": cfg.T * cfg.d * 2, "steps": Ke,
                "us_per_layer": 1e3 * et / Ke}
 
-    # ---- CPU baseline: the oracle on a bounded sample (rank 0, one GPU only) ----
-    cpu = None
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        n, el = time_oracle(cfg, keep_host, budget_s=args.cpu_seconds)
-        cpu = {"value": n / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} single-token steps of layer 0 ({cfg.name}) through the FP32 C++ oracle, "
-                         f"{el:.1f} s on 1 host thread"}
-
     roofline_hbm = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                     "peak_kind": f"{peak_kind} copy bandwidth",
                     "algorithmic_bytes": "unique experts x NVFP4 bytes per expert + FP16 hidden + FP16 h (write+read) + "
                                          "FP32 per-route down outputs"
                                          + (" (written and read back) + route positions and weights + BF16 residual and out"
-                                            if fused_unroute else "")}
+                                            if fused_unroute else ""),
+                    "algorithmic_bytes_per_launch": kbytes / Kk}
     # the wide kernel is a dense contraction: 2 flops per weight per routed row, gate/up
     # (2F x d) and down (d x F) for each of the T * k routes
     tpeak, tpeak_kind = load_tensor_peak()
@@ -464,14 +458,115 @@ def our_arm(args, cfg, dist, torch):
                        "peak_kind": tpeak_kind, "mma": "tcgen05 kind::f16 (FP16 x FP16 -> FP32)",
                        "algorithmic_flops": "6 x T x k x d x ffn per launch",
                        "hbm_achieved_gbs": achieved, "hbm_frac": achieved / peak}
+    roofline = roofline_hbm if run_algo != moe.ALGO_WIDE else roofline_tensor
+    roofline.update({"traffic": traffic,
+                     "traffic_source": (f"profiles/{kname}_{cfg.name}_dram.txt (ncu dram__bytes_read.sum + "
+                                        "dram__bytes_write.sum of one launch; null once the kernel source changed)")
+                     if kname else None,
+                     "kernel": (f"{kname}_kernel" + ("<fused un-route>" if fused_unroute else "")
+                                + (" (after its task-table kernel)" if run_algo == moe.ALGO_WIDE else "")) if kname
+                               else "simt kernels",
+                     "kernel_us": 1e3 * k_avg_ms, "kernel_samples": Kk})
+    return {
+        "t_ms": t_ms, "K": K, "W": W, "us_per_layer": us_per_layer,
+        "tokens_per_s": cfg.T * K * dist.world / (t_ms * 1e-3),
+        "unique_experts_mean": sum(U[l] for l in steps_layers) / K,
+        "unique_bytes_mean": mean_unique,
+        "hbm_frac_layer": (mean_unique / (us_per_layer * 1e-6) / 1e9) / peak,
+        "roofline": roofline, "clocks": clocks, "status": status, "e2e": e2e,
+        "gpu_launches": kernels_per_step * K, "kernels_per_step": kernels_per_step,
+    }
+
+
+# Configurations measured besides the headline one in a default run (the metric is quoted
+# at T = 4 / 32 / 256 / 8192): steps, warm-up and expert-kernel samples of each.
+SUB_CONFIGS = {"b8": (240, 24, 200), "b64": (120, 24, 120), "prefill": (36, 12, 24)}
+
+
+def cpu_info():
+    """Host CPU model name and logical core count."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+            for line in r.stdout.splitlines():
+                if line.strip().lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    import platform
+    return {"model": model or platform.processor() or platform.machine(), "arch": platform.machine(),
+            "nproc": os.cpu_count()}
+
+
+def our_arm(args, cfg, dist, torch):
+    import __graft_entry__
+    __graft_entry__.build()  # no-op when the in-tree library is current
+    import routed_moe_decode_gb300 as moe
+    dev = torch.device(f"cuda:{dist.local}")
+    torch.cuda.set_device(dev)
+    algo = {"auto": moe.ALGO_AUTO, "mma": moe.ALGO_MMA, "tcgen05": moe.ALGO_TCGEN05, "simt": moe.ALGO_SIMT,
+            "wide": moe.ALGO_WIDE}[args.algo]
+    L = args.layers if args.layers is not None else min(12, max(1, cfg.layers))
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[cfg.name]
+    W = args.warmup if args.warmup is not None else max(3, 2 * L)
+    W = max(W, 3)
+    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    clock_gpu = gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}"
+
+    t_gen = time.perf_counter()
+    Wd = load_weight_sets(cfg, L, dev, torch)
+    t_gen = time.perf_counter() - t_gen
+    ksamples = args.kernel_samples if args.kernel_samples is not None else max(400, min(K, 2000))
+    m = measure(cfg, moe, torch, dist, dev, Wd, algo, K, W, ksamples,
+                e2e_steps=0 if args.no_e2e else min(max(K, 200), 3000), clock_gpu=clock_gpu)
+
+    # ---- the metric's other configurations, on the same weight sets (same shapes) ----
+    subs = {}
+    same_shape = lambda c: (c.d, c.ffn, c.E, c.k) == (cfg.d, cfg.ffn, cfg.E, cfg.k)
+    if cfg.name == "b1" and not args.no_sub_configs and algo == moe.ALGO_AUTO:
+        for name, (ks, ws_, kk) in SUB_CONFIGS.items():
+            sc = mi.CONFIGS[name]
+            if not same_shape(sc):
+                continue
+            sm = measure(sc, moe, torch, dist, dev, Wd, algo, ks, ws_, kk, clock_gpu=clock_gpu)
+            subs[name] = {
+                "workload": WORKLOAD[name], "T": sc.T, "steps": ks, "warmup": ws_,
+                "us_per_layer": sm["us_per_layer"], "tokens_per_s": sm["tokens_per_s"],
+                "unique_experts_mean": sm["unique_experts_mean"], "unique_bytes_mean": sm["unique_bytes_mean"],
+                "hbm_frac_layer": sm["hbm_frac_layer"], "roofline": sm["roofline"], "clocks": sm["clocks"],
+                "device_status": sm["status"],
+                "weights": "the headline workload's weight sets (same shapes and distribution)",
+            }
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, one GPU only) ----
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        keep_host = mi.gen_layer(cfg, seed=0, layer=0)
+        n, el = time_oracle(cfg, keep_host, budget_s=args.cpu_seconds)
+        info = cpu_info()
+        cpu = {"value": n / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "host_cpu": info["model"], "host_arch": info["arch"], "host_nproc": info["nproc"],
+               "sample": f"{n} single-token steps of layer 0 ({cfg.name}) through the FP32 C++ oracle, "
+                         f"{el:.1f} s on 1 host thread of {info['nproc']} ({info['model']})"}
+
     line = {
         "metric": METRIC,
-        "value": value,
+        "value": m["tokens_per_s"],
         "unit": "tokens/s",
         "n_gpus": dist.world,
         "steps": K,
         "warmup": W,
-        "ms_per_step": t_ms / K,
+        "ms_per_step": m["t_ms"] / K,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -482,26 +577,23 @@ def our_arm(args, cfg, dist, torch):
             "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU",
             "algo": args.algo, "weights": "NVFP4 (E2M1 + E4M3/16 + FP32)", "mma": "FP16 x FP16 -> FP32",
             "layers_cycled": L, "l2": f"inputs larger than L2: {L} layer weight sets "
-                                      f"({L * cfg.E * bpe / 1e9:.1f} GB) cycled",
+                                      f"({L * cfg.E * mi.weight_bytes_per_expert(cfg) / 1e9:.1f} GB) cycled",
             "timing": f"CUDA graphs of {L} layer calls replayed; events on the launch stream",
-            "us_per_layer": us_per_layer,
-            "unique_experts_mean": sum(U[l] for l in steps_layers) / K,
-            "unique_bytes_mean": mean_unique,
-            "hbm_frac_layer": (mean_unique / (us_per_layer * 1e-6) / 1e9) / peak,
+            "us_per_layer": m["us_per_layer"],
+            "unique_experts_mean": m["unique_experts_mean"],
+            "unique_bytes_mean": m["unique_bytes_mean"],
+            "hbm_frac_layer": m["hbm_frac_layer"],
             "input_gen_s": round(t_gen, 1),
         },
-        "roofline": roofline_hbm if run_algo != moe.ALGO_WIDE else roofline_tensor,
-        "clocks": clocks,
-        "gpu_launches": kernels_per_step * K,
-        "device_status": status,
+        "roofline": m["roofline"],
+        "clocks": m["clocks"],
+        "gpu_launches": m["gpu_launches"],
+        "device_status": m["status"],
     }
-    line["roofline"].update({"traffic": traffic,
-                     "kernel": (f"{kname}_kernel" + ("<fused un-route>" if fused_unroute else "")
-                                + (" (after its task-table kernel)" if run_algo == moe.ALGO_WIDE else "")) if kname
-                               else "simt kernels",
-                     "kernel_us": 1e3 * k_avg_ms})
-    if e2e is not None:
-        line["e2e"] = e2e
+    if subs:
+        line["configs"] = subs
+    if m["e2e"] is not None:
+        line["e2e"] = m["e2e"]
     if cpu is not None:
         line["cpu_baseline"] = cpu
     return line

@@ -246,13 +246,36 @@ MOE_API int moe_layer(const moe_shape* shape, const float* logits, const void* h
  *   w13_codes/w13_scales/w2_codes/w2_scales hold the local experts only: entry e - e_begin
  *   is expert e ([e_end - e_begin, 2*ffn, d/2] and so on).
  * Other arguments, ownership and errors as moe_layer; 0 <= e_begin < e_end <= E, else
- * MOE_ERR_INVALID_ARG.  The range applies to this call on the calling host thread only. */
+ * MOE_ERR_INVALID_ARG.  The range is an argument of this call only: nothing is kept
+ * between calls. */
 MOE_API int moe_layer_expert_range(const moe_shape* shape, int e_begin, int e_end, const float* logits,
                                    const void* hidden, const uint8_t* w13_codes, const uint8_t* w13_scales,
                                    float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales,
                                    float w2_scale, const void* residual, void* out, int32_t* ids,
                                    float* weights, void* workspace, size_t workspace_bytes,
                                    moe_stream_t stream);
+
+/* moe_layer_expert_range as a plan / forward pair, for expert-parallel callers that run
+ * the router themselves (moe_route_topk) and schedule the steps apart:
+ *   moe_plan_expert_range             moe_plan restricted to the experts [e_begin, e_end):
+ *                                     routes to other experts get no position and add
+ *                                     nothing;
+ *   moe_forward_experts_expert_range  moe_forward_experts on that plan with the local
+ *                                     weights (entry e - e_begin holds expert e).
+ * moe_forward_prepare stages the hidden rows in between, as for the full layer.  Both
+ * calls of one layer must be given the same range (the plan holds positions for the local
+ * experts only; the expert kernels index the local weights by e - e_begin).  Arguments,
+ * ownership and errors as moe_plan / moe_forward_experts; 0 <= e_begin < e_end <= E, else
+ * MOE_ERR_INVALID_ARG. */
+MOE_API int moe_plan_expert_range(const moe_shape* shape, int e_begin, int e_end, const int32_t* ids,
+                                  const float* weights, void* workspace, size_t workspace_bytes,
+                                  moe_stream_t stream);
+MOE_API int moe_forward_experts_expert_range(const moe_shape* shape, int e_begin, int e_end,
+                                             const uint8_t* w13_codes, const uint8_t* w13_scales,
+                                             float w13_scale, const uint8_t* w2_codes,
+                                             const uint8_t* w2_scales, float w2_scale, const void* residual,
+                                             void* out, void* workspace, size_t workspace_bytes, int algo,
+                                             moe_stream_t stream);
 
 /* The whole layer (moe_layer) with its scratch in a fixed device array of the library
  * instead of a caller-provided workspace.  The pages have no counterpart for this entry
@@ -270,7 +293,9 @@ MOE_API int moe_layer_expert_range(const moe_shape* shape, int e_begin, int e_en
  *     T = 4 or 32 with d = 2048, ffn = 512, E = 512, k = 10), not large prefill chunks.
  *   - Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call before any
- *     stream capture.
+ *     stream capture.  The address is kept for the life of the process and belongs to the
+ *     device's primary context: do not use this entry point after cudaDeviceReset or from
+ *     another context on the same device.
  *   - Sharing: every call uses the same array and leaves its contents behind; the call
  *     clears what must start at zero (status word, counters) itself.  Calls whose work
  *     overlaps on the GPU (different streams, or several host threads) race on the

@@ -42,7 +42,7 @@ try:  # torch is used only for its BF16 / E4M3 rounding of drawn values
 except ImportError:  # pragma: no cover - torch is present in every supported image
     torch = None
 
-__all__ = ["Config", "CONFIGS", "ZIPF_COEF_CALIBRATED", "ZIPF_COEF_LITERAL",
+__all__ = ["Config", "CONFIGS", "ZIPF_COEF_CALIBRATED", "ZIPF_COEF_LITERAL", "E4M3_FINITE_CODES",
            "gen_logits", "gen_hidden", "gen_residual", "gen_weights", "gen_layer",
            "weight_bytes_per_expert"]
 
@@ -158,22 +158,54 @@ def _gen_scales(rng: np.random.Generator, n: int) -> np.ndarray:
     return _to_e4m3_codes((u * np.float32(1.5) + np.float32(0.5)) * np.float32(0.125))
 
 
-def gen_weights(cfg: Config, seed: int = 0, layer: int = 0) -> dict:
-    """NVFP4 expert weights of one layer (see the module docstring for layouts)."""
+# E4M3 codes that are not NaN (S.1111.111 is the format's only NaN; there is no infinity).
+E4M3_FINITE_CODES = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+
+
+def _gen_band_codes(rng: np.random.Generator, n: int, band: int) -> np.ndarray:
+    """E4M3 codes drawn uniformly from the 16 magnitudes 16*band .. 16*band + 15 (the
+    exponent fields 2*band and 2*band + 1; band 0 holds zero and the subnormals, band 7
+    the largest values up to 448; the NaN code is left out) with a uniform sign bit."""
+    if not 0 <= band <= 7:
+        raise ValueError("band must be in 0..7")
+    mags = np.arange(16 * band, 16 * band + 16, dtype=np.uint8)
+    mags = mags[mags != 0x7F]
+    codes = mags[rng.integers(0, mags.size, size=n)]
+    return codes | (rng.integers(0, 2, size=n, dtype=np.uint8) << 7)
+
+
+def _gen_scale_codes(rng: np.random.Generator, n: int, scales: str) -> np.ndarray:
+    if scales == "default":
+        return _gen_scales(rng, n)
+    if scales == "all_finite":  # every finite code, both signs, uniformly
+        return E4M3_FINITE_CODES[rng.integers(0, E4M3_FINITE_CODES.size, size=n)]
+    if scales.startswith("band"):
+        return _gen_band_codes(rng, n, int(scales[4:]))
+    raise ValueError(f"unknown block-scale distribution {scales!r}")
+
+
+def gen_weights(cfg: Config, seed: int = 0, layer: int = 0, scales: str = "default",
+                w13_ts: float = 1.0, w2_ts: float = 1.0) -> dict:
+    """NVFP4 expert weights of one layer (see the module docstring for layouts).
+
+    `scales` picks the E4M3 block-scale distribution: "default" (the workloads'
+    E4M3(U[0.5, 2] * 2^-3)), "band0" .. "band7" (one band of 16 codes, see
+    _gen_band_codes, random signs) or "all_finite" (every non-NaN code).  The FP32
+    tensor scales are passed through as given (the workloads use 1.0)."""
     E, F, d = cfg.E, cfg.ffn, cfg.d
     if d % 16 or F % 16:
         raise ValueError("d and ffn must be multiples of 16 for NVFP4 blocks")
     w13_codes = _raw_bytes(_rng(seed, cfg, layer, "w13_codes"), E * 2 * F * d // 2)
-    w13_scales = _gen_scales(_rng(seed, cfg, layer, "w13_scales"), E * 2 * F * d // 16)
+    w13_scales = _gen_scale_codes(_rng(seed, cfg, layer, "w13_scales"), E * 2 * F * d // 16, scales)
     w2_codes = _raw_bytes(_rng(seed, cfg, layer, "w2_codes"), E * d * F // 2)
-    w2_scales = _gen_scales(_rng(seed, cfg, layer, "w2_scales"), E * d * F // 16)
+    w2_scales = _gen_scale_codes(_rng(seed, cfg, layer, "w2_scales"), E * d * F // 16, scales)
     return {
         "w13_codes": w13_codes.reshape(E, 2 * F, d // 2),
         "w13_scales": w13_scales.reshape(E, 2 * F, d // 16),
-        "w13_ts": 1.0,
+        "w13_ts": float(w13_ts),
         "w2_codes": w2_codes.reshape(E, d, F // 2),
         "w2_scales": w2_scales.reshape(E, d, F // 16),
-        "w2_ts": 1.0,
+        "w2_ts": float(w2_ts),
     }
 
 

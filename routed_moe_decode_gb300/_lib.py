@@ -66,6 +66,9 @@ SIGNATURES = {
     "moe_layer": (_I, [_SP, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_layer_expert_range": (_I, [_SP, _I, _I, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P,
                                     ctypes.c_size_t, _P]),
+    "moe_plan_expert_range": (_I, [_SP, _I, _I, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_forward_experts_expert_range": (_I, [_SP, _I, _I, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _I,
+                                              _P]),
     "moe_layer_static_workspace": (_I, [_SP, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P]),
     "moe_read_device_status": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint32), _P]),
     "moe_plan_summary": (_I, [_SP, _P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), _P]),
@@ -225,6 +228,22 @@ def layer_expert_range(shape: Shape, e_begin: int, e_end: int, logits, hidden, w
         ctypes.byref(shape), int(e_begin), int(e_end), _ptr(logits), _ptr(hidden), _ptr(w["w13_codes"]),
         _ptr(w["w13_scales"]), float(w["w13_ts"]), _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]),
         _ptr(residual), _ptr(out), _ptr(ids), _ptr(weights), ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def plan_expert_range(shape: Shape, e_begin: int, e_end: int, ids, weights, ws: Workspace, stream=None):
+    """moe_plan restricted to the experts [e_begin, e_end) (one expert-parallel shard)."""
+    _check("moe_plan_expert_range", lib().moe_plan_expert_range(
+        ctypes.byref(shape), int(e_begin), int(e_end), _ptr(ids), _ptr(weights), ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def forward_experts_expert_range(shape: Shape, e_begin: int, e_end: int, w: dict, residual, out, ws: Workspace,
+                                 algo: int = ALGO_AUTO, stream=None):
+    """moe_forward_experts on a plan of moe_plan_expert_range with the same range; `w` holds
+    the local experts' weights only (entry e - e_begin is expert e)."""
+    _check("moe_forward_experts_expert_range", lib().moe_forward_experts_expert_range(
+        ctypes.byref(shape), int(e_begin), int(e_end), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]),
+        float(w["w13_ts"]), _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]), _ptr(residual), _ptr(out),
+        ws.ptr, ws.nbytes, int(algo), _stream(stream)))
 
 
 def read_status(ws: Workspace, clear: bool = True, stream=None) -> int:

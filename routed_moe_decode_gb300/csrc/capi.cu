@@ -138,22 +138,17 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
-// Experts a call computes (moe_layer_expert_range sets it for the duration of its call on
-// this host thread; every other entry point sees all experts).
+// Experts a call plans and computes, [lo, hi): every expert for the ordinary entry points,
+// one block of experts for the expert-parallel ones (the weights passed in then hold that
+// block only, expert e at entry e - lo).  Passed explicitly through every internal call.
 struct ExpertRange {
-  int lo = 0, hi = -1;  // hi < 0: all E experts
+  int lo, hi;
 };
-thread_local ExpertRange g_range;
-struct RangeScope {
-  RangeScope(int lo, int hi) { g_range = ExpertRange{lo, hi}; }
-  ~RangeScope() { g_range = ExpertRange{}; }
-};
-int range_lo() { return g_range.hi < 0 ? 0 : g_range.lo; }
-int range_hi(const moe_shape* s) { return g_range.hi < 0 ? s->E : g_range.hi; }
+ExpertRange all_experts(const moe_shape* s) { return ExpertRange{0, s->E}; }
 
 moe::ExpertArgs expert_args(const moe_shape* s, const WsLayout& L, void* ws, const uint8_t* w13c,
                             const uint8_t* w13s, float w13_ts, const uint8_t* w2c, const uint8_t* w2s, float w2_ts,
-                            const void* residual, void* out) {
+                            const void* residual, void* out, ExpertRange r) {
   moe::ExpertArgs a{};
   a.T = s->T; a.d = s->d; a.F = s->ffn; a.E = s->E; a.k = s->k; a.R = L.R;
   a.S_gu = L.S_gu; a.S_dn = L.S_dn;
@@ -179,7 +174,7 @@ moe::ExpertArgs expert_args(const moe_shape* s, const WsLayout& L, void* ws, con
   a.status = at<int>(ws, L.status);
   a.residual = static_cast<const __nv_bfloat16*>(residual);
   a.out = static_cast<__nv_bfloat16*>(out);
-  a.e_lo = range_lo();
+  a.e_lo = r.lo;
   return a;
 }
 
@@ -254,7 +249,7 @@ int moe_route_topk(const moe_shape* shape, const float* logits, int32_t* ids, fl
 }
 
 static void fill_plan_args(moe::PlanArgs& a, const moe_shape* shape, const WsLayout& L, void* workspace,
-                           const int32_t* ids, const float* weights) {
+                           const int32_t* ids, const float* weights, ExpertRange r) {
   a.T = shape->T; a.E = shape->E; a.k = shape->k; a.S_gu = L.S_gu; a.S_dn = L.S_dn;
   a.ids = ids; a.weights = weights;
   a.status = at<int>(workspace, L.status);
@@ -269,12 +264,12 @@ static void fill_plan_args(moe::PlanArgs& a, const moe_shape* shape, const WsLay
   a.route_w = at<float>(workspace, L.route_w);
   a.tasks = at<moe::TaskEntry>(workspace, L.tasks);
   a.hist = at<int>(workspace, L.hist);
-  a.e_lo = range_lo();
-  a.e_hi = range_hi(shape);
+  a.e_lo = r.lo;
+  a.e_hi = r.hi;
 }
 
-int moe_plan(const moe_shape* shape, const int32_t* ids, const float* weights, void* workspace,
-             size_t workspace_bytes, moe_stream_t stream) {
+static int plan_impl(const moe_shape* shape, const int32_t* ids, const float* weights, void* workspace,
+                     size_t workspace_bytes, ExpertRange r, moe_stream_t stream) {
   int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   if (shape->T == 0) return MOE_OK;
@@ -283,10 +278,17 @@ int moe_plan(const moe_shape* shape, const int32_t* ids, const float* weights, v
   if (rc != MOE_OK) return rc;
   const WsLayout L = moe::ws_layout(*shape);
   moe::PlanArgs a{};
-  fill_plan_args(a, shape, L, workspace, ids, weights);
+  fill_plan_args(a, shape, L, workspace, ids, weights, r);
   cudaError_t e = moe::launch_plan(a, stream);
   if (e != cudaSuccess) { set_error("plan launch", e); return MOE_ERR_CUDA; }
   return MOE_OK;
+}
+
+int moe_plan(const moe_shape* shape, const int32_t* ids, const float* weights, void* workspace,
+             size_t workspace_bytes, moe_stream_t stream) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  return plan_impl(shape, ids, weights, workspace, workspace_bytes, all_experts(shape), stream);
 }
 
 int moe_forward_prepare(const moe_shape* shape, const void* hidden, void* workspace, size_t workspace_bytes,
@@ -315,7 +317,8 @@ enum { kStageExperts = 1, kStageUnroute = 2 };
 static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
                                 float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
                                 const void* residual, void* out, void* workspace, size_t workspace_bytes, int algo,
-                                unsigned long long* trace, moe_stream_t stream, int stages = kStageExperts | kStageUnroute) {
+                                unsigned long long* trace, moe_stream_t stream, ExpertRange r,
+                                int stages = kStageExperts | kStageUnroute) {
   int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   if (shape->T == 0) return MOE_OK;
@@ -330,7 +333,7 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
   if (rc != MOE_OK) return rc;
   const WsLayout L = moe::ws_layout(*shape);
   moe::ExpertArgs a = expert_args(shape, L, workspace, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales,
-                                  w2_scale, residual, out);
+                                  w2_scale, residual, out, r);
   a.trace = trace;
   cudaError_t e;
   if (!(stages & kStageExperts)) {
@@ -358,18 +361,18 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
   const uint32_t box = use_mma ? 128u : 64u;
   CUtensorMap tm13, tm2;
   rc = encode_codes_map(&tm13, w13_codes, static_cast<uint64_t>(shape->d) / 2,
-                        static_cast<uint64_t>(range_hi(shape) - range_lo()) * 2 * shape->ffn, box);
+                        static_cast<uint64_t>(r.hi - r.lo) * 2 * shape->ffn, box);
   if (rc != MOE_OK) return rc;
   rc = encode_codes_map(&tm2, w2_codes, static_cast<uint64_t>(shape->ffn) / 2,
-                        static_cast<uint64_t>(range_hi(shape) - range_lo()) * shape->d, box);
+                        static_cast<uint64_t>(r.hi - r.lo) * shape->d, box);
   if (rc != MOE_OK) return rc;
   if (use_mma) {
     CUtensorMap ts13, ts2;
     rc = moe::encode_scales_map(&ts13, w13_scales, static_cast<uint32_t>(shape->d / 16),
-                                static_cast<uint64_t>(range_hi(shape) - range_lo()) * 2 * shape->ffn, 64);
+                                static_cast<uint64_t>(r.hi - r.lo) * 2 * shape->ffn, 64);
     if (rc != MOE_OK) return rc;
     rc = moe::encode_scales_map(&ts2, w2_scales, static_cast<uint32_t>(shape->ffn / 16),
-                                static_cast<uint64_t>(range_hi(shape) - range_lo()) * shape->d, 64);
+                                static_cast<uint64_t>(r.hi - r.lo) * shape->d, 64);
     if (rc != MOE_OK) return rc;
     // for few tokens the decode kernel runs the un-route as trailing tasks of its own
     a.ncb = (stages & kStageUnroute) ? moe::expert_mma_unroute_tasks(shape->T, L.S_dn) : 0;
@@ -400,22 +403,53 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
 int moe_forward_expert_kernels(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
                                float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
                                void* workspace, size_t workspace_bytes, int algo, moe_stream_t stream) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
   return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, nullptr,
-                              nullptr, workspace, workspace_bytes, algo, nullptr, stream, kStageExperts);
+                              nullptr, workspace, workspace_bytes, algo, nullptr, stream, all_experts(shape),
+                              kStageExperts);
 }
 
 int moe_forward_unroute(const moe_shape* shape, const void* residual, void* out, void* workspace,
                         size_t workspace_bytes, moe_stream_t stream) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
   return forward_experts_impl(shape, nullptr, nullptr, 0.f, nullptr, nullptr, 0.f, residual, out, workspace,
-                              workspace_bytes, MOE_ALGO_AUTO, nullptr, stream, kStageUnroute);
+                              workspace_bytes, MOE_ALGO_AUTO, nullptr, stream, all_experts(shape), kStageUnroute);
 }
 
 int moe_forward_experts(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
                         float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
                         const void* residual, void* out, void* workspace, size_t workspace_bytes, int algo,
                         moe_stream_t stream) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
   return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
-                              workspace, workspace_bytes, algo, nullptr, stream);
+                              workspace, workspace_bytes, algo, nullptr, stream, all_experts(shape));
+}
+
+static int check_range(const moe_shape* shape, int e_begin, int e_end) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (e_begin < 0 || e_end > shape->E || e_begin >= e_end) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+int moe_plan_expert_range(const moe_shape* shape, int e_begin, int e_end, const int32_t* ids, const float* weights,
+                          void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  const int rc = check_range(shape, e_begin, e_end);
+  if (rc != MOE_OK) return rc;
+  return plan_impl(shape, ids, weights, workspace, workspace_bytes, ExpertRange{e_begin, e_end}, stream);
+}
+
+int moe_forward_experts_expert_range(const moe_shape* shape, int e_begin, int e_end, const uint8_t* w13_codes,
+                                     const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes,
+                                     const uint8_t* w2_scales, float w2_scale, const void* residual, void* out,
+                                     void* workspace, size_t workspace_bytes, int algo, moe_stream_t stream) {
+  const int rc = check_range(shape, e_begin, e_end);
+  if (rc != MOE_OK) return rc;
+  return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
+                              workspace, workspace_bytes, algo, nullptr, stream, ExpertRange{e_begin, e_end});
 }
 
 int moe_selftest_expert_trace(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
@@ -423,8 +457,10 @@ int moe_selftest_expert_trace(const moe_shape* shape, const uint8_t* w13_codes, 
                               const void* residual, void* out, void* workspace, size_t workspace_bytes,
                               unsigned long long* trace, moe_stream_t stream) {
   if (!trace) return MOE_ERR_INVALID_ARG;
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
   return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
-                              workspace, workspace_bytes, MOE_ALGO_AUTO, trace, stream);
+                              workspace, workspace_bytes, MOE_ALGO_AUTO, trace, stream, all_experts(shape));
 }
 
 int moe_forward_algo(const moe_shape* shape, const void* hidden, const uint8_t* w13_codes,
@@ -452,8 +488,8 @@ int moe_forward(const moe_shape* shape, const void* hidden, const uint8_t* w13_c
                           out, workspace, workspace_bytes, MOE_ALGO_AUTO, stream);
 }
 
-int moe_front(const moe_shape* shape, const float* logits, const void* hidden, int32_t* ids, float* weights,
-              void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+static int front_impl(const moe_shape* shape, const float* logits, const void* hidden, int32_t* ids, float* weights,
+                      void* workspace, size_t workspace_bytes, ExpertRange r, moe_stream_t stream) {
   int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   if (shape->T == 0) return MOE_OK;
@@ -461,7 +497,7 @@ int moe_front(const moe_shape* shape, const float* logits, const void* hidden, i
     // large batches: separate router, plan and preparation kernels
     rc = moe_route_topk(shape, logits, ids, weights, stream);
     if (rc != MOE_OK) return rc;
-    rc = moe_plan(shape, ids, weights, workspace, workspace_bytes, stream);
+    rc = plan_impl(shape, ids, weights, workspace, workspace_bytes, r, stream);
     if (rc != MOE_OK) return rc;
     return moe_forward_prepare(shape, hidden, workspace, workspace_bytes, stream);
   }
@@ -472,7 +508,7 @@ int moe_front(const moe_shape* shape, const float* logits, const void* hidden, i
   if (rc != MOE_OK) return rc;
   const WsLayout L = moe::ws_layout(*shape);
   moe::FrontArgs f{};
-  fill_plan_args(f.plan, shape, L, workspace, ids, weights);
+  fill_plan_args(f.plan, shape, L, workspace, ids, weights, r);
   f.d = shape->d;
   f.logits = logits;
   f.hidden = static_cast<const __nv_bfloat16*>(hidden);
@@ -485,18 +521,35 @@ int moe_front(const moe_shape* shape, const float* logits, const void* hidden, i
   return MOE_OK;
 }
 
-int moe_layer(const moe_shape* shape, const float* logits, const void* hidden, const uint8_t* w13_codes,
-              const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales,
-              float w2_scale, const void* residual, void* out, int32_t* ids, float* weights, void* workspace,
-              size_t workspace_bytes, moe_stream_t stream) {
+int moe_front(const moe_shape* shape, const float* logits, const void* hidden, int32_t* ids, float* weights,
+              void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  return front_impl(shape, logits, hidden, ids, weights, workspace, workspace_bytes, all_experts(shape), stream);
+}
+
+static int layer_impl(const moe_shape* shape, const float* logits, const void* hidden, const uint8_t* w13_codes,
+                      const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales,
+                      float w2_scale, const void* residual, void* out, int32_t* ids, float* weights, void* workspace,
+                      size_t workspace_bytes, ExpertRange r, moe_stream_t stream) {
   int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   if (shape->T == 0) return MOE_OK;
   if (!w13_codes || !w13_scales || !w2_codes || !w2_scales || !out) return MOE_ERR_INVALID_ARG;
-  rc = moe_front(shape, logits, hidden, ids, weights, workspace, workspace_bytes, stream);
+  rc = front_impl(shape, logits, hidden, ids, weights, workspace, workspace_bytes, r, stream);
   if (rc != MOE_OK) return rc;
   return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
-                              workspace, workspace_bytes, MOE_ALGO_AUTO, nullptr, stream);
+                              workspace, workspace_bytes, MOE_ALGO_AUTO, nullptr, stream, r);
+}
+
+int moe_layer(const moe_shape* shape, const float* logits, const void* hidden, const uint8_t* w13_codes,
+              const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales,
+              float w2_scale, const void* residual, void* out, int32_t* ids, float* weights, void* workspace,
+              size_t workspace_bytes, moe_stream_t stream) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  return layer_impl(shape, logits, hidden, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual,
+                    out, ids, weights, workspace, workspace_bytes, all_experts(shape), stream);
 }
 
 int moe_layer_expert_range(const moe_shape* shape, int e_begin, int e_end, const float* logits, const void* hidden,
@@ -504,12 +557,10 @@ int moe_layer_expert_range(const moe_shape* shape, int e_begin, int e_end, const
                            const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale, const void* residual,
                            void* out, int32_t* ids, float* weights, void* workspace, size_t workspace_bytes,
                            moe_stream_t stream) {
-  int rc = check_shape(shape);
+  const int rc = check_range(shape, e_begin, e_end);
   if (rc != MOE_OK) return rc;
-  if (e_begin < 0 || e_end > shape->E || e_begin >= e_end) return MOE_ERR_INVALID_ARG;
-  RangeScope scope(e_begin, e_end);
-  return moe_layer(shape, logits, hidden, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual,
-                   out, ids, weights, workspace, workspace_bytes, stream);
+  return layer_impl(shape, logits, hidden, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual,
+                    out, ids, weights, workspace, workspace_bytes, ExpertRange{e_begin, e_end}, stream);
 }
 
 int moe_read_device_status(const void* workspace, int clear, uint32_t* status_bits, moe_stream_t stream) {

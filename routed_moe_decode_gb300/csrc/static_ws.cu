@@ -18,10 +18,19 @@ std::mutex g_static_mutex;
 
 // Device address of the array on the current device, looked up once per device.  In host
 // code `g_static_workspace` only names a host-side stand-in; kernels must be given this
-// address instead.
+// address instead.  The cached address belongs to the device's primary context as the
+// first call found it: a process that resets the device (cudaDeviceReset) or drives it
+// through another context must not use this entry point afterwards.
 int static_workspace_address(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    moe::set_last_error_message("moe_layer_static_workspace: cudaGetDevice failed");
+    return MOE_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    moe::set_last_error_message("moe_layer_static_workspace: device ordinal beyond the library's table of 64");
+    return MOE_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lock(g_static_mutex);
   if (!g_static_ptr[dev]) {
     void* p = nullptr;
@@ -60,7 +69,10 @@ int moe_layer_static_workspace(const moe_shape* shape, const float* logits, cons
   const int arc = static_workspace_address(&ws);
   if (arc != MOE_OK) return arc;
   // the status word must start at zero; every other field is rewritten by the call
-  if (cudaMemsetAsync(ws, 0, 256, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, 256, stream) != cudaSuccess) {
+    moe::set_last_error_message("moe_layer_static_workspace: clearing the status block failed");
+    return MOE_ERR_CUDA;
+  }
   return moe_layer(shape, logits, hidden, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale,
                    residual, out, ids, weights, ws, need, stream);
 }

@@ -447,6 +447,41 @@ def test_expert_parallel_shards_sum_to_layer(name, bounds):
     assert_parity(total.astype(np.float32), full, f"{name} sum of {len(bounds) - 1} shards")
 
 
+@pytest.mark.parametrize("name,e0,e1", [("b1", 128, 384), ("b8", 0, 200), ("tiny", 9, 16)])
+def test_expert_range_plan_forward_pair_matches_one_call(name, e0, e1):
+    """moe_route_topk + moe_plan_expert_range + moe_forward_prepare +
+    moe_forward_experts_expert_range (the range passed to each call) gives the bits of one
+    moe_layer_expert_range call."""
+    import routed_moe_decode_gb300 as moe
+    cfg = mi.CONFIGS[name]
+    inp = config_inputs(name)
+    dev = torch.device("cuda")
+    shape = moe.shape_of(cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k)
+    logits = torch.from_numpy(np.ascontiguousarray(inp["logits"])).to(dev)
+    hidden = bf16_tensor(inp["hidden"], dev)
+    res = bf16_tensor(inp["residual"], dev)
+    local = {n: np.ascontiguousarray(inp[n][e0:e1]) for n in ("w13_codes", "w13_scales", "w2_codes", "w2_scales")}
+    local["w13_ts"], local["w2_ts"] = inp["w13_ts"], inp["w2_ts"]
+    w = device_weights(local, dev)
+    outs = []
+    for split in (False, True):
+        ws = moe.Workspace(shape)
+        ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+        wts = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
+        out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
+        if split:
+            moe.route_topk(shape, logits, ids, wts)
+            moe.plan_expert_range(shape, e0, e1, ids, wts, ws)
+            moe.forward_prepare(shape, hidden, ws)
+            moe.forward_experts_expert_range(shape, e0, e1, w, res, out, ws)
+        else:
+            moe.layer_expert_range(shape, e0, e1, logits, hidden, w, res, out, ids, wts, ws)
+        torch.cuda.synchronize()
+        assert moe.read_status(ws) == 0
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_expert_range_rejects_bad_bounds():
     import routed_moe_decode_gb300 as moe
     cfg = mi.CONFIGS["tiny"]
