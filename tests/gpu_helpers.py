@@ -54,9 +54,27 @@ def parity_metrics(got: np.ndarray, ref: np.ndarray):
     return float(err.max()) / rms, float(err.sum() / np.abs(ref).sum())
 
 
-def assert_parity(got: np.ndarray, ref: np.ndarray, what=""):
+# The layer's output is BF16, whose own round-to-nearest error reaches 2^-8 of the value
+# (half a unit in the last place at the bottom of a binade).  Where a case's outputs have a
+# heavier tail than the workloads' (max |out| above ~5 RMS), that rounding alone can exceed
+# 2e-2 RMS; such cases compare with the rounding allowed on top of the tolerance.
+BF16_HALF_ULP_REL = 2.0 ** -8
+
+
+def parity_metrics_bf16(got: np.ndarray, ref: np.ndarray):
+    """max over elements of (|d| - 2^-8 |ref|) / RMS(ref): the error left after the output's
+    own BF16 rounding is allowed for."""
+    ref = ref.astype(np.float64)
+    err = np.abs(got.astype(np.float64) - ref) - BF16_HALF_ULP_REL * np.abs(ref)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    return float(err.max()) / rms
+
+
+def assert_parity(got: np.ndarray, ref: np.ndarray, what="", bf16_rounding=False):
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     mx, mean_rel = parity_metrics(got, ref)
+    if bf16_rounding:
+        mx = parity_metrics_bf16(got, ref)
     log = os.environ.get("MOE_PARITY_LOG")
     if log:
         with open(log, "a") as f:

@@ -15,6 +15,10 @@ few tokens, a kernel of its own otherwise) runs against the CPU oracle with:
     the bands' exact results are identical up to the powers of two);
   - block scales spread over every finite E4M3 code at once.
 Intermediates that leave the FP16 store range must set the documented status bits.
+
+The output is compared with max |d_i| <= 2e-2 RMS(ref) + 2^-8 |ref_i| (the output's own
+BF16 rounding allowed on top of the layer's tolerance: these cases reach |out| ~ 6 RMS,
+where BF16 rounding alone can exceed 2e-2 RMS) and sum |d| / sum |ref| <= 5e-3.
 """
 import numpy as np
 import pytest
@@ -63,7 +67,9 @@ def _parity(cfg, inp, algo, what):
     ids_ref, w_ref = O.route_topk(inp["logits"], cfg.k)
     np.testing.assert_array_equal(ids, ids_ref)
     ref = O.moe_experts((cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k), inp["hidden"], ids_ref, w_ref, inp, inp["residual"])
-    return assert_parity(out, ref, what)
+    # block scales from one band give heavier-tailed outputs than the workloads' (up to
+    # ~6 RMS), so the output's own BF16 rounding is allowed on top of the tolerance
+    return assert_parity(out, ref, what, bf16_rounding=True)
 
 
 @pytest.mark.parametrize("scales,ts13,ts2", SCALE_CASES, ids=[f"{c[0]}-{c[1]:.4g}-{c[2]:.4g}" for c in SCALE_CASES])
