@@ -44,8 +44,11 @@ MOE_API int moe_selftest_mma(const void* A, const void* B, float* D, moe_stream_
  * Warp-MMA kernel: role 0 weight producer (1 task published, 2 chunk issued), 1 activation
  * producer (3 readiness met, 4 chunk issued), 2 and 3 first and last compute warp (5 task
  * taken, index bit 15 = down task; 6 chunks done; 12 un-route wait begins, 13 wait met),
- * 4 publisher (9 task released), 5 CTA (10 start, 11 end).  tcgen05 kernel: roles 0 and 1 as above, 2 first
- * dequantisation warp (5 chunk landed, 6 chunk in tensor memory), 3 MMA (7 chunk issued),
+ * 4 publisher (9 task released), 5 CTA (10 start, 11 end).  Decode kernel for at most eight
+ * tokens: as the warp-MMA kernel, with role 1 event 3 = a down task's h rows requested, role 2
+ * events 7 / 8 = a barrier round of two chunks begins / its data has landed, role 5 event 14 =
+ * kernel entry (before the wait for the preceding kernel).  tcgen05 kernel: roles 0 and 1 as
+ * above, 2 first dequantisation warp (5 chunk landed, 6 chunk in tensor memory), 3 MMA (7 chunk issued),
  * 4 epilogue (8 accumulator ready, 9 task done), 5 CTA (10 start, 11 end). */
 MOE_API int moe_selftest_expert_trace(const moe_shape* shape, const uint8_t* w13_codes,
                                       const uint8_t* w13_scales, float w13_scale,

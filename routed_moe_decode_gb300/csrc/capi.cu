@@ -376,8 +376,14 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     if (rc != MOE_OK) return rc;
     // for few tokens the decode kernel runs the un-route as trailing tasks of its own
     a.ncb = (stages & kStageUnroute) ? moe::expert_mma_unroute_tasks(shape->T, L.S_dn) : 0;
-    e = moe::launch_expert_mma(a, tm13, tm2, ts13, ts2, di.num_sms, stream);
-    if (e != cudaSuccess) { set_error("expert_mma launch", e); return MOE_ERR_CUDA; }
+    // at most eight tokens: the variant with the hidden rows resident in shared memory
+    if (moe::expert_dec_supports(shape->T, shape->d, shape->ffn)) {
+      e = moe::launch_expert_dec(a, tm13, tm2, ts13, ts2, di.num_sms, stream);
+      if (e != cudaSuccess) { set_error("expert_dec launch", e); return MOE_ERR_CUDA; }
+    } else {
+      e = moe::launch_expert_mma(a, tm13, tm2, ts13, ts2, di.num_sms, stream);
+      if (e != cudaSuccess) { set_error("expert_mma launch", e); return MOE_ERR_CUDA; }
+    }
     if (a.ncb > 0) return MOE_OK;
   } else if (use_wide) {
     // the wide kernel's own task table (passes of kWideRows rows), from the plan's arrays

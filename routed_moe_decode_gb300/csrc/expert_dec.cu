@@ -1,0 +1,568 @@
+// Decode expert kernel for verify steps of at most eight tokens (T <= 8), so that no expert
+// holds more than eight routed rows and every task is one 8-column MMA tile.
+//
+// Same weight stream and MMA core as the warp-MMA kernel of expert_mma.cu (one resident CTA
+// per SM, tasks from the plan's task table through tickets, 256-K chunks of E2M1 codes and
+// block scales by TMA into a ring, in-register dequantisation into the A fragments of
+// mma.sync m16n8k16), but the activations never travel with the chunks:
+//   - the FP16 hidden rows of all T tokens (at most 8 x 2d bytes) are copied into shared
+//     memory once, when the kernel starts, and every gate/up task reads its routed rows
+//     there (the token of each routed row comes with the task entry);
+//   - each down task's h rows (at most 8 x 2F bytes, published by the gate/up tasks of its
+//     expert) are copied once per task into one of two to four slots, as soon as the expert's
+//     readiness counter allows, while the compute warps still work on earlier tasks.
+// So a chunk's stage is full once its weight bytes have landed; compute warps wait on one
+// barrier per chunk and the weight producer is the only per-chunk issuer.
+//
+// Warps: 0 task fetcher + weight producer, 1 activation producer (hidden rows once, h rows
+// per down task), 2 publisher (one GPU-scope release per finished task), 3-10 compute (16
+// weight rows each of the 128-row task tile, as in expert_mma.cu), and with the un-route
+// fused, trailing un-route tasks (one token's 128 columns of a stripe per compute warp)
+// once the stripe's down tasks have been released.
+#include "mma_parts.cuh"
+
+namespace moe {
+
+namespace dk {
+
+using namespace mk;
+
+constexpr int kStages = 9;
+constexpr int kMaxRows = 8;  // routed rows per expert: at most T <= 8
+// The fetcher claims its next ticket once at most kReserve of its chunks are in flight: a
+// claim (ticket atomic, then the entry, then a gate/up task's tokens) takes about three L2
+// round trips, which this many chunks cover.
+constexpr int kReserve = 6;
+constexpr int kTaskConsumers = 2 + kComputeWarps;  // activation producer, publisher, compute
+constexpr int kPubSlots = 2 * kTaskSlots;
+constexpr int kMaxHSlots = 4;
+
+struct Smem {
+  uint8_t ring[kStages][kStageA];
+  TaskEntry task[kTaskSlots];
+  int task_tok[kTaskSlots][kMaxRows];  // token of each routed row of a gate/up task
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t task_full[kTaskSlots];
+  uint64_t task_empty[kTaskSlots];
+  uint64_t pub_full[kPubSlots];
+  uint64_t x_full;
+  uint64_t h_full[kMaxHSlots];
+  uint64_t h_empty[kMaxHSlots];
+  int abort_flag;
+};
+
+constexpr int kSmemLimit = 227 * 1024;
+
+// Activation arena after Smem: FP16 hidden rows [T][xpitch], then `hslots` (2 to 4, as many
+// as fit) slots of h rows [T][hpitch]; the 16-byte pad per row keeps consecutive rows off the
+// same banks.
+struct Arena {
+  int xpitch, hpitch, x_bytes, slot_bytes, hslots;
+};
+
+__host__ __device__ inline size_t fixed_smem_bytes() { return 1024 + ((sizeof(Smem) + 127) & ~size_t(127)); }
+
+__host__ __device__ inline Arena arena_of(int T, int d, int F) {
+  Arena r;
+  r.xpitch = 2 * d + 16;
+  r.hpitch = 2 * F + 16;
+  r.x_bytes = T * r.xpitch;
+  r.slot_bytes = T * r.hpitch;
+  const long long room = static_cast<long long>(kSmemLimit) - static_cast<long long>(fixed_smem_bytes()) - r.x_bytes;
+  const long long fit = r.slot_bytes > 0 ? room / r.slot_bytes : 0;
+  r.hslots = static_cast<int>(fit < kMaxHSlots ? fit : kMaxHSlots);
+  return r;
+}
+
+// Ticket order of this kernel: the plan's gate/up tasks, one per ticket; then its down tasks
+// in table order (expert-major, so the down tasks of the experts whose gate/up tasks were
+// claimed first come first) -- two per ticket (stripes 2m and 2m + 1 of one expert: S_dn is
+// even, and the table holds an expert's stripes consecutively), except the last `nsingle`
+// (one per CTA of the grid), one per ticket, so that the final claims are short; then, with
+// the un-route fused, one un-route task per down stripe (T <= 8 tokens, one per compute
+// warp).  Pairing halves the claims and lets the second task's h rows arrive with the first's.
+struct TicketMap {
+  int ngu, npair, nsingle, ndn_tickets;
+};
+
+__device__ __forceinline__ TicketMap ticket_map(int ngu, int ndn, int grid) {
+  TicketMap m;
+  m.ngu = ngu;
+  m.nsingle = min(ndn, grid & ~1);  // even, so that the pairs cover an even number of tasks
+  m.npair = (ndn - m.nsingle) / 2;
+  m.ndn_tickets = m.npair + m.nsingle;
+  return m;
+}
+
+__device__ __forceinline__ void task_of(const ExpertArgs& a, int i, const TicketMap& m, TaskEntry& e0, TaskEntry& e1,
+                                        bool& two) {
+  two = false;
+  if (i < m.ngu) {
+    e0 = a.tasks[i];
+  } else if (i < m.ngu + m.npair) {
+    const int j = m.ngu + 2 * (i - m.ngu);
+    e0 = a.tasks[j];
+    e1 = a.tasks[j + 1];
+    two = true;
+  } else if (i < m.ngu + m.ndn_tickets) {
+    e0 = a.tasks[i + m.npair];
+  } else {
+    e0 = TaskEntry{0, 0, 1 << 18, i - m.ngu - m.ndn_tickets};
+  }
+}
+
+__device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int g, int& tok, int* status) {
+  const int q = n % kTaskSlots;
+  const uint32_t ph = static_cast<uint32_t>((n / kTaskSlots) & 1);
+  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, &sm.abort_flag, status)) return false;
+  out = sm.task[q];
+  tok = sm.task_tok[q][g & (kMaxRows - 1)];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&sm.task_empty[q]));
+  return true;
+}
+
+// One chunk of a task for one compute warp: per sub-chunk h, the B fragments (elements
+// [256c + 128h + 32q, +32) of the routed row as four 16-byte pieces), the dequantised A
+// fragments of rows g and g + 8, and 8 MMAs into 8 independent accumulators.
+__device__ __forceinline__ void chunk_mma(const ChunkCodes& cc, const uint8_t* bc, bool live, float (&acc)[8][4]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint4 xb[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      xb[j] = live ? *reinterpret_cast<const uint4*>(bc + 256 * h + 16 * j) : make_uint4(0, 0, 0, 0);
+    uint32_t fa[16], fb[16];
+    dequant32(cc.ca[h], cc.sa[h], fa);
+    dequant32(cc.cb[h], cc.sb[h], fb);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      mma_16816(acc[2 * j], fa[4 * j + 0], fb[4 * j + 0], fa[4 * j + 1], fb[4 * j + 1], xb[j].x, xb[j].y);
+      mma_16816(acc[2 * j + 1], fa[4 * j + 2], fb[4 * j + 2], fa[4 * j + 3], fb[4 * j + 3], xb[j].z, xb[j].w);
+    }
+  }
+}
+
+// The chunk loop of one task for one compute warp, two chunks per barrier round: wait for
+// both stages, copy their codes and scales into registers, hand both stages back, then run
+// the MMAs.  Each lane waits on its own (no warp vote per chunk); a wait that gives up leaves
+// the lane computing on stale data until the task ends, where the warp decides together
+// (every later wait returns at once because the CTA's abort flag is raised).  The 16
+// k-steps of a chunk go to 8 independent accumulators, summed in a fixed order at the end.
+// `brow` is the thread's activation row (routed row g) in shared memory.
+__device__ __forceinline__ bool run_task_chunks(Smem& sm, const ExpertArgs& a, int& stage, uint32_t& phase,
+                                                float (&acc)[8][4], int lra, int lrb, int nck, const uint8_t* brow,
+                                                bool live, int q, bool tr, int& tcnt) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+  bool ok = true;
+  for (int c = 0; c < nck; c += 2) {
+    const bool two = c + 1 < nck;
+    ChunkCodes c0, c1;
+    if (tr) trace_ev(a, 2, tcnt, 7, c);
+    ok &= bounded_wait(smem_addr(&sm.full[stage]), phase, &sm.abort_flag, a.status);
+    if (tr) trace_ev(a, 2, tcnt, 8, c);
+    load_chunk_codes(&sm.ring[stage][0], lra, lrb, q, c0);
+    const int st0 = stage;
+    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+    int st1 = st0;
+    if (two) {
+      ok &= bounded_wait(smem_addr(&sm.full[stage]), phase, &sm.abort_flag, a.status);
+      load_chunk_codes(&sm.ring[stage][0], lra, lrb, q, c1);
+      st1 = stage;
+      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+    }
+    // the stages' bytes are in registers: hand them back to the producer
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(smem_addr(&sm.empty[st0]));
+      if (two) mbar_arrive(smem_addr(&sm.empty[st1]));
+    }
+    const uint8_t* bc = brow + 2 * kChunk * c + 64 * q;
+    chunk_mma(c0, bc, live, acc);
+    if (two) chunk_mma(c1, bc + 2 * kChunk, live, acc);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    acc[0][i] = ((acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i])) + ((acc[4][i] + acc[5][i]) + (acc[6][i] + acc[7][i]));
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait for the last phase of a barrier this warp's copies complete on (drain).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < kTimeoutCycles) {}
+}
+
+}  // namespace dk
+
+using namespace dk;
+
+template <bool kFused>
+__global__ void __launch_bounds__(kThreads, 1)
+    expert_dec_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_w2,
+                      const __grid_constant__ CUtensorMap tm_s13, const __grid_constant__ CUtensorMap tm_s2,
+                      const __grid_constant__ ExpertArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* arena = reinterpret_cast<uint8_t*>(&sm) + ((sizeof(Smem) + 127) & ~size_t(127));
+  const Arena ar = arena_of(a.T, a.d, a.F);
+  uint8_t* xs = arena;                 // hidden rows
+  uint8_t* hs = arena + ar.x_bytes;    // h slots
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int tcnt0 = 2;
+  if (tid == 0) trace_ev(a, 5, tcnt0, 14, 0);  // kernel entry, before the dependency wait
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_addr(&sm.full[i]), 1);
+      mbar_init(smem_addr(&sm.empty[i]), kComputeWarps);
+    }
+    for (int i = 0; i < kTaskSlots; ++i) {
+      mbar_init(smem_addr(&sm.task_full[i]), 1);
+      mbar_init(smem_addr(&sm.task_empty[i]), kTaskConsumers);
+    }
+    for (int i = 0; i < kPubSlots; ++i) mbar_init(smem_addr(&sm.pub_full[i]), kComputeWarps);
+    mbar_init(smem_addr(&sm.x_full), 1);
+    for (int i = 0; i < kMaxHSlots; ++i) {
+      mbar_init(smem_addr(&sm.h_full[i]), 1);
+      mbar_init(smem_addr(&sm.h_empty[i]), kComputeWarps);
+    }
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_w13);
+    prefetch_tmap(&tm_w2);
+    prefetch_tmap(&tm_s13);
+    prefetch_tmap(&tm_s2);
+  }
+  // everything above is local to the CTA; the plan, the counters and the FP16 hidden rows
+  // come from the preceding kernel
+  pdl_wait();
+  pdl_launch_dependents();
+  __syncthreads();
+  const uint32_t ring0 = smem_addr(&sm.ring[0][0]);
+  int tcnt = 0;
+  if (tid == 0) trace_ev(a, 5, tcnt, 10, 0);
+
+  if (warp == 0) {
+    // ------------- task fetcher + weight producer -------------
+    const uint64_t pol = policy_evict_first();
+    const int ngu = __ldg(a.meta + META_NGU), ndn = __ldg(a.meta + META_NDN);
+    const TicketMap tmap = ticket_map(ngu, ndn, static_cast<int>(gridDim.x));
+    const int ntot = ngu + tmap.ndn_tickets + (kFused ? a.ncb : 0);  // tickets
+    const TaskEntry kEnd = TaskEntry{-1, 0, 0, 0};
+    int stage = 0, issued = 0, n = 0, chunk_seq = 0;
+    uint32_t phase = 0;
+    int cur = blockIdx.x;
+    TaskEntry entry = kEnd, entry2 = kEnd;
+    bool pair = false;  // entry2 is the second down task of the claimed ticket
+    if (lane == 0) {
+      if (cur < ntot) task_of(a, cur, tmap, entry, entry2, pair);
+      else entry = kEnd;
+    }
+    // the tokens of a gate/up task's routed rows, loaded as soon as its entry is known
+    auto load_tokens = [&]() {
+      const int ey = __shfl_sync(0xffffffffu, entry.y, 0), ez = __shfl_sync(0xffffffffu, entry.z, 0);
+      const bool gu = __shfl_sync(0xffffffffu, cur, 0) < ngu;
+      return (gu && lane < (ez & 0xffff)) ? __ldg(a.pos_tok + ey + lane) : 0;
+    };
+    int tok = load_tokens();
+    bool ok = true;
+    while (ok) {
+      const int q = n % kTaskSlots;
+      if (!warp_wait(smem_addr(&sm.task_empty[q]), static_cast<uint32_t>(((n / kTaskSlots) & 1) ^ 1),
+                     &sm.abort_flag, a.status)) {
+        ok = false;
+        break;
+      }
+      const bool live = __shfl_sync(0xffffffffu, cur, 0) < ntot;
+      // publish the entry (and the tokens, whose load may still be in flight) to the other
+      // roles: after the task's first chunk has been issued -- its stage is freed by earlier,
+      // already published tasks -- and before any later chunk may wait on a stage that only
+      // this task's own chunks would free
+      bool published = false;
+      auto publish = [&]() {
+        int tk[kMaxRows];
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r) tk[r] = __shfl_sync(0xffffffffu, tok, r);
+        if (lane == 0) {
+          sm.task[q] = live ? entry : kEnd;
+#pragma unroll
+          for (int r = 0; r < kMaxRows; ++r) sm.task_tok[q][r] = tk[r];
+          mbar_arrive(smem_addr(&sm.task_full[q]));
+          trace_ev(a, 0, tcnt, 1, cur);
+        }
+        published = true;
+      };
+      if (!live) {
+        publish();
+        break;
+      }
+      const int x = __shfl_sync(0xffffffffu, entry.x, 0);
+      const int z = __shfl_sync(0xffffffffu, entry.z, 0);
+      const int s = __shfl_sync(0xffffffffu, entry.w, 0);
+      const int e = x & 0xffff;
+      const bool is_dn = ((z >> 16) & 1) != 0;
+      int rA0, rA1, nck;
+      const CUtensorMap* tm;
+      if (!is_dn) {
+        rA0 = (e - a.e_lo) * 2 * a.F + s * kGuRows;
+        rA1 = rA0 + a.F;
+        tm = &tm_w13;
+        nck = a.d / kChunk;
+      } else {
+        rA0 = (e - a.e_lo) * a.d + s * kDnRows;
+        rA1 = rA0 + 64;
+        tm = &tm_w2;
+        nck = a.F / kChunk;
+      }
+      if (kFused && ((z >> 18) & 1)) nck = 0;  // un-route task: no weights
+      const CUtensorMap* tms = is_dn ? &tm_s2 : &tm_s13;
+      ++n;
+      for (int c = 0; c < nck; ++c) {
+        if (!warp_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, &sm.abort_flag, a.status)) { ok = false; break; }
+        if (lane == 0) {
+          const uint32_t sb = ring0 + stage * kStageA;
+          const uint32_t fa = smem_addr(&sm.full[stage]);
+          mbar_arrive_expect_tx(fa, kStageA);
+          tma_load_2d(sb, tm, c * (kChunk / 2), rA0, fa, pol);
+          tma_load_2d(sb + kCodeBytes / 2, tm, c * (kChunk / 2), rA1, fa, pol);
+          tma_load_2d(sb + kCodeBytes, tms, c * (kChunk / 16), rA0, fa, pol);
+          tma_load_2d(sb + kCodeBytes + kScaleBytes / 2, tms, c * (kChunk / 16), rA1, fa, pol);
+          trace_ev(a, 0, tcnt, 2, chunk_seq);
+        }
+        ++chunk_seq;
+        ++issued;
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (c == 0) publish();
+      }
+      if (!published) publish();  // un-route task (no chunks), or the first wait gave up
+      if (!ok) break;
+      if (__shfl_sync(0xffffffffu, pair ? 1 : 0, 0)) {
+        // the ticket's second down task, right away: no claim, same expert and rows (no tokens)
+        if (lane == 0) {
+          entry = entry2;
+          pair = false;
+        }
+        tok = 0;
+        continue;
+      }
+      // take the next ticket once at most kReserve chunks are in flight (2 among the last
+      // gridDim.x tickets, so that the final tasks go to the CTAs that run dry first)
+      const int reserve = __shfl_sync(0xffffffffu, cur, 0) + static_cast<int>(gridDim.x) >= ntot ? 2 : kReserve;
+      if (issued > reserve) {
+        const int sq = issued - 1 - reserve + kStages;  // the issue that reuses that chunk's stage
+        if (!warp_wait(smem_addr(&sm.empty[sq % kStages]), static_cast<uint32_t>(((sq / kStages) & 1) ^ 1),
+                       &sm.abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+      }
+      if (lane == 0) {
+        cur = static_cast<int>(atomicAdd(a.ticket, 1u)) + static_cast<int>(gridDim.x);
+        if (cur < ntot) task_of(a, cur, tmap, entry, entry2, pair);
+        else entry = kEnd;
+      }
+      tok = load_tokens();
+    }
+    // drain: every copy this warp started has landed before the CTA exits
+    if (lane == 0) {
+      int st = stage;
+      uint32_t ph = phase;
+      for (int i = 0; i < min(issued, kStages); ++i) {
+        if (--st < 0) { st = kStages - 1; ph ^= 1u; }
+        drain_wait(smem_addr(&sm.full[st]), ph);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------- activation producer: hidden rows once, h rows per down task -------------
+    if (lane == 0) mbar_arrive_expect_tx(smem_addr(&sm.x_full), static_cast<uint32_t>(a.T * 2 * a.d));
+    __syncwarp();
+    if (lane < a.T)
+      bulk_copy_g2s(smem_addr(xs + lane * ar.xpitch), a.x16 + static_cast<size_t>(lane) * a.d, 2 * a.d,
+                    smem_addr(&sm.x_full));
+    int n = 0, ndn = 0, unused_tok = 0;
+    while (true) {
+      TaskEntry te;
+      if (!take_task(sm, n++, te, 0, unused_tok, a.status)) break;
+      if (te.x < 0) break;
+      if (kFused && is_unroute(te)) continue;
+      if (((te.z >> 16) & 1) == 0) continue;  // gate/up: its rows are resident
+      const int slot = ndn % ar.hslots;
+      const uint32_t use = static_cast<uint32_t>(ndn / ar.hslots);
+      if (!warp_wait(smem_addr(&sm.h_empty[slot]), (use & 1u) ^ 1u, &sm.abort_flag, a.status)) break;
+      // every gate/up task (one pass, S_gu stripes) of this expert must have published its h rows
+      const int u = (te.x >> 16) & 0xffff, row0 = te.y, rows = te.z & 0xffff;
+      const bool good = warp_wait_counter(a.ready + u, static_cast<uint32_t>(a.S_gu), &sm.abort_flag, a.status,
+                                          kTimeoutCycles);
+      if (!good) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(smem_addr(&sm.h_full[slot]), static_cast<uint32_t>(rows * 2 * a.F));
+        trace_ev(a, 1, tcnt, 3, ndn);
+      }
+      __syncwarp();
+      if (lane < rows)
+        bulk_copy_g2s(smem_addr(hs + slot * ar.slot_bytes + lane * ar.hpitch),
+                      a.hs16 + static_cast<size_t>(row0 + lane) * a.F, 2 * a.F, smem_addr(&sm.h_full[slot]));
+      ++ndn;
+    }
+    // drain: every copy this warp started has landed before the CTA exits
+    if (lane == 0) {
+      drain_wait(smem_addr(&sm.x_full), 0);
+      for (int i = max(0, ndn - ar.hslots); i < ndn; ++i)
+        drain_wait(smem_addr(&sm.h_full[i % ar.hslots]), static_cast<uint32_t>((i / ar.hslots) & 1));
+    }
+  } else if (warp == 2) {
+    // ------------- publisher: release each finished gate/up task's h rows (fused: and each
+    // finished down task's y rows, counted per stripe) -------------
+    int n = 0, pub_n = 0, unused_tok = 0;
+    while (true) {
+      TaskEntry te;
+      if (!take_task(sm, n++, te, 0, unused_tok, a.status)) break;
+      if (te.x < 0) break;
+      if (kFused && is_unroute(te)) continue;
+      const bool dn = ((te.z >> 16) & 1) != 0;
+      if (dn && !kFused) continue;  // down task, un-route in its own kernel: nothing to publish
+      uint32_t* ctr = dn ? a.dn_done + te.w : a.ready + ((te.x >> 16) & 0xffff);
+      const int slot = pub_n % kPubSlots;
+      const uint32_t ph = static_cast<uint32_t>((pub_n / kPubSlots) & 1);
+      ++pub_n;
+      if (!warp_wait(smem_addr(&sm.pub_full[slot]), ph, &sm.abort_flag, a.status)) break;
+      if (lane == 0) {
+        fence_acq_rel_gpu();
+        red_add_relaxed_gpu_u32(ctr, 1u);
+        trace_ev(a, 4, tcnt, 9, pub_n);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ------------- compute warps: dequantise into A fragments, mma.sync, epilogue -------------
+    const int cw = warp - kFirstCompute;  // 0..7
+    const int g = lane >> 2, q = lane & 3;
+    const int fr = frag_row(g);
+    int stage = 0, n = 0, pub_n = 0, ndn = 0;
+    uint32_t phase = 0;
+    bool ok = true, have_x = false;
+    const bool tr = a.trace != nullptr && lane == 0 && (cw == 0 || cw == kComputeWarps - 1);
+    const int trole = cw == 0 ? 2 : 3;
+    while (ok) {
+      TaskEntry te;
+      int tok = 0;
+      if (!take_task(sm, n, te, g, tok, a.status)) break;
+      if (te.x < 0) break;
+      if constexpr (kFused) {
+        if (is_unroute(te)) {
+          ++n;
+          const int t = min(te.y + cw, a.T - 1), c = te.w * kDnRows + 4 * lane;
+          Unroute4Pre u;
+          unroute4_pre(a, t, c, u);
+          // every down task of the stripe has published its y columns
+          const uint32_t dn_per_stripe = static_cast<uint32_t>(__ldg(a.meta + META_NDN) / a.S_dn);
+          if (tr) trace_ev(a, trole, tcnt, 12, n);
+          if (!warp_wait_counter(a.dn_done + te.w, dn_per_stripe, &sm.abort_flag, a.status, kTimeoutCycles)) break;
+          if (tr) trace_ev(a, trole, tcnt, 13, n);
+          if (te.y + cw < a.T) unroute4_post(a, t, c, u);
+          continue;
+        }
+      }
+      if (tr) trace_ev(a, trole, tcnt, 5, (((te.z >> 16) & 1) << 15) | (n & 0x7fff));
+      const int row0 = te.y, rows = te.z & 0xffff, s = te.w;
+      const bool is_dn = ((te.z >> 16) & 1) != 0;
+      const int nck = (is_dn ? a.F : a.d) / kChunk;
+      const bool live = g < rows;
+      const uint8_t* brow;
+      int slot = 0;
+      if (!is_dn) {
+        if (!have_x) {
+          if (!warp_wait(smem_addr(&sm.x_full), 0u, &sm.abort_flag, a.status)) break;
+          have_x = true;
+        }
+        brow = xs + (live ? tok : 0) * ar.xpitch;
+      } else {
+        slot = ndn % ar.hslots;
+        if (!warp_wait(smem_addr(&sm.h_full[slot]), static_cast<uint32_t>((ndn / ar.hslots) & 1), &sm.abort_flag,
+                       a.status))
+          break;
+        brow = hs + slot * ar.slot_bytes + g * ar.hpitch;
+      }
+      // tile rows (0..127) of fragment rows g and g + 8
+      const int lra = is_dn ? 16 * cw + fr : 8 * cw + fr;
+      const int lrb = is_dn ? 16 * cw + 8 + fr : 64 + 8 * cw + fr;
+      float acc[8][4];
+      ok = run_task_chunks(sm, a, stage, phase, acc, lra, lrb, nck, brow, live, q, tr && cw == 0, tcnt);
+      if (!ok) break;
+      if (is_dn) {
+        // the slot's h rows are consumed
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.h_empty[slot]));
+        ++ndn;
+      }
+      if (tr) trace_ev(a, trole, tcnt, 6, n);
+      ++n;
+      // ---- epilogue: fragment rows g / g+8, routed rows 2q, 2q + 1 ----
+      if (!is_dn) {
+        const int nidx = s * kGuRows + 8 * cw + fr;  // element n of h
+        const float sc = a.w13_ts;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int r = 2 * q + cc;
+          if (r < rows)
+            a.hs16[static_cast<size_t>(row0 + r) * a.F + nidx] =
+                h_store_value(silu_mul(acc[0][cc] * sc, acc[0][2 + cc] * sc), a.status);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.pub_full[pub_n % kPubSlots]));
+        ++pub_n;
+      } else {
+        const float sc = a.w2_ts * kHUnscale;
+        const int ra = s * kDnRows + lra, rb = s * kDnRows + lrb;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int r = 2 * q + cc;
+          if (r < rows) {
+            float* yrow = a.y + static_cast<size_t>(row0 + r) * a.d;
+            yrow[ra] = acc[0][cc] * sc;
+            yrow[rb] = acc[0][2 + cc] * sc;
+          }
+        }
+        if constexpr (kFused) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&sm.pub_full[pub_n % kPubSlots]));
+          ++pub_n;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int c2 = 1;
+    trace_ev(a, 5, c2, 11, 0);
+  }
+}
+
+size_t expert_dec_smem_bytes(int T, int d, int F) {
+  const Arena ar = arena_of(T, d, F);
+  return fixed_smem_bytes() + ar.x_bytes + static_cast<size_t>(ar.hslots) * ar.slot_bytes;
+}
+
+bool expert_dec_supports(int T, int d, int F) {
+  return T >= 1 && T <= kMaxRows && expert_mma_supports(d, F) && arena_of(T, d, F).hslots >= 2 &&
+         expert_dec_smem_bytes(T, d, F) <= static_cast<size_t>(kSmemLimit);
+}
+
+cudaError_t launch_expert_dec(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
+                              const CUtensorMap& tm_s13, const CUtensorMap& tm_s2, int num_sms,
+                              cudaStream_t stream) {
+  const size_t smem = expert_dec_smem_bytes(a.T, a.d, a.F);
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const ExpertArgs) =
+      a.ncb > 0 ? expert_dec_kernel<true> : expert_dec_kernel<false>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  return launch_pdl(kern, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, tm_s13, tm_s2, a);
+}
+
+}  // namespace moe

@@ -31,31 +31,22 @@
 // most 6 significant bits), feeds 16 MMAs per 8-row tile with FP32 accumulation, and
 // writes h (FP16) or per-route down outputs (FP32) at the end of the task.  Only the TMA
 // and bulk-copy engines write shared memory, so the consumers need no proxy fences.
-#include "moe_kernels.cuh"
+#include "mma_parts.cuh"
 
 namespace moe {
 
 namespace mk {
 
-constexpr int kChunk = 256;                     // K elements per chunk (128 B of codes per row)
 constexpr int kStagesA = 9;
-constexpr int kCodeBytes = 16384;               // codes: 2 halves x 64 rows x 128 B (SWIZZLE_128B)
-constexpr int kScaleBytes = 2048;               // block scales: 128 rows x 16 B (the chunk's 16 blocks)
-constexpr int kStageA = kCodeBytes + kScaleBytes;
 constexpr int kStagesB = 12;
 constexpr int kTileRows = 8;
 constexpr int kRowPitchB = 2 * kChunk + 16;     // padded FP16 row of one chunk (528 B)
 constexpr int kStageB = kTileRows * kRowPitchB;  // 4224
 constexpr int kMaxTiles = kRowsPerPass / kTileRows;  // 8
-constexpr int kComputeWarps = 8;
-constexpr int kFirstCompute = 3;
-constexpr int kThreads = 32 * (kFirstCompute + kComputeWarps);
-constexpr int kTaskSlots = 8;
 constexpr int kTaskConsumers = 2 + kComputeWarps;  // activation producer, publisher, compute
 // Compute warps run at most kTaskSlots tasks ahead of the publisher (it frees each task
 // slot before waiting on that task), so twice as many publication slots never wrap early.
 constexpr int kPubSlots = 2 * kTaskSlots;
-constexpr long long kTimeoutCycles = 1ll << 33;
 // The producer claims its next task (ticket) only once at most kReserve of its chunks are
 // in flight: late enough that the last tasks go to whichever CTA frees up first, early
 // enough that the ticket and table round trips are hidden behind the chunks still queued.
@@ -74,57 +65,14 @@ struct Smem {
   int abort_flag;
 };
 
-__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
-      *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
-      atomicOr(status, static_cast<int>(MOE_DEV_TIMEOUT));
-      return false;
-    }
-  }
-  return true;
-}
-
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status) {
-  const bool ok = bounded_wait(bar, parity, sm, status);
-  return __all_sync(0xffffffffu, ok);
-}
-
 __device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* status) {
   const int q = n % kTaskSlots;
   const uint32_t ph = static_cast<uint32_t>((n / kTaskSlots) & 1);
-  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, sm, status)) return false;
+  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, &sm.abort_flag, status)) return false;
   out = sm.task[q];
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&sm.task_empty[q]));
   return true;
-}
-
-// Task i of the ticket order: entry i of the plan's table, or, past its ntask entries, one of
-// the a.ncb un-route tasks: stripe c mod S_dn (128 output columns) of the tokens
-// [8 (c / S_dn), +8), one token per compute warp (c = i - ntask).
-__device__ __forceinline__ TaskEntry task_at(const ExpertArgs& a, int i, int ntask) {
-  if (i < ntask) return a.tasks[i];
-  const int c = i - ntask;
-  return TaskEntry{0, kComputeWarps * (c / a.S_dn), 1 << 18, c % a.S_dn};
-}
-
-__device__ __forceinline__ bool is_unroute(const TaskEntry& t) { return ((t.z >> 18) & 1) != 0; }
-
-// Tile row (0..7 within an 8-row group) held by fragment row g: 0, 4, 1, 5, 2, 6, 3, 7.
-__device__ __forceinline__ int frag_row(int g) { return ((g & 1) << 2) | (g >> 1); }
-
-// D += A * B for one m16n8k16 step (FP16 inputs, FP32 accumulators).
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // B fragments of one 8-row activation tile for sub-chunk h: tile row g, elements
@@ -134,49 +82,6 @@ __device__ __forceinline__ void load_b_frag(const uint8_t* tile, int g, int q, i
   const uint8_t* row = tile + g * kRowPitchB + 64 * q + 256 * h;
 #pragma unroll
   for (int j = 0; j < 4; ++j) x[j] = live ? *reinterpret_cast<const uint4*>(row + 16 * j) : make_uint4(0, 0, 0, 0);
-}
-
-// One thread's share of a 256-K chunk: per sub-chunk h the 16 code bytes and the two block
-// scales of its rows a (fragment row g) and b (fragment row g + 8).
-struct ChunkCodes {
-  uint4 ca[2], cb[2];
-  uint32_t sa[2], sb[2];
-};
-
-// codes: sub-chunk h covers K [128h, 128h+128); thread q its elements [32q, 32q+32), i.e.
-// 16-byte piece 4h + q of the 128-byte row, stored at (piece ^ (row & 7)); scales: the
-// chunk's blocks 8h + 2q and 8h + 2q + 1, i.e. bytes 8h + 2q of the row's 16 scale bytes.
-__device__ __forceinline__ void load_chunk_codes(const uint8_t* stage, int lra, int lrb, int q, ChunkCodes& o) {
-  const int ra = lra & 63, rb = lrb & 63;
-  const uint8_t* pa = stage + (lra >> 6) * (kCodeBytes / 2) + ra * 128;
-  const uint8_t* pb = stage + (lrb >> 6) * (kCodeBytes / 2) + rb * 128;
-  const uint8_t* qa = stage + kCodeBytes + lra * 16 + 2 * q;
-  const uint8_t* qb = stage + kCodeBytes + lrb * 16 + 2 * q;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    o.ca[h] = *reinterpret_cast<const uint4*>(pa + (((4 * h + q) ^ (ra & 7)) << 4));
-    o.cb[h] = *reinterpret_cast<const uint4*>(pb + (((4 * h + q) ^ (rb & 7)) << 4));
-    o.sa[h] = *reinterpret_cast<const uint16_t*>(qa + 8 * h);
-    o.sb[h] = *reinterpret_cast<const uint16_t*>(qb + 8 * h);
-  }
-}
-
-// Dequantise 32 elements (16 bytes of codes, two 16-element scale blocks) of one row into
-// 16 FP16x2 registers in fragment order: register 4j + i holds elements (8j + 2i, 8j + 2i + 1).
-__device__ __forceinline__ void dequant32(const uint4 codes, uint32_t scale_pair_bytes, uint32_t (&o)[16]) {
-  const uint32_t s2 = e4m3x2_to_f16x2(scale_pair_bytes);  // (block 0, block 1)
-  const uint32_t sb0 = bcast_lo_half(s2), sb1 = bcast_hi_half(s2);
-  const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t scale = j < 2 ? sb0 : sb1;
-    uint32_t r0, r1, r2, r3;
-    e2m1x8_to_f16x2x4(w[j], r0, r1, r2, r3);
-    o[4 * j + 0] = hmul2_bits(r0, scale);
-    o[4 * j + 1] = hmul2_bits(r1, scale);
-    o[4 * j + 2] = hmul2_bits(r2, scale);
-    o[4 * j + 3] = hmul2_bits(r3, scale);
-  }
 }
 
 // Per-warp pipeline position of the compute warps.
@@ -208,7 +113,7 @@ __device__ __forceinline__ bool run_chunks(Smem& sm, const ExpertArgs& a, Comput
   // then loaded after the release.
   const bool early = MODE != 0 || 2 * nt <= kStagesB;
   ChunkCodes next;
-  if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, sm, a.status)) return false;
+  if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, &sm.abort_flag, a.status)) return false;
   load_chunk_codes(&sm.ring_a[cs.stage_a][0], lra, lrb, q, next);
   for (int c = 0; c < nck; ++c) {
     const ChunkCodes cur = next;
@@ -217,7 +122,7 @@ __device__ __forceinline__ bool run_chunks(Smem& sm, const ExpertArgs& a, Comput
     if (lane == 0) mbar_arrive(smem_addr(&sm.empty_a[cs.stage_a]));
     if (++cs.stage_a == kStagesA) { cs.stage_a = 0; cs.phase_a ^= 1u; }
     if (early && c + 1 < nck) {
-      if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, sm, a.status)) return false;
+      if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, &sm.abort_flag, a.status)) return false;
       load_chunk_codes(&sm.ring_a[cs.stage_a][0], lra, lrb, q, next);
     }
     // Per sub-chunk h: activation fragments first (their latency overlaps the
@@ -299,7 +204,7 @@ __device__ __forceinline__ bool run_chunks(Smem& sm, const ExpertArgs& a, Comput
     cs.stage_b += nt;
     if (cs.stage_b >= kStagesB) cs.stage_b -= kStagesB;
     if (!early && c + 1 < nck) {
-      if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, sm, a.status)) return false;
+      if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, &sm.abort_flag, a.status)) return false;
       load_chunk_codes(&sm.ring_a[cs.stage_a][0], lra, lrb, q, next);
     }
   }
@@ -316,28 +221,6 @@ __device__ __forceinline__ bool run_chunks(Smem& sm, const ExpertArgs& a, Comput
     }
   }
   return true;
-}
-
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
-
-__device__ __forceinline__ __half h_store_value(float h, int* status) {
-  float v = h * kHScale;
-  if (fabsf(v) > 65504.f) {
-    atomicOr(status, static_cast<int>(MOE_DEV_H_SATURATED));
-    v = copysignf(65504.f, v);
-  }
-  return __float2half_rn(v);
-}
-
-__device__ __forceinline__ void trace_ev(const ExpertArgs& a, int role, int& cnt, int code, int idx) {
-  if (a.trace != nullptr && cnt < kTracePerRole) {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    a.trace[(static_cast<size_t>(blockIdx.x) * kTraceRoles + role) * kTracePerRole + cnt] =
-        (static_cast<unsigned long long>(code) << 56) | (static_cast<unsigned long long>(idx & 0xffff) << 40) |
-        (t & 0xffffffffffull);
-    ++cnt;
-  }
 }
 
 }  // namespace mk
@@ -406,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (ok) {
       const int q = n % kTaskSlots;
-      if (!warp_wait(smem_addr(&sm.task_empty[q]), static_cast<uint32_t>(((n / kTaskSlots) & 1) ^ 1), sm,
+      if (!warp_wait(smem_addr(&sm.task_empty[q]), static_cast<uint32_t>(((n / kTaskSlots) & 1) ^ 1), &sm.abort_flag,
                      a.status)) {
         ok = false;
         break;
@@ -440,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* tms = is_dn ? &tm_s2 : &tm_s13;
       ++n;
       for (int c = 0; c < nck; ++c) {
-        if (!warp_wait(smem_addr(&sm.empty_a[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&sm.empty_a[stage]), phase ^ 1u, &sm.abort_flag, a.status)) { ok = false; break; }
         if (lane == 0) {
           const uint32_t sb = ringa0 + stage * kStageA;
           const uint32_t fa = smem_addr(&sm.full_a[stage]);
@@ -461,8 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // claimed shortly before this CTA can start it
       if (issued > kReserve) {
         const int sq = issued - 1 - kReserve + kStagesA;  // the issue that reuses that chunk's stage
-        if (!warp_wait(smem_addr(&sm.empty_a[sq % kStagesA]), static_cast<uint32_t>(((sq / kStagesA) & 1) ^ 1), sm,
-                       a.status)) {
+        if (!warp_wait(smem_addr(&sm.empty_a[sq % kStagesA]), static_cast<uint32_t>(((sq / kStagesA) & 1) ^ 1),
+                       &sm.abort_flag, a.status)) {
           ok = false;
           break;
         }
@@ -520,11 +403,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nt = (rows + kTileRows - 1) / kTileRows;
       for (int c = 0; ok && c < nck; ++c) {
         // the chunk's weight stage must be free before this chunk's bytes are announced on it
-        if (!warp_wait(smem_addr(&sm.empty_a[stage_a]), phase_a ^ 1u, sm, a.status)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&sm.empty_a[stage_a]), phase_a ^ 1u, &sm.abort_flag, a.status)) { ok = false; break; }
         const uint32_t fa = smem_addr(&sm.full_a[stage_a]);
         if (lane == 0) mbar_arrive_expect_tx(fa, static_cast<uint32_t>(rows) * (2 * kChunk));
         for (int t = 0; t < nt; ++t) {
-          if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
+          if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, &sm.abort_flag, a.status)) { ok = false; break; }
           const int trows = min(kTileRows, rows - t * kTileRows);
           // lanes 0..trows-1 copy their tile row: routed row r = 8t + lane
           const int r = t * kTileRows + lane;
@@ -573,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the compute warps' h stores are ordered before their arrivals (warp barrier, then a
       // release arrive); this acquire wait plus a GPU-scope fence makes the reduction below
       // release all of them
-      if (!warp_wait(smem_addr(&sm.pub_full[slot]), ph, sm, a.status)) break;
+      if (!warp_wait(smem_addr(&sm.pub_full[slot]), ph, &sm.abort_flag, a.status)) break;
       if (lane == 0) {
         fence_acq_rel_gpu();
         red_add_relaxed_gpu_u32(ctr, 1u);

@@ -249,9 +249,15 @@ constexpr int kTracePerRole = 128;
 
 // Launch `kernel` as a programmatic dependent of the preceding work in `stream` (it may
 // begin while its predecessor finishes; the kernels order themselves with pdl_wait).
+// Every kernel of the library asks for the largest shared-memory carveout, so that an SM
+// need not be reconfigured between the small front kernels and the expert kernels (which
+// use ~200 KB): a reconfiguration waits for the SM to drain and defeats the early start.
 template <typename... Params, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                        Args&&... args) {
+  cudaError_t ce = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                        static_cast<int>(cudaSharedmemCarveoutMaxShared));
+  if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -285,6 +291,14 @@ size_t expert_wide_smem_bytes();
 cudaError_t launch_combine(const ExpertArgs& a, cudaStream_t stream);
 size_t expert_tc_smem_bytes();
 size_t expert_mma_smem_bytes();
+// The decode kernel for at most eight tokens (expert_dec.cu): hidden rows resident in shared
+// memory, h rows copied once per down task; same task table, counters and outputs as
+// launch_expert_mma, which it replaces where expert_dec_supports holds.
+cudaError_t launch_expert_dec(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
+                              const CUtensorMap& tm_s13, const CUtensorMap& tm_s2, int num_sms,
+                              cudaStream_t stream);
+bool expert_dec_supports(int T, int d, int F);
+size_t expert_dec_smem_bytes(int T, int d, int F);
 // number of un-route tasks the decode kernel appends when it runs the un-route itself
 int expert_mma_unroute_tasks(int T, int S_dn);
 int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes);
