@@ -57,6 +57,28 @@ MOE_API int moe_selftest_expert_trace(const moe_shape* shape, const uint8_t* w13
                                       void* workspace, size_t workspace_bytes,
                                       unsigned long long* trace, moe_stream_t stream);
 
+/* The failure path of the expert kernels' bounded waits, for tests.  After moe_front (or
+ * moe_route_topk + moe_plan + moe_forward_prepare) has left a plan in `workspace`, the down task
+ * number `dn_task` of the table the chosen kernel reads is rewritten to wait for the readiness
+ * counter of a touched-expert index that no gate/up task publishes (U, one past the last
+ * touched expert, which needs U < E); then the expert kernel and the un-route run as
+ * moe_forward_experts(algo) does, with every bounded wait limited to `wait_limit_cycles`
+ * clock cycles (the library's own limit is 2^33).  The wait that cannot be met gives up, the
+ * CTA sets MOE_DEV_TIMEOUT in the workspace status word and stops, its roles drain the copies
+ * they started (tensor memory is released in the tcgen05 kernels), and the other CTAs stop in
+ * turn when they wait for work the stopped CTA had claimed: the launch completes, outputs are
+ * undefined.  The plan must be rebuilt before the workspace is used again (moe_front or
+ * moe_plan).  Blocking: synchronises `stream` to read and rewrite the table entry.
+ *   algo: MOE_ALGO_AUTO, MOE_ALGO_MMA, MOE_ALGO_TCGEN05 or MOE_ALGO_WIDE.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG (no such down task, U == E, algo MOE_ALGO_SIMT, limit
+ * not positive) or another moe_status. */
+MOE_API int moe_selftest_expert_timeout(const moe_shape* shape, const uint8_t* w13_codes,
+                                        const uint8_t* w13_scales, float w13_scale,
+                                        const uint8_t* w2_codes, const uint8_t* w2_scales,
+                                        float w2_scale, const void* residual, void* out,
+                                        void* workspace, size_t workspace_bytes, int algo, int dn_task,
+                                        long long wait_limit_cycles, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

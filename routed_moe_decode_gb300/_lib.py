@@ -73,6 +73,9 @@ SIGNATURES = {
     "moe_read_device_status": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint32), _P]),
     "moe_plan_summary": (_I, [_SP, _P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), _P]),
     "moe_plan_views": (_I, [_SP, _P] + [ctypes.POINTER(ctypes.c_void_p)] * 5),
+    # include/moe_selftest.h
+    "moe_selftest_expert_timeout": (_I, [_SP, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _I, _I,
+                                         ctypes.c_longlong, _P]),
 }
 
 _lock = threading.Lock()
@@ -244,6 +247,16 @@ def forward_experts_expert_range(shape: Shape, e_begin: int, e_end: int, w: dict
         ctypes.byref(shape), int(e_begin), int(e_end), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]),
         float(w["w13_ts"]), _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]), _ptr(residual), _ptr(out),
         ws.ptr, ws.nbytes, int(algo), _stream(stream)))
+
+
+def selftest_expert_timeout(shape: Shape, w: dict, residual, out, ws: Workspace, algo: int, dn_task: int,
+                            wait_limit_cycles: int, stream=None):
+    """Run the expert kernel on the plan in `ws` with one down task made to wait for a readiness
+    counter nobody publishes and every wait limited to `wait_limit_cycles` (include/moe_selftest.h)."""
+    _check("moe_selftest_expert_timeout", lib().moe_selftest_expert_timeout(
+        ctypes.byref(shape), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]), float(w["w13_ts"]), _ptr(w["w2_codes"]),
+        _ptr(w["w2_scales"]), float(w["w2_ts"]), _ptr(residual), _ptr(out), ws.ptr, ws.nbytes, int(algo),
+        int(dn_task), int(wait_limit_cycles), _stream(stream)))
 
 
 def read_status(ws: Workspace, clear: bool = True, stream=None) -> int:

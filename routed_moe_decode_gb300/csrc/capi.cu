@@ -175,6 +175,7 @@ moe::ExpertArgs expert_args(const moe_shape* s, const WsLayout& L, void* ws, con
   a.residual = static_cast<const __nv_bfloat16*>(residual);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.e_lo = r.lo;
+  a.wait_limit = moe::kDefaultWaitLimit;
   return a;
 }
 
@@ -318,7 +319,8 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
                                 float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
                                 const void* residual, void* out, void* workspace, size_t workspace_bytes, int algo,
                                 unsigned long long* trace, moe_stream_t stream, ExpertRange r,
-                                int stages = kStageExperts | kStageUnroute) {
+                                int stages = kStageExperts | kStageUnroute,
+                                long long wait_limit = moe::kDefaultWaitLimit, int poison_dn_task = -1) {
   int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   if (shape->T == 0) return MOE_OK;
@@ -335,6 +337,7 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
   moe::ExpertArgs a = expert_args(shape, L, workspace, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales,
                                   w2_scale, residual, out, r);
   a.trace = trace;
+  a.wait_limit = wait_limit;
   cudaError_t e;
   if (!(stages & kStageExperts)) {
     e = moe::launch_combine(a, stream);
@@ -366,7 +369,30 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
   rc = encode_codes_map(&tm2, w2_codes, static_cast<uint64_t>(shape->ffn) / 2,
                         static_cast<uint64_t>(r.hi - r.lo) * shape->d, box);
   if (rc != MOE_OK) return rc;
+  // self test of the failure path: down task `poison_dn_task` of the table the expert kernel
+  // will read is made to wait for a touched-expert index that no gate/up task publishes
+  auto poison = [&](moe::TaskEntry* table, int meta_ngu_word) -> int {
+    if (poison_dn_task < 0) return MOE_OK;
+    int32_t meta[moe::META_WORDS];
+    cudaError_t pe = cudaMemcpyAsync(meta, static_cast<char*>(workspace) + L.meta, sizeof meta, cudaMemcpyDeviceToHost,
+                                     stream);
+    if (pe == cudaSuccess) pe = cudaStreamSynchronize(stream);
+    if (pe != cudaSuccess) { set_error("self test meta read", pe); return MOE_ERR_CUDA; }
+    const int U = meta[moe::META_U], ngu = meta[meta_ngu_word], ndn = meta[meta_ngu_word + 1];
+    if (poison_dn_task >= ndn || U >= shape->E) return MOE_ERR_INVALID_ARG;
+    moe::TaskEntry t;
+    pe = cudaMemcpyAsync(&t, table + ngu + poison_dn_task, sizeof t, cudaMemcpyDeviceToHost, stream);
+    if (pe == cudaSuccess) pe = cudaStreamSynchronize(stream);
+    if (pe != cudaSuccess) { set_error("self test task read", pe); return MOE_ERR_CUDA; }
+    t.x = (t.x & 0xffff) | (U << 16);
+    pe = cudaMemcpyAsync(table + ngu + poison_dn_task, &t, sizeof t, cudaMemcpyHostToDevice, stream);
+    if (pe == cudaSuccess) pe = cudaStreamSynchronize(stream);
+    if (pe != cudaSuccess) { set_error("self test task write", pe); return MOE_ERR_CUDA; }
+    return MOE_OK;
+  };
   if (use_mma) {
+    rc = poison(at<moe::TaskEntry>(workspace, L.tasks), moe::META_NGU);
+    if (rc != MOE_OK) return rc;
     CUtensorMap ts13, ts2;
     rc = moe::encode_scales_map(&ts13, w13_scales, static_cast<uint32_t>(shape->d / 16),
                                 static_cast<uint64_t>(r.hi - r.lo) * 2 * shape->ffn, 64);
@@ -390,12 +416,16 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     moe::TaskEntry* tasks_w = at<moe::TaskEntry>(workspace, L.tasks_w);
     e = moe::launch_wide_plan(a, tasks_w, stream);
     if (e != cudaSuccess) { set_error("wide plan launch", e); return MOE_ERR_CUDA; }
+    rc = poison(tasks_w, moe::META_WGU);
+    if (rc != MOE_OK) return rc;
     moe::ExpertArgs aw = a;
     aw.tasks = tasks_w;
     aw.task_cap = L.max_tasks_w;
     e = moe::launch_expert_wide(aw, tm13, tm2, di.num_sms, stream);
     if (e != cudaSuccess) { set_error("expert_wide launch", e); return MOE_ERR_CUDA; }
   } else {
+    rc = poison(at<moe::TaskEntry>(workspace, L.tasks), moe::META_NGU);
+    if (rc != MOE_OK) return rc;
     e = moe::launch_expert_tc(a, tm13, tm2, di.num_sms, stream);
     if (e != cudaSuccess) { set_error("expert_tc launch", e); return MOE_ERR_CUDA; }
   }
@@ -467,6 +497,18 @@ int moe_selftest_expert_trace(const moe_shape* shape, const uint8_t* w13_codes, 
   if (rc != MOE_OK) return rc;
   return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
                               workspace, workspace_bytes, MOE_ALGO_AUTO, trace, stream, all_experts(shape));
+}
+
+int moe_selftest_expert_timeout(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
+                                float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+                                const void* residual, void* out, void* workspace, size_t workspace_bytes, int algo,
+                                int dn_task, long long wait_limit_cycles, moe_stream_t stream) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (dn_task < 0 || wait_limit_cycles <= 0 || algo == MOE_ALGO_SIMT) return MOE_ERR_INVALID_ARG;
+  return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
+                              workspace, workspace_bytes, algo, nullptr, stream, all_experts(shape),
+                              kStageExperts | kStageUnroute, wait_limit_cycles, dn_task);
 }
 
 int moe_forward_algo(const moe_shape* shape, const void* hidden, const uint8_t* w13_codes,

@@ -112,10 +112,10 @@ __device__ __forceinline__ void task_of(const ExpertArgs& a, int i, const Ticket
   }
 }
 
-__device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int g, int& tok, int* status) {
+__device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int g, int& tok, int* status, long long limit) {
   const int q = n % kTaskSlots;
   const uint32_t ph = static_cast<uint32_t>((n / kTaskSlots) & 1);
-  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, &sm.abort_flag, status)) return false;
+  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, &sm.abort_flag, status, limit)) return false;
   out = sm.task[q];
   tok = sm.task_tok[q][g & (kMaxRows - 1)];
   __syncwarp();
@@ -162,14 +162,14 @@ __device__ __forceinline__ bool run_task_chunks(Smem& sm, const ExpertArgs& a, i
     const bool two = c + 1 < nck;
     ChunkCodes c0, c1;
     if (tr) trace_ev(a, 2, tcnt, 7, c);
-    ok &= bounded_wait(smem_addr(&sm.full[stage]), phase, &sm.abort_flag, a.status);
+    ok &= bounded_wait(smem_addr(&sm.full[stage]), phase, &sm.abort_flag, a.status, a.wait_limit);
     if (tr) trace_ev(a, 2, tcnt, 8, c);
     load_chunk_codes(&sm.ring[stage][0], lra, lrb, q, c0);
     const int st0 = stage;
     if (++stage == kStages) { stage = 0; phase ^= 1u; }
     int st1 = st0;
     if (two) {
-      ok &= bounded_wait(smem_addr(&sm.full[stage]), phase, &sm.abort_flag, a.status);
+      ok &= bounded_wait(smem_addr(&sm.full[stage]), phase, &sm.abort_flag, a.status, a.wait_limit);
       load_chunk_codes(&sm.ring[stage][0], lra, lrb, q, c1);
       st1 = stage;
       if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -193,7 +193,7 @@ __device__ __forceinline__ bool run_task_chunks(Smem& sm, const ExpertArgs& a, i
 // Bounded wait for the last phase of a barrier this warp's copies complete on (drain).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity) && clock64() - t0 < kTimeoutCycles) {}
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < kDrainCycles) {}
 }
 
 }  // namespace dk
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok) {
       const int q = n % kTaskSlots;
       if (!warp_wait(smem_addr(&sm.task_empty[q]), static_cast<uint32_t>(((n / kTaskSlots) & 1) ^ 1),
-                     &sm.abort_flag, a.status)) {
+                     &sm.abort_flag, a.status, a.wait_limit)) {
         ok = false;
         break;
       }
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* tms = is_dn ? &tm_s2 : &tm_s13;
       ++n;
       for (int c = 0; c < nck; ++c) {
-        if (!warp_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, &sm.abort_flag, a.status)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, &sm.abort_flag, a.status, a.wait_limit)) { ok = false; break; }
         if (lane == 0) {
           const uint32_t sb = ring0 + stage * kStageA;
           const uint32_t fa = smem_addr(&sm.full[stage]);
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (issued > reserve) {
         const int sq = issued - 1 - reserve + kStages;  // the issue that reuses that chunk's stage
         if (!warp_wait(smem_addr(&sm.empty[sq % kStages]), static_cast<uint32_t>(((sq / kStages) & 1) ^ 1),
-                       &sm.abort_flag, a.status)) {
+                       &sm.abort_flag, a.status, a.wait_limit)) {
           ok = false;
           break;
         }
@@ -388,17 +388,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n = 0, ndn = 0, unused_tok = 0;
     while (true) {
       TaskEntry te;
-      if (!take_task(sm, n++, te, 0, unused_tok, a.status)) break;
+      if (!take_task(sm, n++, te, 0, unused_tok, a.status, a.wait_limit)) break;
       if (te.x < 0) break;
       if (kFused && is_unroute(te)) continue;
       if (((te.z >> 16) & 1) == 0) continue;  // gate/up: its rows are resident
       const int slot = ndn % ar.hslots;
       const uint32_t use = static_cast<uint32_t>(ndn / ar.hslots);
-      if (!warp_wait(smem_addr(&sm.h_empty[slot]), (use & 1u) ^ 1u, &sm.abort_flag, a.status)) break;
+      if (!warp_wait(smem_addr(&sm.h_empty[slot]), (use & 1u) ^ 1u, &sm.abort_flag, a.status, a.wait_limit)) break;
       // every gate/up task (one pass, S_gu stripes) of this expert must have published its h rows
       const int u = (te.x >> 16) & 0xffff, row0 = te.y, rows = te.z & 0xffff;
       const bool good = warp_wait_counter(a.ready + u, static_cast<uint32_t>(a.S_gu), &sm.abort_flag, a.status,
-                                          kTimeoutCycles);
+                                          a.wait_limit);
       if (!good) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(smem_addr(&sm.h_full[slot]), static_cast<uint32_t>(rows * 2 * a.F));
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n = 0, pub_n = 0, unused_tok = 0;
     while (true) {
       TaskEntry te;
-      if (!take_task(sm, n++, te, 0, unused_tok, a.status)) break;
+      if (!take_task(sm, n++, te, 0, unused_tok, a.status, a.wait_limit)) break;
       if (te.x < 0) break;
       if (kFused && is_unroute(te)) continue;
       const bool dn = ((te.z >> 16) & 1) != 0;
@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int slot = pub_n % kPubSlots;
       const uint32_t ph = static_cast<uint32_t>((pub_n / kPubSlots) & 1);
       ++pub_n;
-      if (!warp_wait(smem_addr(&sm.pub_full[slot]), ph, &sm.abort_flag, a.status)) break;
+      if (!warp_wait(smem_addr(&sm.pub_full[slot]), ph, &sm.abort_flag, a.status, a.wait_limit)) break;
       if (lane == 0) {
         fence_acq_rel_gpu();
         red_add_relaxed_gpu_u32(ctr, 1u);
@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok) {
       TaskEntry te;
       int tok = 0;
-      if (!take_task(sm, n, te, g, tok, a.status)) break;
+      if (!take_task(sm, n, te, g, tok, a.status, a.wait_limit)) break;
       if (te.x < 0) break;
       if constexpr (kFused) {
         if (is_unroute(te)) {
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // every down task of the stripe has published its y columns
           const uint32_t dn_per_stripe = static_cast<uint32_t>(__ldg(a.meta + META_NDN) / a.S_dn);
           if (tr) trace_ev(a, trole, tcnt, 12, n);
-          if (!warp_wait_counter(a.dn_done + te.w, dn_per_stripe, &sm.abort_flag, a.status, kTimeoutCycles)) break;
+          if (!warp_wait_counter(a.dn_done + te.w, dn_per_stripe, &sm.abort_flag, a.status, a.wait_limit)) break;
           if (tr) trace_ev(a, trole, tcnt, 13, n);
           if (te.y + cw < a.T) unroute4_post(a, t, c, u);
           continue;
@@ -478,14 +478,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int slot = 0;
       if (!is_dn) {
         if (!have_x) {
-          if (!warp_wait(smem_addr(&sm.x_full), 0u, &sm.abort_flag, a.status)) break;
+          if (!warp_wait(smem_addr(&sm.x_full), 0u, &sm.abort_flag, a.status, a.wait_limit)) break;
           have_x = true;
         }
         brow = xs + (live ? tok : 0) * ar.xpitch;
       } else {
         slot = ndn % ar.hslots;
         if (!warp_wait(smem_addr(&sm.h_full[slot]), static_cast<uint32_t>((ndn / ar.hslots) & 1), &sm.abort_flag,
-                       a.status))
+                       a.status, a.wait_limit))
           break;
         brow = hs + slot * ar.slot_bytes + g * ar.hpitch;
       }

@@ -65,10 +65,10 @@ struct Smem {
   int abort_flag;
 };
 
-__device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* status) {
+__device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* status, long long limit) {
   const int q = n % kTaskSlots;
   const uint32_t ph = static_cast<uint32_t>((n / kTaskSlots) & 1);
-  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, &sm.abort_flag, status)) return false;
+  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, &sm.abort_flag, status, limit)) return false;
   out = sm.task[q];
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&sm.task_empty[q]));
@@ -113,7 +113,7 @@ __device__ __forceinline__ bool run_chunks(Smem& sm, const ExpertArgs& a, Comput
   // then loaded after the release.
   const bool early = MODE != 0 || 2 * nt <= kStagesB;
   ChunkCodes next;
-  if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, &sm.abort_flag, a.status)) return false;
+  if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, &sm.abort_flag, a.status, a.wait_limit)) return false;
   load_chunk_codes(&sm.ring_a[cs.stage_a][0], lra, lrb, q, next);
   for (int c = 0; c < nck; ++c) {
     const ChunkCodes cur = next;
@@ -122,7 +122,7 @@ __device__ __forceinline__ bool run_chunks(Smem& sm, const ExpertArgs& a, Comput
     if (lane == 0) mbar_arrive(smem_addr(&sm.empty_a[cs.stage_a]));
     if (++cs.stage_a == kStagesA) { cs.stage_a = 0; cs.phase_a ^= 1u; }
     if (early && c + 1 < nck) {
-      if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, &sm.abort_flag, a.status)) return false;
+      if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, &sm.abort_flag, a.status, a.wait_limit)) return false;
       load_chunk_codes(&sm.ring_a[cs.stage_a][0], lra, lrb, q, next);
     }
     // Per sub-chunk h: activation fragments first (their latency overlaps the
@@ -204,7 +204,7 @@ __device__ __forceinline__ bool run_chunks(Smem& sm, const ExpertArgs& a, Comput
     cs.stage_b += nt;
     if (cs.stage_b >= kStagesB) cs.stage_b -= kStagesB;
     if (!early && c + 1 < nck) {
-      if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, &sm.abort_flag, a.status)) return false;
+      if (!warp_wait(smem_addr(&sm.full_a[cs.stage_a]), cs.phase_a, &sm.abort_flag, a.status, a.wait_limit)) return false;
       load_chunk_codes(&sm.ring_a[cs.stage_a][0], lra, lrb, q, next);
     }
   }
@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok) {
       const int q = n % kTaskSlots;
       if (!warp_wait(smem_addr(&sm.task_empty[q]), static_cast<uint32_t>(((n / kTaskSlots) & 1) ^ 1), &sm.abort_flag,
-                     a.status)) {
+                     a.status, a.wait_limit)) {
         ok = false;
         break;
       }
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* tms = is_dn ? &tm_s2 : &tm_s13;
       ++n;
       for (int c = 0; c < nck; ++c) {
-        if (!warp_wait(smem_addr(&sm.empty_a[stage]), phase ^ 1u, &sm.abort_flag, a.status)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&sm.empty_a[stage]), phase ^ 1u, &sm.abort_flag, a.status, a.wait_limit)) { ok = false; break; }
         if (lane == 0) {
           const uint32_t sb = ringa0 + stage * kStageA;
           const uint32_t fa = smem_addr(&sm.full_a[stage]);
@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (issued > kReserve) {
         const int sq = issued - 1 - kReserve + kStagesA;  // the issue that reuses that chunk's stage
         if (!warp_wait(smem_addr(&sm.empty_a[sq % kStagesA]), static_cast<uint32_t>(((sq / kStagesA) & 1) ^ 1),
-                       &sm.abort_flag, a.status)) {
+                       &sm.abort_flag, a.status, a.wait_limit)) {
           ok = false;
           break;
         }
@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < min(issued, kStagesA); ++i) {
         if (--st < 0) { st = kStagesA - 1; ph ^= 1u; }
         const long long t0 = clock64();
-        while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kTimeoutCycles) {}
+        while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kDrainCycles) {}
       }
     }
   } else if (warp == 1) {
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (ok) {
       TaskEntry te;
-      if (!take_task(sm, n++, te, a.status)) break;
+      if (!take_task(sm, n++, te, a.status, a.wait_limit)) break;
       if (te.x < 0) break;
       if (kFused && is_unroute(te)) continue;
       const int e = te.x & 0xffff, u = (te.x >> 16) & 0xffff, row0 = te.y, rows = te.z & 0xffff;
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every gate/up task of every stripe (all passes) of this expert must have published
         const int npass = (__ldg(a.counts + e) + kRowsPerPass - 1) / kRowsPerPass;
         const uint32_t target = static_cast<uint32_t>(npass * a.S_gu);
-        const bool good = warp_wait_counter(a.ready + u, target, &sm.abort_flag, a.status, kTimeoutCycles);
+        const bool good = warp_wait_counter(a.ready + u, target, &sm.abort_flag, a.status, a.wait_limit);
         if (lane == 0) trace_ev(a, 1, tcnt, 3, n);
         if (!good) break;
       }
@@ -403,11 +403,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nt = (rows + kTileRows - 1) / kTileRows;
       for (int c = 0; ok && c < nck; ++c) {
         // the chunk's weight stage must be free before this chunk's bytes are announced on it
-        if (!warp_wait(smem_addr(&sm.empty_a[stage_a]), phase_a ^ 1u, &sm.abort_flag, a.status)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&sm.empty_a[stage_a]), phase_a ^ 1u, &sm.abort_flag, a.status, a.wait_limit)) { ok = false; break; }
         const uint32_t fa = smem_addr(&sm.full_a[stage_a]);
         if (lane == 0) mbar_arrive_expect_tx(fa, static_cast<uint32_t>(rows) * (2 * kChunk));
         for (int t = 0; t < nt; ++t) {
-          if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, &sm.abort_flag, a.status)) { ok = false; break; }
+          if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, &sm.abort_flag, a.status, a.wait_limit)) { ok = false; break; }
           const int trows = min(kTileRows, rows - t * kTileRows);
           // lanes 0..trows-1 copy their tile row: routed row r = 8t + lane
           const int r = t * kTileRows + lane;
@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < min(chunk_seq, kStagesA); ++i) {
         if (--st < 0) { st = kStagesA - 1; ph ^= 1u; }
         const long long t0 = clock64();
-        while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kTimeoutCycles) {}
+        while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kDrainCycles) {}
       }
     }
     (void)issued;
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n = 0, gu_n = 0;
     while (true) {
       TaskEntry te;
-      if (!take_task(sm, n++, te, a.status)) break;
+      if (!take_task(sm, n++, te, a.status, a.wait_limit)) break;
       if (te.x < 0) break;
       if (kFused && is_unroute(te)) continue;
       const bool dn = ((te.z >> 16) & 1) != 0;
@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the compute warps' h stores are ordered before their arrivals (warp barrier, then a
       // release arrive); this acquire wait plus a GPU-scope fence makes the reduction below
       // release all of them
-      if (!warp_wait(smem_addr(&sm.pub_full[slot]), ph, &sm.abort_flag, a.status)) break;
+      if (!warp_wait(smem_addr(&sm.pub_full[slot]), ph, &sm.abort_flag, a.status, a.wait_limit)) break;
       if (lane == 0) {
         fence_acq_rel_gpu();
         red_add_relaxed_gpu_u32(ctr, 1u);
@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int trole = cw == 0 ? 2 : 3;
     while (ok) {
       TaskEntry te;
-      if (!take_task(sm, n, te, a.status)) break;
+      if (!take_task(sm, n, te, a.status, a.wait_limit)) break;
       if (te.x < 0) break;
       if constexpr (kFused) {
         if (is_unroute(te)) {
@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // every down task of the stripe (one per pass) has published its y columns
           const uint32_t dn_per_stripe = static_cast<uint32_t>(__ldg(a.meta + META_NDN) / a.S_dn);
           if (tr) trace_ev(a, trole, tcnt, 12, n);
-          if (!warp_wait_counter(a.dn_done + te.w, dn_per_stripe, &sm.abort_flag, a.status, kTimeoutCycles)) break;
+          if (!warp_wait_counter(a.dn_done + te.w, dn_per_stripe, &sm.abort_flag, a.status, a.wait_limit)) break;
           if (tr) trace_ev(a, trole, tcnt, 13, n);
           if (te.y + cw < a.T) unroute4_post(a, t, c, u);
           continue;

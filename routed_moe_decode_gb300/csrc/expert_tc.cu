@@ -49,7 +49,9 @@ constexpr int kTmemCols = 512;
 constexpr int kTaskSlots = 8;
 constexpr int kTaskConsumers = 10;  // activation producer, 4 dequant warps, MMA, 4 epilogue warps
 constexpr int kThreads = 352;
-constexpr long long kTimeoutCycles = 1ll << 33;  // ~4 s at 2 GHz
+// Bound of the drain waits at exit (copies and MMAs already issued complete within
+// microseconds; after an abort a barrier may lack the arrival of a role that gave up).
+constexpr long long kDrainCycles = 1ll << 24;
 
 struct Smem {
   uint8_t ring_b[kStagesB][kStageB];
@@ -91,12 +93,13 @@ __device__ __forceinline__ Task unpack(const TaskEntry& t, const ExpertArgs& a) 
   return k;
 }
 
-__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status) {
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status,
+                                             long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
+    if (clock64() - t0 > limit) {
       *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
       atomicOr(status, static_cast<int>(MOE_DEV_TIMEOUT));
       return false;
@@ -107,17 +110,17 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Smem
 
 // Every lane waits; the warp then agrees on the outcome, so that no lane runs a
 // warp-collective (.sync.aligned) instruction that another lane has abandoned.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status) {
-  const bool ok = bounded_wait(bar, parity, sm, status);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status, long long limit) {
+  const bool ok = bounded_wait(bar, parity, sm, status, limit);
   return __all_sync(0xffffffffu, ok);
 }
 
 // Task-ring consumer: wait for slot n, copy the entry, release the slot (one arrival per
 // consuming warp, made by lane 0 after the warp has the entry).
-__device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* status) {
+__device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* status, long long limit) {
   const int q = n % kTaskSlots;
   const uint32_t ph = static_cast<uint32_t>((n / kTaskSlots) & 1);
-  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, sm, status)) return false;
+  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, sm, status, limit)) return false;
   out = sm.task[q];
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&sm.task_empty[q]));
@@ -227,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // publish the current task (or the end-of-work sentinel) to the consumers
       const int q = n % kTaskSlots;
       if (!warp_wait(smem_addr(&sm.task_empty[q]), static_cast<uint32_t>(((n / kTaskSlots) & 1) ^ 1), sm,
-                     a.status)) {
+                     a.status, a.wait_limit)) {
         ok = false;
         break;
       }
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         nck = a.nck_dn;
       }
       for (int c = 0; c < nck; ++c) {
-        if (!warp_wait(smem_addr(&sm.empty_a[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&sm.empty_a[stage]), phase ^ 1u, sm, a.status, a.wait_limit)) { ok = false; break; }
         const int kb = c * kChunkK;
         const uint32_t sb = ringa0 + stage * kStageA;
         const uint32_t fa = smem_addr(&sm.full_a[stage]);
@@ -302,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < min(issued, kStagesA); ++i) {
         if (--st < 0) { st = kStagesA - 1; ph ^= 1u; }
         const long long t0 = clock64();
-        while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kTimeoutCycles) {}
+        while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kDrainCycles) {}
       }
     }
   } else if (warp == 9) {
@@ -312,14 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (ok) {
       TaskEntry te;
-      if (!take_task(sm, n++, te, a.status)) break;
+      if (!take_task(sm, n++, te, a.status, a.wait_limit)) break;
       const Task tk = unpack(te, a);
       if (!tk.valid) break;
       if (tk.is_dn) {
         // every gate/up stripe of this expert (all passes) must have published its h rows
         const int npass = (__ldg(a.counts + tk.e) + kRowsPerPass - 1) / kRowsPerPass;
         const uint32_t target = static_cast<uint32_t>(npass * a.S_gu);
-        const bool good = warp_wait_counter(a.ready + tk.u, target, &sm.abort_flag, a.status, kTimeoutCycles);
+        const bool good = warp_wait_counter(a.ready + tk.u, target, &sm.abort_flag, a.status, a.wait_limit);
         if (lane == 0) trace_ev(a, 1, tcnt, 3, n);
         if (!good) break;
       }
@@ -341,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; ok && c < tk.nck; ++c) {
         const int kb = c * kChunkK;
         for (int grp = 0; grp < G; ++grp) {
-          if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
+          if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, sm, a.status, a.wait_limit)) { ok = false; break; }
           const uint32_t bbase = ringb0 + stage * kStageB;
           const int rend = min(tk.rows, (grp + 1) * kGroupRows);
           for (int r0 = grp * kGroupRows; r0 < rend; r0 += 2) {
@@ -376,11 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (ok) {
       TaskEntry te;
-      if (!take_task(sm, n++, te, a.status)) break;
+      if (!take_task(sm, n++, te, a.status, a.wait_limit)) break;
       const Task tk = unpack(te, a);
       if (!tk.valid) break;
       for (int c = 0; c < tk.nck; ++c) {
-        if (!warp_wait(smem_addr(&sm.full_a[stage]), phase, sm, a.status)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&sm.full_a[stage]), phase, sm, a.status, a.wait_limit)) { ok = false; break; }
         if (warp == 4 && lane == 0) trace_ev(a, 2, tcnt, 5, chunk_seq);
         const uint8_t* st = &sm.ring_a[stage][0];
         const uint8_t* crow = st + half * (kStageCodes / 2) + r * 64;
@@ -413,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the weight stage is consumed (its bytes are in registers): hand it back
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.empty_a[stage]));
-        if (!warp_wait(smem_addr(&sm.a_empty[abuf]), aphase ^ 1u, sm, a.status)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&sm.a_empty[abuf]), aphase ^ 1u, sm, a.status, a.wait_limit)) { ok = false; break; }
         if (warp == 4 && lane == 0) trace_ev(a, 7, tcnt2, 15, chunk_seq);
         tc_fence_after();
         tmem_st_x64(tmem + lane_base + abuf * 64, v);
@@ -435,22 +438,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (ok) {
       TaskEntry te;
-      if (!take_task(sm, n++, te, a.status)) break;
+      if (!take_task(sm, n++, te, a.status, a.wait_limit)) break;
       const Task tk = unpack(te, a);
       if (!tk.valid) break;
       if (lane == 0) {
         const int G = (tk.rows + kGroupRows - 1) / kGroupRows;
-        if (!bounded_wait(smem_addr(&sm.d_empty[dbuf]), dphase ^ 1u, sm, a.status)) ok = false;
+        if (!bounded_wait(smem_addr(&sm.d_empty[dbuf]), dphase ^ 1u, sm, a.status, a.wait_limit)) ok = false;
         tc_fence_after();
         const uint32_t dcol = tmem + kDCol0 + dbuf * 64;
         for (int c = 0; ok && c < tk.nck; ++c) {
-          if (!bounded_wait(smem_addr(&sm.a_full[abuf]), aphase, sm, a.status)) { ok = false; break; }
+          if (!bounded_wait(smem_addr(&sm.a_full[abuf]), aphase, sm, a.status, a.wait_limit)) { ok = false; break; }
           trace_ev(a, 6, tcnt, 12, chunk_seq);
           tc_fence_after();
           for (int g = 0; ok && g < G; ++g) {
             const int bst = (stage + g) % kStagesB;
             const uint32_t bph = phase ^ static_cast<uint32_t>((stage + g) >= kStagesB ? 1 : 0);
-            if (!bounded_wait(smem_addr(&sm.full_b[bst]), bph, sm, a.status)) { ok = false; break; }
+            if (!bounded_wait(smem_addr(&sm.full_b[bst]), bph, sm, a.status, a.wait_limit)) { ok = false; break; }
             tc_fence_after();
             fence_proxy_async_smem();
             if (g == 0) trace_ev(a, 6, tcnt, 13, chunk_seq);
@@ -481,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every issued MMA completes before tensor memory is released
       tc_commit(smem_addr(&sm.drain));
       const long long t0 = clock64();
-      while (!mbar_try_wait(smem_addr(&sm.drain), 0) && clock64() - t0 < kTimeoutCycles) {}
+      while (!mbar_try_wait(smem_addr(&sm.drain), 0) && clock64() - t0 < kDrainCycles) {}
     }
     __syncwarp();
   } else {
@@ -492,12 +495,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t dphase = 0;
     while (true) {
       TaskEntry te;
-      const bool got_task = take_task(sm, n++, te, a.status);
+      const bool got_task = take_task(sm, n++, te, a.status, a.wait_limit);
       if (!named_bar_and(2, 128, got_task)) break;
       const Task tk = unpack(te, a);
       if (!tk.valid) break;
       const int G = (tk.rows + kGroupRows - 1) / kGroupRows;
-      const bool got = warp_wait(smem_addr(&sm.d_full[dbuf]), dphase, sm, a.status);
+      const bool got = warp_wait(smem_addr(&sm.d_full[dbuf]), dphase, sm, a.status, a.wait_limit);
       if (!named_bar_and(2, 128, got)) break;
       if (tid == 0) trace_ev(a, 4, tcnt, 8, n);
       tc_fence_after();

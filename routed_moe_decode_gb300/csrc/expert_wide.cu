@@ -50,7 +50,9 @@ constexpr int kWarpAct0 = kWarpFetch + 1;                      // 13-16
 constexpr int kWarpMma = kWarpAct0 + kActWarps;                // 17
 constexpr int kThreads = 32 * (kWarpMma + 1);                  // 576
 constexpr int kTaskConsumers = kActWarps + 4 + 1 + kEpiWarps;  // activation, dequant, MMA, epilogue warps
-constexpr long long kTimeoutCycles = 1ll << 33;
+// Bound of the drain waits at exit (copies and MMAs already issued complete within
+// microseconds; after an abort a barrier may lack the arrival of a role that gave up).
+constexpr long long kDrainCycles = 1ll << 24;
 
 static_assert(kDCol0 + kNumD * kWideRows <= kTmemCols, "tensor memory budget");
 static_assert(kWideRows % 16 == 0 && kWideRows <= 256, "MMA N limit");
@@ -96,12 +98,13 @@ __device__ __forceinline__ Task unpack(const TaskEntry& t, const ExpertArgs& a) 
   return k;
 }
 
-__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status) {
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status,
+                                             long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
+    if (clock64() - t0 > limit) {
       *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
       atomicOr(status, static_cast<int>(MOE_DEV_TIMEOUT));
       return false;
@@ -110,15 +113,15 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Smem
   return true;
 }
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status) {
-  const bool ok = bounded_wait(bar, parity, sm, status);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Smem& sm, int* status, long long limit) {
+  const bool ok = bounded_wait(bar, parity, sm, status, limit);
   return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* status) {
+__device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* status, long long limit) {
   const int q = n % kTaskSlots;
   const uint32_t ph = static_cast<uint32_t>((n / kTaskSlots) & 1);
-  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, sm, status)) return false;
+  if (!warp_wait(smem_addr(&sm.task_full[q]), ph, sm, status, limit)) return false;
   out = sm.task[q];
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&sm.task_empty[q]));
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok) {
       const int q = n % kTaskSlots;
       if (!warp_wait(smem_addr(&sm.task_empty[q]), static_cast<uint32_t>(((n / kTaskSlots) & 1) ^ 1), sm,
-                     a.status)) {
+                     a.status, a.wait_limit)) {
         ok = false;
         break;
       }
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* sbase = is_dn ? a.w2_scales : a.w13_scales;
       const int nck = is_dn ? a.nck_dn : a.nck_gu;
       for (int c = 0; c < nck; ++c) {
-        if (!warp_wait(smem_addr(&sm.empty_a[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&sm.empty_a[stage]), phase ^ 1u, sm, a.status, a.wait_limit)) { ok = false; break; }
         const int kb = c * kChunkK;
         const uint32_t sb = ringa0 + stage * kStageA;
         const uint32_t fa = smem_addr(&sm.full_a[stage]);
@@ -334,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < min(issued, kStagesA); ++i) {
         if (--st < 0) { st = kStagesA - 1; ph ^= 1u; }
         const long long t0 = clock64();
-        while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kTimeoutCycles) {}
+        while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kDrainCycles) {}
       }
     }
   } else if (warp >= kWarpAct0 && warp < kWarpAct0 + kActWarps) {
@@ -353,14 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (ok) {
       TaskEntry te;
-      if (!take_task(sm, n++, te, a.status)) break;
+      if (!take_task(sm, n++, te, a.status, a.wait_limit)) break;
       const Task tk = unpack(te, a);
       if (!tk.valid) break;
       if (tk.is_dn) {
         // every gate/up stripe of this expert (all passes) has published its h rows
         const int npass = (__ldg(a.counts + tk.e) + kWideRows - 1) / kWideRows;
         const uint32_t target = static_cast<uint32_t>(npass * a.S_gu);
-        if (!warp_wait_counter(a.ready + tk.u, target, &sm.abort_flag, a.status, kTimeoutCycles)) break;
+        if (!warp_wait_counter(a.ready + tk.u, target, &sm.abort_flag, a.status, a.wait_limit)) break;
       }
       for (int idx = lane; idx < kWideRows / kActWarps; idx += 32) {
         const int r = (idx >> 1) * 8 + 2 * aw + (idx & 1);
@@ -375,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint4* src_base = reinterpret_cast<const uint4*>(tk.is_dn ? a.hs16 : a.x16);
       const int ngroups = (tk.rows + 7) / 8;
       for (int c = 0; ok && c < tk.nck; ++c) {
-        if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, sm, a.status)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, sm, a.status, a.wait_limit)) { ok = false; break; }
         const uint32_t bbase = ringb0 + stage * kStageB + atom * kAtomB + rsub * 128 + ((ch ^ rsub) << 4);
         const uint32_t kb16 = static_cast<uint32_t>(c * (kChunkK / 8) + gi);  // 16-byte units
         // eight row groups per batch: the offsets are read first, then the copies issued
@@ -403,11 +406,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (ok) {
       TaskEntry te;
-      if (!take_task(sm, n++, te, a.status)) break;
+      if (!take_task(sm, n++, te, a.status, a.wait_limit)) break;
       const Task tk = unpack(te, a);
       if (!tk.valid) break;
       for (int c = 0; c < tk.nck; ++c) {
-        if (!warp_wait(smem_addr(&sm.full_a[stage]), phase, sm, a.status)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&sm.full_a[stage]), phase, sm, a.status, a.wait_limit)) { ok = false; break; }
         const uint8_t* st = &sm.ring_a[stage][0];
         const uint8_t* crow = st + half * (kStageCodes / 2) + r * 64;
         uint4 q[4];
@@ -436,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the weight stage is consumed (its bytes are in registers): hand it back
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.empty_a[stage]));
-        if (!warp_wait(smem_addr(&sm.a_empty[abuf]), aphase ^ 1u, sm, a.status)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&sm.a_empty[abuf]), aphase ^ 1u, sm, a.status, a.wait_limit)) { ok = false; break; }
         tc_fence_after();
         tmem_st_x64(tmem + lane_base + abuf * 64, v);
         tc_wait_st();
@@ -454,17 +457,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (ok) {
       TaskEntry te;
-      if (!take_task(sm, n++, te, a.status)) break;
+      if (!take_task(sm, n++, te, a.status, a.wait_limit)) break;
       const Task tk = unpack(te, a);
       if (!tk.valid) break;
       if (lane == 0) {
         const uint32_t idesc = idesc_f16_f32(128, mma_n(tk.rows));
-        if (!bounded_wait(smem_addr(&sm.d_empty[dbuf]), dphase ^ 1u, sm, a.status)) ok = false;
+        if (!bounded_wait(smem_addr(&sm.d_empty[dbuf]), dphase ^ 1u, sm, a.status, a.wait_limit)) ok = false;
         tc_fence_after();
         const uint32_t dcol = tmem + kDCol0 + dbuf * kWideRows;
         for (int c = 0; ok && c < tk.nck; ++c) {
-          if (!bounded_wait(smem_addr(&sm.a_full[abuf]), aphase, sm, a.status)) { ok = false; break; }
-          if (!bounded_wait(smem_addr(&sm.full_b[stage]), phase, sm, a.status)) { ok = false; break; }
+          if (!bounded_wait(smem_addr(&sm.a_full[abuf]), aphase, sm, a.status, a.wait_limit)) { ok = false; break; }
+          if (!bounded_wait(smem_addr(&sm.full_b[stage]), phase, sm, a.status, a.wait_limit)) { ok = false; break; }
           tc_fence_after();
           fence_proxy_async_smem();
           const uint32_t bbase = ringb0 + stage * kStageB;
@@ -487,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every issued MMA completes before tensor memory is released
       tc_commit(smem_addr(&sm.drain));
       const long long t0 = clock64();
-      while (!mbar_try_wait(smem_addr(&sm.drain), 0) && clock64() - t0 < kTimeoutCycles) {}
+      while (!mbar_try_wait(smem_addr(&sm.drain), 0) && clock64() - t0 < kDrainCycles) {}
     }
     __syncwarp();
   } else {
@@ -500,11 +503,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t dphase = 0;
     while (true) {
       TaskEntry te;
-      const bool got_task = take_task(sm, n++, te, a.status);
+      const bool got_task = take_task(sm, n++, te, a.status, a.wait_limit);
       if (!named_bar_and(2, 32 * kEpiWarps, got_task)) break;
       const Task tk = unpack(te, a);
       if (!tk.valid) break;
-      const bool got = warp_wait(smem_addr(&sm.d_full[dbuf]), dphase, sm, a.status);
+      const bool got = warp_wait(smem_addr(&sm.d_full[dbuf]), dphase, sm, a.status, a.wait_limit);
       if (!named_bar_and(2, 32 * kEpiWarps, got)) break;
       tc_fence_after();
       const uint32_t dcol = tmem + lane_base + kDCol0 + dbuf * kWideRows;

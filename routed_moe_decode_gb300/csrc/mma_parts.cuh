@@ -16,16 +16,20 @@ constexpr int kComputeWarps = 8;
 constexpr int kFirstCompute = 3;
 constexpr int kThreads = 32 * (kFirstCompute + kComputeWarps);
 constexpr int kTaskSlots = 8;
-constexpr long long kTimeoutCycles = 1ll << 33;
+// Bound of the drain waits at exit: copies already issued land within microseconds, but after
+// an abort a stage's barrier may lack the arrival of a role that gave up, so the drain waits
+// this long (~8 ms) at most per barrier rather than for a completion that may never come.
+constexpr long long kDrainCycles = 1ll << 24;
 
-// Wait for phase `parity` of mbarrier `bar`, giving up after kTimeoutCycles (sets *abort_flag
+// Wait for phase `parity` of mbarrier `bar`, giving up after `limit` cycles (sets *abort_flag
 // and MOE_DEV_TIMEOUT) or as soon as another role of the CTA has raised *abort_flag.
-__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, int* abort_flag, int* status) {
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, int* abort_flag, int* status,
+                                             long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
+    if (clock64() - t0 > limit) {
       *reinterpret_cast<volatile int*>(abort_flag) = 1;
       atomicOr(status, static_cast<int>(MOE_DEV_TIMEOUT));
       return false;
@@ -35,8 +39,9 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, int*
 }
 
 // bounded_wait by every lane of a warp, one decision for the warp.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* abort_flag, int* status) {
-  const bool ok = bounded_wait(bar, parity, abort_flag, status);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* abort_flag, int* status,
+                                          long long limit) {
+  const bool ok = bounded_wait(bar, parity, abort_flag, status, limit);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -29,6 +29,7 @@ constexpr int kGroupRows = 16;      // MMA N per group
 constexpr int kMaxGroups = kRowsPerPass / kGroupRows;
 constexpr int kWideRows = 192;      // routed rows per pass of the wide (many-rows) kernel
 constexpr int kPlanSlice = 4096;    // routes per CTA of the multi-CTA plan (many routes)
+constexpr long long kDefaultWaitLimit = 1ll << 33;  // clock cycles (~4 s at 2 GHz) before a wait gives up
 constexpr float kHScale = 0.0625f;  // h is stored as FP16(h * 2^-4)
 constexpr float kHUnscale = 16.0f;
 

@@ -77,6 +77,9 @@ struct ExpertArgs {
   int e_lo;  // first expert of the weight tensors passed in (expert e's weights are entry e - e_lo)
   int ncb;  // un-route tasks appended to the task order (0: the un-route runs as its own kernel)
   int task_cap;  // entries the task table has room for
+  // every bounded wait of the expert kernels gives up after this many clock cycles
+  // (kDefaultWaitLimit; the self tests shorten it to exercise the failure path)
+  long long wait_limit;
   // optional timeline (diagnostics, off when null): per CTA kTraceRoles x kTracePerRole
   // uint64 events = event code << 56 | index << 40 | %globaltimer low 40 bits
   unsigned long long* trace;
