@@ -136,11 +136,13 @@ int route_topk(int T, int E, int k, const float* logits, int32_t* ids, Acc* weig
 //   h_n = silu(g_n) * u_n,        silu(z) = z / (1 + exp(-z))
 //   y_r = sum_n h_n W2[e][r][n]                                         (r < d)
 //   out[t][r] = residual[t][r] + sum_{j=0..k-1} w_{t,j} y_{t,j,r}
+// The FP32 tensor scale of each weight tensor is either one value for all experts or, when
+// the per-expert array is given, entry e for expert e (one scale per expert's W13 and W2).
 template <typename Acc>
 int moe_experts(int T, int d, int F, int E, int k, const uint16_t* hidden, const int32_t* ids,
                 const Acc* weights, const uint8_t* w13c, const uint8_t* w13s, float w13_ts,
                 const uint8_t* w2c, const uint8_t* w2s, float w2_ts, const uint16_t* residual,
-                const uint8_t* mask, Acc* out) {
+                const uint8_t* mask, Acc* out, const float* w13_ts_e = nullptr, const float* w2_ts_e = nullptr) {
   if (T < 0 || d <= 0 || F <= 0 || E <= 0 || k <= 0 || k > E || d % 16 || F % 16) return -1;
   const DecodeTables& tb = tables();
   const size_t d2 = static_cast<size_t>(d) / 2, d16 = static_cast<size_t>(d) / 16;
@@ -153,12 +155,14 @@ int moe_experts(int T, int d, int F, int E, int k, const uint16_t* hidden, const
     for (int j = 0; j < k; ++j) {
       const int e = ids[static_cast<size_t>(t) * k + j];
       if (e < 0 || e >= E) return -1;
+      const float ts13 = w13_ts_e ? w13_ts_e[e] : w13_ts;
+      const float ts2 = w2_ts_e ? w2_ts_e[e] : w2_ts;
       for (int n = 0; n < F; ++n) {
         const size_t rg = static_cast<size_t>(e) * 2 * F + n;      // gate row
         const size_t ru = static_cast<size_t>(e) * 2 * F + F + n;  // up row
         Acc sg = 0, su = 0;
-        for (int c = 0; c < d; ++c) sg += x[c] * nvfp4_weight<Acc>(tb, w13c + rg * d2, w13s + rg * d16, w13_ts, c);
-        for (int c = 0; c < d; ++c) su += x[c] * nvfp4_weight<Acc>(tb, w13c + ru * d2, w13s + ru * d16, w13_ts, c);
+        for (int c = 0; c < d; ++c) sg += x[c] * nvfp4_weight<Acc>(tb, w13c + rg * d2, w13s + rg * d16, ts13, c);
+        for (int c = 0; c < d; ++c) su += x[c] * nvfp4_weight<Acc>(tb, w13c + ru * d2, w13s + ru * d16, ts13, c);
         g[n] = sg;
         u[n] = su;
       }
@@ -166,7 +170,7 @@ int moe_experts(int T, int d, int F, int E, int k, const uint16_t* hidden, const
       for (int r = 0; r < d; ++r) {
         const size_t rr = static_cast<size_t>(e) * d + r;
         Acc s = 0;
-        for (int n = 0; n < F; ++n) s += h[n] * nvfp4_weight<Acc>(tb, w2c + rr * f2, w2s + rr * f16, w2_ts, n);
+        for (int n = 0; n < F; ++n) s += h[n] * nvfp4_weight<Acc>(tb, w2c + rr * f2, w2s + rr * f16, ts2, n);
         y[r] = s;
       }
       const Acc wj = weights[static_cast<size_t>(t) * k + j];
@@ -180,9 +184,110 @@ int moe_experts(int T, int d, int F, int E, int k, const uint16_t* hidden, const
   return 0;
 }
 
+// BF16 of a binary32 value, round to nearest, ties to even (the rounding a BF16 store of a
+// float performs); NaN stays NaN (quiet), infinities and zeros keep their sign.
+uint16_t bf16_round(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return static_cast<uint16_t>((u >> 16) | 0x0040u);
+  const uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7fffu + lsb;
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// Router projection ("Router: selection and expert-task production": the projection whose
+// results feed selection): logits[t][e] = sum_c x[t][c] * Wr[e][c] with the BF16 hidden row
+// and the BF16 router weight row, in the accumulation type, ascending c.
+template <typename Acc>
+int router_logits(int T, int d, int E, const uint16_t* hidden, const uint16_t* wr, Acc* logits) {
+  if (T < 0 || d <= 0 || E <= 0) return -1;
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < E; ++e) {
+      Acc s = 0;
+      for (int c = 0; c < d; ++c)
+        s += static_cast<Acc>(bf16_to_float(hidden[static_cast<size_t>(t) * d + c])) *
+             static_cast<Acc>(bf16_to_float(wr[static_cast<size_t>(e) * d + c]));
+      logits[static_cast<size_t>(t) * E + e] = s;
+    }
+  }
+  return 0;
+}
+
+// Gated residual update and the next normalisation (TokenSpeed, "Residual update and
+// normalization fusion"), per token t and residual branch g < G:
+//   R'[g][t] = R[g][t] + 2 sigmoid(a[t][g]) O[t]          stored (and kept) as BF16
+//   N[g][t]  = GemmaRMSNorm(R'[g][t], w[g])
+//   GemmaRMSNorm(x, w)_c = x_c / sqrt(mean_c(x_c^2) + eps) * (1 + w_c)
+// O is the sublayer's output (here the routed-MoE sum over the token's routes, without a
+// residual); the normalisation reads the residual after its rounding to the storage type.
+// sigmoid(z) = 1 / (1 + exp(-z)).  Sums ascend in c.
+template <typename Acc>
+int gated_residual_norm(int T, int d, int G, const Acc* O, const uint16_t* R, const float* a, const uint16_t* w,
+                        float eps, uint16_t* r_out, Acc* n_out) {
+  if (T < 0 || d <= 0 || G <= 0) return -1;
+  std::vector<Acc> rr(d);
+  for (int t = 0; t < T; ++t) {
+    for (int g = 0; g < G; ++g) {
+      const Acc z = static_cast<Acc>(a[static_cast<size_t>(t) * G + g]);
+      const Acc gate = static_cast<Acc>(2) * (static_cast<Acc>(1) / (static_cast<Acc>(1) + std::exp(-z)));
+      const size_t row = (static_cast<size_t>(g) * T + t) * d;
+      Acc ss = 0;
+      for (int c = 0; c < d; ++c) {
+        const Acc v = static_cast<Acc>(bf16_to_float(R[row + c])) + gate * O[static_cast<size_t>(t) * d + c];
+        const uint16_t b = bf16_round(static_cast<float>(v));
+        r_out[row + c] = b;
+        rr[c] = static_cast<Acc>(bf16_to_float(b));
+        ss += rr[c] * rr[c];
+      }
+      const Acc inv = static_cast<Acc>(1) / std::sqrt(ss / static_cast<Acc>(d) + static_cast<Acc>(eps));
+      for (int c = 0; c < d; ++c) {
+        const Acc wc = static_cast<Acc>(bf16_to_float(w[static_cast<size_t>(g) * d + c]));
+        n_out[row + c] = rr[c] * inv * (static_cast<Acc>(1) + wc);
+      }
+    }
+  }
+  return 0;
+}
+
 }  // namespace
 
 extern "C" {
+
+uint16_t oracle_bf16_round(float x) { return bf16_round(x); }
+
+int oracle_router_logits_f32(int T, int d, int E, const uint16_t* hidden_bf16, const uint16_t* router_w_bf16,
+                             float* logits) {
+  return router_logits<float>(T, d, E, hidden_bf16, router_w_bf16, logits);
+}
+
+int oracle_router_logits_f64(int T, int d, int E, const uint16_t* hidden_bf16, const uint16_t* router_w_bf16,
+                             double* logits) {
+  return router_logits<double>(T, d, E, hidden_bf16, router_w_bf16, logits);
+}
+
+int oracle_gated_residual_norm_f32(int T, int d, int G, const float* moe_out, const uint16_t* residual_bf16,
+                                   const float* inject_logits, const uint16_t* norm_w_bf16, float eps,
+                                   uint16_t* residual_out_bf16, float* normed) {
+  return gated_residual_norm<float>(T, d, G, moe_out, residual_bf16, inject_logits, norm_w_bf16, eps,
+                                    residual_out_bf16, normed);
+}
+
+int oracle_gated_residual_norm_f64(int T, int d, int G, const double* moe_out, const uint16_t* residual_bf16,
+                                   const float* inject_logits, const uint16_t* norm_w_bf16, float eps,
+                                   uint16_t* residual_out_bf16, double* normed) {
+  return gated_residual_norm<double>(T, d, G, moe_out, residual_bf16, inject_logits, norm_w_bf16, eps,
+                                     residual_out_bf16, normed);
+}
+
+int oracle_moe_experts_ts_f32(int T, int d, int F, int E, int k, const uint16_t* hidden_bf16, const int32_t* ids,
+                              const float* weights, const uint8_t* w13_codes, const uint8_t* w13_scales,
+                              const float* w13_ts_e, const uint8_t* w2_codes, const uint8_t* w2_scales,
+                              const float* w2_ts_e, const uint16_t* residual_bf16, const uint8_t* token_mask,
+                              float* out) {
+  if (!w13_ts_e || !w2_ts_e) return -1;
+  return moe_experts<float>(T, d, F, E, k, hidden_bf16, ids, weights, w13_codes, w13_scales, 1.0f, w2_codes,
+                            w2_scales, 1.0f, residual_bf16, token_mask, out, w13_ts_e, w2_ts_e);
+}
 
 float oracle_e2m1_value(uint32_t nibble) { return static_cast<float>(e2m1_exact(nibble & 15u)); }
 

@@ -24,6 +24,10 @@
  *    expert index, selection plus normalisation; section "First implementation
  *    boundary": compact expert-presence list, fused gate/up with SiLU/multiply, down
  *    fused with the weighted unroute, routes summed in a fixed order.
+ *  - "TokenSpeed: Qwen3.8-Flash-Next optimisations", section "Residual update and
+ *    normalization fusion": R' = R + 2 sigmoid(a) O per residual branch, then
+ *    GemmaRMSNorm(R', w) of the consuming mixer, the residual rounded to its storage type
+ *    before the normalisation reads it.
  *  - NVFP4 bit formats: the pages only name "NVFP4"; the element format follows the
  *    OCP Microscaling (MX) v1.0 definitions of E2M1 (FP4, exponent bias 1, no
  *    inf/NaN) and E4M3 (FP8, bias 7, no infinities, S.1111.111 = NaN), with one E4M3
@@ -84,6 +88,37 @@ int oracle_moe_experts_f64(int T, int d, int F, int E, int k,
                            const uint8_t* w13_codes, const uint8_t* w13_scales, float w13_ts,
                            const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_ts,
                            const uint16_t* residual_bf16, const uint8_t* token_mask, double* out);
+
+/* BF16 bit pattern of `x`, round to nearest, ties to even (NaN stays NaN). */
+uint16_t oracle_bf16_round(float x);
+
+/* Router projection: logits[t][e] = sum_c hidden[t][c] * router_w[e][c] (BF16 inputs, sums in
+ * the accumulation type, ascending c).  hidden [T, d], router_w [E, d], logits [T, E].
+ * Returns 0, or -1 on invalid sizes. */
+int oracle_router_logits_f32(int T, int d, int E, const uint16_t* hidden_bf16, const uint16_t* router_w_bf16,
+                             float* logits);
+int oracle_router_logits_f64(int T, int d, int E, const uint16_t* hidden_bf16, const uint16_t* router_w_bf16,
+                             double* logits);
+
+/* Gated residual update and normalisation for G residual branches:
+ *   R'[g][t] = BF16(R[g][t] + 2 sigmoid(a[t][g]) O[t]),
+ *   N[g][t]  = R'[g][t] / sqrt(mean(R'[g][t]^2) + eps) * (1 + w[g])
+ * moe_out O [T, d] (the sublayer output), residual R [G, T, d] BF16, inject_logits a [T, G],
+ * norm_w w [G, d] BF16; residual_out R' [G, T, d] BF16, normed N [G, T, d].  Returns 0 or -1. */
+int oracle_gated_residual_norm_f32(int T, int d, int G, const float* moe_out, const uint16_t* residual_bf16,
+                                   const float* inject_logits, const uint16_t* norm_w_bf16, float eps,
+                                   uint16_t* residual_out_bf16, float* normed);
+int oracle_gated_residual_norm_f64(int T, int d, int G, const double* moe_out, const uint16_t* residual_bf16,
+                                   const float* inject_logits, const uint16_t* norm_w_bf16, float eps,
+                                   uint16_t* residual_out_bf16, double* normed);
+
+/* oracle_moe_experts_f32 with one FP32 tensor scale per expert and weight tensor:
+ * w13_ts_e [E] and w2_ts_e [E] (entry e scales expert e's W13 / W2). */
+int oracle_moe_experts_ts_f32(int T, int d, int F, int E, int k, const uint16_t* hidden_bf16, const int32_t* ids,
+                              const float* weights, const uint8_t* w13_codes, const uint8_t* w13_scales,
+                              const float* w13_ts_e, const uint8_t* w2_codes, const uint8_t* w2_scales,
+                              const float* w2_ts_e, const uint16_t* residual_bf16, const uint8_t* token_mask,
+                              float* out);
 
 #ifdef __cplusplus
 }

@@ -55,6 +55,13 @@ def lib():
             for name in ("oracle_moe_experts_f32", "oracle_moe_experts_f64"):
                 getattr(L, name).argtypes = ([ctypes.c_int] * 5 + [_P] * 5 + [ctypes.c_float]
                                              + [_P] * 2 + [ctypes.c_float] + [_P] * 3)
+            L.oracle_moe_experts_ts_f32.argtypes = [ctypes.c_int] * 5 + [_P] * 12
+            L.oracle_bf16_round.restype = ctypes.c_uint16
+            L.oracle_bf16_round.argtypes = [ctypes.c_float]
+            for name in ("oracle_router_logits_f32", "oracle_router_logits_f64"):
+                getattr(L, name).argtypes = [ctypes.c_int] * 3 + [_P] * 3
+            for name in ("oracle_gated_residual_norm_f32", "oracle_gated_residual_norm_f64"):
+                getattr(L, name).argtypes = [ctypes.c_int] * 3 + [_P] * 4 + [ctypes.c_float] + [_P] * 2
             _lib = L
     return _lib
 
@@ -148,3 +155,67 @@ def moe_layer(cfg, inputs: dict, token_mask=None, precision: str = "f32"):
     out = moe_experts((cfg.T, cfg.d, cfg.ffn, cfg.E, cfg.k), inputs["hidden"], ids, wts, inputs,
                       inputs.get("residual"), token_mask, precision)
     return ids, wts, out
+
+
+def bf16_round(x) -> np.ndarray:
+    """BF16 bit patterns (uint16) of float32 values, round to nearest even."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    f = lib().oracle_bf16_round
+    return np.array([f(float(v)) for v in x.ravel()], dtype=np.uint16).reshape(x.shape)
+
+
+def router_logits(hidden_bf16: np.ndarray, router_w_bf16: np.ndarray, precision: str = "f32") -> np.ndarray:
+    """logits [T, E] = hidden [T, d] (BF16 bits) x router_w [E, d] (BF16 bits)^T."""
+    hidden_bf16 = np.ascontiguousarray(hidden_bf16, dtype=np.uint16)
+    router_w_bf16 = np.ascontiguousarray(router_w_bf16, dtype=np.uint16)
+    T, d = hidden_bf16.shape
+    E, d2 = router_w_bf16.shape
+    assert d == d2
+    dt = np.float32 if precision == "f32" else np.float64
+    out = np.empty((T, E), dtype=dt)
+    fn = lib().oracle_router_logits_f32 if precision == "f32" else lib().oracle_router_logits_f64
+    if fn(T, d, E, _ptr(hidden_bf16), _ptr(router_w_bf16), _ptr(out)) != 0:
+        raise ValueError("oracle_router_logits: invalid arguments")
+    return out
+
+
+def gated_residual_norm(moe_out: np.ndarray, residual_bf16: np.ndarray, inject_logits: np.ndarray,
+                        norm_w_bf16: np.ndarray, eps: float = 1e-6, precision: str = "f32"):
+    """(R' [G, T, d] BF16 bits, N [G, T, d]) of the gated residual update and GemmaRMSNorm."""
+    dt = np.float32 if precision == "f32" else np.float64
+    moe_out = np.ascontiguousarray(moe_out, dtype=dt)
+    residual_bf16 = np.ascontiguousarray(residual_bf16, dtype=np.uint16)
+    inject_logits = np.ascontiguousarray(inject_logits, dtype=np.float32)
+    norm_w_bf16 = np.ascontiguousarray(norm_w_bf16, dtype=np.uint16)
+    G, T, d = residual_bf16.shape
+    assert moe_out.shape == (T, d) and inject_logits.shape == (T, G) and norm_w_bf16.shape == (G, d)
+    r_out = np.empty((G, T, d), dtype=np.uint16)
+    n_out = np.empty((G, T, d), dtype=dt)
+    fn = lib().oracle_gated_residual_norm_f32 if precision == "f32" else lib().oracle_gated_residual_norm_f64
+    if fn(T, d, G, _ptr(moe_out), _ptr(residual_bf16), _ptr(inject_logits), _ptr(norm_w_bf16), float(eps),
+          _ptr(r_out), _ptr(n_out)) != 0:
+        raise ValueError("oracle_gated_residual_norm: invalid arguments")
+    return r_out, n_out
+
+
+def moe_experts_ts(dims, hidden_bf16, ids, weights, w: dict, w13_ts_e, w2_ts_e, residual_bf16=None,
+                   token_mask=None) -> np.ndarray:
+    """oracle moe_experts (FP32) with per-expert tensor scales w13_ts_e [E], w2_ts_e [E]."""
+    T, d, F, E, k = (int(v) for v in dims)
+    hidden_bf16 = np.ascontiguousarray(hidden_bf16, dtype=np.uint16)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    weights = np.ascontiguousarray(weights, dtype=np.float32)
+    arrs = [np.ascontiguousarray(w[n], dtype=np.uint8) for n in ("w13_codes", "w13_scales", "w2_codes", "w2_scales")]
+    t13 = np.ascontiguousarray(w13_ts_e, dtype=np.float32)
+    t2 = np.ascontiguousarray(w2_ts_e, dtype=np.float32)
+    assert t13.shape == (E,) and t2.shape == (E,)
+    res = None if residual_bf16 is None else np.ascontiguousarray(residual_bf16, dtype=np.uint16)
+    mask = None if token_mask is None else np.ascontiguousarray(token_mask, dtype=np.uint8)
+    out = np.full((T, d), np.nan, dtype=np.float32)
+    rc = lib().oracle_moe_experts_ts_f32(T, d, F, E, k, _ptr(hidden_bf16), _ptr(ids), _ptr(weights), _ptr(arrs[0]),
+                                         _ptr(arrs[1]), _ptr(t13), _ptr(arrs[2]), _ptr(arrs[3]), _ptr(t2),
+                                         0 if res is None else _ptr(res), 0 if mask is None else _ptr(mask),
+                                         _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_moe_experts_ts: invalid arguments")
+    return out
