@@ -277,6 +277,60 @@ MOE_API int moe_forward_experts_expert_range(const moe_shape* shape, int e_begin
                                              void* out, void* workspace, size_t workspace_bytes, int algo,
                                              moe_stream_t stream);
 
+/* Router projection, the producer of the router logits ("Persistent execution for Flash-Next
+ * GGUF on SM70", section "Router: selection and expert-task production": the projection whose
+ * results the selection consumes, with an explicit hand-off to the final producer):
+ *   logits[t][e] = sum_c hidden[t][c] * router_w[e][c]   (BF16 inputs, FP32 sums)
+ *   hidden   [T, d] BF16;  router_w [E, d] BF16 (row e = expert e);  logits [T, E] FP32 out.
+ * Written as the weight-prefetch GEMV of "How I forked vLLM and made Qwen3.8-Flash-Next decode
+ * 1.6x faster on one GPU" (section 5, paragraph "PDL weight-prefetch GEMV"): each CTA copies its
+ * 16 router-weight rows into shared memory before it waits for the preceding kernel in the
+ * stream, so under programmatic dependent launch the weights stream while that kernel (the
+ * previous layer) finishes; the partial sums of its four K quarters are added in a fixed order
+ * (no atomics), so the logits, and the routing, are the same on every run.  Supported: E a
+ * multiple of 16, d a multiple of 64 up to 4096.  MOE_ERR_UNSUPPORTED otherwise. */
+MOE_API int moe_router_logits(const moe_shape* shape, const void* hidden, const void* router_w, float* logits,
+                              moe_stream_t stream);
+
+/* moe_router_logits followed by moe_layer on its logits: the layer from the hidden states and
+ * the router weight.  `logits` [T, E] FP32 is the caller's buffer for the projection (also an
+ * output).  Other arguments, ownership and errors as moe_layer. */
+MOE_API int moe_layer_from_hidden(const moe_shape* shape, const void* hidden, const void* router_w, float* logits,
+                                  const uint8_t* w13_codes, const uint8_t* w13_scales, float w13_scale,
+                                  const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+                                  const void* residual, void* out, int32_t* ids, float* weights, void* workspace,
+                                  size_t workspace_bytes, moe_stream_t stream);
+
+/* Gated residual update and the next normalisation, in place of the plain un-route, for a
+ * model whose residual stream has G branches ("TokenSpeed: Qwen3.8-Flash-Next optimisations",
+ * section "Residual update and normalization fusion").  With O[t] = sum_j w_{t,j} y_{t,j} the
+ * token's weighted routes (slots in order, FP32, from the per-route outputs that
+ * moe_forward_expert_kernels left in `workspace`), for every token t and branch g < G:
+ *   residual_out[g][t] = BF16(residual[g][t] + 2 sigmoid(inject_logits[t][g]) O[t])
+ *   normed_out[g][t]   = GemmaRMSNorm(residual_out[g][t], norm_weight[g])
+ *   GemmaRMSNorm(x, w)_c = x_c / sqrt(mean_c(x_c^2) + eps) * (1 + w_c)
+ * The normalisation reads the updated residual after its rounding to BF16 (kept on chip; both
+ * outputs are stored).  One CTA per token.
+ *   residual      [G, T, d] BF16 (16-byte aligned)
+ *   inject_logits [T, G]    FP32
+ *   norm_weight   [G, d]    BF16
+ *   eps           >= 0 (the pages give none; Gemma's own is 1e-6)
+ *   residual_out  [G, T, d] BF16, may alias residual;  normed_out [G, T, d] BF16
+ * Supported: 1 <= G <= 8, d <= 4096 (MOE_ERR_UNSUPPORTED otherwise).  Errors as moe_forward. */
+MOE_API int moe_forward_unroute_gated(const moe_shape* shape, int G, const void* residual,
+                                      const float* inject_logits, const void* norm_weight, float eps,
+                                      void* residual_out, void* normed_out, void* workspace,
+                                      size_t workspace_bytes, moe_stream_t stream);
+
+/* Whole layer with the gated epilogue: moe_front, moe_forward_expert_kernels (MOE_ALGO_AUTO) and
+ * moe_forward_unroute_gated.  Arguments as those calls; ids/weights as moe_layer. */
+MOE_API int moe_layer_gated(const moe_shape* shape, int G, const float* logits, const void* hidden,
+                            const uint8_t* w13_codes, const uint8_t* w13_scales, float w13_scale,
+                            const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+                            const void* residual, const float* inject_logits, const void* norm_weight, float eps,
+                            void* residual_out, void* normed_out, int32_t* ids, float* weights, void* workspace,
+                            size_t workspace_bytes, moe_stream_t stream);
+
 /* The whole layer (moe_layer) with its scratch in a fixed device array of the library
  * instead of a caller-provided workspace.  The pages have no counterpart for this entry
  * point.  It is for callers that cannot allocate device memory: code running while a

@@ -43,7 +43,8 @@ except ImportError:  # pragma: no cover - torch is present in every supported im
     torch = None
 
 __all__ = ["Config", "CONFIGS", "ZIPF_COEF_CALIBRATED", "ZIPF_COEF_LITERAL", "E4M3_FINITE_CODES",
-           "gen_logits", "gen_hidden", "gen_residual", "gen_weights", "gen_layer",
+           "gen_logits", "gen_hidden", "gen_residual", "gen_weights", "gen_layer", "gen_router_weight",
+           "gen_gated_inputs", "gen_expert_tensor_scales",
            "weight_bytes_per_expert"]
 
 # Zipf popularity bias for the T=256 decode batch.  The literal coefficient (1.5 on the
@@ -55,7 +56,8 @@ ZIPF_COEF_CALIBRATED = 0.25
 ZIPF_COEF_LITERAL = 1.5
 
 _TENSOR_TAGS = {"logits": 1, "hidden": 2, "residual": 3, "w13_codes": 4, "w13_scales": 5,
-                "w2_codes": 6, "w2_scales": 7, "bias_pick": 8, "bias_val": 9, "zipf_perm": 10}
+                "w2_codes": 6, "w2_scales": 7, "bias_pick": 8, "bias_val": 9, "zipf_perm": 10,
+                "router_w": 11, "branches": 12, "inject": 13, "norm_w": 14, "ts_e": 15}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -207,6 +209,37 @@ def gen_weights(cfg: Config, seed: int = 0, layer: int = 0, scales: str = "defau
         "w2_scales": w2_scales.reshape(E, d, F // 16),
         "w2_ts": float(w2_ts),
     }
+
+
+def gen_router_weight(cfg: Config, seed: int = 0, layer: int = 0) -> np.ndarray:
+    """BF16 router weight [E, d] (uint16 bits), values N(0, 1/d) rounded RNE, so that the
+    projected logits of N(0,1) hidden rows are about N(0,1) like the workloads' logits."""
+    rng = _rng(seed, cfg, layer, "router_w")
+    return _to_bf16_bits(rng.standard_normal((cfg.E, cfg.d), dtype=np.float32) / np.float32(np.sqrt(cfg.d)))
+
+
+def gen_gated_inputs(cfg: Config, G: int, seed: int = 0, layer: int = 0) -> dict:
+    """Inputs of the gated residual update for G residual branches: the branches [G, T, d]
+    (BF16 bits, N(0,1)), the injection logits [T, G] (float32, N(0,1)) and the consuming
+    normalisation's weight [G, d] (BF16 bits, N(0, 0.1^2): GemmaRMSNorm scales by 1 + w)."""
+    return {
+        "branches": _to_bf16_bits(_rng(seed, cfg, layer, "branches").standard_normal((G, cfg.T, cfg.d),
+                                                                                  dtype=np.float32)),
+        "inject": _rng(seed, cfg, layer, "inject").standard_normal((cfg.T, G), dtype=np.float32),
+        "norm_w": _to_bf16_bits(_rng(seed, cfg, layer, "norm_w").standard_normal((G, cfg.d), dtype=np.float32)
+                                * np.float32(0.1)),
+    }
+
+
+def gen_expert_tensor_scales(cfg: Config, seed: int = 0, layer: int = 0) -> tuple:
+    """Per-expert FP32 tensor scales (w13 [E], w2 [E]): powers of two from 2^-2 to 2^2 times
+    one of (0.75, 1, 1.3), drawn independently per expert and tensor."""
+    rng = _rng(seed, cfg, layer, "ts_e")
+    t13 = (np.float32(2.0) ** rng.integers(-2, 3, cfg.E).astype(np.float32)) * \
+        rng.choice(np.array([0.75, 1.0, 1.3], np.float32), cfg.E)
+    t2 = (np.float32(2.0) ** rng.integers(-2, 3, cfg.E).astype(np.float32)) * \
+        rng.choice(np.array([0.75, 1.0, 1.3], np.float32), cfg.E)
+    return t13.astype(np.float32), t2.astype(np.float32)
 
 
 def gen_layer(cfg: Config, seed: int = 0, layer: int = 0, weights: bool = True) -> dict:

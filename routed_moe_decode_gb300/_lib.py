@@ -69,6 +69,11 @@ SIGNATURES = {
     "moe_plan_expert_range": (_I, [_SP, _I, _I, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_forward_experts_expert_range": (_I, [_SP, _I, _I, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _I,
                                               _P]),
+    "moe_router_logits": (_I, [_SP, _P, _P, _P, _P]),
+    "moe_layer_from_hidden": (_I, [_SP, _P, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_forward_unroute_gated": (_I, [_SP, _I, _P, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_layer_gated": (_I, [_SP, _I, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _F, _P, _P, _P, _P, _P,
+                             ctypes.c_size_t, _P]),
     "moe_layer_static_workspace": (_I, [_SP, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P]),
     "moe_read_device_status": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint32), _P]),
     "moe_plan_summary": (_I, [_SP, _P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), _P]),
@@ -257,6 +262,39 @@ def selftest_expert_timeout(shape: Shape, w: dict, residual, out, ws: Workspace,
         ctypes.byref(shape), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]), float(w["w13_ts"]), _ptr(w["w2_codes"]),
         _ptr(w["w2_scales"]), float(w["w2_ts"]), _ptr(residual), _ptr(out), ws.ptr, ws.nbytes, int(algo),
         int(dn_task), int(wait_limit_cycles), _stream(stream)))
+
+
+def router_logits(shape: Shape, hidden, router_w, logits, stream=None):
+    """logits [T, E] FP32 = hidden [T, d] BF16 x router_w [E, d] BF16^T (weight-prefetch GEMV)."""
+    _check("moe_router_logits", lib().moe_router_logits(ctypes.byref(shape), _ptr(hidden), _ptr(router_w),
+                                                        _ptr(logits), _stream(stream)))
+
+
+def layer_from_hidden(shape: Shape, hidden, router_w, logits, w: dict, residual, out, ids, weights, ws: Workspace,
+                      stream=None):
+    """The router projection into `logits`, then the whole layer on them (moe_layer)."""
+    _check("moe_layer_from_hidden", lib().moe_layer_from_hidden(
+        ctypes.byref(shape), _ptr(hidden), _ptr(router_w), _ptr(logits), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]),
+        float(w["w13_ts"]), _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]), _ptr(residual), _ptr(out),
+        _ptr(ids), _ptr(weights), ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def forward_unroute_gated(shape: Shape, G: int, residual, inject_logits, norm_weight, eps: float, residual_out,
+                          normed_out, ws: Workspace, stream=None):
+    """Gated residual update of G branches plus GemmaRMSNorm from the per-route outputs in `ws`."""
+    _check("moe_forward_unroute_gated", lib().moe_forward_unroute_gated(
+        ctypes.byref(shape), int(G), _ptr(residual), _ptr(inject_logits), _ptr(norm_weight), float(eps),
+        _ptr(residual_out), _ptr(normed_out), ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def layer_gated(shape: Shape, G: int, logits, hidden, w: dict, residual, inject_logits, norm_weight, eps: float,
+                residual_out, normed_out, ids, weights, ws: Workspace, stream=None):
+    """Whole layer with the gated residual update and GemmaRMSNorm in place of the plain un-route."""
+    _check("moe_layer_gated", lib().moe_layer_gated(
+        ctypes.byref(shape), int(G), _ptr(logits), _ptr(hidden), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]),
+        float(w["w13_ts"]), _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]), _ptr(residual),
+        _ptr(inject_logits), _ptr(norm_weight), float(eps), _ptr(residual_out), _ptr(normed_out), _ptr(ids),
+        _ptr(weights), ws.ptr, ws.nbytes, _stream(stream)))
 
 
 def read_status(ws: Workspace, clear: bool = True, stream=None) -> int:

@@ -611,6 +611,76 @@ int moe_layer_expert_range(const moe_shape* shape, int e_begin, int e_end, const
                     out, ids, weights, workspace, workspace_bytes, ExpertRange{e_begin, e_end}, stream);
 }
 
+int moe_router_logits(const moe_shape* shape, const void* hidden, const void* router_w, float* logits,
+                      moe_stream_t stream) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (shape->T == 0) return MOE_OK;
+  if (!hidden || !router_w || !logits || !aligned(hidden, 16) || !aligned(router_w, 16) || !aligned(logits, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (!moe::router_gemv_supports(shape->T, shape->d, shape->E)) return MOE_ERR_UNSUPPORTED;
+  const cudaError_t e = moe::launch_router_gemv(static_cast<const __nv_bfloat16*>(hidden),
+                                                static_cast<const __nv_bfloat16*>(router_w), logits, shape->T,
+                                                shape->d, shape->E, stream);
+  if (e != cudaSuccess) { set_error("router launch", e); return MOE_ERR_CUDA; }
+  return MOE_OK;
+}
+
+int moe_layer_from_hidden(const moe_shape* shape, const void* hidden, const void* router_w, float* logits,
+                          const uint8_t* w13_codes, const uint8_t* w13_scales, float w13_scale,
+                          const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale, const void* residual,
+                          void* out, int32_t* ids, float* weights, void* workspace, size_t workspace_bytes,
+                          moe_stream_t stream) {
+  const int rc = moe_router_logits(shape, hidden, router_w, logits, stream);
+  if (rc != MOE_OK) return rc;
+  return layer_impl(shape, logits, hidden, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual,
+                    out, ids, weights, workspace, workspace_bytes, all_experts(shape), stream);
+}
+
+int moe_forward_unroute_gated(const moe_shape* shape, int G, const void* residual, const float* inject_logits,
+                              const void* norm_weight, float eps, void* residual_out, void* normed_out,
+                              void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (G < 1 || !(eps >= 0.f) || !(eps < 1e30f)) return MOE_ERR_INVALID_ARG;
+  if (!moe::gated_unroute_supports(shape->d, G)) return MOE_ERR_UNSUPPORTED;
+  if (shape->T == 0) return MOE_OK;
+  if (!residual || !inject_logits || !norm_weight || !residual_out || !normed_out || !aligned(residual, 16) ||
+      !aligned(norm_weight, 16) || !aligned(residual_out, 16) || !aligned(normed_out, 16) || !aligned(inject_logits, 4))
+    return MOE_ERR_INVALID_ARG;
+  rc = check_ws(shape, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
+  const WsLayout L = moe::ws_layout(*shape);
+  const moe::ExpertArgs a = expert_args(shape, L, workspace, nullptr, nullptr, 0.f, nullptr, nullptr, 0.f, nullptr,
+                                        nullptr, all_experts(shape));
+  const cudaError_t e = moe::launch_gated_unroute(
+      a, G, static_cast<const __nv_bfloat16*>(residual), inject_logits, static_cast<const __nv_bfloat16*>(norm_weight),
+      eps, static_cast<__nv_bfloat16*>(residual_out), static_cast<__nv_bfloat16*>(normed_out), stream);
+  if (e != cudaSuccess) { set_error("gated un-route launch", e); return MOE_ERR_CUDA; }
+  return MOE_OK;
+}
+
+int moe_layer_gated(const moe_shape* shape, int G, const float* logits, const void* hidden, const uint8_t* w13_codes,
+                    const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales,
+                    float w2_scale, const void* residual, const float* inject_logits, const void* norm_weight,
+                    float eps, void* residual_out, void* normed_out, int32_t* ids, float* weights, void* workspace,
+                    size_t workspace_bytes, moe_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (G < 1 || !(eps >= 0.f) || !(eps < 1e30f)) return MOE_ERR_INVALID_ARG;
+  if (!moe::gated_unroute_supports(shape->d, G)) return MOE_ERR_UNSUPPORTED;
+  if (shape->T == 0) return MOE_OK;
+  if (!w13_codes || !w13_scales || !w2_codes || !w2_scales) return MOE_ERR_INVALID_ARG;
+  rc = front_impl(shape, logits, hidden, ids, weights, workspace, workspace_bytes, all_experts(shape), stream);
+  if (rc != MOE_OK) return rc;
+  rc = forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, nullptr, nullptr,
+                            workspace, workspace_bytes, MOE_ALGO_AUTO, nullptr, stream, all_experts(shape),
+                            kStageExperts);
+  if (rc != MOE_OK) return rc;
+  return moe_forward_unroute_gated(shape, G, residual, inject_logits, norm_weight, eps, residual_out, normed_out,
+                                   workspace, workspace_bytes, stream);
+}
+
 int moe_read_device_status(const void* workspace, int clear, uint32_t* status_bits, moe_stream_t stream) {
   if (!workspace || !status_bits || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
   uint32_t v = 0;

@@ -310,6 +310,18 @@ int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint
 int encode_scales_map(CUtensorMap* tm, const void* base, uint32_t row_bytes, uint64_t rows, uint32_t box_rows);
 // Shapes the decode (warp-MMA) kernel handles: d and ffn powers of two from 256 to 2048.
 bool expert_mma_supports(int d, int F);
+// Router projection logits = hidden x Wr^T (BF16 in, FP32 out) with the weight tile copied
+// before the wait for the preceding kernel (router_norm.cu); E a multiple of 16, d of 64.
+bool router_gemv_supports(int T, int d, int E);
+size_t router_smem_bytes(int d);
+cudaError_t launch_router_gemv(const __nv_bfloat16* hidden, const __nv_bfloat16* wr, float* logits, int T, int d,
+                               int E, cudaStream_t stream);
+// Gated un-route: R'[g] = BF16(R[g] + 2 sigmoid(a[g]) O), N[g] = GemmaRMSNorm(R'[g], w[g]) for
+// G residual branches, O the token's weighted routes (router_norm.cu); d <= 4096, G <= 8.
+bool gated_unroute_supports(int d, int G);
+cudaError_t launch_gated_unroute(const ExpertArgs& a, int G, const __nv_bfloat16* residual, const float* inject,
+                                 const __nv_bfloat16* norm_w, float eps, __nv_bfloat16* residual_out,
+                                 __nv_bfloat16* normed, cudaStream_t stream);
 // Record a message for moe_last_cuda_error on the calling host thread.
 void set_last_error_message(const char* msg);
 
