@@ -277,6 +277,16 @@ MOE_API int moe_forward_experts_expert_range(const moe_shape* shape, int e_begin
                                              void* out, void* workspace, size_t workspace_bytes, int algo,
                                              moe_stream_t stream);
 
+/* moe_layer with one FP32 tensor scale per expert for each weight tensor instead of one for
+ * all experts: expert e's W13 is scaled by w13_scales_e[e] and its W2 by w2_scales_e[e]
+ * (device arrays of E floats; NVFP4 checkpoints that quantise each expert separately carry
+ * such per-expert global scales).  Other arguments, ownership and errors as moe_layer. */
+MOE_API int moe_layer_expert_scales(const moe_shape* shape, const float* logits, const void* hidden,
+                                    const uint8_t* w13_codes, const uint8_t* w13_scales, const float* w13_scales_e,
+                                    const uint8_t* w2_codes, const uint8_t* w2_scales, const float* w2_scales_e,
+                                    const void* residual, void* out, int32_t* ids, float* weights,
+                                    void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* Router projection, the producer of the router logits ("Persistent execution for Flash-Next
  * GGUF on SM70", section "Router: selection and expert-task production": the projection whose
  * results the selection consumes, with an explicit hand-off to the final producer):

@@ -69,6 +69,7 @@ SIGNATURES = {
     "moe_plan_expert_range": (_I, [_SP, _I, _I, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_forward_experts_expert_range": (_I, [_SP, _I, _I, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _I,
                                               _P]),
+    "moe_layer_expert_scales": (_I, [_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_router_logits": (_I, [_SP, _P, _P, _P, _P]),
     "moe_layer_from_hidden": (_I, [_SP, _P, _P, _P, _P, _P, _F, _P, _P, _F, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_forward_unroute_gated": (_I, [_SP, _I, _P, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -262,6 +263,15 @@ def selftest_expert_timeout(shape: Shape, w: dict, residual, out, ws: Workspace,
         ctypes.byref(shape), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]), float(w["w13_ts"]), _ptr(w["w2_codes"]),
         _ptr(w["w2_scales"]), float(w["w2_ts"]), _ptr(residual), _ptr(out), ws.ptr, ws.nbytes, int(algo),
         int(dn_task), int(wait_limit_cycles), _stream(stream)))
+
+
+def layer_expert_scales(shape: Shape, logits, hidden, w: dict, w13_ts_e, w2_ts_e, residual, out, ids, weights,
+                        ws: Workspace, stream=None):
+    """moe_layer with per-expert FP32 tensor scales (device tensors [E]) for W13 and W2."""
+    _check("moe_layer_expert_scales", lib().moe_layer_expert_scales(
+        ctypes.byref(shape), _ptr(logits), _ptr(hidden), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]), _ptr(w13_ts_e),
+        _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), _ptr(w2_ts_e), _ptr(residual), _ptr(out), _ptr(ids),
+        _ptr(weights), ws.ptr, ws.nbytes, _stream(stream)))
 
 
 def router_logits(shape: Shape, hidden, router_w, logits, stream=None):

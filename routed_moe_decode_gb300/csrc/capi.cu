@@ -320,7 +320,8 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
                                 const void* residual, void* out, void* workspace, size_t workspace_bytes, int algo,
                                 unsigned long long* trace, moe_stream_t stream, ExpertRange r,
                                 int stages = kStageExperts | kStageUnroute,
-                                long long wait_limit = moe::kDefaultWaitLimit, int poison_dn_task = -1) {
+                                long long wait_limit = moe::kDefaultWaitLimit, int poison_dn_task = -1,
+                                const float* w13_ts_e = nullptr, const float* w2_ts_e = nullptr) {
   int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   if (shape->T == 0) return MOE_OK;
@@ -338,6 +339,8 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
                                   w2_scale, residual, out, r);
   a.trace = trace;
   a.wait_limit = wait_limit;
+  a.w13_ts_e = w13_ts_e;
+  a.w2_ts_e = w2_ts_e;
   cudaError_t e;
   if (!(stages & kStageExperts)) {
     e = moe::launch_combine(a, stream);
@@ -679,6 +682,24 @@ int moe_layer_gated(const moe_shape* shape, int G, const float* logits, const vo
   if (rc != MOE_OK) return rc;
   return moe_forward_unroute_gated(shape, G, residual, inject_logits, norm_weight, eps, residual_out, normed_out,
                                    workspace, workspace_bytes, stream);
+}
+
+int moe_layer_expert_scales(const moe_shape* shape, const float* logits, const void* hidden,
+                            const uint8_t* w13_codes, const uint8_t* w13_scales, const float* w13_scales_e,
+                            const uint8_t* w2_codes, const uint8_t* w2_scales, const float* w2_scales_e,
+                            const void* residual, void* out, int32_t* ids, float* weights, void* workspace,
+                            size_t workspace_bytes, moe_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (shape->T == 0) return MOE_OK;
+  if (!w13_codes || !w13_scales || !w2_codes || !w2_scales || !out || !w13_scales_e || !w2_scales_e ||
+      !aligned(w13_scales_e, 4) || !aligned(w2_scales_e, 4))
+    return MOE_ERR_INVALID_ARG;
+  rc = front_impl(shape, logits, hidden, ids, weights, workspace, workspace_bytes, all_experts(shape), stream);
+  if (rc != MOE_OK) return rc;
+  return forward_experts_impl(shape, w13_codes, w13_scales, 1.f, w2_codes, w2_scales, 1.f, residual, out, workspace,
+                              workspace_bytes, MOE_ALGO_AUTO, nullptr, stream, all_experts(shape),
+                              kStageExperts | kStageUnroute, moe::kDefaultWaitLimit, -1, w13_scales_e, w2_scales_e);
 }
 
 int moe_read_device_status(const void* workspace, int clear, uint32_t* status_bits, moe_stream_t stream) {

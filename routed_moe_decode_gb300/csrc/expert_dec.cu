@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- epilogue: fragment rows g / g+8, routed rows 2q, 2q + 1 ----
       if (!is_dn) {
         const int nidx = s * kGuRows + 8 * cw + fr;  // element n of h
-        const float sc = a.w13_ts;
+        const float sc = ts13_of(a, te.x & 0xffff);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int r = 2 * q + cc;
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(smem_addr(&sm.pub_full[pub_n % kPubSlots]));
         ++pub_n;
       } else {
-        const float sc = a.w2_ts * kHUnscale;
+        const float sc = ts2_of(a, te.x & 0xffff) * kHUnscale;
         const int ra = s * kDnRows + lra, rb = s * kDnRows + lrb;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {

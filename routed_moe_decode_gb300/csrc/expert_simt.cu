@@ -99,8 +99,8 @@ __global__ void __launch_bounds__(256) simt_gateup_kernel(ExpertArgs a) {
 #pragma unroll
         for (int j = 0; j < kTok; ++j)
           if (j == lane) { gv = g[j]; uv = up[j]; }
-        gv *= a.w13_ts;
-        uv *= a.w13_ts;
+        gv *= ts13_of(a, e);
+        uv *= ts13_of(a, e);
         float h = gv / (1.0f + __expf(-gv)) * uv * kHScale;
         if (fabsf(h) > 65504.f) {
           atomicOr(a.status, static_cast<int>(MOE_DEV_H_SATURATED));
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(256) simt_down_kernel(ExpertArgs a) {
 #pragma unroll
         for (int j = 0; j < kTok; ++j)
           if (j == lane) yv = y[j];
-        a.y[static_cast<size_t>(off + r0 + lane) * a.d + r] = yv * a.w2_ts * kHUnscale;
+        a.y[static_cast<size_t>(off + r0 + lane) * a.d + r] = yv * ts2_of(a, e) * kHUnscale;
       }
     }
   }

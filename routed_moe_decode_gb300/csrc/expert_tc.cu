@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, 128);
         if (i < 64) {
           const int nidx = tk.s * kGuRows + i;  // element n of h
-          const float sc13 = a.w13_ts;
+          const float sc13 = ts13_of(a, tk.e);
 #pragma unroll
           for (int c = 0; c < kRowsPerPass; ++c) {
             if (c < tk.rows) {
@@ -542,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // down stripe: per-route FP32 outputs (summed over routes by the un-route kernel)
         const int rcol = tk.s * kDnRows + i;
-        const float scale = a.w2_ts * kHUnscale;
+        const float scale = ts2_of(a, tk.e) * kHUnscale;
 #pragma unroll
         for (int c = 0; c < kRowsPerPass; ++c)
           if (c < tk.rows)

@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!named_bar_and(2, 32 * kEpiWarps, got)) break;
       tc_fence_after();
       const uint32_t dcol = tmem + lane_base + kDCol0 + dbuf * kWideRows;
-      const float sc13 = a.w13_ts, sc2 = a.w2_ts * kHUnscale;
+      const float sc13 = ts13_of(a, tk.e), sc2 = ts2_of(a, tk.e) * kHUnscale;
       for (int c0 = 32 * grp; c0 < tk.rows; c0 += 64) {
         uint32_t v[32];
         tmem_ld_x32(dcol + c0, v);

@@ -53,6 +53,10 @@ struct PrepArgs {
 struct ExpertArgs {
   int T, d, F, E, k, R, S_gu, S_dn, nck_gu, nck_dn;
   float w13_ts, w2_ts;
+  // per-expert FP32 tensor scales (entry e - e_lo, like the weights), or null for the one
+  // value above for every expert
+  const float* w13_ts_e;
+  const float* w2_ts_e;
   const uint8_t* w13_codes;
   const uint8_t* w13_scales;
   const uint8_t* w2_codes;
@@ -84,6 +88,15 @@ struct ExpertArgs {
   // uint64 events = event code << 56 | index << 40 | %globaltimer low 40 bits
   unsigned long long* trace;
 };
+
+// FP32 tensor scale of expert e's W13 / W2: the per-expert array when given, else the one
+// value for every expert.
+__device__ __forceinline__ float ts13_of(const ExpertArgs& a, int e) {
+  return a.w13_ts_e ? __ldg(a.w13_ts_e + (e - a.e_lo)) : a.w13_ts;
+}
+__device__ __forceinline__ float ts2_of(const ExpertArgs& a, int e) {
+  return a.w2_ts_e ? __ldg(a.w2_ts_e + (e - a.e_lo)) : a.w2_ts;
+}
 
 // Un-route of four consecutive columns [c, c + 4) of token t: out = residual + sum_j w_{t,j}
 // y_{pos(t,j)}, FP32, slots in order, one BF16 rounding ("First implementation boundary",

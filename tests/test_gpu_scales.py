@@ -137,3 +137,32 @@ def test_decode_kernels_keep_large_y_exact(algo):
     ts13, ts2 = _band_ts(3)
     cfg, inp = _inputs("dec4", "band3", ts13, ts2 * 2.0 ** 14)
     _parity(cfg, inp, algo, "dec4 large y")
+
+
+@pytest.mark.parametrize("T,d,F,E,k", [(4, 256, 256, 16, 2), (40, 512, 256, 32, 4), (8, 384, 256, 16, 2),
+                                       (512, 256, 256, 16, 2), (4, 2048, 512, 512, 10)])
+def test_per_expert_tensor_scales(T, d, F, E, k):
+    # moe_layer_expert_scales through MOE_ALGO_AUTO, which picks the decode kernel for <= 8 tokens,
+    # the warp-MMA kernel, the 16-row tcgen05 kernel (d = 384) and the wide kernel (64 rows/expert)
+    import routed_moe_decode_gb300 as moe
+    import torch
+    from gpu_helpers import bf16_tensor, device_weights
+    cfg = mi.CONFIGS["tiny"].replace(name=f"ts_e{T}x{d}", T=T, d=d, ffn=F, E=E, k=k, tag=640 + T)
+    inp = mi.gen_layer(cfg, seed=12)
+    t13, t2 = mi.gen_expert_tensor_scales(cfg, seed=12)
+    dev = "cuda"
+    shape = moe.shape_of(T, d, F, E, k)
+    ws = moe.Workspace(shape)
+    w = device_weights(inp, dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
+    out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    moe.layer_expert_scales(shape, torch.from_numpy(inp["logits"]).to(dev), bf16_tensor(inp["hidden"], dev), w,
+                            torch.from_numpy(t13).to(dev), torch.from_numpy(t2).to(dev),
+                            bf16_tensor(inp["residual"], dev), out, ids, wts, ws)
+    torch.cuda.synchronize()
+    assert moe.read_status(ws) == 0
+    ids_ref, w_ref = O.route_topk(inp["logits"], k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+    ref = O.moe_experts_ts((T, d, F, E, k), inp["hidden"], ids_ref, w_ref, inp, t13, t2, inp["residual"])
+    assert_parity(out.float().cpu().numpy(), ref, f"per-expert scales T={T} d={d}", bf16_rounding=True)
