@@ -394,8 +394,10 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     return MOE_OK;
   };
   if (use_mma) {
-    rc = poison(at<moe::TaskEntry>(workspace, L.tasks), moe::META_NGU);
-    if (rc != MOE_OK) return rc;
+    if (!(moe::expert_dec_supports(shape->T, shape->d, shape->ffn) && moe::expert_dec_gathers(shape->T))) {
+      rc = poison(at<moe::TaskEntry>(workspace, L.tasks), moe::META_NGU);
+      if (rc != MOE_OK) return rc;
+    }
     CUtensorMap ts13, ts2;
     rc = moe::encode_scales_map(&ts13, w13_scales, static_cast<uint32_t>(shape->d / 16),
                                 static_cast<uint64_t>(r.hi - r.lo) * 2 * shape->ffn, 64);
@@ -405,9 +407,20 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     if (rc != MOE_OK) return rc;
     // for few tokens the decode kernel runs the un-route as trailing tasks of its own
     a.ncb = (stages & kStageUnroute) ? moe::expert_mma_unroute_tasks(shape->T, L.S_dn) : 0;
-    // at most eight tokens: the variant with the hidden rows resident in shared memory
+    // up to 64 tokens: the decode kernel with the hidden rows in shared memory (all of them
+    // for <= 8 tokens; per task, from its own table of 8-row passes, above)
     if (moe::expert_dec_supports(shape->T, shape->d, shape->ffn)) {
-      e = moe::launch_expert_dec(a, tm13, tm2, ts13, ts2, di.num_sms, stream);
+      moe::ExpertArgs ad = a;
+      if (moe::expert_dec_gathers(shape->T)) {
+        moe::TaskEntry* tasks_d = at<moe::TaskEntry>(workspace, L.tasks_d);
+        e = moe::launch_dec_plan(a, tasks_d, stream);
+        if (e != cudaSuccess) { set_error("decode task table launch", e); return MOE_ERR_CUDA; }
+        rc = poison(tasks_d, moe::META_DGU);
+        if (rc != MOE_OK) return rc;
+        ad.tasks = tasks_d;
+        ad.task_cap = L.max_tasks_d;
+      }
+      e = moe::launch_expert_dec(ad, tm13, tm2, ts13, ts2, di.num_sms, stream);
       if (e != cudaSuccess) { set_error("expert_dec launch", e); return MOE_ERR_CUDA; }
     } else {
       e = moe::launch_expert_mma(a, tm13, tm2, ts13, ts2, di.num_sms, stream);

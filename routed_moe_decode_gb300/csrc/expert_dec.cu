@@ -27,8 +27,10 @@ namespace dk {
 
 using namespace mk;
 
-constexpr int kStages = 9;
-constexpr int kMaxRows = 8;  // routed rows per expert: at most T <= 8
+constexpr int kStagesResident = 9;  // weight ring with all hidden rows resident (T <= 8)
+constexpr int kStagesGathered = 7;  // weight ring beside the gathered-row slots (8 < T <= 64)
+constexpr int kMaxRows = 8;         // routed rows per task (T <= 8, or 8-row passes)
+constexpr int kXSlots = 2;          // gathered hidden-row slots
 // The fetcher claims its next ticket once at most kReserve of its chunks are in flight: a
 // claim (ticket atomic, then the entry, then a gate/up task's tokens) takes about three L2
 // round trips, which this many chunks cover.
@@ -37,16 +39,18 @@ constexpr int kTaskConsumers = 2 + kComputeWarps;  // activation producer, publi
 constexpr int kPubSlots = 2 * kTaskSlots;
 constexpr int kMaxHSlots = 4;
 
-struct Smem {
-  uint8_t ring[kStages][kStageA];
+template <int S>
+struct SmemT {
+  uint8_t ring[S][kStageA];
   TaskEntry task[kTaskSlots];
   int task_tok[kTaskSlots][kMaxRows];  // token of each routed row of a gate/up task
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[S];
+  uint64_t empty[S];
   uint64_t task_full[kTaskSlots];
   uint64_t task_empty[kTaskSlots];
   uint64_t pub_full[kPubSlots];
-  uint64_t x_full;
+  uint64_t x_full[kXSlots];   // resident mode: [0] once; gathered mode: per slot
+  uint64_t x_empty[kXSlots];
   uint64_t h_full[kMaxHSlots];
   uint64_t h_empty[kMaxHSlots];
   int abort_flag;
@@ -54,22 +58,30 @@ struct Smem {
 
 constexpr int kSmemLimit = 227 * 1024;
 
-// Activation arena after Smem: FP16 hidden rows [T][xpitch], then `hslots` (2 to 4, as many
-// as fit) slots of h rows [T][hpitch]; the 16-byte pad per row keeps consecutive rows off the
-// same banks.
+template <bool kGather>
+__host__ __device__ inline size_t fixed_smem_bytes() {
+  return 1024 + ((sizeof(SmemT<kGather ? kStagesGathered : kStagesResident>) + 127) & ~size_t(127));
+}
+
+// Activation arena after the fixed part: the FP16 hidden rows -- all T rows [T][xpitch]
+// (resident mode), or kXSlots slots of one task's rows [8][xpitch] (gathered mode) -- then
+// `hslots` (2 to 4, as many as fit) slots of one down task's h rows [rows][hpitch]; the 16-byte
+// pad per row keeps consecutive rows off the same banks.
 struct Arena {
-  int xpitch, hpitch, x_bytes, slot_bytes, hslots;
+  int xpitch, hpitch, x_bytes, xslot_bytes, slot_bytes, hslots;
 };
 
-__host__ __device__ inline size_t fixed_smem_bytes() { return 1024 + ((sizeof(Smem) + 127) & ~size_t(127)); }
-
+template <bool kGather>
 __host__ __device__ inline Arena arena_of(int T, int d, int F) {
   Arena r;
+  const int rows = T < kMaxRows ? T : kMaxRows;
   r.xpitch = 2 * d + 16;
   r.hpitch = 2 * F + 16;
-  r.x_bytes = T * r.xpitch;
-  r.slot_bytes = T * r.hpitch;
-  const long long room = static_cast<long long>(kSmemLimit) - static_cast<long long>(fixed_smem_bytes()) - r.x_bytes;
+  r.xslot_bytes = rows * r.xpitch;
+  r.x_bytes = kGather ? kXSlots * r.xslot_bytes : T * r.xpitch;
+  r.slot_bytes = rows * r.hpitch;
+  const long long room =
+      static_cast<long long>(kSmemLimit) - static_cast<long long>(fixed_smem_bytes<kGather>()) - r.x_bytes;
   const long long fit = r.slot_bytes > 0 ? room / r.slot_bytes : 0;
   r.hslots = static_cast<int>(fit < kMaxHSlots ? fit : kMaxHSlots);
   return r;
@@ -112,6 +124,7 @@ __device__ __forceinline__ void task_of(const ExpertArgs& a, int i, const Ticket
   }
 }
 
+template <typename Smem>
 __device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int g, int& tok, int* status, long long limit) {
   const int q = n % kTaskSlots;
   const uint32_t ph = static_cast<uint32_t>((n / kTaskSlots) & 1);
@@ -151,6 +164,7 @@ __device__ __forceinline__ void chunk_mma(const ChunkCodes& cc, const uint8_t* b
 // (every later wait returns at once because the CTA's abort flag is raised).  The 16
 // k-steps of a chunk go to 8 independent accumulators, summed in a fixed order at the end.
 // `brow` is the thread's activation row (routed row g) in shared memory.
+template <int kStages, typename Smem>
 __device__ __forceinline__ bool run_task_chunks(Smem& sm, const ExpertArgs& a, int& stage, uint32_t& phase,
                                                 float (&acc)[8][4], int lra, int lrb, int nck, const uint8_t* brow,
                                                 bool live, int q, bool tr, int& tcnt) {
@@ -200,16 +214,21 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 using namespace dk;
 
-template <bool kFused>
+// kGather false: T <= 8, every token's hidden row resident (plan's task table, one pass per
+// expert, optionally the fused un-route); kGather true: 8 < T <= 64, each gate/up task's rows
+// gathered into one of kXSlots slots, task table of 8-row passes (built by dec_plan_kernel).
+template <bool kFused, bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_dec_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_w2,
                       const __grid_constant__ CUtensorMap tm_s13, const __grid_constant__ CUtensorMap tm_s2,
                       const __grid_constant__ ExpertArgs a) {
+  constexpr int kStages = kGather ? kStagesGathered : kStagesResident;
+  using Smem = SmemT<kStages>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* arena = reinterpret_cast<uint8_t*>(&sm) + ((sizeof(Smem) + 127) & ~size_t(127));
-  const Arena ar = arena_of(a.T, a.d, a.F);
-  uint8_t* xs = arena;                 // hidden rows
+  const Arena ar = arena_of<kGather>(a.T, a.d, a.F);
+  uint8_t* xs = arena;                 // hidden rows (resident) or the gathered-row slots
   uint8_t* hs = arena + ar.x_bytes;    // h slots
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int tcnt0 = 2;
@@ -225,7 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&sm.task_empty[i]), kTaskConsumers);
     }
     for (int i = 0; i < kPubSlots; ++i) mbar_init(smem_addr(&sm.pub_full[i]), kComputeWarps);
-    mbar_init(smem_addr(&sm.x_full), 1);
+    for (int i = 0; i < kXSlots; ++i) {
+      mbar_init(smem_addr(&sm.x_full[i]), 1);
+      mbar_init(smem_addr(&sm.x_empty[i]), kComputeWarps);
+    }
     for (int i = 0; i < kMaxHSlots; ++i) {
       mbar_init(smem_addr(&sm.h_full[i]), 1);
       mbar_init(smem_addr(&sm.h_empty[i]), kComputeWarps);
@@ -251,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------- task fetcher + weight producer -------------
     const uint64_t pol = policy_evict_first();
-    const int ngu = __ldg(a.meta + META_NGU), ndn = __ldg(a.meta + META_NDN);
+    const int ngu = __ldg(a.meta + (kGather ? META_DGU : META_NGU));
+    const int ndn = __ldg(a.meta + (kGather ? META_DDN : META_NDN));
     const TicketMap tmap = ticket_map(ngu, ndn, static_cast<int>(gridDim.x));
     const int ntot = ngu + tmap.ndn_tickets + (kFused ? a.ncb : 0);  // tickets
     const TaskEntry kEnd = TaskEntry{-1, 0, 0, 0};
@@ -379,26 +402,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------- activation producer: hidden rows once, h rows per down task -------------
-    if (lane == 0) mbar_arrive_expect_tx(smem_addr(&sm.x_full), static_cast<uint32_t>(a.T * 2 * a.d));
-    __syncwarp();
-    if (lane < a.T)
-      bulk_copy_g2s(smem_addr(xs + lane * ar.xpitch), a.x16 + static_cast<size_t>(lane) * a.d, 2 * a.d,
-                    smem_addr(&sm.x_full));
-    int n = 0, ndn = 0, unused_tok = 0;
+    // ------------- activation producer: hidden rows (all at once when resident, per gate/up
+    // task when gathered), h rows per down task -------------
+    if (!kGather) {
+      if (lane == 0) mbar_arrive_expect_tx(smem_addr(&sm.x_full[0]), static_cast<uint32_t>(a.T * 2 * a.d));
+      __syncwarp();
+      if (lane < a.T)
+        bulk_copy_g2s(smem_addr(xs + lane * ar.xpitch), a.x16 + static_cast<size_t>(lane) * a.d, 2 * a.d,
+                      smem_addr(&sm.x_full[0]));
+    }
+    int n = 0, ndn = 0, ngu = 0;
     while (true) {
       TaskEntry te;
-      if (!take_task(sm, n++, te, 0, unused_tok, a.status, a.wait_limit)) break;
+      int tok = 0;
+      if (!take_task(sm, n++, te, lane, tok, a.status, a.wait_limit)) break;
       if (te.x < 0) break;
       if (kFused && is_unroute(te)) continue;
-      if (((te.z >> 16) & 1) == 0) continue;  // gate/up: its rows are resident
+      if (((te.z >> 16) & 1) == 0) {
+        if (!kGather) continue;  // gate/up: its rows are resident
+        // gate/up: copy the task's routed rows (lane r: the row of token tok_r) into a slot
+        const int xslot = ngu % kXSlots;
+        if (!warp_wait(smem_addr(&sm.x_empty[xslot]), static_cast<uint32_t>(((ngu / kXSlots) & 1) ^ 1),
+                       &sm.abort_flag, a.status, a.wait_limit))
+          break;
+        const int rows = te.z & 0xffff;
+        if (lane == 0) mbar_arrive_expect_tx(smem_addr(&sm.x_full[xslot]), static_cast<uint32_t>(rows * 2 * a.d));
+        __syncwarp();
+        if (lane < rows)
+          bulk_copy_g2s(smem_addr(xs + xslot * ar.xslot_bytes + lane * ar.xpitch),
+                        a.x16 + static_cast<size_t>(tok) * a.d, 2 * a.d, smem_addr(&sm.x_full[xslot]));
+        ++ngu;
+        continue;
+      }
       const int slot = ndn % ar.hslots;
       const uint32_t use = static_cast<uint32_t>(ndn / ar.hslots);
       if (!warp_wait(smem_addr(&sm.h_empty[slot]), (use & 1u) ^ 1u, &sm.abort_flag, a.status, a.wait_limit)) break;
-      // every gate/up task (one pass, S_gu stripes) of this expert must have published its h rows
+      // every gate/up task (all passes, S_gu stripes each) of this expert must have published
+      // its h rows; the entry carries the pass count in bits 20+ (0: one pass)
       const int u = (te.x >> 16) & 0xffff, row0 = te.y, rows = te.z & 0xffff;
-      const bool good = warp_wait_counter(a.ready + u, static_cast<uint32_t>(a.S_gu), &sm.abort_flag, a.status,
-                                          a.wait_limit);
+      const int npass = max(1, (te.z >> 20) & 0xfff);
+      const bool good = warp_wait_counter(a.ready + u, static_cast<uint32_t>(npass * a.S_gu), &sm.abort_flag,
+                                          a.status, a.wait_limit);
       if (!good) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(smem_addr(&sm.h_full[slot]), static_cast<uint32_t>(rows * 2 * a.F));
@@ -412,7 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // drain: every copy this warp started has landed before the CTA exits
     if (lane == 0) {
-      drain_wait(smem_addr(&sm.x_full), 0);
+      if (!kGather) drain_wait(smem_addr(&sm.x_full[0]), 0);
+      for (int i = max(0, ngu - kXSlots); i < ngu; ++i)
+        drain_wait(smem_addr(&sm.x_full[i % kXSlots]), static_cast<uint32_t>((i / kXSlots) & 1));
       for (int i = max(0, ndn - ar.hslots); i < ndn; ++i)
         drain_wait(smem_addr(&sm.h_full[i % ar.hslots]), static_cast<uint32_t>((i / ar.hslots) & 1));
     }
@@ -444,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cw = warp - kFirstCompute;  // 0..7
     const int g = lane >> 2, q = lane & 3;
     const int fr = frag_row(g);
-    int stage = 0, n = 0, pub_n = 0, ndn = 0;
+    int stage = 0, n = 0, pub_n = 0, ndn = 0, ngu = 0;
     uint32_t phase = 0;
     bool ok = true, have_x = false;
     const bool tr = a.trace != nullptr && lane == 0 && (cw == 0 || cw == kComputeWarps - 1);
@@ -476,9 +522,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool live = g < rows;
       const uint8_t* brow;
       int slot = 0;
-      if (!is_dn) {
+      if (!is_dn && kGather) {
+        slot = ngu % kXSlots;
+        if (!warp_wait(smem_addr(&sm.x_full[slot]), static_cast<uint32_t>((ngu / kXSlots) & 1), &sm.abort_flag,
+                       a.status, a.wait_limit))
+          break;
+        brow = xs + slot * ar.xslot_bytes + g * ar.xpitch;
+      } else if (!is_dn) {
         if (!have_x) {
-          if (!warp_wait(smem_addr(&sm.x_full), 0u, &sm.abort_flag, a.status, a.wait_limit)) break;
+          if (!warp_wait(smem_addr(&sm.x_full[0]), 0u, &sm.abort_flag, a.status, a.wait_limit)) break;
           have_x = true;
         }
         brow = xs + (live ? tok : 0) * ar.xpitch;
@@ -493,8 +545,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lra = is_dn ? 16 * cw + fr : 8 * cw + fr;
       const int lrb = is_dn ? 16 * cw + 8 + fr : 64 + 8 * cw + fr;
       float acc[8][4];
-      ok = run_task_chunks(sm, a, stage, phase, acc, lra, lrb, nck, brow, live, q, tr && cw == 0, tcnt);
+      ok = run_task_chunks<kStages>(sm, a, stage, phase, acc, lra, lrb, nck, brow, live, q, tr && cw == 0, tcnt);
       if (!ok) break;
+      if (!is_dn && kGather) {
+        // the slot's hidden rows are consumed
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.x_empty[slot]));
+        ++ngu;
+      }
       if (is_dn) {
         // the slot's h rows are consumed
         __syncwarp();
@@ -544,22 +602,98 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Task table of the gathered mode: from the plan's per-expert arrays, passes of at most
+// kMaxRows routed rows (each its own weight pass), all gate/up tasks (touched order, pass,
+// stripe) then all down tasks; entry z carries the expert's pass count in bits 20+ for the
+// readiness target of its down tasks.  One CTA.
+__global__ void __launch_bounds__(1024) dec_plan_kernel(const int* meta_in, int* meta, const int* touched,
+                                                        const int* counts, const int* offsets, TaskEntry* tasks,
+                                                        int S_gu, int S_dn) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ int s_warp[32];
+  __shared__ int s_total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int U = __ldcg(meta_in + META_U);
+  int e = 0, m = 0, np = 0;
+  if (tid < U) {
+    e = __ldcg(touched + tid);
+    m = __ldcg(counts + e);
+    np = (m + kMaxRows - 1) / kMaxRows;
+  }
+  int incl = np;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = s_warp[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    s_warp[lane] = wi - w;
+    if (lane == 31) s_total = wi;
+  }
+  __syncthreads();
+  const int before = s_warp[warp] + incl - np;
+  const int total = s_total;
+  if (tid < U) {
+    const int base = __ldcg(offsets + e);
+    int gi = before * S_gu;
+    int di = total * S_gu + before * S_dn;
+    for (int p = 0; p < np; ++p) {
+      const int rows = min(kMaxRows, m - p * kMaxRows);
+      const int z = rows | (np > 1 ? 1 << 17 : 0) | (np << 20);
+      const int row0 = base + p * kMaxRows;
+      for (int s2 = 0; s2 < S_gu; ++s2) tasks[gi++] = TaskEntry{e | (tid << 16), row0, z, s2};
+      for (int s2 = 0; s2 < S_dn; ++s2) tasks[di++] = TaskEntry{e | (tid << 16), row0, z | (1 << 16), s2};
+    }
+  }
+  if (tid == 0) {
+    meta[META_DGU] = total * S_gu;
+    meta[META_DDN] = total * S_dn;
+  }
+}
+
+// T at or below which every token's hidden row stays resident; above it (up to kMaxGatherT)
+// each gate/up task's rows are gathered.
+constexpr int kMaxGatherT = 64;
+
 size_t expert_dec_smem_bytes(int T, int d, int F) {
-  const Arena ar = arena_of(T, d, F);
-  return fixed_smem_bytes() + ar.x_bytes + static_cast<size_t>(ar.hslots) * ar.slot_bytes;
+  if (T <= kMaxRows) {
+    const Arena ar = arena_of<false>(T, d, F);
+    return fixed_smem_bytes<false>() + ar.x_bytes + static_cast<size_t>(ar.hslots) * ar.slot_bytes;
+  }
+  const Arena ar = arena_of<true>(T, d, F);
+  return fixed_smem_bytes<true>() + ar.x_bytes + static_cast<size_t>(ar.hslots) * ar.slot_bytes;
 }
 
 bool expert_dec_supports(int T, int d, int F) {
-  return T >= 1 && T <= kMaxRows && expert_mma_supports(d, F) && arena_of(T, d, F).hslots >= 2 &&
-         expert_dec_smem_bytes(T, d, F) <= static_cast<size_t>(kSmemLimit);
+  if (T < 1 || T > kMaxGatherT || !expert_mma_supports(d, F)) return false;
+  const int hslots = T <= kMaxRows ? arena_of<false>(T, d, F).hslots : arena_of<true>(T, d, F).hslots;
+  return hslots >= 2 && expert_dec_smem_bytes(T, d, F) <= static_cast<size_t>(kSmemLimit);
+}
+
+bool expert_dec_gathers(int T) { return T > kMaxRows; }
+
+cudaError_t launch_dec_plan(const ExpertArgs& a, TaskEntry* tasks_d, cudaStream_t stream) {
+  return launch_pdl(dec_plan_kernel, dim3(1), dim3(1024), 0, stream, a.meta, const_cast<int*>(a.meta), a.touched,
+                    a.counts, a.offsets, tasks_d, a.S_gu, a.S_dn);
 }
 
 cudaError_t launch_expert_dec(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
                               const CUtensorMap& tm_s13, const CUtensorMap& tm_s2, int num_sms,
                               cudaStream_t stream) {
   const size_t smem = expert_dec_smem_bytes(a.T, a.d, a.F);
-  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const ExpertArgs) =
-      a.ncb > 0 ? expert_dec_kernel<true> : expert_dec_kernel<false>;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const ExpertArgs);
+  if (a.T > kMaxRows) kern = expert_dec_kernel<false, true>;  // the un-route is fused for T <= 8 only
+  else kern = a.ncb > 0 ? expert_dec_kernel<true, false> : expert_dec_kernel<false, false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   return launch_pdl(kern, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, tm_s13, tm_s2, a);

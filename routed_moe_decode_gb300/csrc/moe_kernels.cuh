@@ -315,6 +315,10 @@ cudaError_t launch_expert_dec(const ExpertArgs& a, const CUtensorMap& tm_w13, co
                               cudaStream_t stream);
 bool expert_dec_supports(int T, int d, int F);
 size_t expert_dec_smem_bytes(int T, int d, int F);
+// true when the decode kernel gathers each task's hidden rows (T > 8): it then reads its own
+// task table of 8-row passes, built from the plan by launch_dec_plan into tasks_d
+bool expert_dec_gathers(int T);
+cudaError_t launch_dec_plan(const ExpertArgs& a, TaskEntry* tasks_d, cudaStream_t stream);
 // number of un-route tasks the decode kernel appends when it runs the un-route itself
 int expert_mma_unroute_tasks(int T, int S_dn);
 int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes);
