@@ -125,8 +125,10 @@ MOE_API const char* moe_last_cuda_error(void);
  * It must be 256-byte aligned.  Pure host function: needs no GPU. */
 MOE_API size_t moe_workspace_bytes(const moe_shape* shape);
 
-/* Zero the status word of a freshly allocated workspace (enqueued on `stream`).  Call once
- * after allocation; every other field is (re)written by moe_plan / moe_forward. */
+/* Zero the status block and the decode kernel's two counter sets (the first 8960 bytes, or
+ * all of a smaller buffer) of a freshly allocated workspace (enqueued on `stream`).  Call
+ * once after allocation; every other field is (re)written by moe_plan / moe_forward, and the
+ * counter sets are left zeroed by every call that uses them. */
 MOE_API int moe_workspace_init(void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /* Check a shape without touching the GPU: MOE_OK, MOE_ERR_INVALID_ARG or
@@ -226,9 +228,13 @@ MOE_API int moe_front(const moe_shape* shape, const float* logits, const void* h
                       float* weights, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /* Whole layer: router, plan and forward on one stream, with ids/weights written to the
- * caller's [T, k] buffers.  For T * k up to 16384 the router, the FP16 staging of hidden
- * and the plan run as one fused launch (moe_front); moe_layer is moe_front followed by
- * moe_forward_experts with MOE_ALGO_AUTO. */
+ * caller's [T, k] buffers.  For T <= 8 (T * k <= 256, E <= 1024) where MOE_ALGO_AUTO picks
+ * the warp-MMA decode kernel, the whole layer is ONE launch: every CTA of the decode kernel
+ * routes the T tokens and builds the plan in shared memory before its weight stream starts
+ * (results identical to the split steps), and the routing, the plan and the FP16 hidden rows
+ * are still written into the workspace for later calls.  Otherwise, for T * k up to 16384
+ * the router, the FP16 staging of hidden and the plan run as one fused launch (moe_front),
+ * and moe_layer is moe_front followed by moe_forward_experts with MOE_ALGO_AUTO. */
 MOE_API int moe_layer(const moe_shape* shape, const float* logits, const void* hidden,
               const uint8_t* w13_codes, const uint8_t* w13_scales, float w13_scale,
               const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,

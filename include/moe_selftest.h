@@ -39,8 +39,8 @@ MOE_API int moe_selftest_mma(const void* A, const void* B, float* D, moe_stream_
 
 /* The expert kernel and the un-route kernel exactly as moe_forward_experts runs them with
  * MOE_ALGO_AUTO (after moe_plan and moe_forward_prepare), with a timeline recorded into
- * `trace`: per CTA 8 roles x 128 uint64 events (event code << 56 | index << 40 | low 40
- * bits of %globaltimer in ns); zero-initialise the buffer (multiProcessorCount x 8192 bytes).
+ * `trace`: per CTA 8 roles x 256 uint64 events (event code << 56 | index << 40 | low 40
+ * bits of %globaltimer in ns); zero-initialise the buffer (multiProcessorCount x 16384 bytes).
  * Warp-MMA kernel: role 0 weight producer (1 task published, 2 chunk issued), 1 activation
  * producer (3 readiness met, 4 chunk issued), 2 and 3 first and last compute warp (5 task
  * taken, index bit 15 = down task; 6 chunks done; 12 un-route wait begins, 13 wait met),
@@ -56,6 +56,19 @@ MOE_API int moe_selftest_expert_trace(const moe_shape* shape, const uint8_t* w13
                                       float w2_scale, const void* residual, void* out,
                                       void* workspace, size_t workspace_bytes,
                                       unsigned long long* trace, moe_stream_t stream);
+
+/* moe_layer with the same timeline as moe_selftest_expert_trace recorded by its expert
+ * kernel.  For T <= 8 that is the one-launch layer, whose prologue routes and plans: role 5
+ * event 10 is then taken after that prologue, and it adds role 6 events 16 (token 0 routed),
+ * 18 (routes in shared memory), 19 (route positions done), role 7 event 17 (hidden rows
+ * converted), and role 0 events 20 (first task entry and tokens known), 21 (first task slot
+ * free), 22 / 23 (before / after the first weight copy is issued). */
+MOE_API int moe_selftest_layer_trace(const moe_shape* shape, const float* logits, const void* hidden,
+                                     const uint8_t* w13_codes, const uint8_t* w13_scales, float w13_scale,
+                                     const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+                                     const void* residual, void* out, int32_t* ids, float* weights,
+                                     void* workspace, size_t workspace_bytes, unsigned long long* trace,
+                                     moe_stream_t stream);
 
 /* The failure path of the expert kernels' bounded waits, for tests.  After moe_front (or
  * moe_route_topk + moe_plan + moe_forward_prepare) has left a plan in `workspace`, the down task

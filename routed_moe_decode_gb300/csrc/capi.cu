@@ -1,6 +1,7 @@
 // Host entry points of the C ABI declared in include/moe.h.
 #include <cuda.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -232,7 +233,7 @@ size_t moe_workspace_bytes(const moe_shape* shape) {
 
 int moe_workspace_init(void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return MOE_ERR_WORKSPACE;
-  cudaError_t e = cudaMemsetAsync(workspace, 0, 256, stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, std::min(workspace_bytes, moe::kZeroedPrefix), stream);
   if (e != cudaSuccess) { set_error("cudaMemsetAsync", e); return MOE_ERR_CUDA; }
   return MOE_OK;
 }
@@ -321,7 +322,8 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
                                 unsigned long long* trace, moe_stream_t stream, ExpertRange r,
                                 int stages = kStageExperts | kStageUnroute,
                                 long long wait_limit = moe::kDefaultWaitLimit, int poison_dn_task = -1,
-                                const float* w13_ts_e = nullptr, const float* w2_ts_e = nullptr) {
+                                const float* w13_ts_e = nullptr, const float* w2_ts_e = nullptr,
+                                const moe::DecFront* own_front = nullptr) {
   int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   if (shape->T == 0) return MOE_OK;
@@ -409,7 +411,11 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     a.ncb = (stages & kStageUnroute) ? moe::expert_mma_unroute_tasks(shape->T, L.S_dn) : 0;
     // up to 64 tokens: the decode kernel with the hidden rows in shared memory (all of them
     // for <= 8 tokens; per task, from its own table of 8-row passes, above)
-    if (moe::expert_dec_supports(shape->T, shape->d, shape->ffn)) {
+    if (own_front) {
+      // the layer in one launch: the decode kernel routes and plans for itself
+      e = moe::launch_expert_dec_front(a, *own_front, tm13, tm2, ts13, ts2, di.num_sms, stream);
+      if (e != cudaSuccess) { set_error("expert_dec (own front) launch", e); return MOE_ERR_CUDA; }
+    } else if (moe::expert_dec_supports(shape->T, shape->d, shape->ffn)) {
       moe::ExpertArgs ad = a;
       if (moe::expert_dec_gathers(shape->T)) {
         moe::TaskEntry* tasks_d = at<moe::TaskEntry>(workspace, L.tasks_d);
@@ -592,6 +598,59 @@ int moe_front(const moe_shape* shape, const float* logits, const void* hidden, i
   return front_impl(shape, logits, hidden, ids, weights, workspace, workspace_bytes, all_experts(shape), stream);
 }
 
+// Whether a whole layer runs as one launch of the decode kernel with its own front: at most
+// eight tokens (un-route fused), all experts, the warp-MMA path chosen by MOE_ALGO_AUTO.
+static bool use_own_front(const moe_shape* s, ExpertRange r) {
+  return r.lo == 0 && r.hi == s->E && s->T >= 1 && auto_choice(s) == MOE_ALGO_MMA &&
+         moe::expert_mma_unroute_tasks(s->T, moe::ws_layout(*s).S_dn) > 0 &&
+         moe::expert_dec_front_supports(s->T, s->d, s->ffn, s->E, s->k);
+}
+
+// Router, plan and forward of a layer: one launch when use_own_front holds, else the fused
+// front (or its separate steps) followed by the expert kernels.
+static int layer_steps(const moe_shape* shape, const float* logits, const void* hidden, const uint8_t* w13_codes,
+                       const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales,
+                       float w2_scale, const void* residual, void* out, int32_t* ids, float* weights,
+                       void* workspace, size_t workspace_bytes, ExpertRange r, moe_stream_t stream,
+                       const float* w13_ts_e = nullptr, const float* w2_ts_e = nullptr,
+                       unsigned long long* trace = nullptr) {
+  if (use_own_front(shape, r)) {
+    if (!logits || !hidden || !ids || !weights || !aligned(logits, 16) || !aligned(hidden, 16) || !aligned(ids, 4) ||
+        !aligned(weights, 4))
+      return MOE_ERR_INVALID_ARG;
+    const int rc = check_ws(shape, workspace, workspace_bytes);
+    if (rc != MOE_OK) return rc;
+    const WsLayout L = moe::ws_layout(*shape);
+    moe::DecFront f{};
+    f.logits = logits;
+    f.hidden = static_cast<const __nv_bfloat16*>(hidden);
+    f.ids = ids;
+    f.weights = weights;
+    f.meta = at<int>(workspace, L.meta);
+    f.counts = at<int>(workspace, L.counts);
+    f.offsets = at<int>(workspace, L.offsets);
+    f.touched = at<int>(workspace, L.touched);
+    f.gu_start = at<int>(workspace, L.gu_start);
+    f.dn_start = at<int>(workspace, L.dn_start);
+    f.route_pos = at<int>(workspace, L.route_pos);
+    f.pos_tok = at<int>(workspace, L.pos_tok);
+    f.route_w = at<float>(workspace, L.route_w);
+    f.tasks = at<moe::TaskEntry>(workspace, L.tasks);
+    f.x16 = at<__half>(workspace, L.x16);
+    f.sets = at<uint32_t>(workspace, L.dec_sets);
+    f.parity = at<uint32_t>(workspace, L.dec_parity);
+    f.done = at<uint32_t>(workspace, L.dec_done);
+    return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual,
+                                out, workspace, workspace_bytes, MOE_ALGO_AUTO, trace, stream, r,
+                                kStageExperts | kStageUnroute, moe::kDefaultWaitLimit, -1, w13_ts_e, w2_ts_e, &f);
+  }
+  const int rc = front_impl(shape, logits, hidden, ids, weights, workspace, workspace_bytes, r, stream);
+  if (rc != MOE_OK) return rc;
+  return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
+                              workspace, workspace_bytes, MOE_ALGO_AUTO, trace, stream, r,
+                              kStageExperts | kStageUnroute, moe::kDefaultWaitLimit, -1, w13_ts_e, w2_ts_e);
+}
+
 static int layer_impl(const moe_shape* shape, const float* logits, const void* hidden, const uint8_t* w13_codes,
                       const uint8_t* w13_scales, float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales,
                       float w2_scale, const void* residual, void* out, int32_t* ids, float* weights, void* workspace,
@@ -600,10 +659,8 @@ static int layer_impl(const moe_shape* shape, const float* logits, const void* h
   if (rc != MOE_OK) return rc;
   if (shape->T == 0) return MOE_OK;
   if (!w13_codes || !w13_scales || !w2_codes || !w2_scales || !out) return MOE_ERR_INVALID_ARG;
-  rc = front_impl(shape, logits, hidden, ids, weights, workspace, workspace_bytes, r, stream);
-  if (rc != MOE_OK) return rc;
-  return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
-                              workspace, workspace_bytes, MOE_ALGO_AUTO, nullptr, stream, r);
+  return layer_steps(shape, logits, hidden, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale,
+                     residual, out, ids, weights, workspace, workspace_bytes, r, stream);
 }
 
 int moe_layer(const moe_shape* shape, const float* logits, const void* hidden, const uint8_t* w13_codes,
@@ -708,11 +765,23 @@ int moe_layer_expert_scales(const moe_shape* shape, const float* logits, const v
   if (!w13_codes || !w13_scales || !w2_codes || !w2_scales || !out || !w13_scales_e || !w2_scales_e ||
       !aligned(w13_scales_e, 4) || !aligned(w2_scales_e, 4))
     return MOE_ERR_INVALID_ARG;
-  rc = front_impl(shape, logits, hidden, ids, weights, workspace, workspace_bytes, all_experts(shape), stream);
+  return layer_steps(shape, logits, hidden, w13_codes, w13_scales, 1.f, w2_codes, w2_scales, 1.f, residual, out, ids,
+                     weights, workspace, workspace_bytes, all_experts(shape), stream, w13_scales_e, w2_scales_e);
+}
+
+int moe_selftest_layer_trace(const moe_shape* shape, const float* logits, const void* hidden,
+                             const uint8_t* w13_codes, const uint8_t* w13_scales, float w13_scale,
+                             const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale, const void* residual,
+                             void* out, int32_t* ids, float* weights, void* workspace, size_t workspace_bytes,
+                             unsigned long long* trace, moe_stream_t stream) {
+  if (!trace) return MOE_ERR_INVALID_ARG;
+  int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
-  return forward_experts_impl(shape, w13_codes, w13_scales, 1.f, w2_codes, w2_scales, 1.f, residual, out, workspace,
-                              workspace_bytes, MOE_ALGO_AUTO, nullptr, stream, all_experts(shape),
-                              kStageExperts | kStageUnroute, moe::kDefaultWaitLimit, -1, w13_scales_e, w2_scales_e);
+  if (shape->T == 0) return MOE_OK;
+  if (!w13_codes || !w13_scales || !w2_codes || !w2_scales || !out) return MOE_ERR_INVALID_ARG;
+  return layer_steps(shape, logits, hidden, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale,
+                     residual, out, ids, weights, workspace, workspace_bytes, all_experts(shape), stream, nullptr,
+                     nullptr, trace);
 }
 
 int moe_read_device_status(const void* workspace, int clear, uint32_t* status_bits, moe_stream_t stream) {

@@ -20,6 +20,7 @@
 // fused, trailing un-route tasks (one token's 128 columns of a stripe per compute warp)
 // once the stripe's down tasks have been released.
 #include "mma_parts.cuh"
+#include "route_select.cuh"
 
 namespace moe {
 
@@ -71,8 +72,23 @@ struct Arena {
   int xpitch, hpitch, x_bytes, xslot_bytes, slot_bytes, hslots;
 };
 
+// The plan of the kernel's own front (T <= 8 tokens, at most 256 routes), after the h slots.
+constexpr int kFrontRoutes = 256;
+struct FrontSmem {
+  int ids[kFrontRoutes];      // route t * k + j -> expert
+  float w[kFrontRoutes];      // route -> renormalised weight
+  int pos[kFrontRoutes];      // route -> position in expert-major order
+  int pos_tok[kFrontRoutes];  // position -> token
+  int first[kFrontRoutes];    // route -> its expert if it is the expert's first route, else a sentinel
+  int touched[kFrontRoutes];  // touched index -> expert (ascending)
+  int ucnt[kFrontRoutes];     // touched index -> routes of the expert
+  int uoff[kFrontRoutes];     // touched index -> first position of its bucket
+  int U;
+  uint32_t parity;
+};
+
 template <bool kGather>
-__host__ __device__ inline Arena arena_of(int T, int d, int F) {
+__host__ __device__ inline Arena arena_of(int T, int d, int F, int extra = 0) {
   Arena r;
   const int rows = T < kMaxRows ? T : kMaxRows;
   r.xpitch = 2 * d + 16;
@@ -81,7 +97,7 @@ __host__ __device__ inline Arena arena_of(int T, int d, int F) {
   r.x_bytes = kGather ? kXSlots * r.xslot_bytes : T * r.xpitch;
   r.slot_bytes = rows * r.hpitch;
   const long long room =
-      static_cast<long long>(kSmemLimit) - static_cast<long long>(fixed_smem_bytes<kGather>()) - r.x_bytes;
+      static_cast<long long>(kSmemLimit) - static_cast<long long>(fixed_smem_bytes<kGather>()) - r.x_bytes - extra;
   const long long fit = r.slot_bytes > 0 ? room / r.slot_bytes : 0;
   r.hslots = static_cast<int>(fit < kMaxHSlots ? fit : kMaxHSlots);
   return r;
@@ -119,6 +135,33 @@ __device__ __forceinline__ void task_of(const ExpertArgs& a, int i, const Ticket
     two = true;
   } else if (i < m.ngu + m.ndn_tickets) {
     e0 = a.tasks[i + m.npair];
+  } else {
+    e0 = TaskEntry{0, 0, 1 << 18, i - m.ngu - m.ndn_tickets};
+  }
+}
+
+// Entry i of the plan's task order from the kernel's own plan: gate/up tasks (touched order,
+// stripe), then down tasks (touched order, stripe); one pass per expert (at most 8 rows).
+__device__ __forceinline__ TaskEntry front_entry(const FrontSmem& fs, int i, int ngu, int S_gu, int S_dn) {
+  const bool dn = i >= ngu;
+  const int j = dn ? i - ngu : i;
+  const int S = dn ? S_dn : S_gu;
+  const int u = j / S;
+  return TaskEntry{fs.touched[u] | (u << 16), fs.uoff[u], fs.ucnt[u] | (dn ? 1 << 16 : 0), j - u * S};
+}
+
+__device__ __forceinline__ void front_task_of(const FrontSmem& fs, int i, const TicketMap& m, int S_gu, int S_dn,
+                                              TaskEntry& e0, TaskEntry& e1, bool& two) {
+  two = false;
+  if (i < m.ngu) {
+    e0 = front_entry(fs, i, m.ngu, S_gu, S_dn);
+  } else if (i < m.ngu + m.npair) {
+    const int j = m.ngu + 2 * (i - m.ngu);
+    e0 = front_entry(fs, j, m.ngu, S_gu, S_dn);
+    e1 = front_entry(fs, j + 1, m.ngu, S_gu, S_dn);
+    two = true;
+  } else if (i < m.ngu + m.ndn_tickets) {
+    e0 = front_entry(fs, i + m.npair, m.ngu, S_gu, S_dn);
   } else {
     e0 = TaskEntry{0, 0, 1 << 18, i - m.ngu - m.ndn_tickets};
   }
@@ -214,22 +257,69 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 using namespace dk;
 
+// This CTA's share (grid-strided by warp lanes) of the workspace copy of the kernel's own
+// plan: the arrays the plan kernel writes, in its layout, for at most 8 rows per expert (one
+// pass each), so that later calls on the same workspace find the plan of this layer.
+__device__ __forceinline__ void write_front_plan(const ExpertArgs& a, const DecFront& f, const FrontSmem& fs, int U) {
+  const int lane = threadIdx.x & 31;
+  const int stride = static_cast<int>(gridDim.x) * 32, first = static_cast<int>(blockIdx.x) * 32 + lane;
+  const int E = a.E, R = a.T * a.k;
+  const int ngu = U * a.S_gu, ntask = U * (a.S_gu + a.S_dn);
+  for (int e = first; e <= E; e += stride) {
+    // bucket start: the routes to lower experts; count: the routes to e
+    int off = 0, cnt = 0;
+    for (int u = 0; u < U; ++u) {
+      const int x = fs.touched[u];
+      off += x < e ? fs.ucnt[u] : 0;
+      cnt += x == e ? fs.ucnt[u] : 0;
+    }
+    f.offsets[e] = off;
+    if (e < E) f.counts[e] = cnt;
+  }
+  for (int u = first; u <= U; u += stride) {
+    if (u < U) f.touched[u] = fs.touched[u];
+    f.gu_start[u] = u * a.S_gu;
+    f.dn_start[u] = u * a.S_dn;
+  }
+  for (int r = first; r < R; r += stride) {
+    f.route_pos[r] = fs.pos[r];
+    f.pos_tok[r] = fs.pos_tok[r];
+    f.route_w[r] = fs.w[r];
+  }
+  for (int i = first; i < ntask; i += stride) f.tasks[i] = front_entry(fs, i, ngu, a.S_gu, a.S_dn);
+  if (blockIdx.x == 0 && lane == 0) {
+    int mx = 0;
+    for (int u = 0; u < U; ++u) mx = max(mx, fs.ucnt[u]);
+    f.meta[META_U] = U;
+    f.meta[META_NGU] = ngu;
+    f.meta[META_NDN] = U * a.S_dn;
+    f.meta[META_MAXROWS] = mx;
+    f.meta[META_YFMT] = 0;
+  }
+}
+
 // kGather false: T <= 8, every token's hidden row resident (plan's task table, one pass per
 // expert, optionally the fused un-route); kGather true: 8 < T <= 64, each gate/up task's rows
 // gathered into one of kXSlots slots, task table of 8-row passes (built by dec_plan_kernel).
-template <bool kFused, bool kGather>
+// kNpl > 0 (T <= 8, un-route fused): the kernel's own front, with kNpl logits per lane in
+// the router (E <= 32 kNpl); the plan comes from shared memory, the counters from the set
+// `f.parity` selects.
+template <bool kFused, bool kGather, int kNpl>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_dec_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_w2,
                       const __grid_constant__ CUtensorMap tm_s13, const __grid_constant__ CUtensorMap tm_s2,
-                      const __grid_constant__ ExpertArgs a) {
+                      const __grid_constant__ ExpertArgs a, const __grid_constant__ DecFront f) {
+  constexpr bool kFront = kNpl > 0;
+  static_assert(!kFront || (kFused && !kGather), "the own front is for the resident, fused variant");
   constexpr int kStages = kGather ? kStagesGathered : kStagesResident;
   using Smem = SmemT<kStages>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* arena = reinterpret_cast<uint8_t*>(&sm) + ((sizeof(Smem) + 127) & ~size_t(127));
-  const Arena ar = arena_of<kGather>(a.T, a.d, a.F);
+  const Arena ar = arena_of<kGather>(a.T, a.d, a.F, kFront ? static_cast<int>(sizeof(FrontSmem)) : 0);
   uint8_t* xs = arena;                 // hidden rows (resident) or the gathered-row slots
   uint8_t* hs = arena + ar.x_bytes;    // h slots
+  FrontSmem& fs = *reinterpret_cast<FrontSmem*>(hs + ar.hslots * ar.slot_bytes);  // kFront only
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int tcnt0 = 2;
   if (tid == 0) trace_ev(a, 5, tcnt0, 14, 0);  // kernel entry, before the dependency wait
@@ -262,10 +352,99 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_s2);
   }
   // everything above is local to the CTA; the plan, the counters and the FP16 hidden rows
-  // come from the preceding kernel
+  // come from the preceding kernel (kFront: the logits, the hidden rows and the counter set)
   pdl_wait();
   pdl_launch_dependents();
-  __syncthreads();
+  uint32_t* ctr_ready = a.ready;
+  uint32_t* ctr_dn = a.dn_done;
+  uint32_t* ctr_ticket = a.ticket;
+  int front_U = 0;
+  if constexpr (kFront) {
+    // ---- the kernel's own front: route, FP16 hidden rows, plan (every CTA the same) ----
+    const int T = a.T, k = a.k, R = T * k;
+    if (tid == 0) fs.parity = __ldcg(f.parity) & 1u;
+    int pcnt = 0;
+    if (warp < T) {
+      route_token<kNpl>(f.logits, warp, a.E, k, blockIdx.x == 0 ? f.ids : nullptr, f.weights, fs.ids, fs.w, warp);
+      if (tid == 0) trace_ev(a, 6, pcnt, 16, 0);  // token 0 routed
+    } else {
+      // hidden rows -> FP16 into the resident rows (CTA 0: also the workspace copy)
+      const int n8 = T * a.d / 8, per_row = a.d / 8;
+      bool bad = false;
+      for (int i = tid - 32 * T; i < n8; i += kThreads - 32 * T) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(f.hidden) + i);
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        uint4 o;
+        __half2* h = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 v = __bfloat1622float2(b[q]);
+          bad |= !(fabsf(v.x) <= 65504.f) || !(fabsf(v.y) <= 65504.f);
+          h[q] = __floats2half2_rn(v.x, v.y);
+        }
+        const int t = i / per_row, c8 = i - t * per_row;
+        *reinterpret_cast<uint4*>(xs + t * ar.xpitch + 16 * c8) = o;
+        if (blockIdx.x == 0) reinterpret_cast<uint4*>(f.x16)[i] = o;
+      }
+      if (bad && blockIdx.x == 0) atomicOr(a.status, static_cast<int>(MOE_DEV_HIDDEN_RANGE));
+      if (tid == 32 * T) trace_ev(a, 7, pcnt, 17, 0);  // first converter's rows done
+    }
+    // pad the route ids to a multiple of 4 with a sentinel above every expert id
+    if (tid >= R && tid < ((R + 3) & ~3)) fs.ids[tid] = 0x7fffffff;
+    __syncthreads();
+    if (tid == 0) trace_ev(a, 6, pcnt, 18, 0);
+    const uint32_t par = fs.parity;
+    ctr_ready = f.sets + par * kDecSetWords;
+    ctr_dn = ctr_ready + kDecReadyWords;
+    ctr_ticket = ctr_ready + kDecTicketWord;
+    if (blockIdx.x == 0) {
+      // the other set, for the next launch (no CTA of this one touches it)
+      uint32_t* other = f.sets + (par ^ 1u) * kDecSetWords;
+      for (int i = tid; i < kDecSetWords; i += kThreads) other[i] = 0u;
+    }
+    // route r: its bucket's first position (routes to lower experts), its rank among the
+    // routes to the same expert (route order), the bucket size
+    const int R4 = (R + 3) >> 2;
+    int e = 0, rank = 0, off = 0, cnt = 0;
+    if (tid < R) {
+      e = fs.ids[tid];
+      const int4* ids4 = reinterpret_cast<const int4*>(fs.ids);
+#pragma unroll 4
+      for (int q = 0; q < R4; ++q) {
+        const int4 x = ids4[q];
+        const int r0 = 4 * q;
+        off += (x.x < e) + (x.y < e) + (x.z < e) + (x.w < e);
+        cnt += (x.x == e) + (x.y == e) + (x.z == e) + (x.w == e);
+        rank += (x.x == e && r0 < tid) + (x.y == e && r0 + 1 < tid) + (x.z == e && r0 + 2 < tid) +
+                (x.w == e && r0 + 3 < tid);
+      }
+      fs.pos[tid] = off + rank;
+      fs.pos_tok[off + rank] = tid / k;
+      fs.first[tid] = rank == 0 ? e : 0x7fffffff;  // the expert, at its first route only
+    } else if (tid < 4 * R4) {
+      fs.first[tid] = 0x7fffffff;
+    }
+    const int U = __syncthreads_count(tid < R && rank == 0);
+    if (tid == 0) trace_ev(a, 6, pcnt, 19, 0);
+    if (tid < R && rank == 0) {
+      // touched index: the distinct experts below e
+      const int4* first4 = reinterpret_cast<const int4*>(fs.first);
+      int u = 0;
+#pragma unroll 4
+      for (int q = 0; q < R4; ++q) {
+        const int4 x = first4[q];
+        u += (x.x < e) + (x.y < e) + (x.z < e) + (x.w < e);
+      }
+      fs.touched[u] = e;
+      fs.ucnt[u] = cnt;
+      fs.uoff[u] = off;
+    }
+    if (tid == 0) fs.U = U;
+    __syncthreads();
+    front_U = U;
+  } else {
+    __syncthreads();
+  }
   const uint32_t ring0 = smem_addr(&sm.ring[0][0]);
   int tcnt = 0;
   if (tid == 0) trace_ev(a, 5, tcnt, 10, 0);
@@ -273,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------- task fetcher + weight producer -------------
     const uint64_t pol = policy_evict_first();
-    const int ngu = __ldg(a.meta + (kGather ? META_DGU : META_NGU));
-    const int ndn = __ldg(a.meta + (kGather ? META_DDN : META_NDN));
+    const int ngu = kFront ? front_U * a.S_gu : __ldg(a.meta + (kGather ? META_DGU : META_NGU));
+    const int ndn = kFront ? front_U * a.S_dn : __ldg(a.meta + (kGather ? META_DDN : META_NDN));
     const TicketMap tmap = ticket_map(ngu, ndn, static_cast<int>(gridDim.x));
     const int ntot = ngu + tmap.ndn_tickets + (kFused ? a.ncb : 0);  // tickets
     const TaskEntry kEnd = TaskEntry{-1, 0, 0, 0};
@@ -284,16 +463,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     TaskEntry entry = kEnd, entry2 = kEnd;
     bool pair = false;  // entry2 is the second down task of the claimed ticket
     if (lane == 0) {
-      if (cur < ntot) task_of(a, cur, tmap, entry, entry2, pair);
-      else entry = kEnd;
+      if (cur >= ntot) entry = kEnd;
+      else if (kFront) front_task_of(fs, cur, tmap, a.S_gu, a.S_dn, entry, entry2, pair);
+      else task_of(a, cur, tmap, entry, entry2, pair);
     }
     // the tokens of a gate/up task's routed rows, loaded as soon as its entry is known
     auto load_tokens = [&]() {
       const int ey = __shfl_sync(0xffffffffu, entry.y, 0), ez = __shfl_sync(0xffffffffu, entry.z, 0);
       const bool gu = __shfl_sync(0xffffffffu, cur, 0) < ngu;
-      return (gu && lane < (ez & 0xffff)) ? __ldg(a.pos_tok + ey + lane) : 0;
+      if (!gu || lane >= (ez & 0xffff)) return 0;
+      return kFront ? fs.pos_tok[ey + lane] : __ldg(a.pos_tok + ey + lane);
     };
     int tok = load_tokens();
+    if (lane == 0 && kFront) trace_ev(a, 0, tcnt, 20, 0);  // first entry and tokens known
     bool ok = true;
     while (ok) {
       const int q = n % kTaskSlots;
@@ -302,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
+      if (lane == 0 && kFront && n == 0) trace_ev(a, 0, tcnt, 21, 0);
       const bool live = __shfl_sync(0xffffffffu, cur, 0) < ntot;
       // publish the entry (and the tokens, whose load may still be in flight) to the other
       // roles: after the task's first chunk has been issued -- its stage is freed by earlier,
@@ -351,8 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           const uint32_t sb = ring0 + stage * kStageA;
           const uint32_t fa = smem_addr(&sm.full[stage]);
+          if (kFront && chunk_seq == 0) trace_ev(a, 0, tcnt, 22, 0);
           mbar_arrive_expect_tx(fa, kStageA);
           tma_load_2d(sb, tm, c * (kChunk / 2), rA0, fa, pol);
+          if (kFront && chunk_seq == 0) trace_ev(a, 0, tcnt, 23, 0);
           tma_load_2d(sb + kCodeBytes / 2, tm, c * (kChunk / 2), rA1, fa, pol);
           tma_load_2d(sb + kCodeBytes, tms, c * (kChunk / 16), rA0, fa, pol);
           tma_load_2d(sb + kCodeBytes + kScaleBytes / 2, tms, c * (kChunk / 16), rA1, fa, pol);
@@ -386,9 +571,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (lane == 0) {
-        cur = static_cast<int>(atomicAdd(a.ticket, 1u)) + static_cast<int>(gridDim.x);
-        if (cur < ntot) task_of(a, cur, tmap, entry, entry2, pair);
-        else entry = kEnd;
+        cur = static_cast<int>(atomicAdd(ctr_ticket, 1u)) + static_cast<int>(gridDim.x);
+        if (cur >= ntot) entry = kEnd;
+        else if (kFront) front_task_of(fs, cur, tmap, a.S_gu, a.S_dn, entry, entry2, pair);
+        else task_of(a, cur, tmap, entry, entry2, pair);
       }
       tok = load_tokens();
     }
@@ -404,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------- activation producer: hidden rows (all at once when resident, per gate/up
     // task when gathered), h rows per down task -------------
-    if (!kGather) {
+    if (!kGather && !kFront) {
       if (lane == 0) mbar_arrive_expect_tx(smem_addr(&sm.x_full[0]), static_cast<uint32_t>(a.T * 2 * a.d));
       __syncwarp();
       if (lane < a.T)
@@ -441,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // its h rows; the entry carries the pass count in bits 20+ (0: one pass)
       const int u = (te.x >> 16) & 0xffff, row0 = te.y, rows = te.z & 0xffff;
       const int npass = max(1, (te.z >> 20) & 0xfff);
-      const bool good = warp_wait_counter(a.ready + u, static_cast<uint32_t>(npass * a.S_gu), &sm.abort_flag,
+      const bool good = warp_wait_counter(ctr_ready + u, static_cast<uint32_t>(npass * a.S_gu), &sm.abort_flag,
                                           a.status, a.wait_limit);
       if (!good) break;
       if (lane == 0) {
@@ -456,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // drain: every copy this warp started has landed before the CTA exits
     if (lane == 0) {
-      if (!kGather) drain_wait(smem_addr(&sm.x_full[0]), 0);
+      if (!kGather && !kFront) drain_wait(smem_addr(&sm.x_full[0]), 0);
       for (int i = max(0, ngu - kXSlots); i < ngu; ++i)
         drain_wait(smem_addr(&sm.x_full[i % kXSlots]), static_cast<uint32_t>((i / kXSlots) & 1));
       for (int i = max(0, ndn - ar.hslots); i < ndn; ++i)
@@ -466,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------- publisher: release each finished gate/up task's h rows (fused: and each
     // finished down task's y rows, counted per stripe) -------------
     int n = 0, pub_n = 0, unused_tok = 0;
+    if constexpr (kFront) write_front_plan(a, f, fs, front_U);
     while (true) {
       TaskEntry te;
       if (!take_task(sm, n++, te, 0, unused_tok, a.status, a.wait_limit)) break;
@@ -473,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kFused && is_unroute(te)) continue;
       const bool dn = ((te.z >> 16) & 1) != 0;
       if (dn && !kFused) continue;  // down task, un-route in its own kernel: nothing to publish
-      uint32_t* ctr = dn ? a.dn_done + te.w : a.ready + ((te.x >> 16) & 0xffff);
+      uint32_t* ctr = dn ? ctr_dn + te.w : ctr_ready + ((te.x >> 16) & 0xffff);
       const int slot = pub_n % kPubSlots;
       const uint32_t ph = static_cast<uint32_t>((pub_n / kPubSlots) & 1);
       ++pub_n;
@@ -492,12 +679,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int fr = frag_row(g);
     int stage = 0, n = 0, pub_n = 0, ndn = 0, ngu = 0;
     uint32_t phase = 0;
-    bool ok = true, have_x = false;
+    bool ok = true, have_x = kFront;  // kFront: the prologue wrote the hidden rows
     const bool tr = a.trace != nullptr && lane == 0 && (cw == 0 || cw == kComputeWarps - 1);
     const int trole = cw == 0 ? 2 : 3;
     while (ok) {
       TaskEntry te;
       int tok = 0;
+      if (tr) trace_ev(a, trole, tcnt, 15, n);
       if (!take_task(sm, n, te, g, tok, a.status, a.wait_limit)) break;
       if (te.x < 0) break;
       if constexpr (kFused) {
@@ -505,13 +693,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++n;
           const int t = min(te.y + cw, a.T - 1), c = te.w * kDnRows + 4 * lane;
           Unroute4Pre u;
-          unroute4_pre(a, t, c, u);
+          unroute4_pre<kFront>(a, t, c, u, fs.pos, fs.w);
           // every down task of the stripe has published its y columns
-          const uint32_t dn_per_stripe = static_cast<uint32_t>(__ldg(a.meta + META_NDN) / a.S_dn);
+          const uint32_t dn_per_stripe =
+              static_cast<uint32_t>(kFront ? front_U : __ldg(a.meta + META_NDN) / a.S_dn);
           if (tr) trace_ev(a, trole, tcnt, 12, n);
-          if (!warp_wait_counter(a.dn_done + te.w, dn_per_stripe, &sm.abort_flag, a.status, a.wait_limit)) break;
+          if (!warp_wait_counter(ctr_dn + te.w, dn_per_stripe, &sm.abort_flag, a.status, a.wait_limit)) break;
           if (tr) trace_ev(a, trole, tcnt, 13, n);
-          if (te.y + cw < a.T) unroute4_post(a, t, c, u);
+          if (te.y + cw < a.T) unroute4_post<kFront>(a, t, c, u, fs.pos, fs.w);
           continue;
         }
       }
@@ -599,6 +788,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     int c2 = 1;
     trace_ev(a, 5, c2, 11, 0);
+    if constexpr (kFront) {
+      // the last CTA out hands the other (zeroed) counter set to the next launch
+      __threadfence();
+      if (atomicAdd(f.done, 1u) == gridDim.x - 1) {
+        *f.done = 0u;
+        *f.parity = fs.parity ^ 1u;
+      }
+    }
   }
 }
 
@@ -674,10 +871,22 @@ size_t expert_dec_smem_bytes(int T, int d, int F) {
   return fixed_smem_bytes<true>() + ar.x_bytes + static_cast<size_t>(ar.hslots) * ar.slot_bytes;
 }
 
+static size_t front_smem_bytes(int T, int d, int F) {
+  const Arena ar = arena_of<false>(T, d, F, static_cast<int>(sizeof(FrontSmem)));
+  return fixed_smem_bytes<false>() + ar.x_bytes + static_cast<size_t>(ar.hslots) * ar.slot_bytes + sizeof(FrontSmem);
+}
+
 bool expert_dec_supports(int T, int d, int F) {
   if (T < 1 || T > kMaxGatherT || !expert_mma_supports(d, F)) return false;
   const int hslots = T <= kMaxRows ? arena_of<false>(T, d, F).hslots : arena_of<true>(T, d, F).hslots;
   return hslots >= 2 && expert_dec_smem_bytes(T, d, F) <= static_cast<size_t>(kSmemLimit);
+}
+
+bool expert_dec_front_supports(int T, int d, int F, int E, int k) {
+  if (T < 1 || T > kMaxRows || T * k > kFrontRoutes || E > kDecReadyWords || !expert_mma_supports(d, F)) return false;
+  if (d / kDnRows > kDecTicketWord - kDecReadyWords) return false;
+  return arena_of<false>(T, d, F, static_cast<int>(sizeof(FrontSmem))).hslots >= 2 &&
+         front_smem_bytes(T, d, F) <= static_cast<size_t>(kSmemLimit);
 }
 
 bool expert_dec_gathers(int T) { return T > kMaxRows; }
@@ -691,12 +900,25 @@ cudaError_t launch_expert_dec(const ExpertArgs& a, const CUtensorMap& tm_w13, co
                               const CUtensorMap& tm_s13, const CUtensorMap& tm_s2, int num_sms,
                               cudaStream_t stream) {
   const size_t smem = expert_dec_smem_bytes(a.T, a.d, a.F);
-  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const ExpertArgs);
-  if (a.T > kMaxRows) kern = expert_dec_kernel<false, true>;  // the un-route is fused for T <= 8 only
-  else kern = a.ncb > 0 ? expert_dec_kernel<true, false> : expert_dec_kernel<false, false>;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const ExpertArgs,
+               const DecFront);
+  if (a.T > kMaxRows) kern = expert_dec_kernel<false, true, 0>;  // the un-route is fused for T <= 8 only
+  else kern = a.ncb > 0 ? expert_dec_kernel<true, false, 0> : expert_dec_kernel<false, false, 0>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  return launch_pdl(kern, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, tm_s13, tm_s2, a);
+  return launch_pdl(kern, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, tm_s13, tm_s2, a, DecFront{});
+}
+
+cudaError_t launch_expert_dec_front(const ExpertArgs& a, const DecFront& f, const CUtensorMap& tm_w13,
+                                    const CUtensorMap& tm_w2, const CUtensorMap& tm_s13, const CUtensorMap& tm_s2,
+                                    int num_sms, cudaStream_t stream) {
+  if (a.ncb <= 0 || !expert_dec_front_supports(a.T, a.d, a.F, a.E, a.k)) return cudaErrorInvalidValue;
+  const size_t smem = front_smem_bytes(a.T, a.d, a.F);
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const ExpertArgs,
+               const DecFront) = a.E <= 512 ? expert_dec_kernel<true, false, 16> : expert_dec_kernel<true, false, 32>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  return launch_pdl(kern, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, tm_s13, tm_s2, a, f);
 }
 
 }  // namespace moe

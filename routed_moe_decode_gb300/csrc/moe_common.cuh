@@ -24,6 +24,14 @@ namespace moe {
 constexpr int kChunkK = 128;
 constexpr int kGuRows = 64;         // F-rows per gate/up task (x2 for gate and up)
 constexpr int kDnRows = 128;        // d-rows per down task
+// One counter set of the decode kernel that routes its own tokens: gate/up readiness per
+// touched expert [1024], down completion per stripe [32], the ticket; two sets alternate
+// between launches.  The workspace initialisation zeroes kZeroedPrefix bytes: the status
+// block and both sets.
+constexpr int kDecSetWords = 1024 + 32 + 32;
+constexpr int kDecReadyWords = 1024;
+constexpr int kDecTicketWord = 1024 + 32;
+constexpr size_t kZeroedPrefix = 256 + size_t(2) * kDecSetWords * 4;
 constexpr int kRowsPerPass = 64;    // token rows handled per pass (4 MMA groups of 16)
 constexpr int kGroupRows = 16;      // MMA N per group
 constexpr int kMaxGroups = kRowsPerPass / kGroupRows;
@@ -42,6 +50,9 @@ struct WsLayout {
   size_t status, meta, counts, offsets, touched, gu_start, dn_start, route_pos, pos_tok, route_w;
   size_t ready, ticket, tasks, tasks_w, tasks_d, hist, x16, hs16, y, total;
   size_t front_done;  // arrival counter of the fused front, inside the zeroed status block
+  size_t dec_parity;  // counter set the decode kernel with its own front uses (zeroed block)
+  size_t dec_done;    // its CTA arrival counter (zeroed block)
+  size_t dec_sets;    // its two counter sets, kDecSetWords words each (zeroed by the init)
   int S_gu;       // gate/up stripes per expert (ffn / 64)
   int S_dn;       // down stripes per expert (d / 128)
   int max_tasks;  // capacity of the task table
@@ -84,6 +95,9 @@ inline WsLayout ws_layout(const moe_shape& s) {
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   L.status = take(64);
   L.front_done = L.status + 64;
+  L.dec_parity = L.status + 68;
+  L.dec_done = L.status + 72;
+  L.dec_sets = take(size_t(2) * kDecSetWords * 4);
   L.meta = take(META_WORDS * 4);
   L.counts = take(size_t(s.E) * 4);
   L.offsets = take(size_t(s.E + 1) * 4);

@@ -201,13 +201,23 @@ struct Unroute4Pre {
   float4 res;
 };
 
-__device__ __forceinline__ void unroute4_pre(const ExpertArgs& a, int t, int c, Unroute4Pre& u) {
-  const int* rp = a.route_pos + static_cast<size_t>(t) * a.k;
-  const float* rw = a.route_w + static_cast<size_t>(t) * a.k;
+// kSmemPlan: the route positions and weights come from shared-memory arrays [T * k] (rp_all,
+// rw_all: the decode kernel's own plan) instead of the workspace's.
+template <bool kSmemPlan, typename V>
+__device__ __forceinline__ V plan_load(const V* p) {
+  if constexpr (kSmemPlan) return *p;
+  else return __ldg(p);
+}
+
+template <bool kSmemPlan = false>
+__device__ __forceinline__ void unroute4_pre(const ExpertArgs& a, int t, int c, Unroute4Pre& u,
+                                             const int* rp_all = nullptr, const float* rw_all = nullptr) {
+  const int* rp = (kSmemPlan ? rp_all : a.route_pos) + static_cast<size_t>(t) * a.k;
+  const float* rw = (kSmemPlan ? rw_all : a.route_w) + static_cast<size_t>(t) * a.k;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    u.pos[j] = j < a.k ? __ldg(rp + j) : -1;
-    u.w[j] = j < a.k ? __ldg(rw + j) : 0.f;
+    u.pos[j] = j < a.k ? plan_load<kSmemPlan>(rp + j) : -1;
+    u.w[j] = j < a.k ? plan_load<kSmemPlan>(rw + j) : 0.f;
   }
   u.res = make_float4(0.f, 0.f, 0.f, 0.f);
   if (a.residual) {
@@ -218,10 +228,12 @@ __device__ __forceinline__ void unroute4_pre(const ExpertArgs& a, int t, int c, 
   }
 }
 
-__device__ __forceinline__ void unroute4_post(const ExpertArgs& a, int t, int c, const Unroute4Pre& u) {
+template <bool kSmemPlan = false>
+__device__ __forceinline__ void unroute4_post(const ExpertArgs& a, int t, int c, const Unroute4Pre& u,
+                                              const int* rp_all = nullptr, const float* rw_all = nullptr) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int* rp = a.route_pos + static_cast<size_t>(t) * a.k;
-  const float* rw = a.route_w + static_cast<size_t>(t) * a.k;
+  const int* rp = (kSmemPlan ? rp_all : a.route_pos) + static_cast<size_t>(t) * a.k;
+  const float* rw = (kSmemPlan ? rw_all : a.route_w) + static_cast<size_t>(t) * a.k;
   for (int j0 = 0; j0 < a.k; j0 += 8) {
     int pos[8];
     float w[8];
@@ -235,8 +247,8 @@ __device__ __forceinline__ void unroute4_post(const ExpertArgs& a, int t, int c,
         pos[jj] = u.pos[8 + jj];
         w[jj] = u.w[8 + jj];
       } else {
-        pos[jj] = j0 + jj < a.k ? __ldg(rp + j0 + jj) : -1;
-        w[jj] = j0 + jj < a.k ? __ldg(rw + j0 + jj) : 0.f;
+        pos[jj] = j0 + jj < a.k ? plan_load<kSmemPlan>(rp + j0 + jj) : -1;
+        w[jj] = j0 + jj < a.k ? plan_load<kSmemPlan>(rw + j0 + jj) : 0.f;
       }
     }
 #pragma unroll
@@ -261,7 +273,7 @@ __device__ __forceinline__ void unroute4_post(const ExpertArgs& a, int t, int c,
 }
 
 constexpr int kTraceRoles = 8;
-constexpr int kTracePerRole = 128;
+constexpr int kTracePerRole = 256;
 
 // Launch `kernel` as a programmatic dependent of the preceding work in `stream` (it may
 // begin while its predecessor finishes; the kernels order themselves with pdl_wait).
@@ -315,6 +327,40 @@ cudaError_t launch_expert_dec(const ExpertArgs& a, const CUtensorMap& tm_w13, co
                               cudaStream_t stream);
 bool expert_dec_supports(int T, int d, int F);
 size_t expert_dec_smem_bytes(int T, int d, int F);
+
+// The decode kernel with its own front, for a whole layer of at most eight tokens: every CTA
+// routes the T tokens (one warp each, the router of route_select.cuh), converts their hidden
+// rows to FP16 straight into shared memory and builds the plan there (the same buckets,
+// touched list and task order as the plan kernel, route positions in route order within a
+// bucket), so the weight stream starts without a separate front launch.  The CTAs also write
+// the routing (ids, weights), the plan and the FP16 hidden rows into the workspace, split
+// between them, for later calls that reuse them.  Its counters alternate between two zeroed
+// sets: the set in use is read at start (after the wait on the preceding kernel), CTA 0
+// zeroes the other one, and the last CTA to finish flips the parity.
+struct DecFront {
+  const float* logits;          // [T, E]
+  const __nv_bfloat16* hidden;  // [T, d]
+  int32_t* ids;                 // [T, k] out
+  float* weights;               // [T, k] out
+  int* meta;
+  int* counts;
+  int* offsets;
+  int* touched;
+  int* gu_start;
+  int* dn_start;
+  int* route_pos;
+  int* pos_tok;
+  float* route_w;
+  TaskEntry* tasks;
+  __half* x16;
+  uint32_t* sets;    // 2 x kDecSetWords
+  uint32_t* parity;  // set of the next launch
+  uint32_t* done;    // CTA arrivals of the current launch
+};
+bool expert_dec_front_supports(int T, int d, int F, int E, int k);
+cudaError_t launch_expert_dec_front(const ExpertArgs& a, const DecFront& f, const CUtensorMap& tm_w13,
+                                    const CUtensorMap& tm_w2, const CUtensorMap& tm_s13, const CUtensorMap& tm_s2,
+                                    int num_sms, cudaStream_t stream);
 // true when the decode kernel gathers each task's hidden rows (T > 8): it then reads its own
 // task table of 8-row passes, built from the plan by launch_dec_plan into tasks_d
 bool expert_dec_gathers(int T);

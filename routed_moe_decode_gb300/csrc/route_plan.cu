@@ -2,12 +2,12 @@
 //
 // Router: one warp per token ("Fused MoE routing" in "How I forked vLLM and made
 // Qwen3.8-Flash-Next decode 1.6x faster on one GPU", section 5; "Router: selection and
-// expert-task production" in "Persistent execution for Flash-Next GGUF on SM70").  Lane
-// l holds logits l + 32 i.  The softmax denominator is a warp reduction; selection is k
-// rounds of a warp arg-max on order-preserving float keys with the lowest expert id
-// winning ties (redux.sync max of the key, then redux.sync min of the candidate ids).
-// Selection compares the logits; softmax is monotone, so this is the same selection as
-// on probabilities and keeps the ids independent of the exponential's rounding.
+// expert-task production" in "Persistent execution for Flash-Next GGUF on SM70"), in
+// route_select.cuh.  Lane l holds a contiguous block of E / 32 logits; selection is k rounds
+// of a warp arg-max on order-preserving float keys with the lowest expert id winning ties
+// (redux.sync max of the key, then redux.sync min of the candidate ids).  Selection compares
+// the logits; softmax is monotone, so this is the same selection as on probabilities and
+// keeps the ids independent of the exponential's rounding.
 //
 // Plan: one CTA.  Per-expert counts (shared-memory atomics), exclusive scan, the
 // ascending touched-expert list, each route's position in expert-major order, and the
@@ -18,146 +18,9 @@
 
 #include "moe_common.cuh"
 #include "moe_kernels.cuh"
+#include "route_select.cuh"
 
 namespace moe {
-
-constexpr uint32_t kFull = 0xffffffffu;
-
-// Inverse of float_key: the float whose key is `k` (+0 for the shared key of +-0).
-__device__ __forceinline__ float key_float(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-// Insert key `x` of slot `i` into the descending list c[0..C) (slots in s[]); slots arrive in
-// ascending order and only a strictly larger key moves ahead, so equal keys keep the lower
-// slot (the lower expert id) first.
-template <int C>
-__device__ __forceinline__ void cache_insert(uint32_t (&c)[C], int (&s)[C], uint32_t x, int i) {
-#pragma unroll
-  for (int m = C - 1; m > 0; --m) {
-    const bool above = x > c[m - 1], here = x > c[m];
-    s[m] = above ? s[m - 1] : (here ? i : s[m]);
-    c[m] = above ? c[m - 1] : (here ? x : c[m]);
-  }
-  s[0] = x > c[0] ? i : s[0];
-  c[0] = x > c[0] ? x : c[0];
-}
-
-// Exact selection by k rounds over all of a lane's keys (no list): the fallback of
-// route_token when a lane runs out of listed keys.  Same ordering and tie rule.
-template <int NPL>
-__device__ __forceinline__ void select_scan(const uint32_t (&key)[NPL], int k, uint32_t& my_key, int& my_id) {
-  const int lane = threadIdx.x & 31;
-  uint32_t used = 0;
-  for (int j = 0; j < k; ++j) {
-    uint32_t bk = 0;
-    int bi = 0;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      if (!((used >> i) & 1u) && key[i] > bk) {
-        bk = key[i];
-        bi = i;
-      }
-    }
-    const uint32_t kmax = __reduce_max_sync(kFull, bk);
-    const uint32_t cand = bk == kmax ? static_cast<uint32_t>(lane + 32 * bi) : 0xffffffffu;
-    const uint32_t idx = __reduce_min_sync(kFull, cand);
-    if (static_cast<int>(idx & 31u) == lane) used |= 1u << (idx >> 5);
-    if (lane == j) {
-      my_key = kmax;
-      my_id = static_cast<int>(idx);
-    }
-  }
-}
-
-// Route token t (one warp): softmax over the E logits, k rounds of arg-max selection,
-// renormalised weights.  Writes ids[t, :k] and weights[t, :k] (and the shared-memory copies
-// s_ids/s_w at row s_row when given).
-//
-// Each lane keeps its best min(NPL, 4) keys in a sorted register list; a round is one
-// warp max over the lanes' heads, one warp min over the expert ids holding that key (the
-// lowest id wins ties), and a shift of the winner's list.  If a lane gave away its whole
-// list while holding further keys, the rounds may have missed one of those, and the
-// selection is redone by full scans.  The selected logit is recovered from its key (the key
-// is a bijection of the float bits); the probabilities are formed after the rounds, one per
-// lane.
-template <int NPL>
-__device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E, int k,
-                                            int32_t* __restrict__ ids, float* __restrict__ weights,
-                                            int* s_ids = nullptr, float* s_w = nullptr, int s_row = 0) {
-  constexpr int C = NPL < 4 ? NPL : 4;
-  const int lane = threadIdx.x & 31;
-  const float* row = logits + static_cast<size_t>(t) * E;
-  float v[NPL];
-  uint32_t key[NPL];
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    const bool ok = e < E;
-    v[i] = ok ? __ldg(row + e) : -FLT_MAX;
-    key[i] = ok ? float_key(v[i]) : 0u;  // 0 is below every real key: never selected
-  }
-  uint32_t ck[C];
-  int cs[C];
-#pragma unroll
-  for (int c = 0; c < C; ++c) {
-    ck[c] = 0u;
-    cs[c] = 0;
-  }
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) cache_insert<C>(ck, cs, key[i], i);
-  // the largest logit: its key is the largest head
-  const uint32_t kmax0 = __reduce_max_sync(kFull, ck[0]);
-  const float mx = key_float(kmax0);
-  float sp[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    if (lane + 32 * i < E) sp[i & 3] += expf(v[i] - mx);
-  }
-  float s = (sp[0] + sp[1]) + (sp[2] + sp[3]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-  const float z = s;
-
-  int nused = 0;
-  uint32_t my_key = 0;
-  int my_id = 0;
-  uint32_t kmax = kmax0;
-  for (int j = 0; j < k; ++j) {
-    if (j > 0) kmax = __reduce_max_sync(kFull, ck[0]);
-    const uint32_t cand = ck[0] == kmax ? static_cast<uint32_t>(lane + 32 * cs[0]) : 0xffffffffu;
-    const uint32_t idx = __reduce_min_sync(kFull, cand);
-    if (lane == j) {
-      my_key = kmax;
-      my_id = static_cast<int>(idx);
-    }
-    const bool own = static_cast<int>(idx & 31u) == lane;
-    nused += own ? 1 : 0;
-#pragma unroll
-    for (int c = 0; c + 1 < C; ++c) {
-      ck[c] = own ? ck[c + 1] : ck[c];
-      cs[c] = own ? cs[c + 1] : cs[c];
-    }
-    ck[C - 1] = own ? 0u : ck[C - 1];
-  }
-  if constexpr (NPL > C) {
-    const int nvalid = min(NPL, (E - lane + 31) / 32);
-    if (__any_sync(kFull, nused >= C && nvalid > C)) select_scan<NPL>(key, k, my_key, my_id);
-  }
-  // renormalise over the selection
-  const float p = lane < k ? expf(key_float(my_key) - mx) / z : 0.f;
-  float sel = p;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sel += __shfl_xor_sync(kFull, sel, o);
-  if (lane < k) {
-    ids[static_cast<size_t>(t) * k + lane] = my_id;
-    weights[static_cast<size_t>(t) * k + lane] = p / sel;
-    if (s_ids != nullptr) {
-      s_ids[s_row * k + lane] = my_id;
-      s_w[s_row * k + lane] = p / sel;
-    }
-  }
-}
 
 template <int NPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,

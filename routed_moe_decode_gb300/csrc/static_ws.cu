@@ -1,6 +1,7 @@
 // Whole-layer entry point whose scratch lives in a fixed device array of this library,
 // for callers that cannot allocate device memory themselves (see moe.h,
 // moe_layer_static_workspace).
+#include <algorithm>
 #include <cstdio>
 #include <mutex>
 
@@ -68,8 +69,9 @@ int moe_layer_static_workspace(const moe_shape* shape, const float* logits, cons
   void* ws = nullptr;
   const int arc = static_workspace_address(&ws);
   if (arc != MOE_OK) return arc;
-  // the status word must start at zero; every other field is rewritten by the call
-  if (cudaMemsetAsync(ws, 0, 256, stream) != cudaSuccess) {
+  // the status block and the decode kernel's counter sets must start at zero; every other
+  // field is rewritten by the call
+  if (cudaMemsetAsync(ws, 0, std::min(need, moe::kZeroedPrefix), stream) != cudaSuccess) {
     moe::set_last_error_message("moe_layer_static_workspace: clearing the status block failed");
     return MOE_ERR_CUDA;
   }

@@ -199,20 +199,25 @@ def test_route_ties_and_signed_zero(E, k):
     np.testing.assert_allclose(w, w_ref, rtol=WEIGHT_RTOL, atol=1e-7)
 
 
-@pytest.mark.parametrize("E,k", [(512, 10), (1024, 32), (96, 12)])
-def test_route_winners_concentrated_in_few_experts_mod_32(E, k):
-    # every winner sits at an expert id of one residue mod 32 (or two), so one warp lane
+@pytest.mark.parametrize("E,k", [(512, 10), (1024, 32), (96, 12), (1000, 32), (510, 10)])
+@pytest.mark.parametrize("layout", ["mod32", "block"])
+def test_route_winners_concentrated_in_few_experts(E, k, layout):
+    # every winner sits in one or two groups of experts: ids of one residue mod 32, or one
+    # contiguous block of E/32 ids -- the ids one warp lane of the router holds -- so one lane
     # holds more winners than it keeps sorted at a time and must rebuild its list
     rng = np.random.default_rng(7 * E + k)
     T = 64
+    npl = 1 << max(0, int(np.ceil(np.log2(max(1, (E + 31) // 32)))))
     logits = rng.standard_normal((T, E)).astype(np.float32)
     for t in range(T):
         lanes = [t % 32] if t % 2 == 0 else [t % 32, (t * 7 + 3) % 32]
         for ln in lanes:
-            sel = np.arange(ln, E, 32)
+            sel = np.arange(ln, E, 32) if layout == "mod32" else np.arange(ln * npl, min(E, ln * npl + npl))
+            if sel.size == 0:
+                continue
             logits[t, sel] = 10.0 + rng.standard_normal(sel.size).astype(np.float32)
             if t % 4 == 0:
-                logits[t, sel[::2]] = 11.0  # exact ties inside the lane
+                logits[t, sel[::2]] = 11.0  # exact ties inside the group
     ids, w = _route_only(logits, k)
     ids_ref, w_ref = O.route_topk(logits, k)
     np.testing.assert_array_equal(ids, ids_ref)
