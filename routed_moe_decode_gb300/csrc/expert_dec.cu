@@ -105,36 +105,47 @@ __host__ __device__ inline Arena arena_of(int T, int d, int F, int extra = 0) {
 
 // Ticket order of this kernel: the plan's gate/up tasks, one per ticket; then its down tasks
 // in table order (expert-major, so the down tasks of the experts whose gate/up tasks were
-// claimed first come first) -- two per ticket (stripes 2m and 2m + 1 of one expert: S_dn is
-// even, and the table holds an expert's stripes consecutively), except the last `nsingle`
-// (one per CTA of the grid), one per ticket, so that the final claims are short; then, with
-// the un-route fused, one un-route task per down stripe (T <= 8 tokens, one per compute
-// warp).  Pairing halves the claims and lets the second task's h rows arrive with the first's.
+// claimed first come first) -- G = min(group, S_dn) stripes of one expert pass per ticket,
+// run as one task (the table holds a pass's S_dn stripes consecutively and S_dn is a multiple
+// of G), except the last `nsingle` (at least one per CTA of the grid), one stripe per ticket,
+// so that the final claims are short; then, with the un-route fused, one un-route task per
+// down stripe (T <= 8 tokens, one per compute warp).  A group task copies its h rows once
+// and pays one claim and one hand-off for G stripes.  The task entry carries G in bits 24-27
+// of z (the expert's pass count of a gathered table sits in bits 20-23).  Group size: 4 when
+// the rows are gathered (many short down tasks: T > 8), 2 with the rows resident (T <= 8,
+// few tasks per CTA, where larger groups cost more in balance than they save).
+constexpr int kDnGroupGathered = 4, kDnGroupResident = 2;
 struct TicketMap {
-  int ngu, npair, nsingle, ndn_tickets;
+  int ngu, G, ngroup, nsingle, ndn_tickets;
 };
 
-__device__ __forceinline__ TicketMap ticket_map(int ngu, int ndn, int grid) {
+__device__ __forceinline__ TicketMap ticket_map(int ngu, int ndn, int grid, int S_dn, int group) {
   TicketMap m;
   m.ngu = ngu;
-  m.nsingle = min(ndn, grid & ~1);  // even, so that the pairs cover an even number of tasks
-  m.npair = (ndn - m.nsingle) / 2;
-  m.ndn_tickets = m.npair + m.nsingle;
+  m.G = min(group, S_dn);
+  m.ngroup = (ndn - min(ndn, grid)) / m.G;
+  m.nsingle = ndn - m.ngroup * m.G;
+  m.ndn_tickets = m.ngroup + m.nsingle;
   return m;
 }
 
-__device__ __forceinline__ void task_of(const ExpertArgs& a, int i, const TicketMap& m, TaskEntry& e0, TaskEntry& e1,
-                                        bool& two) {
-  two = false;
-  if (i < m.ngu) {
-    e0 = a.tasks[i];
-  } else if (i < m.ngu + m.npair) {
-    const int j = m.ngu + 2 * (i - m.ngu);
-    e0 = a.tasks[j];
-    e1 = a.tasks[j + 1];
-    two = true;
-  } else if (i < m.ngu + m.ndn_tickets) {
-    e0 = a.tasks[i + m.npair];
+// entry index in the table and stripe count of ticket i (gate/up or down; i < ngu + ndn_tickets)
+__device__ __forceinline__ int ticket_entry(int i, const TicketMap& m, int& G) {
+  G = 1;
+  if (i < m.ngu) return i;
+  const int j = i - m.ngu;
+  if (j < m.ngroup) {
+    G = m.G;
+    return m.ngu + j * m.G;
+  }
+  return m.ngu + m.ngroup * m.G + (j - m.ngroup);
+}
+
+__device__ __forceinline__ void task_of(const ExpertArgs& a, int i, const TicketMap& m, TaskEntry& e0) {
+  if (i < m.ngu + m.ndn_tickets) {
+    int G;
+    e0 = a.tasks[ticket_entry(i, m, G)];
+    e0.z |= G << 24;
   } else {
     e0 = TaskEntry{0, 0, 1 << 18, i - m.ngu - m.ndn_tickets};
   }
@@ -151,17 +162,11 @@ __device__ __forceinline__ TaskEntry front_entry(const FrontSmem& fs, int i, int
 }
 
 __device__ __forceinline__ void front_task_of(const FrontSmem& fs, int i, const TicketMap& m, int S_gu, int S_dn,
-                                              TaskEntry& e0, TaskEntry& e1, bool& two) {
-  two = false;
-  if (i < m.ngu) {
-    e0 = front_entry(fs, i, m.ngu, S_gu, S_dn);
-  } else if (i < m.ngu + m.npair) {
-    const int j = m.ngu + 2 * (i - m.ngu);
-    e0 = front_entry(fs, j, m.ngu, S_gu, S_dn);
-    e1 = front_entry(fs, j + 1, m.ngu, S_gu, S_dn);
-    two = true;
-  } else if (i < m.ngu + m.ndn_tickets) {
-    e0 = front_entry(fs, i + m.npair, m.ngu, S_gu, S_dn);
+                                              TaskEntry& e0) {
+  if (i < m.ngu + m.ndn_tickets) {
+    int G;
+    e0 = front_entry(fs, ticket_entry(i, m, G), m.ngu, S_gu, S_dn);
+    e0.z |= G << 24;
   } else {
     e0 = TaskEntry{0, 0, 1 << 18, i - m.ngu - m.ndn_tickets};
   }
@@ -454,18 +459,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol = policy_evict_first();
     const int ngu = kFront ? front_U * a.S_gu : __ldg(a.meta + (kGather ? META_DGU : META_NGU));
     const int ndn = kFront ? front_U * a.S_dn : __ldg(a.meta + (kGather ? META_DDN : META_NDN));
-    const TicketMap tmap = ticket_map(ngu, ndn, static_cast<int>(gridDim.x));
+    const TicketMap tmap = ticket_map(ngu, ndn, static_cast<int>(gridDim.x), a.S_dn,
+                                      kGather ? kDnGroupGathered : kDnGroupResident);
     const int ntot = ngu + tmap.ndn_tickets + (kFused ? a.ncb : 0);  // tickets
     const TaskEntry kEnd = TaskEntry{-1, 0, 0, 0};
     int stage = 0, issued = 0, n = 0, chunk_seq = 0;
     uint32_t phase = 0;
     int cur = blockIdx.x;
-    TaskEntry entry = kEnd, entry2 = kEnd;
-    bool pair = false;  // entry2 is the second down task of the claimed ticket
+    TaskEntry entry = kEnd;
     if (lane == 0) {
       if (cur >= ntot) entry = kEnd;
-      else if (kFront) front_task_of(fs, cur, tmap, a.S_gu, a.S_dn, entry, entry2, pair);
-      else task_of(a, cur, tmap, entry, entry2, pair);
+      else if (kFront) front_task_of(fs, cur, tmap, a.S_gu, a.S_dn, entry);
+      else task_of(a, cur, tmap, entry);
     }
     // the tokens of a gate/up task's routed rows, loaded as soon as its entry is known
     auto load_tokens = [&]() {
@@ -513,52 +518,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = __shfl_sync(0xffffffffu, entry.w, 0);
       const int e = x & 0xffff;
       const bool is_dn = ((z >> 16) & 1) != 0;
-      int rA0, rA1, nck;
+      // a down task streams the chunks of its G stripes one stripe after the other
+      const int G = is_dn ? max(1, (z >> 24) & 0xf) : 1;
+      int rA0, nck;
       const CUtensorMap* tm;
       if (!is_dn) {
         rA0 = (e - a.e_lo) * 2 * a.F + s * kGuRows;
-        rA1 = rA0 + a.F;
         tm = &tm_w13;
         nck = a.d / kChunk;
       } else {
         rA0 = (e - a.e_lo) * a.d + s * kDnRows;
-        rA1 = rA0 + 64;
         tm = &tm_w2;
         nck = a.F / kChunk;
       }
-      if (kFused && ((z >> 18) & 1)) nck = 0;  // un-route task: no weights
+      const int half = is_dn ? 64 : a.F;  // second box: 64 rows further (down) or the up rows
+      int nall = G * nck;
+      if (kFused && ((z >> 18) & 1)) nall = 0;  // un-route task: no weights
       const CUtensorMap* tms = is_dn ? &tm_s2 : &tm_s13;
       ++n;
-      for (int c = 0; c < nck; ++c) {
+      for (int c = 0, g = 0, kc = 0; c < nall; ++c) {
         if (!warp_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, &sm.abort_flag, a.status, a.wait_limit)) { ok = false; break; }
         if (lane == 0) {
           const uint32_t sb = ring0 + stage * kStageA;
           const uint32_t fa = smem_addr(&sm.full[stage]);
+          const int r0 = rA0 + g * kDnRows, r1 = r0 + half;
           if (kFront && chunk_seq == 0) trace_ev(a, 0, tcnt, 22, 0);
           mbar_arrive_expect_tx(fa, kStageA);
-          tma_load_2d(sb, tm, c * (kChunk / 2), rA0, fa, pol);
+          tma_load_2d(sb, tm, kc * (kChunk / 2), r0, fa, pol);
           if (kFront && chunk_seq == 0) trace_ev(a, 0, tcnt, 23, 0);
-          tma_load_2d(sb + kCodeBytes / 2, tm, c * (kChunk / 2), rA1, fa, pol);
-          tma_load_2d(sb + kCodeBytes, tms, c * (kChunk / 16), rA0, fa, pol);
-          tma_load_2d(sb + kCodeBytes + kScaleBytes / 2, tms, c * (kChunk / 16), rA1, fa, pol);
+          tma_load_2d(sb + kCodeBytes / 2, tm, kc * (kChunk / 2), r1, fa, pol);
+          tma_load_2d(sb + kCodeBytes, tms, kc * (kChunk / 16), r0, fa, pol);
+          tma_load_2d(sb + kCodeBytes + kScaleBytes / 2, tms, kc * (kChunk / 16), r1, fa, pol);
           trace_ev(a, 0, tcnt, 2, chunk_seq);
         }
         ++chunk_seq;
         ++issued;
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (++kc == nck) { kc = 0; ++g; }
         if (c == 0) publish();
       }
       if (!published) publish();  // un-route task (no chunks), or the first wait gave up
       if (!ok) break;
-      if (__shfl_sync(0xffffffffu, pair ? 1 : 0, 0)) {
-        // the ticket's second down task, right away: no claim, same expert and rows (no tokens)
-        if (lane == 0) {
-          entry = entry2;
-          pair = false;
-        }
-        tok = 0;
-        continue;
-      }
       // take the next ticket once at most kReserve chunks are in flight (2 among the last
       // gridDim.x tickets, so that the final tasks go to the CTAs that run dry first)
       const int reserve = __shfl_sync(0xffffffffu, cur, 0) + static_cast<int>(gridDim.x) >= ntot ? 2 : kReserve;
@@ -573,8 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         cur = static_cast<int>(atomicAdd(ctr_ticket, 1u)) + static_cast<int>(gridDim.x);
         if (cur >= ntot) entry = kEnd;
-        else if (kFront) front_task_of(fs, cur, tmap, a.S_gu, a.S_dn, entry, entry2, pair);
-        else task_of(a, cur, tmap, entry, entry2, pair);
+        else if (kFront) front_task_of(fs, cur, tmap, a.S_gu, a.S_dn, entry);
+        else task_of(a, cur, tmap, entry);
       }
       tok = load_tokens();
     }
@@ -626,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every gate/up task (all passes, S_gu stripes each) of this expert must have published
       // its h rows; the entry carries the pass count in bits 20+ (0: one pass)
       const int u = (te.x >> 16) & 0xffff, row0 = te.y, rows = te.z & 0xffff;
-      const int npass = max(1, (te.z >> 20) & 0xfff);
+      const int npass = max(1, (te.z >> 20) & 0xf);
       const bool good = warp_wait_counter(ctr_ready + u, static_cast<uint32_t>(npass * a.S_gu), &sm.abort_flag,
                                           a.status, a.wait_limit);
       if (!good) break;
@@ -660,17 +660,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kFused && is_unroute(te)) continue;
       const bool dn = ((te.z >> 16) & 1) != 0;
       if (dn && !kFused) continue;  // down task, un-route in its own kernel: nothing to publish
-      uint32_t* ctr = dn ? ctr_dn + te.w : ctr_ready + ((te.x >> 16) & 0xffff);
-      const int slot = pub_n % kPubSlots;
-      const uint32_t ph = static_cast<uint32_t>((pub_n / kPubSlots) & 1);
-      ++pub_n;
-      if (!warp_wait(smem_addr(&sm.pub_full[slot]), ph, &sm.abort_flag, a.status, a.wait_limit)) break;
-      if (lane == 0) {
-        fence_acq_rel_gpu();
-        red_add_relaxed_gpu_u32(ctr, 1u);
-        trace_ev(a, 4, tcnt, 9, pub_n);
+      // one release per gate/up task, one per stripe of a down task
+      const int G = dn ? max(1, (te.z >> 24) & 0xf) : 1;
+      bool good = true;
+      for (int g = 0; g < G && good; ++g) {
+        uint32_t* ctr = dn ? ctr_dn + te.w + g : ctr_ready + ((te.x >> 16) & 0xffff);
+        const int slot = pub_n % kPubSlots;
+        const uint32_t ph = static_cast<uint32_t>((pub_n / kPubSlots) & 1);
+        ++pub_n;
+        good = warp_wait(smem_addr(&sm.pub_full[slot]), ph, &sm.abort_flag, a.status, a.wait_limit);
+        if (good && lane == 0) {
+          fence_acq_rel_gpu();
+          red_add_relaxed_gpu_u32(ctr, 1u);
+          trace_ev(a, 4, tcnt, 9, pub_n);
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      if (!good) break;
     }
   } else {
     // ------------- compute warps: dequantise into A fragments, mma.sync, epilogue -------------
@@ -734,24 +740,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lra = is_dn ? 16 * cw + fr : 8 * cw + fr;
       const int lrb = is_dn ? 16 * cw + 8 + fr : 64 + 8 * cw + fr;
       float acc[8][4];
-      ok = run_task_chunks<kStages>(sm, a, stage, phase, acc, lra, lrb, nck, brow, live, q, tr && cw == 0, tcnt);
-      if (!ok) break;
-      if (!is_dn && kGather) {
-        // the slot's hidden rows are consumed
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sm.x_empty[slot]));
-        ++ngu;
-      }
-      if (is_dn) {
-        // the slot's h rows are consumed
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sm.h_empty[slot]));
-        ++ndn;
-      }
-      if (tr) trace_ev(a, trole, tcnt, 6, n);
-      ++n;
-      // ---- epilogue: fragment rows g / g+8, routed rows 2q, 2q + 1 ----
       if (!is_dn) {
+        ok = run_task_chunks<kStages>(sm, a, stage, phase, acc, lra, lrb, nck, brow, live, q, tr && cw == 0, tcnt);
+        if (!ok) break;
+        if (kGather) {
+          // the slot's hidden rows are consumed
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&sm.x_empty[slot]));
+          ++ngu;
+        }
+        if (tr) trace_ev(a, trole, tcnt, 6, n);
+        ++n;
+        // ---- epilogue: fragment rows g / g+8, routed rows 2q, 2q + 1 ----
         const int nidx = s * kGuRows + 8 * cw + fr;  // element n of h
         const float sc = ts13_of(a, te.x & 0xffff);
 #pragma unroll
@@ -764,9 +764,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.pub_full[pub_n % kPubSlots]));
         ++pub_n;
-      } else {
-        const float sc = ts2_of(a, te.x & 0xffff) * kHUnscale;
-        const int ra = s * kDnRows + lra, rb = s * kDnRows + lrb;
+        continue;
+      }
+      // down task: its G stripes in turn on the same h rows, one epilogue each
+      const int G = max(1, (te.z >> 24) & 0xf);
+      const float sc = ts2_of(a, te.x & 0xffff) * kHUnscale;
+      for (int gs = 0; gs < G; ++gs) {
+        ok = run_task_chunks<kStages>(sm, a, stage, phase, acc, lra, lrb, nck, brow, live, q, tr && cw == 0, tcnt);
+        if (!ok) break;
+        if (gs + 1 == G) {
+          // the slot's h rows are consumed
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&sm.h_empty[slot]));
+          ++ndn;
+          if (tr) trace_ev(a, trole, tcnt, 6, n);
+        }
+        const int ra = (s + gs) * kDnRows + lra, rb = (s + gs) * kDnRows + lrb;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int r = 2 * q + cc;
@@ -782,6 +795,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++pub_n;
         }
       }
+      if (!ok) break;
+      ++n;
     }
   }
   __syncthreads();
