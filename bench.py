@@ -180,14 +180,23 @@ def load_tensor_peak():
     return 1900.0, "fallback bf16 (burst)"
 
 
+def kernel_source_digest(kernel: str) -> str:
+    """First 16 hex digits of the SHA-256 of the kernel's .cu file followed by every shared
+    header of the CUDA sources (sorted by name): the source a DRAM capture was taken of."""
+    csrc = os.path.join(ROOT, "routed_moe_decode_gb300", "csrc")
+    h = hashlib.sha256(open(os.path.join(csrc, f"{kernel}.cu"), "rb").read())
+    for name in sorted(f for f in os.listdir(csrc) if f.endswith(".cuh")):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(config: str, kernel: str):
     """DRAM bytes per expert-kernel launch from the committed ncu summary of this workload,
     or None if there is none or the kernel source changed since it was captured."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{config}_dram.txt")
-    src = os.path.join(ROOT, "routed_moe_decode_gb300", "csrc", f"{kernel}.cu")
     if not os.path.exists(path):
         return None
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    digest = kernel_source_digest(kernel)
     vals = {}
     for line in open(path):
         if line.startswith("#") or ":" not in line:
@@ -286,7 +295,6 @@ def measure(cfg, moe, torch, dist, dev, Wd, algo, K, W, kernel_samples, e2e_step
     ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
     wts = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
     out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
-    fused_front = algo == moe.ALGO_AUTO and cfg.T * cfg.k <= 16384
 
     def step(l):
         if algo == moe.ALGO_AUTO:
@@ -298,13 +306,21 @@ def measure(cfg, moe, torch, dist, dev, Wd, algo, K, W, kernel_samples, e2e_step
         moe.forward_prepare(shape, hidden[l], ws)
         moe.forward_experts(shape, Wd[l], resid[l], out, ws, algo)
 
-    # front kernel(s), expert kernel(s), un-route kernel (none when the expert kernel runs it)
+    # front kernel(s), expert kernel(s), un-route kernel (none when the expert kernel runs it);
+    # the library reports the launches of its own layer call
     fused_unroute = moe.unroute_fused(shape, algo)
     run_algo = moe.auto_algo(shape) if algo == moe.ALGO_AUTO else algo
-    front_kernels = 1 if fused_front else 3
-    # the SIMT path runs two expert kernels, the wide kernel one plus its task-table kernel
-    expert_kernels = 2 if run_algo in (moe.ALGO_SIMT, moe.ALGO_WIDE) else 1
-    kernels_per_step = front_kernels + expert_kernels + (0 if fused_unroute else 1)
+    one_launch = algo == moe.ALGO_AUTO and moe.layer_launches(shape) == 1
+    # the decode kernel (expert_dec.cu) serves the warp-MMA path up to 64 tokens
+    dec_kernel = run_algo == moe.ALGO_MMA and cfg.T <= 64
+    if algo == moe.ALGO_AUTO:
+        kernels_per_step = moe.layer_launches(shape)
+    else:
+        front_kernels = 3
+        # the SIMT path runs two expert kernels, the wide kernel and the gathered decode
+        # kernel one each plus a task-table kernel
+        expert_kernels = 2 if (run_algo in (moe.ALGO_SIMT, moe.ALGO_WIDE) or (dec_kernel and cfg.T > 8)) else 1
+        kernels_per_step = front_kernels + expert_kernels + (0 if fused_unroute else 1)
 
     # ---- unique experts per layer (outside any timed region) ----
     U = []
@@ -322,6 +338,9 @@ def measure(cfg, moe, torch, dist, dev, Wd, algo, K, W, kernel_samples, e2e_step
     if fused_unroute:
         # and the un-route: per-route outputs read back, positions and weights, residual, out
         act_bytes += R * cfg.d * 4 + R * 8 + 2 * cfg.T * cfg.d * 2
+    if one_launch:
+        # and the router's logits
+        act_bytes += cfg.T * cfg.E * 4
     unique_bytes = [u * bpe for u in U]
 
     # ---- CUDA graphs: one of all L layers, one per single layer (for K % L) ----
@@ -395,14 +414,16 @@ def measure(cfg, moe, torch, dist, dev, Wd, algo, K, W, kernel_samples, e2e_step
     us_per_layer = 1e3 * t_ms / K
     mean_unique = sum(unique_bytes[l] for l in steps_layers) / K
 
-    # ---- expert kernel alone: CUDA events around each launch (outside the timed region) ----
-    # A GPU-side sleep first keeps the device busy while the host enqueues the front
-    # kernels, the events and the expert kernel, so the events bracket GPU work only.
-    Kk = kernel_samples
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(Kk)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(Kk)]
-    kbytes = 0.0
-    for i in range(Kk):
+    # ---- the expert kernel's duration ----
+    # The one-launch layer is its own expert kernel: the timed region's events bracket its K
+    # launches and nothing else.  Otherwise, CUDA events around each expert-kernel launch
+    # outside the timed region, after a GPU-side sleep that keeps the device busy while the
+    # host enqueues the front kernels, the events and the expert kernel.
+    Kk = K if one_launch else kernel_samples
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(0 if one_launch else Kk)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(0 if one_launch else Kk)]
+    kbytes = sum(unique_bytes[l] for l in steps_layers) + K * act_bytes if one_launch else 0.0
+    for i in range(0 if one_launch else Kk):
         l = i % L
         torch.cuda._sleep(200_000)
         moe.route_topk(shape, logits[l], ids, wts)
@@ -418,11 +439,12 @@ def measure(cfg, moe, torch, dist, dev, Wd, algo, K, W, kernel_samples, e2e_step
             moe.forward_unroute(shape, resid[l], out, ws)
         kbytes += unique_bytes[l] + act_bytes
     torch.cuda.synchronize()
-    kdur_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    k_avg_ms = sum(kdur_ms) / Kk
+    kdur_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)] if not one_launch else [t_ms / K]
+    k_avg_ms = sum(kdur_ms) / len(kdur_ms)
     achieved = kbytes / Kk / (k_avg_ms * 1e-3) / 1e9
     peak, peak_kind = load_peaks()
-    kname = {moe.ALGO_MMA: "expert_mma", moe.ALGO_TCGEN05: "expert_tc", moe.ALGO_WIDE: "expert_wide"}.get(run_algo)
+    kname = {moe.ALGO_MMA: "expert_dec" if dec_kernel else "expert_mma", moe.ALGO_TCGEN05: "expert_tc",
+             moe.ALGO_WIDE: "expert_wide"}.get(run_algo)
     traffic = profiled_traffic(cfg.name, kname) if kname else None
 
     # ---- end to end through the public C-ABI call with host buffers ----
@@ -479,10 +501,16 @@ def measure(cfg, moe, torch, dist, dev, Wd, algo, K, W, kernel_samples, e2e_step
                      "traffic_source": (f"profiles/{kname}_{cfg.name}_dram.txt (ncu dram__bytes_read.sum + "
                                         "dram__bytes_write.sum of one launch; null once the kernel source changed)")
                      if kname else None,
-                     "kernel": (f"{kname}_kernel" + ("<fused un-route>" if fused_unroute else "")
-                                + (" (after its task-table kernel)" if run_algo == moe.ALGO_WIDE else "")) if kname
+                     "kernel": (f"{kname}_kernel"
+                                + ("<own front, fused un-route> (the whole layer)" if one_launch
+                                   else "<fused un-route>" if fused_unroute
+                                   else "<gathered rows>" if dec_kernel else "")
+                                + (" (after its task-table kernel)"
+                                   if run_algo == moe.ALGO_WIDE or (dec_kernel and cfg.T > 8) else "")) if kname
                                else "simt kernels",
-                     "kernel_us": 1e3 * k_avg_ms, "kernel_samples": Kk})
+                     "kernel_us": 1e3 * k_avg_ms, "kernel_samples": Kk,
+                     "kernel_timing": "the timed region's events (K launches of this one kernel)" if one_launch
+                                      else "CUDA events around each launch, outside the timed region"})
     return {
         "t_ms": t_ms, "K": K, "W": W, "us_per_layer": us_per_layer,
         "tokens_per_s": cfg.T * K * dist.world / (t_ms * 1e-3),

@@ -147,6 +147,11 @@ MOE_API int moe_auto_algo(const moe_shape* shape);
  * or algo.  The two give identical bits.  Pure host function: needs no GPU. */
 MOE_API int moe_unroute_fused(const moe_shape* shape, int algo);
 
+/* Number of kernel launches one moe_layer call makes for `shape` (1 for the one-launch
+ * layer of at most eight tokens), or a negative status for an invalid shape.  Pure host
+ * function: needs no GPU. */
+MOE_API int moe_layer_launches(const moe_shape* shape);
+
 /* Step 1, router ("Fused MoE routing"; "Router: selection and expert-task production").
  *   logits  [T, E]  float32, finite values (non-finite logits are outside the contract)
  *   ids     [T, k]  int32 out: selected experts in selection order (value desc, ties to

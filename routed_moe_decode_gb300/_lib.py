@@ -53,6 +53,7 @@ SIGNATURES = {
     "moe_workspace_init": (_I, [_P, ctypes.c_size_t, _P]),
     "moe_check_shape": (_I, [_SP]),
     "moe_auto_algo": (_I, [_SP]),
+    "moe_layer_launches": (_I, [_SP]),
     "moe_unroute_fused": (_I, [_SP, _I]),
     "moe_route_topk": (_I, [_SP, _P, _P, _P, _P]),
     "moe_plan": (_I, [_SP, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -147,6 +148,14 @@ def unroute_fused(shape: Shape, algo: int = ALGO_AUTO) -> bool:
     if rc < 0:
         raise MoeError("moe_unroute_fused", rc)
     return rc == 1
+
+
+def layer_launches(shape: Shape) -> int:
+    """Kernel launches of one moe_layer call for `shape` (1: the one-launch layer)."""
+    rc = int(lib().moe_layer_launches(ctypes.byref(shape)))
+    if rc < 0:
+        raise MoeError("moe_layer_launches", rc)
+    return rc
 
 
 def auto_algo(shape: Shape) -> int:

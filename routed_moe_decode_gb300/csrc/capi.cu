@@ -784,6 +784,26 @@ int moe_selftest_layer_trace(const moe_shape* shape, const float* logits, const 
                      nullptr, trace);
 }
 
+int moe_layer_launches(const moe_shape* shape) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc < 0 ? rc : -rc;
+  if (shape->T == 0) return 0;
+  if (use_own_front(shape, all_experts(shape))) return 1;
+  const long long R = static_cast<long long>(shape->T) * shape->k;
+  // router + plan + FP16 staging: one fused launch, or router, plan (three launches above
+  // the one-CTA plan's limit) and staging
+  const int front = R <= moe::kFrontMaxRoutes ? 1 : 2 + (R <= 16 * 1024 ? 1 : 3);
+  const int algo = auto_choice(shape);
+  int experts = 1;
+  if (algo == MOE_ALGO_WIDE) experts = 2;  // task-table kernel + wide kernel
+  else if (algo == MOE_ALGO_MMA && moe::expert_dec_supports(shape->T, shape->d, shape->ffn) &&
+           moe::expert_dec_gathers(shape->T))
+    experts = 2;  // 8-row pass table + decode kernel
+  const int unroute =
+      (algo == MOE_ALGO_MMA && moe::expert_mma_unroute_tasks(shape->T, moe::ws_layout(*shape).S_dn) > 0) ? 0 : 1;
+  return front + experts + unroute;
+}
+
 int moe_read_device_status(const void* workspace, int clear, uint32_t* status_bits, moe_stream_t stream) {
   if (!workspace || !status_bits || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
   uint32_t v = 0;

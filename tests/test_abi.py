@@ -123,3 +123,21 @@ def test_expert_range_bounds_rejected_on_host(L):
     assert lib.moe_layer_expert_range(ctypes.byref(bad), 0, 8, *rest) == L.MOE_ERR_UNSUPPORTED
     # a valid block with missing weights fails on the host as moe_layer does
     assert lib.moe_layer_expert_range(sp, 0, 8, *rest) == L.MOE_ERR_INVALID_ARG
+
+
+def test_layer_launch_counts(L):
+    # one launch for a layer of at most eight tokens on the warp-MMA path; otherwise the
+    # front, the expert kernel(s) and the un-route kernel
+    cases = [((4, 2048, 512, 512, 10), 1),     # one-launch layer
+             ((1, 256, 256, 16, 1), 1),
+             ((8, 2048, 512, 512, 32), 1),     # 256 routes: the own front's limit
+             ((8, 2048, 512, 2048 // 2, 33 - 1), 1),
+             ((4, 256, 128, 16, 2), 3),        # ffn below the warp-MMA range: front, tcgen05, un-route
+             ((32, 2048, 512, 512, 10), 4),    # front, 8-row task table, decode kernel, un-route
+             ((256, 2048, 512, 512, 10), 3),   # front, warp-MMA kernel, un-route
+             ((8192, 2048, 512, 512, 10), 8),  # router, 3-launch plan, staging, task table, wide, un-route
+             ((0, 2048, 512, 512, 10), 0)]
+    for dims, n in cases:
+        assert L.layer_launches(L.shape_of(*dims)) == n, dims
+    with pytest.raises(L.MoeError):
+        L.layer_launches(L.shape_of(4, 2048, 512, 512, 600))
