@@ -24,9 +24,10 @@ pytestmark = pytest.mark.gpu
 AUTO, TCGEN05, MMA, WIDE = 0, 1, 3, 4
 WAIT_LIMIT_CYCLES = 1 << 20  # ~0.5 ms at 2 GHz
 
-# (workload, algo): the decode kernel for at most eight tokens (B=1 through AUTO), the
-# warp-MMA kernel for larger batches, the 16-row tcgen05 kernel and the wide tcgen05 kernel
-CASES = [("b1", AUTO), ("b8", MMA), ("b8", TCGEN05), ("b8", WIDE)]
+# (workload, algo): the decode kernel with the rows resident (B=1 through AUTO) and with
+# gathered rows (B=8), the warp-MMA kernel of larger batches (B=64), the 16-row tcgen05
+# kernel and the wide tcgen05 kernel
+CASES = [("b1", AUTO), ("b8", MMA), ("b64", MMA), ("b8", TCGEN05), ("b8", WIDE)]
 
 
 @pytest.fixture(scope="module")
