@@ -311,8 +311,8 @@ def measure(cfg, moe, torch, dist, dev, Wd, algo, K, W, kernel_samples, e2e_step
     fused_unroute = moe.unroute_fused(shape, algo)
     run_algo = moe.auto_algo(shape) if algo == moe.ALGO_AUTO else algo
     one_launch = algo == moe.ALGO_AUTO and moe.layer_launches(shape) == 1
-    # the decode kernel (expert_dec.cu) serves the warp-MMA path up to 64 tokens
-    dec_kernel = run_algo == moe.ALGO_MMA and cfg.T <= 64
+    # the decode kernel (expert_dec.cu) serves the warp-MMA path up to 256 tokens
+    dec_kernel = run_algo == moe.ALGO_MMA and cfg.T <= 256
     if algo == moe.ALGO_AUTO:
         kernels_per_step = moe.layer_launches(shape)
     else:

@@ -409,7 +409,7 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     if (rc != MOE_OK) return rc;
     // for few tokens the decode kernel runs the un-route as trailing tasks of its own
     a.ncb = (stages & kStageUnroute) ? moe::expert_mma_unroute_tasks(shape->T, L.S_dn) : 0;
-    // up to 64 tokens: the decode kernel with the hidden rows in shared memory (all of them
+    // up to 256 tokens: the decode kernel with the hidden rows in shared memory (all of them
     // for <= 8 tokens; per task, from its own table of 8-row passes, above)
     if (own_front) {
       // the layer in one launch: the decode kernel routes and plans for itself

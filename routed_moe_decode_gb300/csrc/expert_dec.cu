@@ -1,24 +1,27 @@
-// Decode expert kernel for verify steps of at most eight tokens (T <= 8), so that no expert
-// holds more than eight routed rows and every task is one 8-column MMA tile.
+// Decode expert kernel: every task is one expert pass of at most eight routed rows, so one
+// 8-column MMA tile.
 //
 // Same weight stream and MMA core as the warp-MMA kernel of expert_mma.cu (one resident CTA
-// per SM, tasks from the plan's task table through tickets, 256-K chunks of E2M1 codes and
-// block scales by TMA into a ring, in-register dequantisation into the A fragments of
-// mma.sync m16n8k16), but the activations never travel with the chunks:
-//   - the FP16 hidden rows of all T tokens (at most 8 x 2d bytes) are copied into shared
-//     memory once, when the kernel starts, and every gate/up task reads its routed rows
-//     there (the token of each routed row comes with the task entry);
+// per SM, tasks through tickets, 256-K chunks of E2M1 codes and block scales by TMA into a
+// ring, in-register dequantisation into the A fragments of mma.sync m16n8k16), but the
+// activations never travel with the chunks:
+//   - T <= 8 (rows resident): the FP16 hidden rows of all T tokens (at most 8 x 2d bytes)
+//     are copied into shared memory once, and every gate/up task reads its routed rows
+//     there (the token of each routed row comes with the task entry); the plan's own task
+//     table serves, or, for a whole layer, the kernel routes and plans for itself;
+//   - 8 < T <= 256 (rows gathered): the kernel's own table of 8-row passes; each gate/up
+//     task's rows are copied into one of two slots when the task is published;
 //   - each down task's h rows (at most 8 x 2F bytes, published by the gate/up tasks of its
 //     expert) are copied once per task into one of two to four slots, as soon as the expert's
 //     readiness counter allows, while the compute warps still work on earlier tasks.
 // So a chunk's stage is full once its weight bytes have landed; compute warps wait on one
 // barrier per chunk and the weight producer is the only per-chunk issuer.
 //
-// Warps: 0 task fetcher + weight producer, 1 activation producer (hidden rows once, h rows
-// per down task), 2 publisher (one GPU-scope release per finished task), 3-10 compute (16
-// weight rows each of the 128-row task tile, as in expert_mma.cu), and with the un-route
-// fused, trailing un-route tasks (one token's 128 columns of a stripe per compute warp)
-// once the stripe's down tasks have been released.
+// Warps: 0 task fetcher + weight producer, 1 activation producer (hidden rows, h rows per
+// down task), 2 publisher (one GPU-scope release per finished gate/up task or down stripe),
+// 3-10 compute (16 weight rows each of the 128-row chunk, as in expert_mma.cu), and with the
+// un-route fused, trailing un-route tasks (one token's 128 columns of a stripe per compute
+// warp) once the stripe's down tasks have been released.
 #include "mma_parts.cuh"
 #include "route_select.cuh"
 
@@ -29,7 +32,7 @@ namespace dk {
 using namespace mk;
 
 constexpr int kStagesResident = 9;  // weight ring with all hidden rows resident (T <= 8)
-constexpr int kStagesGathered = 7;  // weight ring beside the gathered-row slots (8 < T <= 64)
+constexpr int kStagesGathered = 7;  // weight ring beside the gathered-row slots (8 < T <= 256)
 constexpr int kMaxRows = 8;         // routed rows per task (T <= 8, or 8-row passes)
 constexpr int kXSlots = 2;          // gathered hidden-row slots
 // The fetcher claims its next ticket once at most kReserve of its chunks are in flight: a
@@ -110,11 +113,14 @@ __host__ __device__ inline Arena arena_of(int T, int d, int F, int extra = 0) {
 // of G), except the last `nsingle` (at least one per CTA of the grid), one stripe per ticket,
 // so that the final claims are short; then, with the un-route fused, one un-route task per
 // down stripe (T <= 8 tokens, one per compute warp).  A group task copies its h rows once
-// and pays one claim and one hand-off for G stripes.  The task entry carries G in bits 24-27
-// of z (the expert's pass count of a gathered table sits in bits 20-23).  Group size: 4 when
+// and pays one claim and one hand-off for G stripes.  The task entry carries G in bits 28-30
+// of z (the expert's pass count of a gathered table sits in bits 20-27).  Group size: 4 when
 // the rows are gathered (many short down tasks: T > 8), 2 with the rows resident (T <= 8,
 // few tasks per CTA, where larger groups cost more in balance than they save).
 constexpr int kDnGroupGathered = 4, kDnGroupResident = 2;
+constexpr int kNpassShift = 20, kGroupShift = 28;
+__device__ __forceinline__ int task_npass(int z) { return max(1, (z >> kNpassShift) & 0xff); }
+__device__ __forceinline__ int task_group(int z) { return max(1, (z >> kGroupShift) & 0x7); }
 struct TicketMap {
   int ngu, G, ngroup, nsingle, ndn_tickets;
 };
@@ -145,7 +151,7 @@ __device__ __forceinline__ void task_of(const ExpertArgs& a, int i, const Ticket
   if (i < m.ngu + m.ndn_tickets) {
     int G;
     e0 = a.tasks[ticket_entry(i, m, G)];
-    e0.z |= G << 24;
+    e0.z |= G << kGroupShift;
   } else {
     e0 = TaskEntry{0, 0, 1 << 18, i - m.ngu - m.ndn_tickets};
   }
@@ -166,7 +172,7 @@ __device__ __forceinline__ void front_task_of(const FrontSmem& fs, int i, const 
   if (i < m.ngu + m.ndn_tickets) {
     int G;
     e0 = front_entry(fs, ticket_entry(i, m, G), m.ngu, S_gu, S_dn);
-    e0.z |= G << 24;
+    e0.z |= G << kGroupShift;
   } else {
     e0 = TaskEntry{0, 0, 1 << 18, i - m.ngu - m.ndn_tickets};
   }
@@ -304,7 +310,7 @@ __device__ __forceinline__ void write_front_plan(const ExpertArgs& a, const DecF
 }
 
 // kGather false: T <= 8, every token's hidden row resident (plan's task table, one pass per
-// expert, optionally the fused un-route); kGather true: 8 < T <= 64, each gate/up task's rows
+// expert, optionally the fused un-route); kGather true: 8 < T <= 256, each gate/up task's rows
 // gathered into one of kXSlots slots, task table of 8-row passes (built by dec_plan_kernel).
 // kNpl > 0 (T <= 8, un-route fused): the kernel's own front, with kNpl logits per lane in
 // the router (E <= 32 kNpl); the plan comes from shared memory, the counters from the set
@@ -519,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = x & 0xffff;
       const bool is_dn = ((z >> 16) & 1) != 0;
       // a down task streams the chunks of its G stripes one stripe after the other
-      const int G = is_dn ? max(1, (z >> 24) & 0xf) : 1;
+      const int G = is_dn ? task_group(z) : 1;
       int rA0, nck;
       const CUtensorMap* tm;
       if (!is_dn) {
@@ -626,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every gate/up task (all passes, S_gu stripes each) of this expert must have published
       // its h rows; the entry carries the pass count in bits 20+ (0: one pass)
       const int u = (te.x >> 16) & 0xffff, row0 = te.y, rows = te.z & 0xffff;
-      const int npass = max(1, (te.z >> 20) & 0xf);
+      const int npass = task_npass(te.z);
       const bool good = warp_wait_counter(ctr_ready + u, static_cast<uint32_t>(npass * a.S_gu), &sm.abort_flag,
                                           a.status, a.wait_limit);
       if (!good) break;
@@ -661,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool dn = ((te.z >> 16) & 1) != 0;
       if (dn && !kFused) continue;  // down task, un-route in its own kernel: nothing to publish
       // one release per gate/up task, one per stripe of a down task
-      const int G = dn ? max(1, (te.z >> 24) & 0xf) : 1;
+      const int G = dn ? task_group(te.z) : 1;
       bool good = true;
       for (int g = 0; g < G && good; ++g) {
         uint32_t* ctr = dn ? ctr_dn + te.w + g : ctr_ready + ((te.x >> 16) & 0xffff);
@@ -767,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       // down task: its G stripes in turn on the same h rows, one epilogue each
-      const int G = max(1, (te.z >> 24) & 0xf);
+      const int G = task_group(te.z);
       const float sc = ts2_of(a, te.x & 0xffff) * kHUnscale;
       for (int gs = 0; gs < G; ++gs) {
         ok = run_task_chunks<kStages>(sm, a, stage, phase, acc, lra, lrb, nck, brow, live, q, tr && cw == 0, tcnt);
@@ -861,7 +867,7 @@ __global__ void __launch_bounds__(1024) dec_plan_kernel(const int* meta_in, int*
     int di = total * S_gu + before * S_dn;
     for (int p = 0; p < np; ++p) {
       const int rows = min(kMaxRows, m - p * kMaxRows);
-      const int z = rows | (np > 1 ? 1 << 17 : 0) | (np << 20);
+      const int z = rows | (np > 1 ? 1 << 17 : 0) | (np << kNpassShift);
       const int row0 = base + p * kMaxRows;
       for (int s2 = 0; s2 < S_gu; ++s2) tasks[gi++] = TaskEntry{e | (tid << 16), row0, z, s2};
       for (int s2 = 0; s2 < S_dn; ++s2) tasks[di++] = TaskEntry{e | (tid << 16), row0, z | (1 << 16), s2};
@@ -875,7 +881,7 @@ __global__ void __launch_bounds__(1024) dec_plan_kernel(const int* meta_in, int*
 
 // T at or below which every token's hidden row stays resident; above it (up to kMaxGatherT)
 // each gate/up task's rows are gathered.
-constexpr int kMaxGatherT = 64;
+constexpr int kMaxGatherT = 256;
 
 size_t expert_dec_smem_bytes(int T, int d, int F) {
   if (T <= kMaxRows) {
