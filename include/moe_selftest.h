@@ -39,8 +39,8 @@ MOE_API int moe_selftest_mma(const void* A, const void* B, float* D, moe_stream_
 
 /* The expert kernel and the un-route kernel exactly as moe_forward_experts runs them with
  * MOE_ALGO_AUTO (after moe_plan and moe_forward_prepare), with a timeline recorded into
- * `trace`: per CTA 8 roles x 256 uint64 events (event code << 56 | index << 40 | low 40
- * bits of %globaltimer in ns); zero-initialise the buffer (multiProcessorCount x 16384 bytes).
+ * `trace`: per CTA 8 roles x 1024 uint64 events (event code << 56 | index << 40 | low 40
+ * bits of %globaltimer in ns); zero-initialise the buffer (multiProcessorCount x 65536 bytes).
  * Warp-MMA kernel: role 0 weight producer (1 task published, 2 chunk issued), 1 activation
  * producer (3 readiness met, 4 chunk issued), 2 and 3 first and last compute warp (5 task
  * taken, index bit 15 = down task; 6 chunks done; 12 un-route wait begins, 13 wait met),

@@ -273,7 +273,7 @@ __device__ __forceinline__ void unroute4_post(const ExpertArgs& a, int t, int c,
 }
 
 constexpr int kTraceRoles = 8;
-constexpr int kTracePerRole = 256;
+constexpr int kTracePerRole = 1024;
 
 // Launch `kernel` as a programmatic dependent of the preceding work in `stream` (it may
 // begin while its predecessor finishes; the kernels order themselves with pdl_wait).
