@@ -216,6 +216,14 @@ int moe_auto_algo(const moe_shape* shape) {
   return auto_choice(shape);
 }
 
+// Un-route tasks the warp-MMA path's expert kernel runs itself for `shape` (0: the un-route is
+// a kernel of its own): the decode kernel wherever it serves the shape, else the batch
+// kernel for at most eight tokens.
+static int fused_unroute_tasks(const moe_shape* s) {
+  if (moe::expert_dec_supports(s->T, s->d, s->ffn)) return moe::expert_dec_unroute_tasks(s->T, s->d, s->ffn);
+  return moe::expert_mma_unroute_tasks(s->T, moe::ws_layout(*s).S_dn);
+}
+
 int moe_unroute_fused(const moe_shape* shape, int algo) {
   const int rc = check_shape(shape);
   if (rc != MOE_OK) return rc < 0 ? rc : -rc;
@@ -223,7 +231,7 @@ int moe_unroute_fused(const moe_shape* shape, int algo) {
   const bool mma_ok = moe::expert_mma_supports(shape->d, shape->ffn);
   const int run = algo == MOE_ALGO_AUTO ? auto_choice(shape) : algo;
   if (run != MOE_ALGO_MMA || !mma_ok) return 0;  // MOE_ALGO_WIDE, MOE_ALGO_TCGEN05, MOE_ALGO_SIMT
-  return moe::expert_mma_unroute_tasks(shape->T, moe::ws_layout(*shape).S_dn) > 0 ? 1 : 0;
+  return fused_unroute_tasks(shape) > 0 ? 1 : 0;
 }
 
 size_t moe_workspace_bytes(const moe_shape* shape) {
@@ -407,8 +415,8 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     rc = moe::encode_scales_map(&ts2, w2_scales, static_cast<uint32_t>(shape->ffn / 16),
                                 static_cast<uint64_t>(r.hi - r.lo) * shape->d, 64);
     if (rc != MOE_OK) return rc;
-    // for few tokens the decode kernel runs the un-route as trailing tasks of its own
-    a.ncb = (stages & kStageUnroute) ? moe::expert_mma_unroute_tasks(shape->T, L.S_dn) : 0;
+    // the decode kernel runs the un-route as trailing tasks of its own
+    a.ncb = (stages & kStageUnroute) ? fused_unroute_tasks(shape) : 0;
     // up to 256 tokens: the decode kernel with the hidden rows in shared memory (all of them
     // for <= 8 tokens; per task, from its own table of 8-row passes, above)
     if (own_front) {
@@ -602,7 +610,7 @@ int moe_front(const moe_shape* shape, const float* logits, const void* hidden, i
 // eight tokens (un-route fused), all experts, the warp-MMA path chosen by MOE_ALGO_AUTO.
 static bool use_own_front(const moe_shape* s, ExpertRange r) {
   return r.lo == 0 && r.hi == s->E && s->T >= 1 && auto_choice(s) == MOE_ALGO_MMA &&
-         moe::expert_mma_unroute_tasks(s->T, moe::ws_layout(*s).S_dn) > 0 &&
+         fused_unroute_tasks(s) > 0 &&
          moe::expert_dec_front_supports(s->T, s->d, s->ffn, s->E, s->k);
 }
 
@@ -800,7 +808,7 @@ int moe_layer_launches(const moe_shape* shape) {
            moe::expert_dec_gathers(shape->T))
     experts = 2;  // 8-row pass table + decode kernel
   const int unroute =
-      (algo == MOE_ALGO_MMA && moe::expert_mma_unroute_tasks(shape->T, moe::ws_layout(*shape).S_dn) > 0) ? 0 : 1;
+      (algo == MOE_ALGO_MMA && fused_unroute_tasks(shape) > 0) ? 0 : 1;
   return front + experts + unroute;
 }
 

@@ -112,7 +112,8 @@ __host__ __device__ inline Arena arena_of(int T, int d, int F, int extra = 0) {
 // run as one task (the table holds a pass's S_dn stripes consecutively and S_dn is a multiple
 // of G), except the last `nsingle` (at least one per CTA of the grid), one stripe per ticket,
 // so that the final claims are short; then, with the un-route fused, one un-route task per
-// down stripe (T <= 8 tokens, one per compute warp).  A group task copies its h rows once
+// down stripe and group of eight tokens (one token per compute warp).  A group task copies
+// its h rows once
 // and pays one claim and one hand-off for G stripes.  The task entry carries G in bits 28-30
 // of z (the expert's pass count of a gathered table sits in bits 20-27).  Group size: 4 when
 // the rows are gathered (many short down tasks: T > 8), 2 with the rows resident (T <= 8,
@@ -147,13 +148,19 @@ __device__ __forceinline__ int ticket_entry(int i, const TicketMap& m, int& G) {
   return m.ngu + m.ngroup * m.G + (j - m.ngroup);
 }
 
+// Un-route task c: the 128 columns of down stripe c mod S_dn for the tokens
+// [8 (c / S_dn), +8), one token per compute warp.
+__device__ __forceinline__ TaskEntry unroute_entry(int c, int S_dn) {
+  return TaskEntry{0, kComputeWarps * (c / S_dn), 1 << 18, c % S_dn};
+}
+
 __device__ __forceinline__ void task_of(const ExpertArgs& a, int i, const TicketMap& m, TaskEntry& e0) {
   if (i < m.ngu + m.ndn_tickets) {
     int G;
     e0 = a.tasks[ticket_entry(i, m, G)];
     e0.z |= G << kGroupShift;
   } else {
-    e0 = TaskEntry{0, 0, 1 << 18, i - m.ngu - m.ndn_tickets};
+    e0 = unroute_entry(i - m.ngu - m.ndn_tickets, a.S_dn);
   }
 }
 
@@ -174,7 +181,7 @@ __device__ __forceinline__ void front_task_of(const FrontSmem& fs, int i, const 
     e0 = front_entry(fs, ticket_entry(i, m, G), m.ngu, S_gu, S_dn);
     e0.z |= G << kGroupShift;
   } else {
-    e0 = TaskEntry{0, 0, 1 << 18, i - m.ngu - m.ndn_tickets};
+    e0 = unroute_entry(i - m.ngu - m.ndn_tickets, S_dn);
   }
 }
 
@@ -707,8 +714,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           Unroute4Pre u;
           unroute4_pre<kFront>(a, t, c, u, fs.pos, fs.w);
           // every down task of the stripe has published its y columns
-          const uint32_t dn_per_stripe =
-              static_cast<uint32_t>(kFront ? front_U : __ldg(a.meta + META_NDN) / a.S_dn);
+          const uint32_t dn_per_stripe = static_cast<uint32_t>(
+              kFront ? front_U : __ldg(a.meta + (kGather ? META_DDN : META_NDN)) / a.S_dn);
           if (tr) trace_ev(a, trole, tcnt, 12, n);
           if (!warp_wait_counter(ctr_dn + te.w, dn_per_stripe, &sm.abort_flag, a.status, a.wait_limit)) break;
           if (tr) trace_ev(a, trole, tcnt, 13, n);
@@ -911,6 +918,14 @@ bool expert_dec_front_supports(int T, int d, int F, int E, int k) {
 }
 
 bool expert_dec_gathers(int T) { return T > kMaxRows; }
+
+int expert_dec_unroute_tasks(int T, int d, int F) {
+  // fused for the resident rows only: above eight tokens the trailing un-route tasks (one
+  // CTA's eight warps per stripe and token group, each after its stripe's last down task)
+  // measured slower than the separate, fully parallel un-route kernel
+  return T <= kMaxRows && expert_dec_supports(T, d, F) ? (d / kDnRows) * ((T + kComputeWarps - 1) / kComputeWarps)
+                                                       : 0;
+}
 
 cudaError_t launch_dec_plan(const ExpertArgs& a, TaskEntry* tasks_d, cudaStream_t stream) {
   return launch_pdl(dec_plan_kernel, dim3(1), dim3(1024), 0, stream, a.meta, const_cast<int*>(a.meta), a.touched,

@@ -364,6 +364,9 @@ cudaError_t launch_expert_dec_front(const ExpertArgs& a, const DecFront& f, cons
 // true when the decode kernel gathers each task's hidden rows (T > 8): it then reads its own
 // task table of 8-row passes, built from the plan by launch_dec_plan into tasks_d
 bool expert_dec_gathers(int T);
+// un-route tasks the decode kernel appends when it runs the un-route itself (one per down
+// stripe; T <= 8), or 0
+int expert_dec_unroute_tasks(int T, int d, int F);
 cudaError_t launch_dec_plan(const ExpertArgs& a, TaskEntry* tasks_d, cudaStream_t stream);
 // number of un-route tasks the decode kernel appends when it runs the un-route itself
 int expert_mma_unroute_tasks(int T, int S_dn);

@@ -84,6 +84,7 @@ def test_unroute_fused_selection(L):
     assert L.unroute_fused(L.shape_of(8, 2048, 512, 512, 10), L.ALGO_MMA)
     assert not L.unroute_fused(L.shape_of(9, 2048, 512, 512, 10))
     assert not L.unroute_fused(L.shape_of(32, 2048, 512, 512, 10))
+    assert not L.unroute_fused(L.shape_of(257, 2048, 512, 512, 10))
     assert not L.unroute_fused(L.shape_of(4, 2048, 512, 512, 10), L.ALGO_TCGEN05)
     assert not L.unroute_fused(L.shape_of(4, 2048, 512, 512, 10), L.ALGO_SIMT)
     assert not L.unroute_fused(L.shape_of(4, 768, 512, 64, 8))
@@ -134,7 +135,8 @@ def test_layer_launch_counts(L):
              ((8, 2048, 512, 2048 // 2, 33 - 1), 1),
              ((4, 256, 128, 16, 2), 3),        # ffn below the warp-MMA range: front, tcgen05, un-route
              ((32, 2048, 512, 512, 10), 4),    # front, 8-row task table, decode kernel, un-route
-             ((256, 2048, 512, 512, 10), 3),   # front, warp-MMA kernel, un-route
+             ((256, 2048, 512, 512, 10), 4),   # the same up to 256 tokens
+             ((512, 2048, 512, 512, 10), 3),   # front, warp-MMA batch kernel, un-route
              ((8192, 2048, 512, 512, 10), 8),  # router, 3-launch plan, staging, task table, wide, un-route
              ((0, 2048, 512, 512, 10), 0)]
     for dims, n in cases:
