@@ -374,7 +374,8 @@ MOE_API int moe_layer_gated(const moe_shape* shape, int G, const float* logits, 
  *   - Sharing: every call uses the same array and leaves its contents behind; the call
  *     clears what must start at zero (status word, counters) itself.  Calls whose work
  *     overlaps on the GPU (different streams, or several host threads) race on the
- *     array: serialise them.  Device-side status bits are not reported by this call.
+ *     array: serialise them.  Device-side status bits are not returned by this call; read
+ *     them with moe_static_workspace_read_status after it.
  * Returns as moe_layer. */
 MOE_API int moe_layer_static_workspace(const moe_shape* shape, const float* logits,
                                        const void* hidden, const uint8_t* w13_codes,
@@ -382,6 +383,12 @@ MOE_API int moe_layer_static_workspace(const moe_shape* shape, const float* logi
                                        const uint8_t* w2_codes, const uint8_t* w2_scales,
                                        float w2_scale, const void* residual, void* out,
                                        int32_t* ids, float* weights, moe_stream_t stream);
+
+/* The device status word of moe_layer_static_workspace's array, as moe_read_device_status
+ * reads a caller workspace's: blocking copy on `stream`, cleared when `clear` is non-zero,
+ * MOE_OK if no bit is set, MOE_ERR_DEVICE if any is.  Each static call starts by clearing
+ * the word, so read it after a call and before the next. */
+MOE_API int moe_static_workspace_read_status(int clear, uint32_t* status_bits, moe_stream_t stream);
 
 /* Copy the device status word to *status_bits (blocking copy on `stream`; call after the
  * work of interest has been enqueued) and clear it when `clear` is non-zero.  Returns

@@ -54,6 +54,7 @@ SIGNATURES = {
     "moe_check_shape": (_I, [_SP]),
     "moe_auto_algo": (_I, [_SP]),
     "moe_layer_launches": (_I, [_SP]),
+    "moe_static_workspace_read_status": (_I, [_I, ctypes.POINTER(ctypes.c_uint32), _P]),
     "moe_unroute_fused": (_I, [_SP, _I]),
     "moe_route_topk": (_I, [_SP, _P, _P, _P, _P]),
     "moe_plan": (_I, [_SP, _P, _P, _P, ctypes.c_size_t, _P]),

@@ -79,4 +79,12 @@ int moe_layer_static_workspace(const moe_shape* shape, const float* logits, cons
                    residual, out, ids, weights, ws, need, stream);
 }
 
+int moe_static_workspace_read_status(int clear, uint32_t* status_bits, moe_stream_t stream) {
+  if (!status_bits) return MOE_ERR_INVALID_ARG;
+  void* ws = nullptr;
+  const int arc = static_workspace_address(&ws);
+  if (arc != MOE_OK) return arc;
+  return moe_read_device_status(ws, clear, status_bits, stream);
+}
+
 }  // extern "C"
