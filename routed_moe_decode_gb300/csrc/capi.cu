@@ -274,6 +274,9 @@ static void fill_plan_args(moe::PlanArgs& a, const moe_shape* shape, const WsLay
   a.route_w = at<float>(workspace, L.route_w);
   a.tasks = at<moe::TaskEntry>(workspace, L.tasks);
   a.hist = at<int>(workspace, L.hist);
+  a.tasks_d = (shape->T > moe::kDecPassRows && shape->T <= moe::kDecGatherMaxT)
+                  ? at<moe::TaskEntry>(workspace, L.tasks_d)
+                  : nullptr;
   a.e_lo = r.lo;
   a.e_hi = r.hi;
 }
@@ -426,9 +429,8 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     } else if (moe::expert_dec_supports(shape->T, shape->d, shape->ffn)) {
       moe::ExpertArgs ad = a;
       if (moe::expert_dec_gathers(shape->T)) {
+        // the plan wrote the decode kernel's table of 8-row passes
         moe::TaskEntry* tasks_d = at<moe::TaskEntry>(workspace, L.tasks_d);
-        e = moe::launch_dec_plan(a, tasks_d, stream);
-        if (e != cudaSuccess) { set_error("decode task table launch", e); return MOE_ERR_CUDA; }
         rc = poison(tasks_d, moe::META_DGU);
         if (rc != MOE_OK) return rc;
         ad.tasks = tasks_d;
@@ -804,9 +806,6 @@ int moe_layer_launches(const moe_shape* shape) {
   const int algo = auto_choice(shape);
   int experts = 1;
   if (algo == MOE_ALGO_WIDE) experts = 2;  // task-table kernel + wide kernel
-  else if (algo == MOE_ALGO_MMA && moe::expert_dec_supports(shape->T, shape->d, shape->ffn) &&
-           moe::expert_dec_gathers(shape->T))
-    experts = 2;  // 8-row pass table + decode kernel
   const int unroute =
       (algo == MOE_ALGO_MMA && fused_unroute_tasks(shape) > 0) ? 0 : 1;
   return front + experts + unroute;

@@ -318,7 +318,7 @@ __device__ __forceinline__ void write_front_plan(const ExpertArgs& a, const DecF
 
 // kGather false: T <= 8, every token's hidden row resident (plan's task table, one pass per
 // expert, optionally the fused un-route); kGather true: 8 < T <= 256, each gate/up task's rows
-// gathered into one of kXSlots slots, task table of 8-row passes (built by dec_plan_kernel).
+// gathered into one of kXSlots slots, task table of 8-row passes (written by the plan).
 // kNpl > 0 (T <= 8, un-route fused): the kernel's own front, with kNpl logits per lane in
 // the router (E <= 32 kNpl); the plan comes from shared memory, the counters from the set
 // `f.parity` selects.
@@ -827,68 +827,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Task table of the gathered mode: from the plan's per-expert arrays, passes of at most
-// kMaxRows routed rows (each its own weight pass), all gate/up tasks (touched order, pass,
-// stripe) then all down tasks; entry z carries the expert's pass count in bits 20+ for the
-// readiness target of its down tasks.  One CTA.
-__global__ void __launch_bounds__(1024) dec_plan_kernel(const int* meta_in, int* meta, const int* touched,
-                                                        const int* counts, const int* offsets, TaskEntry* tasks,
-                                                        int S_gu, int S_dn) {
-  pdl_wait();
-  pdl_launch_dependents();
-  __shared__ int s_warp[32];
-  __shared__ int s_total;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int U = __ldcg(meta_in + META_U);
-  int e = 0, m = 0, np = 0;
-  if (tid < U) {
-    e = __ldcg(touched + tid);
-    m = __ldcg(counts + e);
-    np = (m + kMaxRows - 1) / kMaxRows;
-  }
-  int incl = np;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = s_warp[lane];
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += v;
-    }
-    s_warp[lane] = wi - w;
-    if (lane == 31) s_total = wi;
-  }
-  __syncthreads();
-  const int before = s_warp[warp] + incl - np;
-  const int total = s_total;
-  if (tid < U) {
-    const int base = __ldcg(offsets + e);
-    int gi = before * S_gu;
-    int di = total * S_gu + before * S_dn;
-    for (int p = 0; p < np; ++p) {
-      const int rows = min(kMaxRows, m - p * kMaxRows);
-      const int z = rows | (np > 1 ? 1 << 17 : 0) | (np << kNpassShift);
-      const int row0 = base + p * kMaxRows;
-      for (int s2 = 0; s2 < S_gu; ++s2) tasks[gi++] = TaskEntry{e | (tid << 16), row0, z, s2};
-      for (int s2 = 0; s2 < S_dn; ++s2) tasks[di++] = TaskEntry{e | (tid << 16), row0, z | (1 << 16), s2};
-    }
-  }
-  if (tid == 0) {
-    meta[META_DGU] = total * S_gu;
-    meta[META_DDN] = total * S_dn;
-  }
-}
-
 // T at or below which every token's hidden row stays resident; above it (up to kMaxGatherT)
-// each gate/up task's rows are gathered.
-constexpr int kMaxGatherT = 256;
+// each gate/up task's rows are gathered, from the plan's table of 8-row passes.
+constexpr int kMaxGatherT = kDecGatherMaxT;
+static_assert(kMaxRows == kDecPassRows, "the plan's decode table has the kernel's pass rows");
 
 size_t expert_dec_smem_bytes(int T, int d, int F) {
   if (T <= kMaxRows) {
@@ -925,11 +867,6 @@ int expert_dec_unroute_tasks(int T, int d, int F) {
   // measured slower than the separate, fully parallel un-route kernel
   return T <= kMaxRows && expert_dec_supports(T, d, F) ? (d / kDnRows) * ((T + kComputeWarps - 1) / kComputeWarps)
                                                        : 0;
-}
-
-cudaError_t launch_dec_plan(const ExpertArgs& a, TaskEntry* tasks_d, cudaStream_t stream) {
-  return launch_pdl(dec_plan_kernel, dim3(1), dim3(1024), 0, stream, a.meta, const_cast<int*>(a.meta), a.touched,
-                    a.counts, a.offsets, tasks_d, a.S_gu, a.S_dn);
 }
 
 cudaError_t launch_expert_dec(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,

@@ -32,6 +32,10 @@ constexpr int kDecSetWords = 1024 + 32 + 32;
 constexpr int kDecReadyWords = 1024;
 constexpr int kDecTicketWord = 1024 + 32;
 constexpr size_t kZeroedPrefix = 256 + size_t(2) * kDecSetWords * 4;
+// The decode kernel's own task table (8-row passes) serves 8 < T <= kDecGatherMaxT; the plan
+// writes it alongside its own table for those batches.
+constexpr int kDecPassRows = 8;
+constexpr int kDecGatherMaxT = 256;
 constexpr int kRowsPerPass = 64;    // token rows handled per pass (4 MMA groups of 16)
 constexpr int kGroupRows = 16;      // MMA N per group
 constexpr int kMaxGroups = kRowsPerPass / kGroupRows;

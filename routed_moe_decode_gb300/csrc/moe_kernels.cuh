@@ -24,6 +24,8 @@ struct PlanArgs {
   float* route_w;
   TaskEntry* tasks;
   int* hist;  // [ceil(T * k / kPlanSlice), E] scratch of the multi-CTA plan (many routes)
+  // the decode kernel's table of 8-row passes (8 < T <= kDecGatherMaxT), or null
+  TaskEntry* tasks_d;
 };
 
 // The fused front (router + plan + FP16 hidden) for T * k up to kFrontMaxRoutes.
@@ -362,12 +364,11 @@ cudaError_t launch_expert_dec_front(const ExpertArgs& a, const DecFront& f, cons
                                     const CUtensorMap& tm_w2, const CUtensorMap& tm_s13, const CUtensorMap& tm_s2,
                                     int num_sms, cudaStream_t stream);
 // true when the decode kernel gathers each task's hidden rows (T > 8): it then reads its own
-// task table of 8-row passes, built from the plan by launch_dec_plan into tasks_d
+// task table of 8-row passes, which the plan writes into tasks_d
 bool expert_dec_gathers(int T);
 // un-route tasks the decode kernel appends when it runs the un-route itself (one per down
 // stripe; T <= 8), or 0
 int expert_dec_unroute_tasks(int T, int d, int F);
-cudaError_t launch_dec_plan(const ExpertArgs& a, TaskEntry* tasks_d, cudaStream_t stream);
 // number of un-route tasks the decode kernel appends when it runs the un-route itself
 int expert_mma_unroute_tasks(int T, int S_dn);
 int encode_codes_map(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes);
