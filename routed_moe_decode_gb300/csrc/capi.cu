@@ -177,6 +177,7 @@ moe::ExpertArgs expert_args(const moe_shape* s, const WsLayout& L, void* ws, con
   a.out = static_cast<__nv_bfloat16*>(out);
   a.e_lo = r.lo;
   a.wait_limit = moe::kDefaultWaitLimit;
+  a.poison_dn = -1;
   return a;
 }
 
@@ -274,9 +275,6 @@ static void fill_plan_args(moe::PlanArgs& a, const moe_shape* shape, const WsLay
   a.route_w = at<float>(workspace, L.route_w);
   a.tasks = at<moe::TaskEntry>(workspace, L.tasks);
   a.hist = at<int>(workspace, L.hist);
-  a.tasks_d = (shape->T > moe::kDecPassRows && shape->T <= moe::kDecGatherMaxT)
-                  ? at<moe::TaskEntry>(workspace, L.tasks_d)
-                  : nullptr;
   a.e_lo = r.lo;
   a.e_hi = r.hi;
 }
@@ -428,14 +426,9 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
       if (e != cudaSuccess) { set_error("expert_dec (own front) launch", e); return MOE_ERR_CUDA; }
     } else if (moe::expert_dec_supports(shape->T, shape->d, shape->ffn)) {
       moe::ExpertArgs ad = a;
-      if (moe::expert_dec_gathers(shape->T)) {
-        // the plan wrote the decode kernel's table of 8-row passes
-        moe::TaskEntry* tasks_d = at<moe::TaskEntry>(workspace, L.tasks_d);
-        rc = poison(tasks_d, moe::META_DGU);
-        if (rc != MOE_OK) return rc;
-        ad.tasks = tasks_d;
-        ad.task_cap = L.max_tasks_d;
-      }
+      // gathered rows: the kernel derives its 8-row passes from the plan's per-expert arrays;
+      // the failure-path self test names the down task to poison instead of rewriting a table
+      if (moe::expert_dec_gathers(shape->T)) ad.poison_dn = poison_dn_task;
       e = moe::launch_expert_dec(ad, tm13, tm2, ts13, ts2, di.num_sms, stream);
       if (e != cudaSuccess) { set_error("expert_dec launch", e); return MOE_ERR_CUDA; }
     } else {

@@ -75,6 +75,11 @@ struct Arena {
   int xpitch, hpitch, x_bytes, xslot_bytes, slot_bytes, hslots;
 };
 
+constexpr int kDnGroupGathered = 4, kDnGroupResident = 2;
+constexpr int kNpassShift = 20, kGroupShift = 28;
+__device__ __forceinline__ int task_npass(int z) { return max(1, (z >> kNpassShift) & 0xff); }
+__device__ __forceinline__ int task_group(int z) { return max(1, (z >> kGroupShift) & 0x7); }
+
 // The plan of the kernel's own front (T <= 8 tokens, at most 256 routes), after the h slots.
 constexpr int kFrontRoutes = 256;
 struct FrontSmem {
@@ -89,6 +94,38 @@ struct FrontSmem {
   int U;
   uint32_t parity;
 };
+
+// The gathered mode's passes, derived by every CTA from the plan's per-expert arrays: per
+// touched index u, a[u] = expert | rows << 16 and b[u] = bucket start | first pass << 16
+// (8-row passes numbered across the touched experts in order), and per pass its touched
+// index (at most E + T k / 8 <= 2048 passes for T <= 256); total = passes.
+struct GatherPlan {
+  uint32_t a[1024];
+  uint32_t b[1024];
+  uint16_t pass_u[2048];
+  int U, total;
+  int wsum[16];  // scratch of the prefix over the pass counts (one per warp)
+};
+
+// Entry i (gate/up tasks by pass and stripe, then down tasks) of the gathered mode: its
+// pass, that pass's touched index, rows, first routed row and the pass count of its expert
+// (S_gu and S_dn are powers of two).  Down task `poison` (self test) waits for touched index
+// U instead.
+__device__ __forceinline__ TaskEntry gather_entry(const GatherPlan& gp, int i, int ngu, int S_gu, int S_dn,
+                                                  int poison) {
+  const bool dn = i >= ngu;
+  const int j = dn ? i - ngu : i;
+  const int S = dn ? S_dn : S_gu;
+  const int P = j >> (__ffs(S) - 1), s2 = j & (S - 1);
+  const int lo = gp.pass_u[P];
+  const int e = static_cast<int>(gp.a[lo] & 0xffffu), c = static_cast<int>(gp.a[lo] >> 16);
+  const int p = P - static_cast<int>(gp.b[lo] >> 16);
+  const int np = (c + kMaxRows - 1) / kMaxRows;
+  const int rows = min(kMaxRows, c - p * kMaxRows);
+  const int z = rows | (dn ? 1 << 16 : 0) | (np > 1 ? 1 << 17 : 0) | (np << kNpassShift);
+  const int u = (dn && j == poison) ? gp.U : lo;
+  return TaskEntry{e | (u << 16), static_cast<int>(gp.b[lo] & 0xffffu) + p * kMaxRows, z, s2};
+}
 
 template <bool kGather>
 __host__ __device__ inline Arena arena_of(int T, int d, int F, int extra = 0) {
@@ -113,15 +150,11 @@ __host__ __device__ inline Arena arena_of(int T, int d, int F, int extra = 0) {
 // of G), except the last `nsingle` (at least one per CTA of the grid), one stripe per ticket,
 // so that the final claims are short; then, with the un-route fused, one un-route task per
 // down stripe and group of eight tokens (one token per compute warp).  A group task copies
-// its h rows once
-// and pays one claim and one hand-off for G stripes.  The task entry carries G in bits 28-30
-// of z (the expert's pass count of a gathered table sits in bits 20-27).  Group size: 4 when
+// its h rows once and pays one claim and one hand-off for G stripes.  The task entry carries
+// G in bits 28-30 of z (the expert's pass count of gathered passes sits in bits 20-27).
+// Group size (constants above): 4 when
 // the rows are gathered (many short down tasks: T > 8), 2 with the rows resident (T <= 8,
 // few tasks per CTA, where larger groups cost more in balance than they save).
-constexpr int kDnGroupGathered = 4, kDnGroupResident = 2;
-constexpr int kNpassShift = 20, kGroupShift = 28;
-__device__ __forceinline__ int task_npass(int z) { return max(1, (z >> kNpassShift) & 0xff); }
-__device__ __forceinline__ int task_group(int z) { return max(1, (z >> kGroupShift) & 0x7); }
 struct TicketMap {
   int ngu, G, ngroup, nsingle, ndn_tickets;
 };
@@ -179,6 +212,17 @@ __device__ __forceinline__ void front_task_of(const FrontSmem& fs, int i, const 
   if (i < m.ngu + m.ndn_tickets) {
     int G;
     e0 = front_entry(fs, ticket_entry(i, m, G), m.ngu, S_gu, S_dn);
+    e0.z |= G << kGroupShift;
+  } else {
+    e0 = unroute_entry(i - m.ngu - m.ndn_tickets, S_dn);
+  }
+}
+
+__device__ __forceinline__ void gather_task_of(const GatherPlan& gp, int i, const TicketMap& m, int S_gu, int S_dn,
+                                               int poison, TaskEntry& e0) {
+  if (i < m.ngu + m.ndn_tickets) {
+    int G;
+    e0 = gather_entry(gp, ticket_entry(i, m, G), m.ngu, S_gu, S_dn, poison);
     e0.z |= G << kGroupShift;
   } else {
     e0 = unroute_entry(i - m.ngu - m.ndn_tickets, S_dn);
@@ -334,10 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* arena = reinterpret_cast<uint8_t*>(&sm) + ((sizeof(Smem) + 127) & ~size_t(127));
-  const Arena ar = arena_of<kGather>(a.T, a.d, a.F, kFront ? static_cast<int>(sizeof(FrontSmem)) : 0);
+  const Arena ar = arena_of<kGather>(
+      a.T, a.d, a.F, kFront ? static_cast<int>(sizeof(FrontSmem)) : kGather ? static_cast<int>(sizeof(GatherPlan)) : 0);
   uint8_t* xs = arena;                 // hidden rows (resident) or the gathered-row slots
   uint8_t* hs = arena + ar.x_bytes;    // h slots
-  FrontSmem& fs = *reinterpret_cast<FrontSmem*>(hs + ar.hslots * ar.slot_bytes);  // kFront only
+  FrontSmem& fs = *reinterpret_cast<FrontSmem*>(hs + ar.hslots * ar.slot_bytes);   // kFront only
+  GatherPlan& gp = *reinterpret_cast<GatherPlan*>(hs + ar.hslots * ar.slot_bytes);  // kGather only
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int tcnt0 = 2;
   if (tid == 0) trace_ev(a, 5, tcnt0, 14, 0);  // kernel entry, before the dependency wait
@@ -460,6 +506,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) fs.U = U;
     __syncthreads();
     front_U = U;
+  } else if constexpr (kGather) {
+    // ---- the 8-row passes from the plan's per-expert arrays (every CTA the same) ----
+    // thread t takes touched indices 3t .. 3t+2: their experts, rows and bucket starts, and
+    // the exclusive prefix of their pass counts (warp scan, then one over the warp totals)
+    const int U = __ldg(a.meta + META_U);
+    int np[3], run = 0;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int u = 3 * tid + j;
+      np[j] = 0;
+      if (u < U) {
+        const int e = __ldg(a.touched + u);
+        const int c = __ldg(a.counts + e);
+        gp.a[u] = static_cast<uint32_t>(e) | (static_cast<uint32_t>(c) << 16);
+        gp.b[u] = static_cast<uint32_t>(__ldg(a.offsets + e));
+        np[j] = (c + kMaxRows - 1) / kMaxRows;
+      }
+      run += np[j];
+    }
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) gp.wsum[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+      int acc = 0;
+      for (int w = 0; w < kThreads / 32; ++w) {
+        const int v = gp.wsum[w];
+        gp.wsum[w] = acc;
+        acc += v;
+      }
+      gp.U = U;
+      gp.total = acc;
+    }
+    __syncthreads();
+    int p0 = gp.wsum[warp] + incl - run;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int u = 3 * tid + j;
+      if (u < U) gp.b[u] |= static_cast<uint32_t>(p0) << 16;
+      for (int p = 0; p < np[j]; ++p) gp.pass_u[p0 + p] = static_cast<uint16_t>(u);
+      p0 += np[j];
+    }
+    __syncthreads();
   } else {
     __syncthreads();
   }
@@ -470,8 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------- task fetcher + weight producer -------------
     const uint64_t pol = policy_evict_first();
-    const int ngu = kFront ? front_U * a.S_gu : __ldg(a.meta + (kGather ? META_DGU : META_NGU));
-    const int ndn = kFront ? front_U * a.S_dn : __ldg(a.meta + (kGather ? META_DDN : META_NDN));
+    const int ngu = kFront ? front_U * a.S_gu : kGather ? gp.total * a.S_gu : __ldg(a.meta + META_NGU);
+    const int ndn = kFront ? front_U * a.S_dn : kGather ? gp.total * a.S_dn : __ldg(a.meta + META_NDN);
     const TicketMap tmap = ticket_map(ngu, ndn, static_cast<int>(gridDim.x), a.S_dn,
                                       kGather ? kDnGroupGathered : kDnGroupResident);
     const int ntot = ngu + tmap.ndn_tickets + (kFused ? a.ncb : 0);  // tickets
@@ -483,6 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       if (cur >= ntot) entry = kEnd;
       else if (kFront) front_task_of(fs, cur, tmap, a.S_gu, a.S_dn, entry);
+      else if (kGather) gather_task_of(gp, cur, tmap, a.S_gu, a.S_dn, a.poison_dn, entry);
       else task_of(a, cur, tmap, entry);
     }
     // the tokens of a gate/up task's routed rows, loaded as soon as its entry is known
@@ -587,6 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur = static_cast<int>(atomicAdd(ctr_ticket, 1u)) + static_cast<int>(gridDim.x);
         if (cur >= ntot) entry = kEnd;
         else if (kFront) front_task_of(fs, cur, tmap, a.S_gu, a.S_dn, entry);
+        else if (kGather) gather_task_of(gp, cur, tmap, a.S_gu, a.S_dn, a.poison_dn, entry);
         else task_of(a, cur, tmap, entry);
       }
       tok = load_tokens();
@@ -715,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           unroute4_pre<kFront>(a, t, c, u, fs.pos, fs.w);
           // every down task of the stripe has published its y columns
           const uint32_t dn_per_stripe = static_cast<uint32_t>(
-              kFront ? front_U : __ldg(a.meta + (kGather ? META_DDN : META_NDN)) / a.S_dn);
+              kFront ? front_U : kGather ? gp.total : __ldg(a.meta + META_NDN) / a.S_dn);
           if (tr) trace_ev(a, trole, tcnt, 12, n);
           if (!warp_wait_counter(ctr_dn + te.w, dn_per_stripe, &sm.abort_flag, a.status, a.wait_limit)) break;
           if (tr) trace_ev(a, trole, tcnt, 13, n);
@@ -828,17 +923,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // T at or below which every token's hidden row stays resident; above it (up to kMaxGatherT)
-// each gate/up task's rows are gathered, from the plan's table of 8-row passes.
-constexpr int kMaxGatherT = kDecGatherMaxT;
-static_assert(kMaxRows == kDecPassRows, "the plan's decode table has the kernel's pass rows");
+// each gate/up task's rows are gathered, its tasks being 8-row passes.
+constexpr int kMaxGatherT = 256;
 
 size_t expert_dec_smem_bytes(int T, int d, int F) {
   if (T <= kMaxRows) {
     const Arena ar = arena_of<false>(T, d, F);
     return fixed_smem_bytes<false>() + ar.x_bytes + static_cast<size_t>(ar.hslots) * ar.slot_bytes;
   }
-  const Arena ar = arena_of<true>(T, d, F);
-  return fixed_smem_bytes<true>() + ar.x_bytes + static_cast<size_t>(ar.hslots) * ar.slot_bytes;
+  const Arena ar = arena_of<true>(T, d, F, static_cast<int>(sizeof(GatherPlan)));
+  return fixed_smem_bytes<true>() + ar.x_bytes + static_cast<size_t>(ar.hslots) * ar.slot_bytes + sizeof(GatherPlan);
 }
 
 static size_t front_smem_bytes(int T, int d, int F) {
@@ -848,7 +942,8 @@ static size_t front_smem_bytes(int T, int d, int F) {
 
 bool expert_dec_supports(int T, int d, int F) {
   if (T < 1 || T > kMaxGatherT || !expert_mma_supports(d, F)) return false;
-  const int hslots = T <= kMaxRows ? arena_of<false>(T, d, F).hslots : arena_of<true>(T, d, F).hslots;
+  const int hslots = T <= kMaxRows ? arena_of<false>(T, d, F).hslots
+                                   : arena_of<true>(T, d, F, static_cast<int>(sizeof(GatherPlan))).hslots;
   return hslots >= 2 && expert_dec_smem_bytes(T, d, F) <= static_cast<size_t>(kSmemLimit);
 }
 

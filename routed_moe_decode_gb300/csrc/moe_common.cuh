@@ -32,10 +32,6 @@ constexpr int kDecSetWords = 1024 + 32 + 32;
 constexpr int kDecReadyWords = 1024;
 constexpr int kDecTicketWord = 1024 + 32;
 constexpr size_t kZeroedPrefix = 256 + size_t(2) * kDecSetWords * 4;
-// The decode kernel's own task table (8-row passes) serves 8 < T <= kDecGatherMaxT; the plan
-// writes it alongside its own table for those batches.
-constexpr int kDecPassRows = 8;
-constexpr int kDecGatherMaxT = 256;
 constexpr int kRowsPerPass = 64;    // token rows handled per pass (4 MMA groups of 16)
 constexpr int kGroupRows = 16;      // MMA N per group
 constexpr int kMaxGroups = kRowsPerPass / kGroupRows;
@@ -52,7 +48,7 @@ constexpr float kHUnscale = 16.0f;
 
 struct WsLayout {
   size_t status, meta, counts, offsets, touched, gu_start, dn_start, route_pos, pos_tok, route_w;
-  size_t ready, ticket, tasks, tasks_w, tasks_d, hist, x16, hs16, y, total;
+  size_t ready, ticket, tasks, tasks_w, hist, x16, hs16, y, total;
   size_t front_done;  // arrival counter of the fused front, inside the zeroed status block
   size_t dec_parity;  // counter set the decode kernel with its own front uses (zeroed block)
   size_t dec_done;    // its CTA arrival counter (zeroed block)
@@ -61,17 +57,14 @@ struct WsLayout {
   int S_dn;       // down stripes per expert (d / 128)
   int max_tasks;  // capacity of the task table
   int max_tasks_w;  // capacity of the wide kernel's task table (passes of kWideRows rows)
-  int max_tasks_d;  // capacity of the decode kernel's task table (passes of 8 rows)
   int R;          // routes = T * k
 };
 
 // meta words
 // META_YFMT: format of the per-route down outputs y: 0 FP32, 1 FP16(y * 2^-4) (wide kernel);
 // the plan writes 0, the wide kernel's task-table kernel 1, the un-route kernel reads it.
-// META_DGU / META_DDN: gate/up and down task counts of the decode kernel's table of 8-row
-// passes (tasks_d), written by its task-table kernel.
 enum { META_U = 0, META_NGU = 1, META_NDN = 2, META_MAXROWS = 3, META_WGU = 4, META_WDN = 5, META_YFMT = 6,
-       META_DGU = 7, META_DDN = 8, META_WORDS = 16 };
+       META_WORDS = 16 };
 constexpr float kYScale = 0.0625f;  // FP16 per-route down outputs hold y * 2^-4
 constexpr float kYUnscale = 16.0f;
 
@@ -94,7 +87,6 @@ inline WsLayout ws_layout(const moe_shape& s) {
   const int max_passes = s.E + (L.R + kRowsPerPass - 1) / kRowsPerPass;
   L.max_tasks = max_passes * (L.S_gu + L.S_dn);
   L.max_tasks_w = (s.E + (L.R + kWideRows - 1) / kWideRows) * (L.S_gu + L.S_dn);
-  L.max_tasks_d = (s.E + (L.R + 7) / 8) * (L.S_gu + L.S_dn);
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   L.status = take(64);
@@ -115,7 +107,6 @@ inline WsLayout ws_layout(const moe_shape& s) {
   L.ticket = take(4);
   L.tasks = take(size_t(L.max_tasks) * sizeof(TaskEntry));
   L.tasks_w = take(size_t(L.max_tasks_w) * sizeof(TaskEntry));
-  L.tasks_d = take(size_t(L.max_tasks_d) * sizeof(TaskEntry));
   L.hist = take(size_t((L.R + kPlanSlice - 1) / kPlanSlice) * s.E * 4);  // multi-CTA plan: a histogram per slice
   L.x16 = take(size_t(s.T) * s.d * 2);
   L.hs16 = take(size_t(L.R) * s.ffn * 2);

@@ -24,8 +24,6 @@ struct PlanArgs {
   float* route_w;
   TaskEntry* tasks;
   int* hist;  // [ceil(T * k / kPlanSlice), E] scratch of the multi-CTA plan (many routes)
-  // the decode kernel's table of 8-row passes (8 < T <= kDecGatherMaxT), or null
-  TaskEntry* tasks_d;
 };
 
 // The fused front (router + plan + FP16 hidden) for T * k up to kFrontMaxRoutes.
@@ -83,6 +81,9 @@ struct ExpertArgs {
   int e_lo;  // first expert of the weight tensors passed in (expert e's weights are entry e - e_lo)
   int ncb;  // un-route tasks appended to the task order (0: the un-route runs as its own kernel)
   int task_cap;  // entries the task table has room for
+  // self test of the failure path: this down task (index among the down tasks of the
+  // decode kernel's 8-row passes) waits for a readiness counter nothing publishes; -1: none
+  int poison_dn;
   // every bounded wait of the expert kernels gives up after this many clock cycles
   // (kDefaultWaitLimit; the self tests shorten it to exercise the failure path)
   long long wait_limit;
@@ -363,8 +364,8 @@ bool expert_dec_front_supports(int T, int d, int F, int E, int k);
 cudaError_t launch_expert_dec_front(const ExpertArgs& a, const DecFront& f, const CUtensorMap& tm_w13,
                                     const CUtensorMap& tm_w2, const CUtensorMap& tm_s13, const CUtensorMap& tm_s2,
                                     int num_sms, cudaStream_t stream);
-// true when the decode kernel gathers each task's hidden rows (T > 8): it then reads its own
-// task table of 8-row passes, which the plan writes into tasks_d
+// true when the decode kernel gathers each task's hidden rows (T > 8): its tasks are then
+// 8-row passes, which every CTA derives from the plan's per-expert arrays
 bool expert_dec_gathers(int T);
 // un-route tasks the decode kernel appends when it runs the un-route itself (one per down
 // stripe; T <= 8), or 0

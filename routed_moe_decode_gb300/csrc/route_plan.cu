@@ -366,30 +366,6 @@ __device__ __forceinline__ void plan_block_cached(const PlanArgs& a, const int* 
     const int z = rows | (dn ? 1 << 16 : 0) | (c > kRowsPerPass ? 1 << 17 : 0);
     tasks[i] = make_int4(e | (rk2 << 16), ps.off[e] + p * kRowsPerPass, z, s2);
   }
-  if (a.tasks_d != nullptr) {
-    // the decode kernel's table: passes of at most kDecPassRows rows, all gate/up tasks
-    // (touched order, pass, stripe) then all down tasks; z carries the expert's pass count in
-    // bits 20-27 (the readiness target of its down tasks) and bit 17 when it has several
-    const int np8 = (cnt + kDecPassRows - 1) / kDecPassRows;
-    uint32_t tot8 = 0;
-    int unused = 0;
-    const int p8 = static_cast<int>(block_scan_max<uint32_t>(static_cast<uint32_t>(np8), 0, ps, tot8, unused));
-    const int ngu8 = static_cast<int>(tot8) * a.S_gu;
-    if (flag) {
-      for (int p = 0; p < np8; ++p) {
-        const int rows = min(kDecPassRows, cnt - p * kDecPassRows);
-        const int z = rows | (np8 > 1 ? 1 << 17 : 0) | (np8 << 20);
-        const int row0 = off + p * kDecPassRows, x = tid | (rank << 16);
-        for (int s2 = 0; s2 < a.S_gu; ++s2) a.tasks_d[(p8 + p) * a.S_gu + s2] = TaskEntry{x, row0, z, s2};
-        for (int s2 = 0; s2 < a.S_dn; ++s2)
-          a.tasks_d[ngu8 + (p8 + p) * a.S_dn + s2] = TaskEntry{x, row0, z | (1 << 16), s2};
-      }
-    }
-    if (tid == 0) {
-      a.meta[META_DGU] = ngu8;
-      a.meta[META_DDN] = static_cast<int>(tot8) * a.S_dn;
-    }
-  }
 }
 
 // plan of the routes in ids_src/w_src by the best-fitting variant (R <= kPlanCached * 1024)
