@@ -60,7 +60,10 @@ static_assert(kWideRows % 16 == 0 && kWideRows <= 256, "MMA N limit");
 struct Smem {
   uint8_t ring_b[kStagesB][kStageB];
   uint8_t ring_a[kStagesA][kStageA];
-  float xch[2][32 * 64];           // per epilogue group: gate/up values exchanged between lane halves
+  // per epilogue group: gate/up values exchanged between lane halves; the FP16 down outputs
+  // of a 32-column slice staged for row-contiguous stores
+  float xch[2][32 * 64];
+  __half hstage[2][32 * 64];       // per epilogue group: the FP16 h values of a slice
   // per activation warp: source of each of its rows in 16-byte units (fits 32 bits for every
   // supported shape: T * d and T * k * ffn elements are below 2^34)
   uint32_t rowoff16[kActWarps][kWideRows / kActWarps];
@@ -451,40 +454,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kWarpMma) {
-    // ---------------- MMA issuer (one lane; the whole warp takes the tasks) ----------------
+    // ---------------- MMA issuer: the warp waits, one elected lane issues ----------------
+    // Descriptors and tensor-memory addresses are computed by the whole warp in converged
+    // code; only the tcgen05 instructions run on the elected lane.
     int stage = 0, abuf = 0, dbuf = 0, n = 0;
     uint32_t phase = 0, aphase = 0, dphase = 0;
     bool ok = true;
+    const uint64_t bdesc0 = smem_desc_sw128(ringb0, 1024);
     while (ok) {
       TaskEntry te;
       if (!take_task(sm, n++, te, a.status, a.wait_limit)) break;
       const Task tk = unpack(te, a);
       if (!tk.valid) break;
-      if (lane == 0) {
-        const uint32_t idesc = idesc_f16_f32(128, mma_n(tk.rows));
-        if (!bounded_wait(smem_addr(&sm.d_empty[dbuf]), dphase ^ 1u, sm, a.status, a.wait_limit)) ok = false;
+      const uint32_t idesc = idesc_f16_f32(128, mma_n(tk.rows));
+      if (!warp_wait(smem_addr(&sm.d_empty[dbuf]), dphase ^ 1u, sm, a.status, a.wait_limit)) break;
+      tc_fence_after();
+      const uint32_t dcol = tmem + kDCol0 + dbuf * kWideRows;
+      for (int c = 0; c < tk.nck; ++c) {
+        if (!warp_wait(smem_addr(&sm.a_full[abuf]), aphase, sm, a.status, a.wait_limit)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&sm.full_b[stage]), phase, sm, a.status, a.wait_limit)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t dcol = tmem + kDCol0 + dbuf * kWideRows;
-        for (int c = 0; ok && c < tk.nck; ++c) {
-          if (!bounded_wait(smem_addr(&sm.a_full[abuf]), aphase, sm, a.status, a.wait_limit)) { ok = false; break; }
-          if (!bounded_wait(smem_addr(&sm.full_b[stage]), phase, sm, a.status, a.wait_limit)) { ok = false; break; }
-          tc_fence_after();
+        const uint64_t bd = bdesc0 + static_cast<uint64_t>((stage * kStageB) >> 4);
+        const uint32_t acol = tmem + abuf * 64;
+        if (elect_one()) {
           fence_proxy_async_smem();
-          const uint32_t bbase = ringb0 + stage * kStageB;
 #pragma unroll
-          for (int kk = 0; kk < kChunkK / 16; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(bbase + (kk >> 2) * kAtomB + (kk & 3) * 32, 1024);
-            tc_mma_f16_ts(dcol, tmem + abuf * 64 + kk * 8, bdesc, idesc, (c > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kChunkK / 16; ++kk)
+            tc_mma_f16_ts(dcol, acol + kk * 8, bd + static_cast<uint64_t>(((kk >> 2) * kAtomB + (kk & 3) * 32) >> 4),
+                          idesc, (c > 0 || kk > 0) ? 1u : 0u);
           tc_commit(smem_addr(&sm.empty_b[stage]));
           tc_commit(smem_addr(&sm.a_empty[abuf]));
-          if (++stage == kStagesB) { stage = 0; phase ^= 1u; }
-          if (++abuf == kNumA) { abuf = 0; aphase ^= 1u; }
         }
-        if (ok) tc_commit(smem_addr(&sm.d_full[dbuf]));
+        __syncwarp();
+        if (++stage == kStagesB) { stage = 0; phase ^= 1u; }
+        if (++abuf == kNumA) { abuf = 0; aphase ^= 1u; }
       }
+      if (!ok) break;
+      if (elect_one()) tc_commit(smem_addr(&sm.d_full[dbuf]));
+      __syncwarp();
       if (++dbuf == kNumD) { dbuf = 0; dphase ^= 1u; }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
     if (lane == 0) {
       // every issued MMA completes before tensor memory is released
@@ -525,33 +533,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) xch[(up ? j : 16 + j) * 64 + nF] = __uint_as_float(up ? v[j] : v[16 + j]);
           named_bar_sync(4 + grp, 128);
-          __half* hcol = a.hs16 + static_cast<size_t>(tk.row0) * a.F + tk.s * kGuRows + nF;
+          __half* hst = sm.hstage[grp];
           const int j0 = up ? 16 : 0;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int c = c0 + j0 + j;
             const float own = __uint_as_float(up ? v[16 + j] : v[j]) * sc13, other = xch[(j0 + j) * 64 + nF] * sc13;
             const float g = up ? other : own, u = up ? own : other;
-            if (c < tk.rows)
-              hcol[static_cast<size_t>(c) * a.F] = h_store_value(__fdividef(g, 1.0f + __expf(-g)) * u, a.status);
+            hst[(j0 + j) * 64 + nF] =
+                c < tk.rows ? h_store_value(__fdividef(g, 1.0f + __expf(-g)) * u, a.status) : __float2half_rn(0.f);
           }
           named_bar_sync(4 + grp, 128);
+          // the slice's h rows (32 routed rows x 64 F values) in 16-byte pieces
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int q = i + 128 * t, r = q >> 3, part = q & 7;
+            if (c0 + r < tk.rows)
+              *reinterpret_cast<uint4*>(a.hs16 + static_cast<size_t>(tk.row0 + c0 + r) * a.F + tk.s * kGuRows + part * 8) =
+                  *reinterpret_cast<const uint4*>(hst + r * 64 + part * 8);
+          }
         } else {
-          // per-route outputs as FP16(y * 2^-4): half the bytes of FP32 for the un-route to read
-          __half* ycol = reinterpret_cast<__half*>(a.y) + static_cast<size_t>(tk.row0) * a.d + tk.s * kDnRows + i;
+          // per-route outputs as FP16(y * 2^-4), staged so that each routed row's 128 values
+          // leave in 16-byte pieces
+          __half* yst = reinterpret_cast<__half*>(xch);
           bool sat = false;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if (c0 + j < tk.rows) {
-              float yv = __uint_as_float(v[j]) * (sc2 * kYScale);
-              if (fabsf(yv) > 65504.f) {
-                sat = true;
-                yv = copysignf(65504.f, yv);
-              }
-              ycol[static_cast<size_t>(c0 + j) * a.d] = __float2half_rn(yv);
+            float yv = __uint_as_float(v[j]) * (sc2 * kYScale);
+            if (c0 + j < tk.rows && fabsf(yv) > 65504.f) {
+              sat = true;
+              yv = copysignf(65504.f, yv);
             }
+            yst[j * kDnRows + i] = __float2half_rn(yv);
           }
           if (sat) atomicOr(a.status, static_cast<int>(MOE_DEV_Y_SATURATED));
+          named_bar_sync(4 + grp, 128);
+          __half* y16 = reinterpret_cast<__half*>(a.y);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int q = i + 128 * t, r = q >> 4, part = q & 15;
+            if (c0 + r < tk.rows)
+              *reinterpret_cast<uint4*>(y16 + static_cast<size_t>(tk.row0 + c0 + r) * a.d + tk.s * kDnRows + part * 8) =
+                  *reinterpret_cast<const uint4*>(yst + r * kDnRows + part * 8);
+          }
+          named_bar_sync(4 + grp, 128);
         }
       }
       // the accumulator is read: hand it back to the MMA warp
@@ -575,6 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
 }
+
+static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory per CTA (227 KB)");
 
 size_t expert_wide_smem_bytes() { return sizeof(Smem) + 1024; }
 
