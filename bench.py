@@ -317,8 +317,9 @@ def measure(cfg, moe, torch, dist, dev, Wd, algo, K, W, kernel_samples, e2e_step
         kernels_per_step = moe.layer_launches(shape)
     else:
         front_kernels = 3
-        # the SIMT path runs two expert kernels, the wide kernel one plus its task-table kernel
-        expert_kernels = 2 if run_algo in (moe.ALGO_SIMT, moe.ALGO_WIDE) else 1
+        # the SIMT path runs two expert kernels; the wide kernel runs after its route-order
+        # gather and its task-table kernel
+        expert_kernels = {moe.ALGO_SIMT: 2, moe.ALGO_WIDE: 3}.get(run_algo, 1)
         kernels_per_step = front_kernels + expert_kernels + (0 if fused_unroute else 1)
 
     # ---- unique experts per layer (outside any timed region) ----
@@ -504,7 +505,7 @@ def measure(cfg, moe, torch, dist, dev, Wd, algo, K, W, kernel_samples, e2e_step
                                 + ("<own front, fused un-route> (the whole layer)" if one_launch
                                    else "<fused un-route>" if fused_unroute
                                    else "<gathered rows>" if dec_kernel else "")
-                                + (" (after its task-table kernel)" if run_algo == moe.ALGO_WIDE else "")) if kname
+                                + (" (with its route-order gather and task-table kernels)" if run_algo == moe.ALGO_WIDE else "")) if kname
                                else "simt kernels",
                      "kernel_us": 1e3 * k_avg_ms, "kernel_samples": Kk,
                      "kernel_timing": "the timed region's events (K launches of this one kernel)" if one_launch

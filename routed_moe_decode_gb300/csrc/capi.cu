@@ -108,6 +108,26 @@ int encode_scales_map(CUtensorMap* tm, const void* base, uint32_t row_bytes, uin
   return MOE_OK;
 }
 
+// 2-D FP16 tensor map over a row-major [rows, cols] matrix: 64-element (128-byte) wide boxes
+// of box_rows rows with the 128-byte swizzle (the K-major operand layout of the MMAs).
+int encode_f16_rows_map(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn enc = nullptr;
+  if (get_encoder(&enc) != MOE_OK) { snprintf(g_last_error, sizeof g_last_error, "no cuTensorMapEncodeTiled"); return MOE_ERR_CUDA; }
+  if (cols % 64 || box_rows == 0 || box_rows > 256) return MOE_ERR_INVALID_ARG;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
 void set_last_error_message(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
 
 }  // namespace moe
@@ -437,6 +457,11 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     }
     if (a.ncb > 0) return MOE_OK;
   } else if (use_wide) {
+    // the hidden rows in route order, in the upper half of the per-route output buffer (the
+    // wide kernel's per-route outputs are FP16 and fill only the lower half)
+    __half* xs = reinterpret_cast<__half*>(a.y) + static_cast<size_t>(L.R) * shape->d;
+    e = moe::launch_wide_gather(a, xs, di.num_sms, stream);
+    if (e != cudaSuccess) { set_error("wide gather launch", e); return MOE_ERR_CUDA; }
     // the wide kernel's own task table (passes of kWideRows rows), from the plan's arrays
     moe::TaskEntry* tasks_w = at<moe::TaskEntry>(workspace, L.tasks_w);
     e = moe::launch_wide_plan(a, tasks_w, stream);
@@ -446,7 +471,14 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     moe::ExpertArgs aw = a;
     aw.tasks = tasks_w;
     aw.task_cap = L.max_tasks_w;
-    e = moe::launch_expert_wide(aw, tm13, tm2, di.num_sms, stream);
+    // gate/up passes read their hidden rows, down passes the expert's h rows, as contiguous
+    // rows in 64-row boxes
+    CUtensorMap tmxs, tmh;
+    rc = moe::encode_f16_rows_map(&tmxs, xs, static_cast<uint64_t>(shape->d), static_cast<uint64_t>(L.R), 64);
+    if (rc != MOE_OK) return rc;
+    rc = moe::encode_f16_rows_map(&tmh, a.hs16, static_cast<uint64_t>(shape->ffn), static_cast<uint64_t>(L.R), 64);
+    if (rc != MOE_OK) return rc;
+    e = moe::launch_expert_wide(aw, tm13, tm2, tmxs, tmh, di.num_sms, stream);
     if (e != cudaSuccess) { set_error("expert_wide launch", e); return MOE_ERR_CUDA; }
   } else {
     rc = poison(at<moe::TaskEntry>(workspace, L.tasks), moe::META_NGU);
@@ -798,7 +830,7 @@ int moe_layer_launches(const moe_shape* shape) {
   const int front = R <= moe::kFrontMaxRoutes ? 1 : 2 + (R <= 16 * 1024 ? 1 : 3);
   const int algo = auto_choice(shape);
   int experts = 1;
-  if (algo == MOE_ALGO_WIDE) experts = 2;  // task-table kernel + wide kernel
+  if (algo == MOE_ALGO_WIDE) experts = 3;  // route-order gather + task-table kernel + wide kernel
   const int unroute =
       (algo == MOE_ALGO_MMA && fused_unroute_tasks(shape) > 0) ? 0 : 1;
   return front + experts + unroute;

@@ -18,11 +18,13 @@
 //         64-byte swizzle) and its E4M3 block scales become exact FP16 in registers and are
 //         stored into tensor memory, where they are the A operand (M = 128);
 //   12    task fetcher + weight producer (TMA codes, cp.async scales);
-//   13-16 activation producers: the pass's routed rows (FP16 hidden rows for gate/up, FP16 h
-//         rows for down) copied 16 bytes at a time into 128-byte swizzled K-major tiles, the B
-//         operand (N up to 192);
-//   17    MMA issuer and tensor-memory owner: 8 kind::f16 MMAs per chunk into one of two
-//         accumulator buffers, so the epilogue of a task overlaps the next task's MMAs.
+//   13    activation producer: the pass's routed rows as 128-byte swizzled K-major tiles, the
+//         B operand (N up to 192), by TMA in 64-row boxes.  The rows of a pass are contiguous:
+//         for gate/up the FP16 hidden rows in route order (wide_gather_kernel writes them
+//         before this kernel), for down the expert's h rows;
+//   14    MMA issuer and tensor-memory owner: 8 kind::f16 MMAs per chunk into one of two
+//         accumulator buffers, so the epilogue of a task overlaps the next task's MMAs; the
+//         warp waits and forms the descriptors, one elected lane issues.
 // Tensor memory (512 columns): two A buffers of 64 columns, two accumulators of 192 columns.
 #include "moe_kernels.cuh"
 
@@ -42,13 +44,14 @@ constexpr int kNumD = 2;                             // accumulators (kWideRows 
 constexpr int kDCol0 = kNumA * 64;
 constexpr int kTmemCols = 512;
 constexpr int kTaskSlots = 8;
-constexpr int kActWarps = 4;
+constexpr int kActWarps = 1;
 constexpr int kEpiWarps = 8;   // two groups of four: alternate 32-column slices of an accumulator
 constexpr int kWarpDeq0 = kEpiWarps;                           // 8-11
 constexpr int kWarpFetch = kWarpDeq0 + 4;                      // 12
-constexpr int kWarpAct0 = kWarpFetch + 1;                      // 13-16
-constexpr int kWarpMma = kWarpAct0 + kActWarps;                // 17
-constexpr int kThreads = 32 * (kWarpMma + 1);                  // 576
+constexpr int kWarpAct0 = kWarpFetch + 1;                      // 13
+constexpr int kWarpMma = kWarpAct0 + kActWarps;                // 14
+constexpr int kThreads = 32 * (kWarpMma + 1);                  // 480
+constexpr int kBoxRows = 64;                                   // rows per TMA box of a pass's activation rows
 constexpr int kTaskConsumers = kActWarps + 4 + 1 + kEpiWarps;  // activation, dequant, MMA, epilogue warps
 // Bound of the drain waits at exit (copies and MMAs already issued complete within
 // microseconds; after an abort a barrier may lack the arrival of a role that gave up).
@@ -64,9 +67,6 @@ struct Smem {
   // of a 32-column slice staged for row-contiguous stores
   float xch[2][32 * 64];
   __half hstage[2][32 * 64];       // per epilogue group: the FP16 h values of a slice
-  // per activation warp: source of each of its rows in 16-byte units (fits 32 bits for every
-  // supported shape: T * d and T * k * ffn elements are below 2^34)
-  uint32_t rowoff16[kActWarps][kWideRows / kActWarps];
   TaskEntry task[kTaskSlots];
   uint64_t full_a[kStagesA];
   uint64_t empty_a[kStagesA];
@@ -129,15 +129,6 @@ __device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* 
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&sm.task_empty[q]));
   return true;
-}
-
-__device__ __forceinline__ __half h_store_value(float h, int* status) {
-  float v = h * kHScale;
-  if (fabsf(v) > 65504.f) {
-    atomicOr(status, static_cast<int>(MOE_DEV_H_SATURATED));
-    v = copysignf(65504.f, v);
-  }
-  return __float2half_rn(v);
 }
 
 // MMA N for a pass of `rows` routed rows: a multiple of 16 (kind::f16 with M = 128).
@@ -210,8 +201,44 @@ __global__ void __launch_bounds__(1024) wide_plan_kernel(const int* meta_in, int
   }
 }
 
+// ---------------------------------------------------------------------------------
+// The FP16 hidden rows in route order, xs[pos] = x16[pos_tok[pos]] for the plan's routed rows,
+// so that the rows of every gate/up pass are contiguous (TMA boxes instead of row gathers).
+// One warp per row at a time, 16-byte pieces.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) wide_gather_kernel(const __half* __restrict__ x16, const int* __restrict__ pos_tok,
+                                                          const int* __restrict__ offsets, int E, int R, int d,
+                                                          __half* __restrict__ xs) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int n = min(__ldcg(offsets + E), R);
+  const int lane = threadIdx.x & 31;
+  const int w0 = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int nw = static_cast<int>((gridDim.x * blockDim.x) >> 5);
+  const int q = d / 8;  // 16-byte pieces per row
+  for (int pos = w0; pos < n; pos += nw) {
+    const int t = __ldcg(pos_tok + pos);
+    const uint4* src = reinterpret_cast<const uint4*>(x16 + static_cast<size_t>(t) * d);
+    uint4* dst = reinterpret_cast<uint4*>(xs + static_cast<size_t>(pos) * d);
+    for (int j0 = 0; j0 < q; j0 += 32 * 4) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + 32 * u + lane;
+        if (j < q) v[u] = src[j];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + 32 * u + lane;
+        if (j < q) dst[j] = v[u];
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     expert_wide_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_w2,
+                       const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_h,
                        const __grid_constant__ ExpertArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -227,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&sm.empty_a[i]), 4);  // the four dequantisation warps
     }
     for (int i = 0; i < kStagesB; ++i) {
-      mbar_init(smem_addr(&sm.full_b[i]), 32 * kActWarps);
+      mbar_init(smem_addr(&sm.full_b[i]), 1);  // expect_tx arrival of the activation producer
       mbar_init(smem_addr(&sm.empty_b[i]), 1);  // MMA commit
     }
     for (int i = 0; i < kNumA; ++i) {
@@ -249,6 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpFetch && lane == 0) {
     prefetch_tmap(&tm_w13);
     prefetch_tmap(&tm_w2);
+  }
+  if (warp == kWarpAct0 && lane == 0) {
+    prefetch_tmap(&tm_xs);
+    prefetch_tmap(&tm_h);
   }
   // everything above is local to the CTA; the task table and the counters come from the
   // preceding kernels
@@ -343,18 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (!mbar_try_wait(smem_addr(&sm.full_a[st]), ph) && clock64() - t0 < kDrainCycles) {}
       }
     }
-  } else if (warp >= kWarpAct0 && warp < kWarpAct0 + kActWarps) {
-    // ------------- activation producers: the pass's routed rows via cp.async -------------
-    // Lane L (0..127 over the four warps) copies 16-byte granule L % 16 of rows r0 + L / 16,
-    // r0 = 0, 8, 16, ...: warp aw serves the rows r with (r % 8) / 2 == aw and keeps their
-    // source offsets in its own table (entry (r / 8) * 2 + r % 2).
-    const int aw = warp - kWarpAct0;
-    const int L = 32 * aw + lane;
-    const int gi = L & 15, atom = gi >> 3, ch = gi & 7;
-    const int rsub = L >> 4;  // row within each group of 8 rows
-    uint32_t* rowoff16 = sm.rowoff16[aw];
-    constexpr uint32_t kNoRow = 0xffffffffu;
-    int stage = 0, n = 0;
+  } else if (warp == kWarpAct0) {
+    // ------------- activation producer: the pass's routed rows by TMA -------------
+    // Lane j < 2 * nbox loads 64-row box j % nbox of atom j / nbox (64 K elements each).  Rows
+    // past the pass, up to the box boundary (other passes' rows, or zeros past the tensor),
+    // feed accumulator columns that the epilogue never reads.
+    int stage = 0, n = 0, issued = 0;
     uint32_t phase = 0;
     bool ok = true;
     while (ok) {
@@ -368,37 +393,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t target = static_cast<uint32_t>(npass * a.S_gu);
         if (!warp_wait_counter(a.ready + tk.u, target, &sm.abort_flag, a.status, a.wait_limit)) break;
       }
-      for (int idx = lane; idx < kWideRows / kActWarps; idx += 32) {
-        const int r = (idx >> 1) * 8 + 2 * aw + (idx & 1);
-        uint32_t off = kNoRow;
-        if (r < tk.rows) {
-          const size_t row = tk.is_dn ? static_cast<size_t>(tk.row0 + r) : static_cast<size_t>(__ldg(a.pos_tok + tk.row0 + r));
-          off = static_cast<uint32_t>(row * (tk.is_dn ? a.F : a.d) / 8);
-        }
-        rowoff16[idx] = off;
-      }
-      __syncwarp();
-      const uint4* src_base = reinterpret_cast<const uint4*>(tk.is_dn ? a.hs16 : a.x16);
-      const int ngroups = (tk.rows + 7) / 8;
-      for (int c = 0; ok && c < tk.nck; ++c) {
+      const CUtensorMap* tm = tk.is_dn ? &tm_h : &tm_xs;
+      const int nbox = (tk.rows + kBoxRows - 1) / kBoxRows;
+      const uint32_t bytes = static_cast<uint32_t>(nbox * 2 * kBoxRows * 128);
+      for (int c = 0; c < tk.nck; ++c) {
         if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, sm, a.status, a.wait_limit)) { ok = false; break; }
-        const uint32_t bbase = ringb0 + stage * kStageB + atom * kAtomB + rsub * 128 + ((ch ^ rsub) << 4);
-        const uint32_t kb16 = static_cast<uint32_t>(c * (kChunkK / 8) + gi);  // 16-byte units
-        // eight row groups per batch: the offsets are read first, then the copies issued
-        for (int g0 = 0; g0 < ngroups; g0 += 8) {
-          uint32_t off[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) off[u] = g0 + u < ngroups ? rowoff16[(g0 + u) * 2 + (rsub & 1)] : kNoRow;
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (off[u] != kNoRow) cp_async_16(bbase + (g0 + u) * 1024, src_base + (off[u] + kb16));
+        const uint32_t fb = smem_addr(&sm.full_b[stage]);
+        if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
+        __syncwarp();
+        if (lane < 2 * nbox) {
+          const int at = lane >= nbox ? 1 : 0, b = lane - at * nbox;
+          tma_load_2d_plain(ringb0 + stage * kStageB + at * kAtomB + b * (kBoxRows * 128), tm, c * kChunkK + 64 * at,
+                            tk.row0 + kBoxRows * b, fb);
         }
-        cp_async_arrive_noinc(smem_addr(&sm.full_b[stage]));
+        ++issued;
         if (++stage == kStagesB) { stage = 0; phase ^= 1u; }
       }
-      __syncwarp();
     }
-    cp_async_wait_all();
+    // drain: the last phase issued on every stage has landed before the CTA exits
+    if (lane == 0) {
+      int st = stage;
+      uint32_t ph = phase;
+      for (int i = 0; i < min(issued, kStagesB); ++i) {
+        if (--st < 0) { st = kStagesB - 1; ph ^= 1u; }
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_addr(&sm.full_b[st]), ph) && clock64() - t0 < kDrainCycles) {}
+      }
+    }
+    __syncwarp();
   } else if (warp >= kWarpDeq0 && warp < kWarpDeq0 + 4) {
     // ---------------- dequantisation: NVFP4 -> FP16 A tile in tensor memory ----------------
     const int i = tid - 32 * kWarpDeq0;  // A row of this thread (= tensor-memory lane)
@@ -456,7 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer: the warp waits, one elected lane issues ----------------
     // Descriptors and tensor-memory addresses are computed by the whole warp in converged
-    // code; only the tcgen05 instructions run on the elected lane.
+    // code; only the tcgen05 instructions run on the elected lane.  Both operands are written
+    // by the async proxy (TMA; tcgen05.st ordered by the tensor-core fences and barriers), so
+    // no proxy fence precedes the MMAs.
     int stage = 0, abuf = 0, dbuf = 0, n = 0;
     uint32_t phase = 0, aphase = 0, dphase = 0;
     bool ok = true;
@@ -477,7 +501,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bd = bdesc0 + static_cast<uint64_t>((stage * kStageB) >> 4);
         const uint32_t acol = tmem + abuf * 64;
         if (elect_one()) {
-          fence_proxy_async_smem();
 #pragma unroll
           for (int kk = 0; kk < kChunkK / 16; ++kk)
             tc_mma_f16_ts(dcol, acol + kk * 8, bd + static_cast<uint64_t>(((kk >> 2) * kAtomB + (kk & 3) * 32) >> 4),
@@ -535,14 +558,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_bar_sync(4 + grp, 128);
           __half* hst = sm.hstage[grp];
           const int j0 = up ? 16 : 0;
+          // branch-free, so that the 16 independent SiLU chains interleave; one status update
+          bool sat = false;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int c = c0 + j0 + j;
             const float own = __uint_as_float(up ? v[16 + j] : v[j]) * sc13, other = xch[(j0 + j) * 64 + nF] * sc13;
             const float g = up ? other : own, u = up ? own : other;
-            hst[(j0 + j) * 64 + nF] =
-                c < tk.rows ? h_store_value(__fdividef(g, 1.0f + __expf(-g)) * u, a.status) : __float2half_rn(0.f);
+            float hv = __fdividef(g, 1.0f + __expf(-g)) * u * kHScale;
+            const bool big = fabsf(hv) > 65504.f;
+            sat = sat || (big && c < tk.rows);
+            hv = big ? copysignf(65504.f, hv) : hv;
+            hst[(j0 + j) * 64 + nF] = __float2half_rn(c < tk.rows ? hv : 0.f);
           }
+          if (sat) atomicOr(a.status, static_cast<int>(MOE_DEV_H_SATURATED));
           named_bar_sync(4 + grp, 128);
           // the slice's h rows (32 routed rows x 64 F values) in 16-byte pieces
 #pragma unroll
@@ -605,13 +634,18 @@ static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory per CTA (227 KB)");
 
 size_t expert_wide_smem_bytes() { return sizeof(Smem) + 1024; }
 
+cudaError_t launch_wide_gather(const ExpertArgs& a, __half* xs, int num_sms, cudaStream_t stream) {
+  return launch_pdl(wide_gather_kernel, dim3(num_sms * 8), dim3(256), 0, stream, a.x16, a.pos_tok, a.offsets, a.E, a.R,
+                    a.d, xs);
+}
+
 cudaError_t launch_expert_wide(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
-                               int num_sms, cudaStream_t stream) {
+                               const CUtensorMap& tm_xs, const CUtensorMap& tm_h, int num_sms, cudaStream_t stream) {
   const size_t smem = expert_wide_smem_bytes();
   cudaError_t err = cudaFuncSetAttribute(expert_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  return launch_pdl(expert_wide_kernel, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, a);
+  return launch_pdl(expert_wide_kernel, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, tm_xs, tm_h, a);
 }
 
 cudaError_t launch_wide_plan(const ExpertArgs& a, TaskEntry* tasks_w, cudaStream_t stream) {

@@ -177,6 +177,14 @@ MOE_DEVICE void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32
       "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
+// 2-D tile load without a cache hint (L2 evict-normal).
+MOE_DEVICE void tma_load_2d_plain(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16),
 // completing on `bar` through its transaction count.
 MOE_DEVICE void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -215,6 +223,16 @@ MOE_DEVICE void tmem_relinquish() {
 }
 MOE_DEVICE void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// True on one lane of the converged warp (the same lane for every lane's view).
+MOE_DEVICE bool elect_one() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 x;\n\t"
+      "elect.sync x|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r));
+  return r != 0;
 }
 MOE_DEVICE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 MOE_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }

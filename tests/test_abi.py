@@ -134,10 +134,10 @@ def test_layer_launch_counts(L):
              ((8, 2048, 512, 512, 32), 1),     # 256 routes: the own front's limit
              ((8, 2048, 512, 2048 // 2, 33 - 1), 1),
              ((4, 256, 128, 16, 2), 3),        # ffn below the warp-MMA range: front, tcgen05, un-route
-             ((32, 2048, 512, 512, 10), 3),    # front (its plan writes the 8-row table), decode kernel, un-route
+             ((32, 2048, 512, 512, 10), 3),    # front, decode kernel (8-row passes derived in the kernel), un-route
              ((256, 2048, 512, 512, 10), 3),   # the same up to 256 tokens
              ((512, 2048, 512, 512, 10), 3),   # front, warp-MMA batch kernel, un-route
-             ((8192, 2048, 512, 512, 10), 8),  # router, 3-launch plan, staging, task table, wide, un-route
+             ((8192, 2048, 512, 512, 10), 9),  # router, 3-launch plan, staging, gather, task table, wide, un-route
              ((0, 2048, 512, 512, 10), 0)]
     for dims, n in cases:
         assert L.layer_launches(L.shape_of(*dims)) == n, dims
