@@ -66,7 +66,8 @@ struct Smem {
   // per epilogue group: gate/up values exchanged between lane halves; the FP16 down outputs
   // of a 32-column slice staged for row-contiguous stores
   float xch[2][32 * 64];
-  __half hstage[2][32 * 64];       // per epilogue group: the FP16 h values of a slice
+  // per epilogue group: the FP16 h values of a slice, two routed rows per word
+  uint32_t hstage[2][16 * 64];
   TaskEntry task[kTaskSlots];
   uint64_t full_a[kStagesA];
   uint64_t empty_a[kStagesA];
@@ -129,6 +130,14 @@ __device__ __forceinline__ bool take_task(Smem& sm, int n, TaskEntry& out, int* 
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&sm.task_empty[q]));
   return true;
+}
+
+// Two FP32 values to FP16 (round to nearest), magnitudes past the FP16 range clamped to
+// +-65504 (NaN stays NaN); lo in the low half.
+__device__ __forceinline__ uint32_t f16x2_satfinite(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // MMA N for a pass of `rows` routed rows: a multiple of 16 (kind::f16 with M = 128).
@@ -556,54 +565,69 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) xch[(up ? j : 16 + j) * 64 + nF] = __uint_as_float(up ? v[j] : v[16 + j]);
           named_bar_sync(4 + grp, 128);
-          __half* hst = sm.hstage[grp];
+          uint32_t* hst = sm.hstage[grp];
           const int j0 = up ? 16 : 0;
-          // branch-free, so that the 16 independent SiLU chains interleave; one status update
-          bool sat = false;
+          // branch-free, so that the independent SiLU chains interleave; the largest magnitude
+          // of the valid columns decides the one status update.  Word (r / 2) * 64 + nF holds
+          // rows r (low half) and r + 1 (high half) of column nF.
+          const int nv = tk.rows - c0 - j0;  // valid columns among this thread's 16
+          float hv[16];
+          float mx = 0.f;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int c = c0 + j0 + j;
-            const float own = __uint_as_float(up ? v[16 + j] : v[j]) * sc13, other = xch[(j0 + j) * 64 + nF] * sc13;
+            const float own = __uint_as_float(up ? v[16 + j] : v[j]) * sc13;
+            const float other = xch[(j0 + j) * 64 + nF] * sc13;
             const float g = up ? other : own, u = up ? own : other;
-            float hv = __fdividef(g, 1.0f + __expf(-g)) * u * kHScale;
-            const bool big = fabsf(hv) > 65504.f;
-            sat = sat || (big && c < tk.rows);
-            hv = big ? copysignf(65504.f, hv) : hv;
-            hst[(j0 + j) * 64 + nF] = __float2half_rn(c < tk.rows ? hv : 0.f);
+            const float h = __fdividef(g, 1.0f + __expf(-g)) * u * kHScale;
+            mx = j < nv ? fmaxf(mx, fabsf(h)) : mx;
+            hv[j] = j < nv ? h : 0.f;
           }
-          if (sat) atomicOr(a.status, static_cast<int>(MOE_DEV_H_SATURATED));
-          named_bar_sync(4 + grp, 128);
-          // the slice's h rows (32 routed rows x 64 F values) in 16-byte pieces
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int q = i + 128 * t, r = q >> 3, part = q & 7;
-            if (c0 + r < tk.rows)
-              *reinterpret_cast<uint4*>(a.hs16 + static_cast<size_t>(tk.row0 + c0 + r) * a.F + tk.s * kGuRows + part * 8) =
-                  *reinterpret_cast<const uint4*>(hst + r * 64 + part * 8);
+          for (int j = 0; j < 16; j += 2) hst[((j0 + j) >> 1) * 64 + nF] = f16x2_satfinite(hv[j], hv[j + 1]);
+          if (mx > 65504.f) atomicOr(a.status, static_cast<int>(MOE_DEV_H_SATURATED));
+          named_bar_sync(4 + grp, 128);
+          // rows 2p and 2p + 1, 8 F values each, from 8 words: one thread per (p, piece)
+          {
+            const int pp = i >> 3, part = i & 7;
+            const uint4 w0 = *reinterpret_cast<const uint4*>(hst + pp * 64 + part * 8);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(hst + pp * 64 + part * 8 + 4);
+            const uint4 lo = make_uint4(__byte_perm(w0.x, w0.y, 0x5410), __byte_perm(w0.z, w0.w, 0x5410),
+                                        __byte_perm(w1.x, w1.y, 0x5410), __byte_perm(w1.z, w1.w, 0x5410));
+            const uint4 hi = make_uint4(__byte_perm(w0.x, w0.y, 0x7632), __byte_perm(w0.z, w0.w, 0x7632),
+                                        __byte_perm(w1.x, w1.y, 0x7632), __byte_perm(w1.z, w1.w, 0x7632));
+            __half* hrow = a.hs16 + static_cast<size_t>(tk.row0 + c0 + 2 * pp) * a.F + tk.s * kGuRows + part * 8;
+            if (c0 + 2 * pp < tk.rows) *reinterpret_cast<uint4*>(hrow) = lo;
+            if (c0 + 2 * pp + 1 < tk.rows) *reinterpret_cast<uint4*>(hrow + a.F) = hi;
           }
         } else {
           // per-route outputs as FP16(y * 2^-4), staged so that each routed row's 128 values
-          // leave in 16-byte pieces
-          __half* yst = reinterpret_cast<__half*>(xch);
-          bool sat = false;
+          // leave in 16-byte pieces; word (r / 2) * 128 + i holds rows r and r + 1 of d-row i
+          uint32_t* yst = reinterpret_cast<uint32_t*>(xch);
+          const float ys = sc2 * kYScale;
+          const int nv = tk.rows - c0;  // valid columns of the slice
+          float mx = 0.f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float yv = __uint_as_float(v[j]) * (sc2 * kYScale);
-            if (c0 + j < tk.rows && fabsf(yv) > 65504.f) {
-              sat = true;
-              yv = copysignf(65504.f, yv);
-            }
-            yst[j * kDnRows + i] = __float2half_rn(yv);
+          for (int j = 0; j < 32; j += 2) {
+            const float y0 = __uint_as_float(v[j]) * ys, y1 = __uint_as_float(v[j + 1]) * ys;
+            mx = j < nv ? fmaxf(mx, fabsf(y0)) : mx;
+            mx = j + 1 < nv ? fmaxf(mx, fabsf(y1)) : mx;
+            yst[(j >> 1) * kDnRows + i] = f16x2_satfinite(y0, y1);
           }
-          if (sat) atomicOr(a.status, static_cast<int>(MOE_DEV_Y_SATURATED));
+          if (mx > 65504.f) atomicOr(a.status, static_cast<int>(MOE_DEV_Y_SATURATED));
           named_bar_sync(4 + grp, 128);
           __half* y16 = reinterpret_cast<__half*>(a.y);
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int q = i + 128 * t, r = q >> 4, part = q & 15;
-            if (c0 + r < tk.rows)
-              *reinterpret_cast<uint4*>(y16 + static_cast<size_t>(tk.row0 + c0 + r) * a.d + tk.s * kDnRows + part * 8) =
-                  *reinterpret_cast<const uint4*>(yst + r * kDnRows + part * 8);
+          for (int t = 0; t < 2; ++t) {
+            const int q = i + 128 * t, pp = q >> 4, part = q & 15;
+            const uint4 w0 = *reinterpret_cast<const uint4*>(yst + pp * kDnRows + part * 8);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(yst + pp * kDnRows + part * 8 + 4);
+            const uint4 lo = make_uint4(__byte_perm(w0.x, w0.y, 0x5410), __byte_perm(w0.z, w0.w, 0x5410),
+                                        __byte_perm(w1.x, w1.y, 0x5410), __byte_perm(w1.z, w1.w, 0x5410));
+            const uint4 hi = make_uint4(__byte_perm(w0.x, w0.y, 0x7632), __byte_perm(w0.z, w0.w, 0x7632),
+                                        __byte_perm(w1.x, w1.y, 0x7632), __byte_perm(w1.z, w1.w, 0x7632));
+            __half* yrow = y16 + static_cast<size_t>(tk.row0 + c0 + 2 * pp) * a.d + tk.s * kDnRows + part * 8;
+            if (c0 + 2 * pp < tk.rows) *reinterpret_cast<uint4*>(yrow) = lo;
+            if (c0 + 2 * pp + 1 < tk.rows) *reinterpret_cast<uint4*>(yrow + a.d) = hi;
           }
           named_bar_sync(4 + grp, 128);
         }
