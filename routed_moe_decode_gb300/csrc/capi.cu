@@ -472,13 +472,16 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     aw.tasks = tasks_w;
     aw.task_cap = L.max_tasks_w;
     // gate/up passes read their hidden rows, down passes the expert's h rows, as contiguous
-    // rows in 64-row boxes
-    CUtensorMap tmxs, tmh;
-    rc = moe::encode_f16_rows_map(&tmxs, xs, static_cast<uint64_t>(shape->d), static_cast<uint64_t>(L.R), 64);
-    if (rc != MOE_OK) return rc;
-    rc = moe::encode_f16_rows_map(&tmh, a.hs16, static_cast<uint64_t>(shape->ffn), static_cast<uint64_t>(L.R), 64);
-    if (rc != MOE_OK) return rc;
-    e = moe::launch_expert_wide(aw, tm13, tm2, tmxs, tmh, di.num_sms, stream);
+    // rows in boxes of 64, 128 or 192 rows
+    moe::WideActMaps am;
+    for (int j = 0; j < 3; ++j) {
+      const uint32_t rows = static_cast<uint32_t>(64 * (j + 1));
+      rc = moe::encode_f16_rows_map(&am.xs[j], xs, static_cast<uint64_t>(shape->d), static_cast<uint64_t>(L.R), rows);
+      if (rc != MOE_OK) return rc;
+      rc = moe::encode_f16_rows_map(&am.h[j], a.hs16, static_cast<uint64_t>(shape->ffn), static_cast<uint64_t>(L.R), rows);
+      if (rc != MOE_OK) return rc;
+    }
+    e = moe::launch_expert_wide(aw, tm13, tm2, am, di.num_sms, stream);
     if (e != cudaSuccess) { set_error("expert_wide launch", e); return MOE_ERR_CUDA; }
   } else {
     rc = poison(at<moe::TaskEntry>(workspace, L.tasks), moe::META_NGU);

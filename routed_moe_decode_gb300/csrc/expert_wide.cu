@@ -19,9 +19,9 @@
 //         stored into tensor memory, where they are the A operand (M = 128);
 //   12    task fetcher + weight producer (TMA codes, cp.async scales);
 //   13    activation producer: the pass's routed rows as 128-byte swizzled K-major tiles, the
-//         B operand (N up to 192), by TMA in 64-row boxes.  The rows of a pass are contiguous:
-//         for gate/up the FP16 hidden rows in route order (wide_gather_kernel writes them
-//         before this kernel), for down the expert's h rows;
+//         B operand (N up to 192), by TMA: one box of 64, 128 or 192 rows per 64-K atom.  The
+//         rows of a pass are contiguous: for gate/up the FP16 hidden rows in route order
+//         (wide_gather_kernel writes them before this kernel), for down the expert's h rows;
 //   14    MMA issuer and tensor-memory owner: 8 kind::f16 MMAs per chunk into one of two
 //         accumulator buffers, so the epilogue of a task overlaps the next task's MMAs; the
 //         warp waits and forms the descriptors, one elected lane issues.
@@ -51,7 +51,9 @@ constexpr int kWarpFetch = kWarpDeq0 + 4;                      // 12
 constexpr int kWarpAct0 = kWarpFetch + 1;                      // 13
 constexpr int kWarpMma = kWarpAct0 + kActWarps;                // 14
 constexpr int kThreads = 32 * (kWarpMma + 1);                  // 480
-constexpr int kBoxRows = 64;                                   // rows per TMA box of a pass's activation rows
+constexpr int kBoxRows = 64;                                   // activation box heights: 64, 128, 192 rows
+constexpr int kBoxMaps = kWideRows / kBoxRows;                 // tensor maps per activation operand
+static_assert(kBoxMaps == 3, "WideActMaps holds three box heights");
 constexpr int kTaskConsumers = kActWarps + 4 + 1 + kEpiWarps;  // activation, dequant, MMA, epilogue warps
 // Bound of the drain waits at exit (copies and MMAs already issued complete within
 // microseconds; after an abort a barrier may lack the arrival of a role that gave up).
@@ -247,8 +249,7 @@ __global__ void __launch_bounds__(256) wide_gather_kernel(const __half* __restri
 
 __global__ void __launch_bounds__(kThreads, 1)
     expert_wide_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_w2,
-                       const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_h,
-                       const __grid_constant__ ExpertArgs a) {
+                       const __grid_constant__ WideActMaps am, const __grid_constant__ ExpertArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -286,10 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_w13);
     prefetch_tmap(&tm_w2);
   }
-  if (warp == kWarpAct0 && lane == 0) {
-    prefetch_tmap(&tm_xs);
-    prefetch_tmap(&tm_h);
-  }
+  if (warp == kWarpAct0 && lane < 2 * kBoxMaps) prefetch_tmap(lane < kBoxMaps ? &am.xs[lane] : &am.h[lane - kBoxMaps]);
   // everything above is local to the CTA; the task table and the counters come from the
   // preceding kernels
   pdl_wait();
@@ -385,9 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpAct0) {
     // ------------- activation producer: the pass's routed rows by TMA -------------
-    // Lane j < 2 * nbox loads 64-row box j % nbox of atom j / nbox (64 K elements each).  Rows
-    // past the pass, up to the box boundary (other passes' rows, or zeros past the tensor),
-    // feed accumulator columns that the epilogue never reads.
+    // Lanes 0 and 1 load atoms 0 and 1 of a chunk (64 K elements each), one box of the
+    // smallest height (64, 128 or 192 rows) that covers the pass.  Rows past the pass (other
+    // passes' rows, or zeros past the tensor) feed accumulator columns the epilogue never reads.
     int stage = 0, n = 0, issued = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -402,19 +400,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t target = static_cast<uint32_t>(npass * a.S_gu);
         if (!warp_wait_counter(a.ready + tk.u, target, &sm.abort_flag, a.status, a.wait_limit)) break;
       }
-      const CUtensorMap* tm = tk.is_dn ? &tm_h : &tm_xs;
       const int nbox = (tk.rows + kBoxRows - 1) / kBoxRows;
+      const CUtensorMap* tm = tk.is_dn ? &am.h[nbox - 1] : &am.xs[nbox - 1];
       const uint32_t bytes = static_cast<uint32_t>(nbox * 2 * kBoxRows * 128);
       for (int c = 0; c < tk.nck; ++c) {
         if (!warp_wait(smem_addr(&sm.empty_b[stage]), phase ^ 1u, sm, a.status, a.wait_limit)) { ok = false; break; }
         const uint32_t fb = smem_addr(&sm.full_b[stage]);
         if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
         __syncwarp();
-        if (lane < 2 * nbox) {
-          const int at = lane >= nbox ? 1 : 0, b = lane - at * nbox;
-          tma_load_2d_plain(ringb0 + stage * kStageB + at * kAtomB + b * (kBoxRows * 128), tm, c * kChunkK + 64 * at,
-                            tk.row0 + kBoxRows * b, fb);
-        }
+        if (lane < 2) tma_load_2d_plain(ringb0 + stage * kStageB + lane * kAtomB, tm, c * kChunkK + 64 * lane, tk.row0, fb);
         ++issued;
         if (++stage == kStagesB) { stage = 0; phase ^= 1u; }
       }
@@ -664,12 +658,12 @@ cudaError_t launch_wide_gather(const ExpertArgs& a, __half* xs, int num_sms, cud
 }
 
 cudaError_t launch_expert_wide(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
-                               const CUtensorMap& tm_xs, const CUtensorMap& tm_h, int num_sms, cudaStream_t stream) {
+                               const WideActMaps& am, int num_sms, cudaStream_t stream) {
   const size_t smem = expert_wide_smem_bytes();
   cudaError_t err = cudaFuncSetAttribute(expert_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  return launch_pdl(expert_wide_kernel, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, tm_xs, tm_h, a);
+  return launch_pdl(expert_wide_kernel, dim3(num_sms), dim3(kThreads), smem, stream, tm_w13, tm_w2, am, a);
 }
 
 cudaError_t launch_wide_plan(const ExpertArgs& a, TaskEntry* tasks_w, cudaStream_t stream) {

@@ -317,11 +317,16 @@ cudaError_t launch_expert_simt(const ExpertArgs& a, cudaStream_t stream);
 // per-expert arrays by launch_wide_plan, then launch_expert_wide runs with a.tasks = that table.
 cudaError_t launch_wide_plan(const ExpertArgs& a, TaskEntry* tasks_w, cudaStream_t stream);
 // launch_wide_gather writes the FP16 hidden rows in route order (xs[pos] = x16[pos_tok[pos]])
-// for the wide kernel's gate/up passes.  tm_xs: those rows [R, d]; tm_h: FP16 h rows [R, ffn];
-// both 64-element (128-byte) by 64-row boxes with the 128-byte swizzle.
+// for the wide kernel's gate/up passes.  The wide kernel reads those rows [R, d] and the FP16 h
+// rows [R, ffn] through tensor maps of 64-element (128-byte) wide boxes with the 128-byte
+// swizzle, entry j of each array with boxes of 64 (j + 1) rows.
+struct WideActMaps {
+  CUtensorMap xs[3];
+  CUtensorMap h[3];
+};
 cudaError_t launch_wide_gather(const ExpertArgs& a, __half* xs, int num_sms, cudaStream_t stream);
 cudaError_t launch_expert_wide(const ExpertArgs& a, const CUtensorMap& tm_w13, const CUtensorMap& tm_w2,
-                               const CUtensorMap& tm_xs, const CUtensorMap& tm_h, int num_sms, cudaStream_t stream);
+                               const WideActMaps& am, int num_sms, cudaStream_t stream);
 int encode_f16_rows_map(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows);
 size_t expert_wide_smem_bytes();
 cudaError_t launch_combine(const ExpertArgs& a, cudaStream_t stream);
