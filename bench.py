@@ -429,12 +429,16 @@ def measure(cfg, moe, torch, dist, dev, Wd, algo, K, W, kernel_samples, e2e_step
         moe.route_topk(shape, logits[l], ids, wts)
         moe.plan(shape, ids, wts, ws)
         moe.forward_prepare(shape, hidden[l], ws)
-        starts[i].record()
         if fused_unroute:
+            starts[i].record()
             moe.forward_experts(shape, Wd[l], resid[l], out, ws, algo)  # one kernel
             ends[i].record()
         else:
-            moe.forward_expert_kernels(shape, Wd[l], ws, algo)
+            # the kernels that prepare the expert kernel's input (the wide path's route-order
+            # gather and task table) run before the events, the expert kernel between them
+            moe.selftest_expert_part(shape, Wd[l], ws, algo, 0)
+            starts[i].record()
+            moe.selftest_expert_part(shape, Wd[l], ws, algo, 1)
             ends[i].record()
             moe.forward_unroute(shape, resid[l], out, ws)
         kbytes += unique_bytes[l] + act_bytes
@@ -505,7 +509,7 @@ def measure(cfg, moe, torch, dist, dev, Wd, algo, K, W, kernel_samples, e2e_step
                                 + ("<own front, fused un-route> (the whole layer)" if one_launch
                                    else "<fused un-route>" if fused_unroute
                                    else "<gathered rows>" if dec_kernel else "")
-                                + (" (with its route-order gather and task-table kernels)" if run_algo == moe.ALGO_WIDE else "")) if kname
+                                + (" (timed alone: its route-order gather and task table run before the events)" if run_algo == moe.ALGO_WIDE else "")) if kname
                                else "simt kernels",
                      "kernel_us": 1e3 * k_avg_ms, "kernel_samples": Kk,
                      "kernel_timing": "the timed region's events (K launches of this one kernel)" if one_launch

@@ -92,6 +92,18 @@ MOE_API int moe_selftest_expert_timeout(const moe_shape* shape, const uint8_t* w
                                         void* workspace, size_t workspace_bytes, int algo, int dn_task,
                                         long long wait_limit_cycles, moe_stream_t stream);
 
+/* moe_forward_expert_kernels in two parts, so that the expert kernel can be timed alone:
+ * part 0 launches the kernels that prepare its input (for MOE_ALGO_WIDE, or AUTO choosing
+ * it: the hidden rows gathered into route order and the wide kernel's task table; nothing
+ * for the other kernels), part 1 the expert kernel itself, which reads what part 0 left in the
+ * workspace.  Part 0 followed by part 1 on the same stream equals moe_forward_expert_kernels.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG (part not 0 or 1) or another moe_status. */
+MOE_API int moe_selftest_expert_part(const moe_shape* shape, const uint8_t* w13_codes,
+                                     const uint8_t* w13_scales, float w13_scale,
+                                     const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+                                     void* workspace, size_t workspace_bytes, int algo, int part,
+                                     moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -84,6 +84,7 @@ SIGNATURES = {
     # include/moe_selftest.h
     "moe_selftest_expert_timeout": (_I, [_SP, _P, _P, _F, _P, _P, _F, _P, _P, _P, ctypes.c_size_t, _I, _I,
                                          ctypes.c_longlong, _P]),
+    "moe_selftest_expert_part": (_I, [_SP, _P, _P, _F, _P, _P, _F, _P, ctypes.c_size_t, _I, _I, _P]),
 }
 
 _lock = threading.Lock()
@@ -219,6 +220,15 @@ def forward_expert_kernels(shape: Shape, w: dict, ws: Workspace, algo: int = ALG
     _check("moe_forward_expert_kernels", lib().moe_forward_expert_kernels(
         ctypes.byref(shape), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]), float(w["w13_ts"]),
         _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]), ws.ptr, ws.nbytes, algo, _stream(stream)))
+
+
+def selftest_expert_part(shape: Shape, w: dict, ws: Workspace, algo: int, part: int, stream=None):
+    """moe_forward_expert_kernels in two parts (include/moe_selftest.h): part 0 the kernels that
+    prepare the expert kernel's input (wide path only), part 1 the expert kernel alone."""
+    _check("moe_selftest_expert_part", lib().moe_selftest_expert_part(
+        ctypes.byref(shape), _ptr(w["w13_codes"]), _ptr(w["w13_scales"]), float(w["w13_ts"]),
+        _ptr(w["w2_codes"]), _ptr(w["w2_scales"]), float(w["w2_ts"]), ws.ptr, ws.nbytes, int(algo), int(part),
+        _stream(stream)))
 
 
 def forward_unroute(shape: Shape, residual, out, ws: Workspace, stream=None):

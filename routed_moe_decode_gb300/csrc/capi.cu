@@ -343,7 +343,9 @@ int moe_forward_prepare(const moe_shape* shape, const void* hidden, void* worksp
   return MOE_OK;
 }
 
-enum { kStageExperts = 1, kStageUnroute = 2 };
+// kStageExperts: the expert kernel and the kernels that prepare its input (the wide path's
+// route-order gather and task table); kStagePrepOnly / kStageKernelOnly narrow it to either.
+enum { kStageExperts = 1, kStageUnroute = 2, kStagePrepOnly = 4, kStageKernelOnly = 8 };
 
 static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
                                 float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
@@ -378,6 +380,7 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     if (e != cudaSuccess) { set_error("combine launch", e); return MOE_ERR_CUDA; }
     return MOE_OK;
   }
+  if (algo == MOE_ALGO_SIMT && (stages & kStagePrepOnly)) return MOE_OK;
   if (algo == MOE_ALGO_SIMT) {
     e = moe::launch_expert_simt(a, stream);
     if (e != cudaSuccess) { set_error("simt launch", e); return MOE_ERR_CUDA; }
@@ -395,6 +398,8 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
   const int run = algo == MOE_ALGO_AUTO ? auto_choice(shape) : algo;
   const bool use_wide = run == MOE_ALGO_WIDE;
   const bool use_mma = run == MOE_ALGO_MMA;
+  // only the wide path has kernels that prepare the expert kernel's input
+  if ((stages & kStagePrepOnly) && !use_wide) return MOE_OK;
   const uint32_t box = use_mma ? 128u : 64u;
   CUtensorMap tm13, tm2;
   rc = encode_codes_map(&tm13, w13_codes, static_cast<uint64_t>(shape->d) / 2,
@@ -460,14 +465,17 @@ static int forward_experts_impl(const moe_shape* shape, const uint8_t* w13_codes
     // the hidden rows in route order, in the upper half of the per-route output buffer (the
     // wide kernel's per-route outputs are FP16 and fill only the lower half)
     __half* xs = reinterpret_cast<__half*>(a.y) + static_cast<size_t>(L.R) * shape->d;
-    e = moe::launch_wide_gather(a, xs, di.num_sms, stream);
-    if (e != cudaSuccess) { set_error("wide gather launch", e); return MOE_ERR_CUDA; }
-    // the wide kernel's own task table (passes of kWideRows rows), from the plan's arrays
     moe::TaskEntry* tasks_w = at<moe::TaskEntry>(workspace, L.tasks_w);
-    e = moe::launch_wide_plan(a, tasks_w, stream);
-    if (e != cudaSuccess) { set_error("wide plan launch", e); return MOE_ERR_CUDA; }
-    rc = poison(tasks_w, moe::META_WGU);
-    if (rc != MOE_OK) return rc;
+    if (!(stages & kStageKernelOnly)) {
+      e = moe::launch_wide_gather(a, xs, di.num_sms, stream);
+      if (e != cudaSuccess) { set_error("wide gather launch", e); return MOE_ERR_CUDA; }
+      // the wide kernel's own task table (passes of kWideRows rows), from the plan's arrays
+      e = moe::launch_wide_plan(a, tasks_w, stream);
+      if (e != cudaSuccess) { set_error("wide plan launch", e); return MOE_ERR_CUDA; }
+      rc = poison(tasks_w, moe::META_WGU);
+      if (rc != MOE_OK) return rc;
+    }
+    if (stages & kStagePrepOnly) return MOE_OK;
     moe::ExpertArgs aw = a;
     aw.tasks = tasks_w;
     aw.task_cap = L.max_tasks_w;
@@ -504,6 +512,17 @@ int moe_forward_expert_kernels(const moe_shape* shape, const uint8_t* w13_codes,
   return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, nullptr,
                               nullptr, workspace, workspace_bytes, algo, nullptr, stream, all_experts(shape),
                               kStageExperts);
+}
+
+int moe_selftest_expert_part(const moe_shape* shape, const uint8_t* w13_codes, const uint8_t* w13_scales,
+                             float w13_scale, const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,
+                             void* workspace, size_t workspace_bytes, int algo, int part, moe_stream_t stream) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (part != 0 && part != 1) return MOE_ERR_INVALID_ARG;
+  return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, nullptr,
+                              nullptr, workspace, workspace_bytes, algo, nullptr, stream, all_experts(shape),
+                              kStageExperts | (part == 0 ? kStagePrepOnly : kStageKernelOnly));
 }
 
 int moe_forward_unroute(const moe_shape* shape, const void* residual, void* out, void* workspace,

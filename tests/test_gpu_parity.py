@@ -496,3 +496,37 @@ def test_expert_range_rejects_bad_bounds():
             moe.layer_expert_range(shape, e0, e1, None, None, {"w13_codes": None, "w13_scales": None, "w13_ts": 1.0,
                                                               "w2_codes": None, "w2_scales": None, "w2_ts": 1.0},
                                    None, None, None, None, moe.Workspace(shape))
+
+
+@pytest.mark.parametrize("T,d,F,E,k,algo", [(512, 256, 256, 16, 2, "wide"), (256, 512, 256, 32, 4, "wide"),
+                                            (32, 256, 256, 64, 8, "mma"), (4, 256, 128, 16, 2, "tcgen05")])
+def test_expert_kernel_parts_equal_the_whole(T, d, F, E, k, algo):
+    # moe_selftest_expert_part: the preparing kernels (part 0) then the expert kernel alone
+    # (part 1) leave exactly what moe_forward_expert_kernels leaves
+    import routed_moe_decode_gb300 as moe
+    cfg = mi.CONFIGS["tiny"].replace(name=f"parts{T}x{d}x{F}x{E}x{k}", T=T, d=d, ffn=F, E=E, k=k, tag=700 + T)
+    inp = mi.gen_layer(cfg, seed=21)
+    layer = moe.MoeLayer(T, d, F, E, k, algo=ALGOS[algo])
+    w = device_weights(inp, "cuda")
+    logits = torch.from_numpy(inp["logits"]).cuda()
+    hidden = bf16_tensor(inp["hidden"], "cuda")
+    res = bf16_tensor(inp["residual"], "cuda")
+    outs = []
+    for split in (False, True):
+        layer.route(logits)
+        layer.plan()
+        moe.forward_prepare(layer.shape, hidden, layer.ws)
+        if split:
+            moe.selftest_expert_part(layer.shape, w, layer.ws, ALGOS[algo], 0)
+            moe.selftest_expert_part(layer.shape, w, layer.ws, ALGOS[algo], 1)
+        else:
+            moe.forward_expert_kernels(layer.shape, w, layer.ws, ALGOS[algo])
+        out = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+        moe.forward_unroute(layer.shape, res, out, layer.ws)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(outs[0], outs[1])
+    ids_ref, w_ref = O.route_topk(inp["logits"], k)
+    ref = O.moe_experts((T, d, F, E, k), inp["hidden"], ids_ref, w_ref, inp, inp["residual"], None)
+    assert_parity(outs[1].float().cpu().numpy(), ref, f"parts {algo}")
