@@ -152,8 +152,9 @@ using namespace wd;
 // ---------------------------------------------------------------------------------
 // Task table of the wide kernel, built from the plan's per-expert arrays (touched list,
 // counts, offsets): per touched expert, passes of kWideRows rows; all gate/up tasks
-// (touched order, pass, stripe) first, then all down tasks.  One 1024-thread CTA, one thread
-// per touched expert (U <= E <= 1024).
+// (touched order, pass, stripe) first, then all down tasks.  Each 1024-thread CTA scans the
+// pass counts of all touched experts (one thread each, U <= E <= 1024) and writes the entries
+// of its share of them: one CTA alone writes a few hundred KB slowly.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) wide_plan_kernel(const int* meta_in, int* meta, const int* touched,
                                                          const int* counts, const int* offsets, TaskEntry* tasks,
@@ -193,19 +194,30 @@ __global__ void __launch_bounds__(1024) wide_plan_kernel(const int* meta_in, int
   __syncthreads();
   const int before = s_warp[warp] + incl - np;
   const int total = s_total;
+  // one warp per touched expert writes its passes' entries, one lane per stripe, so that each
+  // store instruction covers consecutive entries
+  __shared__ int s_e[1024], s_m[1024], s_before[1024], s_base[1024];
   if (tid < U) {
-    const int base = __ldcg(offsets + e);
-    int gi = before * S_gu;
-    int di = total * S_gu + before * S_dn;
-    for (int p = 0; p < np; ++p) {
-      const int rows = min(kWideRows, m - p * kWideRows);
-      const int z = rows | (np > 1 ? 1 << 17 : 0);
-      const int row0 = base + p * kWideRows;
-      for (int s2 = 0; s2 < S_gu; ++s2) tasks[gi++] = TaskEntry{e | (tid << 16), row0, z, s2};
-      for (int s2 = 0; s2 < S_dn; ++s2) tasks[di++] = TaskEntry{e | (tid << 16), row0, z | (1 << 16), s2};
+    s_e[tid] = e;
+    s_m[tid] = m;
+    s_before[tid] = before;
+    s_base[tid] = __ldcg(offsets + e);
+  }
+  __syncthreads();
+  int4* tasks4 = reinterpret_cast<int4*>(tasks);
+  for (int u = blockIdx.x * 32 + warp; u < U; u += 32 * gridDim.x) {
+    const int eu = s_e[u], mu = s_m[u], npu = (mu + kWideRows - 1) / kWideRows;
+    for (int p = 0; p < npu; ++p) {
+      const int rows = min(kWideRows, mu - p * kWideRows);
+      const int z = rows | (npu > 1 ? 1 << 17 : 0);
+      const int row0 = s_base[u] + p * kWideRows;
+      const int P = s_before[u] + p;
+      for (int s2 = lane; s2 < S_gu; s2 += 32) tasks4[P * S_gu + s2] = make_int4(eu | (u << 16), row0, z, s2);
+      for (int s2 = lane; s2 < S_dn; s2 += 32)
+        tasks4[total * S_gu + P * S_dn + s2] = make_int4(eu | (u << 16), row0, z | (1 << 16), s2);
     }
   }
-  if (tid == 0) {
+  if (blockIdx.x == 0 && tid == 0) {
     meta[META_WGU] = total * S_gu;
     meta[META_WDN] = total * S_dn;
     meta[META_YFMT] = 1;  // this kernel's down tasks store FP16(y * 2^-4)
@@ -215,7 +227,8 @@ __global__ void __launch_bounds__(1024) wide_plan_kernel(const int* meta_in, int
 // ---------------------------------------------------------------------------------
 // The FP16 hidden rows in route order, xs[pos] = x16[pos_tok[pos]] for the plan's routed rows,
 // so that the rows of every gate/up pass are contiguous (TMA boxes instead of row gathers).
-// One warp per row at a time, 16-byte pieces.
+// One warp per row at a time, 16-byte pieces, last positions first: the rows written last,
+// still in L2 when the wide kernel starts, are those of the first experts, which it reads first.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) wide_gather_kernel(const __half* __restrict__ x16, const int* __restrict__ pos_tok,
                                                           const int* __restrict__ offsets, int E, int R, int d,
@@ -227,7 +240,8 @@ __global__ void __launch_bounds__(256) wide_gather_kernel(const __half* __restri
   const int w0 = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int nw = static_cast<int>((gridDim.x * blockDim.x) >> 5);
   const int q = d / 8;  // 16-byte pieces per row
-  for (int pos = w0; pos < n; pos += nw) {
+  for (int i = w0; i < n; i += nw) {
+    const int pos = n - 1 - i;
     const int t = __ldcg(pos_tok + pos);
     const uint4* src = reinterpret_cast<const uint4*>(x16 + static_cast<size_t>(t) * d);
     uint4* dst = reinterpret_cast<uint4*>(xs + static_cast<size_t>(pos) * d);
@@ -667,7 +681,7 @@ cudaError_t launch_expert_wide(const ExpertArgs& a, const CUtensorMap& tm_w13, c
 }
 
 cudaError_t launch_wide_plan(const ExpertArgs& a, TaskEntry* tasks_w, cudaStream_t stream) {
-  return launch_pdl(wide_plan_kernel, dim3(1), dim3(1024), 0, stream, a.meta, const_cast<int*>(a.meta), a.touched,
+  return launch_pdl(wide_plan_kernel, dim3(16), dim3(1024), 0, stream, a.meta, const_cast<int*>(a.meta), a.touched,
                     a.counts, a.offsets, tasks_w, a.S_gu, a.S_dn);
 }
 

@@ -79,7 +79,10 @@ __device__ __forceinline__ bool local_expert(const PlanArgs& a, int e) { return 
 // Everything of the plan that follows from the per-expert counts (thread e of a 1024-thread
 // CTA holds count cnt of expert e): offsets, touched list, task-pass prefix sums, the task
 // table and the meta words.  s_counts is scratch of 1024 ints.  Returns expert tid's offset.
-__device__ __forceinline__ int plan_from_counts(const PlanArgs& a, int cnt, int* s_counts, int* s_scan) {
+// write_table: also write the task table from this block (one CTA writes a few hundred KB
+// slowly; the multi-CTA plan leaves it to its scatter kernel, spread over all its CTAs).
+__device__ __forceinline__ int plan_from_counts(const PlanArgs& a, int cnt, int* s_counts, int* s_scan,
+                                                int* s_pass0, int* s_cnt, int* s_off, bool write_table) {
   const int tid = threadIdx.x;
   const int E = a.E;
   int total = 0;
@@ -117,26 +120,37 @@ __device__ __forceinline__ int plan_from_counts(const PlanArgs& a, int cnt, int*
     a.gu_start[U] = gu_total;
     a.dn_start[U] = dn_total;
   }
-  // the task table: all gate/up tasks (touched order, pass, stripe), then all down tasks
+  // the task table: all gate/up tasks (touched order, pass, stripe), then all down tasks; one
+  // warp per pass (its touched expert found by binary search over the touched experts' first
+  // passes) writes the pass's gate/up and down entries, one lane per stripe, so that each
+  // store instruction covers consecutive entries
   __syncthreads();
   if (flag) {
-    s_counts[rank] = tid;  // expert of touched index `rank`
+    s_counts[rank] = tid;  // expert, row count and first position of touched index `rank`
+    s_cnt[rank] = cnt;
+    s_off[rank] = off;
   }
+  if (tid < U) s_pass0[tid] = gu_start / a.S_gu;
+  if (tid == 0) s_pass0[U] = gu_total / a.S_gu;
   __syncthreads();
-  if (tid < U) {
-    const int e = s_counts[tid];
-    const int m = a.counts[e];
-    const int base = a.offsets[e];
-    const int np = (m + kRowsPerPass - 1) / kRowsPerPass;
-    int gi = gu_start;
-    int di = gu_total + dn_start;
-    for (int p = 0; p < np; ++p) {
-      const int rows = min(kRowsPerPass, m - p * kRowsPerPass);
-      const int row0 = base + p * kRowsPerPass;
-      const int z = rows | (np > 1 ? 1 << 17 : 0);
-      for (int s2 = 0; s2 < a.S_gu; ++s2) a.tasks[gi++] = TaskEntry{e | (tid << 16), row0, z, s2};
-      for (int s2 = 0; s2 < a.S_dn; ++s2) a.tasks[di++] = TaskEntry{e | (tid << 16), row0, z | (1 << 16), s2};
+  int4* tasks = reinterpret_cast<int4*>(a.tasks);
+  const int passes = (U > 0 && write_table) ? s_pass0[U] : 0;
+  const int lane = tid & 31;
+  for (int P = tid >> 5; P < passes; P += blockDim.x >> 5) {
+    int lo = 0, hi = U - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pass0[mid] <= P) lo = mid;
+      else hi = mid - 1;
     }
+    const int e = s_counts[lo];
+    const int p = P - s_pass0[lo];
+    const int c = s_cnt[lo];
+    const int rows = min(kRowsPerPass, c - p * kRowsPerPass);
+    const int z = rows | (c > kRowsPerPass ? 1 << 17 : 0);
+    const int x = e | (lo << 16), row0 = s_off[lo] + p * kRowsPerPass;
+    for (int s2 = lane; s2 < a.S_gu; s2 += 32) tasks[P * a.S_gu + s2] = make_int4(x, row0, z, s2);
+    for (int s2 = lane; s2 < a.S_dn; s2 += 32) tasks[gu_total + P * a.S_dn + s2] = make_int4(x, row0, z | (1 << 16), s2);
   }
   // largest row count over the experts
   int mx = cnt;
@@ -161,7 +175,9 @@ __device__ __forceinline__ int plan_from_counts(const PlanArgs& a, int cnt, int*
 // L1: in the fused front they were written by other CTAs of the same launch.
 __device__ __forceinline__ void plan_block(const PlanArgs& a) {
   __shared__ int s_counts[1024];
-  __shared__ int s_cursor[1024];
+  __shared__ int s_cursor[1025];
+  __shared__ int s_cnt[1024];
+  __shared__ int s_off[1024];
   __shared__ int s_scan[33];
   const int tid = threadIdx.x;
   const int E = a.E, R = a.T * a.k;
@@ -178,7 +194,7 @@ __device__ __forceinline__ void plan_block(const PlanArgs& a) {
   }
   __syncthreads();
   const int cnt = tid < E ? s_counts[tid] : 0;
-  const int off = plan_from_counts(a, cnt, s_counts, s_scan);
+  const int off = plan_from_counts(a, cnt, s_counts, s_scan, s_cursor, s_cnt, s_off, true);
   if (tid < E) s_cursor[tid] = off;
   __syncthreads();
   // route positions in expert-major order
@@ -499,20 +515,42 @@ __global__ void __launch_bounds__(1024) plan_hist_kernel(PlanArgs a, int* hist) 
 __global__ void __launch_bounds__(1024) plan_scan_kernel(PlanArgs a, int* hist, int slices) {
   __shared__ int s_counts[1024];
   __shared__ int s_scan[33];
+  __shared__ int s_pass0[1025];
+  __shared__ int s_cnt[1024];
+  __shared__ int s_off[1024];
   pdl_wait();
   pdl_launch_dependents();
   const int tid = threadIdx.x, E = a.E;
+  // up to kScanCached slices: this expert's per-slice counts stay in registers between the
+  // sum and the per-slice starts (independent loads instead of a dependent chain)
+  constexpr int kScanCached = 32;
+  int hv[kScanCached];
   int cnt = 0;
-  if (tid < E)
+  if (slices <= kScanCached) {
+#pragma unroll
+    for (int g = 0; g < kScanCached; ++g) {
+      hv[g] = (g < slices && tid < E) ? __ldcg(hist + static_cast<size_t>(g) * E + tid) : 0;
+      cnt += hv[g];
+    }
+  } else if (tid < E) {
     for (int g = 0; g < slices; ++g) cnt += __ldcg(hist + static_cast<size_t>(g) * E + tid);
-  const int off = plan_from_counts(a, cnt, s_counts, s_scan);
+  }
+  const int off = plan_from_counts(a, cnt, s_counts, s_scan, s_pass0, s_cnt, s_off, false);
   if (tid < E) {
     int run = off;
-    for (int g = 0; g < slices; ++g) {
-      int* h = hist + static_cast<size_t>(g) * E + tid;
-      const int c = *h;
-      *h = run;
-      run += c;
+    if (slices <= kScanCached) {
+#pragma unroll
+      for (int g = 0; g < kScanCached; ++g) {
+        if (g < slices) hist[static_cast<size_t>(g) * E + tid] = run;
+        run += hv[g];
+      }
+    } else {
+      for (int g = 0; g < slices; ++g) {
+        int* h = hist + static_cast<size_t>(g) * E + tid;
+        const int c = *h;
+        *h = run;
+        run += c;
+      }
     }
   }
 }
@@ -534,6 +572,25 @@ __global__ void __launch_bounds__(1024) plan_scatter_kernel(PlanArgs a, const in
     const int pos = atomicAdd(&s_cursor[e], 1);
     a.route_pos[r] = pos;
     a.pos_tok[pos] = r / a.k;
+  }
+  // the task table of plan_from_counts (written by plan_scan_kernel's arrays): warp w of CTA
+  // b writes the passes of touched indices b * 32 + w, + 32 * gridDim.x, ..., one lane per
+  // stripe, so that each store instruction covers consecutive entries
+  const int lane = tid & 31;
+  const int U = __ldcg(a.meta + META_U), ngu = __ldcg(a.meta + META_NGU);
+  int4* tasks = reinterpret_cast<int4*>(a.tasks);
+  for (int u = blockIdx.x * 32 + (tid >> 5); u < U; u += 32 * gridDim.x) {
+    const int e = __ldcg(a.touched + u);
+    const int c = __ldcg(a.counts + e), base = __ldcg(a.offsets + e);
+    const int P0 = __ldcg(a.gu_start + u) / a.S_gu;
+    const int np = (c + kRowsPerPass - 1) / kRowsPerPass;
+    for (int p = 0; p < np; ++p) {
+      const int rows = min(kRowsPerPass, c - p * kRowsPerPass);
+      const int z = rows | (c > kRowsPerPass ? 1 << 17 : 0);
+      const int x = e | (u << 16), row0 = base + p * kRowsPerPass, P = P0 + p;
+      for (int s2 = lane; s2 < a.S_gu; s2 += 32) tasks[P * a.S_gu + s2] = make_int4(x, row0, z, s2);
+      for (int s2 = lane; s2 < a.S_dn; s2 += 32) tasks[ngu + P * a.S_dn + s2] = make_int4(x, row0, z | (1 << 16), s2);
+    }
   }
 }
 
