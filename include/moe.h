@@ -239,7 +239,11 @@ MOE_API int moe_front(const moe_shape* shape, const float* logits, const void* h
  * (results identical to the split steps), and the routing, the plan and the FP16 hidden rows
  * are still written into the workspace for later calls.  Otherwise, for T * k up to 16384
  * the router, the FP16 staging of hidden and the plan run as one fused launch (moe_front),
- * and moe_layer is moe_front followed by moe_forward_experts with MOE_ALGO_AUTO. */
+ * and moe_layer is moe_front followed by moe_forward_experts with MOE_ALGO_AUTO.  Where the
+ * expert kernel that MOE_ALGO_AUTO picks does not read the plan's task table (the decode
+ * kernel above eight tokens, the wide kernel), the layer leaves the table unwritten and its
+ * task counts at 0: a later moe_forward_experts on that plan must use MOE_ALGO_AUTO (another
+ * algorithm would find no tasks). */
 MOE_API int moe_layer(const moe_shape* shape, const float* logits, const void* hidden,
               const uint8_t* w13_codes, const uint8_t* w13_scales, float w13_scale,
               const uint8_t* w2_codes, const uint8_t* w2_scales, float w2_scale,

@@ -297,10 +297,11 @@ static void fill_plan_args(moe::PlanArgs& a, const moe_shape* shape, const WsLay
   a.hist = at<int>(workspace, L.hist);
   a.e_lo = r.lo;
   a.e_hi = r.hi;
+  a.no_table = 0;
 }
 
 static int plan_impl(const moe_shape* shape, const int32_t* ids, const float* weights, void* workspace,
-                     size_t workspace_bytes, ExpertRange r, moe_stream_t stream) {
+                     size_t workspace_bytes, ExpertRange r, moe_stream_t stream, bool table = true) {
   int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   if (shape->T == 0) return MOE_OK;
@@ -310,6 +311,7 @@ static int plan_impl(const moe_shape* shape, const int32_t* ids, const float* we
   const WsLayout L = moe::ws_layout(*shape);
   moe::PlanArgs a{};
   fill_plan_args(a, shape, L, workspace, ids, weights, r);
+  a.no_table = table ? 0 : 1;
   cudaError_t e = moe::launch_plan(a, stream);
   if (e != cudaSuccess) { set_error("plan launch", e); return MOE_ERR_CUDA; }
   return MOE_OK;
@@ -615,8 +617,11 @@ int moe_forward(const moe_shape* shape, const void* hidden, const uint8_t* w13_c
                           out, workspace, workspace_bytes, MOE_ALGO_AUTO, stream);
 }
 
+// table = false: the plan's task table is left unwritten (the caller's expert kernel does not
+// read it).
 static int front_impl(const moe_shape* shape, const float* logits, const void* hidden, int32_t* ids, float* weights,
-                      void* workspace, size_t workspace_bytes, ExpertRange r, moe_stream_t stream) {
+                      void* workspace, size_t workspace_bytes, ExpertRange r, moe_stream_t stream,
+                      bool table = true) {
   int rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   if (shape->T == 0) return MOE_OK;
@@ -624,7 +629,7 @@ static int front_impl(const moe_shape* shape, const float* logits, const void* h
     // large batches: separate router, plan and preparation kernels
     rc = moe_route_topk(shape, logits, ids, weights, stream);
     if (rc != MOE_OK) return rc;
-    rc = plan_impl(shape, ids, weights, workspace, workspace_bytes, r, stream);
+    rc = plan_impl(shape, ids, weights, workspace, workspace_bytes, r, stream, table);
     if (rc != MOE_OK) return rc;
     return moe_forward_prepare(shape, hidden, workspace, workspace_bytes, stream);
   }
@@ -636,6 +641,7 @@ static int front_impl(const moe_shape* shape, const float* logits, const void* h
   const WsLayout L = moe::ws_layout(*shape);
   moe::FrontArgs f{};
   fill_plan_args(f.plan, shape, L, workspace, ids, weights, r);
+  f.plan.no_table = table ? 0 : 1;
   f.d = shape->d;
   f.logits = logits;
   f.hidden = static_cast<const __nv_bfloat16*>(hidden);
@@ -701,7 +707,13 @@ static int layer_steps(const moe_shape* shape, const float* logits, const void* 
                                 out, workspace, workspace_bytes, MOE_ALGO_AUTO, trace, stream, r,
                                 kStageExperts | kStageUnroute, moe::kDefaultWaitLimit, -1, w13_ts_e, w2_ts_e, &f);
   }
-  const int rc = front_impl(shape, logits, hidden, ids, weights, workspace, workspace_bytes, r, stream);
+  // the gathered decode kernel derives its passes from the plan's per-expert arrays and the wide
+  // kernel builds its own table: neither reads the plan's task table
+  const int run = auto_choice(shape);
+  const bool table = !((run == MOE_ALGO_MMA && moe::expert_dec_supports(shape->T, shape->d, shape->ffn) &&
+                        moe::expert_dec_gathers(shape->T)) ||
+                       run == MOE_ALGO_WIDE);
+  const int rc = front_impl(shape, logits, hidden, ids, weights, workspace, workspace_bytes, r, stream, table);
   if (rc != MOE_OK) return rc;
   return forward_experts_impl(shape, w13_codes, w13_scales, w13_scale, w2_codes, w2_scales, w2_scale, residual, out,
                               workspace, workspace_bytes, MOE_ALGO_AUTO, trace, stream, r,

@@ -24,6 +24,8 @@ struct PlanArgs {
   float* route_w;
   TaskEntry* tasks;
   int* hist;  // [ceil(T * k / kPlanSlice), E] scratch of the multi-CTA plan (many routes)
+  // 1: leave the task table unwritten (a layer whose expert kernel derives its tasks itself)
+  int no_table;
 };
 
 // The fused front (router + plan + FP16 hidden) for T * k up to kFrontMaxRoutes.

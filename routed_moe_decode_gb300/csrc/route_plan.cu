@@ -134,7 +134,7 @@ __device__ __forceinline__ int plan_from_counts(const PlanArgs& a, int cnt, int*
   if (tid == 0) s_pass0[U] = gu_total / a.S_gu;
   __syncthreads();
   int4* tasks = reinterpret_cast<int4*>(a.tasks);
-  const int passes = (U > 0 && write_table) ? s_pass0[U] : 0;
+  const int passes = (U > 0 && write_table && !a.no_table) ? s_pass0[U] : 0;
   const int lane = tid & 31;
   for (int P = tid >> 5; P < passes; P += blockDim.x >> 5) {
     int lo = 0, hi = U - 1;
@@ -162,8 +162,10 @@ __device__ __forceinline__ int plan_from_counts(const PlanArgs& a, int cnt, int*
     int m = 0;
     for (int w = 0; w < 32; ++w) m = max(m, s_scan[w]);
     a.meta[META_U] = U;
-    a.meta[META_NGU] = gu_total;
-    a.meta[META_NDN] = dn_total;
+    // without a table the task counts read 0, so that an expert kernel that follows the table
+    // finds no work rather than stale entries
+    a.meta[META_NGU] = a.no_table ? 0 : gu_total;
+    a.meta[META_NDN] = a.no_table ? 0 : dn_total;
     a.meta[META_MAXROWS] = m;
     a.meta[META_YFMT] = 0;
   }
@@ -343,8 +345,8 @@ __device__ __forceinline__ void plan_block_cached(const PlanArgs& a, const int* 
     a.gu_start[U] = passes * a.S_gu;
     a.dn_start[U] = passes * a.S_dn;
     a.meta[META_U] = U;
-    a.meta[META_NGU] = passes * a.S_gu;
-    a.meta[META_NDN] = passes * a.S_dn;
+    a.meta[META_NGU] = a.no_table ? 0 : passes * a.S_gu;
+    a.meta[META_NDN] = a.no_table ? 0 : passes * a.S_dn;
     a.meta[META_MAXROWS] = mx;
     a.meta[META_YFMT] = 0;
   }
@@ -367,7 +369,7 @@ __device__ __forceinline__ void plan_block_cached(const PlanArgs& a, const int* 
   }
   // the task table: all gate/up tasks (touched order, pass, stripe), then all down tasks;
   // consecutive threads write consecutive 16-byte entries
-  const int ngu = passes * a.S_gu, ntask = ngu + passes * a.S_dn;
+  const int ngu = passes * a.S_gu, ntask = a.no_table ? 0 : ngu + passes * a.S_dn;
   int4* tasks = reinterpret_cast<int4*>(a.tasks);
   for (int i = tid; i < ntask; i += blockDim.x) {
     const bool dn = i >= ngu;
@@ -577,7 +579,7 @@ __global__ void __launch_bounds__(1024) plan_scatter_kernel(PlanArgs a, const in
   // b writes the passes of touched indices b * 32 + w, + 32 * gridDim.x, ..., one lane per
   // stripe, so that each store instruction covers consecutive entries
   const int lane = tid & 31;
-  const int U = __ldcg(a.meta + META_U), ngu = __ldcg(a.meta + META_NGU);
+  const int U = a.no_table ? 0 : __ldcg(a.meta + META_U), ngu = __ldcg(a.meta + META_NGU);
   int4* tasks = reinterpret_cast<int4*>(a.tasks);
   for (int u = blockIdx.x * 32 + (tid >> 5); u < U; u += 32 * gridDim.x) {
     const int e = __ldcg(a.touched + u);
