@@ -530,3 +530,30 @@ def test_expert_kernel_parts_equal_the_whole(T, d, F, E, k, algo):
     ids_ref, w_ref = O.route_topk(inp["logits"], k)
     ref = O.moe_experts((T, d, F, E, k), inp["hidden"], ids_ref, w_ref, inp, inp["residual"], None)
     assert_parity(outs[1].float().cpu().numpy(), ref, f"parts {algo}")
+
+
+@pytest.mark.parametrize("T,E,k", [(32, 64, 8), (512, 16, 2)])
+def test_layer_without_plan_table_then_other_algorithm_finds_no_tasks(T, E, k):
+    # a layer whose expert kernel derives its own tasks (gathered decode kernel at 8 < T <=
+    # 256, the wide kernel for many rows per expert) leaves the plan's task table unwritten and
+    # its task counts at 0; a later forward on that plan with MOE_ALGO_TCGEN05 (which reads the
+    # table) finds no tasks and returns with a clean status (its un-route sums whatever
+    # per-route outputs the workspace holds); AUTO on the same plan reproduces the layer
+    import routed_moe_decode_gb300 as moe
+    d, F = 256, 256
+    cfg = mi.CONFIGS["tiny"].replace(name=f"notable{T}x{E}x{k}", T=T, d=d, ffn=F, E=E, k=k, tag=800 + T)
+    inp = mi.gen_layer(cfg, seed=23)
+    layer = moe.MoeLayer(T, d, F, E, k)
+    assert moe.auto_algo(layer.shape) in (ALGOS["mma"], ALGOS["wide"])
+    w = device_weights(inp, "cuda")
+    logits = torch.from_numpy(inp["logits"]).cuda()
+    hidden = bf16_tensor(inp["hidden"], "cuda")
+    res = bf16_tensor(inp["residual"], "cuda")
+    out = layer(logits, hidden, w, res)
+    again = layer.experts(hidden, w, res)  # AUTO on the left plan
+    other = torch.empty_like(out)
+    moe.forward_experts(layer.shape, w, res, other, layer.ws, ALGOS["tcgen05"])
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(again, out)
+    assert torch.isfinite(other.float()).all()
