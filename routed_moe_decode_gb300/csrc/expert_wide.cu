@@ -8,12 +8,13 @@
 // task only waits for work resident CTAs already hold.  A task streams one 128-row stripe of
 // one touched expert's NVFP4 weights once per pass, whatever the pass's row count.
 //
-// Warp roles (576 threads):
+// Warp roles (480 threads):
 //   0-7   epilogue, two groups of four warps taking alternate 32-column slices of an
 //         accumulator; thread t owns accumulator lane t % 128.  Gate/up tasks exchange half of
 //         the gate and up values between the lane halves through shared memory, so that all
 //         128 threads of a group form h = silu(g) * u (FP16); down tasks store per-route
 //         outputs as FP16(y * 2^-4) (summed by the un-route kernel in slot order, in FP32);
+//         both leave through shared-memory staging in 16-byte stores;
 //   8-11  dequantisation: thread i owns A row i; each 128-K chunk of E2M1 codes (TMA tile,
 //         64-byte swizzle) and its E4M3 block scales become exact FP16 in registers and are
 //         stored into tensor memory, where they are the A operand (M = 128);
