@@ -110,6 +110,12 @@ def test_bad_arguments_rejected_on_host(L):
     # T = 0 is an empty, valid call that enqueues nothing
     z = L.shape_of(0, 256, 128, 16, 2)
     assert lib.moe_route_topk(ctypes.byref(z), None, None, None, None) == 0
+    # the two-part expert entry takes part 0 or 1 only, and checks the shape first
+    part_args = [fake, fake, 1.0, fake, fake, 1.0, fake, 1 << 30, 0]
+    for part in (-1, 2):
+        assert lib.moe_selftest_expert_part(sp, *part_args, part, None) == L.MOE_ERR_INVALID_ARG
+    bad = L.shape_of(4, 200, 128, 16, 2)
+    assert lib.moe_selftest_expert_part(ctypes.byref(bad), *part_args, 0, None) == L.MOE_ERR_UNSUPPORTED
 
 
 def test_expert_range_bounds_rejected_on_host(L):
