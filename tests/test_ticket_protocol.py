@@ -19,10 +19,10 @@ import pytest
 ROWS = 8  # routed rows per pass
 
 
-def plan_passes(ids, E):
+def plan_passes(ids, E, rows=ROWS):
     counts = np.bincount(np.asarray(ids).reshape(-1), minlength=E)
     touched = [e for e in range(E) if counts[e] > 0]
-    return [(e, (int(counts[e]) + ROWS - 1) // ROWS) for e in touched]
+    return [(e, (int(counts[e]) + rows - 1) // rows) for e in touched]
 
 
 def ticket_order(passes, S_gu, S_dn, G, grid, T):
@@ -169,3 +169,20 @@ def test_simulation_detects_a_broken_order():
         check_order(dn + gu + ur, passes, 2, 4)
     ok, _ = simulate(dn + gu + ur, passes, 2, 4, grid, 8, 2, random.Random(0))
     assert not ok
+
+
+@pytest.mark.parametrize("T,E,k,grid", [(2048, 64, 8, 152), (512, 16, 4, 152), (4096, 512, 10, 152), (1024, 32, 8, 5)])
+def test_wide_kernel_ticket_order_forward_progress(T, E, k, grid):
+    # the wide kernel's order: passes of up to 192 routed rows, every gate/up task (touched,
+    # pass, stripe) before every down task, one stripe per down ticket, no un-route tasks; a
+    # down task waits for every gate/up stripe of all passes of its expert
+    rng = np.random.default_rng(T + E + k)
+    S_gu, S_dn = 8, 16
+    for name, ids in routings(T, E, k, rng):
+        passes = plan_passes(ids, E, rows=192)
+        tickets, ngroup = ticket_order(passes, S_gu, S_dn, 1, grid, 0)
+        assert ngroup == sum(n for _, n in passes) * S_dn - min(sum(n for _, n in passes) * S_dn, grid)
+        assert not any(t[0] == "ur" for t in tickets)
+        check_order(tickets, passes, S_gu, S_dn)
+        ok, _ = simulate(tickets, passes, S_gu, S_dn, grid, 16, 4, random.Random(1))
+        assert ok, name
